@@ -1,0 +1,402 @@
+"""Pins of the fp64 oracle against facts fixed outside it.
+
+Each test checks the oracle against something it cannot have copied:
+a printed table, a closed form, a library routine, an invariant of the
+mathematics, or brute force on tiny inputs.  None needs a GPU.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.integrate
+import scipy.linalg
+import scipy.stats
+
+import oracle
+from turboquant_compressed_kv_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, *v = line.split()
+            out[k] = [float(x) for x in v]
+    return out
+
+
+# ------------------------------------------------------------------ codebook
+
+def test_codebook_matches_max_1960_table():
+    g = _golden("lloyd_max_gaussian_8.txt")
+    c, t, mse, it = oracle.lloyd_max8()
+    assert it > 0
+    np.testing.assert_allclose(c[4:], g["levels"], atol=1e-3)
+    np.testing.assert_allclose(t[3:], g["thresholds"], atol=1e-3)
+    assert abs(mse - g["mse"][0]) < 1e-4
+
+
+def test_codebook_symmetry_and_midpoints():
+    c, t, _, _ = oracle.lloyd_max8()
+    assert t[3] == 0.0
+    np.testing.assert_array_equal(c[::-1], -c)
+    np.testing.assert_allclose(t, 0.5 * (c[:-1] + c[1:]), rtol=0, atol=1e-15)
+    assert np.all(np.diff(c) > 0)
+
+
+def test_codebook_is_a_fixed_point_by_numerical_integration():
+    """Centroid condition checked with scipy quadrature, not the closed form."""
+    c, t, mse, _ = oracle.lloyd_max8()
+    edges = [-np.inf] + list(t) + [np.inf]
+    pdf = scipy.stats.norm.pdf
+    err = 0.0
+    for j in range(8):
+        a, b = edges[j], edges[j + 1]
+        m0 = scipy.integrate.quad(pdf, a, b, epsabs=1e-14, epsrel=1e-13)[0]
+        m1 = scipy.integrate.quad(lambda x: x * pdf(x), a, b, epsabs=1e-14, epsrel=1e-13)[0]
+        assert abs(m1 / m0 - c[j]) < 1e-10
+        err += scipy.integrate.quad(lambda x: (x - c[j]) ** 2 * pdf(x), a, b,
+                                    epsabs=1e-14, epsrel=1e-13)[0]
+    assert abs(err - mse) < 1e-10
+
+
+def test_codebook_beats_perturbations():
+    """Lloyd-Max is a local minimum of the distortion: nudging any level raises it."""
+    c, t, mse, _ = oracle.lloyd_max8()
+    pdf = scipy.stats.norm.pdf
+
+    def distortion(levels):
+        levels = np.sort(levels)
+        th = 0.5 * (levels[:-1] + levels[1:])
+        edges = [-np.inf] + list(th) + [np.inf]
+        return sum(scipy.integrate.quad(lambda x: (x - levels[j]) ** 2 * pdf(x),
+                                        edges[j], edges[j + 1])[0] for j in range(8))
+
+    base = distortion(c)
+    assert abs(base - mse) < 1e-9
+    for j in range(8):
+        for eps in (1e-3, -1e-3):
+            cc = c.copy()
+            cc[j] += eps
+            assert distortion(cc) > base
+
+
+# ------------------------------------------------------------------ fp16
+
+def test_fp16_rne_matches_numpy_conversion():
+    rng = np.random.default_rng(5)
+    vals = np.concatenate([
+        rng.standard_normal(4000) * 10.0 ** rng.integers(-9, 6, 4000),
+        rng.uniform(0, 1, 500) * 2.0 ** -24 * 4,      # subnormals
+        np.array([0.0, -0.0, 65504.0, 65520.0, 1e6, -1e6, 2.0 ** -25, 2.0 ** -26,
+                  1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 2049.0, 2051.0]),
+    ])
+    for v in vals:
+        want = np.array([v], np.float64).astype(np.float16).view(np.uint16)[0]
+        assert oracle.fp16_rne(v) == want, v
+        if np.isfinite(np.float16(v)):
+            assert oracle.fp16_value(want) == float(np.float16(v))
+
+
+# ------------------------------------------------------------------ rotation
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_hadamard_orthogonal_integer(d):
+    H = np.array([[oracle.hadamard_entry(i, j) for j in range(d)] for i in range(d)])
+    np.testing.assert_array_equal(H @ H.T, d * np.eye(d, dtype=H.dtype))
+    np.testing.assert_array_equal(H, scipy.linalg.hadamard(d))
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_rotation_matches_library_hadamard(d):
+    D = synth.rotation_signs(d)
+    rng = np.random.default_rng(0)
+    for _ in range(3):
+        x = rng.standard_normal(d)
+        want = scipy.linalg.hadamard(d) @ (D * x) / math.sqrt(d)
+        y = oracle.rotate(D, x)
+        np.testing.assert_allclose(y, want, rtol=0, atol=1e-12)
+        assert abs(np.linalg.norm(y) - np.linalg.norm(x)) < 1e-12
+        np.testing.assert_allclose(oracle.rotate_t(D, y), x, rtol=0, atol=1e-12)
+
+
+def test_rotation_spreads_outliers():
+    """Two channels at 20x: after the rotation no coordinate keeps the spike."""
+    d = 128
+    D = synth.rotation_signs(d)
+    w = synth.workload("tiny")
+    K, _ = synth.kv_tokens(w, 0, 0, 256)
+    before, after = [], []
+    for x in K[:, 0, :].astype(np.float64):
+        xh = x / np.linalg.norm(x)
+        before.append(np.max(np.abs(xh)))
+        after.append(np.max(np.abs(oracle.rotate(D, xh))))
+    assert np.mean(before) > 0.6          # the 20x channels dominate
+    assert np.mean(after) < 3.5 * math.sqrt(2 * math.log(d) / d)
+
+
+# ------------------------------------------------------------------ quantiser
+
+def test_code_is_nearest_centroid():
+    """Threshold counting equals brute-force nearest-centroid search."""
+    c, t, _, _ = oracle.lloyd_max8()
+    d = 128
+    D = synth.rotation_signs(d)
+    S = synth.qjl_matrix(d)
+    rng = np.random.default_rng(1)
+    for _ in range(20):
+        x = rng.standard_normal(d) * rng.lognormal(0, 1, d)
+        r = oracle.encode_vector(False, D, S, x)
+        near = np.argmin(np.abs(r["z"][:, None] - c[None, :]), axis=1)
+        margin = np.min(np.abs(r["z"][:, None] - t[None, :]), axis=1)
+        ok = margin > 1e-6
+        np.testing.assert_array_equal(r["codes"][ok], near[ok])
+        np.testing.assert_allclose(r["z"], math.sqrt(d) * oracle.rotate(D, x / np.linalg.norm(x)),
+                                   atol=1e-12)
+
+
+def test_quantiser_distortion_matches_mse():
+    """E||xhat - Pi^T yhat||^2 ~ Lloyd-Max MSE (the rotated coordinates are near N(0,1/d))."""
+    c, _, mse, _ = oracle.lloyd_max8()
+    d = 128
+    D = synth.rotation_signs(d)
+    S = synth.qjl_matrix(d)
+    rng = np.random.default_rng(2)
+    errs, cells = [], np.zeros(8)
+    for _ in range(400):
+        x = rng.standard_normal(d)
+        r = oracle.encode_vector(True, D, S, x)
+        yhat = c[r["codes"]] / math.sqrt(d)
+        xr = oracle.rotate_t(D, yhat)
+        errs.append(np.sum((x / np.linalg.norm(x) - xr) ** 2))
+        assert abs(r["gamma"] ** 2 - errs[-1]) < 1e-12      # gamma = ||r|| in either domain
+        cells += np.bincount(r["codes"], minlength=8)
+    assert abs(np.mean(errs) - mse) / mse < 0.05
+    edges = np.concatenate([[-np.inf], oracle.lloyd_max8()[1], [np.inf]])
+    probs = np.diff(scipy.stats.norm.cdf(edges))
+    np.testing.assert_allclose(cells / cells.sum(), probs, atol=0.01)
+
+
+def test_encode_scale_invariance_and_zero_vector():
+    d = 128
+    D = synth.rotation_signs(d)
+    S = synth.qjl_matrix(d)
+    x = np.random.default_rng(3).standard_normal(d)
+    a = oracle.encode_vector(True, D, S, x)
+    b = oracle.encode_vector(True, D, S, 8.0 * x)
+    np.testing.assert_array_equal(a["codes"], b["codes"])
+    np.testing.assert_array_equal(a["signs"], b["signs"])
+    assert b["n"] == 8.0 * a["n"] and abs(a["gamma"] - b["gamma"]) < 1e-15
+    z = oracle.encode_vector(True, D, S, np.zeros(d))
+    assert z["n"] == 0.0
+    assert np.all(z["codes"] == 4)          # z = 0 sits on the middle threshold: upper cell
+
+
+def test_qjl_given_codes_mode():
+    d = 128
+    D = synth.rotation_signs(d)
+    S = synth.qjl_matrix(d)
+    x = np.random.default_rng(4).standard_normal(d)
+    a = oracle.encode_vector(True, D, S, x)
+    b = oracle.encode_vector(True, D, S, x, codes_in=a["codes"])
+    np.testing.assert_array_equal(a["signs"], b["signs"])
+    codes = a["codes"].copy()
+    codes[0] = (codes[0] + 1) % 8
+    c = oracle.encode_vector(True, D, S, x, codes_in=codes)
+    assert c["codes"][0] == codes[0]
+    assert abs(c["gamma"] - a["gamma"]) > 1e-6
+
+
+def test_qjl_inner_product_estimator_is_unbiased():
+    """Over many Gaussian S, sqrt(pi/2)/m * gamma * <S qbar, sign(S r)> averages to <qbar, r>."""
+    d = 128
+    c, _, _, _ = oracle.lloyd_max8()
+    D = synth.rotation_signs(d)
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal(d)
+    q = rng.standard_normal(d)
+    qbar = oracle.rotate(D, q)
+    ests = []
+    r_true = None
+    for s in range(1500):
+        S = np.random.default_rng([77, s]).standard_normal((d, d)).astype(np.float32)
+        e = oracle.encode_vector(True, D, S, x)
+        y = oracle.rotate(D, x / np.linalg.norm(x))
+        r = y - c[e["codes"]] / math.sqrt(d)
+        if r_true is None:
+            r_true = r
+        bt = 2.0 * e["signs"] - 1.0
+        u = S.astype(np.float64) @ qbar
+        ests.append(math.sqrt(math.pi / 2) / d * e["gamma"] * np.dot(u, bt))
+        np.testing.assert_array_equal(bt, np.where(S.astype(np.float64) @ r >= 0, 1.0, -1.0))
+    ests = np.array(ests)
+    truth = float(np.dot(qbar, r_true))
+    se = ests.std(ddof=1) / math.sqrt(len(ests))
+    assert abs(ests.mean() - truth) < 5 * se
+    # variance of a single-sketch estimate: (pi/2 ||r||^2||q||^2 - <q,r>^2)/m  (closed form)
+    var_pred = (math.pi / 2 * np.dot(r_true, r_true) * np.dot(qbar, qbar) - truth ** 2) / d
+    assert 0.8 < ests.var(ddof=1) / var_pred < 1.25
+
+
+# ------------------------------------------------------------------ bits
+
+def test_bits_per_dim():
+    for d in (128, 256):
+        kb = oracle.record_bytes(True, d) * 8 / (16 * d)
+        vb = oracle.record_bytes(False, d) * 8 / (16 * d)
+        if d == 128:
+            assert kb == 4.25 and vb == 3.125
+            assert abs((kb + vb) / 2 - 3.6) < 0.1
+            assert abs(16 / ((kb + vb) / 2) - 4.339) < 1e-3
+        else:
+            assert kb == 4.125 and vb == 3.0625
+
+
+@pytest.mark.parametrize("is_k", [True, False])
+@pytest.mark.parametrize("d", [128, 256])
+def test_layout_is_a_bijection(is_k, d):
+    seen = set()
+    for t in range(16):
+        for i in range(d):
+            w, b = oracle.bitpos(is_k, d, t, i)
+            assert 0 <= b < 32 and 0 <= w * 32 + b < 16 * d
+            seen.add(w * 32 + b)
+    assert len(seen) == 16 * d
+
+
+def test_pack_unpack_roundtrip():
+    d, H = 128, 2
+    D = synth.rotation_signs(d)
+    S = synth.qjl_matrix(d)
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((40, H, d)).astype(np.float32)
+    slots = rng.permutation(64)[:40].astype(np.int64)
+    for is_k in (True, False):
+        pool = np.zeros((4, H, oracle.record_bytes(is_k, d)), np.uint8)
+        det = oracle.encode(is_k, D, S, x, slots, pool, want_details=True)
+        back = oracle.unpack(is_k, d, pool, H, slots)
+        np.testing.assert_array_equal(back["codes"], det["codes"])
+        if is_k:
+            np.testing.assert_array_equal(back["signs"], det["signs"])
+        for k in range(40):
+            for h in range(H):
+                assert back["n16"][k, h] == oracle.fp16_rne(det["n"][k, h])
+                if is_k:
+                    assert back["g16"][k, h] == oracle.fp16_rne(det["gamma"][k, h])
+
+
+# ------------------------------------------------------------------ attention
+
+def _small_cache(d, B, Hkv, lens, seed=0, same_key=False):
+    D = synth.rotation_signs(d)
+    S = synth.qjl_matrix(d)
+    rng = np.random.default_rng(seed)
+    nb = [max(1, -(-L // 16)) for L in lens]
+    mb = max(nb)
+    perm = rng.permutation(sum(nb) + 3)
+    bt = np.zeros((B, mb), np.int32)
+    k = 0
+    for b in range(B):
+        bt[b, :nb[b]] = perm[k:k + nb[b]]
+        k += nb[b]
+    nblk = sum(nb) + 3
+    kp = np.zeros((nblk, Hkv, oracle.record_bytes(True, d)), np.uint8)
+    vp = np.zeros((nblk, Hkv, oracle.record_bytes(False, d)), np.uint8)
+    for b in range(B):
+        L = lens[b]
+        if L == 0:
+            continue
+        K = rng.standard_normal((L, Hkv, d)).astype(np.float32) * 3
+        V = rng.standard_normal((L, Hkv, d)).astype(np.float32)
+        if same_key:
+            K[:] = K[0]
+        slots = (bt[b, np.arange(L) // 16].astype(np.int64) * 16 + np.arange(L) % 16)
+        oracle.encode(True, D, S, K, slots, kp)
+        oracle.encode(False, D, S, V, slots, vp)
+    return D, S, bt, kp, vp
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_two_attention_formulations_agree(d):
+    B, Hq, Hkv = 2, 4, 2
+    lens = [37, 20]
+    D, S, bt, kp, vp = _small_cache(d, B, Hkv, lens)
+    q = np.random.default_rng(9).standard_normal((B, Hq, d)).astype(np.float32)
+    a = oracle.decode(D, S, q, Hkv, kp, vp, bt, np.array(lens, np.int32))
+    b = oracle.decode(D, S, q, Hkv, kp, vp, bt, np.array(lens, np.int32), explicit=True)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+def _dequant_v(D, det_codes, n16, d):
+    c = oracle.codebook()[0]
+    return oracle.fp16_value(n16) * oracle.rotate_t(D, c[det_codes] / math.sqrt(d))
+
+
+def test_attention_special_cases():
+    d, Hkv = 128, 1
+    # one cached token: output is that token's dequantised value
+    D, S, bt, kp, vp = _small_cache(d, 1, Hkv, [1], seed=3)
+    q = np.random.default_rng(1).standard_normal((1, 2, d)).astype(np.float32)
+    o = oracle.decode(D, S, q, Hkv, kp, vp, bt, np.array([1], np.int32))
+    u = oracle.unpack(False, d, vp, Hkv, np.array([bt[0, 0] * 16], np.int64))
+    want = _dequant_v(D, u["codes"][0, 0], u["n16"][0, 0], d)
+    np.testing.assert_allclose(o[0, 0], want, atol=1e-12)
+    np.testing.assert_allclose(o[0, 1], want, atol=1e-12)
+    # all keys equal: plain mean of the dequantised values
+    L = 23
+    D, S, bt, kp, vp = _small_cache(d, 1, Hkv, [L], seed=4, same_key=True)
+    o = oracle.decode(D, S, q[:, :1], Hkv, kp, vp, bt, np.array([L], np.int32))
+    slots = bt[0, np.arange(L) // 16].astype(np.int64) * 16 + np.arange(L) % 16
+    u = oracle.unpack(False, d, vp, Hkv, slots)
+    mean = np.mean([_dequant_v(D, u["codes"][j, 0], u["n16"][j, 0], d) for j in range(L)], axis=0)
+    np.testing.assert_allclose(o[0, 0], mean, atol=1e-12)
+    # empty context: zeros
+    o = oracle.decode(D, S, q[:, :1], Hkv, kp, vp, bt, np.array([0], np.int32))
+    assert np.all(o == 0)
+
+
+def test_attention_ignores_physical_block_order():
+    d, Hkv = 128, 2
+    D, S, bt, kp, vp = _small_cache(d, 1, Hkv, [50], seed=5)
+    q = np.random.default_rng(2).standard_normal((1, 4, d)).astype(np.float32)
+    o1 = oracle.decode(D, S, q, Hkv, kp, vp, bt, np.array([50], np.int32))
+    # move every block to a new physical id
+    nblk = kp.shape[0]
+    perm = np.random.default_rng(3).permutation(nblk)
+    kp2 = np.zeros_like(kp)
+    vp2 = np.zeros_like(vp)
+    kp2[perm] = kp
+    vp2[perm] = vp
+    bt2 = perm[bt].astype(np.int32)
+    o2 = oracle.decode(D, S, q, Hkv, kp2, vp2, bt2, np.array([50], np.int32))
+    np.testing.assert_array_equal(o1, o2)
+
+
+def test_attention_close_to_uncompressed():
+    """Information only in spirit, but a gross error would show: cosine > 0.9."""
+    d, Hkv, L = 128, 1, 200
+    D = synth.rotation_signs(d)
+    S = synth.qjl_matrix(d)
+    rng = np.random.default_rng(11)
+    K = rng.standard_normal((L, 1, d)).astype(np.float32)
+    V = rng.standard_normal((L, 1, d)).astype(np.float32)
+    q = rng.standard_normal((1, 1, d)).astype(np.float32)
+    kp = np.zeros((13, 1, oracle.record_bytes(True, d)), np.uint8)
+    vp = np.zeros((13, 1, oracle.record_bytes(False, d)), np.uint8)
+    slots = np.arange(L, dtype=np.int64)
+    oracle.encode(True, D, S, K, slots, kp)
+    oracle.encode(False, D, S, V, slots, vp)
+    bt = np.arange(13, dtype=np.int32)[None]
+    o = oracle.decode(D, S, q, 1, kp, vp, bt, np.array([L], np.int32))[0, 0]
+    s = K[:, 0].astype(np.float64) @ q[0, 0] / math.sqrt(d)
+    p = np.exp(s - s.max())
+    p /= p.sum()
+    ref = p @ V[:, 0].astype(np.float64)
+    cos = np.dot(o, ref) / np.linalg.norm(o) / np.linalg.norm(ref)
+    assert cos > 0.9
