@@ -1,0 +1,416 @@
+#!/usr/bin/env python
+"""Benchmark of the TurboQuant compressed-KV decode step on GB300.
+
+A step is the whole hot path for one batch: tq_paged_append of one new token
+per sequence (K and V encode into the paged pools), then decode attention
+over the compressed cache (query prep, split-K pass, merge + inverse WHT).
+Default workload: 16 sequences x 32 query heads / 8 KV heads, d=128, context
+4096 (4095 cached + 1 appended), 16-token blocks scattered by a random
+permutation, bf16 inputs with lognormal per-channel K scales.
+
+Printed (rank 0, one JSON line): GB/s over the algorithmic bytes of a step
+(compressed cache read by decode + block ids + query/output + append traffic),
+the split-K kernel's live CUDA-event time against the measured HBM peak, the
+end-to-end rate through host buffers, and the fp64 CPU oracle timed on this
+machine's cores on a bounded sample.
+
+  python bench.py [--steps K] [--warmup W] [--gpus N] [--impl tq|reference]
+With --impl reference the same metric is measured for the fp64 CPU oracle.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn compressed-KV GB/s & % of GB300 HBM peak; encode Mtok/s vs CPU oracle"
+WORKLOAD = "llama8b_decode"
+L2_BYTES = 129 * 1024 * 1024
+DECODE_SRC = os.path.join(ROOT, "turboquant_compressed_kv_gb300", "csrc", "tq_decode.cu")
+PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_partial_llama8b_decode.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- bytes
+
+def step_bytes(w) -> dict:
+    """Algorithmic bytes of one step: what the method must move."""
+    d, Hkv = w.head_dim, w.n_kv_heads
+    krec, vrec = (8 * d + 64) / 16, (6 * d + 32) / 16      # bytes per token per kv head
+    tokens = sum(w.ctx_lens)
+    cache = tokens * Hkv * (krec + vrec)
+    blocks = sum(math.ceil(L / 16) for L in w.ctx_lens) * 4
+    in_bytes = 2 if w.dtype == "bf16" else 4
+    q = w.batch * w.n_q_heads * d * in_bytes
+    out = w.batch * w.n_q_heads * d * 4
+    app = w.batch * Hkv * (2 * d * in_bytes + krec + vrec) if w.append else 0
+    return dict(cache=cache, blocks=blocks, q=q, out=out, append=app,
+                partial=cache + blocks, step=cache + blocks + q + out + app)
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling while the timed loop runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0=None, t1=None):
+        rows = []
+        for ts, ln in self.lines:
+            if t0 is not None and not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- oracle (CPU) arm
+
+def oracle_sample_setup(w, nseq):
+    """Cache of the first nseq sequences written by the oracle (setup, untimed)."""
+    import numpy as np
+
+    import oracle
+    from turboquant_compressed_kv_gb300 import synth
+    d = w.head_dim
+    D, S = synth.rotation_signs(d), synth.qjl_matrix(d)
+    bt, nblk = synth.block_tables(w)
+    bt = bt[:nseq]
+    used = np.unique(bt)
+    remap = {int(b): i for i, b in enumerate(used)}
+    bt_s = np.vectorize(remap.get)(bt).astype(np.int32)
+    kp = np.zeros((len(used), w.n_kv_heads, 8 * d + 64), np.uint8)
+    vp = np.zeros((len(used), w.n_kv_heads, 6 * d + 32), np.uint8)
+    for b in range(nseq):
+        L = w.prefill_lens[b]
+        K, V = synth.kv_tokens(w, b, 0, L)
+        sl = synth.slots_for(bt_s, b, 0, L)
+        oracle.encode(True, D, S, K, sl, kp)
+        oracle.encode(False, D, S, V, sl, vp)
+    q = synth.queries(w)[:nseq]
+    kn = np.empty((nseq, w.n_kv_heads, d), np.float32)
+    vn = np.empty_like(kn)
+    for b in range(nseq):
+        k1, v1 = synth.kv_tokens(w, b, w.prefill_lens[b], 1)
+        kn[b], vn[b] = k1[0], v1[0]
+    return dict(D=D, S=S, bt=bt_s, kp=kp, vp=vp, q=q, kn=kn, vn=vn, nseq=nseq)
+
+
+def oracle_step(w, st):
+    import numpy as np
+
+    import oracle
+    from turboquant_compressed_kv_gb300 import synth
+    n = st["nseq"]
+    slots = np.array([synth.slots_for(st["bt"], b, w.prefill_lens[b], 1)[0] for b in range(n)], np.int64)
+    if w.append:
+        oracle.encode(True, st["D"], st["S"], st["kn"], slots, st["kp"])
+        oracle.encode(False, st["D"], st["S"], st["vn"], slots, st["vp"])
+    ctx = np.array(w.ctx_lens[:n], np.int32)
+    return oracle.decode(st["D"], st["S"], st["q"], w.n_kv_heads, st["kp"], st["vp"], st["bt"], ctx)
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_cpu_oracle(w, steps, warmup, nseq):
+    """Times the oracle (as it stands) on the first nseq sequences; returns (GB/s, seconds/step)."""
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores()))
+    from turboquant_compressed_kv_gb300 import synth
+    import dataclasses
+    ws = dataclasses.replace(w, batch=nseq, ctx_lens=w.ctx_lens[:nseq], prefill_lens=w.prefill_lens[:nseq])
+    st = oracle_sample_setup(w, nseq)
+    for _ in range(warmup):
+        oracle_step(w, st)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(w, st)
+    dt = (time.perf_counter() - t0) / steps
+    return step_bytes(ws)["step"] / dt / 1e9, dt, ws
+
+
+def bench_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from turboquant_compressed_kv_gb300 import synth
+    w = synth.workload(WORKLOAD)
+    nseq = 1
+    gbs, dt, ws = run_cpu_oracle(w, args.steps, args.warmup, nseq)
+    n = int(os.environ.get("OMP_NUM_THREADS", cores()))
+    sample = (f"{nseq} of {w.batch} sequences per step: append 1 token x {w.n_kv_heads} kv heads (K+V), "
+              f"decode {w.n_q_heads} query heads over {w.ctx_lens[0]} tokens")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, "fp64 CPU oracle, per-step sample"),
+        "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def workload_config(w, l2_note):
+    return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+            "head_dim": w.head_dim, "ctx": w.ctx_lens[0], "block_size": 16, "kv_dtype_in": w.dtype,
+            "k_scales": w.k_scale, "parallelism": "replicas (one independent batch per GPU)", "l2": l2_note}
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def profile_traffic(bytes_per_launch):
+    """dram bytes per launch from the committed ncu summary, if taken on the current kernel source."""
+    try:
+        with open(PROFILE_JSON) as f:
+            prof = json.load(f)
+        src_hash = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()[:16]
+        if prof.get("source_sha256_16") != src_hash:
+            return None
+        return float(prof["dram_bytes_per_launch_full"])
+    except Exception:
+        return None
+
+
+def bench_tq(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import turboquant_compressed_kv_gb300 as tq
+    from turboquant_compressed_kv_gb300 import synth
+    from turboquant_compressed_kv_gb300.cache import PagedCache, to_device
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tq.load_library()
+
+    w = synth.workload(WORKLOAD)
+    d, B, Hq, Hkv = w.head_dim, w.batch, w.n_q_heads, w.n_kv_heads
+    nb = step_bytes(w)
+    cache = PagedCache.create(w, dev)
+    cache.prefill()
+    # Cycle through enough identical cache copies that a step's reads miss L2.
+    per_cache = cache.k_pool.numel() + cache.v_pool.numel()
+    nrep = max(2, math.ceil(3 * L2_BYTES / per_cache))
+    pools = [(cache.k_pool, cache.v_pool)] + [(cache.k_pool.clone(), cache.v_pool.clone())
+                                              for _ in range(nrep - 1)]
+    K1, V1 = cache.append_inputs()
+    q_np = synth.queries(w)
+    k_new = to_device(K1, w.dtype, dev)
+    v_new = to_device(V1, w.dtype, dev)
+    q = to_device(q_np, w.dtype, dev)
+    pre = torch.tensor(w.prefill_lens, dtype=torch.int32, device=dev)
+    ctx = torch.tensor(w.ctx_lens, dtype=torch.int32, device=dev)
+    max_ctx = max(w.ctx_lens)
+    ws = torch.empty(tq.decode_workspace_bytes(d, B, Hq, max_ctx), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    launches_per_step = 4
+
+    def step(i, ev=None):
+        kp, vp = pools[i % nrep]
+        tq.paged_append(cache.params, d, k_new, v_new, cache.block_table, pre, kp, vp, status=status)
+        tq.decode_qprep(cache.params, d, q, Hkv, max_ctx, ws)
+        if ev is not None:
+            ev[0].record(stream)
+        tq.decode_partial(cache.params, d, B, Hq, Hkv, kp, vp, cache.block_table, ctx, max_ctx, ws, status=status)
+        if ev is not None:
+            ev[1].record(stream)
+        tq.decode_merge(cache.params, d, B, Hq, Hkv, ctx, max_ctx, out, ws)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    # device-time loop: K steps, kernel events inside, one event pair around all
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    t_wall0 = time.time()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(i, kev[i])
+    e1.record(stream)
+    barrier()
+    t_wall1 = time.time()
+    total_ms = e0.elapsed_time(e1)
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    # keep the GPU busy a little longer so the sampler sees the loaded clocks
+    t_c0 = time.time()
+    while time.time() - t_c0 < 1.0:
+        for i in range(50):
+            step(i)
+        torch.cuda.synchronize(dev)
+    t_c1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t_wall0 - 0.15, t_c1)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} during the bench")
+
+    # end-to-end through the public API with pinned host buffers
+    hq = torch.from_numpy(np.ascontiguousarray(q_np)).to(q.dtype).pin_memory()
+    hk = torch.from_numpy(np.ascontiguousarray(K1)).to(k_new.dtype).pin_memory()
+    hv = torch.from_numpy(np.ascontiguousarray(V1)).to(v_new.dtype).pin_memory()
+    hout = torch.empty((B, Hq, d), dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+
+    def e2e_step(i):
+        kp, vp = pools[i % nrep]
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        tq.paged_append(cache.params, d, dk, dv, cache.block_table, pre, kp, vp)
+        tq.decode_attn(cache.params, d, dq, Hkv, kp, vp, cache.block_table, ctx, max_ctx, out=out, workspace=ws)
+        hout.copy_(out, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    barrier()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        e2e_step(i)
+    barrier()
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    h2d = hq.numel() * hq.element_size() + hk.numel() * hk.element_size() + hv.numel() * hv.element_size()
+    d2h = hout.numel() * 4
+
+    # max over ranks
+    t = torch.tensor([total_ms, e2e_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, e2e_s = float(t[0]), float(t[1])
+    ms_step = total_ms / args.steps
+    value = world * nb["step"] / (ms_step * 1e-3) / 1e9
+    e2e_value = world * nb["step"] / e2e_s / 1e9
+
+    kern_avg_ms = statistics.mean(kern_ms)
+    achieved = nb["partial"] / (kern_avg_ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    traffic = profile_traffic(nb["partial"])
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(w, f"{nrep} cache copies cycled ({nrep * per_cache / 2**20:.0f} MiB > L2), "
+                                     "no flush needed"),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 3), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "decode split-K pass (tq_decode_partial)", "peak_source": peak_kind,
+                     "kernel_ms": round(kern_avg_ms, 6), "bytes_per_launch": nb["partial"]},
+        "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
+                   "samples": clocks["samples"]},
+        "bytes_per_step": nb,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, dt, _ = run_cpu_oracle(w, 3, 1, 2)
+        line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
+                                "kind": "oracle",
+                                "sample": "2 of 16 sequences, full step (append + decode of 32 heads over 4096 "
+                                          "tokens), 3 timed repetitions"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return bench_reference(args)
+    return bench_tq(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

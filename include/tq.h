@@ -1,0 +1,190 @@
+/*
+ * tq.h -- C ABI of the TurboQuant compressed KV-cache library for GB300 (sm_103a).
+ *
+ * Method sources (cited by page title and section):
+ *  [README] "SwiftLM" (nomorevibe.com/p/swiftlm), section "TurboQuantization:
+ *           KV Cache Compression" -> "The Algorithm": K-Cache steps 1-5
+ *           (4.25 bits/dim) and the V-Cache paragraph (3.125 bits/dim).
+ *  [ART]    "SwiftLM ... Swift製LLM推論サーバー" (lilting.ch): "Lloyd-Maxコードブックとは"
+ *           (8 levels for N(0,1/d), computed once before inference), "KVキャッシュ圧縮の内訳",
+ *           "Walsh-Hadamard Transform（WHT）の役割".
+ *  [VLLM]   "論文解説: vLLM-MLX" (0h-n0.github.io), "Paged KVキャッシュ": fixed-size
+ *           blocks addressed through a block table.
+ *
+ * Conventions shared by every entry point
+ *  - head_dim d is 128 or 256; a paged block holds TQ_BLOCK_SIZE (16) token slots.
+ *  - Device pointers are plain CUDA device addresses owned by the caller; the
+ *    library allocates nothing and keeps no state between calls.
+ *  - Every call is asynchronous and ordered on `stream` (a cudaStream_t; NULL =
+ *    legacy default stream), except tq_codebook_init, which synchronises it.
+ *  - Return value: TQ_OK (0) or a negative TQ_ERR_* code.  All argument errors
+ *    are detected on the host before anything is launched.  Errors the host
+ *    cannot see (a block id or slot outside the pool) are reported by the
+ *    kernels in the optional device word `status` (bitwise OR of TQ_STATUS_*);
+ *    the offending element is skipped, never trapped.
+ *  - A K pool is uint8[num_blocks][n_kv_heads][tq_k_record_bytes(d)], a V pool
+ *    uint8[num_blocks][n_kv_heads][tq_v_record_bytes(d)]; both 16-byte aligned.
+ *    A record packs the 16 slots of one block for one kv head: three bit-planes
+ *    of the 3-bit Lloyd-Max cell index (plus, for K, one plane of QJL sign bits),
+ *    followed by fp16 norms (K: ||x|| and ||r|| per slot; V: ||v|| per slot).
+ *  - A slot index is block * 16 + offset.
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *tq_stream_t;   /* identical to cudaStream_t */
+
+#define TQ_BLOCK_SIZE 16
+
+enum {
+    TQ_OK = 0,
+    TQ_ERR_INVALID = -1,        /* a size or count out of range, or a NULL required pointer */
+    TQ_ERR_HEAD_DIM = -2,       /* d is not 128 or 256 */
+    TQ_ERR_GQA = -3,            /* n_q_heads is not a multiple of n_kv_heads, or group > 8 */
+    TQ_ERR_WORKSPACE = -4,      /* workspace or params buffer too small */
+    TQ_ERR_CUDA = -5,           /* a CUDA runtime call or kernel launch failed */
+    TQ_ERR_DTYPE = -6,          /* dtype is not TQ_DTYPE_F32 or TQ_DTYPE_BF16 */
+    TQ_ERR_ALIGN = -7           /* a pool, params or workspace pointer is not 16-byte aligned */
+};
+
+enum { TQ_DTYPE_F32 = 0, TQ_DTYPE_BF16 = 1 };
+
+enum {
+    TQ_STATUS_BAD_SLOT = 1,     /* a slot or block id outside [0, num_blocks) was skipped */
+    TQ_STATUS_BAD_PARAMS = 2    /* the params buffer was not initialised for this d */
+};
+
+/* Bytes of one packed record (16 slots, one kv head).
+ * d=128: K 1088 (= 4.25 bits/dim), V 800 (= 3.125 bits/dim).
+ * d=256: K 2112 (4.125 bits/dim), V 1568 (3.0625 bits/dim).  0 for another d. */
+size_t tq_k_record_bytes(int d);
+size_t tq_v_record_bytes(int d);
+
+/* Size of the device params buffer for head_dim d (0 for an unsupported d). */
+size_t tq_params_bytes(int d);
+
+/* tq_codebook_init -- build the device params for head_dim d.
+ * [ART "Lloyd-Maxコードブックとは": the 8-level Lloyd-Max codebook of the
+ * Gaussian is computed once, before inference, with no calibration data;
+ * README K-Cache steps 2 and 5: the random WHT signs and the QJL matrix.]
+ *   D_host      host int8[d], the rotation's random sign diagonal (+1/-1).
+ *   S_host      host float[d*d], the QJL Gaussian matrix, row-major (row k
+ *               produces sign bit k).
+ *   params_dev  device buffer of >= tq_params_bytes(d) bytes, 16-byte aligned.
+ *   centroids_out8  optional host double[8]: the codebook (unit variance).
+ * The codebook is solved by a kernel in fp64 (fixed-point Lloyd-Max), stored
+ * in fp32.  Copies D and S to the device and derives the tables the kernels
+ * use.  Synchronises `stream`.  Errors: TQ_ERR_HEAD_DIM, TQ_ERR_INVALID (NULL
+ * or a D entry not +-1), TQ_ERR_WORKSPACE, TQ_ERR_ALIGN, TQ_ERR_CUDA. */
+int tq_codebook_init(int d, const int8_t *D_host, const float *S_host, void *params_dev,
+                     size_t params_bytes, double *centroids_out8, tq_stream_t stream);
+
+/* tq_encode_k -- compress keys into a paged K pool.
+ * [README K-Cache steps 1-5; ART "KVキャッシュ圧縮の内訳" steps 1-5]
+ * For every (token, kv head) vector x (length d): n = ||x||; y = Pi (x/n) with
+ * Pi = H diag(D)/sqrt(d); cell_i = number of Lloyd-Max thresholds <= sqrt(d) y_i;
+ * r = y - c[cell]/sqrt(d); gamma = ||r||; sign bit k = [(S r)_k >= 0].
+ * Stores cells, sign bits, fp16(n), fp16(gamma) at slot slot_mapping[token].
+ *   params        device params of head_dim d (tq_codebook_init).
+ *   k             device [n_tokens][n_kv_heads][d], dtype TQ_DTYPE_F32 or _BF16, contiguous.
+ *   slot_mapping  device int64[n_tokens]; a slot outside the pool is skipped
+ *                 and flagged TQ_STATUS_BAD_SLOT; a negative slot is skipped silently
+ *                 (padding).
+ *   k_pool        device K pool with num_blocks blocks.
+ *   status        optional device int32 (may be NULL).
+ * n_tokens == 0 is a no-op.  Errors: TQ_ERR_INVALID, TQ_ERR_HEAD_DIM,
+ * TQ_ERR_DTYPE, TQ_ERR_ALIGN, TQ_ERR_CUDA. */
+int tq_encode_k(const void *params, int d, const void *k, int dtype, int64_t n_tokens,
+                int n_kv_heads, const int64_t *slot_mapping, void *k_pool, int64_t num_blocks,
+                int32_t *status, tq_stream_t stream);
+
+/* tq_encode_v -- compress values into a paged V pool: steps 1-3 only, no
+ * residual and no QJL [README V-Cache paragraph; ART "KVキャッシュ圧縮の内訳", V].
+ * Stores cells and fp16(||v||).  Arguments and errors as tq_encode_k. */
+int tq_encode_v(const void *params, int d, const void *v, int dtype, int64_t n_tokens,
+                int n_kv_heads, const int64_t *slot_mapping, void *v_pool, int64_t num_blocks,
+                int32_t *status, tq_stream_t stream);
+
+/* tq_paged_append -- encode one new token per sequence into its next slot.
+ * [VLLM "Paged KVキャッシュ"; README K-Cache and V-Cache]
+ * For sequence b the slot is block_table[b][ctx_lens[b]/16]*16 + ctx_lens[b]%16,
+ * i.e. ctx_lens holds the lengths BEFORE the append (the library does not
+ * update them).
+ *   k_new, v_new  device [batch][n_kv_heads][d] in dtype.
+ *   block_table   device int32[batch][max_blocks].
+ *   ctx_lens      device int32[batch]; a sequence with ctx_lens[b] < 0 is skipped,
+ *                 one whose slot falls outside its table or the pool is flagged
+ *                 TQ_STATUS_BAD_SLOT and skipped.
+ * Every byte of a record belongs to one slot, so sequences may share a block;
+ * two sequences appending into the same slot race.  One kernel launch.
+ * Errors: as tq_encode_k. */
+int tq_paged_append(const void *params, int d, const void *k_new, const void *v_new, int dtype,
+                    int batch, int n_kv_heads, const int32_t *block_table, int max_blocks,
+                    const int32_t *ctx_lens, void *k_pool, void *v_pool, int64_t num_blocks,
+                    int32_t *status, tq_stream_t stream);
+
+/* Workspace bytes tq_decode_attn needs for this shape (0 for invalid sizes). */
+size_t tq_decode_workspace_bytes(int d, int batch, int n_q_heads, int max_ctx);
+
+/* tq_decode_attn -- one decode step of attention over the compressed paged cache.
+ * [README "The Algorithm" (fused dequantisation inside attention);
+ *  VLLM "Paged KVキャッシュ"]
+ * For query head h of sequence b (kv head h / (n_q_heads/n_kv_heads)), over the
+ * ctx_lens[b] cached tokens (token j in block block_table[b][j/16], slot j%16):
+ *   qbar = Pi q,  u = S qbar,
+ *   s_j  = (n_j/sqrt d) ( <qbar, c[cell_j]>/sqrt d + gamma_j sqrt(pi/2)/d <u, 2 sign_j - 1> ),
+ *   P    = softmax(s),  a = sum_j P_j nv_j c[vcell_j]/sqrt d,  out = Pi^T a.
+ * The scores are computed in the rotated domain, so no key or value is
+ * reconstructed; one inverse rotation per (b, h) is applied at the end.
+ *   q          device [batch][n_q_heads][d] in dtype.
+ *   ctx_lens   device int32[batch]; each must be <= max_ctx (larger values are
+ *              clamped to max_ctx); 0 gives out = 0.
+ *   max_ctx    host upper bound of ctx_lens, sizes the context split.
+ *   out        device float[batch][n_q_heads][d].
+ *   workspace  device scratch of >= tq_decode_workspace_bytes(...) bytes.
+ * n_q_heads/n_kv_heads must be 1..8.  Errors: TQ_ERR_INVALID, TQ_ERR_HEAD_DIM,
+ * TQ_ERR_GQA, TQ_ERR_DTYPE, TQ_ERR_WORKSPACE, TQ_ERR_ALIGN, TQ_ERR_CUDA. */
+int tq_decode_attn(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads,
+                   int n_kv_heads, const void *k_pool, const void *v_pool, int64_t num_blocks,
+                   const int32_t *block_table, int max_blocks, const int32_t *ctx_lens,
+                   int max_ctx, float *out, void *workspace, size_t workspace_bytes,
+                   int32_t *status, tq_stream_t stream);
+
+/* The three stages of tq_decode_attn as separate calls, for callers that
+ * schedule or time them individually.  Called in this order on one stream with
+ * the same shape arguments and workspace, they compute exactly what
+ * tq_decode_attn computes; argument meanings and errors are as there.
+ *   tq_decode_qprep   qbar = Pi q and u = S qbar for every (sequence, query head),
+ *                     written to the workspace.
+ *   tq_decode_partial the pass over the cache: per (sequence, kv head, context
+ *                     split of 512 tokens) the online-softmax state (max score,
+ *                     sum of weights, weighted value sum in the rotated domain)
+ *                     of every query head of the group, written to the workspace.
+ *   tq_decode_merge   combines the splits of each (sequence, query head) and
+ *                     applies the inverse rotation: out = Pi^T a. */
+int tq_decode_qprep(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads,
+                    int n_kv_heads, int max_ctx, void *workspace, size_t workspace_bytes,
+                    tq_stream_t stream);
+int tq_decode_partial(const void *params, int d, int batch, int n_q_heads, int n_kv_heads,
+                      const void *k_pool, const void *v_pool, int64_t num_blocks,
+                      const int32_t *block_table, int max_blocks, const int32_t *ctx_lens,
+                      int max_ctx, void *workspace, size_t workspace_bytes, int32_t *status,
+                      tq_stream_t stream);
+int tq_decode_merge(const void *params, int d, int batch, int n_q_heads, int n_kv_heads,
+                    const int32_t *ctx_lens, int max_ctx, float *out, void *workspace,
+                    size_t workspace_bytes, tq_stream_t stream);
+
+/* Short English text for a TQ_* return code (static storage). */
+const char *tq_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TQ_H_ */

@@ -1,0 +1,255 @@
+"""GPU parity: the CUDA library (through the C ABI) against the fp64 oracle.
+
+Small cases run the oracle on every output; they span several paged blocks
+and context splits with ragged tails.  Tolerances are in tests/parity.py.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import parity
+
+torch = pytest.importorskip("torch")
+import turboquant_compressed_kv_gb300 as tq  # noqa: E402
+from turboquant_compressed_kv_gb300 import synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+FILL = 0xA5
+
+
+def _params(d):
+    D = synth.rotation_signs(d)
+    S = synth.qjl_matrix(d)
+    params, cent = tq.codebook_init(d, D, S, device=DEV)
+    return D, S, params, cent
+
+
+def _upload(x, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    return (t.to(torch.bfloat16) if dtype == "bf16" else t).to(DEV)
+
+
+def _inputs(N, H, d, dtype, seed, outliers=True):
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((N, H, d)).astype(np.float32)
+    if outliers:
+        x *= rng.lognormal(0, 1, (1, H, d)).astype(np.float32)
+        x[:, :, 3] *= 20
+    if N > 2:
+        x[1] = 0.0          # zero vectors
+    return synth.round_dtype(x, dtype)
+
+
+def _slot_owner(is_k, d):
+    """byte offset within a record -> owning slot (from the oracle's layout)."""
+    rec = oracle.record_bytes(is_k, d)
+    owner = np.full(rec, -1, np.int64)
+    planes = 4 if is_k else 3
+    for t in range(16):
+        for i in range(d):
+            w, b = oracle.bitpos(is_k, d, t, i)
+            for p in range(planes):
+                owner[p * 2 * d + w * 4 + b // 8] = t
+    nb = 4 if is_k else 2
+    base = planes * 2 * d
+    for t in range(16):
+        owner[base + nb * t: base + nb * (t + 1)] = t
+    assert (owner >= 0).all()
+    return owner
+
+
+# ------------------------------------------------------------------ codebook
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_codebook_on_device(d):
+    _, _, params, cent = _params(d)
+    c, t, _, _ = oracle.codebook()
+    # both sides stop a linearly convergent iteration at a step below 1e-15;
+    # the fp32 values the kernels use must be identical (checked below)
+    np.testing.assert_allclose(cent, c, rtol=0, atol=1e-12)
+    hdr = params[:256].cpu().numpy()
+    cf = hdr[16:48].view(np.float32)
+    tf = hdr[48:80].view(np.float32)
+    np.testing.assert_array_equal(cf, c.astype(np.float32))
+    np.testing.assert_array_equal(tf[:7], t.astype(np.float32))
+
+
+# ------------------------------------------------------------------ encode
+
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("is_k", [True, False])
+def test_encode_parity(d, dtype, is_k):
+    H, N, nblk = 3, 203, 20
+    D, S, params, _ = _params(d)
+    x = _inputs(N, H, d, dtype, seed=d + (7 if is_k else 0))
+    slots = np.random.default_rng(1).permutation(nblk * 16)[:N].astype(np.int64)
+    rec = tq.k_record_bytes(d) if is_k else tq.v_record_bytes(d)
+    pool = torch.full((nblk, H, rec), FILL, dtype=torch.uint8, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    fn = tq.encode_k if is_k else tq.encode_v
+    fn(params, d, _upload(x, dtype), torch.from_numpy(slots).to(DEV), pool, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    gp = pool.cpu().numpy()
+    st = parity.check_encode(is_k, D, S, x, slots, gp, pool_fill=FILL)
+    assert st["entries"] == N * H * d
+    # bytes of slots that were not written keep the fill pattern
+    owner = _slot_owner(is_k, d)
+    written = np.zeros((nblk, 16), bool)
+    written[slots // 16, slots % 16] = True
+    for blk in range(nblk):
+        untouched = ~written[blk][owner]
+        assert np.all(gp[blk][:, untouched] == FILL)
+
+
+def test_encode_skips_bad_slots_and_flags():
+    d, H = 128, 2
+    D, S, params, _ = _params(d)
+    x = _inputs(5, H, d, "f32", seed=3)
+    slots = np.array([0, 17, -1, 10_000, 33], np.int64)
+    pool = torch.full((4, H, tq.k_record_bytes(d)), FILL, dtype=torch.uint8, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tq.encode_k(params, d, _upload(x, "f32"), torch.from_numpy(slots).to(DEV), pool, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & tq.STATUS_BAD_SLOT
+    ok = np.array([0, 1, 4])
+    parity.check_encode(True, D, S, x[ok], slots[ok], pool.cpu().numpy(), pool_fill=FILL)
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_paged_append_parity(d):
+    H, B = 2, 6
+    D, S, params, _ = _params(d)
+    lens = np.array([0, 15, 16, 33, 100, -1], np.int32)      # -1: skipped
+    mb = 8
+    bt = np.random.default_rng(5).permutation(B * mb).reshape(B, mb).astype(np.int32)
+    nblk = B * mb
+    kp = torch.full((nblk, H, tq.k_record_bytes(d)), FILL, dtype=torch.uint8, device=DEV)
+    vp = torch.full((nblk, H, tq.v_record_bytes(d)), FILL, dtype=torch.uint8, device=DEV)
+    k = _inputs(B, H, d, "bf16", seed=11)
+    v = _inputs(B, H, d, "bf16", seed=12)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tq.paged_append(params, d, _upload(k, "bf16"), _upload(v, "bf16"), torch.from_numpy(bt).to(DEV),
+                    torch.from_numpy(lens).to(DEV), kp, vp, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    sel = np.array([b for b in range(B) if lens[b] >= 0])
+    slots = np.array([bt[b, lens[b] // 16] * 16 + lens[b] % 16 for b in sel], np.int64)
+    parity.check_encode(True, D, S, k[sel], slots, kp.cpu().numpy(), pool_fill=FILL)
+    parity.check_encode(False, D, S, v[sel], slots, vp.cpu().numpy(), pool_fill=FILL)
+    for pool, is_k in ((kp, True), (vp, False)):
+        gp = pool.cpu().numpy()
+        owner = _slot_owner(is_k, d)
+        written = np.zeros((nblk, 16), bool)
+        written[slots // 16, slots % 16] = True
+        for blk in range(nblk):
+            assert np.all(gp[blk][:, ~written[blk][owner]] == FILL)
+
+
+# ------------------------------------------------------------------ decode
+
+def _build_cache(d, Hkv, lens, dtype, seed, spare=3):
+    """Paged cache written by the oracle (CPU) and uploaded: the GPU decode and
+    the oracle decode then read the very same packed records."""
+    D, S, params, _ = _params(d)
+    B = len(lens)
+    need = [max(1, -(-L // 16)) for L in lens]
+    mb = max(need)
+    nblk = sum(need) + spare
+    perm = np.random.default_rng(seed).permutation(nblk)
+    bt = np.zeros((B, mb), np.int32)
+    k0 = 0
+    for b in range(B):
+        bt[b, :need[b]] = perm[k0:k0 + need[b]]
+        k0 += need[b]
+    kp = np.zeros((nblk, Hkv, oracle.record_bytes(True, d)), np.uint8)
+    vp = np.zeros((nblk, Hkv, oracle.record_bytes(False, d)), np.uint8)
+    for b, L in enumerate(lens):
+        if L == 0:
+            continue
+        K = _inputs(L, Hkv, d, dtype, seed=seed * 100 + b)
+        V = _inputs(L, Hkv, d, dtype, seed=seed * 100 + b + 50, outliers=False)
+        sl = synth.slots_for(bt, b, 0, L)
+        oracle.encode(True, D, S, K, sl, kp)
+        oracle.encode(False, D, S, V, sl, vp)
+    return D, S, params, bt, kp, vp
+
+
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 4, 1), (128, 8, 2), (128, 16, 2), (128, 3, 3), (256, 4, 2)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_parity(d, Hq, Hkv, dtype):
+    lens = [1, 17, 512, 513, 1100, 0, 16, 700]
+    D, S, params, bt, kp, vp = _build_cache(d, Hkv, lens, dtype, seed=Hq + d)
+    B = len(lens)
+    q = synth.round_dtype(np.random.default_rng(9).standard_normal((B, Hq, d)).astype(np.float32), dtype)
+    ctx = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = tq.decode_attn(params, d, _upload(q, dtype), Hkv, torch.from_numpy(kp).to(DEV),
+                         torch.from_numpy(vp).to(DEV), torch.from_numpy(bt).to(DEV), ctx, max(lens), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o = out.cpu().numpy()
+    ref = oracle.decode(D, S, q, Hkv, kp, vp, bt, np.array(lens, np.int32))
+    assert np.all(o[lens.index(0)] == 0)
+    parity.check_attention(o, ref)
+
+
+def test_tiny_workload_end_to_end():
+    """1 sequence, 1 head, d=128, 256 fp32 tokens with 20x outlier channels:
+    GPU encode vs oracle encode, then GPU decode vs oracle decode of the
+    oracle-written cache."""
+    w = synth.workload("tiny")
+    from turboquant_compressed_kv_gb300.cache import PagedCache
+    cache = PagedCache.create(w, DEV)
+    cache.prefill()
+    K, V = synth.kv_tokens(w, 0, 0, 256)
+    slots = synth.slots_for(cache.block_table_np, 0, 0, 256)
+    parity.check_encode(True, cache.D, cache.S, K, slots, cache.k_pool.cpu().numpy())
+    parity.check_encode(False, cache.D, cache.S, V, slots, cache.v_pool.cpu().numpy())
+    kp = np.zeros(tuple(cache.k_pool.shape), np.uint8)
+    vp = np.zeros(tuple(cache.v_pool.shape), np.uint8)
+    oracle.encode(True, cache.D, cache.S, K, slots, kp)
+    oracle.encode(False, cache.D, cache.S, V, slots, vp)
+    q = synth.queries(w)
+    out = tq.decode_attn(cache.params, 128, _upload(q, "f32"), 1, torch.from_numpy(kp).to(DEV),
+                         torch.from_numpy(vp).to(DEV), cache.block_table,
+                         torch.tensor([256], dtype=torch.int32, device=DEV), 256)
+    ref = oracle.decode(cache.D, cache.S, q, 1, kp, vp, cache.block_table_np, np.array([256], np.int32))
+    parity.check_attention(out.cpu().numpy(), ref)
+
+
+def test_decode_rejects_bad_arguments():
+    d = 128
+    _, _, params, _ = _params(d)
+    q = torch.zeros((1, 4, d), device=DEV)
+    kp = tq.empty_pool(1, 1, d, "k", DEV)
+    vp = tq.empty_pool(1, 1, d, "v", DEV)
+    bt = torch.zeros((1, 1), dtype=torch.int32, device=DEV)
+    ctx = torch.ones(1, dtype=torch.int32, device=DEV)
+    with pytest.raises(tq.TQError, match="multiple"):
+        tq.decode_attn(params, d, q, 3, kp, vp, bt, ctx, 16)
+    with pytest.raises(tq.TQError, match="head_dim"):
+        tq.decode_attn(params, 64, q, 1, kp, vp, bt, ctx, 16)
+    ws = torch.empty(16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(tq.TQError, match="workspace"):
+        tq.decode_attn(params, d, q, 1, kp, vp, bt, ctx, 16, workspace=ws)
+
+
+def test_decode_bad_block_id_is_flagged():
+    d = 128
+    D, S, params, bt, kp, vp = _build_cache(d, 1, [40], "f32", seed=2)
+    kp = torch.from_numpy(kp).to(DEV)
+    vp = torch.from_numpy(vp).to(DEV)
+    bt_bad = bt.copy()
+    bt_bad[0, 1] = 10_000
+    q = np.random.default_rng(0).standard_normal((1, 2, d)).astype(np.float32)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = tq.decode_attn(params, d, _upload(q, "f32"), 1, kp, vp, torch.from_numpy(bt_bad).to(DEV),
+                         torch.tensor([40], dtype=torch.int32, device=DEV), 40, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & tq.STATUS_BAD_SLOT
+    assert np.all(np.isfinite(out.cpu().numpy()))

@@ -1,0 +1,248 @@
+"""TurboQuant compressed KV cache on GB300: Python binding of libtq.so.
+
+Thin ctypes marshalling over the C ABI in include/tq.h; every step of the
+path runs in the library's CUDA kernels.  PyTorch supplies device memory and
+the current stream.  Importing works without a GPU; calling a compute entry
+point without the built library raises immediately (there is no fallback).
+
+Entry points (same names as the C ABI, minus the ``tq_`` prefix):
+  codebook_init, encode_k, encode_v, paged_append, decode_attn,
+  params_bytes, k_record_bytes, v_record_bytes, decode_workspace_bytes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_build", "libtq.so")
+
+BLOCK_SIZE = 16
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+STATUS_BAD_SLOT = 1
+STATUS_BAD_PARAMS = 2
+
+_lib = None
+
+
+class TQError(RuntimeError):
+    pass
+
+
+def load_library(path: str | None = None):
+    """Load libtq.so (built by turboquant_compressed_kv_gb300.build.build())."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise TQError(f"libtq.so not found at {p}; build it with "
+                      "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(p)
+    _declare(L)
+    if path is None:
+        _lib = L
+    return L
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+
+def _declare(L):
+    L.tq_k_record_bytes.restype = _SZ
+    L.tq_k_record_bytes.argtypes = [_I]
+    L.tq_v_record_bytes.restype = _SZ
+    L.tq_v_record_bytes.argtypes = [_I]
+    L.tq_params_bytes.restype = _SZ
+    L.tq_params_bytes.argtypes = [_I]
+    L.tq_error_string.restype = ctypes.c_char_p
+    L.tq_error_string.argtypes = [_I]
+    L.tq_codebook_init.restype = _I
+    L.tq_codebook_init.argtypes = [_I, _P, _P, _P, _SZ, _P, _P]
+    for name in ("tq_encode_k", "tq_encode_v"):
+        f = getattr(L, name)
+        f.restype = _I
+        f.argtypes = [_P, _I, _P, _I, _I64, _I, _P, _P, _I64, _P, _P]
+    L.tq_paged_append.restype = _I
+    L.tq_paged_append.argtypes = [_P, _I, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P, _I64, _P, _P]
+    L.tq_decode_workspace_bytes.restype = _SZ
+    L.tq_decode_workspace_bytes.argtypes = [_I, _I, _I, _I]
+    L.tq_decode_attn.restype = _I
+    L.tq_decode_attn.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _SZ,
+                                 _P, _P]
+    L.tq_decode_qprep.restype = _I
+    L.tq_decode_qprep.argtypes = [_P, _I, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]
+    L.tq_decode_partial.restype = _I
+    L.tq_decode_partial.argtypes = [_P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _SZ, _P, _P]
+    L.tq_decode_merge.restype = _I
+    L.tq_decode_merge.argtypes = [_P, _I, _I, _I, _I, _P, _I, _P, _P, _SZ, _P]
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        msg = load_library().tq_error_string(rc).decode()
+        raise TQError(f"{what} failed: {msg} (code {rc})")
+
+
+# ---------------------------------------------------------------- sizes
+
+def params_bytes(d: int) -> int:
+    return int(load_library().tq_params_bytes(d))
+
+
+def k_record_bytes(d: int) -> int:
+    return int(load_library().tq_k_record_bytes(d))
+
+
+def v_record_bytes(d: int) -> int:
+    return int(load_library().tq_v_record_bytes(d))
+
+
+def decode_workspace_bytes(d: int, batch: int, n_q_heads: int, max_ctx: int) -> int:
+    return int(load_library().tq_decode_workspace_bytes(d, batch, n_q_heads, max_ctx))
+
+
+# ---------------------------------------------------------------- marshalling helpers
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise TQError(f"unsupported input dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise TQError("all tensors must be CUDA tensors")
+        if t is not None and not t.is_contiguous():
+            raise TQError("all tensors must be contiguous")
+
+
+def empty_pool(num_blocks: int, n_kv_heads: int, d: int, kind: str, device="cuda"):
+    """Zeroed K or V pool tensor uint8[num_blocks][n_kv_heads][record_bytes]."""
+    torch = _torch()
+    rec = k_record_bytes(d) if kind == "k" else v_record_bytes(d)
+    return torch.zeros((num_blocks, n_kv_heads, rec), dtype=torch.uint8, device=device)
+
+
+# ---------------------------------------------------------------- entry points
+
+def codebook_init(d: int, D, S, device="cuda", stream=None):
+    """tq_codebook_init: returns (params uint8 device tensor, centroids list[8]).
+
+    D: int8[d] of +-1 (host array or CPU tensor); S: float32[d][d] (host)."""
+    import numpy as np
+    torch = _torch()
+    Dn = np.ascontiguousarray(np.asarray(D.cpu() if hasattr(D, "cpu") else D), dtype=np.int8)
+    Sn = np.ascontiguousarray(np.asarray(S.cpu() if hasattr(S, "cpu") else S), dtype=np.float32)
+    if Dn.shape != (d,) or Sn.shape != (d, d):
+        raise TQError("D must be [d] and S must be [d][d]")
+    nb = params_bytes(d)
+    if nb == 0:
+        raise TQError(f"unsupported head_dim {d}")
+    params = torch.empty(nb, dtype=torch.uint8, device=device)
+    cent = (ctypes.c_double * 8)()
+    rc = load_library().tq_codebook_init(d, Dn.ctypes.data_as(_P), Sn.ctypes.data_as(_P), _ptr(params), nb,
+                                         cent, _stream(stream))
+    _check(rc, "tq_codebook_init")
+    return params, [float(x) for x in cent]
+
+
+def encode_k(params, d: int, k, slot_mapping, k_pool, status=None, stream=None):
+    """tq_encode_k: k [n_tokens][n_kv_heads][d] (f32/bf16), slot_mapping int64[n_tokens]."""
+    _need_cuda(params, k, slot_mapping, k_pool, status)
+    n, h = k.shape[0], k.shape[1]
+    rc = load_library().tq_encode_k(_ptr(params), d, _ptr(k), _dtype_code(k), n, h, _ptr(slot_mapping),
+                                    _ptr(k_pool), k_pool.shape[0], _ptr(status), _stream(stream))
+    _check(rc, "tq_encode_k")
+
+
+def encode_v(params, d: int, v, slot_mapping, v_pool, status=None, stream=None):
+    """tq_encode_v: v [n_tokens][n_kv_heads][d] (f32/bf16), slot_mapping int64[n_tokens]."""
+    _need_cuda(params, v, slot_mapping, v_pool, status)
+    n, h = v.shape[0], v.shape[1]
+    rc = load_library().tq_encode_v(_ptr(params), d, _ptr(v), _dtype_code(v), n, h, _ptr(slot_mapping),
+                                    _ptr(v_pool), v_pool.shape[0], _ptr(status), _stream(stream))
+    _check(rc, "tq_encode_v")
+
+
+def paged_append(params, d: int, k_new, v_new, block_table, ctx_lens, k_pool, v_pool, status=None, stream=None):
+    """tq_paged_append: one token per sequence at slot ctx_lens[b] (lengths before the append)."""
+    _need_cuda(params, k_new, v_new, block_table, ctx_lens, k_pool, v_pool, status)
+    b, h = k_new.shape[0], k_new.shape[1]
+    rc = load_library().tq_paged_append(_ptr(params), d, _ptr(k_new), _ptr(v_new), _dtype_code(k_new), b, h,
+                                        _ptr(block_table), block_table.shape[1], _ptr(ctx_lens), _ptr(k_pool),
+                                        _ptr(v_pool), k_pool.shape[0], _ptr(status), _stream(stream))
+    _check(rc, "tq_paged_append")
+
+
+def decode_attn(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens, max_ctx: int,
+                out=None, workspace=None, status=None, stream=None):
+    """tq_decode_attn: q [batch][n_q_heads][d] -> out float32 [batch][n_q_heads][d]."""
+    torch = _torch()
+    _need_cuda(params, q, k_pool, v_pool, block_table, ctx_lens, out, workspace, status)
+    B, Hq = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes(d, B, Hq, max_ctx)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = load_library().tq_decode_attn(_ptr(params), d, _ptr(q), _dtype_code(q), B, Hq, n_kv_heads,
+                                       _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
+                                       block_table.shape[1], _ptr(ctx_lens), max_ctx, _ptr(out),
+                                       _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+    _check(rc, "tq_decode_attn")
+    return out
+
+
+# ---------------------------------------------------------------- decode stages
+
+def decode_qprep(params, d: int, q, n_kv_heads: int, max_ctx: int, workspace, stream=None):
+    """tq_decode_qprep: qbar = Pi q, u = S qbar into the workspace."""
+    _need_cuda(params, q, workspace)
+    B, Hq = q.shape[0], q.shape[1]
+    rc = load_library().tq_decode_qprep(_ptr(params), d, _ptr(q), _dtype_code(q), B, Hq, n_kv_heads, max_ctx,
+                                        _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "tq_decode_qprep")
+
+
+def decode_partial(params, d: int, batch: int, n_q_heads: int, n_kv_heads: int, k_pool, v_pool, block_table,
+                   ctx_lens, max_ctx: int, workspace, status=None, stream=None):
+    """tq_decode_partial: the split-K pass over the compressed cache."""
+    _need_cuda(params, k_pool, v_pool, block_table, ctx_lens, workspace, status)
+    rc = load_library().tq_decode_partial(_ptr(params), d, batch, n_q_heads, n_kv_heads, _ptr(k_pool),
+                                          _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
+                                          block_table.shape[1], _ptr(ctx_lens), max_ctx, _ptr(workspace),
+                                          workspace.numel(), _ptr(status), _stream(stream))
+    _check(rc, "tq_decode_partial")
+
+
+def decode_merge(params, d: int, batch: int, n_q_heads: int, n_kv_heads: int, ctx_lens, max_ctx: int, out,
+                 workspace, stream=None):
+    """tq_decode_merge: split merge plus the inverse rotation into out."""
+    _need_cuda(params, ctx_lens, out, workspace)
+    rc = load_library().tq_decode_merge(_ptr(params), d, batch, n_q_heads, n_kv_heads, _ptr(ctx_lens), max_ctx,
+                                        _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "tq_decode_merge")

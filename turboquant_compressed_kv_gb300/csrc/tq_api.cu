@@ -1,0 +1,239 @@
+// tq_api.cu -- the C ABI declared in include/tq.h: argument checks on the host,
+// then kernel launches on the caller's stream.  Allocates no device memory.
+#include <math.h>
+
+#include "tq_internal.cuh"
+
+namespace tq {
+cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const void *x, int64_t n_tokens,
+                          int n_heads, const int64_t *slots, void *pool, int64_t num_blocks, int32_t *status,
+                          cudaStream_t st);
+cudaError_t launch_append(int d, int dtype, const void *params, const void *k_new, const void *v_new, int batch,
+                          int n_heads, const int32_t *bt, int max_blocks, const int32_t *ctx, void *kp, void *vp,
+                          int64_t num_blocks, int32_t *status, cudaStream_t st);
+cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int max_ctx,
+                         void *ws, cudaStream_t st);
+cudaError_t launch_partial(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
+                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
+                           const int32_t *ctx_lens, int max_ctx, void *ws, int32_t *status, cudaStream_t st);
+cudaError_t launch_merge(int d, const void *params, int batch, int hq, const int32_t *ctx_lens, int max_ctx,
+                         float *out, void *ws, cudaStream_t st);
+size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx);
+
+namespace {
+
+// Lloyd-Max fixed point for the unit Gaussian with 8 levels, in fp64 on the
+// device ("Lloyd-Maxコードブックとは", lilting.ch SwiftLM article: computed
+// once before inference, no calibration).  The optimum is symmetric (the
+// Gaussian is symmetric and log-concave, so the optimum is unique), so only
+// the four positive cells are iterated: edges 0, m1, m2, m3, +inf; each level
+// moves to the Gaussian mean of its cell, each inner edge to the midpoint of
+// its two levels.
+__global__ void codebook_kernel(uint8_t *params, int d) {
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    const double inv_sqrt2 = 0.70710678118654752440;
+    const double inv_sqrt2pi = 0.39894228040143267794;
+    double lv[4] = {0.3, 0.8, 1.4, 2.2};
+    for (int it = 0; it < 100000; ++it) {
+        double edge[5] = {0.0, 0.5 * (lv[0] + lv[1]), 0.5 * (lv[1] + lv[2]), 0.5 * (lv[2] + lv[3]), 0.0};
+        double moved = 0.0;
+        for (int k = 0; k < 4; ++k) {
+            const double a = edge[k];
+            const bool last = (k == 3);
+            const double dens_a = inv_sqrt2pi * exp(-0.5 * a * a);
+            const double dens_b = last ? 0.0 : inv_sqrt2pi * exp(-0.5 * edge[k + 1] * edge[k + 1]);
+            const double tail_a = 0.5 * erfc(a * inv_sqrt2);
+            const double tail_b = last ? 0.0 : 0.5 * erfc(edge[k + 1] * inv_sqrt2);
+            const double m = (dens_a - dens_b) / (tail_a - tail_b);
+            moved = fmax(moved, fabs(m - lv[k]));
+            lv[k] = m;
+        }
+        if (moved < 1e-15) break;
+    }
+    ParamsHeader *h = reinterpret_cast<ParamsHeader *>(params);
+    for (int k = 0; k < 4; ++k) {
+        h->centroid64[4 + k] = lv[k];
+        h->centroid64[3 - k] = -lv[k];
+    }
+    for (int j = 0; j < 8; ++j) h->centroid[j] = (float)h->centroid64[j];
+    for (int j = 0; j < 7; ++j) h->threshold[j] = (float)(0.5 * (h->centroid64[j] + h->centroid64[j + 1]));
+    h->threshold[3] = 0.0f;
+    h->threshold[7] = INFINITY;
+    h->d = d;
+    __threadfence();
+    h->magic = kParamsMagic;
+}
+
+// D signs arrive as int8 in a scratch spot (the start of the S region);
+// store them as +-1.0f.
+__global__ void signs_kernel(uint8_t *params, int d) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= d) return;
+    const int8_t s = reinterpret_cast<const int8_t *>(params + params_off_S(d))[i];
+    reinterpret_cast<float *>(params + params_off_D(d))[i] = (s < 0) ? -1.0f : 1.0f;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA; }
+
+}  // namespace
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" {
+
+size_t tq_k_record_bytes(int d) { return valid_d(d) ? k_record(d) : 0; }
+size_t tq_v_record_bytes(int d) { return valid_d(d) ? v_record(d) : 0; }
+size_t tq_params_bytes(int d) { return valid_d(d) ? params_total(d) : 0; }
+
+const char *tq_error_string(int code) {
+    switch (code) {
+        case TQ_OK: return "ok";
+        case TQ_ERR_INVALID: return "invalid argument (size, count or NULL pointer)";
+        case TQ_ERR_HEAD_DIM: return "unsupported head_dim (must be 128 or 256)";
+        case TQ_ERR_GQA: return "n_q_heads must be a multiple of n_kv_heads with group size 1..8";
+        case TQ_ERR_WORKSPACE: return "workspace or params buffer too small";
+        case TQ_ERR_CUDA: return "CUDA launch or runtime error";
+        case TQ_ERR_DTYPE: return "unsupported dtype (TQ_DTYPE_F32 or TQ_DTYPE_BF16)";
+        case TQ_ERR_ALIGN: return "pointer not 16-byte aligned";
+        default: return "unknown error";
+    }
+}
+
+int tq_codebook_init(int d, const int8_t *D_host, const float *S_host, void *params_dev, size_t params_bytes,
+                     double *centroids_out8, tq_stream_t stream) {
+    if (!valid_d(d)) return TQ_ERR_HEAD_DIM;
+    if (!D_host || !S_host || !params_dev) return TQ_ERR_INVALID;
+    if (!aligned16(params_dev)) return TQ_ERR_ALIGN;
+    if (params_bytes < params_total(d)) return TQ_ERR_WORKSPACE;
+    for (int i = 0; i < d; ++i)
+        if (D_host[i] != 1 && D_host[i] != -1) return TQ_ERR_INVALID;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *P = static_cast<uint8_t *>(params_dev);
+    cudaError_t e = cudaMemsetAsync(P, 0, sizeof(ParamsHeader), st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(P + params_off_S(d), D_host, (size_t)d, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) { signs_kernel<<<(d + 127) / 128, 128, 0, st>>>(P, d); e = cudaGetLastError(); }
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(P + params_off_S(d), S_host, sizeof(float) * (size_t)d * d, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) { codebook_kernel<<<1, 32, 0, st>>>(P, d); e = cudaGetLastError(); }
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess && centroids_out8)
+        e = cudaMemcpy(centroids_out8, P + offsetof(ParamsHeader, centroid64), 8 * sizeof(double),
+                       cudaMemcpyDeviceToHost);
+    return cuda_status(e);
+}
+
+static int check_pool_call(const void *params, int d, const void *x, int dtype, int64_t n_tokens, int n_heads,
+                           const void *slots, const void *pool, int64_t num_blocks) {
+    if (!valid_d(d)) return TQ_ERR_HEAD_DIM;
+    if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16) return TQ_ERR_DTYPE;
+    if (n_tokens < 0 || n_heads <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
+    if (n_tokens == 0) return TQ_OK;
+    if (!params || !x || !slots || !pool) return TQ_ERR_INVALID;
+    if (!aligned16(params) || !aligned16(pool)) return TQ_ERR_ALIGN;
+    if (n_tokens > ((int64_t)1 << 40) / n_heads) return TQ_ERR_INVALID;
+    return TQ_OK;
+}
+
+int tq_encode_k(const void *params, int d, const void *k, int dtype, int64_t n_tokens, int n_kv_heads,
+                const int64_t *slot_mapping, void *k_pool, int64_t num_blocks, int32_t *status, tq_stream_t stream) {
+    int rc = check_pool_call(params, d, k, dtype, n_tokens, n_kv_heads, slot_mapping, k_pool, num_blocks);
+    if (rc != TQ_OK || n_tokens == 0) return rc;
+    return cuda_status(launch_encode(true, d, dtype, params, k, n_tokens, n_kv_heads, slot_mapping, k_pool,
+                                     num_blocks, status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int tq_encode_v(const void *params, int d, const void *v, int dtype, int64_t n_tokens, int n_kv_heads,
+                const int64_t *slot_mapping, void *v_pool, int64_t num_blocks, int32_t *status, tq_stream_t stream) {
+    int rc = check_pool_call(params, d, v, dtype, n_tokens, n_kv_heads, slot_mapping, v_pool, num_blocks);
+    if (rc != TQ_OK || n_tokens == 0) return rc;
+    return cuda_status(launch_encode(false, d, dtype, params, v, n_tokens, n_kv_heads, slot_mapping, v_pool,
+                                     num_blocks, status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int tq_paged_append(const void *params, int d, const void *k_new, const void *v_new, int dtype, int batch,
+                    int n_kv_heads, const int32_t *block_table, int max_blocks, const int32_t *ctx_lens,
+                    void *k_pool, void *v_pool, int64_t num_blocks, int32_t *status, tq_stream_t stream) {
+    if (!valid_d(d)) return TQ_ERR_HEAD_DIM;
+    if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16) return TQ_ERR_DTYPE;
+    if (batch < 0 || n_kv_heads <= 0 || max_blocks <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
+    if (batch == 0) return TQ_OK;
+    if (!params || !k_new || !v_new || !block_table || !ctx_lens || !k_pool || !v_pool) return TQ_ERR_INVALID;
+    if (!aligned16(params) || !aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
+    return cuda_status(launch_append(d, dtype, params, k_new, v_new, batch, n_kv_heads, block_table, max_blocks,
+                                     ctx_lens, k_pool, v_pool, num_blocks, status,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t tq_decode_workspace_bytes(int d, int batch, int n_q_heads, int max_ctx) {
+    return decode_workspace_bytes(d, batch, n_q_heads, max_ctx);
+}
+
+static int check_decode(const void *params, int d, int batch, int hq, int hkv, int max_ctx, void *ws,
+                        size_t ws_bytes) {
+    if (!valid_d(d)) return TQ_ERR_HEAD_DIM;
+    if (batch < 0 || hq <= 0 || hkv <= 0 || max_ctx < 0) return TQ_ERR_INVALID;
+    if (hq % hkv != 0 || hq / hkv > 8) return TQ_ERR_GQA;
+    if (batch > 65535 || hkv > 65535) return TQ_ERR_INVALID;
+    if (batch == 0) return TQ_OK;
+    if (!params || !ws) return TQ_ERR_INVALID;
+    if (!aligned16(params) || !aligned16(ws)) return TQ_ERR_ALIGN;
+    if (ws_bytes < decode_workspace_bytes(d, batch, hq, max_ctx)) return TQ_ERR_WORKSPACE;
+    return TQ_OK;
+}
+
+int tq_decode_qprep(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads, int n_kv_heads,
+                    int max_ctx, void *workspace, size_t workspace_bytes, tq_stream_t stream) {
+    int rc = check_decode(params, d, batch, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
+    if (rc != TQ_OK || batch == 0) return rc;
+    if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16) return TQ_ERR_DTYPE;
+    if (!q) return TQ_ERR_INVALID;
+    return cuda_status(launch_qprep(d, dtype, params, q, batch, n_q_heads, max_ctx, workspace,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int tq_decode_partial(const void *params, int d, int batch, int n_q_heads, int n_kv_heads, const void *k_pool,
+                      const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
+                      const int32_t *ctx_lens, int max_ctx, void *workspace, size_t workspace_bytes,
+                      int32_t *status, tq_stream_t stream) {
+    int rc = check_decode(params, d, batch, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
+    if (rc != TQ_OK || batch == 0) return rc;
+    if (max_blocks <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
+    if (!k_pool || !v_pool || !block_table || !ctx_lens) return TQ_ERR_INVALID;
+    if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
+    return cuda_status(launch_partial(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks,
+                                      block_table, max_blocks, ctx_lens, max_ctx, workspace, status,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int tq_decode_merge(const void *params, int d, int batch, int n_q_heads, int n_kv_heads, const int32_t *ctx_lens,
+                    int max_ctx, float *out, void *workspace, size_t workspace_bytes, tq_stream_t stream) {
+    int rc = check_decode(params, d, batch, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
+    if (rc != TQ_OK || batch == 0) return rc;
+    if (!ctx_lens || !out) return TQ_ERR_INVALID;
+    return cuda_status(launch_merge(d, params, batch, n_q_heads, ctx_lens, max_ctx, out, workspace,
+                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int tq_decode_attn(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads, int n_kv_heads,
+                   const void *k_pool, const void *v_pool, int64_t num_blocks, const int32_t *block_table,
+                   int max_blocks, const int32_t *ctx_lens, int max_ctx, float *out, void *workspace,
+                   size_t workspace_bytes, int32_t *status, tq_stream_t stream) {
+    if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16 && valid_d(d)) return TQ_ERR_DTYPE;
+    int rc = check_decode(params, d, batch, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
+    if (rc != TQ_OK || batch == 0) return rc;
+    if (max_blocks <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
+    if (!q || !k_pool || !v_pool || !block_table || !ctx_lens || !out) return TQ_ERR_INVALID;
+    if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_qprep(d, dtype, params, q, batch, n_q_heads, max_ctx, workspace, st);
+    if (e == cudaSuccess)
+        e = launch_partial(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
+                           max_blocks, ctx_lens, max_ctx, workspace, status, st);
+    if (e == cudaSuccess) e = launch_merge(d, params, batch, n_q_heads, ctx_lens, max_ctx, out, workspace, st);
+    return cuda_status(e);
+}
+
+}  // extern "C"
