@@ -181,6 +181,33 @@ int tq_decode_merge(const void *params, int d, int batch, int n_q_heads, int n_k
                     const int32_t *ctx_lens, int max_ctx, float *out, void *workspace,
                     size_t workspace_bytes, tq_stream_t stream);
 
+/* tq_decode_attn_noalloc -- tq_decode_attn without a caller workspace.
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory when they decode: a serving runtime that
+ * reserves all free GPU memory for its KV pool at start-up and allows no
+ * allocation afterwards, or a latency-bound decode loop that must not call
+ * cudaMalloc, which can synchronise the device.
+ * Same arguments, result and errors as tq_decode_attn, minus workspace and
+ * workspace_bytes.  The scratch is a fixed array of TQ_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) compiled into the library; every GPU that loads the library keeps
+ * it until the process exits.  A shape whose tq_decode_workspace_bytes()
+ * exceeds it is rejected with TQ_ERR_WORKSPACE (16 x 32 query heads at
+ * d = 128 and 4096 tokens needs about 2.7 MiB).  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library call.
+ * The scratch used is that of the device current at the call; the stream must
+ * belong to it.  The first call made with a device current looks up the
+ * scratch address on that device (cudaGetSymbolAddress); make that first call
+ * before any stream capture.  All calls share the one array per device: two
+ * calls whose kernels overlap on the GPU (different streams, no ordering) race
+ * and corrupt each other's results.  No part of the scratch needs to start at
+ * zero, so nothing is cleared between calls. */
+#define TQ_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int tq_decode_attn_noalloc(const void *params, int d, const void *q, int dtype, int batch,
+                           int n_q_heads, int n_kv_heads, const void *k_pool, const void *v_pool,
+                           int64_t num_blocks, const int32_t *block_table, int max_blocks,
+                           const int32_t *ctx_lens, int max_ctx, float *out, int32_t *status,
+                           tq_stream_t stream);
+
 /* Short English text for a TQ_* return code (static storage). */
 const char *tq_error_string(int code);
 

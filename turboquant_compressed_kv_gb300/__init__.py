@@ -78,6 +78,8 @@ def _declare(L):
     L.tq_decode_qprep.argtypes = [_P, _I, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]
     L.tq_decode_partial.restype = _I
     L.tq_decode_partial.argtypes = [_P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _SZ, _P, _P]
+    L.tq_decode_attn_noalloc.restype = _I
+    L.tq_decode_attn_noalloc.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _P]
     L.tq_decode_merge.restype = _I
     L.tq_decode_merge.argtypes = [_P, _I, _I, _I, _I, _P, _I, _P, _P, _SZ, _P]
 
@@ -246,3 +248,23 @@ def decode_merge(params, d: int, batch: int, n_q_heads: int, n_kv_heads: int, ct
     rc = load_library().tq_decode_merge(_ptr(params), d, batch, n_q_heads, n_kv_heads, _ptr(ctx_lens), max_ctx,
                                         _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "tq_decode_merge")
+
+
+def decode_attn_noalloc(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens, max_ctx: int,
+                        out=None, status=None, stream=None):
+    """tq_decode_attn_noalloc: decode attention with the library's fixed scratch instead of a workspace.
+
+    For callers that cannot allocate device memory while decoding; shapes whose
+    workspace would exceed 16 MiB are rejected.  Calls that overlap on the GPU
+    share the scratch and race."""
+    torch = _torch()
+    _need_cuda(params, q, k_pool, v_pool, block_table, ctx_lens, out, status)
+    B, Hq = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    rc = load_library().tq_decode_attn_noalloc(_ptr(params), d, _ptr(q), _dtype_code(q), B, Hq, n_kv_heads,
+                                               _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
+                                               block_table.shape[1], _ptr(ctx_lens), max_ctx, _ptr(out),
+                                               _ptr(status), _stream(stream))
+    _check(rc, "tq_decode_attn_noalloc")
+    return out
