@@ -254,27 +254,30 @@ void tqo_encode_vector(int is_k, int d, const int8_t *D, const float *S,
 size_t tqo_k_record_bytes(int d) { return (size_t)4 * (2 * d) + TQO_BLOCK * 4; }
 size_t tqo_v_record_bytes(int d) { return (size_t)3 * (2 * d) + TQO_BLOCK * 2; }
 
-/* K plane: token slot t (0..15), coordinate i (0..d-1) -> (word, bit). */
+/* K plane: token slot t (0..15), coordinate i (0..d-1) -> (word, bit).
+ * Coordinate i = 16*s + k: h = k>>3, tig = (k&7)>>1, e = k&1; lane L = 4*(t&7) + tig;
+ * word (L*2 + (t>>3)) * (d/128) + (s>>3); bit 8*h + (s&7) + 16*e. */
 void tqo_k_bitpos(int d, int t, int i, int *word, int *bit)
 {
     int nw = d / 128;                  /* words per (lane, token) */
-    int c = i >> 5, h = (i >> 4) & 1, tig = (i >> 2) & 3, j = i & 3;
-    int gid = t & 7, th = t >> 3;
-    int lane = 4 * gid + tig;
-    int wj = c >> 2, q = 2 * (c & 3) + h;
-    *word = (lane * 2 + th) * nw + wj;
-    *bit = 8 * j + q;
+    int s = i >> 4, k = i & 15;
+    int h = k >> 3, tig = (k & 7) >> 1, e = k & 1;
+    int lane = 4 * (t & 7) + tig;
+    *word = (lane * 2 + (t >> 3)) * nw + (s >> 3);
+    *bit = 8 * h + (s & 7) + 16 * e;
 }
 
-/* V plane: token slot t, coordinate i -> (word, bit). */
+/* V plane: token slot t, coordinate i -> (word, bit).
+ * Coordinate i = 16*mt + gid + 8*rh; token t: tig = (t&7)>>1, e = t&1, tp = t>>3;
+ * lane L = 4*gid + tig; word L*(d/64) + 2*(mt>>3) + rh; bit 8*tp + (mt&7) + 16*e. */
 void tqo_v_bitpos(int d, int t, int i, int *word, int *bit)
 {
     int nw = d / 64;                   /* words per lane */
     int mt = i >> 4, r = i & 15, gid = r & 7, rh = r >> 3;
-    int tig = t >> 2, j = t & 3;
+    int tig = (t & 7) >> 1, e = t & 1, tp = t >> 3;
     int lane = 4 * gid + tig;
     *word = lane * nw + 2 * (mt >> 3) + rh;
-    *bit = 8 * j + (mt & 7);
+    *bit = 8 * tp + (mt & 7) + 16 * e;
 }
 
 static void set_bit(uint8_t *plane, int word, int bit, int v)

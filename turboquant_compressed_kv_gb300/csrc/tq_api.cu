@@ -11,12 +11,12 @@ cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const
 cudaError_t launch_append(int d, int dtype, const void *params, const void *k_new, const void *v_new, int batch,
                           int n_heads, const int32_t *bt, int max_blocks, const int32_t *ctx, void *kp, void *vp,
                           int64_t num_blocks, int32_t *status, cudaStream_t st);
-cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int max_ctx,
+cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv, int max_ctx,
                          void *ws, cudaStream_t st);
 cudaError_t launch_partial(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
                            const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
                            const int32_t *ctx_lens, int max_ctx, void *ws, int32_t *status, cudaStream_t st);
-cudaError_t launch_merge(int d, const void *params, int batch, int hq, const int32_t *ctx_lens, int max_ctx,
+cudaError_t launch_merge(int d, const void *params, int batch, int hq, int hkv, const int32_t *ctx_lens, int max_ctx,
                          float *out, void *ws, cudaStream_t st);
 size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx);
 
@@ -190,7 +190,7 @@ int tq_decode_qprep(const void *params, int d, const void *q, int dtype, int bat
     if (rc != TQ_OK || batch == 0) return rc;
     if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16) return TQ_ERR_DTYPE;
     if (!q) return TQ_ERR_INVALID;
-    return cuda_status(launch_qprep(d, dtype, params, q, batch, n_q_heads, max_ctx, workspace,
+    return cuda_status(launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, max_ctx, workspace,
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -213,7 +213,7 @@ int tq_decode_merge(const void *params, int d, int batch, int n_q_heads, int n_k
     int rc = check_decode(params, d, batch, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
     if (rc != TQ_OK || batch == 0) return rc;
     if (!ctx_lens || !out) return TQ_ERR_INVALID;
-    return cuda_status(launch_merge(d, params, batch, n_q_heads, ctx_lens, max_ctx, out, workspace,
+    return cuda_status(launch_merge(d, params, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx, out, workspace,
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -228,11 +228,11 @@ int tq_decode_attn(const void *params, int d, const void *q, int dtype, int batc
     if (!q || !k_pool || !v_pool || !block_table || !ctx_lens || !out) return TQ_ERR_INVALID;
     if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_qprep(d, dtype, params, q, batch, n_q_heads, max_ctx, workspace, st);
+    cudaError_t e = launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, max_ctx, workspace, st);
     if (e == cudaSuccess)
         e = launch_partial(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
                            max_blocks, ctx_lens, max_ctx, workspace, status, st);
-    if (e == cudaSuccess) e = launch_merge(d, params, batch, n_q_heads, ctx_lens, max_ctx, out, workspace, st);
+    if (e == cudaSuccess) e = launch_merge(d, params, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx, out, workspace, st);
     return cuda_status(e);
 }
 

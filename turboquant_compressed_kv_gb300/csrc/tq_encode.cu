@@ -120,7 +120,7 @@ __device__ __forceinline__ void encode_vector(const uint8_t *__restrict__ params
         uint8_t *rec = pool + ((size_t)blk * n_heads + head) * v_record(D);
         constexpr int NWV = D / 64;
         constexpr int NM = D / 128;
-        const int tigv = off >> 2, jv = off & 3;
+        const int tigv = (off & 7) >> 1, jb = (off >> 3) + 2 * (off & 1);   // lane tig, byte in word
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const uint32_t w0 = __ballot_sync(0xffffffffu, code[r] & 1);
@@ -131,7 +131,7 @@ __device__ __forceinline__ void encode_vector(const uint8_t *__restrict__ params
                 const int tau = 4 * r + beta;
                 const int mhi = tau % NM, rh = (tau / NM) & 1, gid = tau / (2 * NM);
                 const int L = 4 * gid + tigv;
-                const size_t byte = ((size_t)L * NWV + 2 * mhi + rh) * 4 + jv;
+                const size_t byte = ((size_t)L * NWV + 2 * mhi + rh) * 4 + jb;
                 rec[byte] = (uint8_t)(w0 >> (8 * beta));
                 rec[2 * D + byte] = (uint8_t)(w1 >> (8 * beta));
                 rec[4 * D + byte] = (uint8_t)(w2 >> (8 * beta));

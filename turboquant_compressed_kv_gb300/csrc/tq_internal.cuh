@@ -5,16 +5,15 @@
 //      2*d bytes, then 16 x {fp16 ||x||, fp16 ||r||}.
 //   V: planes 0..2, each 2*d bytes, then 16 x fp16 ||v||.
 // Each plane is an array of 32-bit words indexed by a lane L = 4*gid + tig.
-//   K word ((L*2 + th)*NW + wj), NW = d/128, bit 8*j + q belongs to slot
-//     t = gid + 8*th and coordinate i = 32*c + 16*h + 4*tig + j, where
-//     c = 4*wj + (q >> 1), h = q & 1.
-//   V word (L*NWV + 2*(mt >> 3) + rh), NWV = d/64, bit 8*j + (mt & 7)
-//     belongs to slot t = 4*tig + j and coordinate i = 16*mt + gid + 8*rh.
+//   K: coordinate i = 16*s + 8*h + 2*tig + e of slot t = gid + 8*th sits in
+//      word (L*2 + th)*NW + (s>>3), NW = d/128, at bit 8*h + (s&7) + 16*e.
+//   V: coordinate i = 16*mt + gid + 8*rh of slot t = 2*tig + 8*tp + e sits in
+//      word L*NWV + 2*(mt>>3) + rh, NWV = d/64, at bit 8*tp + (mt&7) + 16*e.
 // In both layouts one byte of a word belongs to one token slot, so slots can
-// be written independently with byte stores.  The arrangement matches the
-// operand fragments of the m16n8k32 e4m3 mma.sync used by decode attention:
-// a single LOP3 turns the bits at position q of the four bytes of a word
-// into four fp8 operands.
+// be written independently with byte stores.  Bits p and p+16 of a word are
+// the two halves of one f16x2 operand register of the m16n8k16 mma.sync used
+// by decode attention (K: token rows x coordinate columns; V: coordinate rows
+// x token columns), so one LOP3 turns them into two f16 operands.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -63,9 +62,8 @@ template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16
 
 template <int D>
 __device__ __forceinline__ int kdim(int lane, int r) {
-    int j = lane >> 3, q = lane & 7;
-    int c = 4 * (r >> 2) + (q >> 1), h = q & 1, tig = r & 3;
-    return 32 * c + 16 * h + 4 * tig + j;
+    const int e = lane >> 4, h = (lane >> 3) & 1, s = 8 * (r >> 2) + (lane & 7), tig = r & 3;
+    return 16 * s + 8 * h + 2 * tig + e;
 }
 
 template <int D>

@@ -12,12 +12,12 @@
 #include "tq_internal.cuh"
 
 namespace tq {
-cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int max_ctx,
+cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv, int max_ctx,
                          void *ws, cudaStream_t st);
 cudaError_t launch_partial(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
                            const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
                            const int32_t *ctx_lens, int max_ctx, void *ws, int32_t *status, cudaStream_t st);
-cudaError_t launch_merge(int d, const void *params, int batch, int hq, const int32_t *ctx_lens, int max_ctx,
+cudaError_t launch_merge(int d, const void *params, int batch, int hq, int hkv, const int32_t *ctx_lens, int max_ctx,
                          float *out, void *ws, cudaStream_t st);
 size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx);
 
@@ -81,10 +81,10 @@ extern "C" int tq_decode_attn_noalloc(const void *params, int d, const void *q, 
     // Every scratch value the kernels read is written earlier in this same
     // call, so the contents left by a previous call need no clearing.
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    e = launch_qprep(d, dtype, params, q, batch, n_q_heads, max_ctx, ws, st);
+    e = launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, max_ctx, ws, st);
     if (e == cudaSuccess)
         e = launch_partial(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
                            max_blocks, ctx_lens, max_ctx, ws, status, st);
-    if (e == cudaSuccess) e = launch_merge(d, params, batch, n_q_heads, ctx_lens, max_ctx, out, ws, st);
+    if (e == cudaSuccess) e = launch_merge(d, params, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx, out, ws, st);
     return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
