@@ -37,7 +37,7 @@ METRIC = "decode-attn compressed-KV GB/s & % of GB300 HBM peak; encode Mtok/s vs
 WORKLOAD = "llama8b_decode"
 L2_BYTES = 129 * 1024 * 1024
 DECODE_SRC = os.path.join(ROOT, "turboquant_compressed_kv_gb300", "csrc", "tq_decode.cu")
-PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_partial_llama8b_decode.json")
+PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_splitk_llama8b_decode.json")
 
 
 def parse():
@@ -285,7 +285,7 @@ def bench_tq(args):
     out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
-    launches_per_step = 4
+    launches_per_step = 3          # append (K and V tiles), query prep, split-K pass with merge
 
     def step(i, ev=None):
         kp, vp = pools[i % nrep]
@@ -293,10 +293,10 @@ def bench_tq(args):
         tq.decode_qprep(cache.params, d, q, Hkv, max_ctx, ws)
         if ev is not None:
             ev[0].record(stream)
-        tq.decode_partial(cache.params, d, B, Hq, Hkv, kp, vp, cache.block_table, ctx, max_ctx, ws, status=status)
+        tq.decode_splitk(cache.params, d, B, Hq, Hkv, kp, vp, cache.block_table, ctx, max_ctx, out, ws,
+                         status=status)
         if ev is not None:
             ev[1].record(stream)
-        tq.decode_merge(cache.params, d, B, Hq, Hkv, ctx, max_ctx, out, ws)
 
     def barrier():
         if world > 1:
@@ -383,7 +383,7 @@ def bench_tq(args):
                                      "no flush needed"),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 3), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "decode split-K pass (tq_decode_partial)", "peak_source": peak_kind,
+                     "kernel": "decode split-K pass with merge (tq_decode_splitk)", "peak_source": peak_kind,
                      "kernel_ms": round(kern_avg_ms, 6), "bytes_per_launch": nb["partial"]},
         "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},

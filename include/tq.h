@@ -157,29 +157,26 @@ int tq_decode_attn(const void *params, int d, const void *q, int dtype, int batc
                    int max_ctx, float *out, void *workspace, size_t workspace_bytes,
                    int32_t *status, tq_stream_t stream);
 
-/* The three stages of tq_decode_attn as separate calls, for callers that
+/* The two stages of tq_decode_attn as separate calls, for callers that
  * schedule or time them individually.  Called in this order on one stream with
  * the same shape arguments and workspace, they compute exactly what
  * tq_decode_attn computes; argument meanings and errors are as there.
  *   tq_decode_qprep   qbar = Pi q and u = S qbar for every (sequence, query head),
- *                     written to the workspace.
- *   tq_decode_partial the pass over the cache: per (sequence, kv head, context
- *                     split of 512 tokens) the online-softmax state (max score,
- *                     sum of weights, weighted value sum in the rotated domain)
- *                     of every query head of the group, written to the workspace.
- *   tq_decode_merge   combines the splits of each (sequence, query head) and
- *                     applies the inverse rotation: out = Pi^T a. */
+ *                     written to the workspace as tensor-core operands.
+ *   tq_decode_splitk  the pass over the cache: per (sequence, kv head, context
+ *                     split) the online-softmax state (max score, sum of weights,
+ *                     weighted value sum in the rotated domain) of every query
+ *                     head of the group; the last split of each (sequence, kv
+ *                     head) to finish combines the splits and writes
+ *                     out = Pi^T a for the group's query heads. */
 int tq_decode_qprep(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads,
                     int n_kv_heads, int max_ctx, void *workspace, size_t workspace_bytes,
                     tq_stream_t stream);
-int tq_decode_partial(const void *params, int d, int batch, int n_q_heads, int n_kv_heads,
-                      const void *k_pool, const void *v_pool, int64_t num_blocks,
-                      const int32_t *block_table, int max_blocks, const int32_t *ctx_lens,
-                      int max_ctx, void *workspace, size_t workspace_bytes, int32_t *status,
-                      tq_stream_t stream);
-int tq_decode_merge(const void *params, int d, int batch, int n_q_heads, int n_kv_heads,
-                    const int32_t *ctx_lens, int max_ctx, float *out, void *workspace,
-                    size_t workspace_bytes, tq_stream_t stream);
+int tq_decode_splitk(const void *params, int d, int batch, int n_q_heads, int n_kv_heads,
+                     const void *k_pool, const void *v_pool, int64_t num_blocks,
+                     const int32_t *block_table, int max_blocks, const int32_t *ctx_lens,
+                     int max_ctx, float *out, void *workspace, size_t workspace_bytes,
+                     int32_t *status, tq_stream_t stream);
 
 /* tq_decode_attn_noalloc -- tq_decode_attn without a caller workspace.
  * The pages have no counterpart to this call; it exists for callers that

@@ -76,12 +76,11 @@ def _declare(L):
                                  _P, _P]
     L.tq_decode_qprep.restype = _I
     L.tq_decode_qprep.argtypes = [_P, _I, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]
-    L.tq_decode_partial.restype = _I
-    L.tq_decode_partial.argtypes = [_P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _SZ, _P, _P]
+    L.tq_decode_splitk.restype = _I
+    L.tq_decode_splitk.argtypes = [_P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _SZ, _P, _P]
     L.tq_decode_attn_noalloc.restype = _I
     L.tq_decode_attn_noalloc.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _P]
-    L.tq_decode_merge.restype = _I
-    L.tq_decode_merge.argtypes = [_P, _I, _I, _I, _I, _P, _I, _P, _P, _SZ, _P]
+
 
 
 def _check(rc: int, what: str):
@@ -230,24 +229,15 @@ def decode_qprep(params, d: int, q, n_kv_heads: int, max_ctx: int, workspace, st
     _check(rc, "tq_decode_qprep")
 
 
-def decode_partial(params, d: int, batch: int, n_q_heads: int, n_kv_heads: int, k_pool, v_pool, block_table,
-                   ctx_lens, max_ctx: int, workspace, status=None, stream=None):
-    """tq_decode_partial: the split-K pass over the compressed cache."""
-    _need_cuda(params, k_pool, v_pool, block_table, ctx_lens, workspace, status)
-    rc = load_library().tq_decode_partial(_ptr(params), d, batch, n_q_heads, n_kv_heads, _ptr(k_pool),
-                                          _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
-                                          block_table.shape[1], _ptr(ctx_lens), max_ctx, _ptr(workspace),
-                                          workspace.numel(), _ptr(status), _stream(stream))
-    _check(rc, "tq_decode_partial")
-
-
-def decode_merge(params, d: int, batch: int, n_q_heads: int, n_kv_heads: int, ctx_lens, max_ctx: int, out,
-                 workspace, stream=None):
-    """tq_decode_merge: split merge plus the inverse rotation into out."""
-    _need_cuda(params, ctx_lens, out, workspace)
-    rc = load_library().tq_decode_merge(_ptr(params), d, batch, n_q_heads, n_kv_heads, _ptr(ctx_lens), max_ctx,
-                                        _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
-    _check(rc, "tq_decode_merge")
+def decode_splitk(params, d: int, batch: int, n_q_heads: int, n_kv_heads: int, k_pool, v_pool, block_table,
+                  ctx_lens, max_ctx: int, out, workspace, status=None, stream=None):
+    """tq_decode_splitk: the split-K pass over the compressed cache, merged into out."""
+    _need_cuda(params, k_pool, v_pool, block_table, ctx_lens, out, workspace, status)
+    rc = load_library().tq_decode_splitk(_ptr(params), d, batch, n_q_heads, n_kv_heads, _ptr(k_pool),
+                                         _ptr(v_pool), k_pool.shape[0], _ptr(block_table), block_table.shape[1],
+                                         _ptr(ctx_lens), max_ctx, _ptr(out), _ptr(workspace), workspace.numel(),
+                                         _ptr(status), _stream(stream))
+    _check(rc, "tq_decode_splitk")
 
 
 def decode_attn_noalloc(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens, max_ctx: int,

@@ -13,11 +13,10 @@ cudaError_t launch_append(int d, int dtype, const void *params, const void *k_ne
                           int64_t num_blocks, int32_t *status, cudaStream_t st);
 cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv, int max_ctx,
                          void *ws, cudaStream_t st);
-cudaError_t launch_partial(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
-                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
-                           const int32_t *ctx_lens, int max_ctx, void *ws, int32_t *status, cudaStream_t st);
-cudaError_t launch_merge(int d, const void *params, int batch, int hq, int hkv, const int32_t *ctx_lens, int max_ctx,
-                         float *out, void *ws, cudaStream_t st);
+cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
+                          const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
+                          const int32_t *ctx_lens, int max_ctx, float *out, void *ws, int32_t *status,
+                          cudaStream_t st);
 size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx);
 
 namespace {
@@ -59,6 +58,7 @@ __global__ void codebook_kernel(uint8_t *params, int d) {
     for (int j = 0; j < 7; ++j) h->threshold[j] = (float)(0.5 * (h->centroid64[j] + h->centroid64[j + 1]));
     h->threshold[3] = 0.0f;
     h->threshold[7] = INFINITY;
+    h->one16x2 = 0x3C003C00u;
     h->d = d;
     __threadfence();
     h->magic = kParamsMagic;
@@ -71,6 +71,14 @@ __global__ void signs_kernel(uint8_t *params, int d) {
     if (i >= d) return;
     const int8_t s = reinterpret_cast<const int8_t *>(params + params_off_S(d))[i];
     reinterpret_cast<float *>(params + params_off_D(d))[i] = (s < 0) ? -1.0f : 1.0f;
+}
+
+// S^T (column k of S as a contiguous row) for coalesced projections.
+__global__ void transpose_kernel(uint8_t *params, int d) {
+    const float *S = reinterpret_cast<const float *>(params + params_off_S(d));
+    float *ST = reinterpret_cast<float *>(params + params_off_ST(d));
+    const int i = blockIdx.x, k = threadIdx.x;
+    if (i < d && k < d) ST[(size_t)i * d + k] = S[(size_t)k * d + i];
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -117,6 +125,7 @@ int tq_codebook_init(int d, const int8_t *D_host, const float *S_host, void *par
     if (e == cudaSuccess) { signs_kernel<<<(d + 127) / 128, 128, 0, st>>>(P, d); e = cudaGetLastError(); }
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(P + params_off_S(d), S_host, sizeof(float) * (size_t)d * d, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) { transpose_kernel<<<d, d, 0, st>>>(P, d); e = cudaGetLastError(); }
     if (e == cudaSuccess) { codebook_kernel<<<1, 32, 0, st>>>(P, d); e = cudaGetLastError(); }
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e == cudaSuccess && centroids_out8)
@@ -194,27 +203,18 @@ int tq_decode_qprep(const void *params, int d, const void *q, int dtype, int bat
                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
-int tq_decode_partial(const void *params, int d, int batch, int n_q_heads, int n_kv_heads, const void *k_pool,
-                      const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
-                      const int32_t *ctx_lens, int max_ctx, void *workspace, size_t workspace_bytes,
-                      int32_t *status, tq_stream_t stream) {
+int tq_decode_splitk(const void *params, int d, int batch, int n_q_heads, int n_kv_heads, const void *k_pool,
+                     const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
+                     const int32_t *ctx_lens, int max_ctx, float *out, void *workspace, size_t workspace_bytes,
+                     int32_t *status, tq_stream_t stream) {
     int rc = check_decode(params, d, batch, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
     if (rc != TQ_OK || batch == 0) return rc;
     if (max_blocks <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
-    if (!k_pool || !v_pool || !block_table || !ctx_lens) return TQ_ERR_INVALID;
+    if (!k_pool || !v_pool || !block_table || !ctx_lens || !out) return TQ_ERR_INVALID;
     if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
-    return cuda_status(launch_partial(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks,
-                                      block_table, max_blocks, ctx_lens, max_ctx, workspace, status,
-                                      reinterpret_cast<cudaStream_t>(stream)));
-}
-
-int tq_decode_merge(const void *params, int d, int batch, int n_q_heads, int n_kv_heads, const int32_t *ctx_lens,
-                    int max_ctx, float *out, void *workspace, size_t workspace_bytes, tq_stream_t stream) {
-    int rc = check_decode(params, d, batch, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
-    if (rc != TQ_OK || batch == 0) return rc;
-    if (!ctx_lens || !out) return TQ_ERR_INVALID;
-    return cuda_status(launch_merge(d, params, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx, out, workspace,
-                                    reinterpret_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_splitk(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks,
+                                     block_table, max_blocks, ctx_lens, max_ctx, out, workspace, status,
+                                     reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int tq_decode_attn(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads, int n_kv_heads,
@@ -230,9 +230,8 @@ int tq_decode_attn(const void *params, int d, const void *q, int dtype, int batc
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, max_ctx, workspace, st);
     if (e == cudaSuccess)
-        e = launch_partial(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
-                           max_blocks, ctx_lens, max_ctx, workspace, status, st);
-    if (e == cudaSuccess) e = launch_merge(d, params, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx, out, workspace, st);
+        e = launch_splitk(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
+                          max_blocks, ctx_lens, max_ctx, out, workspace, status, st);
     return cuda_status(e);
 }
 

@@ -24,9 +24,10 @@
 //    2^-22), the softmax weights as one f16 with a running power-of-two scale;
 //    the tensor core accumulates in fp32.
 //
-// Three launches per call: (1) query prep (qbar, u, e4m3 operand fragments),
-// (2) split-K pass producing an online-softmax partial (m, l, acc[d]) per
-// (seq, q head, split), (3) merge of the splits + one inverse rotation per head.
+// Two launches per call: (1) query prep (qbar, u, f16 operand fragments,
+// offset constants); (2) the split-K pass: an online-softmax partial (m, l,
+// acc[d]) per (seq, q head, split); the last split of each (seq, kv head) to
+// finish merges the partials and applies one inverse rotation per head.
 #include <cuda_fp8.h>
 
 #include "tq_internal.cuh"
@@ -42,12 +43,17 @@ __host__ __device__ constexpr int kPartStride(int d) { return d + 4; }   // m, l
 __host__ __device__ constexpr size_t kPackBytes(int d) { return 64 * (size_t)d + 256; }
 __host__ __device__ constexpr int kPackFloatOff(int d) { return 16 * d; }   // in floats
 
+// Workspace: query packs [B*Hkv] | split counters [B*Hkv] | partials [B*Hq][nsplit][d+4].
+// Sized with Hq >= Hkv and the shortest split, so every layout below fits.
+__host__ __device__ constexpr size_t kCounterBytes(int batch, int hq) {
+    return ((size_t)batch * hq * 4 + 255) & ~(size_t)255;
+}
 size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx) {
     if (!valid_d(d) || batch <= 0 || hq <= 0 || max_ctx < 0) return 0;
     const size_t nsplit = (size_t)((max_ctx + kMinSplit - 1) / kMinSplit);
     const size_t pack = (size_t)batch * hq * kPackBytes(d);
     const size_t part = (size_t)batch * hq * (nsplit ? nsplit : 1) * kPartStride(d) * sizeof(float);
-    return pack + part;
+    return pack + kCounterBytes(batch, hq) + part;
 }
 
 namespace {
@@ -63,7 +69,12 @@ __host__ __device__ constexpr float op_delta(int q) {
     return q == 8 ? 0.25f : q == 9 ? 0.5f : q == 10 ? -0.5f : q == 11 ? -0.75f
          : q == 12 ? -0.9375f : q == 13 ? -0.99609375f : q == 14 ? 2.0f : -2.0f;
 }
-__device__ __forceinline__ uint32_t op(uint32_t w, int q) { return (w & op_mask(q)) ^ op_base(q); }
+// (w & mask) ^ base as a single LOP3 (base held in a register by the caller)
+__device__ __forceinline__ uint32_t lop_and_xor(uint32_t w, uint32_t mask, uint32_t base) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(w), "r"(mask), "r"(base));
+    return d;
+}
 
 __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
@@ -103,81 +114,98 @@ __device__ __forceinline__ void walsh4(const float *cen, float (&A)[4]) {
 }
 
 // ---------------------------------------------------------------- (1) query prep
-// One warp per (sequence, query head).  Writes the head's hi and lo columns
-// (2*hg, 2*hg+1) of the K-side B operand for qbar (qu=0) and u (qu=1) into the
-// pack of its (sequence, kv head), and the offset constants.
+// A CTA handles kQRows (sequence, query head) rows: each warp rotates its rows
+// (qbar = Pi q), then thread k computes u_k = (S qbar)_k for every row from
+// S^T (coalesced, each load shared by the rows), then each warp writes its
+// rows' hi and lo columns (2*hg, 2*hg+1) of the K-side B operand for qbar
+// (qu=0) and u (qu=1) into the pack of the row's (sequence, kv head), and the
+// offset constants.
+constexpr int kQRows = 8;
+
 template <int D, int NTK, typename T>
 __global__ void __launch_bounds__(128)
 qprep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ q, int batch, int hq, int hkv,
-             uint8_t *__restrict__ packs) {
-    constexpr int R = D / 32, NKS = D / 16;
-    __shared__ __align__(16) float qb[4][D];
+             uint8_t *__restrict__ packs, unsigned int *__restrict__ counters) {
+    constexpr int R = D / 32, NKS = D / 16, KPT = D / 128;
+    extern __shared__ __align__(16) uint8_t qsm[];
+    float (*qs)[D] = reinterpret_cast<float (*)[D]>(qsm);                       // [kQRows][D] qbar
+    float (*us)[D] = reinterpret_cast<float (*)[D]>(qsm + kQRows * D * 4);      // [kQRows][D] u
+    float *sbuf = reinterpret_cast<float *>(qsm + 2 * kQRows * D * 4);         // S^T chunks
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 4 + warp;
-    if (row >= batch * hq) return;
-    const int b = row / hq, h = row % hq, G = hq / hkv, kvh = h / G, hg = h % G;
+    const int nrows = batch * hq, row0 = blockIdx.x * kQRows;
     const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
-    const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
-    float v[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) v[r] = to_f32<T>(q[(size_t)row * D + 32 * r + lane]) * __ldg(Dsign + 32 * r + lane);
-    fwht_warp<R>(v, lane);
+    const float *ST = reinterpret_cast<const float *>(params + params_off_ST(D));
     const float inv_sd = rsqrtf((float)D);
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        v[r] *= inv_sd;                      // qbar = H D q / sqrt d  (coordinate 32r + lane)
-        qb[warp][32 * r + lane] = v[r];
-    }
-    __syncwarp();
-    float u[R];
+    for (int j = 0; j < kQRows / 4; ++j) {
+        const int rr = warp + 4 * j, row = row0 + rr;
+        float v[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {            // u_k = sum_i S[k][i] qbar_i
-        const float4 *srow = reinterpret_cast<const float4 *>(S + (size_t)(32 * r + lane) * D);
-        const float4 *qq = reinterpret_cast<const float4 *>(qb[warp]);
-        float acc = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < D / 4; ++i) {
-            const float4 a = __ldg(srow + i), bb = qq[i];
-            acc = fmaf(a.x, bb.x, acc);
-            acc = fmaf(a.y, bb.y, acc);
-            acc = fmaf(a.z, bb.z, acc);
-            acc = fmaf(a.w, bb.w, acc);
-        }
-        u[r] = acc;
-    }
-    uint8_t *pack = packs + ((size_t)b * hkv + kvh) * kPackBytes(D);
-    uint16_t *ph = reinterpret_cast<uint16_t *>(pack);
-    float *pf = reinterpret_cast<float *>(pack) + kPackFloatOff(D);
+        for (int r = 0; r < R; ++r)
+            v[r] = (row < nrows) ? to_f32<T>(q[(size_t)row * D + 32 * r + lane]) * __ldg(Dsign + 32 * r + lane) : 0.f;
+        fwht_warp<R>(v, lane);
 #pragma unroll
-    for (int qu = 0; qu < 2; ++qu) {
-        double cs = 0.0;
+        for (int r = 0; r < R; ++r) qs[rr][32 * r + lane] = v[r] * inv_sd;   // qbar = H D q / sqrt d
+    }
+    {
+        float acc[KPT][kQRows];
+#pragma unroll
+        for (int u = 0; u < KPT; ++u)
+#pragma unroll
+            for (int rr = 0; rr < kQRows; ++rr) acc[u][rr] = 0.f;
+        project_streamed<D, kQRows, 128>(ST, sbuf, qs, acc);     // u = S qbar
+#pragma unroll
+        for (int u = 0; u < KPT; ++u)
+#pragma unroll
+            for (int rr = 0; rr < kQRows; ++rr) us[rr][threadIdx.x + 128 * u] = acc[u][rr];
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int j = 0; j < kQRows / 4; ++j) {
+        const int rr = warp + 4 * j, row = row0 + rr;
+        if (row >= nrows) break;
+        const int b = row / hq, h = row % hq, G = hq / hkv, kvh = h / G, hg = h % G;
+        if (hg == 0 && lane == 0) counters[b * hkv + kvh] = 0u;   // split-K completion counter
+        float v[R], u[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const int dim = 32 * r + lane, s = dim >> 4, k = dim & 15, qd = 8 + (s & 7);
-            const float beta = 2.f * (qu == 0 ? v[r] : u[r]) / op_delta(qd);
-            const __half hi = __float2half_rn(beta);
-            const __half lo = __float2half_rn(beta - __half2float(hi));
-            cs += ((double)__half2float(hi) + (double)__half2float(lo)) * (double)(op_alpha(qd) + 0.5f * op_delta(qd));
-            const int reg = k >> 3, tig = (k & 7) >> 1, e = k & 1;
-#pragma unroll
-            for (int x = 0; x < 2; ++x) {
-                const int col = 2 * hg + x, nt = col >> 3, gid = col & 7;
-                const size_t word = ((size_t)(qu * NKS + s) * NTK + nt) * 64 + (4 * gid + tig) * 2 + reg;
-                ph[word * 2 + e] = __half_as_ushort(x == 0 ? hi : lo);
-            }
+            v[r] = qs[rr][32 * r + lane];
+            u[r] = us[rr][32 * r + lane];
         }
+        uint8_t *pack = packs + ((size_t)b * hkv + kvh) * kPackBytes(D);
+        uint16_t *ph = reinterpret_cast<uint16_t *>(pack);
+        float *pf = reinterpret_cast<float *>(pack) + kPackFloatOff(D);
 #pragma unroll
-        for (int m = 16; m > 0; m >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, m);
-        if (lane == 0) pf[qu * 8 + hg] = (float)cs;
-    }
-    // columns beyond the group's 2*G are zero (written by the group's first head)
-    if (hg == 0) {
-        uint32_t *pw = reinterpret_cast<uint32_t *>(pack);
-        for (int col = 2 * G; col < 8 * NTK; ++col) {
-            const int nt = col >> 3, gid = col & 7;
-            for (int i = lane; i < 2 * NKS * 8; i += 32) {
-                const int qu = i / (NKS * 8), s = (i / 8) % NKS, k = i % 8;
-                pw[((size_t)(qu * NKS + s) * NTK + nt) * 64 + (4 * gid + (k >> 1)) * 2 + (k & 1)] = 0u;
+        for (int qu = 0; qu < 2; ++qu) {
+            double cs = 0.0;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int dim = 32 * r + lane, s = dim >> 4, k = dim & 15, qd = 8 + (s & 7);
+                const float beta = 2.f * (qu == 0 ? v[r] : u[r]) / op_delta(qd);
+                const __half hi = __float2half_rn(beta);
+                const __half lo = __float2half_rn(beta - __half2float(hi));
+                cs += ((double)__half2float(hi) + (double)__half2float(lo)) * (double)(op_alpha(qd) + 0.5f * op_delta(qd));
+                const int reg = k >> 3, tig = (k & 7) >> 1, e = k & 1;
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const int col = 2 * hg + x, nt = col >> 3, gid = col & 7;
+                    const size_t word = ((size_t)(qu * NKS + s) * NTK + nt) * 64 + (4 * gid + tig) * 2 + reg;
+                    ph[word * 2 + e] = __half_as_ushort(x == 0 ? hi : lo);
+                }
+            }
+#pragma unroll
+            for (int m = 16; m > 0; m >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, m);
+            if (lane == 0) pf[qu * 8 + hg] = (float)cs;
+        }
+        // columns beyond the group's 2*G are zero (written by the group's first head)
+        if (hg == 0) {
+            uint32_t *pw = reinterpret_cast<uint32_t *>(pack);
+            for (int col = 2 * G; col < 8 * NTK; ++col) {
+                const int nt = col >> 3, gid = col & 7;
+                for (int i = lane; i < 2 * NKS * 8; i += 32) {
+                    const int qu = i / (NKS * 8), s = (i / 8) % NKS, k = i % 8;
+                    pw[((size_t)(qu * NKS + s) * NTK + nt) * 64 + (4 * gid + (k >> 1)) * 2 + (k & 1)] = 0u;
+                }
             }
         }
     }
@@ -199,17 +227,18 @@ __device__ __forceinline__ int64_t block_of(const int32_t *__restrict__ bt, int 
     return (p >= 0 && p < num_blocks) ? p : -1;
 }
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+#ifndef TQ_SPLITK_BPW
+#define TQ_SPLITK_BPW 2          // blocks scored per warp per chunk
+#endif
+#ifndef TQ_SPLITK_MINBLOCKS
+#define TQ_SPLITK_MINBLOCKS 4    // resident CTAs per SM the register budget is sized for (4-warp CTAs)
+#endif
 
 template <int D, int NWARP>
 struct SplitCfg {
     static constexpr int NT = NWARP * 32;
-    static constexpr int BPW = 2;                    // blocks scored per warp per chunk
+    static constexpr int BPW = TQ_SPLITK_BPW;        // blocks scored per warp per chunk
     static constexpr int BPC = NWARP * BPW;          // blocks per chunk
     static constexpr int CH = kBlock * BPC;          // tokens per chunk
     static constexpr int KREC = (int)k_record(D), VREC = (int)v_record(D);
@@ -224,11 +253,12 @@ constexpr size_t split_smem_bytes() {
 }
 
 template <int D, int G, int NWARP>
-__global__ void __launch_bounds__(NWARP * 32, (NWARP == 4 ? 3 : 1))
+__global__ void __launch_bounds__(NWARP * 32, (NWARP == 4 ? TQ_SPLITK_MINBLOCKS : 1))
 decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ packs, int hq, int hkv,
                   const uint8_t *__restrict__ k_pool, const uint8_t *__restrict__ v_pool, int64_t num_blocks,
                   const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_lens,
-                  int max_ctx, int split, float *__restrict__ part, int nsplit, int32_t *status) {
+                  int max_ctx, int split, float *__restrict__ part, int nsplit, unsigned int *__restrict__ counters,
+                  float *__restrict__ out, int32_t *status) {
     using C = SplitCfg<D, NWARP>;
     constexpr int NT_ = C::NT, BPW = C::BPW, BPC = C::BPC, CH = C::CH;
     constexpr int TPL = CH / 32;               // softmax tokens per lane
@@ -256,7 +286,11 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
     int L = ctx_lens[b];
     if (L > max_ctx) L = max_ctx;
     const int t0 = s * split;
-    if (t0 >= L) return;                       // the merge only reads splits that hold tokens
+    if (t0 >= L) {                             // nothing to attend: split 0 writes out = 0
+        if (L <= 0 && s == 0)
+            for (int i = tid; i < G * D; i += NT_) out[((size_t)b * hq + kh * G) * D + i] = 0.f;
+        return;
+    }
     const int t1 = min(L, t0 + split);
 
     // stage the K and V records of the chunk starting at token tc into buffer buf
@@ -286,6 +320,8 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
     const float Asum = A[0] + A[1] + A[2] + A[3];
     const float inv_sd = rsqrtf((float)D);
     const float qjl = 1.2533141373155003f / (float)D;   // sqrt(pi/2) / d
+    // f16x2 {1.0, 1.0}, read at run time so that it stays in a register for LOP3
+    const uint32_t one16x2 = (uint32_t)ph->one16x2;
 
     // weight rows of heads >= G stay zero
     for (int i = tid; i < (8 - G) * PROW; i += NT_) sP[G * PROW + i] = __float2half(0.f);
@@ -318,7 +354,7 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
     for (int i = 0; i < MTW; ++i) {
         const int q = 8 + ((warp * MTW + i) & 7);
         vmask[i] = 0x00010001u << q;
-        vbase[i] = (q == 14) ? 0u : 0x3C003C00u;
+        vbase[i] = (q == 14) ? 0u : one16x2;
     }
     const int mhi = (warp * MTW) >> 3;
 
@@ -375,46 +411,47 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
                 nrm[r] = __low2float(ng);
                 gam[r] = __high2float(ng);
             }
-            // masks in sequence: code = sum_m A_m (mask m), qjl = mask 4
-            float code[NTK][4], qjv[NTK][4];
+            // five masks as independent accumulator chains: code = sum_m A_m (mask m), qjl = mask 4
+            uint32_t w[5][2][NW], w8[5][2][NW];
 #pragma unroll
-            for (int nt = 0; nt < NTK; ++nt)
-#pragma unroll
-                for (int x = 0; x < 4; ++x) code[nt][x] = qjv[nt][x] = 0.f;
-#pragma unroll
-            for (int m = 0; m < 5; ++m) {
-                uint32_t w[2][NW], w8[2][NW];
+            for (int m = 0; m < 5; ++m)
 #pragma unroll
                 for (int th = 0; th < 2; ++th)
 #pragma unroll
                     for (int wj = 0; wj < NW; ++wj) {
-                        w[th][wj] = (m < 3) ? W[m][th][wj]
-                                  : (m == 3) ? (W[0][th][wj] ^ W[1][th][wj] ^ W[2][th][wj]) : W[3][th][wj];
-                        w8[th][wj] = w[th][wj] << 8;
+                        w[m][th][wj] = (m < 3) ? W[m][th][wj]
+                                     : (m == 3) ? (W[0][th][wj] ^ W[1][th][wj] ^ W[2][th][wj]) : W[3][th][wj];
+                        w8[m][th][wj] = w[m][th][wj] << 8;
                     }
-                float acc[NTK][4];
+            float acc[5][NTK][4];
+#pragma unroll
+            for (int m = 0; m < 5; ++m)
 #pragma unroll
                 for (int nt = 0; nt < NTK; ++nt)
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) acc[nt][x] = 0.f;
-                const int qu = (m == 4) ? 1 : 0;
+                    for (int x = 0; x < 4; ++x) acc[m][nt][x] = 0.f;
 #pragma unroll
-                for (int ks = 0; ks < NKS; ++ks) {
-                    const int q = 8 + (ks & 7), wj = ks >> 3;
-                    const uint32_t a0 = op(w8[0][wj], q), a1 = op(w8[1][wj], q);
-                    const uint32_t a2 = op(w[0][wj], q), a3 = op(w[1][wj], q);
+            for (int ks = 0; ks < NKS; ++ks) {
+                const int q = 8 + (ks & 7), wj = ks >> 3;
+                const uint32_t msk = op_mask(q), bas = (q == 14) ? 0u : one16x2;
+#pragma unroll
+                for (int m = 0; m < 5; ++m) {
+                    const uint32_t a0 = lop_and_xor(w8[m][0][wj], msk, bas), a1 = lop_and_xor(w8[m][1][wj], msk, bas);
+                    const uint32_t a2 = lop_and_xor(w[m][0][wj], msk, bas), a3 = lop_and_xor(w[m][1][wj], msk, bas);
+                    const int qu = (m == 4) ? 1 : 0;
 #pragma unroll
                     for (int nt = 0; nt < NTK; ++nt)
-                        mma_f16(acc[nt], a0, a1, a2, a3, bq[qu][ks][nt][0], bq[qu][ks][nt][1]);
+                        mma_f16(acc[m][nt], a0, a1, a2, a3, bq[qu][ks][nt][0], bq[qu][ks][nt][1]);
                 }
-#pragma unroll
-                for (int nt = 0; nt < NTK; ++nt)
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        if (m < 4) code[nt][x] = fmaf(A[m], acc[nt][x], code[nt][x]);
-                        else qjv[nt][x] = acc[nt][x];
-                    }
             }
+            float code[NTK][4], qjv[NTK][4];
+#pragma unroll
+            for (int nt = 0; nt < NTK; ++nt)
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    code[nt][x] = A[0] * acc[0][nt][x] + A[1] * acc[1][nt][x] + A[2] * acc[2][nt][x] + A[3] * acc[3][nt][x];
+                    qjv[nt][x] = acc[4][nt][x];
+                }
 #pragma unroll
             for (int nt = 0; nt < NTK; ++nt) {
                 const int hg = 4 * nt + tig;
@@ -511,8 +548,8 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
                 const uint32_t x0s = x0 << 8, x1s = x1 << 8;
 #pragma unroll
                 for (int i = 0; i < MTW; ++i) {
-                    const uint32_t a0 = (x0s & vmask[i]) ^ vbase[i], a1 = (x1s & vmask[i]) ^ vbase[i];
-                    const uint32_t a2 = (x0 & vmask[i]) ^ vbase[i], a3 = (x1 & vmask[i]) ^ vbase[i];
+                    const uint32_t a0 = lop_and_xor(x0s, vmask[i], vbase[i]), a1 = lop_and_xor(x1s, vmask[i], vbase[i]);
+                    const uint32_t a2 = lop_and_xor(x0, vmask[i], vbase[i]), a3 = lop_and_xor(x1, vmask[i], vbase[i]);
                     mma_f16(O[m][i], a0, a1, a2, a3, b0, b1);
                 }
             }
@@ -560,51 +597,47 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
             dst[1] = sL[h];
         }
     }
-}
-
-// ---------------------------------------------------------------- (3) merge + inverse rotation
-template <int D>
-__global__ void __launch_bounds__(128)
-merge_kernel(const uint8_t *__restrict__ params, const float *__restrict__ part, const int32_t *__restrict__ ctx_lens,
-             int max_ctx, int split, int hq, int n_rows, int nsplit, float *__restrict__ out) {
+    // ---- the last split of this (sequence, kv head) to finish merges all of them
+    __shared__ bool s_last;
+    __threadfence();                           // every thread publishes its part of the partial
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned int nsb = (unsigned int)((L + split - 1) / split);
+        const unsigned int done = atomicAdd(&counters[b * hkv + kh], 1u) + 1u;
+        s_last = (done == nsb);
+        if (s_last) counters[b * hkv + kh] = 0u;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int nsb = (L + split - 1) / split;
     constexpr int R = D / 32;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int row = blockIdx.x * 4 + warp;
-    if (row >= n_rows) return;
-    const int b = row / hq;
-    int L = ctx_lens[b];
-    if (L > max_ctx) L = max_ctx;
-    float *o = out + (size_t)row * D;
-    if (L <= 0) {
+    for (int h = warp; h < G; h += NWARP) {
+        const int row = b * hq + kh * G + h;
+        const float *p0 = part + (size_t)row * nsplit * kPartStride(D);
+        float M = -INFINITY;
+        for (int t = 0; t < nsb; ++t) M = fmaxf(M, __ldcg(p0 + (size_t)t * kPartStride(D)));
+        float v[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) o[32 * r + lane] = 0.f;
-        return;
+        for (int r = 0; r < R; ++r) v[r] = 0.f;
+        float l = 0.f;
+        for (int t = 0; t < nsb; ++t) {
+            const float *ps = p0 + (size_t)t * kPartStride(D);
+            const float m = __ldcg(ps);
+            const float w = (m == -INFINITY) ? 0.f : __expf(m - M);
+            l = fmaf(__ldcg(ps + 1), w, l);
+#pragma unroll
+            for (int r = 0; r < R; ++r) v[r] = fmaf(__ldcg(ps + 4 + 32 * r + lane), w, v[r]);
+        }
+        const float inv = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+        for (int r = 0; r < R; ++r) v[r] *= inv;
+        // out = Pi^T a = D (H a) / sqrt d
+        fwht_warp<R>(v, lane);
+        const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
+#pragma unroll
+        for (int r = 0; r < R; ++r) out[(size_t)row * D + 32 * r + lane] = v[r] * inv_sd * __ldg(Dsign + 32 * r + lane);
     }
-    const int ns = (L + split - 1) / split;
-    const float *p0 = part + (size_t)row * nsplit * kPartStride(D);
-    float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, p0[(size_t)s * kPartStride(D)]);
-    float v[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) v[r] = 0.f;
-    float l = 0.f;
-    for (int s = 0; s < ns; ++s) {
-        const float *ps = p0 + (size_t)s * kPartStride(D);
-        const float m = ps[0];
-        const float w = (m == -INFINITY) ? 0.f : __expf(m - M);
-        l = fmaf(ps[1], w, l);
-#pragma unroll
-        for (int r = 0; r < R; ++r) v[r] = fmaf(ps[4 + 32 * r + lane], w, v[r]);
-    }
-    const float inv = (l > 0.f) ? 1.f / l : 0.f;
-#pragma unroll
-    for (int r = 0; r < R; ++r) v[r] *= inv;
-    // out = Pi^T a = D (H a) / sqrt d
-    fwht_warp<R>(v, lane);
-    const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
-    const float inv_sd = rsqrtf((float)D);
-#pragma unroll
-    for (int r = 0; r < R; ++r) o[32 * r + lane] = v[r] * inv_sd * __ldg(Dsign + 32 * r + lane);
 }
 
 // Context split length: the shortest power-of-two multiple of 512 tokens that
@@ -619,6 +652,7 @@ int choose_split(int batch, int hkv, int max_ctx) {
 
 struct WsLayout {
     uint8_t *packs;
+    unsigned int *counters;
     float *part;
     int split;
     int nsplit;
@@ -628,38 +662,51 @@ WsLayout ws_layout(void *ws, int d, int batch, int hq, int hkv, int max_ctx) {
     w.split = choose_split(batch, hkv, max_ctx);
     w.nsplit = max(1, (max_ctx + w.split - 1) / w.split);
     w.packs = reinterpret_cast<uint8_t *>(ws);
-    w.part = reinterpret_cast<float *>(w.packs + (size_t)batch * hq * kPackBytes(d));
+    w.counters = reinterpret_cast<unsigned int *>(w.packs + (size_t)batch * hq * kPackBytes(d));
+    w.part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(w.counters) + kCounterBytes(batch, hq));
     return w;
 }
 
+template <int D, int NTK, typename T>
+cudaError_t qprep_launch_t(const uint8_t *P, const void *q, int batch, int hq, int hkv, uint8_t *packs,
+                           unsigned int *counters, cudaStream_t st) {
+    constexpr size_t smem = (size_t)2 * kQRows * D * 4 + (size_t)2 * kProjRows * D * 4;
+    auto kern = qprep_kernel<D, NTK, T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<(batch * hq + kQRows - 1) / kQRows, 128, smem, st>>>(P, (const T *)q, batch, hq, hkv, packs, counters);
+    return cudaGetLastError();
+}
+
 template <int D, typename T>
-void qprep_launch(const uint8_t *P, const void *q, int batch, int hq, int hkv, uint8_t *packs, cudaStream_t st) {
-    const dim3 grid((batch * hq + 3) / 4);
-    const int G = hq / hkv;
+cudaError_t qprep_launch(const uint8_t *P, const void *q, int batch, int hq, int hkv, uint8_t *packs,
+                         unsigned int *counters, cudaStream_t st) {
     // n-tile count of the K-side operand: (2G + 7) / 8, as in decode_mma_kernel
-    if (G <= 4) qprep_kernel<D, 1, T><<<grid, 128, 0, st>>>(P, (const T *)q, batch, hq, hkv, packs);
-    else qprep_kernel<D, 2, T><<<grid, 128, 0, st>>>(P, (const T *)q, batch, hq, hkv, packs);
+    if (hq / hkv <= 4) return qprep_launch_t<D, 1, T>(P, q, batch, hq, hkv, packs, counters, st);
+    return qprep_launch_t<D, 2, T>(P, q, batch, hq, hkv, packs, counters, st);
 }
 
 template <int D, int G>
 cudaError_t partial_launch_g(dim3 grid, cudaStream_t st, const uint8_t *P, const uint8_t *packs, int hq, int hkv,
                              const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
-                             const int32_t *ctx, int max_ctx, int split, float *part, int nsplit, int32_t *status) {
+                             const int32_t *ctx, int max_ctx, int split, float *part, int nsplit,
+                             unsigned int *counters, float *out, int32_t *status) {
     constexpr int NWARP = G <= 4 ? 4 : 8;
     constexpr size_t smem = split_smem_bytes<D, G, NWARP>();
     auto kern = decode_mma_kernel<D, G, NWARP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, NWARP * 32, smem, st>>>(P, packs, hq, hkv, kp, vp, nb, bt, mb, ctx, max_ctx, split, part, nsplit,
-                                        status);
+                                        counters, out, status);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t partial_launch(int G, dim3 grid, cudaStream_t st, const uint8_t *P, const uint8_t *packs, int hq,
                            int hkv, const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
-                           const int32_t *ctx, int max_ctx, int split, float *part, int nsplit, int32_t *status) {
-#define TQ_PART(GG) return partial_launch_g<D, GG>(grid, st, P, packs, hq, hkv, kp, vp, nb, bt, mb, ctx, max_ctx, split, part, nsplit, status)
+                           const int32_t *ctx, int max_ctx, int split, float *part, int nsplit,
+                           unsigned int *counters, float *out, int32_t *status) {
+#define TQ_PART(GG) return partial_launch_g<D, GG>(grid, st, P, packs, hq, hkv, kp, vp, nb, bt, mb, ctx, max_ctx, split, part, nsplit, counters, out, status)
     switch (G) {
         case 1: TQ_PART(1);
         case 2: TQ_PART(2);
@@ -679,19 +726,17 @@ cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, in
                          int max_ctx, void *ws, cudaStream_t st) {
     const WsLayout w = ws_layout(ws, d, batch, hq, hkv, max_ctx);
     const uint8_t *P = (const uint8_t *)params;
-    if (d == 128) {
-        if (dtype == TQ_DTYPE_BF16) qprep_launch<128, __nv_bfloat16>(P, q, batch, hq, hkv, w.packs, st);
-        else qprep_launch<128, float>(P, q, batch, hq, hkv, w.packs, st);
-    } else {
-        if (dtype == TQ_DTYPE_BF16) qprep_launch<256, __nv_bfloat16>(P, q, batch, hq, hkv, w.packs, st);
-        else qprep_launch<256, float>(P, q, batch, hq, hkv, w.packs, st);
-    }
-    return cudaGetLastError();
+    if (d == 128)
+        return dtype == TQ_DTYPE_BF16 ? qprep_launch<128, __nv_bfloat16>(P, q, batch, hq, hkv, w.packs, w.counters, st)
+                                      : qprep_launch<128, float>(P, q, batch, hq, hkv, w.packs, w.counters, st);
+    return dtype == TQ_DTYPE_BF16 ? qprep_launch<256, __nv_bfloat16>(P, q, batch, hq, hkv, w.packs, w.counters, st)
+                                  : qprep_launch<256, float>(P, q, batch, hq, hkv, w.packs, w.counters, st);
 }
 
-cudaError_t launch_partial(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
-                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
-                           const int32_t *ctx_lens, int max_ctx, void *ws, int32_t *status, cudaStream_t st) {
+cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
+                          const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
+                          const int32_t *ctx_lens, int max_ctx, float *out, void *ws, int32_t *status,
+                          cudaStream_t st) {
     const WsLayout w = ws_layout(ws, d, batch, hq, hkv, max_ctx);
     const dim3 grid(w.nsplit, hkv, batch);
     const int G = hq / hkv;
@@ -699,21 +744,10 @@ cudaError_t launch_partial(int d, const void *params, int batch, int hq, int hkv
     if (d == 128)
         return partial_launch<128>(G, grid, st, P, w.packs, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
                                    num_blocks, block_table, max_blocks, ctx_lens, max_ctx, w.split, w.part, w.nsplit,
-                                   status);
+                                   w.counters, out, status);
     return partial_launch<256>(G, grid, st, P, w.packs, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
                                num_blocks, block_table, max_blocks, ctx_lens, max_ctx, w.split, w.part, w.nsplit,
-                               status);
-}
-
-cudaError_t launch_merge(int d, const void *params, int batch, int hq, int hkv, const int32_t *ctx_lens, int max_ctx,
-                         float *out, void *ws, cudaStream_t st) {
-    const int rows = batch * hq;
-    const WsLayout w = ws_layout(ws, d, batch, hq, hkv, max_ctx);
-    const uint8_t *P = (const uint8_t *)params;
-    const dim3 gq((rows + 3) / 4);
-    if (d == 128) merge_kernel<128><<<gq, 128, 0, st>>>(P, w.part, ctx_lens, max_ctx, w.split, hq, rows, w.nsplit, out);
-    else merge_kernel<256><<<gq, 128, 0, st>>>(P, w.part, ctx_lens, max_ctx, w.split, hq, rows, w.nsplit, out);
-    return cudaGetLastError();
+                               w.counters, out, status);
 }
 
 }  // namespace tq

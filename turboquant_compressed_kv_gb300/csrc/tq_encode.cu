@@ -7,272 +7,266 @@
 // same steps.  Slots follow the paged layout of the vLLM-MLX explainer,
 // "Paged KVキャッシュ".
 //
-// One warp encodes one (token, kv head) vector.  Lane l holds coordinates
-// kdim/vdim(l, r) for r < d/32, so the rotation runs in registers and
-// shuffles, and every packed word is one __ballot_sync.
+// A CTA of 4 warps encodes tiles of 16 (bulk) or 4 (append) vectors,
+// persistent over tiles:
+//  1. one warp per vector: norm, rotation (in registers and shuffles), cells,
+//     residual (K) written to shared memory;
+//  2. K only, all threads: the 16 QJL projections S rho, thread k computing
+//     row k for every vector of the tile from S^T in shared memory (resident
+//     for d=128, streamed in chunks for d=256); sign bits to shared memory;
+//  3. one warp per vector: ballot-pack cells and signs, byte/word stores.
+// One launch may carry K (blockIdx.y == 0) and V (blockIdx.y == 1) tiles.
 #include "tq_internal.cuh"
 
 namespace tq {
 namespace {
 
-constexpr int kWarps = 4;   // warps per CTA in the encode kernels
+constexpr int kWarps = 4;                  // warps per CTA
 
-struct EncodeSmem {
-    float centroid[8];
-    float threshold[8];
+// Where vector v of a launch goes: slot (or -1 to skip) and its input row.
+struct SlotMap {
+    const int64_t *slots;                  // bulk: slots[token]
+    const int32_t *block_table;            // append: slot from the block table and length
+    const int32_t *ctx_lens;
+    int max_blocks;
+    int64_t num_blocks;
+    int n_heads;
+    __device__ int64_t slot(int64_t token, int32_t *status, bool report) const {
+        int64_t s = -1;
+        if (slots) {
+            s = slots[token];
+            if (s < 0) return -1;
+        } else {
+            const int Lb = ctx_lens[token];
+            if (Lb < 0) return -1;
+            const int lb = Lb / kBlock;
+            const int64_t blk = (lb < max_blocks) ? (int64_t)block_table[(size_t)token * max_blocks + lb] : -1;
+            s = (blk >= 0) ? blk * kBlock + (Lb % kBlock) : -2;
+            if (s == -2) {   // no block for this position
+                if (report) flag_status(status, TQ_STATUS_BAD_SLOT);
+                return -1;
+            }
+        }
+        if (s / kBlock >= num_blocks) {
+            if (report) flag_status(status, TQ_STATUS_BAD_SLOT);
+            return -1;
+        }
+        return s;
+    }
 };
 
-// Encode the vector at x (d contiguous values) into slot `slot` of the pool.
-// rho_smem: per-warp scratch of d floats (K only).
-template <int D, bool IS_K, typename T>
-__device__ __forceinline__ void encode_vector(const uint8_t *__restrict__ params, const EncodeSmem &sm,
-                                              const T *__restrict__ x, int64_t slot, int head, int n_heads,
-                                              uint8_t *__restrict__ pool, float *rho_smem, int lane) {
-    constexpr int R = D / 32;
-    const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
-    float v[R];
-    int dims[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        dims[r] = IS_K ? kdim<D>(lane, r) : vdim<D>(lane, r);
-        v[r] = to_f32<T>(x[dims[r]]);
-    }
-    // step 1: L2 norm
-    float ss = 0.f;
-#pragma unroll
-    for (int r = 0; r < R; ++r) ss = fmaf(v[r], v[r], ss);
-    const float n = sqrtf(warp_sum(ss));
-    // step 2: randomized WHT; z = sqrt(d) * Pi(x/n) = H(D x) / n
-#pragma unroll
-    for (int r = 0; r < R; ++r) v[r] *= __ldg(Dsign + dims[r]);
-    fwht_warp<R>(v, lane);
-    int code[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const float z = (n > 0.f) ? v[r] / n : 0.f;
-        v[r] = z;
-        // step 3: 3-bit Lloyd-Max cell = number of thresholds <= z
-        int k = 0;
-#pragma unroll
-        for (int j = 0; j < 7; ++j) k += (z >= sm.threshold[j]) ? 1 : 0;
-        code[r] = k;
-    }
-    const int64_t blk = slot / kBlock;
-    const int off = (int)(slot % kBlock);
-    if (IS_K) {
-        // step 4: residual in the rotated, unit-variance domain: rho = z - c[cell]
-        float g2 = 0.f;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const float rho = v[r] - sm.centroid[code[r]];
-            v[r] = rho;
-            g2 = fmaf(rho, rho, g2);
-            rho_smem[dims[r]] = rho;
-        }
-        // gamma = ||y - c/sqrt d|| = ||rho|| / sqrt d
-        const float gamma = sqrtf(warp_sum(g2)) / sqrtf((float)D);
-        __syncwarp();
-        // step 5: QJL signs, bit k = [(S rho)_k >= 0]  (sqrt d > 0 does not change a sign)
-        const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
-        bool sbit[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const float4 *row = reinterpret_cast<const float4 *>(S + (size_t)dims[r] * D);
-            const float4 *rr = reinterpret_cast<const float4 *>(rho_smem);
-            float acc = 0.f;
-#pragma unroll 8
-            for (int i = 0; i < D / 4; ++i) {
-                const float4 a = __ldg(row + i);
-                const float4 b = rr[i];
-                acc = fmaf(a.x, b.x, acc);
-                acc = fmaf(a.y, b.y, acc);
-                acc = fmaf(a.z, b.z, acc);
-                acc = fmaf(a.w, b.w, acc);
-            }
-            sbit[r] = acc >= 0.f;
-        }
-        __syncwarp();
-        uint8_t *rec = pool + ((size_t)blk * n_heads + head) * k_record(D);
-        uint32_t *planes = reinterpret_cast<uint32_t *>(rec);
-        constexpr int NW = D / 128;
-        const int gid = off & 7, th = off >> 3;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint32_t w0 = __ballot_sync(0xffffffffu, code[r] & 1);
-            const uint32_t w1 = __ballot_sync(0xffffffffu, (code[r] >> 1) & 1);
-            const uint32_t w2 = __ballot_sync(0xffffffffu, (code[r] >> 2) & 1);
-            const uint32_t ws = __ballot_sync(0xffffffffu, sbit[r]);
-            if (lane == r) {
-                const int L = 4 * gid + (r & 3);
-                const size_t word = (size_t)(L * 2 + th) * NW + (r >> 2);
-                const size_t plane_words = 2 * D / 4;
-                planes[word] = w0;
-                planes[plane_words + word] = w1;
-                planes[2 * plane_words + word] = w2;
-                planes[3 * plane_words + word] = ws;
-            }
-        }
-        if (lane == 0) {
-            __half2 nh = __halves2half2(__float2half_rn(n), __float2half_rn(gamma));
-            *reinterpret_cast<__half2 *>(rec + 8 * D + 4 * off) = nh;
-        }
-    } else {
-        uint8_t *rec = pool + ((size_t)blk * n_heads + head) * v_record(D);
-        constexpr int NWV = D / 64;
-        constexpr int NM = D / 128;
-        const int tigv = (off & 7) >> 1, jb = (off >> 3) + 2 * (off & 1);   // lane tig, byte in word
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint32_t w0 = __ballot_sync(0xffffffffu, code[r] & 1);
-            const uint32_t w1 = __ballot_sync(0xffffffffu, (code[r] >> 1) & 1);
-            const uint32_t w2 = __ballot_sync(0xffffffffu, (code[r] >> 2) & 1);
-            if ((lane >> 2) == r) {
-                const int beta = lane & 3;
-                const int tau = 4 * r + beta;
-                const int mhi = tau % NM, rh = (tau / NM) & 1, gid = tau / (2 * NM);
-                const int L = 4 * gid + tigv;
-                const size_t byte = ((size_t)L * NWV + 2 * mhi + rh) * 4 + jb;
-                rec[byte] = (uint8_t)(w0 >> (8 * beta));
-                rec[2 * D + byte] = (uint8_t)(w1 >> (8 * beta));
-                rec[4 * D + byte] = (uint8_t)(w2 >> (8 * beta));
-            }
-        }
-        if (lane == 0) *reinterpret_cast<__half *>(rec + 6 * D + 2 * off) = __float2half_rn(n);
-    }
-}
+// TILE vectors per CTA: 16 for bulk encodes (each S^T read serves 16
+// vectors), 4 for the one-token append (more CTAs, shorter latency chains).
+template <int D, int TILE>
+struct EncSmem {
+    static constexpr bool kResident = (D == 128);
+    static constexpr size_t kST = kResident ? (size_t)D * D * 4 : (size_t)2 * kProjRows * D * 4;
+    static constexpr size_t kRho = (size_t)TILE * D * 4;
+    static constexpr size_t kSgn = (size_t)TILE * D;
+    static constexpr size_t kBytes = kST + kRho + kSgn;
+};
 
-__device__ __forceinline__ void load_codebook(const uint8_t *params, EncodeSmem &sm) {
-    const ParamsHeader *h = reinterpret_cast<const ParamsHeader *>(params);
+// kinds: 1 = K only, 2 = V only, 3 = K (blockIdx.y 0) and V (blockIdx.y 1).
+template <int D, int TILE, typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+encode_kernel(const uint8_t *__restrict__ params, const T *__restrict__ xk, const T *__restrict__ xv, int64_t n_vec,
+              SlotMap map, uint8_t *__restrict__ k_pool, uint8_t *__restrict__ v_pool, int kinds, int32_t *status) {
+    constexpr int R = D / 32;
+    constexpr int kTile = TILE, kPerWarp = TILE / kWarps;
+    using SM = EncSmem<D, TILE>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    float *sST = reinterpret_cast<float *>(smem);
+    float (*s_rho)[D] = reinterpret_cast<float (*)[D]>(smem + SM::kST);
+    uint8_t (*s_sgn)[D] = reinterpret_cast<uint8_t (*)[D]>(smem + SM::kST + SM::kRho);
+    __shared__ float s_cent[8], s_thr[8];
+    const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
+    if (ph->magic != kParamsMagic || ph->d != D) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
+        return;
+    }
+    const bool is_k = (kinds == 3) ? (blockIdx.y == 0) : (kinds == 1);
+    const T *__restrict__ x = is_k ? xk : xv;
+    uint8_t *__restrict__ pool = is_k ? k_pool : v_pool;
+    const float *gST = reinterpret_cast<const float *>(params + params_off_ST(D));
+    if (is_k && SM::kResident) stage_st_rows<D, kWarps * 32>(sST, gST, 0, D);   // waited before first use
     if (threadIdx.x < 8) {
-        sm.centroid[threadIdx.x] = h->centroid[threadIdx.x];
-        sm.threshold[threadIdx.x] = h->threshold[threadIdx.x];
+        s_cent[threadIdx.x] = ph->centroid[threadIdx.x];
+        s_thr[threadIdx.x] = ph->threshold[threadIdx.x];
     }
     __syncthreads();
-}
-
-__device__ __forceinline__ bool params_ok(const uint8_t *params, int d) {
-    const ParamsHeader *h = reinterpret_cast<const ParamsHeader *>(params);
-    return h->magic == kParamsMagic && h->d == d;
-}
-
-template <int D, bool IS_K, typename T>
-__global__ void __launch_bounds__(kWarps * 32)
-encode_kernel(const uint8_t *__restrict__ params, const T *__restrict__ x, int64_t n_tokens, int n_heads,
-              const int64_t *__restrict__ slots, uint8_t *__restrict__ pool, int64_t num_blocks,
-              int32_t *status) {
-    __shared__ EncodeSmem sm;
-    __shared__ __align__(16) float rho[kWarps][D];
-    if (!params_ok(params, D)) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
-        return;
-    }
-    load_codebook(params, sm);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t nv = n_tokens * n_heads;
-    for (int64_t v = (int64_t)blockIdx.x * kWarps + warp; v < nv; v += (int64_t)gridDim.x * kWarps) {
-        const int64_t tok = v / n_heads;
-        const int head = (int)(v % n_heads);
-        const int64_t slot = slots[tok];
-        if (slot < 0) continue;
-        if (slot / kBlock >= num_blocks) {
-            if (lane == 0) flag_status(status, TQ_STATUS_BAD_SLOT);
-            continue;
+    const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
+    const int64_t ntiles = (n_vec + kTile - 1) / kTile;
+
+#pragma unroll 1
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t v0 = tile * kTile;
+        int code[kPerWarp][R];
+        float nrm[kPerWarp], gam[kPerWarp];
+        int64_t slot[kPerWarp];
+        // ---- 1. norm, rotation, cells, residual
+#pragma unroll
+        for (int j = 0; j < kPerWarp; ++j) {
+            const int tv = warp + kWarps * j;              // vector within the tile
+            const int64_t v = v0 + tv;
+            slot[j] = -1;
+            if (v < n_vec)   // a bad slot is reported once per token (by the K tile of an append)
+                slot[j] = map.slot(v / map.n_heads, status, (kinds != 3 || is_k) && lane == 0 && (v % map.n_heads) == 0);
+            float val[R];
+            int dims[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                dims[r] = is_k ? kdim<D>(lane, r) : vdim<D>(lane, r);
+                val[r] = (slot[j] >= 0) ? to_f32<T>(x[v * D + dims[r]]) : 0.f;
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) ss = fmaf(val[r], val[r], ss);
+            const float n = sqrtf(warp_sum(ss));
+#pragma unroll
+            for (int r = 0; r < R; ++r) val[r] *= __ldg(Dsign + dims[r]);
+            fwht_warp<R>(val, lane);                       // z = H(D x) / n = sqrt(d) Pi (x/n)
+            float g2 = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float z = (n > 0.f) ? val[r] / n : 0.f;
+                int k = 0;
+#pragma unroll
+                for (int t = 0; t < 7; ++t) k += (z >= s_thr[t]) ? 1 : 0;
+                code[j][r] = k;
+                if (is_k) {
+                    const float rho = z - s_cent[k];     // residual, rotated unit-variance domain
+                    g2 = fmaf(rho, rho, g2);
+                    s_rho[tv][dims[r]] = rho;
+                }
+            }
+            nrm[j] = n;
+            gam[j] = is_k ? sqrtf(warp_sum(g2)) / sqrtf((float)D) : 0.f;   // ||y - c/sqrt d|| = ||rho|| / sqrt d
         }
-        encode_vector<D, IS_K, T>(params, sm, x + v * D, slot, head, n_heads, pool, rho[warp], lane);
+        // ---- 2. QJL projections of the tile (K only): bit k = [(S rho)_k >= 0]
+        if (is_k) {
+            constexpr int KPT = D / (kWarps * 32);
+            float acc[KPT][kTile];
+#pragma unroll
+            for (int u = 0; u < KPT; ++u)
+#pragma unroll
+                for (int t = 0; t < kTile; ++t) acc[u][t] = 0.f;
+            if (SM::kResident) {
+                cp_async_wait_all();
+                __syncthreads();
+                project_rows<D, kTile, kWarps * 32>(sST, 0, D, s_rho, acc);
+            } else {
+                __syncthreads();
+                project_streamed<D, kTile, kWarps * 32>(gST, sST, s_rho, acc);
+            }
+#pragma unroll
+            for (int u = 0; u < KPT; ++u)
+#pragma unroll
+                for (int t = 0; t < kTile; ++t) s_sgn[t][threadIdx.x + 128 * u] = acc[u][t] >= 0.f ? 1 : 0;
+            __syncthreads();
+        }
+        // ---- 3. pack and store
+#pragma unroll
+        for (int j = 0; j < kPerWarp; ++j) {
+            if (slot[j] < 0) continue;                     // warp-uniform
+            const int tv = warp + kWarps * j;
+            const int head = (int)((v0 + tv) % map.n_heads);
+            const int64_t blk = slot[j] / kBlock;
+            const int off = (int)(slot[j] % kBlock);
+            if (is_k) {
+                uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * k_record(D);
+                uint32_t *planes = reinterpret_cast<uint32_t *>(rec);
+                constexpr int NW = D / 128;
+                const int gid = off & 7, th = off >> 3;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t w0 = __ballot_sync(0xffffffffu, code[j][r] & 1);
+                    const uint32_t w1 = __ballot_sync(0xffffffffu, (code[j][r] >> 1) & 1);
+                    const uint32_t w2 = __ballot_sync(0xffffffffu, (code[j][r] >> 2) & 1);
+                    const uint32_t ws = __ballot_sync(0xffffffffu, s_sgn[tv][kdim<D>(lane, r)]);
+                    if (lane == r) {
+                        const int L = 4 * gid + (r & 3);
+                        const size_t word = (size_t)(L * 2 + th) * NW + (r >> 2);
+                        constexpr size_t PW = 2 * D / 4;   // words per plane
+                        planes[word] = w0;
+                        planes[PW + word] = w1;
+                        planes[2 * PW + word] = w2;
+                        planes[3 * PW + word] = ws;
+                    }
+                }
+                if (lane == 0)
+                    *reinterpret_cast<__half2 *>(rec + 8 * D + 4 * off) =
+                        __halves2half2(__float2half_rn(nrm[j]), __float2half_rn(gam[j]));
+            } else {
+                uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * v_record(D);
+                constexpr int NWV = D / 64, NM = D / 128;
+                const int tigv = (off & 7) >> 1, jb = (off >> 3) + 2 * (off & 1);   // lane tig, byte in word
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t w0 = __ballot_sync(0xffffffffu, code[j][r] & 1);
+                    const uint32_t w1 = __ballot_sync(0xffffffffu, (code[j][r] >> 1) & 1);
+                    const uint32_t w2 = __ballot_sync(0xffffffffu, (code[j][r] >> 2) & 1);
+                    if ((lane >> 2) == r) {
+                        const int beta = lane & 3, tau = 4 * r + beta;
+                        const int mhi = tau % NM, rh = (tau / NM) & 1, gid = tau / (2 * NM);
+                        const size_t byte = ((size_t)(4 * gid + tigv) * NWV + 2 * mhi + rh) * 4 + jb;
+                        rec[byte] = (uint8_t)(w0 >> (8 * beta));
+                        rec[2 * D + byte] = (uint8_t)(w1 >> (8 * beta));
+                        rec[4 * D + byte] = (uint8_t)(w2 >> (8 * beta));
+                    }
+                }
+                if (lane == 0) *reinterpret_cast<__half *>(rec + 6 * D + 2 * off) = __float2half_rn(nrm[j]);
+            }
+        }
+        __syncthreads();   // s_rho / s_sgn are rewritten by the next tile
     }
 }
 
-// Paged append: item = (sequence, head, K or V); one warp per item.
-template <int D, typename T>
-__global__ void __launch_bounds__(kWarps * 32)
-append_kernel(const uint8_t *__restrict__ params, const T *__restrict__ k_new, const T *__restrict__ v_new,
-              int batch, int n_heads, const int32_t *__restrict__ block_table, int max_blocks,
-              const int32_t *__restrict__ ctx_lens, uint8_t *__restrict__ k_pool, uint8_t *__restrict__ v_pool,
-              int64_t num_blocks, int32_t *status) {
-    __shared__ EncodeSmem sm;
-    __shared__ __align__(16) float rho[kWarps][D];
-    if (!params_ok(params, D)) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
-        return;
-    }
-    load_codebook(params, sm);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t items = (int64_t)batch * n_heads * 2;
-    for (int64_t it = (int64_t)blockIdx.x * kWarps + warp; it < items; it += (int64_t)gridDim.x * kWarps) {
-        const bool is_k = (it & 1) == 0;
-        const int64_t bh = it >> 1;
-        const int b = (int)(bh / n_heads), head = (int)(bh % n_heads);
-        const int L = ctx_lens[b];
-        if (L < 0) continue;
-        const int lb = L / kBlock;
-        int64_t blk = -1;
-        if (lb < max_blocks) blk = block_table[(size_t)b * max_blocks + lb];
-        if (blk < 0 || blk >= num_blocks) {
-            if (lane == 0 && is_k) flag_status(status, TQ_STATUS_BAD_SLOT);
-            continue;
-        }
-        const int64_t slot = blk * kBlock + (L % kBlock);
-        if (is_k)
-            encode_vector<D, true, T>(params, sm, k_new + bh * D, slot, head, n_heads, k_pool, rho[warp], lane);
-        else
-            encode_vector<D, false, T>(params, sm, v_new + bh * D, slot, head, n_heads, v_pool, rho[warp], lane);
-    }
+template <int D, int TILE, typename T>
+cudaError_t launch_enc(const void *params, const void *xk, const void *xv, int64_t n_vec, const SlotMap &map,
+                       void *kp, void *vp, int kinds, int32_t *status, cudaStream_t st) {
+    const int64_t ntiles = (n_vec + TILE - 1) / TILE;
+    if (ntiles <= 0) return cudaSuccess;
+    const int ny = (kinds == 3) ? 2 : 1;
+    const int64_t cap = 152 * 2;               // persistent: two CTAs per SM
+    const unsigned gx = (unsigned)(ntiles < cap ? ntiles : cap);
+    constexpr size_t smem = EncSmem<D, TILE>::kBytes;
+    auto kern = encode_kernel<D, TILE, T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(gx, ny), kWarps * 32, smem, st>>>((const uint8_t *)params, (const T *)xk, (const T *)xv, n_vec, map,
+                                                  (uint8_t *)kp, (uint8_t *)vp, kinds, status);
+    return cudaGetLastError();
 }
 
-int grid_for(int64_t items) {
-    int64_t g = (items + kWarps - 1) / kWarps;
-    const int64_t cap = 152 * 16;
-    if (g > cap) g = cap;
-    if (g < 1) g = 1;
-    return (int)g;
+template <int TILE>
+cudaError_t launch_any(int d, int dtype, const void *params, const void *xk, const void *xv, int64_t n_vec,
+                       const SlotMap &map, void *kp, void *vp, int kinds, int32_t *status, cudaStream_t st) {
+    if (d == 128)
+        return dtype == TQ_DTYPE_BF16
+                   ? launch_enc<128, TILE, __nv_bfloat16>(params, xk, xv, n_vec, map, kp, vp, kinds, status, st)
+                   : launch_enc<128, TILE, float>(params, xk, xv, n_vec, map, kp, vp, kinds, status, st);
+    return dtype == TQ_DTYPE_BF16
+               ? launch_enc<256, TILE, __nv_bfloat16>(params, xk, xv, n_vec, map, kp, vp, kinds, status, st)
+               : launch_enc<256, TILE, float>(params, xk, xv, n_vec, map, kp, vp, kinds, status, st);
 }
 
 }  // namespace
 
-// ---------------------------------------------------------------- launchers
-
-template <int D, bool IS_K, typename T>
-static cudaError_t launch_encode_t(const void *params, const void *x, int64_t n_tokens, int n_heads,
-                                   const int64_t *slots, void *pool, int64_t num_blocks, int32_t *status,
-                                   cudaStream_t st) {
-    encode_kernel<D, IS_K, T><<<grid_for(n_tokens * n_heads), kWarps * 32, 0, st>>>(
-        (const uint8_t *)params, (const T *)x, n_tokens, n_heads, slots, (uint8_t *)pool, num_blocks, status);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const void *x, int64_t n_tokens,
                           int n_heads, const int64_t *slots, void *pool, int64_t num_blocks, int32_t *status,
                           cudaStream_t st) {
-#define TQ_ENC(DD, K, TT) return launch_encode_t<DD, K, TT>(params, x, n_tokens, n_heads, slots, pool, num_blocks, status, st)
-    if (d == 128) {
-        if (is_k) { if (dtype == TQ_DTYPE_BF16) TQ_ENC(128, true, __nv_bfloat16); TQ_ENC(128, true, float); }
-        if (dtype == TQ_DTYPE_BF16) TQ_ENC(128, false, __nv_bfloat16);
-        TQ_ENC(128, false, float);
-    }
-    if (is_k) { if (dtype == TQ_DTYPE_BF16) TQ_ENC(256, true, __nv_bfloat16); TQ_ENC(256, true, float); }
-    if (dtype == TQ_DTYPE_BF16) TQ_ENC(256, false, __nv_bfloat16);
-    TQ_ENC(256, false, float);
-#undef TQ_ENC
+    SlotMap map{slots, nullptr, nullptr, 0, num_blocks, n_heads};
+    return launch_any<16>(d, dtype, params, is_k ? x : nullptr, is_k ? nullptr : x, n_tokens * n_heads, map,
+                          is_k ? pool : nullptr, is_k ? nullptr : pool, is_k ? 1 : 2, status, st);
 }
 
-template <int D, typename T>
-static cudaError_t launch_append_t(const void *params, const void *k_new, const void *v_new, int batch,
-                                   int n_heads, const int32_t *bt, int max_blocks, const int32_t *ctx,
-                                   void *kp, void *vp, int64_t num_blocks, int32_t *status, cudaStream_t st) {
-    append_kernel<D, T><<<grid_for((int64_t)batch * n_heads * 2), kWarps * 32, 0, st>>>(
-        (const uint8_t *)params, (const T *)k_new, (const T *)v_new, batch, n_heads, bt, max_blocks, ctx,
-        (uint8_t *)kp, (uint8_t *)vp, num_blocks, status);
-    return cudaGetLastError();
-}
-
+// One new token per sequence, K and V in one launch.
 cudaError_t launch_append(int d, int dtype, const void *params, const void *k_new, const void *v_new, int batch,
                           int n_heads, const int32_t *bt, int max_blocks, const int32_t *ctx, void *kp, void *vp,
                           int64_t num_blocks, int32_t *status, cudaStream_t st) {
-#define TQ_APP(DD, TT) return launch_append_t<DD, TT>(params, k_new, v_new, batch, n_heads, bt, max_blocks, ctx, kp, vp, num_blocks, status, st)
-    if (d == 128) { if (dtype == TQ_DTYPE_BF16) TQ_APP(128, __nv_bfloat16); TQ_APP(128, float); }
-    if (dtype == TQ_DTYPE_BF16) TQ_APP(256, __nv_bfloat16);
-    TQ_APP(256, float);
-#undef TQ_APP
+    SlotMap map{nullptr, bt, ctx, max_blocks, num_blocks, n_heads};
+    return launch_any<4>(d, dtype, params, k_new, v_new, (int64_t)batch * n_heads, map, kp, vp, 3, status, st);
 }
 
 }  // namespace tq

@@ -28,7 +28,7 @@ namespace tq {
 constexpr uint32_t kParamsMagic = 0x31505154u;   // "TQP1"
 constexpr int kBlock = 16;
 
-// Device params header (256 bytes); D signs and S follow.
+// Device params header (256 bytes); D signs, S and S^T follow.
 struct ParamsHeader {
     uint32_t magic;
     int32_t d;
@@ -36,13 +36,16 @@ struct ParamsHeader {
     float centroid[8];     // ascending, unit variance
     float threshold[8];    // 7 used: midpoints of neighbouring centroids
     double centroid64[8];  // the same centroids before rounding to fp32
-    float pad[28];
+    uint32_t one16x2;      // 0x3C003C00: f16x2 {1, 1}, operand base of the decode kernels
+    float pad[27];
 };
 static_assert(sizeof(ParamsHeader) == 256, "params header must be 256 bytes");
 
+// Device params: header, D signs (fp32 +-1), S row-major, S transposed.
 __host__ __device__ constexpr size_t params_off_D(int /*d*/) { return 256; }
 __host__ __device__ constexpr size_t params_off_S(int d) { return 256 + 4 * (size_t)d; }
-__host__ __device__ constexpr size_t params_total(int d) { return params_off_S(d) + 4 * (size_t)d * d; }
+__host__ __device__ constexpr size_t params_off_ST(int d) { return params_off_S(d) + 4 * (size_t)d * d; }
+__host__ __device__ constexpr size_t params_total(int d) { return params_off_ST(d) + 4 * (size_t)d * d; }
 
 __host__ __device__ constexpr size_t k_record(int d) { return 8 * (size_t)d + 4 * kBlock; }
 __host__ __device__ constexpr size_t v_record(int d) { return 6 * (size_t)d + 2 * kBlock; }
@@ -115,6 +118,77 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 __device__ __forceinline__ void flag_status(int32_t *status, int bits) {
     if (status) atomicOr(status, bits);
+}
+
+// ---------------------------------------------------------------- async copies
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+    const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// ---------------------------------------------------------------- projections by S
+// out[v][k] = sum_i S[k][i] x[v][i] for NV vectors x[v][*] in shared memory,
+// thread t of NT computing rows k = t + NT*u.  S^T (row i = column i of S)
+// is read from shared memory: either all of it (resident, d*d floats) or in
+// double-buffered chunks of kProjRows rows copied from global memory.
+constexpr int kProjRows = 32;
+
+template <int D, int NV, int NT>
+__device__ __forceinline__ void project_rows(const float *sST_rows, int i0, int nrows, const float (*x)[D],
+                                             float (&acc)[D / NT][NV]) {
+    constexpr int KPT = D / NT;
+    for (int i = 0; i < nrows; i += 4) {
+        float sv[KPT][4];
+#pragma unroll
+        for (int u = 0; u < KPT; ++u)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sv[u][c] = sST_rows[(size_t)(i + c) * D + threadIdx.x + NT * u];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const float4 xv = *reinterpret_cast<const float4 *>(&x[v][i0 + i]);
+#pragma unroll
+            for (int u = 0; u < KPT; ++u) {
+                acc[u][v] = fmaf(sv[u][0], xv.x, acc[u][v]);
+                acc[u][v] = fmaf(sv[u][1], xv.y, acc[u][v]);
+                acc[u][v] = fmaf(sv[u][2], xv.z, acc[u][v]);
+                acc[u][v] = fmaf(sv[u][3], xv.w, acc[u][v]);
+            }
+        }
+    }
+}
+
+// Copy rows [i0, i0 + n) of S^T from global to shared memory (one commit group).
+template <int D, int NT>
+__device__ __forceinline__ void stage_st_rows(float *dst, const float *gST, int i0, int n) {
+    const int chunks = n * D / 4;            // 16-byte pieces
+    const float *src = gST + (size_t)i0 * D;
+    for (int c = threadIdx.x; c < chunks; c += NT) cp_async16(dst + 4 * c, src + 4 * c);
+    cp_async_commit();
+}
+
+// Streamed projection: S^T passes through sbuf (2 x kProjRows x D floats).
+// Every thread of the CTA must call it (it synchronises the CTA).
+template <int D, int NV, int NT>
+__device__ __forceinline__ void project_streamed(const float *gST, float *sbuf, const float (*x)[D],
+                                                 float (&acc)[D / NT][NV]) {
+    constexpr int NCHUNK = D / kProjRows;
+    stage_st_rows<D, NT>(sbuf, gST, 0, kProjRows);
+#pragma unroll 1
+    for (int c = 0; c < NCHUNK; ++c) {
+        if (c + 1 < NCHUNK) {
+            stage_st_rows<D, NT>(sbuf + (size_t)((c + 1) & 1) * kProjRows * D, gST, (c + 1) * kProjRows, kProjRows);
+            cp_async_wait_1();
+        } else {
+            cp_async_wait_all();
+        }
+        __syncthreads();
+        project_rows<D, NV, NT>(sbuf + (size_t)(c & 1) * kProjRows * D, c * kProjRows, kProjRows, x, acc);
+        __syncthreads();
+    }
 }
 
 }  // namespace tq

@@ -4,7 +4,7 @@
 // to provide one: a serving runtime that hands all free HBM to its KV pool at
 // start-up and forbids allocations afterwards, or a decode loop that may not
 // call cudaMalloc because that call can synchronise the whole device.  For
-// them, tq_decode_attn_noalloc runs the same three kernels with their scratch
+// them, tq_decode_attn_noalloc runs the same kernels with their scratch
 // in a fixed array compiled into this library (kNoallocScratchBytes per GPU,
 // held by every GPU that loads the library until the process exits).
 #include <mutex>
@@ -14,11 +14,10 @@
 namespace tq {
 cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv, int max_ctx,
                          void *ws, cudaStream_t st);
-cudaError_t launch_partial(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
-                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
-                           const int32_t *ctx_lens, int max_ctx, void *ws, int32_t *status, cudaStream_t st);
-cudaError_t launch_merge(int d, const void *params, int batch, int hq, int hkv, const int32_t *ctx_lens, int max_ctx,
-                         float *out, void *ws, cudaStream_t st);
+cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
+                          const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
+                          const int32_t *ctx_lens, int max_ctx, float *out, void *ws, int32_t *status,
+                          cudaStream_t st);
 size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx);
 
 namespace {
@@ -79,12 +78,12 @@ extern "C" int tq_decode_attn_noalloc(const void *params, int d, const void *q, 
     cudaError_t e = scratch_for_current_device(&ws);
     if (e != cudaSuccess) return TQ_ERR_CUDA;
     // Every scratch value the kernels read is written earlier in this same
-    // call, so the contents left by a previous call need no clearing.
+    // call (the query-prep kernel also resets the split counters), so the
+    // contents left by a previous call need no clearing.
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     e = launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, max_ctx, ws, st);
     if (e == cudaSuccess)
-        e = launch_partial(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
-                           max_blocks, ctx_lens, max_ctx, ws, status, st);
-    if (e == cudaSuccess) e = launch_merge(d, params, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx, out, ws, st);
+        e = launch_splitk(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
+                          max_blocks, ctx_lens, max_ctx, out, ws, status, st);
     return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }
