@@ -37,7 +37,7 @@ METRIC = "decode-attn compressed-KV GB/s & % of GB300 HBM peak; encode Mtok/s vs
 WORKLOAD = "llama8b_decode"
 L2_BYTES = 129 * 1024 * 1024
 DECODE_SRC = os.path.join(ROOT, "turboquant_compressed_kv_gb300", "csrc", "tq_decode.cu")
-PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_splitk_llama8b_decode.json")
+PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_splitk_llama8b_decode_traffic.txt")
 
 
 def parse():

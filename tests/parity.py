@@ -8,7 +8,8 @@ Tolerances (written here once, used by every parity test):
     the expected rate is about 4e-6 per entry, so a small test (under 400K
     entries, where 1e-5 of them is below 4) allows up to 4 as a Poisson floor;
   * fp16 norms: within 1 ulp;
-  * attention output, computed by the oracle from the GPU's own packed cache:
+  * attention output, with the oracle and the GPU both decoding the same
+    packed cache (written by the oracle and uploaded to the device):
     per (sequence, query head) max|o_gpu - o_ref| <= 2e-3 and
     ||o_gpu - o_ref||_2 / ||o_ref||_2 <= 1e-3.
 """
