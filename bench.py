@@ -290,7 +290,7 @@ def bench_tq(args):
     def step(i, ev=None):
         kp, vp = pools[i % nrep]
         tq.paged_append(cache.params, d, k_new, v_new, cache.block_table, pre, kp, vp, status=status)
-        tq.decode_qprep(cache.params, d, q, Hkv, max_ctx, ws)
+        tq.decode_qprep(cache.params, d, q, Hkv, ctx, max_ctx, ws)
         if ev is not None:
             ev[0].record(stream)
         tq.decode_splitk(cache.params, d, B, Hq, Hkv, kp, vp, cache.block_table, ctx, max_ctx, out, ws,

@@ -130,7 +130,8 @@ int tq_paged_append(const void *params, int d, const void *k_new, const void *v_
                     const int32_t *ctx_lens, void *k_pool, void *v_pool, int64_t num_blocks,
                     int32_t *status, tq_stream_t stream);
 
-/* Workspace bytes tq_decode_attn needs for this shape (0 for invalid sizes). */
+/* Workspace bytes tq_decode_attn needs for this shape (0 for invalid sizes).
+ * It depends on d, batch and n_q_heads only (max_ctx is checked, not used). */
 size_t tq_decode_workspace_bytes(int d, int batch, int n_q_heads, int max_ctx);
 
 /* tq_decode_attn -- one decode step of attention over the compressed paged cache.
@@ -146,7 +147,7 @@ size_t tq_decode_workspace_bytes(int d, int batch, int n_q_heads, int max_ctx);
  *   q          device [batch][n_q_heads][d] in dtype.
  *   ctx_lens   device int32[batch]; each must be <= max_ctx (larger values are
  *              clamped to max_ctx); 0 gives out = 0.
- *   max_ctx    host upper bound of ctx_lens, sizes the context split.
+ *   max_ctx    host upper bound of ctx_lens (larger lengths are clamped to it).
  *   out        device float[batch][n_q_heads][d].
  *   workspace  device scratch of >= tq_decode_workspace_bytes(...) bytes.
  * n_q_heads/n_kv_heads must be 1..8.  Errors: TQ_ERR_INVALID, TQ_ERR_HEAD_DIM,
@@ -159,19 +160,24 @@ int tq_decode_attn(const void *params, int d, const void *q, int dtype, int batc
 
 /* The two stages of tq_decode_attn as separate calls, for callers that
  * schedule or time them individually.  Called in this order on one stream with
- * the same shape arguments and workspace, they compute exactly what
- * tq_decode_attn computes; argument meanings and errors are as there.
+ * the same shape arguments, ctx_lens contents and workspace, they compute
+ * exactly what tq_decode_attn computes; argument meanings and errors are as
+ * there.
  *   tq_decode_qprep   qbar = Pi q and u = S qbar for every (sequence, query head),
- *                     written to the workspace as tensor-core operands.
- *   tq_decode_splitk  the pass over the cache: per (sequence, kv head, context
- *                     split) the online-softmax state (max score, sum of weights,
- *                     weighted value sum in the rotated domain) of every query
- *                     head of the group; the last split of each (sequence, kv
- *                     head) to finish combines the splits and writes
- *                     out = Pi^T a for the group's query heads. */
+ *                     written to the workspace as tensor-core operands, and the
+ *                     work schedule of the pass (read from ctx_lens).
+ *   tq_decode_splitk  the pass over the cache.  The context of each (sequence,
+ *                     kv head) is cut into chunks of 128 tokens (256 when
+ *                     n_q_heads/n_kv_heads > 4); the chunks of all (sequence,
+ *                     kv head) pairs, in that order, are shared out in equal
+ *                     contiguous ranges among a fixed set of resident CTAs.  A
+ *                     pair whose chunks span several CTAs is combined by the
+ *                     last of them from per-CTA online-softmax states; each pair
+ *                     writes out = Pi^T a for its query heads.
+ * ctx_lens must not change between the two calls. */
 int tq_decode_qprep(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads,
-                    int n_kv_heads, int max_ctx, void *workspace, size_t workspace_bytes,
-                    tq_stream_t stream);
+                    int n_kv_heads, const int32_t *ctx_lens, int max_ctx, void *workspace,
+                    size_t workspace_bytes, tq_stream_t stream);
 int tq_decode_splitk(const void *params, int d, int batch, int n_q_heads, int n_kv_heads,
                      const void *k_pool, const void *v_pool, int64_t num_blocks,
                      const int32_t *block_table, int max_blocks, const int32_t *ctx_lens,
@@ -189,7 +195,7 @@ int tq_decode_splitk(const void *params, int d, int batch, int n_q_heads, int n_
  * (16 MiB) compiled into the library; every GPU that loads the library keeps
  * it until the process exits.  A shape whose tq_decode_workspace_bytes()
  * exceeds it is rejected with TQ_ERR_WORKSPACE (16 x 32 query heads at
- * d = 128 and 4096 tokens needs about 2.7 MiB).  Nothing is allocated: no
+ * d = 128 need about 9.3 MiB; 64 x 32 need 21.7 MiB).  Nothing is allocated: no
  * cudaMalloc, cudaFree or allocating library call.
  * The scratch used is that of the device current at the call; the stream must
  * belong to it.  The first call made with a device current looks up the

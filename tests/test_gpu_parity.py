@@ -198,6 +198,46 @@ def test_decode_parity(d, Hq, Hkv, dtype):
     parity.check_attention(o, ref)
 
 
+@pytest.mark.parametrize("d,Hq,Hkv,lens", [
+    (128, 16, 4, [9000, 3000, 12000, 700, 5000, 1, 129, 128]),   # more chunks than resident CTAs
+    (128, 32, 4, [7000, 2500, 10000, 300, 4100, 17]),             # groups of 8: 256-token chunks
+    (256, 4, 2, [20000, 7000, 0, 33]),                            # d=256, long contexts
+])
+def test_decode_parity_many_chunks(d, Hq, Hkv, lens):
+    """Contexts long enough that CTAs cover several chunks of one (sequence,
+    kv head), several units, and units shared by many CTAs."""
+    D, S, params, bt, kp, vp = _build_cache(d, Hkv, lens, "bf16", seed=Hq + d + 7)
+    B = len(lens)
+    q = synth.round_dtype(np.random.default_rng(11).standard_normal((B, Hq, d)).astype(np.float32), "bf16")
+    ctx = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = tq.decode_attn(params, d, _upload(q, "bf16"), Hkv, torch.from_numpy(kp).to(DEV),
+                         torch.from_numpy(vp).to(DEV), torch.from_numpy(bt).to(DEV), ctx, max(lens), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.decode(D, S, q, Hkv, kp, vp, bt, np.array(lens, np.int32))
+    parity.check_attention(out.cpu().numpy(), ref)
+
+
+def test_decode_stages_equal_decode_attn():
+    """tq_decode_qprep then tq_decode_splitk give exactly tq_decode_attn's output."""
+    d, Hq, Hkv = 128, 8, 2
+    lens = [3000, 40, 0, 1500]
+    D, S, params, bt, kp, vp = _build_cache(d, Hkv, lens, "f32", seed=3)
+    B = len(lens)
+    q = _upload(np.random.default_rng(5).standard_normal((B, Hq, d)).astype(np.float32), "f32")
+    kp, vp, bt = torch.from_numpy(kp).to(DEV), torch.from_numpy(vp).to(DEV), torch.from_numpy(bt).to(DEV)
+    ctx = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    want = tq.decode_attn(params, d, q, Hkv, kp, vp, bt, ctx, max(lens))
+    ws = torch.empty(tq.decode_workspace_bytes(d, B, Hq, max(lens)), dtype=torch.uint8, device=DEV)
+    got = torch.full((B, Hq, d), float("nan"), device=DEV)
+    for _ in range(2):   # the second round reuses counters and schedule left by the first
+        tq.decode_qprep(params, d, q, Hkv, ctx, max(lens), ws)
+        tq.decode_splitk(params, d, B, Hq, Hkv, kp, vp, bt, ctx, max(lens), got, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(got, want)
+
+
 def test_tiny_workload_end_to_end():
     """1 sequence, 1 head, d=128, 256 fp32 tokens with 20x outlier channels:
     GPU encode vs oracle encode, then GPU decode vs oracle decode of the

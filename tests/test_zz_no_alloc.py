@@ -62,11 +62,12 @@ def test_noalloc_matches_workspace_decode_on_two_calls(d, Hq, Hkv):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
-    d, Hq, Hkv = 128, 32, 8
-    params, bt, kp, vp = _cache(d, Hkv, [16], seed=5)
-    big_ctx = 1 << 20       # the workspace for this bound exceeds the fixed scratch
-    assert tq.decode_workspace_bytes(d, 1, Hq, big_ctx) > 16 << 20
-    q = torch.zeros((1, Hq, d), device=DEV)
-    ctx = torch.tensor([16], dtype=torch.int32, device=DEV)
+    d, Hq, Hkv, B = 128, 32, 8, 64
+    params, bt1, kp, vp = _cache(d, Hkv, [16], seed=5)
+    # the query packs of 64 x 32 heads alone exceed the fixed scratch
+    assert tq.decode_workspace_bytes(d, B, Hq, 16) > 16 << 20
+    bt = bt1[:1].repeat(B, 1)
+    q = torch.zeros((B, Hq, d), device=DEV)
+    ctx = torch.full((B,), 16, dtype=torch.int32, device=DEV)
     with pytest.raises(tq.TQError, match="workspace"):
-        tq.decode_attn_noalloc(params, d, q, Hkv, kp, vp, bt, ctx, big_ctx)
+        tq.decode_attn_noalloc(params, d, q, Hkv, kp, vp, bt, ctx, 16)

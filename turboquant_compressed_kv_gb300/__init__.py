@@ -75,7 +75,7 @@ def _declare(L):
     L.tq_decode_attn.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _SZ,
                                  _P, _P]
     L.tq_decode_qprep.restype = _I
-    L.tq_decode_qprep.argtypes = [_P, _I, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]
+    L.tq_decode_qprep.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _I, _P, _SZ, _P]
     L.tq_decode_splitk.restype = _I
     L.tq_decode_splitk.argtypes = [_P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _SZ, _P, _P]
     L.tq_decode_attn_noalloc.restype = _I
@@ -220,12 +220,13 @@ def decode_attn(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table,
 
 # ---------------------------------------------------------------- decode stages
 
-def decode_qprep(params, d: int, q, n_kv_heads: int, max_ctx: int, workspace, stream=None):
-    """tq_decode_qprep: qbar = Pi q, u = S qbar into the workspace."""
-    _need_cuda(params, q, workspace)
+def decode_qprep(params, d: int, q, n_kv_heads: int, ctx_lens, max_ctx: int, workspace, stream=None):
+    """tq_decode_qprep: qbar = Pi q, u = S qbar and the pass's work schedule into the workspace."""
+    _need_cuda(params, q, ctx_lens, workspace)
     B, Hq = q.shape[0], q.shape[1]
-    rc = load_library().tq_decode_qprep(_ptr(params), d, _ptr(q), _dtype_code(q), B, Hq, n_kv_heads, max_ctx,
-                                        _ptr(workspace), workspace.numel(), _stream(stream))
+    rc = load_library().tq_decode_qprep(_ptr(params), d, _ptr(q), _dtype_code(q), B, Hq, n_kv_heads,
+                                        _ptr(ctx_lens), max_ctx, _ptr(workspace), workspace.numel(),
+                                        _stream(stream))
     _check(rc, "tq_decode_qprep")
 
 

@@ -5,20 +5,6 @@
 #include "tq_internal.cuh"
 
 namespace tq {
-cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const void *x, int64_t n_tokens,
-                          int n_heads, const int64_t *slots, void *pool, int64_t num_blocks, int32_t *status,
-                          cudaStream_t st);
-cudaError_t launch_append(int d, int dtype, const void *params, const void *k_new, const void *v_new, int batch,
-                          int n_heads, const int32_t *bt, int max_blocks, const int32_t *ctx, void *kp, void *vp,
-                          int64_t num_blocks, int32_t *status, cudaStream_t st);
-cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv, int max_ctx,
-                         void *ws, cudaStream_t st);
-cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
-                          const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
-                          const int32_t *ctx_lens, int max_ctx, float *out, void *ws, int32_t *status,
-                          cudaStream_t st);
-size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx);
-
 namespace {
 
 // Lloyd-Max fixed point for the unit Gaussian with 8 levels, in fp64 on the
@@ -194,13 +180,15 @@ static int check_decode(const void *params, int d, int batch, int hq, int hkv, i
 }
 
 int tq_decode_qprep(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads, int n_kv_heads,
-                    int max_ctx, void *workspace, size_t workspace_bytes, tq_stream_t stream) {
+                    const int32_t *ctx_lens, int max_ctx, void *workspace, size_t workspace_bytes,
+                    tq_stream_t stream) {
     int rc = check_decode(params, d, batch, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
     if (rc != TQ_OK || batch == 0) return rc;
     if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16) return TQ_ERR_DTYPE;
     if (!q) return TQ_ERR_INVALID;
-    return cuda_status(launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, max_ctx, workspace,
-                                    reinterpret_cast<cudaStream_t>(stream)));
+    if (!ctx_lens) return TQ_ERR_INVALID;
+    return cuda_status(launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx,
+                                    workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int tq_decode_splitk(const void *params, int d, int batch, int n_q_heads, int n_kv_heads, const void *k_pool,
@@ -228,7 +216,7 @@ int tq_decode_attn(const void *params, int d, const void *q, int dtype, int batc
     if (!q || !k_pool || !v_pool || !block_table || !ctx_lens || !out) return TQ_ERR_INVALID;
     if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, max_ctx, workspace, st);
+    cudaError_t e = launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx, workspace, st);
     if (e == cudaSuccess)
         e = launch_splitk(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
                           max_blocks, ctx_lens, max_ctx, out, workspace, status, st);

@@ -25,17 +25,21 @@
 //    the tensor core accumulates in fp32.
 //
 // Two launches per call: (1) query prep (qbar, u, f16 operand fragments,
-// offset constants); (2) the split-K pass: an online-softmax partial (m, l,
-// acc[d]) per (seq, q head, split); the last split of each (seq, kv head) to
-// finish merges the partials and applies one inverse rotation per head.
-#include <cuda_fp8.h>
+// offset constants, and the work schedule of the pass); (2) the split-K pass,
+// persistent: the context of every (sequence, kv head) is cut into 128-token
+// chunks (256 for groups of more than 4 query heads), and CTA c of P takes
+// the c-th of P equal, contiguous ranges of the chunk sequence ordered by
+// (sequence, kv head, chunk) ("stream-K").  A (sequence, kv head) inside one
+// CTA's range is finished there; one shared by several CTAs leaves an
+// online-softmax partial (m, l, acc[d]) per query head from each, and the last
+// of them to finish merges the partials.  Either way one inverse rotation per
+// (sequence, query head) is applied at the end.
+#include <atomic>
 
 #include "tq_internal.cuh"
 
 namespace tq {
 
-constexpr int kMinSplit = 512;             // shortest context split (sizes the workspace)
-constexpr int kMaxSplit = 8192;
 __host__ __device__ constexpr int kPartStride(int d) { return d + 4; }   // m, l, pad, pad, acc[d]
 // Per (sequence, kv head) query pack: f16x2 B-operand fragments
 // [2 (qbar, u)][d/16 k-steps][2 n-tiles][32 lanes][2 words], then the offset
@@ -43,18 +47,60 @@ __host__ __device__ constexpr int kPartStride(int d) { return d + 4; }   // m, l
 __host__ __device__ constexpr size_t kPackBytes(int d) { return 64 * (size_t)d + 256; }
 __host__ __device__ constexpr int kPackFloatOff(int d) { return 16 * d; }   // in floats
 
-// Workspace: query packs [B*Hkv] | split counters [B*Hkv] | partials [B*Hq][nsplit][d+4].
-// Sized with Hq >= Hkv and the shortest split, so every layout below fits.
-__host__ __device__ constexpr size_t kCounterBytes(int batch, int hq) {
-    return ((size_t)batch * hq * 4 + 255) & ~(size_t)255;
+#ifndef TQ_SPLITK_BPW
+#define TQ_SPLITK_BPW 2          // blocks scored per warp per chunk
+#endif
+#ifndef TQ_SPLITK_MINBLOCKS
+#define TQ_SPLITK_MINBLOCKS 4    // resident CTAs per SM the register budget is sized for (4-warp CTAs)
+#endif
+constexpr int kCtasPerSm = 4;              // persistent CTAs per SM (at most)
+constexpr int kMaxSms = 160;               // SMs the pass uses at most (GB300 has 152); bounds the workspace
+
+// warps of the pass for a group of G query heads, and tokens per chunk
+__host__ __device__ constexpr int pass_warps(int G) { return G <= 4 ? 4 : 8; }
+__host__ __device__ constexpr int pass_chunk(int G) { return kBlock * pass_warps(G) * TQ_SPLITK_BPW; }
+
+__host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace: query packs [B*Hkv] | completion counters [B*Hkv] | chunk prefix
+// int64[B+1] | first sequence of each CTA int32[P] | partials [P][2][G][d+4].
+// Sized with Hq >= Hkv, G <= min(8, Hq) and P <= kCtasPerSm * kMaxSms.
+struct WsLayout {
+    uint8_t *packs;
+    unsigned int *counters;
+    int64_t *cpre;
+    int32_t *cta_b;
+    float *part;
+};
+__host__ __device__ inline size_t ws_sizes(int d, int batch, int hq, size_t *off) {
+    const int gmax = hq < 8 ? hq : 8;
+    const size_t pmax = (size_t)kCtasPerSm * kMaxSms;
+    off[0] = 0;
+    off[1] = off[0] + align256((size_t)batch * hq * kPackBytes(d));
+    off[2] = off[1] + align256((size_t)batch * hq * 4);
+    off[3] = off[2] + align256(((size_t)batch + 1) * 8);
+    off[4] = off[3] + align256(pmax * 4);
+    return off[4] + pmax * 2 * gmax * kPartStride(d) * sizeof(float);
 }
 size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx) {
     if (!valid_d(d) || batch <= 0 || hq <= 0 || max_ctx < 0) return 0;
-    const size_t nsplit = (size_t)((max_ctx + kMinSplit - 1) / kMinSplit);
-    const size_t pack = (size_t)batch * hq * kPackBytes(d);
-    const size_t part = (size_t)batch * hq * (nsplit ? nsplit : 1) * kPartStride(d) * sizeof(float);
-    return pack + kCounterBytes(batch, hq) + part;
+    size_t off[5];
+    return ws_sizes(d, batch, hq, off);
 }
+WsLayout ws_layout(void *ws, int d, int batch, int hq) {
+    size_t off[5];
+    ws_sizes(d, batch, hq, off);
+    uint8_t *base = reinterpret_cast<uint8_t *>(ws);
+    return WsLayout{base + off[0], reinterpret_cast<unsigned int *>(base + off[1]),
+                    reinterpret_cast<int64_t *>(base + off[2]), reinterpret_cast<int32_t *>(base + off[3]),
+                    reinterpret_cast<float *>(base + off[4])};
+}
+
+// Stream-K ranges: CTA c of P covers global chunks [sk_begin(c), sk_begin(c+1)).
+__host__ __device__ inline int64_t sk_begin(int c, int P, int64_t W) { return (int64_t)c * W / P; }
+// the CTA whose range holds chunk x (0 <= x < W)
+__device__ inline int sk_cta_of(int64_t x, int P, int64_t W) { return (int)(((x + 1) * P - 1) / W); }
+__device__ inline int clamp_len(int L, int max_ctx) { return L < 0 ? 0 : (L > max_ctx ? max_ctx : L); }
 
 namespace {
 
@@ -63,7 +109,6 @@ namespace {
 // Operand bit position q (8..15 within each f16 half): mask, base, and the
 // operand values alpha (bit clear) and alpha + delta (bit set).
 __host__ __device__ constexpr uint32_t op_mask(int q) { return 0x00010001u << q; }
-__host__ __device__ constexpr uint32_t op_base(int q) { return q == 14 ? 0u : 0x3C003C00u; }
 __host__ __device__ constexpr float op_alpha(int q) { return q == 14 ? 0.f : 1.f; }
 __host__ __device__ constexpr float op_delta(int q) {
     return q == 8 ? 0.25f : q == 9 ? 0.5f : q == 10 ? -0.5f : q == 11 ? -0.75f
@@ -114,38 +159,89 @@ __device__ __forceinline__ void walsh4(const float *cen, float (&A)[4]) {
 }
 
 // ---------------------------------------------------------------- (1) query prep
-// A CTA handles kQRows (sequence, query head) rows: each warp rotates its rows
-// (qbar = Pi q), then thread k computes u_k = (S qbar)_k for every row from
-// S^T (coalesced, each load shared by the rows), then each warp writes its
-// rows' hi and lo columns (2*hg, 2*hg+1) of the K-side B operand for qbar
-// (qu=0) and u (qu=1) into the pack of the row's (sequence, kv head), and the
-// offset constants.
-constexpr int kQRows = 8;
+// A CTA handles kQRows (sequence, query head) rows, one per warp: each warp
+// rotates its row (qbar = Pi q), then thread k computes u_k = (S qbar)_k for
+// every row from S^T staged in shared memory (all of it in one copy at d=128,
+// two 64-row chunks in flight at d=256), then each warp writes its row's hi
+// and lo columns (2*hg, 2*hg+1) of the K-side B operand for qbar (qu=0) and
+// u (qu=1) into the pack of the row's (sequence, kv head), and the offset
+// constants.  CTA 0 also lays out the pass's work (build_schedule).
+constexpr int kQRows = 4;
+template <int D> __host__ __device__ constexpr int qprep_st_rows() { return D == 128 ? 128 : 64; }
+template <int D> __host__ __device__ constexpr size_t qprep_smem() {
+    return (size_t)2 * kQRows * D * 4 + (size_t)(D / qprep_st_rows<D>() > 1 ? 2 : 1) * qprep_st_rows<D>() * D * 4;
+}
+
+// Chunk prefix over sequences (cpre[b] = first global chunk of sequence b's
+// first kv head, cpre[B] = W chunks in all) and the sequence holding the
+// first chunk of each of the P CTAs of the pass.  One CTA of 128 threads.
+__device__ void build_schedule(const int32_t *__restrict__ ctx_lens, int batch, int hkv, int max_ctx, int chunk,
+                               int P, int64_t *__restrict__ cpre, int32_t *__restrict__ cta_b) {
+    // P is the pass's grid size; with fewer chunks than CTAs only W CTAs get work
+    __shared__ int64_t s_wsum[4];
+    __shared__ int64_t s_carry;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        s_carry = 0;
+        cpre[0] = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < batch; base += 128) {
+        const int b = base + threadIdx.x;
+        int64_t x = 0;
+        if (b < batch) x = (int64_t)hkv * ((clamp_len(ctx_lens[b], max_ctx) + chunk - 1) / chunk);
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {      // inclusive warp scan
+            const int64_t y = __shfl_up_sync(0xffffffffu, x, m);
+            if (lane >= m) x += y;
+        }
+        if (lane == 31) s_wsum[warp] = x;
+        __syncthreads();
+        int64_t off = s_carry;
+        for (int w = 0; w < warp; ++w) off += s_wsum[w];
+        if (b < batch) cpre[b + 1] = off + x;
+        __syncthreads();                        // every thread has read s_carry and s_wsum
+        if (threadIdx.x == 127) s_carry = off + x;
+        __syncthreads();
+    }
+    const int64_t W = s_carry;
+    if (W < P) P = (int)W;                      // at least one chunk per CTA (the pass does the same)
+    for (int c = threadIdx.x; c < P; c += 128) {
+        const int64_t g0 = sk_begin(c, P, W);
+        int lo = 0, hi = batch - 1;             // first b with cpre[b+1] > g0
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (cpre[mid + 1] > g0) hi = mid;
+            else lo = mid + 1;
+        }
+        cta_b[c] = lo;
+    }
+}
 
 template <int D, int NTK, typename T>
 __global__ void __launch_bounds__(128)
 qprep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ q, int batch, int hq, int hkv,
-             uint8_t *__restrict__ packs, unsigned int *__restrict__ counters) {
+             const int32_t *__restrict__ ctx_lens, int max_ctx, int chunk, int P, uint8_t *__restrict__ packs,
+             unsigned int *__restrict__ counters, int64_t *__restrict__ cpre, int32_t *__restrict__ cta_b) {
     constexpr int R = D / 32, NKS = D / 16, KPT = D / 128;
     extern __shared__ __align__(16) uint8_t qsm[];
     float (*qs)[D] = reinterpret_cast<float (*)[D]>(qsm);                       // [kQRows][D] qbar
     float (*us)[D] = reinterpret_cast<float (*)[D]>(qsm + kQRows * D * 4);      // [kQRows][D] u
-    float *sbuf = reinterpret_cast<float *>(qsm + 2 * kQRows * D * 4);         // S^T chunks
+    float *sbuf = reinterpret_cast<float *>(qsm + 2 * kQRows * D * 4);         // S^T rows
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nrows = batch * hq, row0 = blockIdx.x * kQRows;
     const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
     const float *ST = reinterpret_cast<const float *>(params + params_off_ST(D));
     const float inv_sd = rsqrtf((float)D);
-#pragma unroll
-    for (int j = 0; j < kQRows / 4; ++j) {
-        const int rr = warp + 4 * j, row = row0 + rr;
+    {
+        const int row = row0 + warp;
         float v[R];
 #pragma unroll
         for (int r = 0; r < R; ++r)
             v[r] = (row < nrows) ? to_f32<T>(q[(size_t)row * D + 32 * r + lane]) * __ldg(Dsign + 32 * r + lane) : 0.f;
         fwht_warp<R>(v, lane);
 #pragma unroll
-        for (int r = 0; r < R; ++r) qs[rr][32 * r + lane] = v[r] * inv_sd;   // qbar = H D q / sqrt d
+        for (int r = 0; r < R; ++r) qs[warp][32 * r + lane] = v[r] * inv_sd;   // qbar = H D q / sqrt d
     }
     {
         float acc[KPT][kQRows];
@@ -153,38 +249,36 @@ qprep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ q, int ba
         for (int u = 0; u < KPT; ++u)
 #pragma unroll
             for (int rr = 0; rr < kQRows; ++rr) acc[u][rr] = 0.f;
-        project_streamed<D, kQRows, 128>(ST, sbuf, qs, acc);     // u = S qbar
+        project_streamed<D, kQRows, 128, qprep_st_rows<D>()>(ST, sbuf, qs, acc);     // u = S qbar
 #pragma unroll
         for (int u = 0; u < KPT; ++u)
 #pragma unroll
             for (int rr = 0; rr < kQRows; ++rr) us[rr][threadIdx.x + 128 * u] = acc[u][rr];
     }
     __syncthreads();
-#pragma unroll 1
-    for (int j = 0; j < kQRows / 4; ++j) {
-        const int rr = warp + 4 * j, row = row0 + rr;
-        if (row >= nrows) break;
+    const int row = row0 + warp;
+    if (row < nrows) {
         const int b = row / hq, h = row % hq, G = hq / hkv, kvh = h / G, hg = h % G;
-        if (hg == 0 && lane == 0) counters[b * hkv + kvh] = 0u;   // split-K completion counter
+        if (hg == 0 && lane == 0) counters[b * hkv + kvh] = 0u;   // completion counter of the pass
         float v[R], u[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            v[r] = qs[rr][32 * r + lane];
-            u[r] = us[rr][32 * r + lane];
+            v[r] = qs[warp][32 * r + lane];
+            u[r] = us[warp][32 * r + lane];
         }
         uint8_t *pack = packs + ((size_t)b * hkv + kvh) * kPackBytes(D);
         uint16_t *ph = reinterpret_cast<uint16_t *>(pack);
         float *pf = reinterpret_cast<float *>(pack) + kPackFloatOff(D);
 #pragma unroll
         for (int qu = 0; qu < 2; ++qu) {
-            double cs = 0.0;
+            float cs = 0.f;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int dim = 32 * r + lane, s = dim >> 4, k = dim & 15, qd = 8 + (s & 7);
                 const float beta = 2.f * (qu == 0 ? v[r] : u[r]) / op_delta(qd);
                 const __half hi = __float2half_rn(beta);
                 const __half lo = __float2half_rn(beta - __half2float(hi));
-                cs += ((double)__half2float(hi) + (double)__half2float(lo)) * (double)(op_alpha(qd) + 0.5f * op_delta(qd));
+                cs = fmaf(__half2float(hi) + __half2float(lo), op_alpha(qd) + 0.5f * op_delta(qd), cs);
                 const int reg = k >> 3, tig = (k & 7) >> 1, e = k & 1;
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
@@ -193,9 +287,8 @@ qprep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ q, int ba
                     ph[word * 2 + e] = __half_as_ushort(x == 0 ? hi : lo);
                 }
             }
-#pragma unroll
-            for (int m = 16; m > 0; m >>= 1) cs += __shfl_xor_sync(0xffffffffu, cs, m);
-            if (lane == 0) pf[qu * 8 + hg] = (float)cs;
+            cs = warp_sum(cs);
+            if (lane == 0) pf[qu * 8 + hg] = cs;
         }
         // columns beyond the group's 2*G are zero (written by the group's first head)
         if (hg == 0) {
@@ -209,15 +302,17 @@ qprep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ q, int ba
             }
         }
     }
+    if (blockIdx.x == 0) build_schedule(ctx_lens, batch, hkv, max_ctx, chunk, P, cpre, cta_b);
 }
 
 // ---------------------------------------------------------------- (2) split-K pass
-// grid (splits, Hkv, B), NWARP warps (4 for G <= 4, else 8).  The records of
-// a chunk of 32*NWARP tokens (2 blocks per warp) are staged in shared memory
-// by cp.async one chunk ahead.  Per chunk: warp w scores blocks 2w, 2w+1
-// against all G heads (K side); the warps run the online softmax (warp w owns
-// heads w, w+NWARP); warp w accumulates values for its D/NWARP coordinates
-// over the whole chunk (V side).
+// grid P (persistent), NWARP warps (4 for G <= 4, else 8).  A CTA walks its
+// range of chunks one (sequence, kv head) segment at a time.  The records of a
+// chunk of 32*NWARP tokens (2 blocks per warp) are staged in shared memory by
+// cp.async one chunk ahead.  Per chunk: warp w scores blocks 2w, 2w+1 against
+// all G heads (K side); the warps run the online softmax (warp w owns heads
+// w, w+NWARP); warp w accumulates values for its D/NWARP coordinates over the
+// whole chunk (V side).
 
 // physical block of logical block lb, or -1 (past the table or outside the pool)
 __device__ __forceinline__ int64_t block_of(const int32_t *__restrict__ bt, int b, int max_blocks, int lb,
@@ -226,14 +321,6 @@ __device__ __forceinline__ int64_t block_of(const int32_t *__restrict__ bt, int 
     const int64_t p = bt[(size_t)b * max_blocks + lb];
     return (p >= 0 && p < num_blocks) ? p : -1;
 }
-
-
-#ifndef TQ_SPLITK_BPW
-#define TQ_SPLITK_BPW 2          // blocks scored per warp per chunk
-#endif
-#ifndef TQ_SPLITK_MINBLOCKS
-#define TQ_SPLITK_MINBLOCKS 4    // resident CTAs per SM the register budget is sized for (4-warp CTAs)
-#endif
 
 template <int D, int NWARP>
 struct SplitCfg {
@@ -252,13 +339,29 @@ constexpr size_t split_smem_bytes() {
     return C::kBytes + C::vBytes + (size_t)8 * (C::CH + 8) * 2 + (size_t)C::CH * G * 4;
 }
 
+// out[row] = Pi^T (v / l): D (H v) / (l sqrt d), v spread over the warp as v[r] at lane
+template <int D>
+__device__ __forceinline__ void finish_row(float (&v)[D / 32], float l, const uint8_t *params, float *out_row,
+                                           int lane) {
+    constexpr int R = D / 32;
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) v[r] *= inv;
+    fwht_warp<R>(v, lane);
+    const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
+    const float inv_sd = rsqrtf((float)D);
+#pragma unroll
+    for (int r = 0; r < R; ++r) out_row[32 * r + lane] = v[r] * inv_sd * __ldg(Dsign + 32 * r + lane);
+}
+
 template <int D, int G, int NWARP>
-__global__ void __launch_bounds__(NWARP * 32, (NWARP == 4 ? TQ_SPLITK_MINBLOCKS : 1))
-decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ packs, int hq, int hkv,
+__global__ void __launch_bounds__(NWARP * 32, (NWARP == 4 ? (D == 128 ? TQ_SPLITK_MINBLOCKS : 3) : 1))
+decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ packs, int batch, int hq, int hkv,
                   const uint8_t *__restrict__ k_pool, const uint8_t *__restrict__ v_pool, int64_t num_blocks,
                   const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_lens,
-                  int max_ctx, int split, float *__restrict__ part, int nsplit, unsigned int *__restrict__ counters,
-                  float *__restrict__ out, int32_t *status) {
+                  int max_ctx, const int64_t *__restrict__ cpre, const int32_t *__restrict__ cta_b,
+                  float *__restrict__ part, unsigned int *__restrict__ counters, float *__restrict__ out,
+                  int32_t *status) {
     using C = SplitCfg<D, NWARP>;
     constexpr int NT_ = C::NT, BPW = C::BPW, BPC = C::BPC, CH = C::CH;
     constexpr int TPL = CH / 32;               // softmax tokens per lane
@@ -269,50 +372,33 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
     constexpr int KREC = C::KREC, VREC = C::VREC;
     constexpr int HPW = (G + NWARP - 1) / NWARP;   // heads owned per warp in the softmax
     constexpr int PROW = CH + 8;               // halves per sP row (pad: conflict-free fragment reads)
+    constexpr int R = D / 32;
 
     extern __shared__ __align__(16) uint8_t smem[];
     uint8_t *sK = smem;                                        // [2][BPC][KREC]
     uint8_t *sV = sK + C::kBytes;                              // [2][BPC][VREC]
     __half *sP = reinterpret_cast<__half *>(sV + C::vBytes);   // [8][PROW] weights, head-major
     float *sS = reinterpret_cast<float *>(sP + 8 * PROW);      // [CH][G] scores
-    float *sAcc = reinterpret_cast<float *>(sK);               // [G][D], after the loop
+    float *sAcc = reinterpret_cast<float *>(sK);               // [G][D], between segments
     __shared__ int sOk[2][BPC];
     __shared__ float sF[8];
     __shared__ float sM[8], sL[8], sT[8];
     __shared__ int sE[8];
+    __shared__ bool s_last;
 
-    const int s = blockIdx.x, kh = blockIdx.y, b = blockIdx.z;
+    const int cta = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
-    int L = ctx_lens[b];
-    if (L > max_ctx) L = max_ctx;
-    const int t0 = s * split;
-    if (t0 >= L) {                             // nothing to attend: split 0 writes out = 0
-        if (L <= 0 && s == 0)
-            for (int i = tid; i < G * D; i += NT_) out[((size_t)b * hq + kh * G) * D + i] = 0.f;
-        return;
-    }
-    const int t1 = min(L, t0 + split);
 
-    // stage the K and V records of the chunk starting at token tc into buffer buf
-    auto issue_chunk = [&](int tc, int buf) {
-        const int k = tid % BPC;
-        const bool inrange = tc + kBlock * k < t1;
-        const int64_t p = inrange ? block_of(block_table, b, max_blocks, tc / kBlock + k, num_blocks) : -1;
-        if (tid < BPC) {
-            sOk[buf][k] = p >= 0;
-            if (inrange && p < 0) flag_status(status, TQ_STATUS_BAD_SLOT);
-        }
-        if (p >= 0) {
-            const uint8_t *gk = k_pool + ((size_t)p * hkv + kh) * KREC;
-            const uint8_t *gv = v_pool + ((size_t)p * hkv + kh) * VREC;
-            uint8_t *dk = sK + ((size_t)buf * BPC + k) * KREC;
-            uint8_t *dv = sV + ((size_t)buf * BPC + k) * VREC;
-            for (int j = tid / BPC; j < KREC / 16; j += NT_ / BPC) cp_async16(dk + 16 * j, gk + 16 * j);
-            for (int j = tid / BPC; j < VREC / 16; j += NT_ / BPC) cp_async16(dv + 16 * j, gv + 16 * j);
-        }
-        cp_async_commit();
-    };
-    issue_chunk(t0, 0);
+    // sequences with nothing to attend get out = 0
+    for (int b = cta; b < batch; b += gridDim.x)
+        if (clamp_len(ctx_lens[b], max_ctx) == 0)
+            for (int i = tid; i < hq * D; i += NT_) out[(size_t)b * hq * D + i] = 0.f;
+
+    // P CTAs share the W chunks, at least one chunk each (as in build_schedule)
+    const int64_t W = cpre[batch];
+    const int P = (int)(W < (int64_t)gridDim.x ? W : (int64_t)gridDim.x);
+    if (cta >= P) return;
+    const int64_t g0 = sk_begin(cta, P, W), g1 = sk_begin(cta + 1, P, W);
 
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     float A[4];
@@ -325,29 +411,6 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
 
     // weight rows of heads >= G stay zero
     for (int i = tid; i < (8 - G) * PROW; i += NT_) sP[G * PROW + i] = __float2half(0.f);
-
-    // K-side operand fragments and offset constants of this (sequence, kv head)
-    const uint8_t *pack = packs + ((size_t)b * hkv + kh) * kPackBytes(D);
-    const float *pf = reinterpret_cast<const float *>(pack) + kPackFloatOff(D);
-    uint32_t bq[2][NKS][NTK][2];
-#pragma unroll
-    for (int qu = 0; qu < 2; ++qu)
-#pragma unroll
-        for (int ks = 0; ks < NKS; ++ks)
-#pragma unroll
-            for (int nt = 0; nt < NTK; ++nt) {
-                const uint2 w = *reinterpret_cast<const uint2 *>(
-                    pack + (((size_t)(qu * NKS + ks) * NTK + nt) * 64 + lane * 2) * 4);
-                bq[qu][ks][nt][0] = w.x;
-                bq[qu][ks][nt][1] = w.y;
-            }
-    float cq[NTK], cu[NTK];
-#pragma unroll
-    for (int nt = 0; nt < NTK; ++nt) {
-        const int hg = 4 * nt + tig;           // columns 2tig (hi) and 2tig+1 (lo) of n-tile nt
-        cq[nt] = hg < G ? pf[hg] * Asum : 0.f;
-        cu[nt] = hg < G ? pf[8 + hg] : 0.f;
-    }
     // V side: operand mask/base of this warp's m-tiles
     uint32_t vmask[MTW], vbase[MTW];
 #pragma unroll
@@ -358,396 +421,500 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
     }
     const int mhi = (warp * MTW) >> 3;
 
-    float O[4][MTW][4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m)
-#pragma unroll
-        for (int i = 0; i < MTW; ++i)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) O[m][i][k] = 0.f;
-    float m_run[HPW], l_run[HPW], w_ref[HPW], T_run[HPW];
-    int e_run[HPW];
-#pragma unroll
-    for (int k = 0; k < HPW; ++k) {
-        m_run[k] = -INFINITY;
-        l_run[k] = 0.f;
-        w_ref[k] = 0.f;
-        e_run[k] = 0;
-        T_run[k] = 0.f;
-    }
+    // the first segment: sequence b, kv head kh, global chunk g
+    int b = cta_b[cta];
+    int64_t ub = cpre[b];
+    int nchb = (int)((cpre[b + 1] - ub) / hkv);
+    int kh = (int)((g0 - ub) / nchb);
+    int64_t g = g0;
+    bool first_seg = true;
 
-    int buf = 0;
-    for (int tc = t0; tc < t1; tc += CH, buf ^= 1) {
-        cp_async_wait_all();
-        __syncthreads();   // chunk `buf` staged and visible; the other buffer is free
-        if (tc + CH < t1) issue_chunk(tc + CH, buf ^ 1);
-        const uint8_t *kb_base = sK + (size_t)buf * BPC * KREC;
-        const uint8_t *vb_base = sV + (size_t)buf * BPC * VREC;
-        // ---- K side: warp scores blocks BPW*warp .. BPW*warp+BPW-1 of the chunk
 #pragma unroll 1
-        for (int bw = 0; bw < BPW; ++bw) {
-            const int k = BPW * warp + bw;
-            const bool ok = sOk[buf][k] != 0;
-            const uint8_t *rec = kb_base + (size_t)k * KREC;
-            uint32_t W[4][2][NW];
+    while (true) {
+        const int64_t us = ub + (int64_t)kh * nchb, ue = us + nchb;
+        const int64_t se = (g1 < ue) ? g1 : ue;
+        const int L = clamp_len(ctx_lens[b], max_ctx);
+        const int t0 = (int)(g - us) * CH;
+        const int t1 = min(L, (int)(se - us) * CH);
+
+        // stage the K and V records of the chunk starting at token tc into buffer buf
+        auto issue_chunk = [&](int tc, int buf) {
+            const int k = tid % BPC;
+            const bool inrange = tc + kBlock * k < t1;
+            const int64_t p = inrange ? block_of(block_table, b, max_blocks, tc / kBlock + k, num_blocks) : -1;
+            if (tid < BPC) {
+                sOk[buf][k] = p >= 0;
+                if (inrange && p < 0) flag_status(status, TQ_STATUS_BAD_SLOT);
+            }
+            if (p >= 0) {
+                const uint8_t *gk = k_pool + ((size_t)p * hkv + kh) * KREC;
+                const uint8_t *gv = v_pool + ((size_t)p * hkv + kh) * VREC;
+                uint8_t *dk = sK + ((size_t)buf * BPC + k) * KREC;
+                uint8_t *dv = sV + ((size_t)buf * BPC + k) * VREC;
+                for (int j = tid / BPC; j < KREC / 16; j += NT_ / BPC) cp_async16(dk + 16 * j, gk + 16 * j);
+                for (int j = tid / BPC; j < VREC / 16; j += NT_ / BPC) cp_async16(dv + 16 * j, gv + 16 * j);
+            }
+            cp_async_commit();
+        };
+        issue_chunk(t0, 0);
+
+        // K-side operand fragments and offset constants of this (sequence, kv head)
+        const uint8_t *pack = packs + ((size_t)b * hkv + kh) * kPackBytes(D);
+        const float *pf = reinterpret_cast<const float *>(pack) + kPackFloatOff(D);
+        uint32_t bq[2][NKS][NTK][2];
 #pragma unroll
-            for (int pl = 0; pl < 4; ++pl) {
-                if (NW == 1) {
-                    const uint2 w = *reinterpret_cast<const uint2 *>(rec + pl * 2 * D + lane * 8);
-                    W[pl][0][0] = w.x;
-                    W[pl][1][0] = w.y;
-                } else {
-                    const uint4 w = *reinterpret_cast<const uint4 *>(rec + pl * 2 * D + lane * 16);
-                    W[pl][0][0] = w.x;
-                    W[pl][0][NW - 1] = w.y;
-                    W[pl][1][0] = w.z;
-                    W[pl][1][NW - 1] = w.w;
+        for (int qu = 0; qu < 2; ++qu)
+#pragma unroll
+            for (int ks = 0; ks < NKS; ++ks)
+#pragma unroll
+                for (int nt = 0; nt < NTK; ++nt) {
+                    const uint2 w = *reinterpret_cast<const uint2 *>(
+                        pack + (((size_t)(qu * NKS + ks) * NTK + nt) * 64 + lane * 2) * 4);
+                    bq[qu][ks][nt][0] = w.x;
+                    bq[qu][ks][nt][1] = w.y;
                 }
-            }
-            float nrm[2], gam[2];
+        float cq[NTK], cu[NTK];
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const __half2 ng = *reinterpret_cast<const __half2 *>(rec + 8 * D + 4 * (gid + 8 * r));
-                nrm[r] = __low2float(ng);
-                gam[r] = __high2float(ng);
-            }
-            // five masks as independent accumulator chains: code = sum_m A_m (mask m), qjl = mask 4
-            uint32_t w[5][2][NW], w8[5][2][NW];
+        for (int nt = 0; nt < NTK; ++nt) {
+            const int hg = 4 * nt + tig;           // columns 2tig (hi) and 2tig+1 (lo) of n-tile nt
+            cq[nt] = hg < G ? pf[hg] * Asum : 0.f;
+            cu[nt] = hg < G ? pf[8 + hg] : 0.f;
+        }
+
+        float O[4][MTW][4];
 #pragma unroll
-            for (int m = 0; m < 5; ++m)
+        for (int m = 0; m < 4; ++m)
 #pragma unroll
-                for (int th = 0; th < 2; ++th)
+            for (int i = 0; i < MTW; ++i)
 #pragma unroll
-                    for (int wj = 0; wj < NW; ++wj) {
-                        w[m][th][wj] = (m < 3) ? W[m][th][wj]
-                                     : (m == 3) ? (W[0][th][wj] ^ W[1][th][wj] ^ W[2][th][wj]) : W[3][th][wj];
-                        w8[m][th][wj] = w[m][th][wj] << 8;
+                for (int k = 0; k < 4; ++k) O[m][i][k] = 0.f;
+        float m_run[HPW], l_run[HPW], w_ref[HPW], T_run[HPW];
+        int e_run[HPW];
+#pragma unroll
+        for (int k = 0; k < HPW; ++k) {
+            m_run[k] = -INFINITY;
+            l_run[k] = 0.f;
+            w_ref[k] = 0.f;
+            e_run[k] = 0;
+            T_run[k] = 0.f;
+        }
+
+        int buf = 0;
+#pragma unroll 1
+        for (int tc = t0; tc < t1; tc += CH, buf ^= 1) {
+            cp_async_wait_all();
+            __syncthreads();   // chunk `buf` staged and visible; the other buffer is free
+            if (tc + CH < t1) issue_chunk(tc + CH, buf ^ 1);
+            const uint8_t *kb_base = sK + (size_t)buf * BPC * KREC;
+            const uint8_t *vb_base = sV + (size_t)buf * BPC * VREC;
+            // ---- K side: warp scores blocks BPW*warp .. BPW*warp+BPW-1 of the chunk
+#pragma unroll 1
+            for (int bw = 0; bw < BPW; ++bw) {
+                const int k = BPW * warp + bw;
+                const bool ok = sOk[buf][k] != 0;
+                const uint8_t *rec = kb_base + (size_t)k * KREC;
+                uint32_t Wd[4][2][NW];
+#pragma unroll
+                for (int pl = 0; pl < 4; ++pl) {
+                    if (NW == 1) {
+                        const uint2 w = *reinterpret_cast<const uint2 *>(rec + pl * 2 * D + lane * 8);
+                        Wd[pl][0][0] = w.x;
+                        Wd[pl][1][0] = w.y;
+                    } else {
+                        const uint4 w = *reinterpret_cast<const uint4 *>(rec + pl * 2 * D + lane * 16);
+                        Wd[pl][0][0] = w.x;
+                        Wd[pl][0][NW - 1] = w.y;
+                        Wd[pl][1][0] = w.z;
+                        Wd[pl][1][NW - 1] = w.w;
                     }
-            float acc[5][NTK][4];
-#pragma unroll
-            for (int m = 0; m < 5; ++m)
-#pragma unroll
-                for (int nt = 0; nt < NTK; ++nt)
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) acc[m][nt][x] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < NKS; ++ks) {
-                const int q = 8 + (ks & 7), wj = ks >> 3;
-                const uint32_t msk = op_mask(q), bas = (q == 14) ? 0u : one16x2;
-#pragma unroll
-                for (int m = 0; m < 5; ++m) {
-                    const uint32_t a0 = lop_and_xor(w8[m][0][wj], msk, bas), a1 = lop_and_xor(w8[m][1][wj], msk, bas);
-                    const uint32_t a2 = lop_and_xor(w[m][0][wj], msk, bas), a3 = lop_and_xor(w[m][1][wj], msk, bas);
-                    const int qu = (m == 4) ? 1 : 0;
-#pragma unroll
-                    for (int nt = 0; nt < NTK; ++nt)
-                        mma_f16(acc[m][nt], a0, a1, a2, a3, bq[qu][ks][nt][0], bq[qu][ks][nt][1]);
                 }
-            }
-            float code[NTK][4], qjv[NTK][4];
-#pragma unroll
-            for (int nt = 0; nt < NTK; ++nt)
-#pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    code[nt][x] = A[0] * acc[0][nt][x] + A[1] * acc[1][nt][x] + A[2] * acc[2][nt][x] + A[3] * acc[3][nt][x];
-                    qjv[nt][x] = acc[4][nt][x];
-                }
-#pragma unroll
-            for (int nt = 0; nt < NTK; ++nt) {
-                const int hg = 4 * nt + tig;
+                float nrm[2], gam[2];
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const float dot_c = code[nt][2 * r] + code[nt][2 * r + 1] - cq[nt];
-                    const float dot_q = qjv[nt][2 * r] + qjv[nt][2 * r + 1] - cu[nt];
-                    const int tl = kBlock * k + gid + 8 * r;           // token within the chunk
-                    const bool valid = ok && (tc + tl < t1);
-                    const float sc = nrm[r] * inv_sd * (dot_c * inv_sd + gam[r] * qjl * dot_q);
-                    if (hg < G) sS[tl * G + hg] = valid ? sc : -INFINITY;
+                    const __half2 ng = *reinterpret_cast<const __half2 *>(rec + 8 * D + 4 * (gid + 8 * r));
+                    nrm[r] = __low2float(ng);
+                    gam[r] = __high2float(ng);
+                }
+                // five masks as independent accumulator chains: code = sum_m A_m (mask m), qjl = mask 4
+                uint32_t w[5][2][NW], w8[5][2][NW];
+#pragma unroll
+                for (int m = 0; m < 5; ++m)
+#pragma unroll
+                    for (int th = 0; th < 2; ++th)
+#pragma unroll
+                        for (int wj = 0; wj < NW; ++wj) {
+                            w[m][th][wj] = (m < 3) ? Wd[m][th][wj]
+                                         : (m == 3) ? (Wd[0][th][wj] ^ Wd[1][th][wj] ^ Wd[2][th][wj]) : Wd[3][th][wj];
+                            w8[m][th][wj] = w[m][th][wj] << 8;
+                        }
+                float acc[5][NTK][4];
+#pragma unroll
+                for (int m = 0; m < 5; ++m)
+#pragma unroll
+                    for (int nt = 0; nt < NTK; ++nt)
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) acc[m][nt][x] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < NKS; ++ks) {
+                    const int q = 8 + (ks & 7), wj = ks >> 3;
+                    const uint32_t msk = op_mask(q), bas = (q == 14) ? 0u : one16x2;
+#pragma unroll
+                    for (int m = 0; m < 5; ++m) {
+                        const uint32_t a0 = lop_and_xor(w8[m][0][wj], msk, bas), a1 = lop_and_xor(w8[m][1][wj], msk, bas);
+                        const uint32_t a2 = lop_and_xor(w[m][0][wj], msk, bas), a3 = lop_and_xor(w[m][1][wj], msk, bas);
+                        const int qu = (m == 4) ? 1 : 0;
+#pragma unroll
+                        for (int nt = 0; nt < NTK; ++nt)
+                            mma_f16(acc[m][nt], a0, a1, a2, a3, bq[qu][ks][nt][0], bq[qu][ks][nt][1]);
+                    }
+                }
+#pragma unroll
+                for (int nt = 0; nt < NTK; ++nt) {
+                    const int hg = 4 * nt + tig;
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        float code2 = 0.f;
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) code2 = fmaf(A[m], acc[m][nt][2 * r] + acc[m][nt][2 * r + 1], code2);
+                        const float dot_c = code2 - cq[nt];
+                        const float dot_q = acc[4][nt][2 * r] + acc[4][nt][2 * r + 1] - cu[nt];
+                        const int tl = kBlock * k + gid + 8 * r;           // token within the chunk
+                        const bool valid = ok && (tc + tl < t1);
+                        const float sc = nrm[r] * inv_sd * (dot_c * inv_sd + gam[r] * qjl * dot_q);
+                        if (hg < G) sS[tl * G + hg] = valid ? sc : -INFINITY;
+                    }
+                }
+            }
+            __syncthreads();   // scores of the chunk are in sS
+            // ---- online softmax: warp owns heads warp, warp + NWARP
+#pragma unroll
+            for (int hk = 0; hk < HPW; ++hk) {
+                const int h = warp + NWARP * hk;
+                if (h < G) {
+                    float sc[TPL], wv[TPL];
+                    float cmax = -INFINITY;
+#pragma unroll
+                    for (int i = 0; i < TPL; ++i) {
+                        sc[i] = sS[(lane + 32 * i) * G + h];
+                        cmax = fmaxf(cmax, sc[i]);
+                    }
+                    cmax = warp_max(cmax);
+                    const float m_new = fmaxf(m_run[hk], cmax);
+                    const float alpha = (m_run[hk] == -INFINITY) ? 0.f : __expf(m_run[hk] - m_new);
+                    float psum = 0.f, wmax = 0.f;
+#pragma unroll
+                    for (int i = 0; i < TPL; ++i) {
+                        const int tl = lane + 32 * i;
+                        const float p = (sc[i] == -INFINITY) ? 0.f : __expf(sc[i] - m_new);
+                        const float nv = __half2float(*reinterpret_cast<const __half *>(
+                            vb_base + (size_t)(tl >> 4) * VREC + 6 * D + 2 * (tl & 15)));
+                        wv[i] = (p > 0.f) ? p * nv * inv_sd : 0.f;
+                        psum += p;
+                        wmax = fmaxf(wmax, fabsf(wv[i]));
+                    }
+                    psum = warp_sum(psum);
+                    wmax = warp_max(wmax);
+                    const float wr = fmaxf(w_ref[hk] * alpha, wmax);
+                    const int e_new = wr > 0.f ? scale_exp(wr) : e_run[hk];
+                    const float f = ldexpf(alpha, e_new - e_run[hk]);
+                    const float sc2 = ldexpf(1.f, e_new);
+                    float tsum = 0.f;
+#pragma unroll
+                    for (int i = 0; i < TPL; ++i) {
+                        const __half hv = __float2half_rn(wv[i] * sc2);
+                        sP[h * PROW + lane + 32 * i] = hv;
+                        tsum += __half2float(hv);
+                    }
+                    T_run[hk] = T_run[hk] * f + warp_sum(tsum);
+                    l_run[hk] = l_run[hk] * alpha + psum;
+                    m_run[hk] = m_new;
+                    w_ref[hk] = wr;
+                    e_run[hk] = e_new;
+                    if (lane == 0) sF[h] = f;
+                }
+            }
+            __syncthreads();   // weights of the chunk are in sP, factors in sF
+            // ---- V side: coordinates of m-tiles warp*MTW .. warp*MTW+MTW-1 (columns = heads)
+            {
+                const float f0 = (2 * tig < G) ? sF[2 * tig] : 0.f;
+                const float f1 = (2 * tig + 1 < G) ? sF[2 * tig + 1] : 0.f;
+#pragma unroll
+                for (int m = 0; m < 4; ++m)
+#pragma unroll
+                    for (int i = 0; i < MTW; ++i) {
+                        O[m][i][0] *= f0;
+                        O[m][i][1] *= f1;
+                        O[m][i][2] *= f0;
+                        O[m][i][3] *= f1;
+                    }
+            }
+#pragma unroll 2
+            for (int kb = 0; kb < BPC; ++kb) {
+                const uint8_t *rec = vb_base + (size_t)kb * VREC;
+                uint32_t x[3][2];
+#pragma unroll
+                for (int pl = 0; pl < 3; ++pl) {
+                    const uint2 wv = *reinterpret_cast<const uint2 *>(rec + pl * 2 * D + (lane * NWV + 2 * mhi) * 4);
+                    x[pl][0] = wv.x;
+                    x[pl][1] = wv.y;
+                }
+                const __half *prow = sP + gid * PROW + kBlock * kb + 2 * tig;
+                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(prow);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(prow + 8);
+#pragma unroll
+                for (int m = 0; m < 4; ++m) {
+                    const uint32_t x0 = (m < 3) ? x[m][0] : (x[0][0] ^ x[1][0] ^ x[2][0]);
+                    const uint32_t x1 = (m < 3) ? x[m][1] : (x[0][1] ^ x[1][1] ^ x[2][1]);
+                    const uint32_t x0s = x0 << 8, x1s = x1 << 8;
+#pragma unroll
+                    for (int i = 0; i < MTW; ++i) {
+                        const uint32_t a0 = lop_and_xor(x0s, vmask[i], vbase[i]), a1 = lop_and_xor(x1s, vmask[i], vbase[i]);
+                        const uint32_t a2 = lop_and_xor(x0, vmask[i], vbase[i]), a3 = lop_and_xor(x1, vmask[i], vbase[i]);
+                        mma_f16(O[m][i], a0, a1, a2, a3, b0, b1);
+                    }
                 }
             }
         }
-        __syncthreads();   // scores of the chunk are in sS
-        // ---- online softmax: warp owns heads warp, warp + NWARP
+
+        // ---- segment epilogue: combine the masks, undo the operand offsets and the weight scale
 #pragma unroll
         for (int hk = 0; hk < HPW; ++hk) {
             const int h = warp + NWARP * hk;
-            if (h < G) {
-                float sc[TPL], w[TPL], p[TPL];
-                float cmax = -INFINITY;
-#pragma unroll
-                for (int i = 0; i < TPL; ++i) {
-                    sc[i] = sS[(lane + 32 * i) * G + h];
-                    cmax = fmaxf(cmax, sc[i]);
-                }
-                cmax = warp_max(cmax);
-                const float m_new = fmaxf(m_run[hk], cmax);
-                const float alpha = (m_run[hk] == -INFINITY) ? 0.f : __expf(m_run[hk] - m_new);
-                float psum = 0.f, wmax = 0.f;
-#pragma unroll
-                for (int i = 0; i < TPL; ++i) {
-                    const int tl = lane + 32 * i;
-                    p[i] = (sc[i] == -INFINITY) ? 0.f : __expf(sc[i] - m_new);
-                    const float nv = __half2float(*reinterpret_cast<const __half *>(
-                        vb_base + (size_t)(tl >> 4) * VREC + 6 * D + 2 * (tl & 15)));
-                    w[i] = (p[i] > 0.f) ? p[i] * nv * inv_sd : 0.f;
-                    psum += p[i];
-                    wmax = fmaxf(wmax, fabsf(w[i]));
-                }
-                psum = warp_sum(psum);
-                wmax = warp_max(wmax);
-                const float wr = fmaxf(w_ref[hk] * alpha, wmax);
-                const int e_new = wr > 0.f ? scale_exp(wr) : e_run[hk];
-                const float f = ldexpf(alpha, e_new - e_run[hk]);
-                float tsum = 0.f;
-#pragma unroll
-                for (int i = 0; i < TPL; ++i) {
-                    const __half hv = __float2half_rn(ldexpf(w[i], e_new));
-                    sP[h * PROW + lane + 32 * i] = hv;
-                    tsum += __half2float(hv);
-                }
-                T_run[hk] = T_run[hk] * f + warp_sum(tsum);
-                l_run[hk] = l_run[hk] * alpha + psum;
-                m_run[hk] = m_new;
-                w_ref[hk] = wr;
-                e_run[hk] = e_new;
-                if (lane == 0) sF[h] = f;
+            if (h < G && lane == 0) {
+                sM[h] = m_run[hk];
+                sL[h] = l_run[hk];
+                sE[h] = e_run[hk];
+                sT[h] = T_run[hk];
             }
         }
-        __syncthreads();   // weights of the chunk are in sP, factors in sF
-        // ---- V side: coordinates of m-tiles warp*MTW .. warp*MTW+MTW-1 (columns = heads)
-        {
-            const float f0 = (2 * tig < G) ? sF[2 * tig] : 0.f;
-            const float f1 = (2 * tig + 1 < G) ? sF[2 * tig + 1] : 0.f;
+        __syncthreads();   // the staging buffers are no longer read; sAcc reuses them
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
+        for (int i = 0; i < MTW; ++i) {
+            const int mt = warp * MTW + i, q = 8 + (mt & 7);
+            const float al = op_alpha(q), inv_de = 2.f / op_delta(q);
 #pragma unroll
-                for (int i = 0; i < MTW; ++i) {
-                    O[m][i][0] *= f0;
-                    O[m][i][1] *= f1;
-                    O[m][i][2] *= f0;
-                    O[m][i][3] *= f1;
-                }
-        }
-#pragma unroll 2
-        for (int kb = 0; kb < BPC; ++kb) {
-            const uint8_t *rec = vb_base + (size_t)kb * VREC;
-            uint32_t x[3][2];
+            for (int e = 0; e < 2; ++e) {
+                const int h = 2 * tig + e;
+                if (h < G) {
+                    const float T = sT[h];
 #pragma unroll
-            for (int pl = 0; pl < 3; ++pl) {
-                const uint2 wv = *reinterpret_cast<const uint2 *>(rec + pl * 2 * D + (lane * NWV + 2 * mhi) * 4);
-                x[pl][0] = wv.x;
-                x[pl][1] = wv.y;
-            }
-            const __half *prow = sP + gid * PROW + kBlock * kb + 2 * tig;
-            const uint32_t b0 = *reinterpret_cast<const uint32_t *>(prow);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t *>(prow + 8);
+                    for (int r = 0; r < 2; ++r) {
+                        float v = 0.f;
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const uint32_t x0 = (m < 3) ? x[m][0] : (x[0][0] ^ x[1][0] ^ x[2][0]);
-                const uint32_t x1 = (m < 3) ? x[m][1] : (x[0][1] ^ x[1][1] ^ x[2][1]);
-                const uint32_t x0s = x0 << 8, x1s = x1 << 8;
-#pragma unroll
-                for (int i = 0; i < MTW; ++i) {
-                    const uint32_t a0 = lop_and_xor(x0s, vmask[i], vbase[i]), a1 = lop_and_xor(x1s, vmask[i], vbase[i]);
-                    const uint32_t a2 = lop_and_xor(x0, vmask[i], vbase[i]), a3 = lop_and_xor(x1, vmask[i], vbase[i]);
-                    mma_f16(O[m][i], a0, a1, a2, a3, b0, b1);
+                        for (int m = 0; m < 4; ++m) v += A[m] * ((O[m][i][2 * r + e] - al * T) * inv_de - T);
+                        sAcc[h * D + 16 * mt + gid + 8 * r] = ldexpf(v, -sE[h]);
+                    }
                 }
             }
         }
-    }
+        __syncthreads();
+        const int lo = sk_cta_of(us, P, W), hi = sk_cta_of(ue - 1, P, W);
+        const size_t row0 = (size_t)b * hq + (size_t)kh * G;
+        if (lo == hi) {
+            // the whole (sequence, kv head) was in this CTA: finish it here
+            for (int h = warp; h < G; h += NWARP) {
+                float v[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) v[r] = sAcc[h * D + 32 * r + lane];
+                finish_row<D>(v, sL[h], params, out + (row0 + h) * D, lane);
+            }
+        } else {
+            // leave a partial in this CTA's slot (0: its first segment, 1: its last)
+            const int slot = first_seg ? 0 : 1;
+#pragma unroll 1
+            for (int h = 0; h < G; ++h) {
+                float *dst = part + (((size_t)cta * 2 + slot) * G + h) * kPartStride(D);
+                for (int i = tid; i < D; i += NT_) dst[4 + i] = sAcc[h * D + i];
+                if (tid == 0) {
+                    dst[0] = sM[h];
+                    dst[1] = sL[h];
+                }
+            }
+            __threadfence();                           // every thread publishes its part of the partial
+            __syncthreads();
+            if (tid == 0) {
+                const unsigned int nseg = (unsigned int)(hi - lo + 1);
+                const unsigned int done = atomicAdd(&counters[b * hkv + kh], 1u) + 1u;
+                s_last = (done == nseg);
+                if (s_last) counters[b * hkv + kh] = 0u;   // every segment has arrived
+            }
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                // the partial of CTA c for this unit sits in slot 0, except for the
+                // first CTA when the unit does not start its range (then slot 1)
+                const int slot_lo = (sk_begin(lo, P, W) >= us) ? 0 : 1;
+                for (int h = warp; h < G; h += NWARP) {
+                    float M = -INFINITY;
+                    for (int c2 = lo; c2 <= hi; ++c2) {
+                        const int sl = (c2 == lo) ? slot_lo : 0;
+                        M = fmaxf(M, __ldcg(part + (((size_t)c2 * 2 + sl) * G + h) * kPartStride(D)));
+                    }
+                    float v[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) v[r] = 0.f;
+                    float l = 0.f;
+                    for (int c2 = lo; c2 <= hi; ++c2) {
+                        const int sl = (c2 == lo) ? slot_lo : 0;
+                        const float *ps = part + (((size_t)c2 * 2 + sl) * G + h) * kPartStride(D);
+                        const float m = __ldcg(ps);
+                        const float wgt = (m == -INFINITY) ? 0.f : __expf(m - M);
+                        l = fmaf(__ldcg(ps + 1), wgt, l);
+#pragma unroll
+                        for (int r = 0; r < R; ++r) v[r] = fmaf(__ldcg(ps + 4 + 32 * r + lane), wgt, v[r]);
+                    }
+                    finish_row<D>(v, l, params, out + (row0 + h) * D, lane);
+                }
+            }
+        }
+        __syncthreads();   // sAcc and the small shared arrays are rewritten by the next segment
 
-    // ---- epilogue: combine the masks, undo the operand offsets and the weight scale
-#pragma unroll
-    for (int hk = 0; hk < HPW; ++hk) {
-        const int h = warp + NWARP * hk;
-        if (h < G && lane == 0) {
-            sM[h] = m_run[hk];
-            sL[h] = l_run[hk];
-            sE[h] = e_run[hk];
-            sT[h] = T_run[hk];
+        g = se;
+        if (g >= g1) break;
+        first_seg = false;
+        if (++kh == hkv) {         // next sequence with a nonempty context
+            kh = 0;
+            do {
+                ++b;
+                ub = cpre[b];
+                nchb = (int)((cpre[b + 1] - ub) / hkv);
+            } while (nchb == 0);
         }
-    }
-    __syncthreads();   // sK is no longer read; sAcc reuses it
-#pragma unroll
-    for (int i = 0; i < MTW; ++i) {
-        const int mt = warp * MTW + i, q = 8 + (mt & 7);
-        const float al = op_alpha(q), inv_de = 2.f / op_delta(q);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int h = 2 * tig + e;
-            if (h < G) {
-                const float T = sT[h];
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    float v = 0.f;
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) v += A[m] * ((O[m][i][2 * r + e] - al * T) * inv_de - T);
-                    sAcc[h * D + 16 * mt + gid + 8 * r] = ldexpf(v, -sE[h]);
-                }
-            }
-        }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-        float *dst = part + (((size_t)b * hq + kh * G + h) * nsplit + s) * kPartStride(D);
-        for (int i = tid; i < D; i += NT_) dst[4 + i] = sAcc[h * D + i];
-        if (tid == 0) {
-            dst[0] = sM[h];
-            dst[1] = sL[h];
-        }
-    }
-    // ---- the last split of this (sequence, kv head) to finish merges all of them
-    __shared__ bool s_last;
-    __threadfence();                           // every thread publishes its part of the partial
-    __syncthreads();
-    if (tid == 0) {
-        const unsigned int nsb = (unsigned int)((L + split - 1) / split);
-        const unsigned int done = atomicAdd(&counters[b * hkv + kh], 1u) + 1u;
-        s_last = (done == nsb);
-        if (s_last) counters[b * hkv + kh] = 0u;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    const int nsb = (L + split - 1) / split;
-    constexpr int R = D / 32;
-    for (int h = warp; h < G; h += NWARP) {
-        const int row = b * hq + kh * G + h;
-        const float *p0 = part + (size_t)row * nsplit * kPartStride(D);
-        float M = -INFINITY;
-        for (int t = 0; t < nsb; ++t) M = fmaxf(M, __ldcg(p0 + (size_t)t * kPartStride(D)));
-        float v[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) v[r] = 0.f;
-        float l = 0.f;
-        for (int t = 0; t < nsb; ++t) {
-            const float *ps = p0 + (size_t)t * kPartStride(D);
-            const float m = __ldcg(ps);
-            const float w = (m == -INFINITY) ? 0.f : __expf(m - M);
-            l = fmaf(__ldcg(ps + 1), w, l);
-#pragma unroll
-            for (int r = 0; r < R; ++r) v[r] = fmaf(__ldcg(ps + 4 + 32 * r + lane), w, v[r]);
-        }
-        const float inv = (l > 0.f) ? 1.f / l : 0.f;
-#pragma unroll
-        for (int r = 0; r < R; ++r) v[r] *= inv;
-        // out = Pi^T a = D (H a) / sqrt d
-        fwht_warp<R>(v, lane);
-        const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
-#pragma unroll
-        for (int r = 0; r < R; ++r) out[(size_t)row * D + 32 * r + lane] = v[r] * inv_sd * __ldg(Dsign + 32 * r + lane);
     }
 }
 
-// Context split length: the shortest power-of-two multiple of 512 tokens that
-// still gives about 4 waves of CTAs (3 per SM) over the (sequence, kv head) units.
-int choose_split(int batch, int hkv, int max_ctx) {
-    const long long units = (long long)batch * hkv;
-    const long long target = 152LL * 3 * 4;
-    int split = kMinSplit;
-    while (split < kMaxSplit && units * ((max_ctx + 2LL * split - 1) / (2LL * split)) >= target) split *= 2;
-    return split;
+// Persistent CTAs of the pass on the current device: up to kCtasPerSm per SM
+// (fewer if the kernel's resources allow fewer), for at most kMaxSms SMs.
+template <int D, int G>
+int pass_ctas() {
+    int dev = 0, sms = 0, occ = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    constexpr int NWARP = pass_warps(G);
+    constexpr size_t smem = split_smem_bytes<D, G, NWARP>();
+    auto kern = decode_mma_kernel<D, G, NWARP>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, NWARP * 32, smem) != cudaSuccess) return 0;
+    occ = occ < 1 ? 1 : (occ > kCtasPerSm ? kCtasPerSm : occ);
+    sms = sms > kMaxSms ? kMaxSms : sms;
+    return occ * sms;
 }
 
-struct WsLayout {
-    uint8_t *packs;
-    unsigned int *counters;
-    float *part;
-    int split;
-    int nsplit;
-};
-WsLayout ws_layout(void *ws, int d, int batch, int hq, int hkv, int max_ctx) {
-    WsLayout w;
-    w.split = choose_split(batch, hkv, max_ctx);
-    w.nsplit = max(1, (max_ctx + w.split - 1) / w.split);
-    w.packs = reinterpret_cast<uint8_t *>(ws);
-    w.counters = reinterpret_cast<unsigned int *>(w.packs + (size_t)batch * hq * kPackBytes(d));
-    w.part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(w.counters) + kCounterBytes(batch, hq));
-    return w;
+template <int D>
+int pass_ctas_g(int G) {
+    switch (G) {
+        case 1: return pass_ctas<D, 1>();
+        case 2: return pass_ctas<D, 2>();
+        case 3: return pass_ctas<D, 3>();
+        case 4: return pass_ctas<D, 4>();
+        case 5: return pass_ctas<D, 5>();
+        case 6: return pass_ctas<D, 6>();
+        case 7: return pass_ctas<D, 7>();
+        default: return pass_ctas<D, 8>();
+    }
+}
+
+// Cached per (device, d, G): query prep and the pass must agree on it, and the
+// occupancy query is not free.
+int pass_ctas_any(int d, int G) {
+    constexpr int kDevs = 64;
+    static std::atomic<int> cache[kDevs][2][9];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || G < 1 || G > 8) return 0;
+    if (dev >= kDevs) return d == 128 ? pass_ctas_g<128>(G) : pass_ctas_g<256>(G);
+    std::atomic<int> &slot = cache[dev][d == 128 ? 0 : 1][G];
+    int n = slot.load(std::memory_order_relaxed);
+    if (n == 0) {
+        n = d == 128 ? pass_ctas_g<128>(G) : pass_ctas_g<256>(G);
+        slot.store(n, std::memory_order_relaxed);
+    }
+    return n;
 }
 
 template <int D, int NTK, typename T>
-cudaError_t qprep_launch_t(const uint8_t *P, const void *q, int batch, int hq, int hkv, uint8_t *packs,
-                           unsigned int *counters, cudaStream_t st) {
-    constexpr size_t smem = (size_t)2 * kQRows * D * 4 + (size_t)2 * kProjRows * D * 4;
+cudaError_t qprep_launch_t(const uint8_t *P, const void *q, int batch, int hq, int hkv, const int32_t *ctx_lens,
+                           int max_ctx, int nctas, const WsLayout &w, cudaStream_t st) {
+    constexpr size_t smem = qprep_smem<D>();
     auto kern = qprep_kernel<D, NTK, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<(batch * hq + kQRows - 1) / kQRows, 128, smem, st>>>(P, (const T *)q, batch, hq, hkv, packs, counters);
+    kern<<<(batch * hq + kQRows - 1) / kQRows, 128, smem, st>>>(P, (const T *)q, batch, hq, hkv, ctx_lens, max_ctx,
+                                                               pass_chunk(hq / hkv), nctas, w.packs, w.counters,
+                                                               w.cpre, w.cta_b);
     return cudaGetLastError();
 }
 
 template <int D, typename T>
-cudaError_t qprep_launch(const uint8_t *P, const void *q, int batch, int hq, int hkv, uint8_t *packs,
-                         unsigned int *counters, cudaStream_t st) {
+cudaError_t qprep_launch(const uint8_t *P, const void *q, int batch, int hq, int hkv, const int32_t *ctx_lens,
+                         int max_ctx, int nctas, const WsLayout &w, cudaStream_t st) {
     // n-tile count of the K-side operand: (2G + 7) / 8, as in decode_mma_kernel
-    if (hq / hkv <= 4) return qprep_launch_t<D, 1, T>(P, q, batch, hq, hkv, packs, counters, st);
-    return qprep_launch_t<D, 2, T>(P, q, batch, hq, hkv, packs, counters, st);
+    if (hq / hkv <= 4) return qprep_launch_t<D, 1, T>(P, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w, st);
+    return qprep_launch_t<D, 2, T>(P, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w, st);
 }
 
 template <int D, int G>
-cudaError_t partial_launch_g(dim3 grid, cudaStream_t st, const uint8_t *P, const uint8_t *packs, int hq, int hkv,
-                             const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
-                             const int32_t *ctx, int max_ctx, int split, float *part, int nsplit,
-                             unsigned int *counters, float *out, int32_t *status) {
-    constexpr int NWARP = G <= 4 ? 4 : 8;
+cudaError_t pass_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batch, int hq, int hkv,
+                          const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
+                          const int32_t *ctx, int max_ctx, const WsLayout &w, float *out, int32_t *status) {
+    constexpr int NWARP = pass_warps(G);
     constexpr size_t smem = split_smem_bytes<D, G, NWARP>();
     auto kern = decode_mma_kernel<D, G, NWARP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, NWARP * 32, smem, st>>>(P, packs, hq, hkv, kp, vp, nb, bt, mb, ctx, max_ctx, split, part, nsplit,
-                                        counters, out, status);
+    kern<<<nctas, NWARP * 32, smem, st>>>(P, w.packs, batch, hq, hkv, kp, vp, nb, bt, mb, ctx, max_ctx, w.cpre,
+                                         w.cta_b, w.part, w.counters, out, status);
     return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t partial_launch(int G, dim3 grid, cudaStream_t st, const uint8_t *P, const uint8_t *packs, int hq,
-                           int hkv, const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
-                           const int32_t *ctx, int max_ctx, int split, float *part, int nsplit,
-                           unsigned int *counters, float *out, int32_t *status) {
-#define TQ_PART(GG) return partial_launch_g<D, GG>(grid, st, P, packs, hq, hkv, kp, vp, nb, bt, mb, ctx, max_ctx, split, part, nsplit, counters, out, status)
+cudaError_t pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int hq, int hkv,
+                        const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
+                        const int32_t *ctx, int max_ctx, const WsLayout &w, float *out, int32_t *status) {
+#define TQ_PASS(GG) return pass_launch_g<D, GG>(nctas, st, P, batch, hq, hkv, kp, vp, nb, bt, mb, ctx, max_ctx, w, out, status)
     switch (G) {
-        case 1: TQ_PART(1);
-        case 2: TQ_PART(2);
-        case 3: TQ_PART(3);
-        case 4: TQ_PART(4);
-        case 5: TQ_PART(5);
-        case 6: TQ_PART(6);
-        case 7: TQ_PART(7);
-        default: TQ_PART(8);
+        case 1: TQ_PASS(1);
+        case 2: TQ_PASS(2);
+        case 3: TQ_PASS(3);
+        case 4: TQ_PASS(4);
+        case 5: TQ_PASS(5);
+        case 6: TQ_PASS(6);
+        case 7: TQ_PASS(7);
+        default: TQ_PASS(8);
     }
-#undef TQ_PART
+#undef TQ_PASS
 }
 
 }  // namespace
 
 cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv,
-                         int max_ctx, void *ws, cudaStream_t st) {
-    const WsLayout w = ws_layout(ws, d, batch, hq, hkv, max_ctx);
+                         const int32_t *ctx_lens, int max_ctx, void *ws, cudaStream_t st) {
+    const WsLayout w = ws_layout(ws, d, batch, hq);
+    const int nctas = pass_ctas_any(d, hq / hkv);
+    if (nctas <= 0) return cudaErrorInvalidConfiguration;
     const uint8_t *P = (const uint8_t *)params;
     if (d == 128)
-        return dtype == TQ_DTYPE_BF16 ? qprep_launch<128, __nv_bfloat16>(P, q, batch, hq, hkv, w.packs, w.counters, st)
-                                      : qprep_launch<128, float>(P, q, batch, hq, hkv, w.packs, w.counters, st);
-    return dtype == TQ_DTYPE_BF16 ? qprep_launch<256, __nv_bfloat16>(P, q, batch, hq, hkv, w.packs, w.counters, st)
-                                  : qprep_launch<256, float>(P, q, batch, hq, hkv, w.packs, w.counters, st);
+        return dtype == TQ_DTYPE_BF16
+                   ? qprep_launch<128, __nv_bfloat16>(P, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w, st)
+                   : qprep_launch<128, float>(P, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w, st);
+    return dtype == TQ_DTYPE_BF16
+               ? qprep_launch<256, __nv_bfloat16>(P, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w, st)
+               : qprep_launch<256, float>(P, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w, st);
 }
 
 cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
                           const int32_t *ctx_lens, int max_ctx, float *out, void *ws, int32_t *status,
                           cudaStream_t st) {
-    const WsLayout w = ws_layout(ws, d, batch, hq, hkv, max_ctx);
-    const dim3 grid(w.nsplit, hkv, batch);
+    const WsLayout w = ws_layout(ws, d, batch, hq);
     const int G = hq / hkv;
+    const int nctas = pass_ctas_any(d, G);
+    if (nctas <= 0) return cudaErrorInvalidConfiguration;
     const uint8_t *P = (const uint8_t *)params;
     if (d == 128)
-        return partial_launch<128>(G, grid, st, P, w.packs, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
-                                   num_blocks, block_table, max_blocks, ctx_lens, max_ctx, w.split, w.part, w.nsplit,
-                                   w.counters, out, status);
-    return partial_launch<256>(G, grid, st, P, w.packs, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
-                               num_blocks, block_table, max_blocks, ctx_lens, max_ctx, w.split, w.part, w.nsplit,
-                               w.counters, out, status);
+        return pass_launch<128>(G, nctas, st, P, batch, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
+                                num_blocks, block_table, max_blocks, ctx_lens, max_ctx, w, out, status);
+    return pass_launch<256>(G, nctas, st, P, batch, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
+                            num_blocks, block_table, max_blocks, ctx_lens, max_ctx, w, out, status);
 }
 
 }  // namespace tq

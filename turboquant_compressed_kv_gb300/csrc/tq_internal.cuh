@@ -170,25 +170,42 @@ __device__ __forceinline__ void stage_st_rows(float *dst, const float *gST, int 
     cp_async_commit();
 }
 
-// Streamed projection: S^T passes through sbuf (2 x kProjRows x D floats).
-// Every thread of the CTA must call it (it synchronises the CTA).
-template <int D, int NV, int NT>
+// Streamed projection: S^T passes through sbuf (2 x ROWS x D floats, or
+// ROWS x D when one chunk holds all of S^T).  Every thread of the CTA must
+// call it (it synchronises the CTA).
+template <int D, int NV, int NT, int ROWS = kProjRows>
 __device__ __forceinline__ void project_streamed(const float *gST, float *sbuf, const float (*x)[D],
                                                  float (&acc)[D / NT][NV]) {
-    constexpr int NCHUNK = D / kProjRows;
-    stage_st_rows<D, NT>(sbuf, gST, 0, kProjRows);
+    constexpr int NCHUNK = D / ROWS;
+    stage_st_rows<D, NT>(sbuf, gST, 0, ROWS);
 #pragma unroll 1
     for (int c = 0; c < NCHUNK; ++c) {
         if (c + 1 < NCHUNK) {
-            stage_st_rows<D, NT>(sbuf + (size_t)((c + 1) & 1) * kProjRows * D, gST, (c + 1) * kProjRows, kProjRows);
+            stage_st_rows<D, NT>(sbuf + (size_t)((c + 1) & 1) * ROWS * D, gST, (c + 1) * ROWS, ROWS);
             cp_async_wait_1();
         } else {
             cp_async_wait_all();
         }
         __syncthreads();
-        project_rows<D, NV, NT>(sbuf + (size_t)(c & 1) * kProjRows * D, c * kProjRows, kProjRows, x, acc);
+        project_rows<D, NV, NT>(sbuf + (size_t)(c & 1) * ROWS * D, c * ROWS, ROWS, x, acc);
         __syncthreads();
     }
 }
+
+// ---------------------------------------------------------------- launchers (defined in the .cu files)
+
+cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const void *x, int64_t n_tokens,
+                          int n_heads, const int64_t *slots, void *pool, int64_t num_blocks, int32_t *status,
+                          cudaStream_t st);
+cudaError_t launch_append(int d, int dtype, const void *params, const void *k_new, const void *v_new, int batch,
+                          int n_heads, const int32_t *bt, int max_blocks, const int32_t *ctx, void *kp, void *vp,
+                          int64_t num_blocks, int32_t *status, cudaStream_t st);
+size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx);
+cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv,
+                         const int32_t *ctx_lens, int max_ctx, void *ws, cudaStream_t st);
+cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
+                          const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
+                          const int32_t *ctx_lens, int max_ctx, float *out, void *ws, int32_t *status,
+                          cudaStream_t st);
 
 }  // namespace tq

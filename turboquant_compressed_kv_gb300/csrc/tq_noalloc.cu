@@ -12,14 +12,6 @@
 #include "tq_internal.cuh"
 
 namespace tq {
-cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv, int max_ctx,
-                         void *ws, cudaStream_t st);
-cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
-                          const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
-                          const int32_t *ctx_lens, int max_ctx, float *out, void *ws, int32_t *status,
-                          cudaStream_t st);
-size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx);
-
 namespace {
 
 constexpr size_t kNoallocScratchBytes = TQ_NOALLOC_SCRATCH_BYTES;   // 16 MiB per GPU
@@ -81,7 +73,7 @@ extern "C" int tq_decode_attn_noalloc(const void *params, int d, const void *q, 
     // call (the query-prep kernel also resets the split counters), so the
     // contents left by a previous call need no clearing.
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    e = launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, max_ctx, ws, st);
+    e = launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx, ws, st);
     if (e == cudaSuccess)
         e = launch_splitk(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
                           max_blocks, ctx_lens, max_ctx, out, ws, status, st);
