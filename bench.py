@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--main-only", action="store_true",
+                    help="skip the ragged / long-context decode and the prefill encode measurements")
     return ap.parse_args()
 
 
@@ -245,6 +247,135 @@ def profile_traffic(bytes_per_launch):
         return None
 
 
+def extra_decode(name, steps, warmup, dev):
+    """Decode pass (query prep + split-K) on another decode workload; inputs drawn on the device."""
+    import torch
+
+    import turboquant_compressed_kv_gb300 as tq
+    from turboquant_compressed_kv_gb300 import synth
+    from turboquant_compressed_kv_gb300.cache import PagedCache, to_device
+    w = synth.workload(name)
+    d, B, Hq, Hkv = w.head_dim, w.batch, w.n_q_heads, w.n_kv_heads
+    nb = step_bytes(w)
+    cache = PagedCache.create(w, dev)
+    cache.prefill_device()
+    per_cache = cache.k_pool.numel() + cache.v_pool.numel()
+    nrep = max(2, math.ceil(3 * L2_BYTES / per_cache))
+    pools = [(cache.k_pool, cache.v_pool)] + [(cache.k_pool.clone(), cache.v_pool.clone())
+                                              for _ in range(nrep - 1)]
+    q = to_device(synth.queries(w), w.dtype, dev)
+    ctx = torch.tensor(w.ctx_lens, dtype=torch.int32, device=dev)
+    max_ctx = max(w.ctx_lens)
+    ws = torch.empty(tq.decode_workspace_bytes(d, B, Hq, max_ctx), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i, ev=None):
+        kp, vp = pools[i % nrep]
+        tq.decode_qprep(cache.params, d, q, Hkv, ctx, max_ctx, ws)
+        if ev is not None:
+            ev[0].record(stream)
+        tq.decode_splitk(cache.params, d, B, Hq, Hkv, kp, vp, cache.block_table, ctx, max_ctx, out, ws,
+                         status=status)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(i, kev[i])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in {name}")
+    ms = e0.elapsed_time(e1) / steps
+    kms = statistics.mean(a.elapsed_time(b) for a, b in kev)
+    peak, _ = measured_peak()
+    res = {"config": workload_config(w, f"{nrep} cache copies cycled ({nrep * per_cache / 2**20:.0f} MiB > L2)"),
+           "value": round(nb["step"] / (ms * 1e-3) / 1e9, 3), "unit": "GB/s", "ms_per_step": round(ms, 6),
+           "steps": steps, "warmup": warmup, "launches_per_step": 2,
+           "roofline": {"bound": "hbm", "kernel": "tq_decode_splitk", "kernel_ms": round(kms, 6),
+                        "achieved": round(nb["partial"] / (kms * 1e-3) / 1e9, 3), "peak": peak, "unit": "GB/s",
+                        "frac": round(nb["partial"] / (kms * 1e-3) / 1e9 / peak, 4),
+                        "bytes_per_launch": nb["partial"]}}
+    del pools, cache
+    torch.cuda.empty_cache()
+    return res
+
+
+def extra_encode(steps, warmup, dev):
+    """Bulk encode of the prefill workload (8 x 32768 tokens x 8 kv heads, d=128, bf16) into paged storage."""
+    import torch
+
+    import turboquant_compressed_kv_gb300 as tq
+    from turboquant_compressed_kv_gb300 import synth
+    from turboquant_compressed_kv_gb300.cache import PagedCache
+    w = synth.workload("prefill")
+    d, Hkv = w.head_dim, w.n_kv_heads
+    cache = PagedCache.create(w, dev)
+    ntok = sum(w.prefill_lens)
+    Ks, Vs, slots = [], [], []
+    for b in range(w.batch):
+        K, V = synth.kv_tokens_device(w, b, 0, w.prefill_lens[b], dev)
+        Ks.append(K)
+        Vs.append(V)
+        slots.append(torch.from_numpy(synth.slots_for(cache.block_table_np, b, 0, w.prefill_lens[b])))
+    K = torch.cat(Ks)
+    V = torch.cat(Vs)
+    del Ks, Vs
+    sl = torch.cat(slots).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        tq.encode_k(cache.params, d, K, sl, cache.k_pool, status=status)
+        if ev is not None:
+            ev[1].record(stream)
+        tq.encode_v(cache.params, d, V, sl, cache.v_pool, status=status)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the encode")
+    ms = statistics.mean(a.elapsed_time(c) for a, _, c in evs)
+    kms = statistics.mean(a.elapsed_time(b) for a, b, _ in evs)
+    vms = statistics.mean(b.elapsed_time(c) for _, b, c in evs)
+    in_b = 2 if w.dtype == "bf16" else 4
+    krec, vrec = (8 * d + 64) / 16, (6 * d + 32) / 16
+    kbytes = ntok * Hkv * (d * in_b + krec)
+    vbytes = ntok * Hkv * (d * in_b + vrec)
+    peak, _ = measured_peak()
+    res = {"config": {"workload": w.name, "sequences": w.batch, "tokens_per_sequence": w.prefill_lens[0],
+                      "n_kv_heads": Hkv, "head_dim": d, "kv_dtype_in": w.dtype, "k_scales": w.k_scale,
+                      "l2": f"inputs {(K.numel() + V.numel()) * in_b / 2**20:.0f} MiB > L2, no flush needed"},
+           "value": round(ntok / (ms * 1e-3) / 1e6, 3), "unit": "Mtok/s",
+           "gbs": round((kbytes + vbytes) / (ms * 1e-3) / 1e9, 3), "ms_per_step": round(ms, 6),
+           "steps": steps, "warmup": warmup, "launches_per_step": 2,
+           "roofline": {"bound": "hbm", "peak": peak, "unit": "GB/s",
+                        "k": {"kernel_ms": round(kms, 6), "achieved": round(kbytes / (kms * 1e-3) / 1e9, 3),
+                              "frac": round(kbytes / (kms * 1e-3) / 1e9 / peak, 4), "bytes_per_launch": kbytes},
+                        "v": {"kernel_ms": round(vms, 6), "achieved": round(vbytes / (vms * 1e-3) / 1e9, 3),
+                              "frac": round(vbytes / (vms * 1e-3) / 1e9 / peak, 4), "bytes_per_launch": vbytes}}}
+    del K, V, cache
+    torch.cuda.empty_cache()
+    return res
+
+
 def bench_tq(args):
     import numpy as np
     import torch
@@ -392,6 +523,11 @@ def bench_tq(args):
                    "samples": clocks["samples"]},
         "bytes_per_step": nb,
     }
+    if not args.main_only:
+        ksteps = max(3, min(args.steps, 200))
+        line["workloads"] = {"ragged": extra_decode("ragged", ksteps, max(3, args.warmup), dev),
+                             "long256": extra_decode("long256", ksteps, max(3, args.warmup), dev),
+                             "prefill_encode": extra_encode(max(3, min(args.steps, 50)), max(3, args.warmup), dev)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, dt, _ = run_cpu_oracle(w, 3, 1, 2)
         line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": int(os.environ["OMP_NUM_THREADS"]),

@@ -58,7 +58,8 @@ enum { TQ_DTYPE_F32 = 0, TQ_DTYPE_BF16 = 1 };
 
 enum {
     TQ_STATUS_BAD_SLOT = 1,     /* a slot or block id outside [0, num_blocks) was skipped */
-    TQ_STATUS_BAD_PARAMS = 2    /* the params buffer was not initialised for this d */
+    TQ_STATUS_BAD_PARAMS = 2,   /* the params buffer was not initialised for this d */
+    TQ_STATUS_TIMEOUT = 4       /* a device-side wait gave up (bounded); the call's output is invalid */
 };
 
 /* Bytes of one packed record (16 slots, one kv head).

@@ -63,6 +63,21 @@ class PagedCache:
                 tq.encode_v(self.params, w.head_dim, to_device(V, w.dtype, dev), slots, self.v_pool)
         torch.cuda.synchronize(dev)
 
+    def prefill_device(self, chunk: int = 65536):
+        """Like prefill, with inputs drawn on the device (synth.kv_tokens_device)."""
+        import torch
+        w = self.w
+        dev = self.k_pool.device
+        for b in range(w.batch):
+            L = w.prefill_lens[b]
+            for s0 in range(0, L, chunk):
+                n = min(chunk, L - s0)
+                K, V = synth.kv_tokens_device(w, b, s0, n, dev)
+                slots = torch.from_numpy(synth.slots_for(self.block_table_np, b, s0, n)).to(dev)
+                tq.encode_k(self.params, w.head_dim, K, slots, self.k_pool)
+                tq.encode_v(self.params, w.head_dim, V, slots, self.v_pool)
+        torch.cuda.synchronize(dev)
+
     def append_inputs(self, step: int = 0):
         """The token appended by the decode step (position prefill_lens[b]): K/V [B][Hkv][d]."""
         w = self.w

@@ -40,12 +40,17 @@
 
 namespace tq {
 
-__host__ __device__ constexpr int kPartStride(int d) { return d + 4; }   // m, l, pad, pad, acc[d]
 // Per (sequence, kv head) query pack: f16x2 B-operand fragments
 // [2 (qbar, u)][d/16 k-steps][2 n-tiles][32 lanes][2 words], then the offset
 // constants [2][8 heads] as floats.
 __host__ __device__ constexpr size_t kPackBytes(int d) { return 64 * (size_t)d + 256; }
 __host__ __device__ constexpr int kPackFloatOff(int d) { return 16 * d; }   // in floats
+
+// head_dim 128 runs on the tcgen05 pass (tq_decode_tc.cu) when TQ_DECODE_TC is 1.
+#ifndef TQ_DECODE_TC
+#define TQ_DECODE_TC 0
+#endif
+constexpr bool kTcPass = TQ_DECODE_TC != 0;
 
 #ifndef TQ_SPLITK_BPW
 #define TQ_SPLITK_BPW 2          // blocks scored per warp per chunk
@@ -54,7 +59,6 @@ __host__ __device__ constexpr int kPackFloatOff(int d) { return 16 * d; }   // i
 #define TQ_SPLITK_MINBLOCKS 4    // resident CTAs per SM the register budget is sized for (4-warp CTAs)
 #endif
 constexpr int kCtasPerSm = 4;              // persistent CTAs per SM (at most)
-constexpr int kMaxSms = 160;               // SMs the pass uses at most (GB300 has 152); bounds the workspace
 
 // warps of the pass for a group of G query heads, and tokens per chunk
 __host__ __device__ constexpr int pass_warps(int G) { return G <= 4 ? 4 : 8; }
@@ -72,11 +76,12 @@ struct WsLayout {
     int32_t *cta_b;
     float *part;
 };
-__host__ __device__ inline size_t ws_sizes(int d, int batch, int hq, size_t *off) {
+inline size_t ws_sizes(int d, int batch, int hq, size_t *off) {
     const int gmax = hq < 8 ? hq : 8;
     const size_t pmax = (size_t)kCtasPerSm * kMaxSms;
+    const size_t per_head = (kTcPass && d == 128) ? tc_pack_bytes_per_head() : kPackBytes(d);
     off[0] = 0;
-    off[1] = off[0] + align256((size_t)batch * hq * kPackBytes(d));
+    off[1] = off[0] + align256((size_t)batch * hq * per_head);
     off[2] = off[1] + align256((size_t)batch * hq * 4);
     off[3] = off[2] + align256(((size_t)batch + 1) * 8);
     off[4] = off[3] + align256(pmax * 4);
@@ -96,11 +101,6 @@ WsLayout ws_layout(void *ws, int d, int batch, int hq) {
                     reinterpret_cast<float *>(base + off[4])};
 }
 
-// Stream-K ranges: CTA c of P covers global chunks [sk_begin(c), sk_begin(c+1)).
-__host__ __device__ inline int64_t sk_begin(int c, int P, int64_t W) { return (int64_t)c * W / P; }
-// the CTA whose range holds chunk x (0 <= x < W)
-__device__ inline int sk_cta_of(int64_t x, int P, int64_t W) { return (int)(((x + 1) * P - 1) / W); }
-__device__ inline int clamp_len(int L, int max_ctx) { return L < 0 ? 0 : (L > max_ctx ? max_ctx : L); }
 
 namespace {
 
@@ -113,12 +113,6 @@ __host__ __device__ constexpr float op_alpha(int q) { return q == 14 ? 0.f : 1.f
 __host__ __device__ constexpr float op_delta(int q) {
     return q == 8 ? 0.25f : q == 9 ? 0.5f : q == 10 ? -0.5f : q == 11 ? -0.75f
          : q == 12 ? -0.9375f : q == 13 ? -0.99609375f : q == 14 ? 2.0f : -2.0f;
-}
-// (w & mask) ^ base as a single LOP3 (base held in a register by the caller)
-__device__ __forceinline__ uint32_t lop_and_xor(uint32_t w, uint32_t mask, uint32_t base) {
-    uint32_t d;
-    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(w), "r"(mask), "r"(base));
-    return d;
 }
 
 __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -135,28 +129,7 @@ __device__ __forceinline__ int scale_exp(float x) {
     return 8 - ex;
 }
 
-__device__ __forceinline__ float warp_max(float x) {
-#pragma unroll
-    for (int m = 16; m > 0; m >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, m));
-    return x;
-}
 
-// Walsh coefficients A0..A3 of the 8 levels (c[k] = sum_m A_m sigma_m(k)).
-__device__ __forceinline__ void walsh4(const float *cen, float (&A)[4]) {
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float s0 = (k & 1) ? 1.f : -1.f, s1 = (k & 2) ? 1.f : -1.f, s2 = (k & 4) ? 1.f : -1.f;
-        a0 += cen[k] * s0;
-        a1 += cen[k] * s1;
-        a2 += cen[k] * s2;
-        a3 += cen[k] * s0 * s1 * s2;
-    }
-    A[0] = a0 * 0.125f;
-    A[1] = a1 * 0.125f;
-    A[2] = a2 * 0.125f;
-    A[3] = a3 * 0.125f;
-}
 
 // ---------------------------------------------------------------- (1) query prep
 // A CTA handles kQRows (sequence, query head) rows, one per warp: each warp
@@ -172,51 +145,6 @@ template <int D> __host__ __device__ constexpr size_t qprep_smem() {
     return (size_t)2 * kQRows * D * 4 + (size_t)(D / qprep_st_rows<D>() > 1 ? 2 : 1) * qprep_st_rows<D>() * D * 4;
 }
 
-// Chunk prefix over sequences (cpre[b] = first global chunk of sequence b's
-// first kv head, cpre[B] = W chunks in all) and the sequence holding the
-// first chunk of each of the P CTAs of the pass.  One CTA of 128 threads.
-__device__ void build_schedule(const int32_t *__restrict__ ctx_lens, int batch, int hkv, int max_ctx, int chunk,
-                               int P, int64_t *__restrict__ cpre, int32_t *__restrict__ cta_b) {
-    // P is the pass's grid size; with fewer chunks than CTAs only W CTAs get work
-    __shared__ int64_t s_wsum[4];
-    __shared__ int64_t s_carry;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        s_carry = 0;
-        cpre[0] = 0;
-    }
-    __syncthreads();
-    for (int base = 0; base < batch; base += 128) {
-        const int b = base + threadIdx.x;
-        int64_t x = 0;
-        if (b < batch) x = (int64_t)hkv * ((clamp_len(ctx_lens[b], max_ctx) + chunk - 1) / chunk);
-#pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {      // inclusive warp scan
-            const int64_t y = __shfl_up_sync(0xffffffffu, x, m);
-            if (lane >= m) x += y;
-        }
-        if (lane == 31) s_wsum[warp] = x;
-        __syncthreads();
-        int64_t off = s_carry;
-        for (int w = 0; w < warp; ++w) off += s_wsum[w];
-        if (b < batch) cpre[b + 1] = off + x;
-        __syncthreads();                        // every thread has read s_carry and s_wsum
-        if (threadIdx.x == 127) s_carry = off + x;
-        __syncthreads();
-    }
-    const int64_t W = s_carry;
-    if (W < P) P = (int)W;                      // at least one chunk per CTA (the pass does the same)
-    for (int c = threadIdx.x; c < P; c += 128) {
-        const int64_t g0 = sk_begin(c, P, W);
-        int lo = 0, hi = batch - 1;             // first b with cpre[b+1] > g0
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (cpre[mid + 1] > g0) hi = mid;
-            else lo = mid + 1;
-        }
-        cta_b[c] = lo;
-    }
-}
 
 template <int D, int NTK, typename T>
 __global__ void __launch_bounds__(128)
@@ -889,6 +817,12 @@ cudaError_t pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int
 cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv,
                          const int32_t *ctx_lens, int max_ctx, void *ws, cudaStream_t st) {
     const WsLayout w = ws_layout(ws, d, batch, hq);
+    if (kTcPass && d == 128) {
+        const int nctas = tc_pass_ctas();
+        if (nctas <= 0) return cudaErrorInvalidConfiguration;
+        return launch_qprep_tc(dtype, params, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w.packs, w.counters,
+                               w.cpre, w.cta_b, st);
+    }
     const int nctas = pass_ctas_any(d, hq / hkv);
     if (nctas <= 0) return cudaErrorInvalidConfiguration;
     const uint8_t *P = (const uint8_t *)params;
@@ -907,6 +841,12 @@ cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv,
                           cudaStream_t st) {
     const WsLayout w = ws_layout(ws, d, batch, hq);
     const int G = hq / hkv;
+    if (kTcPass && d == 128) {
+        const int nctas = tc_pass_ctas();
+        if (nctas <= 0) return cudaErrorInvalidConfiguration;
+        return launch_pass_tc(nctas, params, batch, hq, hkv, k_pool, v_pool, num_blocks, block_table, max_blocks,
+                              ctx_lens, max_ctx, w.packs, w.cpre, w.cta_b, w.part, w.counters, out, status, st);
+    }
     const int nctas = pass_ctas_any(d, G);
     if (nctas <= 0) return cudaErrorInvalidConfiguration;
     const uint8_t *P = (const uint8_t *)params;

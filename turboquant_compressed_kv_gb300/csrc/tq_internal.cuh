@@ -116,6 +116,29 @@ __device__ __forceinline__ float warp_sum(float x) {
     return x;
 }
 
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, m));
+    return x;
+}
+
+// Walsh coefficients A0..A3 of the 8 levels (c[k] = sum_m A_m sigma_m(k)).
+__device__ __forceinline__ void walsh4(const float *cen, float (&A)[4]) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float s0 = (k & 1) ? 1.f : -1.f, s1 = (k & 2) ? 1.f : -1.f, s2 = (k & 4) ? 1.f : -1.f;
+        a0 += cen[k] * s0;
+        a1 += cen[k] * s1;
+        a2 += cen[k] * s2;
+        a3 += cen[k] * s0 * s1 * s2;
+    }
+    A[0] = a0 * 0.125f;
+    A[1] = a1 * 0.125f;
+    A[2] = a2 * 0.125f;
+    A[3] = a3 * 0.125f;
+}
+
 __device__ __forceinline__ void flag_status(int32_t *status, int bits) {
     if (status) atomicOr(status, bits);
 }
@@ -192,6 +215,69 @@ __device__ __forceinline__ void project_streamed(const float *gST, float *sbuf, 
     }
 }
 
+// ---------------------------------------------------------------- decode work split (stream-K)
+__host__ __device__ constexpr int kPartStride(int d) { return d + 4; }   // partial: m, l, pad, pad, acc[d]
+constexpr int kMaxSms = 160;               // SMs a decode pass uses at most (GB300 has 152); bounds the workspace
+
+// Stream-K ranges: CTA c of P covers global chunks [sk_begin(c), sk_begin(c+1)).
+__host__ __device__ inline int64_t sk_begin(int c, int P, int64_t W) { return (int64_t)c * W / P; }
+// the CTA whose range holds chunk x (0 <= x < W)
+__device__ inline int sk_cta_of(int64_t x, int P, int64_t W) { return (int)(((x + 1) * P - 1) / W); }
+__device__ inline int clamp_len(int L, int max_ctx) { return L < 0 ? 0 : (L > max_ctx ? max_ctx : L); }
+
+// (w & mask) ^ base as a single LOP3 (base held in a register by the caller)
+__device__ __forceinline__ uint32_t lop_and_xor(uint32_t w, uint32_t mask, uint32_t base) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(w), "r"(mask), "r"(base));
+    return d;
+}
+
+// Chunk prefix over sequences (cpre[b] = first global chunk of sequence b's
+// first kv head, cpre[B] = W chunks in all) and the sequence holding the
+// first chunk of each of the P CTAs of the pass.  One CTA of 128 threads.
+__device__ inline void build_schedule(const int32_t *__restrict__ ctx_lens, int batch, int hkv, int max_ctx, int chunk,
+                               int P, int64_t *__restrict__ cpre, int32_t *__restrict__ cta_b) {
+    // P is the pass's grid size; with fewer chunks than CTAs only W CTAs get work
+    __shared__ int64_t s_wsum[4];
+    __shared__ int64_t s_carry;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        s_carry = 0;
+        cpre[0] = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < batch; base += 128) {
+        const int b = base + threadIdx.x;
+        int64_t x = 0;
+        if (b < batch) x = (int64_t)hkv * ((clamp_len(ctx_lens[b], max_ctx) + chunk - 1) / chunk);
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {      // inclusive warp scan
+            const int64_t y = __shfl_up_sync(0xffffffffu, x, m);
+            if (lane >= m) x += y;
+        }
+        if (lane == 31) s_wsum[warp] = x;
+        __syncthreads();
+        int64_t off = s_carry;
+        for (int w = 0; w < warp; ++w) off += s_wsum[w];
+        if (b < batch) cpre[b + 1] = off + x;
+        __syncthreads();                        // every thread has read s_carry and s_wsum
+        if (threadIdx.x == 127) s_carry = off + x;
+        __syncthreads();
+    }
+    const int64_t W = s_carry;
+    if (W < P) P = (int)W;                      // at least one chunk per CTA (the pass does the same)
+    for (int c = threadIdx.x; c < P; c += 128) {
+        const int64_t g0 = sk_begin(c, P, W);
+        int lo = 0, hi = batch - 1;             // first b with cpre[b+1] > g0
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (cpre[mid + 1] > g0) hi = mid;
+            else lo = mid + 1;
+        }
+        cta_b[c] = lo;
+    }
+}
+
 // ---------------------------------------------------------------- launchers (defined in the .cu files)
 
 cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const void *x, int64_t n_tokens,
@@ -201,6 +287,17 @@ cudaError_t launch_append(int d, int dtype, const void *params, const void *k_ne
                           int n_heads, const int32_t *bt, int max_blocks, const int32_t *ctx, void *kp, void *vp,
                           int64_t num_blocks, int32_t *status, cudaStream_t st);
 size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx);
+// tcgen05 decode at d = 128 (tq_decode_tc.cu)
+int tc_pass_ctas();
+size_t tc_pack_bytes_per_head();
+cudaError_t launch_qprep_tc(int dtype, const void *params, const void *q, int batch, int hq, int hkv,
+                            const int32_t *ctx_lens, int max_ctx, int nctas, uint8_t *packs, unsigned int *counters,
+                            int64_t *cpre, int32_t *cta_b, cudaStream_t st);
+cudaError_t launch_pass_tc(int nctas, const void *params, int batch, int hq, int hkv, const void *k_pool,
+                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
+                           const int32_t *ctx_lens, int max_ctx, const uint8_t *packs, const int64_t *cpre,
+                           const int32_t *cta_b, float *part, unsigned int *counters, float *out, int32_t *status,
+                           cudaStream_t st);
 cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv,
                          const int32_t *ctx_lens, int max_ctx, void *ws, cudaStream_t st);
 cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,

@@ -168,3 +168,21 @@ def block_tables(w: Workload):
 def slots_for(bt: np.ndarray, b: int, start: int, count: int) -> np.ndarray:
     j = np.arange(start, start + count)
     return (bt[b, j // BLOCK].astype(np.int64) * BLOCK + (j % BLOCK)).astype(np.int64)
+
+
+def kv_tokens_device(w: Workload, b: int, start: int, count: int, device):
+    """K and V of tokens [start, start+count) of sequence b drawn on the device:
+    the same distributions as kv_tokens (N(0,1), K times k_channel_scale,
+    rounded to the input dtype), from torch's seeded CUDA generator instead of
+    numpy's, so that the large throughput workloads need no host-side draws.
+    Returns two tensors [count][Hkv][d] in the input dtype (bf16 or fp32).
+    The values differ from kv_tokens'; tests use kv_tokens."""
+    import torch
+    d, H = w.head_dim, w.n_kv_heads
+    g = torch.Generator(device=device)
+    g.manual_seed(((w.seed * 1_000_003 + b) * 1_000_003 + start) & 0x7FFFFFFFFFFFFFFF)
+    scale = torch.from_numpy(k_channel_scale(w)).to(device)
+    K = torch.randn((count, H, d), generator=g, device=device, dtype=torch.float32) * scale
+    V = torch.randn((count, H, d), generator=g, device=device, dtype=torch.float32)
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    return K.to(dt), V.to(dt)
