@@ -46,12 +46,6 @@ namespace tq {
 __host__ __device__ constexpr size_t kPackBytes(int d) { return 64 * (size_t)d + 256; }
 __host__ __device__ constexpr int kPackFloatOff(int d) { return 16 * d; }   // in floats
 
-// head_dim 128 runs on the tcgen05 pass (tq_decode_tc.cu) when TQ_DECODE_TC is 1.
-#ifndef TQ_DECODE_TC
-#define TQ_DECODE_TC 0
-#endif
-constexpr bool kTcPass = TQ_DECODE_TC != 0;
-
 #ifndef TQ_SPLITK_BPW
 #define TQ_SPLITK_BPW 2          // blocks scored per warp per chunk
 #endif
@@ -79,7 +73,7 @@ struct WsLayout {
 inline size_t ws_sizes(int d, int batch, int hq, size_t *off) {
     const int gmax = hq < 8 ? hq : 8;
     const size_t pmax = (size_t)kCtasPerSm * kMaxSms;
-    const size_t per_head = (kTcPass && d == 128) ? tc_pack_bytes_per_head() : kPackBytes(d);
+    const size_t per_head = kPackBytes(d);
     off[0] = 0;
     off[1] = off[0] + align256((size_t)batch * hq * per_head);
     off[2] = off[1] + align256((size_t)batch * hq * 4);
@@ -817,12 +811,6 @@ cudaError_t pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int
 cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv,
                          const int32_t *ctx_lens, int max_ctx, void *ws, cudaStream_t st) {
     const WsLayout w = ws_layout(ws, d, batch, hq);
-    if (kTcPass && d == 128) {
-        const int nctas = tc_pass_ctas();
-        if (nctas <= 0) return cudaErrorInvalidConfiguration;
-        return launch_qprep_tc(dtype, params, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w.packs, w.counters,
-                               w.cpre, w.cta_b, st);
-    }
     const int nctas = pass_ctas_any(d, hq / hkv);
     if (nctas <= 0) return cudaErrorInvalidConfiguration;
     const uint8_t *P = (const uint8_t *)params;
@@ -841,12 +829,6 @@ cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv,
                           cudaStream_t st) {
     const WsLayout w = ws_layout(ws, d, batch, hq);
     const int G = hq / hkv;
-    if (kTcPass && d == 128) {
-        const int nctas = tc_pass_ctas();
-        if (nctas <= 0) return cudaErrorInvalidConfiguration;
-        return launch_pass_tc(nctas, params, batch, hq, hkv, k_pool, v_pool, num_blocks, block_table, max_blocks,
-                              ctx_lens, max_ctx, w.packs, w.cpre, w.cta_b, w.part, w.counters, out, status, st);
-    }
     const int nctas = pass_ctas_any(d, G);
     if (nctas <= 0) return cudaErrorInvalidConfiguration;
     const uint8_t *P = (const uint8_t *)params;

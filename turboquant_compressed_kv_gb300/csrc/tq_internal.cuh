@@ -287,17 +287,6 @@ cudaError_t launch_append(int d, int dtype, const void *params, const void *k_ne
                           int n_heads, const int32_t *bt, int max_blocks, const int32_t *ctx, void *kp, void *vp,
                           int64_t num_blocks, int32_t *status, cudaStream_t st);
 size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx);
-// tcgen05 decode at d = 128 (tq_decode_tc.cu)
-int tc_pass_ctas();
-size_t tc_pack_bytes_per_head();
-cudaError_t launch_qprep_tc(int dtype, const void *params, const void *q, int batch, int hq, int hkv,
-                            const int32_t *ctx_lens, int max_ctx, int nctas, uint8_t *packs, unsigned int *counters,
-                            int64_t *cpre, int32_t *cta_b, cudaStream_t st);
-cudaError_t launch_pass_tc(int nctas, const void *params, int batch, int hq, int hkv, const void *k_pool,
-                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
-                           const int32_t *ctx_lens, int max_ctx, const uint8_t *packs, const int64_t *cpre,
-                           const int32_t *cta_b, float *part, unsigned int *counters, float *out, int32_t *status,
-                           cudaStream_t st);
 cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv,
                          const int32_t *ctx_lens, int max_ctx, void *ws, cudaStream_t st);
 cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
