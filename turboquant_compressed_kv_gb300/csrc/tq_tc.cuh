@@ -135,3 +135,33 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 
 }  // namespace tc
 }  // namespace tq
+
+namespace tq {
+namespace tc {
+
+// ---------------------------------------------------------------- f16 operands, 128-byte swizzle
+// K-major operand of 2-byte elements with 128-byte swizzling: the K extent is cut into blocks of
+// 64 elements (one 128-byte row each); block kb holds all `rows` rows, 8-row groups 1024 bytes
+// apart, and 16-byte chunk c of row r sits at chunk position c ^ (r % 8).  The base must be
+// 1024-byte aligned.
+__host__ __device__ constexpr int sw128_off(int r, int k, int rows) {
+    return (k >> 6) * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + ((((k & 63) >> 3) ^ (r & 7)) << 4) + (k & 7) * 2;
+}
+// Descriptor of K-step ks (16 elements) of such an operand.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t base, int ks, int rows) {
+    const uint32_t a = base + (uint32_t)((ks >> 2) * rows * 128 + (ks & 3) * 32);
+    return (uint64_t)((a >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) |
+           ((uint64_t)2 << 61);
+}
+// Instruction descriptor of kind::f16 with f16 A and B, f32 accumulator, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int m, int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+// D[tmem] (+)= A[smem] x B[smem]; issued by one thread.
+__device__ __forceinline__ void mma_ss_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, bool acc) {
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+                 ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)acc));
+}
+
+}  // namespace tc
+}  // namespace tq
