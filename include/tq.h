@@ -185,6 +185,25 @@ int tq_decode_splitk(const void *params, int d, int batch, int n_q_heads, int n_
                      int max_ctx, float *out, void *workspace, size_t workspace_bytes,
                      int32_t *status, tq_stream_t stream);
 
+/* tq_decode_step -- one decode step: append one token per sequence, then attend.
+ * [VLLM "Paged KVキャッシュ" (the slot of the new token); README "The Algorithm" (its
+ *  encoding); then tq_decode_attn over the grown cache]
+ * For each sequence b with pre_lens[b] >= 0: K and V of the new token (k_new[b], v_new[b])
+ * are encoded into the slot of position pre_lens[b] (as tq_paged_append), and query head h
+ * of sequence b attends the pre_lens[b] + 1 tokens (as tq_decode_attn, clamped to
+ * max_ctx).  A sequence with pre_lens[b] < 0 appends nothing and gets out = 0.
+ * The append and the query preparation run in one launch, followed by the split-K pass;
+ * the result equals tq_paged_append followed by tq_decode_attn with ctx_lens = pre_lens + 1.
+ *   k_new, v_new  device [batch][n_kv_heads][d] in dtype;  q  device [batch][n_q_heads][d].
+ *   pre_lens      device int32[batch].
+ *   workspace     >= tq_decode_workspace_bytes(d, batch, n_q_heads, max_ctx) bytes.
+ * Errors: as tq_paged_append and tq_decode_attn. */
+int tq_decode_step(const void *params, int d, const void *k_new, const void *v_new, const void *q, int dtype,
+                   int batch, int n_q_heads, int n_kv_heads, const int32_t *block_table, int max_blocks,
+                   const int32_t *pre_lens, int max_ctx, void *k_pool, void *v_pool, int64_t num_blocks,
+                   float *out, void *workspace, size_t workspace_bytes, int32_t *status,
+                   tq_stream_t stream);
+
 /* tq_decode_attn_noalloc -- tq_decode_attn without a caller workspace.
  * The pages have no counterpart to this call; it exists for callers that
  * cannot allocate device memory when they decode: a serving runtime that

@@ -238,6 +238,63 @@ def test_decode_stages_equal_decode_attn():
         assert torch.equal(got, want)
 
 
+@pytest.mark.parametrize("d,Hq,Hkv,dtype", [(128, 8, 2, "bf16"), (128, 4, 4, "f32"), (256, 4, 2, "bf16")])
+def test_decode_step_appends_then_attends(d, Hq, Hkv, dtype):
+    """tq_decode_step on a cache of pre_lens[b] tokens equals the oracle's attention over
+    pre_lens[b] + 1 tokens (the oracle encodes every token itself, the new one included),
+    and equals tq_paged_append followed by tq_decode_attn bit for bit."""
+    pre = [15, 600, -1, 129, 0, 1023]
+    B = len(pre)
+    full = [p + 1 if p >= 0 else 0 for p in pre]
+    D, S, params, _ = _params(d)
+    need = [max(1, -(-L // 16)) for L in full]
+    nblk = sum(need) + 2
+    perm = np.random.default_rng(17).permutation(nblk)
+    bt = np.zeros((B, max(need)), np.int32)
+    k0 = 0
+    for b, n in enumerate(need):
+        bt[b, :n] = perm[k0:k0 + n]
+        k0 += n
+    kp_pre = np.zeros((nblk, Hkv, oracle.record_bytes(True, d)), np.uint8)
+    vp_pre = np.zeros((nblk, Hkv, oracle.record_bytes(False, d)), np.uint8)
+    kp_full, vp_full = kp_pre.copy(), vp_pre.copy()
+    k_new = np.zeros((B, Hkv, d), np.float32)
+    v_new = np.zeros((B, Hkv, d), np.float32)
+    for b, L in enumerate(full):
+        if L == 0:
+            continue
+        rng = np.random.default_rng([23, b])
+        K = synth.round_dtype(rng.standard_normal((L, Hkv, d)).astype(np.float32) * 2, dtype)
+        V = synth.round_dtype(rng.standard_normal((L, Hkv, d)).astype(np.float32), dtype)
+        sl = synth.slots_for(bt, b, 0, L)
+        oracle.encode(True, D, S, K, sl, kp_full)
+        oracle.encode(False, D, S, V, sl, vp_full)
+        if L > 1:
+            oracle.encode(True, D, S, K[:-1], sl[:-1], kp_pre)
+            oracle.encode(False, D, S, V[:-1], sl[:-1], vp_pre)
+        k_new[b], v_new[b] = K[-1], V[-1]
+    q = synth.round_dtype(np.random.default_rng(29).standard_normal((B, Hq, d)).astype(np.float32), dtype)
+    max_ctx = max(full)
+    dq, dk, dv = _upload(q, dtype), _upload(k_new, dtype), _upload(v_new, dtype)
+    dbt = torch.from_numpy(bt).to(DEV)
+    pre_t = torch.tensor(pre, dtype=torch.int32, device=DEV)
+    kp1, vp1 = torch.from_numpy(kp_pre).to(DEV), torch.from_numpy(vp_pre).to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = tq.decode_step(params, d, dk, dv, dq, Hkv, kp1, vp1, dbt, pre_t, max_ctx, status=status)
+    kp2, vp2 = torch.from_numpy(kp_pre).to(DEV), torch.from_numpy(vp_pre).to(DEV)
+    tq.paged_append(params, d, dk, dv, dbt, pre_t, kp2, vp2)
+    full_t = torch.tensor(full, dtype=torch.int32, device=DEV)
+    want = tq.decode_attn(params, d, dq, Hkv, kp2, vp2, dbt, full_t, max_ctx)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(kp1, kp2) and torch.equal(vp1, vp2)
+    assert torch.equal(out, want)
+    ref = oracle.decode(D, S, q, Hkv, kp_full, vp_full, bt, np.array(full, np.int32))
+    o = out.cpu().numpy()
+    assert np.all(o[pre.index(-1)] == 0)
+    parity.check_attention(o, ref)
+
+
 def test_tiny_workload_end_to_end():
     """1 sequence, 1 head, d=128, 256 fp32 tokens with 20x outlier channels:
     GPU encode vs oracle encode, then GPU decode vs oracle decode of the

@@ -78,6 +78,9 @@ def _declare(L):
     L.tq_decode_qprep.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _I, _P, _SZ, _P]
     L.tq_decode_splitk.restype = _I
     L.tq_decode_splitk.argtypes = [_P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _SZ, _P, _P]
+    L.tq_decode_step.restype = _I
+    L.tq_decode_step.argtypes = [_P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _P, _P, _I64, _P, _P, _SZ, _P,
+                                 _P]
     L.tq_decode_attn_noalloc.restype = _I
     L.tq_decode_attn_noalloc.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _P]
 
@@ -239,6 +242,27 @@ def decode_splitk(params, d: int, batch: int, n_q_heads: int, n_kv_heads: int, k
                                          _ptr(ctx_lens), max_ctx, _ptr(out), _ptr(workspace), workspace.numel(),
                                          _ptr(status), _stream(stream))
     _check(rc, "tq_decode_splitk")
+
+
+def decode_step(params, d: int, k_new, v_new, q, n_kv_heads: int, k_pool, v_pool, block_table, pre_lens,
+                max_ctx: int, out=None, workspace=None, status=None, stream=None):
+    """tq_decode_step: append (k_new, v_new) at position pre_lens[b], then attend pre_lens[b] + 1 tokens."""
+    torch = _torch()
+    _need_cuda(params, k_new, v_new, q, k_pool, v_pool, block_table, pre_lens, out, workspace, status)
+    B, Hq = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes(d, B, Hq, max_ctx)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if k_new.dtype != q.dtype or v_new.dtype != q.dtype:
+        raise TQError("k_new, v_new and q must share one dtype")
+    rc = load_library().tq_decode_step(_ptr(params), d, _ptr(k_new), _ptr(v_new), _ptr(q), _dtype_code(q), B, Hq,
+                                       n_kv_heads, _ptr(block_table), block_table.shape[1], _ptr(pre_lens), max_ctx,
+                                       _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(out), _ptr(workspace),
+                                       workspace.numel(), _ptr(status), _stream(stream))
+    _check(rc, "tq_decode_step")
+    return out
 
 
 def decode_attn_noalloc(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens, max_ctx: int,

@@ -201,7 +201,7 @@ int tq_decode_splitk(const void *params, int d, int batch, int n_q_heads, int n_
     if (!k_pool || !v_pool || !block_table || !ctx_lens || !out) return TQ_ERR_INVALID;
     if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
     return cuda_status(launch_splitk(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks,
-                                     block_table, max_blocks, ctx_lens, max_ctx, out, workspace, status,
+                                     block_table, max_blocks, ctx_lens, 0, max_ctx, out, workspace, status,
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -219,8 +219,23 @@ int tq_decode_attn(const void *params, int d, const void *q, int dtype, int batc
     cudaError_t e = launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx, workspace, st);
     if (e == cudaSuccess)
         e = launch_splitk(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
-                          max_blocks, ctx_lens, max_ctx, out, workspace, status, st);
+                          max_blocks, ctx_lens, 0, max_ctx, out, workspace, status, st);
     return cuda_status(e);
+}
+
+int tq_decode_step(const void *params, int d, const void *k_new, const void *v_new, const void *q, int dtype,
+                   int batch, int n_q_heads, int n_kv_heads, const int32_t *block_table, int max_blocks,
+                   const int32_t *pre_lens, int max_ctx, void *k_pool, void *v_pool, int64_t num_blocks, float *out,
+                   void *workspace, size_t workspace_bytes, int32_t *status, tq_stream_t stream) {
+    if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16 && valid_d(d)) return TQ_ERR_DTYPE;
+    int rc = check_decode(params, d, batch, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
+    if (rc != TQ_OK || batch == 0) return rc;
+    if (max_blocks <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
+    if (!k_new || !v_new || !q || !k_pool || !v_pool || !block_table || !pre_lens || !out) return TQ_ERR_INVALID;
+    if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
+    return cuda_status(launch_step(d, dtype, params, k_new, v_new, q, batch, n_q_heads, n_kv_heads, block_table,
+                                   max_blocks, pre_lens, max_ctx, k_pool, v_pool, num_blocks, out, workspace, status,
+                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

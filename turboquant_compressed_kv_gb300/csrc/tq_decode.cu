@@ -37,14 +37,9 @@
 #include <atomic>
 
 #include "tq_internal.cuh"
+#include "tq_prep.cuh"
 
 namespace tq {
-
-// Per (sequence, kv head) query pack: f16x2 B-operand fragments
-// [2 (qbar, u)][d/16 k-steps][2 n-tiles][32 lanes][2 words], then the offset
-// constants [2][8 heads] as floats.
-__host__ __device__ constexpr size_t kPackBytes(int d) { return 64 * (size_t)d + 256; }
-__host__ __device__ constexpr int kPackFloatOff(int d) { return 16 * d; }   // in floats
 
 #ifndef TQ_SPLITK_BPW
 #define TQ_SPLITK_BPW 2          // blocks scored per warp per chunk
@@ -98,133 +93,15 @@ WsLayout ws_layout(void *ws, int d, int batch, int hq) {
 
 namespace {
 
-// ---------------------------------------------------------------- f16 operand helpers
-
-// Operand bit position q (8..15 within each f16 half): mask, base, and the
-// operand values alpha (bit clear) and alpha + delta (bit set).
-__host__ __device__ constexpr uint32_t op_mask(int q) { return 0x00010001u << q; }
-__host__ __device__ constexpr float op_alpha(int q) { return q == 14 ? 0.f : 1.f; }
-__host__ __device__ constexpr float op_delta(int q) {
-    return q == 8 ? 0.25f : q == 9 ? 0.5f : q == 10 ? -0.5f : q == 11 ? -0.75f
-         : q == 12 ? -0.9375f : q == 13 ? -0.99609375f : q == 14 ? 2.0f : -2.0f;
-}
-
-__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                        uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// exponent e with x * 2^e in [128, 256) for x > 0
-__device__ __forceinline__ int scale_exp(float x) {
-    int ex;
-    frexpf(x, &ex);
-    return 8 - ex;
-}
-
-
-
-// ---------------------------------------------------------------- (1) query prep
-// A CTA handles kQRows (sequence, query head) rows, one per warp: each warp
-// rotates its row (qbar = Pi q), then thread k computes u_k = (S qbar)_k for
-// every row from S^T staged in shared memory (all of it in one copy at d=128,
-// two 64-row chunks in flight at d=256), then each warp writes its row's hi
-// and lo columns (2*hg, 2*hg+1) of the K-side B operand for qbar (qu=0) and
-// u (qu=1) into the pack of the row's (sequence, kv head), and the offset
-// constants.  CTA 0 also lays out the pass's work (build_schedule).
-constexpr int kQRows = 4;
-template <int D> __host__ __device__ constexpr int qprep_st_rows() { return D == 128 ? 128 : 64; }
-template <int D> __host__ __device__ constexpr size_t qprep_smem() {
-    return (size_t)2 * kQRows * D * 4 + (size_t)(D / qprep_st_rows<D>() > 1 ? 2 : 1) * qprep_st_rows<D>() * D * 4;
-}
-
-
+// ---------------------------------------------------------------- (1) query prep (body in tq_prep.cuh)
 template <int D, int NTK, typename T>
 __global__ void __launch_bounds__(128)
 qprep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ q, int batch, int hq, int hkv,
              const int32_t *__restrict__ ctx_lens, int max_ctx, int chunk, int P, uint8_t *__restrict__ packs,
              unsigned int *__restrict__ counters, int64_t *__restrict__ cpre, int32_t *__restrict__ cta_b) {
-    constexpr int R = D / 32, NKS = D / 16, KPT = D / 128;
     extern __shared__ __align__(16) uint8_t qsm[];
-    float (*qs)[D] = reinterpret_cast<float (*)[D]>(qsm);                       // [kQRows][D] qbar
-    float (*us)[D] = reinterpret_cast<float (*)[D]>(qsm + kQRows * D * 4);      // [kQRows][D] u
-    float *sbuf = reinterpret_cast<float *>(qsm + 2 * kQRows * D * 4);         // S^T rows
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nrows = batch * hq, row0 = blockIdx.x * kQRows;
-    const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
-    const float *ST = reinterpret_cast<const float *>(params + params_off_ST(D));
-    const float inv_sd = rsqrtf((float)D);
-    {
-        const int row = row0 + warp;
-        float v[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-            v[r] = (row < nrows) ? to_f32<T>(q[(size_t)row * D + 32 * r + lane]) * __ldg(Dsign + 32 * r + lane) : 0.f;
-        fwht_warp<R>(v, lane);
-#pragma unroll
-        for (int r = 0; r < R; ++r) qs[warp][32 * r + lane] = v[r] * inv_sd;   // qbar = H D q / sqrt d
-    }
-    {
-        float acc[KPT][kQRows];
-#pragma unroll
-        for (int u = 0; u < KPT; ++u)
-#pragma unroll
-            for (int rr = 0; rr < kQRows; ++rr) acc[u][rr] = 0.f;
-        project_streamed<D, kQRows, 128, qprep_st_rows<D>()>(ST, sbuf, qs, acc);     // u = S qbar
-#pragma unroll
-        for (int u = 0; u < KPT; ++u)
-#pragma unroll
-            for (int rr = 0; rr < kQRows; ++rr) us[rr][threadIdx.x + 128 * u] = acc[u][rr];
-    }
-    __syncthreads();
-    const int row = row0 + warp;
-    if (row < nrows) {
-        const int b = row / hq, h = row % hq, G = hq / hkv, kvh = h / G, hg = h % G;
-        if (hg == 0 && lane == 0) counters[b * hkv + kvh] = 0u;   // completion counter of the pass
-        float v[R], u[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            v[r] = qs[warp][32 * r + lane];
-            u[r] = us[warp][32 * r + lane];
-        }
-        uint8_t *pack = packs + ((size_t)b * hkv + kvh) * kPackBytes(D);
-        uint16_t *ph = reinterpret_cast<uint16_t *>(pack);
-        float *pf = reinterpret_cast<float *>(pack) + kPackFloatOff(D);
-#pragma unroll
-        for (int qu = 0; qu < 2; ++qu) {
-            float cs = 0.f;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int dim = 32 * r + lane, s = dim >> 4, k = dim & 15, qd = 8 + (s & 7);
-                const float beta = 2.f * (qu == 0 ? v[r] : u[r]) / op_delta(qd);
-                const __half hi = __float2half_rn(beta);
-                const __half lo = __float2half_rn(beta - __half2float(hi));
-                cs = fmaf(__half2float(hi) + __half2float(lo), op_alpha(qd) + 0.5f * op_delta(qd), cs);
-                const int reg = k >> 3, tig = (k & 7) >> 1, e = k & 1;
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const int col = 2 * hg + x, nt = col >> 3, gid = col & 7;
-                    const size_t word = ((size_t)(qu * NKS + s) * NTK + nt) * 64 + (4 * gid + tig) * 2 + reg;
-                    ph[word * 2 + e] = __half_as_ushort(x == 0 ? hi : lo);
-                }
-            }
-            cs = warp_sum(cs);
-            if (lane == 0) pf[qu * 8 + hg] = cs;
-        }
-        // columns beyond the group's 2*G are zero (written by the group's first head)
-        if (hg == 0) {
-            uint32_t *pw = reinterpret_cast<uint32_t *>(pack);
-            for (int col = 2 * G; col < 8 * NTK; ++col) {
-                const int nt = col >> 3, gid = col & 7;
-                for (int i = lane; i < 2 * NKS * 8; i += 32) {
-                    const int qu = i / (NKS * 8), s = (i / 8) % NKS, k = i % 8;
-                    pw[((size_t)(qu * NKS + s) * NTK + nt) * 64 + (4 * gid + (k >> 1)) * 2 + (k & 1)] = 0u;
-                }
-            }
-        }
-    }
-    if (blockIdx.x == 0) build_schedule(ctx_lens, batch, hkv, max_ctx, chunk, P, cpre, cta_b);
+    qprep_rows<D, NTK, T>(params, q, batch, hq, hkv, ctx_lens, 0, max_ctx, chunk, P, packs, counters, cpre, cta_b,
+                          blockIdx.x, qsm);
 }
 
 // ---------------------------------------------------------------- (2) split-K pass
@@ -281,7 +158,7 @@ __global__ void __launch_bounds__(NWARP * 32, (NWARP == 4 ? (D == 128 ? TQ_SPLIT
 decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ packs, int batch, int hq, int hkv,
                   const uint8_t *__restrict__ k_pool, const uint8_t *__restrict__ v_pool, int64_t num_blocks,
                   const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_lens,
-                  int max_ctx, const int64_t *__restrict__ cpre, const int32_t *__restrict__ cta_b,
+                  int ctx_add, int max_ctx, const int64_t *__restrict__ cpre, const int32_t *__restrict__ cta_b,
                   float *__restrict__ part, unsigned int *__restrict__ counters, float *__restrict__ out,
                   int32_t *status) {
     using C = SplitCfg<D, NWARP>;
@@ -313,7 +190,7 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
 
     // sequences with nothing to attend get out = 0
     for (int b = cta; b < batch; b += gridDim.x)
-        if (clamp_len(ctx_lens[b], max_ctx) == 0)
+        if (attended_len(ctx_lens[b], ctx_add, max_ctx) == 0)
             for (int i = tid; i < hq * D; i += NT_) out[(size_t)b * hq * D + i] = 0.f;
 
     // P CTAs share the W chunks, at least one chunk each (as in build_schedule)
@@ -355,7 +232,7 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
     while (true) {
         const int64_t us = ub + (int64_t)kh * nchb, ue = us + nchb;
         const int64_t se = (g1 < ue) ? g1 : ue;
-        const int L = clamp_len(ctx_lens[b], max_ctx);
+        const int L = attended_len(ctx_lens[b], ctx_add, max_ctx);
         const int t0 = (int)(g - us) * CH;
         const int t1 = min(L, (int)(se - us) * CH);
 
@@ -777,22 +654,24 @@ cudaError_t qprep_launch(const uint8_t *P, const void *q, int batch, int hq, int
 template <int D, int G>
 cudaError_t pass_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batch, int hq, int hkv,
                           const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
-                          const int32_t *ctx, int max_ctx, const WsLayout &w, float *out, int32_t *status) {
+                          const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
+                          int32_t *status) {
     constexpr int NWARP = pass_warps(G);
     constexpr size_t smem = split_smem_bytes<D, G, NWARP>();
     auto kern = decode_mma_kernel<D, G, NWARP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<nctas, NWARP * 32, smem, st>>>(P, w.packs, batch, hq, hkv, kp, vp, nb, bt, mb, ctx, max_ctx, w.cpre,
-                                         w.cta_b, w.part, w.counters, out, status);
+    kern<<<nctas, NWARP * 32, smem, st>>>(P, w.packs, batch, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx,
+                                         w.cpre, w.cta_b, w.part, w.counters, out, status);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int hq, int hkv,
                         const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
-                        const int32_t *ctx, int max_ctx, const WsLayout &w, float *out, int32_t *status) {
-#define TQ_PASS(GG) return pass_launch_g<D, GG>(nctas, st, P, batch, hq, hkv, kp, vp, nb, bt, mb, ctx, max_ctx, w, out, status)
+                        const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
+                        int32_t *status) {
+#define TQ_PASS(GG) return pass_launch_g<D, GG>(nctas, st, P, batch, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out, status)
     switch (G) {
         case 1: TQ_PASS(1);
         case 2: TQ_PASS(2);
@@ -825,7 +704,7 @@ cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, in
 
 cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
-                          const int32_t *ctx_lens, int max_ctx, float *out, void *ws, int32_t *status,
+                          const int32_t *ctx_lens, int ctx_add, int max_ctx, float *out, void *ws, int32_t *status,
                           cudaStream_t st) {
     const WsLayout w = ws_layout(ws, d, batch, hq);
     const int G = hq / hkv;
@@ -834,9 +713,90 @@ cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv,
     const uint8_t *P = (const uint8_t *)params;
     if (d == 128)
         return pass_launch<128>(G, nctas, st, P, batch, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
-                                num_blocks, block_table, max_blocks, ctx_lens, max_ctx, w, out, status);
+                                num_blocks, block_table, max_blocks, ctx_lens, ctx_add, max_ctx, w, out, status);
     return pass_launch<256>(G, nctas, st, P, batch, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
-                            num_blocks, block_table, max_blocks, ctx_lens, max_ctx, w, out, status);
+                            num_blocks, block_table, max_blocks, ctx_lens, ctx_add, max_ctx, w, out, status);
+}
+
+// ---------------------------------------------------------------- the decode step: append, then attend
+// One launch runs the append of one token per sequence (K tiles, V tiles) and the query prep
+// side by side; the pass follows.  pre_lens[b] is the position of the new token, and the pass
+// attends pre_lens[b] + 1 tokens.
+namespace {
+constexpr int kAppendTile = 4;
+
+template <int D, int NTK, typename T>
+__global__ void __launch_bounds__(128)
+step_prep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ k_new, const T *__restrict__ v_new,
+                 const T *__restrict__ q, int batch, int hq, int hkv, SlotMap map, uint8_t *__restrict__ k_pool,
+                 uint8_t *__restrict__ v_pool, int n_app, int max_ctx, int chunk, int P, uint8_t *__restrict__ packs,
+                 unsigned int *__restrict__ counters, int64_t *__restrict__ cpre, int32_t *__restrict__ cta_b,
+                 int32_t *status) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int blk = blockIdx.x;
+    if (blk < 2 * n_app) {
+        const bool is_k = blk < n_app;
+        encode_tiles<D, kAppendTile, T>(params, is_k ? k_new : v_new, (int64_t)batch * hkv, map,
+                                        is_k ? k_pool : v_pool, is_k, is_k, is_k ? blk : blk - n_app, n_app, smem,
+                                        status);
+    } else {
+        qprep_rows<D, NTK, T>(params, q, batch, hq, hkv, map.ctx_lens, 1, max_ctx, chunk, P, packs, counters, cpre,
+                              cta_b, blk - 2 * n_app, smem);
+    }
+}
+
+template <int D, int NTK, typename T>
+cudaError_t step_prep_launch(const uint8_t *P, const void *k_new, const void *v_new, const void *q, int batch,
+                             int hq, int hkv, const SlotMap &map, void *kp, void *vp, int max_ctx, int nctas,
+                             const WsLayout &w, int32_t *status, cudaStream_t st) {
+    constexpr size_t es = EncSmem<D, kAppendTile>::kBytes, qs = qprep_smem<D>();
+    constexpr size_t smem = es > qs ? es : qs;
+    auto kern = step_prep_kernel<D, NTK, T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int n_app = (batch * hkv + kAppendTile - 1) / kAppendTile;
+    const int n_q = (batch * hq + kQRows - 1) / kQRows;
+    kern<<<2 * n_app + n_q, 128, smem, st>>>(P, (const T *)k_new, (const T *)v_new, (const T *)q, batch, hq, hkv, map,
+                                             (uint8_t *)kp, (uint8_t *)vp, n_app, max_ctx, pass_chunk(hq / hkv),
+                                             nctas, w.packs, w.counters, w.cpre, w.cta_b, status);
+    return cudaGetLastError();
+}
+
+template <int D, typename T>
+cudaError_t step_prep_any(const uint8_t *P, const void *k_new, const void *v_new, const void *q, int batch, int hq,
+                          int hkv, const SlotMap &map, void *kp, void *vp, int max_ctx, int nctas, const WsLayout &w,
+                          int32_t *status, cudaStream_t st) {
+    if (hq / hkv <= 4)
+        return step_prep_launch<D, 1, T>(P, k_new, v_new, q, batch, hq, hkv, map, kp, vp, max_ctx, nctas, w, status, st);
+    return step_prep_launch<D, 2, T>(P, k_new, v_new, q, batch, hq, hkv, map, kp, vp, max_ctx, nctas, w, status, st);
+}
+}  // namespace
+
+cudaError_t launch_step(int d, int dtype, const void *params, const void *k_new, const void *v_new, const void *q,
+                        int batch, int hq, int hkv, const int32_t *block_table, int max_blocks,
+                        const int32_t *pre_lens, int max_ctx, void *k_pool, void *v_pool, int64_t num_blocks,
+                        float *out, void *ws, int32_t *status, cudaStream_t st) {
+    const WsLayout w = ws_layout(ws, d, batch, hq);
+    const int nctas = pass_ctas_any(d, hq / hkv);
+    if (nctas <= 0) return cudaErrorInvalidConfiguration;
+    const uint8_t *P = (const uint8_t *)params;
+    const SlotMap map{nullptr, block_table, pre_lens, max_blocks, num_blocks, hkv};
+    cudaError_t e;
+    if (d == 128)
+        e = dtype == TQ_DTYPE_BF16
+                ? step_prep_any<128, __nv_bfloat16>(P, k_new, v_new, q, batch, hq, hkv, map, k_pool, v_pool, max_ctx,
+                                                    nctas, w, status, st)
+                : step_prep_any<128, float>(P, k_new, v_new, q, batch, hq, hkv, map, k_pool, v_pool, max_ctx, nctas, w,
+                                            status, st);
+    else
+        e = dtype == TQ_DTYPE_BF16
+                ? step_prep_any<256, __nv_bfloat16>(P, k_new, v_new, q, batch, hq, hkv, map, k_pool, v_pool, max_ctx,
+                                                    nctas, w, status, st)
+                : step_prep_any<256, float>(P, k_new, v_new, q, batch, hq, hkv, map, k_pool, v_pool, max_ctx, nctas, w,
+                                            status, st);
+    if (e != cudaSuccess) return e;
+    return launch_splitk(d, params, batch, hq, hkv, k_pool, v_pool, num_blocks, block_table, max_blocks, pre_lens, 1,
+                         max_ctx, out, ws, status, st);
 }
 
 }  // namespace tq

@@ -235,21 +235,32 @@ __device__ __forceinline__ uint32_t lop_and_xor(uint32_t w, uint32_t mask, uint3
 // Chunk prefix over sequences (cpre[b] = first global chunk of sequence b's
 // first kv head, cpre[B] = W chunks in all) and the sequence holding the
 // first chunk of each of the P CTAs of the pass.  One CTA of 128 threads.
-__device__ inline void build_schedule(const int32_t *__restrict__ ctx_lens, int batch, int hkv, int max_ctx, int chunk,
-                               int P, int64_t *__restrict__ cpre, int32_t *__restrict__ cta_b) {
+// Context length attended for sequence b: the stored length c (plus ctx_add, 1 when the
+// step appends a token first), clamped to [0, max_ctx]; c < 0 means nothing to attend.
+__device__ inline int attended_len(int c, int ctx_add, int max_ctx) {
+    return c < 0 ? 0 : clamp_len(c + ctx_add, max_ctx);
+}
+
+constexpr int kSchedCache = 1024;          // sequences whose chunk prefix is searched in shared memory
+
+__device__ inline void build_schedule(const int32_t *__restrict__ ctx_lens, int ctx_add, int batch, int hkv,
+                                      int max_ctx, int chunk, int P, int64_t *__restrict__ cpre,
+                                      int32_t *__restrict__ cta_b) {
     // P is the pass's grid size; with fewer chunks than CTAs only W CTAs get work
     __shared__ int64_t s_wsum[4];
     __shared__ int64_t s_carry;
+    __shared__ int64_t s_cpre[kSchedCache + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         s_carry = 0;
         cpre[0] = 0;
+        s_cpre[0] = 0;
     }
     __syncthreads();
     for (int base = 0; base < batch; base += 128) {
         const int b = base + threadIdx.x;
         int64_t x = 0;
-        if (b < batch) x = (int64_t)hkv * ((clamp_len(ctx_lens[b], max_ctx) + chunk - 1) / chunk);
+        if (b < batch) x = (int64_t)hkv * ((attended_len(ctx_lens[b], ctx_add, max_ctx) + chunk - 1) / chunk);
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1) {      // inclusive warp scan
             const int64_t y = __shfl_up_sync(0xffffffffu, x, m);
@@ -259,7 +270,10 @@ __device__ inline void build_schedule(const int32_t *__restrict__ ctx_lens, int 
         __syncthreads();
         int64_t off = s_carry;
         for (int w = 0; w < warp; ++w) off += s_wsum[w];
-        if (b < batch) cpre[b + 1] = off + x;
+        if (b < batch) {
+            cpre[b + 1] = off + x;
+            if (b < kSchedCache) s_cpre[b + 1] = off + x;
+        }
         __syncthreads();                        // every thread has read s_carry and s_wsum
         if (threadIdx.x == 127) s_carry = off + x;
         __syncthreads();
@@ -271,7 +285,8 @@ __device__ inline void build_schedule(const int32_t *__restrict__ ctx_lens, int 
         int lo = 0, hi = batch - 1;             // first b with cpre[b+1] > g0
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
-            if (cpre[mid + 1] > g0) hi = mid;
+            const int64_t cm = (mid < kSchedCache) ? s_cpre[mid + 1] : cpre[mid + 1];
+            if (cm > g0) hi = mid;
             else lo = mid + 1;
         }
         cta_b[c] = lo;
@@ -291,7 +306,11 @@ cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, in
                          const int32_t *ctx_lens, int max_ctx, void *ws, cudaStream_t st);
 cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
-                          const int32_t *ctx_lens, int max_ctx, float *out, void *ws, int32_t *status,
+                          const int32_t *ctx_lens, int ctx_add, int max_ctx, float *out, void *ws, int32_t *status,
                           cudaStream_t st);
+cudaError_t launch_step(int d, int dtype, const void *params, const void *k_new, const void *v_new, const void *q,
+                        int batch, int hq, int hkv, const int32_t *block_table, int max_blocks,
+                        const int32_t *pre_lens, int max_ctx, void *k_pool, void *v_pool, int64_t num_blocks,
+                        float *out, void *ws, int32_t *status, cudaStream_t st);
 
 }  // namespace tq

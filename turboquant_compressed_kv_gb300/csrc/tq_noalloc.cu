@@ -76,6 +76,6 @@ extern "C" int tq_decode_attn_noalloc(const void *params, int d, const void *q, 
     e = launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx, ws, st);
     if (e == cudaSuccess)
         e = launch_splitk(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
-                          max_blocks, ctx_lens, max_ctx, out, ws, status, st);
+                          max_blocks, ctx_lens, 0, max_ctx, out, ws, status, st);
     return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

@@ -1,0 +1,354 @@
+// tq_prep.cuh -- the two small kernels that precede the decode pass, as device functions so
+// that they can run in one launch: the paged append's encode (tiles of vectors) and the
+// query prep (rotation, S projection, operand packs, work schedule).
+#pragma once
+
+#include "tq_internal.cuh"
+
+namespace tq {
+
+constexpr int kEncWarps = 4;               // warps per encode CTA
+
+// Where vector v of a launch goes: slot (or -1 to skip) and its input row.
+struct SlotMap {
+    const int64_t *slots;                  // bulk: slots[token]
+    const int32_t *block_table;            // append: slot from the block table and length
+    const int32_t *ctx_lens;
+    int max_blocks;
+    int64_t num_blocks;
+    int n_heads;
+    __device__ int64_t slot(int64_t token, int32_t *status, bool report) const {
+        int64_t s = -1;
+        if (slots) {
+            s = slots[token];
+            if (s < 0) return -1;
+        } else {
+            const int Lb = ctx_lens[token];
+            if (Lb < 0) return -1;
+            const int lb = Lb / kBlock;
+            const int64_t blk = (lb < max_blocks) ? (int64_t)block_table[(size_t)token * max_blocks + lb] : -1;
+            s = (blk >= 0) ? blk * kBlock + (Lb % kBlock) : -2;
+            if (s == -2) {   // no block for this position
+                if (report) flag_status(status, TQ_STATUS_BAD_SLOT);
+                return -1;
+            }
+        }
+        if (s / kBlock >= num_blocks) {
+            if (report) flag_status(status, TQ_STATUS_BAD_SLOT);
+            return -1;
+        }
+        return s;
+    }
+};
+
+// TILE vectors per CTA: 16 for bulk encodes (each S^T read serves 16
+// vectors), 4 for the one-token append (more CTAs, shorter latency chains).
+template <int D, int TILE>
+struct EncSmem {
+    static constexpr bool kResident = (D == 128);
+    static constexpr size_t kST = kResident ? (size_t)D * D * 4 : (size_t)2 * kProjRows * D * 4;
+    static constexpr size_t kRho = (size_t)TILE * D * 4;
+    static constexpr size_t kSgn = (size_t)TILE * D;
+    static constexpr size_t kBytes = kST + kRho + kSgn;
+};
+
+
+// Encode tiles blk, blk + nblk, ... of TILE vectors (K if is_k, else V) with one CTA of
+// 4 warps; `smem` holds EncSmem<D, TILE>::kBytes.  A bad slot is reported by the K tiles
+// (or, without K tiles, by the V tiles) when report_bad is set.
+template <int D, int TILE, typename T>
+__device__ __forceinline__ void encode_tiles(const uint8_t *__restrict__ params, const T *__restrict__ x,
+                                             int64_t n_vec, const SlotMap &map, uint8_t *__restrict__ pool, bool is_k,
+                                             bool report_bad, int blk, int nblk, uint8_t *smem, int32_t *status) {
+    constexpr int R = D / 32;
+    constexpr int kTile = TILE, kPerWarp = TILE / kEncWarps;
+    using SM = EncSmem<D, TILE>;
+    float *sST = reinterpret_cast<float *>(smem);
+    float (*s_rho)[D] = reinterpret_cast<float (*)[D]>(smem + SM::kST);
+    uint8_t (*s_sgn)[D] = reinterpret_cast<uint8_t (*)[D]>(smem + SM::kST + SM::kRho);
+    __shared__ float s_cent[8], s_thr[8];
+    const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
+    if (ph->magic != kParamsMagic || ph->d != D) {
+        if (threadIdx.x == 0 && blk == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
+        return;
+    }
+    const float *gST = reinterpret_cast<const float *>(params + params_off_ST(D));
+    if (is_k && SM::kResident) stage_st_rows<D, kEncWarps * 32>(sST, gST, 0, D);   // waited before first use
+    if (threadIdx.x < 8) {
+        s_cent[threadIdx.x] = ph->centroid[threadIdx.x];
+        s_thr[threadIdx.x] = ph->threshold[threadIdx.x];
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
+    const int64_t ntiles = (n_vec + kTile - 1) / kTile;
+
+#pragma unroll 1
+    for (int64_t tile = blk; tile < ntiles; tile += nblk) {
+        const int64_t v0 = tile * kTile;
+        int code[kPerWarp][R];
+        float nrm[kPerWarp], gam[kPerWarp];
+        int64_t slot[kPerWarp];
+        // ---- 1. norm, rotation, cells, residual
+#pragma unroll
+        for (int j = 0; j < kPerWarp; ++j) {
+            const int tv = warp + kEncWarps * j;              // vector within the tile
+            const int64_t v = v0 + tv;
+            float val[R];
+            int dims[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {   // the input row does not depend on the slot: load it first
+                dims[r] = is_k ? kdim<D>(lane, r) : vdim<D>(lane, r);
+                val[r] = (v < n_vec) ? to_f32<T>(x[v * D + dims[r]]) : 0.f;
+            }
+            slot[j] = -1;
+            if (v < n_vec)   // a bad slot is reported once per token
+                slot[j] = map.slot(v / map.n_heads, status, report_bad && lane == 0 && (v % map.n_heads) == 0);
+            if (slot[j] < 0) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) val[r] = 0.f;
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) ss = fmaf(val[r], val[r], ss);
+            const float n = sqrtf(warp_sum(ss));
+#pragma unroll
+            for (int r = 0; r < R; ++r) val[r] *= __ldg(Dsign + dims[r]);
+            fwht_warp<R>(val, lane);                       // z = H(D x) / n = sqrt(d) Pi (x/n)
+            float g2 = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const float z = (n > 0.f) ? val[r] / n : 0.f;
+                int k = 0;
+#pragma unroll
+                for (int t = 0; t < 7; ++t) k += (z >= s_thr[t]) ? 1 : 0;
+                code[j][r] = k;
+                if (is_k) {
+                    const float rho = z - s_cent[k];     // residual, rotated unit-variance domain
+                    g2 = fmaf(rho, rho, g2);
+                    s_rho[tv][dims[r]] = rho;
+                }
+            }
+            nrm[j] = n;
+            gam[j] = is_k ? sqrtf(warp_sum(g2)) / sqrtf((float)D) : 0.f;   // ||y - c/sqrt d|| = ||rho|| / sqrt d
+        }
+        // ---- 2. QJL projections of the tile (K only): bit k = [(S rho)_k >= 0]
+        if (is_k) {
+            constexpr int KPT = D / (kEncWarps * 32);
+            float acc[KPT][kTile];
+#pragma unroll
+            for (int u = 0; u < KPT; ++u)
+#pragma unroll
+                for (int t = 0; t < kTile; ++t) acc[u][t] = 0.f;
+            if (SM::kResident) {
+                cp_async_wait_all();
+                __syncthreads();
+                project_rows<D, kTile, kEncWarps * 32>(sST, 0, D, s_rho, acc);
+            } else {
+                __syncthreads();
+                project_streamed<D, kTile, kEncWarps * 32>(gST, sST, s_rho, acc);
+            }
+#pragma unroll
+            for (int u = 0; u < KPT; ++u)
+#pragma unroll
+                for (int t = 0; t < kTile; ++t) s_sgn[t][threadIdx.x + 128 * u] = acc[u][t] >= 0.f ? 1 : 0;
+            __syncthreads();
+        }
+        // ---- 3. pack and store
+#pragma unroll
+        for (int j = 0; j < kPerWarp; ++j) {
+            if (slot[j] < 0) continue;                     // warp-uniform
+            const int tv = warp + kEncWarps * j;
+            const int head = (int)((v0 + tv) % map.n_heads);
+            const int64_t blk = slot[j] / kBlock;
+            const int off = (int)(slot[j] % kBlock);
+            if (is_k) {
+                uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * k_record(D);
+                uint32_t *planes = reinterpret_cast<uint32_t *>(rec);
+                constexpr int NW = D / 128;
+                const int gid = off & 7, th = off >> 3;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t w0 = __ballot_sync(0xffffffffu, code[j][r] & 1);
+                    const uint32_t w1 = __ballot_sync(0xffffffffu, (code[j][r] >> 1) & 1);
+                    const uint32_t w2 = __ballot_sync(0xffffffffu, (code[j][r] >> 2) & 1);
+                    const uint32_t ws = __ballot_sync(0xffffffffu, s_sgn[tv][kdim<D>(lane, r)]);
+                    if (lane == r) {
+                        const int L = 4 * gid + (r & 3);
+                        const size_t word = (size_t)(L * 2 + th) * NW + (r >> 2);
+                        constexpr size_t PW = 2 * D / 4;   // words per plane
+                        planes[word] = w0;
+                        planes[PW + word] = w1;
+                        planes[2 * PW + word] = w2;
+                        planes[3 * PW + word] = ws;
+                    }
+                }
+                if (lane == 0)
+                    *reinterpret_cast<__half2 *>(rec + 8 * D + 4 * off) =
+                        __halves2half2(__float2half_rn(nrm[j]), __float2half_rn(gam[j]));
+            } else {
+                uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * v_record(D);
+                constexpr int NWV = D / 64, NM = D / 128;
+                const int tigv = (off & 7) >> 1, jb = (off >> 3) + 2 * (off & 1);   // lane tig, byte in word
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint32_t w0 = __ballot_sync(0xffffffffu, code[j][r] & 1);
+                    const uint32_t w1 = __ballot_sync(0xffffffffu, (code[j][r] >> 1) & 1);
+                    const uint32_t w2 = __ballot_sync(0xffffffffu, (code[j][r] >> 2) & 1);
+                    if ((lane >> 2) == r) {
+                        const int beta = lane & 3, tau = 4 * r + beta;
+                        const int mhi = tau % NM, rh = (tau / NM) & 1, gid = tau / (2 * NM);
+                        const size_t byte = ((size_t)(4 * gid + tigv) * NWV + 2 * mhi + rh) * 4 + jb;
+                        rec[byte] = (uint8_t)(w0 >> (8 * beta));
+                        rec[2 * D + byte] = (uint8_t)(w1 >> (8 * beta));
+                        rec[4 * D + byte] = (uint8_t)(w2 >> (8 * beta));
+                    }
+                }
+                if (lane == 0) *reinterpret_cast<__half *>(rec + 6 * D + 2 * off) = __float2half_rn(nrm[j]);
+            }
+        }
+        __syncthreads();   // s_rho / s_sgn are rewritten by the next tile
+    }
+}
+
+
+// ---------------------------------------------------------------- f16 operand helpers
+
+// Operand bit position q (8..15 within each f16 half): mask, base, and the
+// operand values alpha (bit clear) and alpha + delta (bit set).
+__host__ __device__ constexpr uint32_t op_mask(int q) { return 0x00010001u << q; }
+__host__ __device__ constexpr float op_alpha(int q) { return q == 14 ? 0.f : 1.f; }
+__host__ __device__ constexpr float op_delta(int q) {
+    return q == 8 ? 0.25f : q == 9 ? 0.5f : q == 10 ? -0.5f : q == 11 ? -0.75f
+         : q == 12 ? -0.9375f : q == 13 ? -0.99609375f : q == 14 ? 2.0f : -2.0f;
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// exponent e with x * 2^e in [128, 256) for x > 0
+__device__ __forceinline__ int scale_exp(float x) {
+    int ex;
+    frexpf(x, &ex);
+    return 8 - ex;
+}
+
+
+
+// Per (sequence, kv head) query pack: f16x2 B-operand fragments
+// [2 (qbar, u)][d/16 k-steps][2 n-tiles][32 lanes][2 words], then the offset
+// constants [2][8 heads] as floats.
+__host__ __device__ constexpr size_t kPackBytes(int d) { return 64 * (size_t)d + 256; }
+__host__ __device__ constexpr int kPackFloatOff(int d) { return 16 * d; }   // in floats
+
+// ---------------------------------------------------------------- (1) query prep
+// A CTA handles kQRows (sequence, query head) rows, one per warp: each warp
+// rotates its row (qbar = Pi q), then thread k computes u_k = (S qbar)_k for
+// every row from S^T staged in shared memory (all of it in one copy at d=128,
+// two 64-row chunks in flight at d=256), then each warp writes its row's hi
+// and lo columns (2*hg, 2*hg+1) of the K-side B operand for qbar (qu=0) and
+// u (qu=1) into the pack of the row's (sequence, kv head), and the offset
+// constants.  CTA 0 also lays out the pass's work (build_schedule).
+constexpr int kQRows = 4;
+template <int D> __host__ __device__ constexpr int qprep_st_rows() { return D == 128 ? 128 : 64; }
+template <int D> __host__ __device__ constexpr size_t qprep_smem() {
+    return (size_t)2 * kQRows * D * 4 + (size_t)(D / qprep_st_rows<D>() > 1 ? 2 : 1) * qprep_st_rows<D>() * D * 4;
+}
+
+
+// Rows 4*blk .. 4*blk+3 of the query prep, one CTA of 128 threads; `qsm` holds
+// qprep_smem<D>() bytes.  Block 0 also builds the pass's work schedule; ctx_add is added to
+// every non-negative length (1 when the step appends one token first).
+template <int D, int NTK, typename T>
+__device__ __forceinline__ void qprep_rows(const uint8_t *__restrict__ params, const T *__restrict__ q, int batch,
+                                           int hq, int hkv, const int32_t *__restrict__ ctx_lens, int ctx_add,
+                                           int max_ctx, int chunk, int P, uint8_t *__restrict__ packs,
+                                           unsigned int *__restrict__ counters, int64_t *__restrict__ cpre,
+                                           int32_t *__restrict__ cta_b, int blk, uint8_t *qsm) {
+    constexpr int R = D / 32, NKS = D / 16, KPT = D / 128;
+    float (*qs)[D] = reinterpret_cast<float (*)[D]>(qsm);                       // [kQRows][D] qbar
+    float (*us)[D] = reinterpret_cast<float (*)[D]>(qsm + kQRows * D * 4);      // [kQRows][D] u
+    float *sbuf = reinterpret_cast<float *>(qsm + 2 * kQRows * D * 4);         // S^T rows
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nrows = batch * hq, row0 = blk * kQRows;
+    const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
+    const float *ST = reinterpret_cast<const float *>(params + params_off_ST(D));
+    const float inv_sd = rsqrtf((float)D);
+    {
+        const int row = row0 + warp;
+        float v[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            v[r] = (row < nrows) ? to_f32<T>(q[(size_t)row * D + 32 * r + lane]) * __ldg(Dsign + 32 * r + lane) : 0.f;
+        fwht_warp<R>(v, lane);
+#pragma unroll
+        for (int r = 0; r < R; ++r) qs[warp][32 * r + lane] = v[r] * inv_sd;   // qbar = H D q / sqrt d
+    }
+    {
+        float acc[KPT][kQRows];
+#pragma unroll
+        for (int u = 0; u < KPT; ++u)
+#pragma unroll
+            for (int rr = 0; rr < kQRows; ++rr) acc[u][rr] = 0.f;
+        project_streamed<D, kQRows, 128, qprep_st_rows<D>()>(ST, sbuf, qs, acc);     // u = S qbar
+#pragma unroll
+        for (int u = 0; u < KPT; ++u)
+#pragma unroll
+            for (int rr = 0; rr < kQRows; ++rr) us[rr][threadIdx.x + 128 * u] = acc[u][rr];
+    }
+    __syncthreads();
+    const int row = row0 + warp;
+    if (row < nrows) {
+        const int b = row / hq, h = row % hq, G = hq / hkv, kvh = h / G, hg = h % G;
+        if (hg == 0 && lane == 0) counters[b * hkv + kvh] = 0u;   // completion counter of the pass
+        float v[R], u[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            v[r] = qs[warp][32 * r + lane];
+            u[r] = us[warp][32 * r + lane];
+        }
+        uint8_t *pack = packs + ((size_t)b * hkv + kvh) * kPackBytes(D);
+        uint16_t *ph = reinterpret_cast<uint16_t *>(pack);
+        float *pf = reinterpret_cast<float *>(pack) + kPackFloatOff(D);
+#pragma unroll
+        for (int qu = 0; qu < 2; ++qu) {
+            float cs = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int dim = 32 * r + lane, s = dim >> 4, k = dim & 15, qd = 8 + (s & 7);
+                const float beta = 2.f * (qu == 0 ? v[r] : u[r]) / op_delta(qd);
+                const __half hi = __float2half_rn(beta);
+                const __half lo = __float2half_rn(beta - __half2float(hi));
+                cs = fmaf(__half2float(hi) + __half2float(lo), op_alpha(qd) + 0.5f * op_delta(qd), cs);
+                const int reg = k >> 3, tig = (k & 7) >> 1, e = k & 1;
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const int col = 2 * hg + x, nt = col >> 3, gid = col & 7;
+                    const size_t word = ((size_t)(qu * NKS + s) * NTK + nt) * 64 + (4 * gid + tig) * 2 + reg;
+                    ph[word * 2 + e] = __half_as_ushort(x == 0 ? hi : lo);
+                }
+            }
+            cs = warp_sum(cs);
+            if (lane == 0) pf[qu * 8 + hg] = cs;
+        }
+        // columns beyond the group's 2*G are zero (written by the group's first head)
+        if (hg == 0) {
+            uint32_t *pw = reinterpret_cast<uint32_t *>(pack);
+            for (int col = 2 * G; col < 8 * NTK; ++col) {
+                const int nt = col >> 3, gid = col & 7;
+                for (int i = lane; i < 2 * NKS * 8; i += 32) {
+                    const int qu = i / (NKS * 8), s = (i / 8) % NKS, k = i % 8;
+                    pw[((size_t)(qu * NKS + s) * NTK + nt) * 64 + (4 * gid + (k >> 1)) * 2 + (k & 1)] = 0u;
+                }
+            }
+        }
+    }
+    if (blk == 0) build_schedule(ctx_lens, ctx_add, batch, hkv, max_ctx, chunk, P, cpre, cta_b);
+}
+
+
+}  // namespace tq
