@@ -47,10 +47,16 @@ namespace tq {
 #ifndef TQ_SPLITK_MINBLOCKS
 #define TQ_SPLITK_MINBLOCKS 4    // resident CTAs per SM the register budget is sized for (4-warp CTAs)
 #endif
-constexpr int kCtasPerSm = 4;              // persistent CTAs per SM (at most)
+#ifndef TQ_SPLITK_CTAS_PER_SM
+#define TQ_SPLITK_CTAS_PER_SM 4
+#endif
+constexpr int kCtasPerSm = TQ_SPLITK_CTAS_PER_SM;   // persistent CTAs per SM (at most)
 
 // warps of the pass for a group of G query heads, and tokens per chunk
-__host__ __device__ constexpr int pass_warps(int G) { return G <= 4 ? 4 : 8; }
+#ifndef TQ_SPLITK_WIDE_G
+#define TQ_SPLITK_WIDE_G 8       // groups larger than this use 8-warp CTAs (none: 4-warp CTAs measured faster)
+#endif
+__host__ __device__ constexpr int pass_warps(int G) { return G <= TQ_SPLITK_WIDE_G ? 4 : 8; }
 __host__ __device__ constexpr int pass_chunk(int G) { return kBlock * pass_warps(G) * TQ_SPLITK_BPW; }
 
 __host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -153,8 +159,11 @@ __device__ __forceinline__ void finish_row(float (&v)[D / 32], float l, const ui
     for (int r = 0; r < R; ++r) out_row[32 * r + lane] = v[r] * inv_sd * __ldg(Dsign + 32 * r + lane);
 }
 
+#ifndef TQ_SPLITK_MINBLOCKS_WIDE
+#define TQ_SPLITK_MINBLOCKS_WIDE 3   // resident CTAs for d = 256 or groups of more than 4 heads
+#endif
 template <int D, int G, int NWARP>
-__global__ void __launch_bounds__(NWARP * 32, (NWARP == 4 ? (D == 128 ? TQ_SPLITK_MINBLOCKS : 3) : 1))
+__global__ void __launch_bounds__(NWARP * 32, (NWARP == 4 ? (D == 128 && G <= 4 ? TQ_SPLITK_MINBLOCKS : TQ_SPLITK_MINBLOCKS_WIDE) : 1))
 decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ packs, int batch, int hq, int hkv,
                   const uint8_t *__restrict__ k_pool, const uint8_t *__restrict__ v_pool, int64_t num_blocks,
                   const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_lens,
