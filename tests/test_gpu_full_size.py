@@ -1,0 +1,72 @@
+"""Full-size decode parity on the benchmark-sized workloads, sampled by (sequence, kv head).
+
+The whole batch is prefilled on the device (synth.kv_tokens_device) and decoded in one call, at
+the sizes and launch configuration the benchmark uses.  For a few sampled (sequence, kv head)
+units, the oracle encodes every token of the unit itself (synth.kv_tokens, seeded) into a
+one-unit cache; those records are written over the unit's slots in the device pools, and the
+oracle decodes the unit's query heads.  A unit's attention reads only its own records, so the
+device output of the sampled heads must match the oracle's within the attention tolerance.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import turboquant_compressed_kv_gb300 as tq
+from turboquant_compressed_kv_gb300 import synth
+from turboquant_compressed_kv_gb300.cache import PagedCache, to_device
+from tests import parity
+
+DEV = "cuda"
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_unit(w, cache, b, kvh):
+    """Oracle-written records of unit (b, kvh), as [blocks][1][record] arrays, and the unit's block ids."""
+    d, L = w.head_dim, w.ctx_lens[b]
+    K, V = synth.kv_tokens(w, b, 0, L)
+    nb = (L + 15) // 16
+    kp = np.zeros((nb, 1, oracle.record_bytes(True, d)), np.uint8)
+    vp = np.zeros((nb, 1, oracle.record_bytes(False, d)), np.uint8)
+    slots = np.arange(L, dtype=np.int64)              # identity block table of the one-unit cache
+    oracle.encode(True, cache.D, cache.S, np.ascontiguousarray(K[:, kvh:kvh + 1]), slots, kp)
+    oracle.encode(False, cache.D, cache.S, np.ascontiguousarray(V[:, kvh:kvh + 1]), slots, vp)
+    return kp, vp, cache.block_table_np[b, :nb]
+
+
+@pytest.mark.parametrize("name,units", [
+    ("llama8b_decode", [(0, 0), (9, 5), (15, 7)]),     # 16 x 32/8 heads, d=128, 4096 tokens
+    ("ragged", [(3, 1), (41, 3)]),                      # 64 x 32/4 heads, d=128, 512..32768 tokens
+    ("long256", [(2, 6)]),                              # 4 x 16/8 heads, d=256, 131072 tokens
+])
+def test_full_size_sampled_parity(name, units):
+    w = synth.workload(name)
+    w = dataclasses.replace(w, prefill_lens=list(w.ctx_lens), append=False)
+    d, B, Hq, Hkv, G = w.head_dim, w.batch, w.n_q_heads, w.n_kv_heads, w.group
+    tq.load_library()
+    cache = PagedCache.create(w, DEV)
+    cache.prefill_device()
+    refs = {}
+    for b, kvh in units:
+        kp, vp, blocks = _oracle_unit(w, cache, b, kvh)
+        idx = torch.from_numpy(blocks.astype(np.int64)).to(DEV)
+        cache.k_pool[idx, kvh] = torch.from_numpy(kp[:, 0]).to(DEV)
+        cache.v_pool[idx, kvh] = torch.from_numpy(vp[:, 0]).to(DEV)
+        refs[(b, kvh)] = (kp, vp)
+    q = synth.queries(w)
+    ctx = torch.tensor(w.ctx_lens, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = tq.decode_attn(cache.params, d, to_device(q, w.dtype, DEV), Hkv, cache.k_pool, cache.v_pool,
+                         cache.block_table, ctx, max(w.ctx_lens), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o = out.cpu().numpy()
+    for (b, kvh), (kp, vp) in refs.items():
+        L = w.ctx_lens[b]
+        nb = kp.shape[0]
+        qu = np.ascontiguousarray(q[b:b + 1, kvh * G:(kvh + 1) * G])
+        ref = oracle.decode(cache.D, cache.S, qu, 1, kp, vp, np.arange(nb, dtype=np.int32)[None],
+                            np.array([L], np.int32))
+        parity.check_attention(o[b:b + 1, kvh * G:(kvh + 1) * G], ref)

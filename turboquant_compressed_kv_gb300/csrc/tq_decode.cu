@@ -127,6 +127,19 @@ __device__ __forceinline__ int64_t block_of(const int32_t *__restrict__ bt, int 
     return (p >= 0 && p < num_blocks) ? p : -1;
 }
 
+// V-side operand encoding.  The value sums run over whole contexts (up to 10^5 tokens), so
+// the operands carry no offset: with base 0 the f16 with only bit q set is 0 or delta_q
+// (2^-16 .. 2 for q = 8..14, the first two subnormal); bit 15 toggles the sign of 2^-14, so
+// the operand is +-2^-14 and the sum is the +-1 sum itself.  (An offset alpha would leave
+// alpha * sum(P) in the fp32 accumulator and cost (2 alpha / delta)-fold of its rounding.)
+__host__ __device__ constexpr uint32_t vop_base(int q) { return q == 15 ? 0x04000400u : 0u; }
+__host__ __device__ constexpr float vop_alpha(int q) { return q == 15 ? 0.00006103515625f : 0.f; }   // 2^-14
+__host__ __device__ constexpr float vop_delta(int q) {
+    return q == 8 ? 1.52587890625e-05f : q == 9 ? 3.0517578125e-05f : q == 10 ? 6.103515625e-05f
+         : q == 11 ? 0.0001220703125f : q == 12 ? 0.00048828125f : q == 13 ? 0.0078125f : q == 14 ? 2.f
+         : -0.0001220703125f;
+}
+
 template <int D, int NWARP>
 struct SplitCfg {
     static constexpr int NT = NWARP * 32;
@@ -219,13 +232,13 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
 
     // weight rows of heads >= G stay zero
     for (int i = tid; i < (8 - G) * PROW; i += NT_) sP[G * PROW + i] = __float2half(0.f);
-    // V side: operand mask/base of this warp's m-tiles
+    // V side: operand mask/base of this warp's m-tiles (v_base: no offset, see vop_alpha)
     uint32_t vmask[MTW], vbase[MTW];
 #pragma unroll
     for (int i = 0; i < MTW; ++i) {
         const int q = 8 + ((warp * MTW + i) & 7);
         vmask[i] = 0x00010001u << q;
-        vbase[i] = (q == 14) ? 0u : one16x2;
+        vbase[i] = vop_base(q);
     }
     const int mhi = (warp * MTW) >> 3;
 
@@ -499,7 +512,7 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
 #pragma unroll
         for (int i = 0; i < MTW; ++i) {
             const int mt = warp * MTW + i, q = 8 + (mt & 7);
-            const float al = op_alpha(q), inv_de = 2.f / op_delta(q);
+            const float al = vop_alpha(q), inv_de = 2.f / vop_delta(q);
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int h = 2 * tig + e;
