@@ -69,4 +69,5 @@ def test_full_size_sampled_parity(name, units):
         qu = np.ascontiguousarray(q[b:b + 1, kvh * G:(kvh + 1) * G])
         ref = oracle.decode(cache.D, cache.S, qu, 1, kp, vp, np.arange(nb, dtype=np.int32)[None],
                             np.array([L], np.int32))
-        parity.check_attention(o[b:b + 1, kvh * G:(kvh + 1) * G], ref)
+        worst = parity.check_attention(o[b:b + 1, kvh * G:(kvh + 1) * G], ref)
+        print(f"{name} unit ({b}, {kvh}): worst max-abs {worst[0]:.3e}, worst relative {worst[1]:.3e}")

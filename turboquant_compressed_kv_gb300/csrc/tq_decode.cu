@@ -36,66 +36,15 @@
 // (sequence, query head) is applied at the end.
 #include <atomic>
 
-#include "tq_internal.cuh"
-#include "tq_prep.cuh"
+#include "tq_split.cuh"
 
 namespace tq {
 
-#ifndef TQ_SPLITK_BPW
-#define TQ_SPLITK_BPW 2          // blocks scored per warp per chunk
-#endif
-#ifndef TQ_SPLITK_MINBLOCKS
-#define TQ_SPLITK_MINBLOCKS 4    // resident CTAs per SM the register budget is sized for (4-warp CTAs)
-#endif
-#ifndef TQ_SPLITK_CTAS_PER_SM
-#define TQ_SPLITK_CTAS_PER_SM 4
-#endif
-constexpr int kCtasPerSm = TQ_SPLITK_CTAS_PER_SM;   // persistent CTAs per SM (at most)
-
-// warps of the pass for a group of G query heads, and tokens per chunk
-#ifndef TQ_SPLITK_WIDE_G
-#define TQ_SPLITK_WIDE_G 8       // groups larger than this use 8-warp CTAs (none: 4-warp CTAs measured faster)
-#endif
-__host__ __device__ constexpr int pass_warps(int G) { return G <= TQ_SPLITK_WIDE_G ? 4 : 8; }
-__host__ __device__ constexpr int pass_chunk(int G) { return kBlock * pass_warps(G) * TQ_SPLITK_BPW; }
-
-__host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
-
-// Workspace: query packs [B*Hkv] | completion counters [B*Hkv] | chunk prefix
-// int64[B+1] | first sequence of each CTA int32[P] | partials [P][2][G][d+4].
-// Sized with Hq >= Hkv, G <= min(8, Hq) and P <= kCtasPerSm * kMaxSms.
-struct WsLayout {
-    uint8_t *packs;
-    unsigned int *counters;
-    int64_t *cpre;
-    int32_t *cta_b;
-    float *part;
-};
-inline size_t ws_sizes(int d, int batch, int hq, size_t *off) {
-    const int gmax = hq < 8 ? hq : 8;
-    const size_t pmax = (size_t)kCtasPerSm * kMaxSms;
-    const size_t per_head = kPackBytes(d);
-    off[0] = 0;
-    off[1] = off[0] + align256((size_t)batch * hq * per_head);
-    off[2] = off[1] + align256((size_t)batch * hq * 4);
-    off[3] = off[2] + align256(((size_t)batch + 1) * 8);
-    off[4] = off[3] + align256(pmax * 4);
-    return off[4] + pmax * 2 * gmax * kPartStride(d) * sizeof(float);
-}
 size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx) {
     if (!valid_d(d) || batch <= 0 || hq <= 0 || max_ctx < 0) return 0;
     size_t off[5];
     return ws_sizes(d, batch, hq, off);
 }
-WsLayout ws_layout(void *ws, int d, int batch, int hq) {
-    size_t off[5];
-    ws_sizes(d, batch, hq, off);
-    uint8_t *base = reinterpret_cast<uint8_t *>(ws);
-    return WsLayout{base + off[0], reinterpret_cast<unsigned int *>(base + off[1]),
-                    reinterpret_cast<int64_t *>(base + off[2]), reinterpret_cast<int32_t *>(base + off[3]),
-                    reinterpret_cast<float *>(base + off[4])};
-}
-
 
 namespace {
 
@@ -119,27 +68,6 @@ qprep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ q, int ba
 // w, w+NWARP); warp w accumulates values for its D/NWARP coordinates over the
 // whole chunk (V side).
 
-// physical block of logical block lb, or -1 (past the table or outside the pool)
-__device__ __forceinline__ int64_t block_of(const int32_t *__restrict__ bt, int b, int max_blocks, int lb,
-                                            int64_t num_blocks) {
-    if (lb >= max_blocks) return -1;
-    const int64_t p = bt[(size_t)b * max_blocks + lb];
-    return (p >= 0 && p < num_blocks) ? p : -1;
-}
-
-// V-side operand encoding.  The value sums run over whole contexts (up to 10^5 tokens), so
-// the operands carry no offset: with base 0 the f16 with only bit q set is 0 or delta_q
-// (2^-16 .. 2 for q = 8..14, the first two subnormal); bit 15 toggles the sign of 2^-14, so
-// the operand is +-2^-14 and the sum is the +-1 sum itself.  (An offset alpha would leave
-// alpha * sum(P) in the fp32 accumulator and cost (2 alpha / delta)-fold of its rounding.)
-__host__ __device__ constexpr uint32_t vop_base(int q) { return q == 15 ? 0x04000400u : 0u; }
-__host__ __device__ constexpr float vop_alpha(int q) { return q == 15 ? 0.00006103515625f : 0.f; }   // 2^-14
-__host__ __device__ constexpr float vop_delta(int q) {
-    return q == 8 ? 1.52587890625e-05f : q == 9 ? 3.0517578125e-05f : q == 10 ? 6.103515625e-05f
-         : q == 11 ? 0.0001220703125f : q == 12 ? 0.00048828125f : q == 13 ? 0.0078125f : q == 14 ? 2.f
-         : -0.0001220703125f;
-}
-
 template <int D, int NWARP>
 struct SplitCfg {
     static constexpr int NT = NWARP * 32;
@@ -155,21 +83,6 @@ template <int D, int G, int NWARP>
 constexpr size_t split_smem_bytes() {
     using C = SplitCfg<D, NWARP>;
     return C::kBytes + C::vBytes + (size_t)8 * (C::CH + 8) * 2 + (size_t)C::CH * G * 4;
-}
-
-// out[row] = Pi^T (v / l): D (H v) / (l sqrt d), v spread over the warp as v[r] at lane
-template <int D>
-__device__ __forceinline__ void finish_row(float (&v)[D / 32], float l, const uint8_t *params, float *out_row,
-                                           int lane) {
-    constexpr int R = D / 32;
-    const float inv = (l > 0.f) ? 1.f / l : 0.f;
-#pragma unroll
-    for (int r = 0; r < R; ++r) v[r] *= inv;
-    fwht_warp<R>(v, lane);
-    const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
-    const float inv_sd = rsqrtf((float)D);
-#pragma unroll
-    for (int r = 0; r < R; ++r) out_row[32 * r + lane] = v[r] * inv_sd * __ldg(Dsign + 32 * r + lane);
 }
 
 #ifndef TQ_SPLITK_MINBLOCKS_WIDE
@@ -203,7 +116,7 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
     float *sAcc = reinterpret_cast<float *>(sK);               // [G][D], between segments
     __shared__ int sOk[2][BPC];
     __shared__ float sF[8];
-    __shared__ float sM[8], sL[8], sT[8];
+    __shared__ float sM[8], sL[8], sTc[8];
     __shared__ int sE[8];
     __shared__ bool s_last;
 
@@ -302,14 +215,13 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
             cu[nt] = hg < G ? pf[8 + hg] : 0.f;
         }
 
-        float O[4][MTW][4];
+        // value sums of this warp's coordinates, planes combined, in the running weight scale
+        float arun[MTW][4];
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+        for (int i = 0; i < MTW; ++i)
 #pragma unroll
-            for (int i = 0; i < MTW; ++i)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) O[m][i][k] = 0.f;
-        float m_run[HPW], l_run[HPW], w_ref[HPW], T_run[HPW];
+            for (int k = 0; k < 4; ++k) arun[i][k] = 0.f;
+        float m_run[HPW], l_run[HPW], w_ref[HPW];
         int e_run[HPW];
 #pragma unroll
         for (int k = 0; k < HPW; ++k) {
@@ -317,7 +229,6 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
             l_run[k] = 0.f;
             w_ref[k] = 0.f;
             e_run[k] = 0;
-            T_run[k] = 0.f;
         }
 
         int buf = 0;
@@ -446,29 +357,39 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
                         sP[h * PROW + lane + 32 * i] = hv;
                         tsum += __half2float(hv);
                     }
-                    T_run[hk] = T_run[hk] * f + warp_sum(tsum);
+                    tsum = warp_sum(tsum);
                     l_run[hk] = l_run[hk] * alpha + psum;
                     m_run[hk] = m_new;
                     w_ref[hk] = wr;
                     e_run[hk] = e_new;
-                    if (lane == 0) sF[h] = f;
+                    if (lane == 0) {
+                        sF[h] = f;
+                        sTc[h] = tsum;
+                    }
                 }
             }
-            __syncthreads();   // weights of the chunk are in sP, factors in sF
+            __syncthreads();   // weights of the chunk are in sP, factors in sF, weight sums in sTc
             // ---- V side: coordinates of m-tiles warp*MTW .. warp*MTW+MTW-1 (columns = heads)
             {
                 const float f0 = (2 * tig < G) ? sF[2 * tig] : 0.f;
                 const float f1 = (2 * tig + 1 < G) ? sF[2 * tig + 1] : 0.f;
 #pragma unroll
-                for (int m = 0; m < 4; ++m)
-#pragma unroll
-                    for (int i = 0; i < MTW; ++i) {
-                        O[m][i][0] *= f0;
-                        O[m][i][1] *= f1;
-                        O[m][i][2] *= f0;
-                        O[m][i][3] *= f1;
-                    }
+                for (int i = 0; i < MTW; ++i) {
+                    arun[i][0] *= f0;
+                    arun[i][1] *= f1;
+                    arun[i][2] *= f0;
+                    arun[i][3] *= f1;
+                }
             }
+            // the chunk's plane sums start from zero: chained tensor-core accumulation over a
+            // whole context is not accurate enough for the 2 sum(w b) - sum(w) cancellation
+            float O[4][MTW][4];
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+#pragma unroll
+                for (int i = 0; i < MTW; ++i)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) O[m][i][k] = 0.f;
 #pragma unroll 2
             for (int kb = 0; kb < BPC; ++kb) {
                 const uint8_t *rec = vb_base + (size_t)kb * VREC;
@@ -495,9 +416,24 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
                     }
                 }
             }
+            // combine the planes, undo the operand offsets: sum_m A_m ((O_m - al T) 2/delta - T)
+            {
+                const float t0 = (2 * tig < G) ? sTc[2 * tig] : 0.f;
+                const float t1c = (2 * tig + 1 < G) ? sTc[2 * tig + 1] : 0.f;
+#pragma unroll
+                for (int i = 0; i < MTW; ++i) {
+                    const int q = 8 + ((warp * MTW + i) & 7);
+                    const float inv_de = 2.f / vop_delta(q), off = (vop_alpha(q) * inv_de + 1.f) * Asum;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float s4 = fmaf(A[0], O[0][i][k], fmaf(A[1], O[1][i][k], fmaf(A[2], O[2][i][k], A[3] * O[3][i][k])));
+                        arun[i][k] += fmaf(s4, inv_de, -off * ((k & 1) ? t1c : t0));
+                    }
+                }
+            }
         }
 
-        // ---- segment epilogue: combine the masks, undo the operand offsets and the weight scale
+        // ---- segment epilogue: undo the weight scale
 #pragma unroll
         for (int hk = 0; hk < HPW; ++hk) {
             const int h = warp + NWARP * hk;
@@ -505,26 +441,18 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
                 sM[h] = m_run[hk];
                 sL[h] = l_run[hk];
                 sE[h] = e_run[hk];
-                sT[h] = T_run[hk];
             }
         }
         __syncthreads();   // the staging buffers are no longer read; sAcc reuses them
 #pragma unroll
         for (int i = 0; i < MTW; ++i) {
-            const int mt = warp * MTW + i, q = 8 + (mt & 7);
-            const float al = vop_alpha(q), inv_de = 2.f / vop_delta(q);
+            const int mt = warp * MTW + i;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int h = 2 * tig + e;
                 if (h < G) {
-                    const float T = sT[h];
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        float v = 0.f;
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) v += A[m] * ((O[m][i][2 * r + e] - al * T) * inv_de - T);
-                        sAcc[h * D + 16 * mt + gid + 8 * r] = ldexpf(v, -sE[h]);
-                    }
+                    for (int r = 0; r < 2; ++r) sAcc[h * D + 16 * mt + gid + 8 * r] = ldexpf(arun[i][2 * r + e], -sE[h]);
                 }
             }
         }
@@ -642,11 +570,11 @@ int pass_ctas_any(int d, int G) {
     static std::atomic<int> cache[kDevs][2][9];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || G < 1 || G > 8) return 0;
-    if (dev >= kDevs) return d == 128 ? pass_ctas_g<128>(G) : pass_ctas_g<256>(G);
+    if (dev >= kDevs) return d == 128 ? (TQ_DECODE_WARP ? warp_pass_ctas(G) : pass_ctas_g<128>(G)) : pass_ctas_g<256>(G);
     std::atomic<int> &slot = cache[dev][d == 128 ? 0 : 1][G];
     int n = slot.load(std::memory_order_relaxed);
     if (n == 0) {
-        n = d == 128 ? pass_ctas_g<128>(G) : pass_ctas_g<256>(G);
+        n = d == 128 ? (TQ_DECODE_WARP ? warp_pass_ctas(G) : pass_ctas_g<128>(G)) : pass_ctas_g<256>(G);
         slot.store(n, std::memory_order_relaxed);
     }
     return n;
@@ -733,6 +661,9 @@ cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv,
     const int nctas = pass_ctas_any(d, G);
     if (nctas <= 0) return cudaErrorInvalidConfiguration;
     const uint8_t *P = (const uint8_t *)params;
+    if (d == 128 && TQ_DECODE_WARP)
+        return warp_pass_launch(G, nctas, st, P, batch, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
+                                num_blocks, block_table, max_blocks, ctx_lens, ctx_add, max_ctx, w, out, status);
     if (d == 128)
         return pass_launch<128>(G, nctas, st, P, batch, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
                                 num_blocks, block_table, max_blocks, ctx_lens, ctx_add, max_ctx, w, out, status);

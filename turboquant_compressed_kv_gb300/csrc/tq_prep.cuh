@@ -230,6 +230,17 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// d = a b with a zero accumulator.  Long chains of mma.sync accumulation lose precision (the
+// tensor core's fp32 accumulation is not rounded to nearest: measured on GB300, 235 ulp of the
+// sum after 1024 chained m16n8k16 and 1439 after 4096), so sums over many tokens start each
+// block from zero and are added up with FADD.
+__device__ __forceinline__ void mma_f16_z(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 // exponent e with x * 2^e in [128, 256) for x > 0
 __device__ __forceinline__ int scale_exp(float x) {
     int ex;

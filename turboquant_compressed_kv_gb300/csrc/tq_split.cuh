@@ -1,0 +1,112 @@
+// tq_split.cuh -- pieces shared by the two decode passes (tq_decode.cu: the
+// coordinate-split pass used at d = 256; tq_decode_warp.cu: the warp-local pass used at
+// d = 128): tuning switches, the workspace layout, block-table lookup, the V-side
+// operand encoding and the final inverse rotation.
+#pragma once
+
+#include "tq_internal.cuh"
+#include "tq_prep.cuh"
+
+namespace tq {
+
+#ifndef TQ_SPLITK_BPW
+#define TQ_SPLITK_BPW 2          // blocks scored per warp per chunk
+#endif
+#ifndef TQ_SPLITK_MINBLOCKS
+#define TQ_SPLITK_MINBLOCKS 4    // resident CTAs per SM the register budget is sized for (4-warp CTAs)
+#endif
+#ifndef TQ_SPLITK_CTAS_PER_SM
+#define TQ_SPLITK_CTAS_PER_SM 3
+#endif
+constexpr int kCtasPerSm = TQ_SPLITK_CTAS_PER_SM;
+
+#ifndef TQ_DECODE_WARP
+#define TQ_DECODE_WARP 1         // d = 128 runs the warp-local pass (tq_decode_warp.cu)
+#endif   // persistent CTAs per SM (at most)
+
+// warps of the pass for a group of G query heads, and tokens per chunk
+#ifndef TQ_SPLITK_WIDE_G
+#define TQ_SPLITK_WIDE_G 8       // groups larger than this use 8-warp CTAs (none: 4-warp CTAs measured faster)
+#endif
+__host__ __device__ constexpr int pass_warps(int G) { return G <= TQ_SPLITK_WIDE_G ? 4 : 8; }
+__host__ __device__ constexpr int pass_chunk(int G) { return kBlock * pass_warps(G) * TQ_SPLITK_BPW; }
+
+__host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace: query packs [B*Hkv] | completion counters [B*Hkv] | chunk prefix
+// int64[B+1] | first sequence of each CTA int32[P] | partials [P][2][G][d+4].
+// Sized with Hq >= Hkv, G <= min(8, Hq) and P <= kCtasPerSm * kMaxSms.
+struct WsLayout {
+    uint8_t *packs;
+    unsigned int *counters;
+    int64_t *cpre;
+    int32_t *cta_b;
+    float *part;
+};
+inline size_t ws_sizes(int d, int batch, int hq, size_t *off) {
+    const int gmax = hq < 8 ? hq : 8;
+    const size_t pmax = (size_t)kCtasPerSm * kMaxSms;
+    const size_t per_head = kPackBytes(d);
+    off[0] = 0;
+    off[1] = off[0] + align256((size_t)batch * hq * per_head);
+    off[2] = off[1] + align256((size_t)batch * hq * 4);
+    off[3] = off[2] + align256(((size_t)batch + 1) * 8);
+    off[4] = off[3] + align256(pmax * 4);
+    return off[4] + pmax * 2 * gmax * kPartStride(d) * sizeof(float);
+}
+inline WsLayout ws_layout(void *ws, int d, int batch, int hq) {
+    size_t off[5];
+    ws_sizes(d, batch, hq, off);
+    uint8_t *base = reinterpret_cast<uint8_t *>(ws);
+    return WsLayout{base + off[0], reinterpret_cast<unsigned int *>(base + off[1]),
+                    reinterpret_cast<int64_t *>(base + off[2]), reinterpret_cast<int32_t *>(base + off[3]),
+                    reinterpret_cast<float *>(base + off[4])};
+}
+
+// physical block of logical block lb, or -1 (past the table or outside the pool)
+__device__ __forceinline__ int64_t block_of(const int32_t *__restrict__ bt, int b, int max_blocks, int lb,
+                                            int64_t num_blocks) {
+    if (lb >= max_blocks) return -1;
+    const int64_t p = bt[(size_t)b * max_blocks + lb];
+    return (p >= 0 && p < num_blocks) ? p : -1;
+}
+
+// V-side operand encoding.  The value sums run over whole contexts (up to 10^5 tokens), so
+// the operands carry no offset: with base 0 the f16 with only bit q set is 0 or delta_q
+// (2^-16 .. 2 for q = 8..14, the first two subnormal); bit 15 toggles the sign of 2^-14, so
+// the operand is +-2^-14 and the sum is the +-1 sum itself.  (An offset alpha would leave
+// alpha * sum(P) in the fp32 accumulator and cost (2 alpha / delta)-fold of its rounding.)
+__host__ __device__ constexpr uint32_t vop_base(int q) { return q == 15 ? 0x04000400u : 0u; }
+__host__ __device__ constexpr float vop_alpha(int q) { return q == 15 ? 0.00006103515625f : 0.f; }   // 2^-14
+__host__ __device__ constexpr float vop_delta(int q) {
+    return q == 8 ? 1.52587890625e-05f : q == 9 ? 3.0517578125e-05f : q == 10 ? 6.103515625e-05f
+         : q == 11 ? 0.0001220703125f : q == 12 ? 0.00048828125f : q == 13 ? 0.0078125f : q == 14 ? 2.f
+         : -0.0001220703125f;
+}
+
+// out[row] = Pi^T (v / l): D (H v) / (l sqrt d), v spread over the warp as v[r] at lane
+template <int D>
+__device__ __forceinline__ void finish_row(float (&v)[D / 32], float l, const uint8_t *params, float *out_row,
+                                           int lane) {
+    constexpr int R = D / 32;
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) v[r] *= inv;
+    fwht_warp<R>(v, lane);
+    const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
+    const float inv_sd = rsqrtf((float)D);
+#pragma unroll
+    for (int r = 0; r < R; ++r) out_row[32 * r + lane] = v[r] * inv_sd * __ldg(Dsign + 32 * r + lane);
+}
+
+
+// The warp-local pass at d = 128 (tq_decode_warp.cu): persistent CTAs it runs with on the
+// current device, and its launch.  Same schedule, workspace and partial format as the
+// coordinate-split pass.
+int warp_pass_ctas(int G);
+cudaError_t warp_pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int hq, int hkv,
+                             const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
+                             const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
+                             int32_t *status);
+
+}  // namespace tq
