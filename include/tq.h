@@ -168,8 +168,7 @@ int tq_decode_attn(const void *params, int d, const void *q, int dtype, int batc
  *                     written to the workspace as tensor-core operands, and the
  *                     work schedule of the pass (read from ctx_lens).
  *   tq_decode_splitk  the pass over the cache.  The context of each (sequence,
- *                     kv head) is cut into chunks of 128 tokens (256 when
- *                     n_q_heads/n_kv_heads > 4); the chunks of all (sequence,
+ *                     kv head) is cut into chunks of 128 tokens; the chunks of all (sequence,
  *                     kv head) pairs, in that order, are shared out in equal
  *                     contiguous ranges among a fixed set of resident CTAs.  A
  *                     pair whose chunks span several CTAs is combined by the
@@ -204,6 +203,39 @@ int tq_decode_step(const void *params, int d, const void *k_new, const void *v_n
                    float *out, void *workspace, size_t workspace_bytes, int32_t *status,
                    tq_stream_t stream);
 
+/* Multi-query decode: q_len new tokens per sequence are verified in one pass over the
+ * cache (speculative or multi-token-prediction decoding), so the compressed records are
+ * read once for all of them.  [README "Performance: MTP Speculative Decoding", key
+ * takeaways: a verification batch of several draft tokens shares one read of the KV
+ * cache; the attention of each query is that of tq_decode_attn]
+ * The q_len tokens are the last q_len of the ctx_lens[b] cached tokens, and query i
+ * (0-based) sees the tokens up to itself (causal): it attends the first
+ * ctx_lens[b] - (q_len - 1 - i) tokens (none if that is <= 0; ctx_lens[b] is clamped to
+ * max_ctx first).  Otherwise each query is exactly tq_decode_attn's.
+ *   q, out     device [batch][q_len][n_q_heads][d] (q in dtype, out fp32).
+ *   workspace  >= tq_decode_workspace_bytes_mq(d, batch, q_len, n_q_heads, max_ctx) bytes.
+ * q_len * n_q_heads / n_kv_heads must be <= 8 (TQ_ERR_GQA otherwise); q_len = 1 is
+ * tq_decode_attn.  Other arguments and errors as tq_decode_attn. */
+size_t tq_decode_workspace_bytes_mq(int d, int batch, int q_len, int n_q_heads, int max_ctx);
+int tq_decode_attn_mq(const void *params, int d, const void *q, int dtype, int batch, int q_len,
+                      int n_q_heads, int n_kv_heads, const void *k_pool, const void *v_pool,
+                      int64_t num_blocks, const int32_t *block_table, int max_blocks,
+                      const int32_t *ctx_lens, int max_ctx, float *out, void *workspace,
+                      size_t workspace_bytes, int32_t *status, tq_stream_t stream);
+
+/* tq_decode_step_mq -- tq_decode_step for q_len tokens per sequence: K and V of token i
+ * (k_new[b][i], v_new[b][i], device [batch][q_len][n_kv_heads][d]) are encoded into the slot
+ * of position pre_lens[b] + i, then the q_len queries attend as in tq_decode_attn_mq with
+ * ctx_lens = pre_lens + q_len (query i sees pre_lens[b] + 1 + i tokens).  A sequence with
+ * pre_lens[b] < 0 appends nothing and gets out = 0.  One launch for the append and the query
+ * preparation, one for the pass; the result equals tq_paged_append of each token followed
+ * by tq_decode_attn_mq.  Errors as tq_decode_step and tq_decode_attn_mq. */
+int tq_decode_step_mq(const void *params, int d, const void *k_new, const void *v_new, const void *q,
+                      int dtype, int batch, int q_len, int n_q_heads, int n_kv_heads,
+                      const int32_t *block_table, int max_blocks, const int32_t *pre_lens, int max_ctx,
+                      void *k_pool, void *v_pool, int64_t num_blocks, float *out, void *workspace,
+                      size_t workspace_bytes, int32_t *status, tq_stream_t stream);
+
 /* tq_decode_attn_noalloc -- tq_decode_attn without a caller workspace.
  * The pages have no counterpart to this call; it exists for callers that
  * cannot allocate device memory when they decode: a serving runtime that
@@ -215,7 +247,7 @@ int tq_decode_step(const void *params, int d, const void *k_new, const void *v_n
  * (16 MiB) compiled into the library; every GPU that loads the library keeps
  * it until the process exits.  A shape whose tq_decode_workspace_bytes()
  * exceeds it is rejected with TQ_ERR_WORKSPACE (16 x 32 query heads at
- * d = 128 need about 9.3 MiB; 64 x 32 need 21.7 MiB).  Nothing is allocated: no
+ * d = 128 need about 8.0 MiB; 64 x 32 need 20.4 MiB).  Nothing is allocated: no
  * cudaMalloc, cudaFree or allocating library call.
  * The scratch used is that of the device current at the call; the stream must
  * belong to it.  The first call made with a device current looks up the

@@ -277,3 +277,19 @@ def decode(D, S, q: np.ndarray, Hkv: int, kpool, vpool, block_table, ctx_lens,
     if rc != 0:
         raise ValueError("oracle decode: Hq must be a multiple of Hkv")
     return out
+
+
+def decode_mq(D, S, q: np.ndarray, Hkv: int, kpool, vpool, block_table, ctx_lens, explicit=False,
+              centroids=None):
+    """Multi-query decode: q[B][Q][Hq][d] -> out[B][Q][Hq][d] fp64.  The Q queries verify the
+    last Q of the ctx_lens[b] cached tokens (speculative / multi-token-prediction decoding,
+    SwiftLM README "Performance: MTP Speculative Decoding"), so query i sees the tokens up to
+    itself: it is the single-query decode of the first ctx_lens[b] - (Q - 1 - i) tokens."""
+    B, Q, Hq, d = q.shape
+    out = np.zeros((B, Q, Hq, d), np.float64)
+    lens = np.asarray(ctx_lens, np.int64)
+    for i in range(Q):
+        li = np.maximum(lens - (Q - 1 - i), 0).astype(np.int32)
+        out[:, i] = decode(D, S, np.ascontiguousarray(q[:, i]), Hkv, kpool, vpool, block_table, li,
+                           explicit=explicit, centroids=centroids)
+    return out

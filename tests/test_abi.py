@@ -39,6 +39,9 @@ def test_sizes(lib):
     assert tq.params_bytes(128) >= 128 * 128 * 4
     assert tq.decode_workspace_bytes(128, 16, 32, 4096) > 0
     assert tq.decode_workspace_bytes(100, 16, 32, 4096) == 0
+    assert tq.decode_workspace_bytes_mq(128, 16, 1, 32, 4096) == tq.decode_workspace_bytes(128, 16, 32, 4096)
+    assert tq.decode_workspace_bytes_mq(128, 16, 2, 32, 4096) == tq.decode_workspace_bytes(128, 16, 64, 4096)
+    assert tq.decode_workspace_bytes_mq(128, 16, 0, 32, 4096) == 0
 
 
 def test_host_side_argument_errors(lib):
@@ -57,6 +60,12 @@ def test_host_side_argument_errors(lib):
     args[5], args[6] = 32, 8
     args[16] = 10
     assert lib.tq_decode_attn(*args) == -4                      # workspace too small
+    mq = [fake, 128, fake, 0, 2, 3, 32, 8, fake, fake, 4, fake, 1, fake, 16, fake, fake, 1 << 30, None, None]
+    assert lib.tq_decode_attn_mq(*mq) == -3                     # 3 queries x group 4 > 8
+    mq[5] = 0
+    assert lib.tq_decode_attn_mq(*mq) == -1                     # q_len 0
+    mq[5], mq[17] = 2, 10
+    assert lib.tq_decode_attn_mq(*mq) == -4                     # workspace too small
     assert lib.tq_paged_append(fake, 128, fake, fake, 0, 0, 8, fake, 4, fake, fake, fake, 4, None, None) == 0
     D = (ctypes.c_int8 * 128)(*([1] * 127 + [3]))
     S = (ctypes.c_float * (128 * 128))()

@@ -295,6 +295,105 @@ def test_decode_step_appends_then_attends(d, Hq, Hkv, dtype):
     parity.check_attention(o, ref)
 
 
+@pytest.mark.parametrize("d,Hq,Hkv,Q", [(128, 8, 2, 2), (128, 4, 2, 4), (128, 3, 3, 3), (128, 2, 2, 8),
+                                         (256, 4, 2, 2), (256, 1, 1, 5)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_mq_parity(d, Hq, Hkv, Q, dtype):
+    """Multi-query decode: query i of Q attends the first ctx - (Q - 1 - i) tokens.  Lengths below Q
+    leave the first queries with nothing to attend (out = 0)."""
+    lens = [1, 17, 512, 513, 1100, 0, 16, 700, 2, 3]
+    D, S, params, bt, kp, vp = _build_cache(d, Hkv, lens, dtype, seed=Hq + d + Q)
+    B = len(lens)
+    q = synth.round_dtype(np.random.default_rng(12).standard_normal((B, Q, Hq, d)).astype(np.float32), dtype)
+    ctx = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = tq.decode_attn_mq(params, d, _upload(q, dtype), Hkv, torch.from_numpy(kp).to(DEV),
+                            torch.from_numpy(vp).to(DEV), torch.from_numpy(bt).to(DEV), ctx, max(lens), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o = out.cpu().numpy()
+    ref = oracle.decode_mq(D, S, q, Hkv, kp, vp, bt, np.array(lens, np.int32))
+    for b, L in enumerate(lens):
+        for i in range(Q):
+            if L - (Q - 1 - i) <= 0:
+                assert np.all(o[b, i] == 0)
+    parity.check_attention(o.reshape(B * Q, Hq, d), ref.reshape(B * Q, Hq, d))
+
+
+def test_decode_mq_single_query_is_decode_attn():
+    """q_len = 1 through the multi-query entry point is tq_decode_attn, bit for bit."""
+    d, Hq, Hkv = 128, 8, 2
+    lens = [3000, 40, 0, 1500]
+    D, S, params, bt, kp, vp = _build_cache(d, Hkv, lens, "bf16", seed=31)
+    B = len(lens)
+    q = _upload(np.random.default_rng(6).standard_normal((B, 1, Hq, d)).astype(np.float32), "bf16")
+    kp, vp, bt = torch.from_numpy(kp).to(DEV), torch.from_numpy(vp).to(DEV), torch.from_numpy(bt).to(DEV)
+    ctx = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    a = tq.decode_attn_mq(params, d, q, Hkv, kp, vp, bt, ctx, max(lens))
+    b = tq.decode_attn(params, d, q[:, 0].contiguous(), Hkv, kp, vp, bt, ctx, max(lens))
+    torch.cuda.synchronize()
+    assert torch.equal(a[:, 0], b)
+
+
+@pytest.mark.parametrize("d,Hq,Hkv,Q,dtype", [(128, 8, 2, 2, "bf16"), (128, 2, 2, 4, "f32"), (256, 4, 2, 2, "bf16")])
+def test_decode_step_mq_appends_then_attends(d, Hq, Hkv, Q, dtype):
+    """tq_decode_step_mq on a cache of pre_lens[b] tokens: the Q new tokens land at pre_lens[b] + i
+    (bit-exact against one tq_paged_append per token), the Q queries then equal tq_decode_attn_mq
+    over pre_lens + Q tokens bit for bit, and the oracle's multi-query attention within tolerance."""
+    pre = [15, 600, -1, 129, 0, 1022]
+    B = len(pre)
+    full = [p + Q if p >= 0 else 0 for p in pre]
+    D, S, params, _ = _params(d)
+    need = [max(1, -(-L // 16)) for L in full]
+    nblk = sum(need) + 2
+    perm = np.random.default_rng(19).permutation(nblk)
+    bt = np.zeros((B, max(need)), np.int32)
+    k0 = 0
+    for b, n in enumerate(need):
+        bt[b, :n] = perm[k0:k0 + n]
+        k0 += n
+    kp_pre = np.zeros((nblk, Hkv, oracle.record_bytes(True, d)), np.uint8)
+    vp_pre = np.zeros((nblk, Hkv, oracle.record_bytes(False, d)), np.uint8)
+    kp_full, vp_full = kp_pre.copy(), vp_pre.copy()
+    k_new = np.zeros((B, Q, Hkv, d), np.float32)
+    v_new = np.zeros((B, Q, Hkv, d), np.float32)
+    for b, L in enumerate(full):
+        if L == 0:
+            continue
+        rng = np.random.default_rng([29, b])
+        K = synth.round_dtype(rng.standard_normal((L, Hkv, d)).astype(np.float32) * 2, dtype)
+        V = synth.round_dtype(rng.standard_normal((L, Hkv, d)).astype(np.float32), dtype)
+        sl = synth.slots_for(bt, b, 0, L)
+        oracle.encode(True, D, S, K, sl, kp_full)
+        oracle.encode(False, D, S, V, sl, vp_full)
+        if L > Q:
+            oracle.encode(True, D, S, K[:-Q], sl[:-Q], kp_pre)
+            oracle.encode(False, D, S, V[:-Q], sl[:-Q], vp_pre)
+        k_new[b], v_new[b] = K[-Q:], V[-Q:]
+    q = synth.round_dtype(np.random.default_rng(37).standard_normal((B, Q, Hq, d)).astype(np.float32), dtype)
+    max_ctx = max(full)
+    dq, dk, dv = _upload(q, dtype), _upload(k_new, dtype), _upload(v_new, dtype)
+    dbt = torch.from_numpy(bt).to(DEV)
+    pre_t = torch.tensor(pre, dtype=torch.int32, device=DEV)
+    kp1, vp1 = torch.from_numpy(kp_pre).to(DEV), torch.from_numpy(vp_pre).to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = tq.decode_step_mq(params, d, dk, dv, dq, Hkv, kp1, vp1, dbt, pre_t, max_ctx, status=status)
+    kp2, vp2 = torch.from_numpy(kp_pre).to(DEV), torch.from_numpy(vp_pre).to(DEV)
+    for i in range(Q):
+        pos = torch.tensor([p + i if p >= 0 else -1 for p in pre], dtype=torch.int32, device=DEV)
+        tq.paged_append(params, d, dk[:, i].contiguous(), dv[:, i].contiguous(), dbt, pos, kp2, vp2)
+    full_t = torch.tensor(full, dtype=torch.int32, device=DEV)
+    want = tq.decode_attn_mq(params, d, dq, Hkv, kp2, vp2, dbt, full_t, max_ctx)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(kp1, kp2) and torch.equal(vp1, vp2)
+    assert torch.equal(out, want)
+    ref = oracle.decode_mq(D, S, q, Hkv, kp_full, vp_full, bt, np.array(full, np.int32))
+    o = out.cpu().numpy()
+    assert np.all(o[pre.index(-1)] == 0)
+    parity.check_attention(o.reshape(B * Q, Hq, d), ref.reshape(B * Q, Hq, d))
+
+
 def test_tiny_workload_end_to_end():
     """1 sequence, 1 head, d=128, 256 fp32 tokens with 20x outlier channels:
     GPU encode vs oracle encode, then GPU decode vs oracle decode of the

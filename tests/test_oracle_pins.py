@@ -361,6 +361,51 @@ def test_attention_special_cases():
     assert np.all(o == 0)
 
 
+def test_multi_query_decode_is_causal_over_the_new_tokens():
+    """decode_mq: query i of Q sees the cache up to token L - Q + i.  Pinned against a brute-force
+    softmax over the explicitly dequantised keys and values of the oracle's second formulation,
+    and by causality: rewriting the last cached token moves only the last query."""
+    d, Hkv, Hq, L, Q = 128, 2, 4, 40, 3
+    D, S, bt, kp, vp = _small_cache(d, 1, Hkv, [L], seed=8)
+    q = np.random.default_rng(4).standard_normal((1, Q, Hq, d)).astype(np.float32)
+    o = oracle.decode_mq(D, S, q, Hkv, kp, vp, bt, np.array([L], np.int32))
+    assert o.shape == (1, Q, Hq, d)
+    # query 0 of a Q = 1 call is the single-query decode
+    o1 = oracle.decode_mq(D, S, q[:, -1:], Hkv, kp, vp, bt, np.array([L], np.int32))
+    np.testing.assert_array_equal(o1[:, 0], oracle.decode(D, S, np.ascontiguousarray(q[:, -1]), Hkv, kp, vp, bt,
+                                                          np.array([L], np.int32)))
+    # brute force: dequantise every token (K with its QJL term) and run a plain softmax per prefix
+    slots = bt[0, np.arange(L) // 16].astype(np.int64) * 16 + np.arange(L) % 16
+    uk = oracle.unpack(True, d, kp, Hkv, slots)
+    uv = oracle.unpack(False, d, vp, Hkv, slots)
+    c = oracle.codebook()[0]
+    Sd = S.astype(np.float64)
+    G = Hq // Hkv
+    for h in range(Hq):
+        kv = h // G
+        keys = np.array([oracle.fp16_value(uk["n16"][t, kv]) * oracle.rotate_t(
+            D, c[uk["codes"][t, kv]] / math.sqrt(d) + math.sqrt(math.pi / 2) / d * oracle.fp16_value(
+                uk["g16"][t, kv]) * (Sd.T @ (2.0 * uk["signs"][t, kv] - 1))) for t in range(L)])
+        vals = np.array([_dequant_v(D, uv["codes"][t, kv], uv["n16"][t, kv], d) for t in range(L)])
+        for i in range(Q):
+            n = L - (Q - 1 - i)
+            s = keys[:n] @ q[0, i, h].astype(np.float64) / math.sqrt(d)
+            p = np.exp(s - s.max())
+            want = (p[:, None] * vals[:n]).sum(0) / p.sum()
+            np.testing.assert_allclose(o[0, i, h], want, rtol=1e-10, atol=1e-10)
+    # causality: a different last token changes query Q-1 only
+    kp2, vp2 = kp.copy(), vp.copy()
+    x = np.random.default_rng(77).standard_normal((1, Hkv, d)).astype(np.float32)
+    oracle.encode(True, D, S, x, slots[-1:], kp2)
+    oracle.encode(False, D, S, x, slots[-1:], vp2)
+    o2 = oracle.decode_mq(D, S, q, Hkv, kp2, vp2, bt, np.array([L], np.int32))
+    np.testing.assert_array_equal(o2[:, :Q - 1], o[:, :Q - 1])
+    assert np.abs(o2[:, Q - 1] - o[:, Q - 1]).max() > 1e-6
+    # a query with no token before it gets zeros
+    o3 = oracle.decode_mq(D, S, q, Hkv, kp, vp, bt, np.array([1], np.int32))
+    assert np.all(o3[:, :Q - 1] == 0) and np.abs(o3[:, Q - 1]).max() > 0
+
+
 def test_attention_ignores_physical_block_order():
     d, Hkv = 128, 2
     D, S, bt, kp, vp = _small_cache(d, 1, Hkv, [50], seed=5)

@@ -81,6 +81,14 @@ def _declare(L):
     L.tq_decode_step.restype = _I
     L.tq_decode_step.argtypes = [_P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _I, _P, _P, _I64, _P, _P, _SZ, _P,
                                  _P]
+    L.tq_decode_workspace_bytes_mq.restype = _SZ
+    L.tq_decode_workspace_bytes_mq.argtypes = [_I, _I, _I, _I, _I]
+    L.tq_decode_attn_mq.restype = _I
+    L.tq_decode_attn_mq.argtypes = [_P, _I, _P, _I, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _SZ,
+                                    _P, _P]
+    L.tq_decode_step_mq.restype = _I
+    L.tq_decode_step_mq.argtypes = [_P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _I, _P, _P, _I64, _P, _P,
+                                    _SZ, _P, _P]
     L.tq_decode_attn_noalloc.restype = _I
     L.tq_decode_attn_noalloc.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _P]
 
@@ -108,6 +116,10 @@ def v_record_bytes(d: int) -> int:
 
 def decode_workspace_bytes(d: int, batch: int, n_q_heads: int, max_ctx: int) -> int:
     return int(load_library().tq_decode_workspace_bytes(d, batch, n_q_heads, max_ctx))
+
+
+def decode_workspace_bytes_mq(d: int, batch: int, q_len: int, n_q_heads: int, max_ctx: int) -> int:
+    return int(load_library().tq_decode_workspace_bytes_mq(d, batch, q_len, n_q_heads, max_ctx))
 
 
 # ---------------------------------------------------------------- marshalling helpers
@@ -262,6 +274,50 @@ def decode_step(params, d: int, k_new, v_new, q, n_kv_heads: int, k_pool, v_pool
                                        _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(out), _ptr(workspace),
                                        workspace.numel(), _ptr(status), _stream(stream))
     _check(rc, "tq_decode_step")
+    return out
+
+
+def decode_attn_mq(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens, max_ctx: int,
+                   out=None, workspace=None, status=None, stream=None):
+    """tq_decode_attn_mq: q [batch][q_len][n_q_heads][d] -> out float32 of the same shape.
+
+    ctx_lens counts the q_len new tokens; query i attends ctx_lens[b] - (q_len - 1 - i) tokens."""
+    torch = _torch()
+    _need_cuda(params, q, k_pool, v_pool, block_table, ctx_lens, out, workspace, status)
+    B, Q, Hq = q.shape[0], q.shape[1], q.shape[2]
+    if out is None:
+        out = torch.empty((B, Q, Hq, d), dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes_mq(d, B, Q, Hq, max_ctx)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = load_library().tq_decode_attn_mq(_ptr(params), d, _ptr(q), _dtype_code(q), B, Q, Hq, n_kv_heads,
+                                          _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
+                                          block_table.shape[1], _ptr(ctx_lens), max_ctx, _ptr(out),
+                                          _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+    _check(rc, "tq_decode_attn_mq")
+    return out
+
+
+def decode_step_mq(params, d: int, k_new, v_new, q, n_kv_heads: int, k_pool, v_pool, block_table, pre_lens,
+                   max_ctx: int, out=None, workspace=None, status=None, stream=None):
+    """tq_decode_step_mq: append k_new/v_new [batch][q_len][n_kv_heads][d] at pre_lens[b] + i, then
+    query i of q [batch][q_len][n_q_heads][d] attends pre_lens[b] + 1 + i tokens."""
+    torch = _torch()
+    _need_cuda(params, k_new, v_new, q, k_pool, v_pool, block_table, pre_lens, out, workspace, status)
+    B, Q, Hq = q.shape[0], q.shape[1], q.shape[2]
+    if out is None:
+        out = torch.empty((B, Q, Hq, d), dtype=torch.float32, device=q.device)
+    need = decode_workspace_bytes_mq(d, B, Q, Hq, max_ctx)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if k_new.dtype != q.dtype or v_new.dtype != q.dtype:
+        raise TQError("k_new, v_new and q must share one dtype")
+    rc = load_library().tq_decode_step_mq(_ptr(params), d, _ptr(k_new), _ptr(v_new), _ptr(q), _dtype_code(q), B,
+                                          Q, Hq, n_kv_heads, _ptr(block_table), block_table.shape[1],
+                                          _ptr(pre_lens), max_ctx, _ptr(k_pool), _ptr(v_pool), k_pool.shape[0],
+                                          _ptr(out), _ptr(workspace), workspace.numel(), _ptr(status),
+                                          _stream(stream))
+    _check(rc, "tq_decode_step_mq")
     return out
 
 

@@ -166,28 +166,33 @@ size_t tq_decode_workspace_bytes(int d, int batch, int n_q_heads, int max_ctx) {
     return decode_workspace_bytes(d, batch, n_q_heads, max_ctx);
 }
 
-static int check_decode(const void *params, int d, int batch, int hq, int hkv, int max_ctx, void *ws,
+size_t tq_decode_workspace_bytes_mq(int d, int batch, int q_len, int n_q_heads, int max_ctx) {
+    if (q_len <= 0 || q_len > 8 || n_q_heads <= 0) return 0;
+    return decode_workspace_bytes(d, batch, q_len * n_q_heads, max_ctx);
+}
+
+static int check_decode(const void *params, int d, int batch, int q_len, int hq, int hkv, int max_ctx, void *ws,
                         size_t ws_bytes) {
     if (!valid_d(d)) return TQ_ERR_HEAD_DIM;
-    if (batch < 0 || hq <= 0 || hkv <= 0 || max_ctx < 0) return TQ_ERR_INVALID;
-    if (hq % hkv != 0 || hq / hkv > 8) return TQ_ERR_GQA;
+    if (batch < 0 || q_len <= 0 || hq <= 0 || hkv <= 0 || max_ctx < 0) return TQ_ERR_INVALID;
+    if (hq % hkv != 0 || q_len > 8 || q_len * (hq / hkv) > 8) return TQ_ERR_GQA;
     if (batch > 65535 || hkv > 65535) return TQ_ERR_INVALID;
     if (batch == 0) return TQ_OK;
     if (!params || !ws) return TQ_ERR_INVALID;
     if (!aligned16(params) || !aligned16(ws)) return TQ_ERR_ALIGN;
-    if (ws_bytes < decode_workspace_bytes(d, batch, hq, max_ctx)) return TQ_ERR_WORKSPACE;
+    if (ws_bytes < decode_workspace_bytes(d, batch, q_len * hq, max_ctx)) return TQ_ERR_WORKSPACE;
     return TQ_OK;
 }
 
 int tq_decode_qprep(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads, int n_kv_heads,
                     const int32_t *ctx_lens, int max_ctx, void *workspace, size_t workspace_bytes,
                     tq_stream_t stream) {
-    int rc = check_decode(params, d, batch, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
+    int rc = check_decode(params, d, batch, 1, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
     if (rc != TQ_OK || batch == 0) return rc;
     if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16) return TQ_ERR_DTYPE;
     if (!q) return TQ_ERR_INVALID;
     if (!ctx_lens) return TQ_ERR_INVALID;
-    return cuda_status(launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx,
+    return cuda_status(launch_qprep(d, dtype, params, q, batch, 1, n_q_heads, n_kv_heads, ctx_lens, max_ctx,
                                     workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -195,47 +200,67 @@ int tq_decode_splitk(const void *params, int d, int batch, int n_q_heads, int n_
                      const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
                      const int32_t *ctx_lens, int max_ctx, float *out, void *workspace, size_t workspace_bytes,
                      int32_t *status, tq_stream_t stream) {
-    int rc = check_decode(params, d, batch, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
+    int rc = check_decode(params, d, batch, 1, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
     if (rc != TQ_OK || batch == 0) return rc;
     if (max_blocks <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
     if (!k_pool || !v_pool || !block_table || !ctx_lens || !out) return TQ_ERR_INVALID;
     if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
-    return cuda_status(launch_splitk(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks,
+    return cuda_status(launch_splitk(d, params, batch, 1, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks,
                                      block_table, max_blocks, ctx_lens, 0, max_ctx, out, workspace, status,
                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int tq_decode_attn_mq(const void *params, int d, const void *q, int dtype, int batch, int q_len, int n_q_heads,
+                      int n_kv_heads, const void *k_pool, const void *v_pool, int64_t num_blocks,
+                      const int32_t *block_table, int max_blocks, const int32_t *ctx_lens, int max_ctx, float *out,
+                      void *workspace, size_t workspace_bytes, int32_t *status, tq_stream_t stream) {
+    if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16 && valid_d(d)) return TQ_ERR_DTYPE;
+    int rc = check_decode(params, d, batch, q_len, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
+    if (rc != TQ_OK || batch == 0) return rc;
+    if (max_blocks <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
+    if (!q || !k_pool || !v_pool || !block_table || !ctx_lens || !out) return TQ_ERR_INVALID;
+    if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_qprep(d, dtype, params, q, batch, q_len, n_q_heads, n_kv_heads, ctx_lens, max_ctx,
+                                 workspace, st);
+    if (e == cudaSuccess)
+        e = launch_splitk(d, params, batch, q_len, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
+                          max_blocks, ctx_lens, 0, max_ctx, out, workspace, status, st);
+    return cuda_status(e);
 }
 
 int tq_decode_attn(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads, int n_kv_heads,
                    const void *k_pool, const void *v_pool, int64_t num_blocks, const int32_t *block_table,
                    int max_blocks, const int32_t *ctx_lens, int max_ctx, float *out, void *workspace,
                    size_t workspace_bytes, int32_t *status, tq_stream_t stream) {
+    return tq_decode_attn_mq(params, d, q, dtype, batch, 1, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks,
+                             block_table, max_blocks, ctx_lens, max_ctx, out, workspace, workspace_bytes, status,
+                             stream);
+}
+
+int tq_decode_step_mq(const void *params, int d, const void *k_new, const void *v_new, const void *q, int dtype,
+                      int batch, int q_len, int n_q_heads, int n_kv_heads, const int32_t *block_table,
+                      int max_blocks, const int32_t *pre_lens, int max_ctx, void *k_pool, void *v_pool,
+                      int64_t num_blocks, float *out, void *workspace, size_t workspace_bytes, int32_t *status,
+                      tq_stream_t stream) {
     if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16 && valid_d(d)) return TQ_ERR_DTYPE;
-    int rc = check_decode(params, d, batch, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
+    int rc = check_decode(params, d, batch, q_len, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
     if (rc != TQ_OK || batch == 0) return rc;
     if (max_blocks <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
-    if (!q || !k_pool || !v_pool || !block_table || !ctx_lens || !out) return TQ_ERR_INVALID;
+    if (!k_new || !v_new || !q || !k_pool || !v_pool || !block_table || !pre_lens || !out) return TQ_ERR_INVALID;
     if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx, workspace, st);
-    if (e == cudaSuccess)
-        e = launch_splitk(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
-                          max_blocks, ctx_lens, 0, max_ctx, out, workspace, status, st);
-    return cuda_status(e);
+    return cuda_status(launch_step(d, dtype, params, k_new, v_new, q, batch, q_len, n_q_heads, n_kv_heads,
+                                   block_table, max_blocks, pre_lens, max_ctx, k_pool, v_pool, num_blocks, out,
+                                   workspace, status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int tq_decode_step(const void *params, int d, const void *k_new, const void *v_new, const void *q, int dtype,
                    int batch, int n_q_heads, int n_kv_heads, const int32_t *block_table, int max_blocks,
                    const int32_t *pre_lens, int max_ctx, void *k_pool, void *v_pool, int64_t num_blocks, float *out,
                    void *workspace, size_t workspace_bytes, int32_t *status, tq_stream_t stream) {
-    if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16 && valid_d(d)) return TQ_ERR_DTYPE;
-    int rc = check_decode(params, d, batch, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
-    if (rc != TQ_OK || batch == 0) return rc;
-    if (max_blocks <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
-    if (!k_new || !v_new || !q || !k_pool || !v_pool || !block_table || !pre_lens || !out) return TQ_ERR_INVALID;
-    if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
-    return cuda_status(launch_step(d, dtype, params, k_new, v_new, q, batch, n_q_heads, n_kv_heads, block_table,
-                                   max_blocks, pre_lens, max_ctx, k_pool, v_pool, num_blocks, out, workspace, status,
-                                   reinterpret_cast<cudaStream_t>(stream)));
+    return tq_decode_step_mq(params, d, k_new, v_new, q, dtype, batch, 1, n_q_heads, n_kv_heads, block_table,
+                             max_blocks, pre_lens, max_ctx, k_pool, v_pool, num_blocks, out, workspace,
+                             workspace_bytes, status, stream);
 }
 
 }  // extern "C"

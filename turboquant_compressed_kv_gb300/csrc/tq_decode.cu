@@ -51,11 +51,11 @@ namespace {
 // ---------------------------------------------------------------- (1) query prep (body in tq_prep.cuh)
 template <int D, int NTK, typename T>
 __global__ void __launch_bounds__(128)
-qprep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ q, int batch, int hq, int hkv,
+qprep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ q, int batch, int q_len, int hq, int hkv,
              const int32_t *__restrict__ ctx_lens, int max_ctx, int chunk, int P, uint8_t *__restrict__ packs,
              unsigned int *__restrict__ counters, int64_t *__restrict__ cpre, int32_t *__restrict__ cta_b) {
     extern __shared__ __align__(16) uint8_t qsm[];
-    qprep_rows<D, NTK, T>(params, q, batch, hq, hkv, ctx_lens, 0, max_ctx, chunk, P, packs, counters, cpre, cta_b,
+    qprep_rows<D, NTK, T>(params, q, batch, q_len, hq, hkv, ctx_lens, 0, max_ctx, chunk, P, packs, counters, cpre, cta_b,
                           blockIdx.x, qsm);
 }
 
@@ -90,7 +90,7 @@ constexpr size_t split_smem_bytes() {
 #endif
 template <int D, int G, int NWARP>
 __global__ void __launch_bounds__(NWARP * 32, (NWARP == 4 ? (D == 128 && G <= 4 ? TQ_SPLITK_MINBLOCKS : TQ_SPLITK_MINBLOCKS_WIDE) : 1))
-decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ packs, int batch, int hq, int hkv,
+decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ packs, int batch, int q_len, int hq, int hkv,
                   const uint8_t *__restrict__ k_pool, const uint8_t *__restrict__ v_pool, int64_t num_blocks,
                   const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_lens,
                   int ctx_add, int max_ctx, const int64_t *__restrict__ cpre, const int32_t *__restrict__ cta_b,
@@ -126,7 +126,7 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
     // sequences with nothing to attend get out = 0
     for (int b = cta; b < batch; b += gridDim.x)
         if (attended_len(ctx_lens[b], ctx_add, max_ctx) == 0)
-            for (int i = tid; i < hq * D; i += NT_) out[(size_t)b * hq * D + i] = 0.f;
+            for (int i = tid; i < q_len * hq * D; i += NT_) out[(size_t)b * q_len * hq * D + i] = 0.f;
 
     // P CTAs share the W chunks, at least one chunk each (as in build_schedule)
     const int64_t W = cpre[batch];
@@ -208,11 +208,13 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
                     bq[qu][ks][nt][1] = w.y;
                 }
         float cq[NTK], cu[NTK];
+        int tlim[NTK];   // tokens column hg attends in this segment (query i: L - (q_len - 1 - i))
 #pragma unroll
         for (int nt = 0; nt < NTK; ++nt) {
             const int hg = 4 * nt + tig;           // columns 2tig (hi) and 2tig+1 (lo) of n-tile nt
             cq[nt] = hg < G ? pf[hg] * Asum : 0.f;
             cu[nt] = hg < G ? pf[8 + hg] : 0.f;
+            tlim[nt] = hg < G ? min(t1, L - (q_len - 1 - hg / (G / q_len))) : 0;
         }
 
         // value sums of this warp's coordinates, planes combined, in the running weight scale
@@ -311,7 +313,7 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
                         const float dot_c = code2 - cq[nt];
                         const float dot_q = acc[4][nt][2 * r] + acc[4][nt][2 * r + 1] - cu[nt];
                         const int tl = kBlock * k + gid + 8 * r;           // token within the chunk
-                        const bool valid = ok && (tc + tl < t1);
+                        const bool valid = ok && (tc + tl < tlim[nt]);
                         const float sc = nrm[r] * inv_sd * (dot_c * inv_sd + gam[r] * qjl * dot_q);
                         if (hg < G) sS[tl * G + hg] = valid ? sc : -INFINITY;
                     }
@@ -458,14 +460,16 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
         }
         __syncthreads();
         const int lo = sk_cta_of(us, P, W), hi = sk_cta_of(ue - 1, P, W);
-        const size_t row0 = (size_t)b * hq + (size_t)kh * G;
+        // output row of operand column h: query h / gq of head kh * gq + h % gq
+        const int gq = G / q_len;
+        auto out_row = [&](int h) { return ((size_t)b * q_len + h / gq) * hq + (size_t)kh * gq + h % gq; };
         if (lo == hi) {
             // the whole (sequence, kv head) was in this CTA: finish it here
             for (int h = warp; h < G; h += NWARP) {
                 float v[R];
 #pragma unroll
                 for (int r = 0; r < R; ++r) v[r] = sAcc[h * D + 32 * r + lane];
-                finish_row<D>(v, sL[h], params, out + (row0 + h) * D, lane);
+                finish_row<D>(v, sL[h], params, out + out_row(h) * D, lane);
             }
         } else {
             // leave a partial in this CTA's slot (0: its first segment, 1: its last)
@@ -512,7 +516,7 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
 #pragma unroll
                         for (int r = 0; r < R; ++r) v[r] = fmaf(__ldcg(ps + 4 + 32 * r + lane), wgt, v[r]);
                     }
-                    finish_row<D>(v, l, params, out + (row0 + h) * D, lane);
+                    finish_row<D>(v, l, params, out + out_row(h) * D, lane);
                 }
             }
         }
@@ -581,28 +585,29 @@ int pass_ctas_any(int d, int G) {
 }
 
 template <int D, int NTK, typename T>
-cudaError_t qprep_launch_t(const uint8_t *P, const void *q, int batch, int hq, int hkv, const int32_t *ctx_lens,
-                           int max_ctx, int nctas, const WsLayout &w, cudaStream_t st) {
+cudaError_t qprep_launch_t(const uint8_t *P, const void *q, int batch, int q_len, int hq, int hkv,
+                           const int32_t *ctx_lens, int max_ctx, int nctas, const WsLayout &w, cudaStream_t st) {
     constexpr size_t smem = qprep_smem<D>();
     auto kern = qprep_kernel<D, NTK, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<(batch * hq + kQRows - 1) / kQRows, 128, smem, st>>>(P, (const T *)q, batch, hq, hkv, ctx_lens, max_ctx,
-                                                               pass_chunk(hq / hkv), nctas, w.packs, w.counters,
-                                                               w.cpre, w.cta_b);
+    kern<<<(batch * q_len * hq + kQRows - 1) / kQRows, 128, smem, st>>>(P, (const T *)q, batch, q_len, hq, hkv, ctx_lens,
+                                                                       max_ctx, pass_chunk(q_len * hq / hkv), nctas,
+                                                                       w.packs, w.counters, w.cpre, w.cta_b);
     return cudaGetLastError();
 }
 
 template <int D, typename T>
-cudaError_t qprep_launch(const uint8_t *P, const void *q, int batch, int hq, int hkv, const int32_t *ctx_lens,
-                         int max_ctx, int nctas, const WsLayout &w, cudaStream_t st) {
-    // n-tile count of the K-side operand: (2G + 7) / 8, as in decode_mma_kernel
-    if (hq / hkv <= 4) return qprep_launch_t<D, 1, T>(P, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w, st);
-    return qprep_launch_t<D, 2, T>(P, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w, st);
+cudaError_t qprep_launch(const uint8_t *P, const void *q, int batch, int q_len, int hq, int hkv,
+                         const int32_t *ctx_lens, int max_ctx, int nctas, const WsLayout &w, cudaStream_t st) {
+    // n-tile count of the K-side operand: (2G + 7) / 8 for G = q_len * hq / hkv columns, as in the passes
+    if (q_len * hq / hkv <= 4)
+        return qprep_launch_t<D, 1, T>(P, q, batch, q_len, hq, hkv, ctx_lens, max_ctx, nctas, w, st);
+    return qprep_launch_t<D, 2, T>(P, q, batch, q_len, hq, hkv, ctx_lens, max_ctx, nctas, w, st);
 }
 
 template <int D, int G>
-cudaError_t pass_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batch, int hq, int hkv,
+cudaError_t pass_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
                           const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
                           const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
                           int32_t *status) {
@@ -611,17 +616,17 @@ cudaError_t pass_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batc
     auto kern = decode_mma_kernel<D, G, NWARP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<nctas, NWARP * 32, smem, st>>>(P, w.packs, batch, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx,
+    kern<<<nctas, NWARP * 32, smem, st>>>(P, w.packs, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx,
                                          w.cpre, w.cta_b, w.part, w.counters, out, status);
     return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int hq, int hkv,
+cudaError_t pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
                         const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
                         const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
                         int32_t *status) {
-#define TQ_PASS(GG) return pass_launch_g<D, GG>(nctas, st, P, batch, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out, status)
+#define TQ_PASS(GG) return pass_launch_g<D, GG>(nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out, status)
     switch (G) {
         case 1: TQ_PASS(1);
         case 2: TQ_PASS(2);
@@ -637,37 +642,37 @@ cudaError_t pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int
 
 }  // namespace
 
-cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv,
-                         const int32_t *ctx_lens, int max_ctx, void *ws, cudaStream_t st) {
-    const WsLayout w = ws_layout(ws, d, batch, hq);
-    const int nctas = pass_ctas_any(d, hq / hkv);
+cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int q_len, int hq,
+                         int hkv, const int32_t *ctx_lens, int max_ctx, void *ws, cudaStream_t st) {
+    const WsLayout w = ws_layout(ws, d, batch, q_len * hq);
+    const int nctas = pass_ctas_any(d, q_len * hq / hkv);
     if (nctas <= 0) return cudaErrorInvalidConfiguration;
     const uint8_t *P = (const uint8_t *)params;
     if (d == 128)
         return dtype == TQ_DTYPE_BF16
-                   ? qprep_launch<128, __nv_bfloat16>(P, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w, st)
-                   : qprep_launch<128, float>(P, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w, st);
+                   ? qprep_launch<128, __nv_bfloat16>(P, q, batch, q_len, hq, hkv, ctx_lens, max_ctx, nctas, w, st)
+                   : qprep_launch<128, float>(P, q, batch, q_len, hq, hkv, ctx_lens, max_ctx, nctas, w, st);
     return dtype == TQ_DTYPE_BF16
-               ? qprep_launch<256, __nv_bfloat16>(P, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w, st)
-               : qprep_launch<256, float>(P, q, batch, hq, hkv, ctx_lens, max_ctx, nctas, w, st);
+               ? qprep_launch<256, __nv_bfloat16>(P, q, batch, q_len, hq, hkv, ctx_lens, max_ctx, nctas, w, st)
+               : qprep_launch<256, float>(P, q, batch, q_len, hq, hkv, ctx_lens, max_ctx, nctas, w, st);
 }
 
-cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
+cudaError_t launch_splitk(int d, const void *params, int batch, int q_len, int hq, int hkv, const void *k_pool,
                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
                           const int32_t *ctx_lens, int ctx_add, int max_ctx, float *out, void *ws, int32_t *status,
                           cudaStream_t st) {
-    const WsLayout w = ws_layout(ws, d, batch, hq);
-    const int G = hq / hkv;
+    const WsLayout w = ws_layout(ws, d, batch, q_len * hq);
+    const int G = q_len * hq / hkv;   // operand columns per kv head
     const int nctas = pass_ctas_any(d, G);
     if (nctas <= 0) return cudaErrorInvalidConfiguration;
     const uint8_t *P = (const uint8_t *)params;
     if (d == 128 && TQ_DECODE_WARP)
-        return warp_pass_launch(G, nctas, st, P, batch, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
+        return warp_pass_launch(G, nctas, st, P, batch, q_len, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
                                 num_blocks, block_table, max_blocks, ctx_lens, ctx_add, max_ctx, w, out, status);
     if (d == 128)
-        return pass_launch<128>(G, nctas, st, P, batch, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
+        return pass_launch<128>(G, nctas, st, P, batch, q_len, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
                                 num_blocks, block_table, max_blocks, ctx_lens, ctx_add, max_ctx, w, out, status);
-    return pass_launch<256>(G, nctas, st, P, batch, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
+    return pass_launch<256>(G, nctas, st, P, batch, q_len, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
                             num_blocks, block_table, max_blocks, ctx_lens, ctx_add, max_ctx, w, out, status);
 }
 
@@ -681,7 +686,7 @@ constexpr int kAppendTile = 4;
 template <int D, int NTK, typename T>
 __global__ void __launch_bounds__(128)
 step_prep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ k_new, const T *__restrict__ v_new,
-                 const T *__restrict__ q, int batch, int hq, int hkv, SlotMap map, uint8_t *__restrict__ k_pool,
+                 const T *__restrict__ q, int batch, int q_len, int hq, int hkv, SlotMap map, uint8_t *__restrict__ k_pool,
                  uint8_t *__restrict__ v_pool, int n_app, int max_ctx, int chunk, int P, uint8_t *__restrict__ packs,
                  unsigned int *__restrict__ counters, int64_t *__restrict__ cpre, int32_t *__restrict__ cta_b,
                  int32_t *status) {
@@ -689,67 +694,71 @@ step_prep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ k_new
     const int blk = blockIdx.x;
     if (blk < 2 * n_app) {
         const bool is_k = blk < n_app;
-        encode_tiles<D, kAppendTile, T>(params, is_k ? k_new : v_new, (int64_t)batch * hkv, map,
+        encode_tiles<D, kAppendTile, T>(params, is_k ? k_new : v_new, (int64_t)batch * q_len * hkv, map,
                                         is_k ? k_pool : v_pool, is_k, is_k, is_k ? blk : blk - n_app, n_app, smem,
                                         status);
     } else {
-        qprep_rows<D, NTK, T>(params, q, batch, hq, hkv, map.ctx_lens, 1, max_ctx, chunk, P, packs, counters, cpre,
+        qprep_rows<D, NTK, T>(params, q, batch, q_len, hq, hkv, map.ctx_lens, q_len, max_ctx, chunk, P, packs, counters, cpre,
                               cta_b, blk - 2 * n_app, smem);
     }
 }
 
 template <int D, int NTK, typename T>
 cudaError_t step_prep_launch(const uint8_t *P, const void *k_new, const void *v_new, const void *q, int batch,
-                             int hq, int hkv, const SlotMap &map, void *kp, void *vp, int max_ctx, int nctas,
-                             const WsLayout &w, int32_t *status, cudaStream_t st) {
+                             int q_len, int hq, int hkv, const SlotMap &map, void *kp, void *vp, int max_ctx,
+                             int nctas, const WsLayout &w, int32_t *status, cudaStream_t st) {
     constexpr size_t es = EncSmem<D, kAppendTile>::kBytes, qs = qprep_smem<D>();
     constexpr size_t smem = es > qs ? es : qs;
     auto kern = step_prep_kernel<D, NTK, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int n_app = (batch * hkv + kAppendTile - 1) / kAppendTile;
-    const int n_q = (batch * hq + kQRows - 1) / kQRows;
-    kern<<<2 * n_app + n_q, 128, smem, st>>>(P, (const T *)k_new, (const T *)v_new, (const T *)q, batch, hq, hkv, map,
-                                             (uint8_t *)kp, (uint8_t *)vp, n_app, max_ctx, pass_chunk(hq / hkv),
-                                             nctas, w.packs, w.counters, w.cpre, w.cta_b, status);
+    const int n_app = (batch * q_len * hkv + kAppendTile - 1) / kAppendTile;
+    const int n_q = (batch * q_len * hq + kQRows - 1) / kQRows;
+    kern<<<2 * n_app + n_q, 128, smem, st>>>(P, (const T *)k_new, (const T *)v_new, (const T *)q, batch, q_len, hq,
+                                             hkv, map, (uint8_t *)kp, (uint8_t *)vp, n_app, max_ctx,
+                                             pass_chunk(q_len * hq / hkv), nctas, w.packs, w.counters, w.cpre, w.cta_b,
+                                             status);
     return cudaGetLastError();
 }
 
 template <int D, typename T>
-cudaError_t step_prep_any(const uint8_t *P, const void *k_new, const void *v_new, const void *q, int batch, int hq,
-                          int hkv, const SlotMap &map, void *kp, void *vp, int max_ctx, int nctas, const WsLayout &w,
-                          int32_t *status, cudaStream_t st) {
-    if (hq / hkv <= 4)
-        return step_prep_launch<D, 1, T>(P, k_new, v_new, q, batch, hq, hkv, map, kp, vp, max_ctx, nctas, w, status, st);
-    return step_prep_launch<D, 2, T>(P, k_new, v_new, q, batch, hq, hkv, map, kp, vp, max_ctx, nctas, w, status, st);
+cudaError_t step_prep_any(const uint8_t *P, const void *k_new, const void *v_new, const void *q, int batch, int q_len,
+                          int hq, int hkv, const SlotMap &map, void *kp, void *vp, int max_ctx, int nctas,
+                          const WsLayout &w, int32_t *status, cudaStream_t st) {
+    if (q_len * hq / hkv <= 4)
+        return step_prep_launch<D, 1, T>(P, k_new, v_new, q, batch, q_len, hq, hkv, map, kp, vp, max_ctx, nctas, w,
+                                         status, st);
+    return step_prep_launch<D, 2, T>(P, k_new, v_new, q, batch, q_len, hq, hkv, map, kp, vp, max_ctx, nctas, w,
+                                     status, st);
 }
 }  // namespace
 
 cudaError_t launch_step(int d, int dtype, const void *params, const void *k_new, const void *v_new, const void *q,
-                        int batch, int hq, int hkv, const int32_t *block_table, int max_blocks,
+                        int batch, int q_len, int hq, int hkv, const int32_t *block_table, int max_blocks,
                         const int32_t *pre_lens, int max_ctx, void *k_pool, void *v_pool, int64_t num_blocks,
                         float *out, void *ws, int32_t *status, cudaStream_t st) {
-    const WsLayout w = ws_layout(ws, d, batch, hq);
-    const int nctas = pass_ctas_any(d, hq / hkv);
+    const WsLayout w = ws_layout(ws, d, batch, q_len * hq);
+    const int nctas = pass_ctas_any(d, q_len * hq / hkv);
     if (nctas <= 0) return cudaErrorInvalidConfiguration;
     const uint8_t *P = (const uint8_t *)params;
-    const SlotMap map{nullptr, block_table, pre_lens, max_blocks, num_blocks, hkv};
+    SlotMap map{nullptr, block_table, pre_lens, max_blocks, num_blocks, hkv};
+    map.q_len = q_len;
     cudaError_t e;
     if (d == 128)
         e = dtype == TQ_DTYPE_BF16
-                ? step_prep_any<128, __nv_bfloat16>(P, k_new, v_new, q, batch, hq, hkv, map, k_pool, v_pool, max_ctx,
-                                                    nctas, w, status, st)
-                : step_prep_any<128, float>(P, k_new, v_new, q, batch, hq, hkv, map, k_pool, v_pool, max_ctx, nctas, w,
-                                            status, st);
+                ? step_prep_any<128, __nv_bfloat16>(P, k_new, v_new, q, batch, q_len, hq, hkv, map, k_pool, v_pool,
+                                                    max_ctx, nctas, w, status, st)
+                : step_prep_any<128, float>(P, k_new, v_new, q, batch, q_len, hq, hkv, map, k_pool, v_pool, max_ctx,
+                                            nctas, w, status, st);
     else
         e = dtype == TQ_DTYPE_BF16
-                ? step_prep_any<256, __nv_bfloat16>(P, k_new, v_new, q, batch, hq, hkv, map, k_pool, v_pool, max_ctx,
-                                                    nctas, w, status, st)
-                : step_prep_any<256, float>(P, k_new, v_new, q, batch, hq, hkv, map, k_pool, v_pool, max_ctx, nctas, w,
-                                            status, st);
+                ? step_prep_any<256, __nv_bfloat16>(P, k_new, v_new, q, batch, q_len, hq, hkv, map, k_pool, v_pool,
+                                                    max_ctx, nctas, w, status, st)
+                : step_prep_any<256, float>(P, k_new, v_new, q, batch, q_len, hq, hkv, map, k_pool, v_pool, max_ctx,
+                                            nctas, w, status, st);
     if (e != cudaSuccess) return e;
-    return launch_splitk(d, params, batch, hq, hkv, k_pool, v_pool, num_blocks, block_table, max_blocks, pre_lens, 1,
-                         max_ctx, out, ws, status, st);
+    return launch_splitk(d, params, batch, q_len, hq, hkv, k_pool, v_pool, num_blocks, block_table, max_blocks,
+                         pre_lens, q_len, max_ctx, out, ws, status, st);
 }
 
 }  // namespace tq

@@ -79,7 +79,7 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 
 template <int G>
 __global__ void __launch_bounds__(kWWarps * 32, G <= 4 ? TQ_WARP_MINBLOCKS : TQ_WARP_MINBLOCKS_WIDE)
-decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ packs, int batch, int hq, int hkv,
+decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ packs, int batch, int q_len, int hq, int hkv,
                    const uint8_t *__restrict__ k_pool, const uint8_t *__restrict__ v_pool, int64_t num_blocks,
                    const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_lens,
                    int ctx_add, int max_ctx, const int64_t *__restrict__ cpre, const int32_t *__restrict__ cta_b,
@@ -107,7 +107,7 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
 
     for (int b = cta; b < batch; b += gridDim.x)
         if (attended_len(ctx_lens[b], ctx_add, max_ctx) == 0)
-            for (int i = tid; i < hq * D; i += NT) out[(size_t)b * hq * D + i] = 0.f;
+            for (int i = tid; i < q_len * hq * D; i += NT) out[(size_t)b * q_len * hq * D + i] = 0.f;
 
     const int64_t W = cpre[batch];
     const int P = (int)(W < (int64_t)gridDim.x ? W : (int64_t)gridDim.x);
@@ -125,7 +125,7 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
 
     // The CTA's range [g0, g1) of global chunks, walked one (sequence, kv head) segment at a time.
     struct Seg {
-        int b, kh, t0, t1;
+        int b, kh, t0, t1, L;
         int64_t us, ue, se;
     };
     auto make_seg = [&](int b, int kh, int64_t ub, int nchb, int64_t g) {
@@ -136,7 +136,8 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
         s.ue = s.us + nchb;
         s.se = (g1 < s.ue) ? g1 : s.ue;
         s.t0 = (int)(g - s.us) * CH;
-        s.t1 = min(attended_len(ctx_lens[b], ctx_add, max_ctx), (int)(s.se - s.us) * CH);
+        s.L = attended_len(ctx_lens[b], ctx_add, max_ctx);
+        s.t1 = min(s.L, (int)(s.se - s.us) * CH);
         return s;
     };
     // the segment after s, if the range has one
@@ -228,11 +229,13 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                     }
         }
         float cq[NTK], cu[NTK];
+        int tlim[NTK];   // tokens column 4 nt + tig attends in this segment (query i: L - (q_len - 1 - i))
 #pragma unroll
         for (int nt = 0; nt < NTK; ++nt) {
             const int hg = 4 * nt + tig;
             cq[nt] = hg < G ? pf[hg] * Asum : 0.f;
             cu[nt] = hg < G ? pf[8 + hg] : 0.f;
+            tlim[nt] = hg < G ? min(t1, s.L - (q_len - 1 - hg / (G / q_len))) : 0;
         }
 
         // running value sums (fp32 adds of the per-block mma results) and offset sums
@@ -357,7 +360,7 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                                 code2 = fmaf(A[m], acc[m][nt][2 * r] + acc[m][nt][2 * r + 1], code2);
                             const float dot_c = code2 - cq[nt];
                             const float dot_q = acc[4][nt][2 * r] + acc[4][nt][2 * r + 1] - cu[nt];
-                            const bool valid = ok && (tb + gid + 8 * r < t1) && hg < G;
+                            const bool valid = ok && (tb + gid + 8 * r < tlim[nt]);
                             s2[nt][r] = valid ? nrm[r] * c_sc * (dot_c * inv_sd + gam[r] * qjl * dot_q) : -INFINITY;
                         }
                     }
@@ -580,13 +583,15 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
         __syncthreads();
 
         const int lo = sk_cta_of(us, P, W), hi = sk_cta_of(ue - 1, P, W);
-        const size_t row0 = (size_t)b * hq + (size_t)kh * G;
+        // output row of operand column h: query h / gq of head kh * gq + h % gq
+        const int gq = G / q_len;
+        auto out_row = [&](int h) { return ((size_t)b * q_len + h / gq) * hq + (size_t)kh * gq + h % gq; };
         if (lo == hi) {
             for (int h = warp; h < G; h += NWARP) {
                 float v[R];
 #pragma unroll
                 for (int r = 0; r < R; ++r) v[r] = sAcc[h * D + 32 * r + lane];
-                finish_row<D>(v, sL[h], params, out + (row0 + h) * D, lane);
+                finish_row<D>(v, sL[h], params, out + out_row(h) * D, lane);
             }
         } else {
             const int slot = first_seg ? 0 : 1;
@@ -630,7 +635,7 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
 #pragma unroll
                         for (int r = 0; r < R; ++r) v[r] = fmaf(__ldcg(ps + 4 + 32 * r + lane), wgt, v[r]);
                     }
-                    finish_row<D>(v, l, params, out + (row0 + h) * D, lane);
+                    finish_row<D>(v, l, params, out + out_row(h) * D, lane);
                 }
             }
         }
@@ -655,7 +660,7 @@ int warp_ctas_g() {
 }
 
 template <int G>
-cudaError_t warp_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batch, int hq, int hkv,
+cudaError_t warp_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
                           const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
                           const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
                           int32_t *status) {
@@ -663,7 +668,7 @@ cudaError_t warp_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batc
     auto kern = decode_warp_kernel<G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<nctas, kWWarps * 32, smem, st>>>(P, w.packs, batch, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx,
+    kern<<<nctas, kWWarps * 32, smem, st>>>(P, w.packs, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx,
                                             w.cpre, w.cta_b, w.part, w.counters, out, status);
     return cudaGetLastError();
 }
@@ -683,11 +688,11 @@ int warp_pass_ctas(int G) {
     }
 }
 
-cudaError_t warp_pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int hq, int hkv,
+cudaError_t warp_pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
                              const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
                              const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
                              int32_t *status) {
-#define TQ_WPASS(GG) return warp_launch_g<GG>(nctas, st, P, batch, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out, status)
+#define TQ_WPASS(GG) return warp_launch_g<GG>(nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out, status)
     switch (G) {
         case 1: TQ_WPASS(1);
         case 2: TQ_WPASS(2);

@@ -302,14 +302,17 @@ cudaError_t launch_append(int d, int dtype, const void *params, const void *k_ne
                           int n_heads, const int32_t *bt, int max_blocks, const int32_t *ctx, void *kp, void *vp,
                           int64_t num_blocks, int32_t *status, cudaStream_t st);
 size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx);
-cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int hq, int hkv,
-                         const int32_t *ctx_lens, int max_ctx, void *ws, cudaStream_t st);
-cudaError_t launch_splitk(int d, const void *params, int batch, int hq, int hkv, const void *k_pool,
+// Decode launches take q_len queries per sequence (q[b][i][h], out[b][i][h]); query i attends
+// the first L - (q_len - 1 - i) of the sequence's L attended tokens.  The workspace is laid
+// out for batch sequences of q_len * hq query rows.
+cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int q_len, int hq,
+                         int hkv, const int32_t *ctx_lens, int max_ctx, void *ws, cudaStream_t st);
+cudaError_t launch_splitk(int d, const void *params, int batch, int q_len, int hq, int hkv, const void *k_pool,
                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
                           const int32_t *ctx_lens, int ctx_add, int max_ctx, float *out, void *ws, int32_t *status,
                           cudaStream_t st);
 cudaError_t launch_step(int d, int dtype, const void *params, const void *k_new, const void *v_new, const void *q,
-                        int batch, int hq, int hkv, const int32_t *block_table, int max_blocks,
+                        int batch, int q_len, int hq, int hkv, const int32_t *block_table, int max_blocks,
                         const int32_t *pre_lens, int max_ctx, void *k_pool, void *v_pool, int64_t num_blocks,
                         float *out, void *ws, int32_t *status, cudaStream_t st);
 

@@ -73,9 +73,9 @@ extern "C" int tq_decode_attn_noalloc(const void *params, int d, const void *q, 
     // call (the query-prep kernel also resets the split counters), so the
     // contents left by a previous call need no clearing.
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    e = launch_qprep(d, dtype, params, q, batch, n_q_heads, n_kv_heads, ctx_lens, max_ctx, ws, st);
+    e = launch_qprep(d, dtype, params, q, batch, 1, n_q_heads, n_kv_heads, ctx_lens, max_ctx, ws, st);
     if (e == cudaSuccess)
-        e = launch_splitk(d, params, batch, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
+        e = launch_splitk(d, params, batch, 1, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
                           max_blocks, ctx_lens, 0, max_ctx, out, ws, status, st);
     return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

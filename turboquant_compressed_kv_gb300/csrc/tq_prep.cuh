@@ -17,16 +17,19 @@ struct SlotMap {
     int max_blocks;
     int64_t num_blocks;
     int n_heads;
+    int q_len = 1;                         // append: tokens per sequence (token t is number t % q_len of sequence t / q_len)
     __device__ int64_t slot(int64_t token, int32_t *status, bool report) const {
         int64_t s = -1;
         if (slots) {
             s = slots[token];
             if (s < 0) return -1;
         } else {
-            const int Lb = ctx_lens[token];
-            if (Lb < 0) return -1;
+            const int64_t seq = token / q_len;
+            const int L0 = ctx_lens[seq];
+            if (L0 < 0) return -1;
+            const int Lb = L0 + (int)(token - seq * q_len);
             const int lb = Lb / kBlock;
-            const int64_t blk = (lb < max_blocks) ? (int64_t)block_table[(size_t)token * max_blocks + lb] : -1;
+            const int64_t blk = (lb < max_blocks) ? (int64_t)block_table[(size_t)seq * max_blocks + lb] : -1;
             s = (blk >= 0) ? blk * kBlock + (Lb % kBlock) : -2;
             if (s == -2) {   // no block for this position
                 if (report) flag_status(status, TQ_STATUS_BAD_SLOT);
@@ -273,11 +276,13 @@ template <int D> __host__ __device__ constexpr size_t qprep_smem() {
 
 // Rows 4*blk .. 4*blk+3 of the query prep, one CTA of 128 threads; `qsm` holds
 // qprep_smem<D>() bytes.  Block 0 also builds the pass's work schedule; ctx_add is added to
-// every non-negative length (1 when the step appends one token first).
+// every non-negative length (the number of tokens the step appends first).  With q_len > 1
+// queries per sequence (q[b][i][h]), query i of head hg of a kv head is operand column
+// i * G + hg of the kv head's pack.
 template <int D, int NTK, typename T>
 __device__ __forceinline__ void qprep_rows(const uint8_t *__restrict__ params, const T *__restrict__ q, int batch,
-                                           int hq, int hkv, const int32_t *__restrict__ ctx_lens, int ctx_add,
-                                           int max_ctx, int chunk, int P, uint8_t *__restrict__ packs,
+                                           int q_len, int hq, int hkv, const int32_t *__restrict__ ctx_lens,
+                                           int ctx_add, int max_ctx, int chunk, int P, uint8_t *__restrict__ packs,
                                            unsigned int *__restrict__ counters, int64_t *__restrict__ cpre,
                                            int32_t *__restrict__ cta_b, int blk, uint8_t *qsm) {
     constexpr int R = D / 32, NKS = D / 16, KPT = D / 128;
@@ -285,7 +290,7 @@ __device__ __forceinline__ void qprep_rows(const uint8_t *__restrict__ params, c
     float (*us)[D] = reinterpret_cast<float (*)[D]>(qsm + kQRows * D * 4);      // [kQRows][D] u
     float *sbuf = reinterpret_cast<float *>(qsm + 2 * kQRows * D * 4);         // S^T rows
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nrows = batch * hq, row0 = blk * kQRows;
+    const int nrows = batch * q_len * hq, row0 = blk * kQRows;
     const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
     const float *ST = reinterpret_cast<const float *>(params + params_off_ST(D));
     const float inv_sd = rsqrtf((float)D);
@@ -314,7 +319,9 @@ __device__ __forceinline__ void qprep_rows(const uint8_t *__restrict__ params, c
     __syncthreads();
     const int row = row0 + warp;
     if (row < nrows) {
-        const int b = row / hq, h = row % hq, G = hq / hkv, kvh = h / G, hg = h % G;
+        const int b = row / (hq * q_len), qi = (row / hq) % q_len, h = row % hq, G = hq / hkv, kvh = h / G;
+        const int hg = qi * G + h % G;                            // operand column of this query row
+        const int GQ = G * q_len;
         if (hg == 0 && lane == 0) counters[b * hkv + kvh] = 0u;   // completion counter of the pass
         float v[R], u[R];
 #pragma unroll
@@ -346,10 +353,10 @@ __device__ __forceinline__ void qprep_rows(const uint8_t *__restrict__ params, c
             cs = warp_sum(cs);
             if (lane == 0) pf[qu * 8 + hg] = cs;
         }
-        // columns beyond the group's 2*G are zero (written by the group's first head)
+        // columns beyond the group's 2*G*q_len are zero (written by the group's first row)
         if (hg == 0) {
             uint32_t *pw = reinterpret_cast<uint32_t *>(pack);
-            for (int col = 2 * G; col < 8 * NTK; ++col) {
+            for (int col = 2 * GQ; col < 8 * NTK; ++col) {
                 const int nt = col >> 3, gid = col & 7;
                 for (int i = lane; i < 2 * NKS * 8; i += 32) {
                     const int qu = i / (NKS * 8), s = (i / 8) % NKS, k = i % 8;

@@ -102,9 +102,10 @@ __device__ __forceinline__ void finish_row(float (&v)[D / 32], float l, const ui
 
 // The warp-local pass at d = 128 (tq_decode_warp.cu): persistent CTAs it runs with on the
 // current device, and its launch.  Same schedule, workspace and partial format as the
-// coordinate-split pass.
+// coordinate-split pass.  G counts operand columns: q_len queries x the query heads of a kv
+// head.
 int warp_pass_ctas(int G);
-cudaError_t warp_pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int hq, int hkv,
+cudaError_t warp_pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
                              const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
                              const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
                              int32_t *status);
