@@ -308,6 +308,67 @@ def extra_decode(name, steps, warmup, dev):
     return res
 
 
+def extra_verify(steps, warmup, dev, q_len=2):
+    """Speculative verify on the llama8b_decode shape: every sequence appends q_len draft tokens and
+    verifies them with q_len causal queries in one tq_decode_step_mq (one read of the cache)."""
+    import dataclasses
+
+    import torch
+
+    import turboquant_compressed_kv_gb300 as tq
+    from turboquant_compressed_kv_gb300 import synth
+    from turboquant_compressed_kv_gb300.cache import PagedCache
+    w0 = synth.workload("llama8b_decode")
+    w = dataclasses.replace(w0, prefill_lens=[L - q_len for L in w0.ctx_lens])
+    d, B, Hq, Hkv = w.head_dim, w.batch, w.n_q_heads, w.n_kv_heads
+    cache = PagedCache.create(w, dev)
+    cache.prefill_device()
+    per_cache = cache.k_pool.numel() + cache.v_pool.numel()
+    nrep = max(2, math.ceil(3 * L2_BYTES / per_cache))
+    pools = [(cache.k_pool, cache.v_pool)] + [(cache.k_pool.clone(), cache.v_pool.clone())
+                                              for _ in range(nrep - 1)]
+    g = torch.Generator(device=dev).manual_seed(1234)
+    k_new = torch.randn((B, q_len, Hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    v_new = torch.randn((B, q_len, Hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    q = torch.randn((B, q_len, Hq, d), generator=g, device=dev).to(torch.bfloat16)
+    pre = torch.tensor(w.prefill_lens, dtype=torch.int32, device=dev)
+    max_ctx = max(w.ctx_lens)
+    ws = torch.empty(tq.decode_workspace_bytes_mq(d, B, q_len, Hq, max_ctx), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, q_len, Hq, d), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        kp, vp = pools[i % nrep]
+        tq.decode_step_mq(cache.params, d, k_new, v_new, q, Hkv, kp, vp, cache.block_table, pre, max_ctx, out=out,
+                          workspace=ws, status=status)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the verify step")
+    ms = e0.elapsed_time(e1) / steps
+    nb = step_bytes(w0)
+    krec, vrec = (8 * d + 64) / 16, (6 * d + 32) / 16
+    step_b = nb["partial"] + q_len * (nb["q"] + nb["out"]) + q_len * B * Hkv * (2 * d * 2 + krec + vrec)
+    res = {"config": {"workload": "llama8b_verify", "batch": B, "q_len": q_len, "n_q_heads": Hq, "n_kv_heads": Hkv,
+                      "head_dim": d, "ctx": max_ctx, "drafts_appended_per_step": q_len,
+                      "l2": f"{nrep} cache copies cycled ({nrep * per_cache / 2**20:.0f} MiB > L2)"},
+           "value": round(step_b / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+           "queries_per_s": round(B * q_len * Hq / (ms * 1e-3), 1), "ms_per_step": round(ms, 6),
+           "steps": steps, "warmup": warmup, "launches_per_step": 2}
+    del pools, cache
+    torch.cuda.empty_cache()
+    return res
+
+
 def extra_encode(steps, warmup, dev):
     """Bulk encode of the prefill workload (8 x 32768 tokens x 8 kv heads, d=128, bf16) into paged storage."""
     import torch
@@ -535,6 +596,7 @@ def bench_tq(args):
         ksteps = max(3, min(args.steps, 200))
         line["workloads"] = {"ragged": extra_decode("ragged", ksteps, max(3, args.warmup), dev),
                              "long256": extra_decode("long256", ksteps, max(3, args.warmup), dev),
+                             "verify_q2": extra_verify(ksteps, max(3, args.warmup), dev),
                              "prefill_encode": extra_encode(max(3, min(args.steps, 50)), max(3, args.warmup), dev)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, dt, _ = run_cpu_oracle(w, 3, 1, 2)

@@ -131,6 +131,28 @@ int tq_paged_append(const void *params, int d, const void *k_new, const void *v_
                     const int32_t *ctx_lens, void *k_pool, void *v_pool, int64_t num_blocks,
                     int32_t *status, tq_stream_t stream);
 
+/* tq_dequant_k / tq_dequant_v -- dense vectors of whole paged blocks, for a prefill (or any
+ * dense attention) over a compressed prefix.  [README "TurboQuantization: KV Cache
+ * Compression" -> "The Algorithm": the codebook value of each rotated coordinate, plus for K
+ * the QJL estimate of the residual; README "Throughput & Inference Memory Profile": prompts
+ * are processed in chunks (chunked prefill), each chunk attending the cached prefix]
+ * For j < n_ids, slot t < 16 of block block_ids[j] and kv head h:
+ *   K: out[16 j + t][h] = n  Pi^T ( c[cell]/sqrt d + sqrt(pi/2)/d gamma S^T (2 sign - 1) )
+ *   V: out[16 j + t][h] = nv Pi^T ( c[cell]/sqrt d ),          Pi^T y = D (H y) / sqrt d,
+ * so that q . out_K / sqrt d is exactly the score tq_decode_attn computes and a softmax over
+ * these vectors is exactly its attention.
+ *   block_ids  device int32[n_ids]; an id outside [0, num_blocks) gives zeros for its 16 rows
+ *              and sets TQ_STATUS_BAD_SLOT in *status.
+ *   out        device [n_ids * 16][n_kv_heads][d] in out_dtype (TQ_DTYPE_F32 or TQ_DTYPE_BF16,
+ *              rounded to nearest even).  Slots never written hold whatever the pool held.
+ * Errors: TQ_ERR_HEAD_DIM, TQ_ERR_DTYPE, TQ_ERR_INVALID, TQ_ERR_ALIGN, TQ_ERR_CUDA. */
+int tq_dequant_k(const void *params, int d, const void *k_pool, int64_t num_blocks, int n_kv_heads,
+                 const int32_t *block_ids, int n_ids, void *out, int out_dtype, int32_t *status,
+                 tq_stream_t stream);
+int tq_dequant_v(const void *params, int d, const void *v_pool, int64_t num_blocks, int n_kv_heads,
+                 const int32_t *block_ids, int n_ids, void *out, int out_dtype, int32_t *status,
+                 tq_stream_t stream);
+
 /* Workspace bytes tq_decode_attn needs for this shape (0 for invalid sizes).
  * It depends on d, batch and n_q_heads only (max_ctx is checked, not used). */
 size_t tq_decode_workspace_bytes(int d, int batch, int n_q_heads, int max_ctx);

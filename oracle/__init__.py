@@ -293,3 +293,28 @@ def decode_mq(D, S, q: np.ndarray, Hkv: int, kpool, vpool, block_table, ctx_lens
         out[:, i] = decode(D, S, np.ascontiguousarray(q[:, i]), Hkv, kpool, vpool, block_table, li,
                            explicit=explicit, centroids=centroids)
     return out
+
+
+def dequant(is_k: bool, D, S, pool, H: int, block_ids, centroids=None):
+    """Dense vectors of whole blocks: [len(block_ids) * 16][H][d] fp64 (SwiftLM README,
+    "TurboQuantization: KV Cache Compression" -> "The Algorithm", each step undone):
+      K: n  Pi^T ( c[cell]/sqrt d + sqrt(pi/2)/d gamma S^T (2 sign - 1) )
+      V: nv Pi^T ( c[cell]/sqrt d )"""
+    d = len(D)
+    c = np.asarray(codebook()[0] if centroids is None else centroids, np.float64)
+    ids = np.asarray(block_ids, np.int64)
+    slots = (ids[:, None] * BLOCK + np.arange(BLOCK)).reshape(-1)
+    u = unpack(is_k, d, pool, H, slots)
+    f16 = lambda h: np.asarray(h, np.uint16).view(np.float16).astype(np.float64)
+    y = c[u["codes"]] / np.sqrt(d)                                   # [N][H][d]
+    if is_k:
+        bt = 2.0 * u["signs"].astype(np.float64) - 1.0
+        y = y + np.sqrt(np.pi / 2) / d * f16(u["g16"])[..., None] * (bt @ np.asarray(S, np.float64))
+    N = len(slots)
+    out = np.zeros((N, H, d), np.float64)
+    n = f16(u["n16"])
+    for i in range(N):
+        for h in range(H):
+            out[i, h] = n[i, h] * rotate_t(D, y[i, h])
+    return out
+

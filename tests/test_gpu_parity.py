@@ -394,6 +394,39 @@ def test_decode_step_mq_appends_then_attends(d, Hq, Hkv, Q, dtype):
     parity.check_attention(o.reshape(B * Q, Hq, d), ref.reshape(B * Q, Hq, d))
 
 
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("is_k", [True, False])
+def test_dequant_parity(d, is_k):
+    """Dense K / V of whole blocks against the oracle's reconstruction: fp32 output within 1e-5
+    relative per vector, bf16 output within one bf16 rounding of the fp32 result; a bad block
+    id gives zero rows and sets the status."""
+    Hkv = 3
+    lens = [40, 70, 16]
+    D, S, params, bt, kp, vp = _build_cache(d, Hkv, lens, "f32", seed=41 + d)
+    pool_np = kp if is_k else vp
+    pool = torch.from_numpy(pool_np).to(DEV)
+    ids_np = np.concatenate([bt[b, :-(-L // 16)] for b, L in enumerate(lens)]).astype(np.int32)
+    ids = torch.from_numpy(ids_np).to(DEV)
+    fn = tq.dequant_k if is_k else tq.dequant_v
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o32 = fn(params, d, pool, ids, out_dtype=torch.float32, status=status)
+    o16 = fn(params, d, pool, ids, out_dtype=torch.bfloat16, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oracle.dequant(is_k, D, S, pool_np, Hkv, ids_np)
+    g = o32.cpu().numpy().astype(np.float64)
+    err = np.linalg.norm(g - ref, axis=-1) / np.maximum(np.linalg.norm(ref, axis=-1), 1e-30)
+    assert err.max() < 1e-5, err.max()
+    b16 = o16.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(b16 - g) <= np.abs(g) * 2.0 ** -8 + 1e-30)
+    # an id outside the pool: zero rows, status flagged
+    bad = torch.tensor([ids_np[0], pool.shape[0] + 5], dtype=torch.int32, device=DEV)
+    ob = fn(params, d, pool, bad, out_dtype=torch.float32, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 1            # TQ_STATUS_BAD_SLOT
+    assert torch.all(ob[16:] == 0) and torch.equal(ob[:16], o32[:16])
+
+
 def test_tiny_workload_end_to_end():
     """1 sequence, 1 head, d=128, 256 fp32 tokens with 20x outlier channels:
     GPU encode vs oracle encode, then GPU decode vs oracle decode of the

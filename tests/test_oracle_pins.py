@@ -406,6 +406,33 @@ def test_multi_query_decode_is_causal_over_the_new_tokens():
     assert np.all(o3[:, :Q - 1] == 0) and np.abs(o3[:, Q - 1]).max() > 0
 
 
+def test_dequant_gives_the_decode_attention():
+    """Attention by a plain softmax over the dequantised K and V (numpy) equals the oracle's
+    rotated-domain decode (C) to 1e-12, and V's reconstruction error on Gaussian vectors is the
+    codebook MSE."""
+    d, Hkv, Hq, L = 128, 2, 4, 45
+    D, S, bt, kp, vp = _small_cache(d, 1, Hkv, [L], seed=12)
+    nb = -(-L // 16)
+    K = oracle.dequant(True, D, S, kp, Hkv, bt[0, :nb])[:L]
+    V = oracle.dequant(False, D, S, vp, Hkv, bt[0, :nb])[:L]
+    q = np.random.default_rng(6).standard_normal((1, Hq, d)).astype(np.float32)
+    o = oracle.decode(D, S, q, Hkv, kp, vp, bt, np.array([L], np.int32))
+    for h in range(Hq):
+        kv = h // (Hq // Hkv)
+        s = K[:, kv] @ q[0, h].astype(np.float64) / math.sqrt(d)
+        p = np.exp(s - s.max())
+        np.testing.assert_allclose(o[0, h], (p[:, None] * V[:, kv]).sum(0) / p.sum(), rtol=1e-12, atol=1e-12)
+    # V: E ||v - v~||^2 / ||v||^2 over Gaussian vectors is the Lloyd-Max MSE of N(0,1)
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((64, 1, d)).astype(np.float32)
+    pool = np.zeros((4, 1, oracle.record_bytes(False, d)), np.uint8)
+    oracle.encode(False, D, S, x, np.arange(64, dtype=np.int64), pool)
+    xr = oracle.dequant(False, D, S, pool, 1, np.arange(4))
+    err = np.sum((xr[:, 0] - x[:, 0]) ** 2, axis=1) / np.sum(x[:, 0].astype(np.float64) ** 2, axis=1)
+    mse = oracle.codebook()[2]
+    assert abs(err.mean() / mse - 1) < 0.1, (err.mean(), mse)
+
+
 def test_attention_ignores_physical_block_order():
     d, Hkv = 128, 2
     D, S, bt, kp, vp = _small_cache(d, 1, Hkv, [50], seed=5)

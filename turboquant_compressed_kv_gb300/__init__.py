@@ -89,6 +89,10 @@ def _declare(L):
     L.tq_decode_step_mq.restype = _I
     L.tq_decode_step_mq.argtypes = [_P, _I, _P, _P, _P, _I, _I, _I, _I, _I, _P, _I, _P, _I, _P, _P, _I64, _P, _P,
                                     _SZ, _P, _P]
+    for name in ("tq_dequant_k", "tq_dequant_v"):
+        f = getattr(L, name)
+        f.restype = _I
+        f.argtypes = [_P, _I, _P, _I64, _I, _P, _I, _P, _I, _P, _P]
     L.tq_decode_attn_noalloc.restype = _I
     L.tq_decode_attn_noalloc.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _P]
 
@@ -275,6 +279,29 @@ def decode_step(params, d: int, k_new, v_new, q, n_kv_heads: int, k_pool, v_pool
                                        workspace.numel(), _ptr(status), _stream(stream))
     _check(rc, "tq_decode_step")
     return out
+
+
+def _dequant(is_k: bool, params, d: int, pool, block_ids, out_dtype, out, status, stream):
+    torch = _torch()
+    _need_cuda(params, pool, block_ids, out, status)
+    n, H = block_ids.numel(), pool.shape[1]
+    if out is None:
+        out = torch.empty((n * 16, H, d), dtype=out_dtype, device=pool.device)
+    name = "tq_dequant_k" if is_k else "tq_dequant_v"
+    rc = getattr(load_library(), name)(_ptr(params), d, _ptr(pool), pool.shape[0], H, _ptr(block_ids), n, _ptr(out),
+                                       _dtype_code(out), _ptr(status), _stream(stream))
+    _check(rc, name)
+    return out
+
+
+def dequant_k(params, d: int, k_pool, block_ids, out_dtype=None, out=None, status=None, stream=None):
+    """tq_dequant_k: dense K [len(block_ids) * 16][n_kv_heads][d] of whole paged blocks."""
+    return _dequant(True, params, d, k_pool, block_ids, out_dtype or _torch().bfloat16, out, status, stream)
+
+
+def dequant_v(params, d: int, v_pool, block_ids, out_dtype=None, out=None, status=None, stream=None):
+    """tq_dequant_v: dense V [len(block_ids) * 16][n_kv_heads][d] of whole paged blocks."""
+    return _dequant(False, params, d, v_pool, block_ids, out_dtype or _torch().bfloat16, out, status, stream)
 
 
 def decode_attn_mq(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens, max_ctx: int,

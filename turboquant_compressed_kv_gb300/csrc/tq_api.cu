@@ -162,6 +162,31 @@ int tq_paged_append(const void *params, int d, const void *k_new, const void *v_
                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
+static int dequant_call(bool is_k, const void *params, int d, const void *pool, int64_t num_blocks, int n_kv_heads,
+                        const int32_t *block_ids, int n_ids, void *out, int out_dtype, int32_t *status,
+                        tq_stream_t stream) {
+    if (!valid_d(d)) return TQ_ERR_HEAD_DIM;
+    if (out_dtype != TQ_DTYPE_F32 && out_dtype != TQ_DTYPE_BF16) return TQ_ERR_DTYPE;
+    if (n_ids < 0 || n_kv_heads <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
+    if (n_ids == 0) return TQ_OK;
+    if (!params || !pool || !block_ids || !out) return TQ_ERR_INVALID;
+    if (!aligned16(params) || !aligned16(pool)) return TQ_ERR_ALIGN;
+    return cuda_status(launch_dequant(is_k, d, out_dtype, params, pool, num_blocks, n_kv_heads, block_ids, n_ids, out,
+                                      status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int tq_dequant_k(const void *params, int d, const void *k_pool, int64_t num_blocks, int n_kv_heads,
+                 const int32_t *block_ids, int n_ids, void *out, int out_dtype, int32_t *status, tq_stream_t stream) {
+    return dequant_call(true, params, d, k_pool, num_blocks, n_kv_heads, block_ids, n_ids, out, out_dtype, status,
+                        stream);
+}
+
+int tq_dequant_v(const void *params, int d, const void *v_pool, int64_t num_blocks, int n_kv_heads,
+                 const int32_t *block_ids, int n_ids, void *out, int out_dtype, int32_t *status, tq_stream_t stream) {
+    return dequant_call(false, params, d, v_pool, num_blocks, n_kv_heads, block_ids, n_ids, out, out_dtype, status,
+                        stream);
+}
+
 size_t tq_decode_workspace_bytes(int d, int batch, int n_q_heads, int max_ctx) {
     return decode_workspace_bytes(d, batch, n_q_heads, max_ctx);
 }

@@ -301,6 +301,9 @@ cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const
 cudaError_t launch_append(int d, int dtype, const void *params, const void *k_new, const void *v_new, int batch,
                           int n_heads, const int32_t *bt, int max_blocks, const int32_t *ctx, void *kp, void *vp,
                           int64_t num_blocks, int32_t *status, cudaStream_t st);
+cudaError_t launch_dequant(bool is_k, int d, int out_dtype, const void *params, const void *pool, int64_t num_blocks,
+                           int n_heads, const int32_t *block_ids, int n_ids, void *out, int32_t *status,
+                           cudaStream_t st);
 size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx);
 // Decode launches take q_len queries per sequence (q[b][i][h], out[b][i][h]); query i attends
 // the first L - (q_len - 1 - i) of the sequence's L attended tokens.  The workspace is laid
