@@ -369,6 +369,70 @@ def extra_verify(steps, warmup, dev, q_len=2):
     return res
 
 
+def extra_dequant(steps, warmup, dev):
+    """Bulk dequantisation of the prefill workload's cache (8 x 32768 tokens x 8 kv heads, d=128)
+    back to dense bf16 K and V: the input of a chunked prefill over a compressed prefix."""
+    import torch
+
+    import turboquant_compressed_kv_gb300 as tq
+    from turboquant_compressed_kv_gb300 import synth
+    from turboquant_compressed_kv_gb300.cache import PagedCache
+    w = synth.workload("prefill")
+    d, Hkv = w.head_dim, w.n_kv_heads
+    cache = PagedCache.create(w, dev)
+    cache.prefill_device()
+    ids = torch.cat([cache.block_table[b, :w.prefill_lens[b] // 16] for b in range(w.batch)]).contiguous()
+    n = ids.numel()
+    ko = torch.empty((n * 16, Hkv, d), dtype=torch.bfloat16, device=dev)
+    vo = torch.empty_like(ko)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        tq.dequant_k(cache.params, d, cache.k_pool, ids, out=ko, status=status)
+        if ev is not None:
+            ev[1].record(stream)
+        tq.dequant_v(cache.params, d, cache.v_pool, ids, out=vo, status=status)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        step(evs[i])
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the dequantisation")
+    ms = statistics.mean(a.elapsed_time(c) for a, _, c in evs)
+    kms = statistics.mean(a.elapsed_time(b) for a, b, _ in evs)
+    vms = statistics.mean(b.elapsed_time(c) for _, b, c in evs)
+    ntok = n * 16
+    krec, vrec = (8 * d + 64) / 16, (6 * d + 32) / 16
+    kbytes = ntok * Hkv * (krec + d * 2) + n * 4
+    vbytes = ntok * Hkv * (vrec + d * 2) + n * 4
+    peak, _ = measured_peak()
+    res = {"config": {"workload": "prefill_dequant", "sequences": w.batch, "tokens_per_sequence": w.prefill_lens[0],
+                      "n_kv_heads": Hkv, "head_dim": d, "out_dtype": "bf16",
+                      "l2": f"records {(cache.k_pool.numel() + cache.v_pool.numel()) / 2**20:.0f} MiB in, "
+                            f"{2 * ko.numel() * 2 / 2**20:.0f} MiB out (> L2)"},
+           "value": round(ntok / (ms * 1e-3) / 1e6, 3), "unit": "Mtok/s",
+           "gbs": round((kbytes + vbytes) / (ms * 1e-3) / 1e9, 3), "ms_per_step": round(ms, 6),
+           "steps": steps, "warmup": warmup, "launches_per_step": 2,
+           "roofline": {"bound": "hbm", "peak": peak, "unit": "GB/s",
+                        "k": {"kernel_ms": round(kms, 6), "achieved": round(kbytes / (kms * 1e-3) / 1e9, 3),
+                              "frac": round(kbytes / (kms * 1e-3) / 1e9 / peak, 4), "bytes_per_launch": kbytes},
+                        "v": {"kernel_ms": round(vms, 6), "achieved": round(vbytes / (vms * 1e-3) / 1e9, 3),
+                              "frac": round(vbytes / (vms * 1e-3) / 1e9 / peak, 4), "bytes_per_launch": vbytes}}}
+    del ko, vo, cache
+    torch.cuda.empty_cache()
+    return res
+
+
 def extra_encode(steps, warmup, dev):
     """Bulk encode of the prefill workload (8 x 32768 tokens x 8 kv heads, d=128, bf16) into paged storage."""
     import torch
@@ -597,7 +661,8 @@ def bench_tq(args):
         line["workloads"] = {"ragged": extra_decode("ragged", ksteps, max(3, args.warmup), dev),
                              "long256": extra_decode("long256", ksteps, max(3, args.warmup), dev),
                              "verify_q2": extra_verify(ksteps, max(3, args.warmup), dev),
-                             "prefill_encode": extra_encode(max(3, min(args.steps, 50)), max(3, args.warmup), dev)}
+                             "prefill_encode": extra_encode(max(3, min(args.steps, 50)), max(3, args.warmup), dev),
+                             "prefill_dequant": extra_dequant(max(3, min(args.steps, 50)), max(3, args.warmup), dev)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, dt, _ = run_cpu_oracle(w, 3, 1, 2)
         line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
