@@ -258,6 +258,28 @@ int tq_decode_step_mq(const void *params, int d, const void *k_new, const void *
                       void *k_pool, void *v_pool, int64_t num_blocks, float *out, void *workspace,
                       size_t workspace_bytes, int32_t *status, tq_stream_t stream);
 
+/* tq_decode_attn_hybrid -- decode attention over a hybrid cache: the compressed paged history
+ * plus a window of recent tokens kept uncompressed, in one softmax.  [README: compression
+ * starts past 2048 tokens ("--turbo-kv" in the options table, "After 2048 tokens" in the
+ * kv_bits / --turbo-kv comparison), and attention covers the recent hot window together with
+ * the compressed history (the "--turbo-kv long-range recall" note)]
+ * For query head h of sequence b the attended set is the ctx_lens[b] compressed tokens (scored
+ * as in tq_decode_attn) and the win_lens[b] window tokens j < win_lens[b] (row
+ * win_k[b][j][kv head], scored q . k / sqrt d in the original domain); out = sum_j P_j v_j
+ * over both, with one softmax P.  Window slots are an unordered set, so a ring buffer of the
+ * most recent tokens can be passed as it is.
+ *   win_k, win_v  device [batch][win_cap][n_kv_heads][d] in win_dtype (TQ_DTYPE_F32 or
+ *                 TQ_DTYPE_BF16); win_lens device int32[batch], clamped to [0, win_cap].
+ *   workspace     >= tq_decode_workspace_bytes_hybrid(d, batch, n_q_heads, max_ctx, win_cap).
+ * Other arguments and errors as tq_decode_attn; win_cap = 0 is tq_decode_attn. */
+size_t tq_decode_workspace_bytes_hybrid(int d, int batch, int n_q_heads, int max_ctx, int win_cap);
+int tq_decode_attn_hybrid(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads,
+                          int n_kv_heads, const void *k_pool, const void *v_pool, int64_t num_blocks,
+                          const int32_t *block_table, int max_blocks, const int32_t *ctx_lens, int max_ctx,
+                          const void *win_k, const void *win_v, int win_dtype, int win_cap,
+                          const int32_t *win_lens, float *out, void *workspace, size_t workspace_bytes,
+                          int32_t *status, tq_stream_t stream);
+
 /* tq_decode_attn_noalloc -- tq_decode_attn without a caller workspace.
  * The pages have no counterpart to this call; it exists for callers that
  * cannot allocate device memory when they decode: a serving runtime that

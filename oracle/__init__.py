@@ -318,3 +318,31 @@ def dequant(is_k: bool, D, S, pool, H: int, block_ids, centroids=None):
             out[i, h] = n[i, h] * rotate_t(D, y[i, h])
     return out
 
+
+def decode_hybrid(D, S, q: np.ndarray, Hkv: int, kpool, vpool, block_table, ctx_lens, win_k, win_v, win_lens):
+    """Attention over a hybrid cache (SwiftLM README: compression starts past 2048 tokens, and
+    attention covers the uncompressed recent window together with the compressed history):
+    one softmax over the ctx_lens[b] compressed tokens (their dequantised K / V, the decode's
+    estimator) and the win_lens[b] window rows win_k[b][j] / win_v[b][j] taken as given.
+    q[B][Hq][d] -> out[B][Hq][d] fp64."""
+    B, Hq, d = q.shape
+    G = Hq // Hkv
+    out = np.zeros((B, Hq, d), np.float64)
+    for b in range(B):
+        L, W = int(ctx_lens[b]), int(win_lens[b])
+        nb = -(-L // BLOCK)
+        Kc = dequant(True, D, S, kpool, Hkv, block_table[b, :nb])[:L] if L > 0 else np.zeros((0, Hkv, d))
+        Vc = dequant(False, D, S, vpool, Hkv, block_table[b, :nb])[:L] if L > 0 else np.zeros((0, Hkv, d))
+        Kw = np.asarray(win_k[b, :W], np.float64)
+        Vw = np.asarray(win_v[b, :W], np.float64)
+        for h in range(Hq):
+            kv = h // G
+            keys = np.concatenate([Kc[:, kv], Kw[:, kv]])
+            vals = np.concatenate([Vc[:, kv], Vw[:, kv]])
+            if len(keys) == 0:
+                continue
+            s = keys @ np.asarray(q[b, h], np.float64) / np.sqrt(d)
+            p = np.exp(s - s.max())
+            out[b, h] = (p[:, None] * vals).sum(0) / p.sum()
+    return out
+

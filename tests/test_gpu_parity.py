@@ -427,6 +427,42 @@ def test_dequant_parity(d, is_k):
     assert torch.all(ob[16:] == 0) and torch.equal(ob[:16], o32[:16])
 
 
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 8, 2), (128, 4, 4), (128, 16, 2), (256, 4, 2)])
+@pytest.mark.parametrize("wdtype", ["f32", "bf16"])
+def test_decode_hybrid_parity(d, Hq, Hkv, wdtype):
+    """One softmax over the compressed history and an uncompressed window (ragged lengths, an
+    empty history, an empty window, both empty) against the oracle; win_cap = 0 is
+    tq_decode_attn bit for bit."""
+    lens = [600, 0, 17, 1500, 33, 0]
+    wl = [300, 129, 0, 128, 5, 0]
+    cap = 300
+    D, S, params, bt, kp, vp = _build_cache(d, Hkv, lens, "bf16", seed=Hq + d + 5)
+    B = len(lens)
+    rng = np.random.default_rng(51)
+    q = synth.round_dtype(rng.standard_normal((B, Hq, d)).astype(np.float32), "bf16")
+    wk = synth.round_dtype(rng.standard_normal((B, cap, Hkv, d)).astype(np.float32) * 2, wdtype)
+    wv = synth.round_dtype(rng.standard_normal((B, cap, Hkv, d)).astype(np.float32), wdtype)
+    dkp, dvp, dbt = torch.from_numpy(kp).to(DEV), torch.from_numpy(vp).to(DEV), torch.from_numpy(bt).to(DEV)
+    ctx = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    wlt = torch.tensor(wl, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    dq = _upload(q, "bf16")
+    out = tq.decode_attn_hybrid(params, d, dq, Hkv, dkp, dvp, dbt, ctx, max(lens), _upload(wk, wdtype),
+                                _upload(wv, wdtype), wlt, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o = out.cpu().numpy()
+    ref = oracle.decode_hybrid(D, S, q, Hkv, kp, vp, bt, lens, wk, wv, wl)
+    assert np.all(o[5] == 0)
+    parity.check_attention(o, ref)
+    # no window at all: exactly the compressed decode
+    e = torch.zeros((B, 0, Hkv, d), dtype=torch.float32, device=DEV)
+    o0 = tq.decode_attn_hybrid(params, d, dq, Hkv, dkp, dvp, dbt, ctx, max(lens), e, e, wlt)
+    want = tq.decode_attn(params, d, dq, Hkv, dkp, dvp, dbt, ctx, max(lens))
+    torch.cuda.synchronize()
+    assert torch.equal(o0, want)
+
+
 def test_tiny_workload_end_to_end():
     """1 sequence, 1 head, d=128, 256 fp32 tokens with 20x outlier channels:
     GPU encode vs oracle encode, then GPU decode vs oracle decode of the

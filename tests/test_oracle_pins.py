@@ -433,6 +433,36 @@ def test_dequant_gives_the_decode_attention():
     assert abs(err.mean() / mse - 1) < 0.1, (err.mean(), mse)
 
 
+def test_hybrid_attention_merges_history_and_window():
+    """decode_hybrid (one softmax over dequantised history and raw window rows) equals the
+    log-sum-exp merge of the rotated-domain decode over the history and a plain softmax over the
+    window; an empty window gives the decode; the order of window slots does not matter."""
+    d, Hkv, Hq, L, W = 128, 2, 4, 37, 11
+    D, S, bt, kp, vp = _small_cache(d, 1, Hkv, [L], seed=21)
+    rng = np.random.default_rng(22)
+    q = rng.standard_normal((1, Hq, d)).astype(np.float32)
+    wk = rng.standard_normal((1, W + 3, Hkv, d)).astype(np.float32) * 2
+    wv = rng.standard_normal((1, W + 3, Hkv, d)).astype(np.float32)
+    o = oracle.decode_hybrid(D, S, q, Hkv, kp, vp, bt, [L], wk, wv, [W])
+    oc = oracle.decode(D, S, q, Hkv, kp, vp, bt, np.array([L], np.int32))
+    np.testing.assert_allclose(oracle.decode_hybrid(D, S, q, Hkv, kp, vp, bt, [L], wk, wv, [0]), oc, rtol=1e-12,
+                               atol=1e-12)
+    # the merge: lse of the history from its scores, the window by a plain softmax
+    nb = -(-L // 16)
+    Kc = oracle.dequant(True, D, S, kp, Hkv, bt[0, :nb])[:L]
+    for h in range(Hq):
+        kv = h // (Hq // Hkv)
+        sc = Kc[:, kv] @ q[0, h].astype(np.float64) / math.sqrt(d)
+        sw = wk[0, :W, kv].astype(np.float64) @ q[0, h].astype(np.float64) / math.sqrt(d)
+        M = max(sc.max(), sw.max())
+        ec, ew = np.exp(sc - M).sum(), np.exp(sw - M)
+        want = (oc[0, h] * ec + (ew[:, None] * wv[0, :W, kv]).sum(0)) / (ec + ew.sum())
+        np.testing.assert_allclose(o[0, h], want, rtol=1e-11, atol=1e-12)
+    perm = rng.permutation(W)
+    o2 = oracle.decode_hybrid(D, S, q, Hkv, kp, vp, bt, [L], wk[:, perm], wv[:, perm], [W])
+    np.testing.assert_allclose(o2, o, rtol=1e-12, atol=1e-12)
+
+
 def test_attention_ignores_physical_block_order():
     d, Hkv = 128, 2
     D, S, bt, kp, vp = _small_cache(d, 1, Hkv, [50], seed=5)

@@ -93,6 +93,11 @@ def _declare(L):
         f = getattr(L, name)
         f.restype = _I
         f.argtypes = [_P, _I, _P, _I64, _I, _P, _I, _P, _I, _P, _P]
+    L.tq_decode_workspace_bytes_hybrid.restype = _SZ
+    L.tq_decode_workspace_bytes_hybrid.argtypes = [_I, _I, _I, _I, _I]
+    L.tq_decode_attn_hybrid.restype = _I
+    L.tq_decode_attn_hybrid.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _I, _I, _P,
+                                        _P, _P, _SZ, _P, _P]
     L.tq_decode_attn_noalloc.restype = _I
     L.tq_decode_attn_noalloc.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _P]
 
@@ -302,6 +307,28 @@ def dequant_k(params, d: int, k_pool, block_ids, out_dtype=None, out=None, statu
 def dequant_v(params, d: int, v_pool, block_ids, out_dtype=None, out=None, status=None, stream=None):
     """tq_dequant_v: dense V [len(block_ids) * 16][n_kv_heads][d] of whole paged blocks."""
     return _dequant(False, params, d, v_pool, block_ids, out_dtype or _torch().bfloat16, out, status, stream)
+
+
+def decode_attn_hybrid(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens, max_ctx: int,
+                       win_k, win_v, win_lens, out=None, workspace=None, status=None, stream=None):
+    """tq_decode_attn_hybrid: one softmax over the compressed history (ctx_lens[b] tokens) and the
+    uncompressed window rows win_k/win_v [batch][win_cap][n_kv_heads][d] (win_lens[b] of them)."""
+    torch = _torch()
+    _need_cuda(params, q, k_pool, v_pool, block_table, ctx_lens, win_k, win_v, win_lens, out, workspace, status)
+    B, Hq = q.shape[0], q.shape[1]
+    cap = win_k.shape[1]
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    need = int(load_library().tq_decode_workspace_bytes_hybrid(d, B, Hq, max_ctx, cap))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = load_library().tq_decode_attn_hybrid(_ptr(params), d, _ptr(q), _dtype_code(q), B, Hq, n_kv_heads,
+                                              _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
+                                              block_table.shape[1], _ptr(ctx_lens), max_ctx, _ptr(win_k),
+                                              _ptr(win_v), _dtype_code(win_k), cap, _ptr(win_lens), _ptr(out),
+                                              _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+    _check(rc, "tq_decode_attn_hybrid")
+    return out
 
 
 def decode_attn_mq(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens, max_ctx: int,

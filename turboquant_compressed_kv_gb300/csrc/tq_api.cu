@@ -254,6 +254,46 @@ int tq_decode_attn_mq(const void *params, int d, const void *q, int dtype, int b
     return cuda_status(e);
 }
 
+static size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t tq_decode_workspace_bytes_hybrid(int d, int batch, int n_q_heads, int max_ctx, int win_cap) {
+    const size_t base = decode_workspace_bytes(d, batch, n_q_heads, max_ctx);
+    if (base == 0 || win_cap < 0) return 0;
+    return al256(base) + al256((size_t)batch * n_q_heads * sizeof(float)) +
+           hybrid_part_bytes(d, batch, n_q_heads, win_cap);
+}
+
+int tq_decode_attn_hybrid(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads,
+                          int n_kv_heads, const void *k_pool, const void *v_pool, int64_t num_blocks,
+                          const int32_t *block_table, int max_blocks, const int32_t *ctx_lens, int max_ctx,
+                          const void *win_k, const void *win_v, int win_dtype, int win_cap, const int32_t *win_lens,
+                          float *out, void *workspace, size_t workspace_bytes, int32_t *status, tq_stream_t stream) {
+    if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16 && valid_d(d)) return TQ_ERR_DTYPE;
+    if (win_dtype != TQ_DTYPE_F32 && win_dtype != TQ_DTYPE_BF16 && valid_d(d)) return TQ_ERR_DTYPE;
+    int rc = check_decode(params, d, batch, 1, n_q_heads, n_kv_heads, max_ctx, workspace, workspace_bytes);
+    if (rc != TQ_OK || batch == 0) return rc;
+    if (win_cap < 0 || max_blocks <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
+    if (workspace_bytes < tq_decode_workspace_bytes_hybrid(d, batch, n_q_heads, max_ctx, win_cap))
+        return TQ_ERR_WORKSPACE;
+    if (!q || !k_pool || !v_pool || !block_table || !ctx_lens || !out) return TQ_ERR_INVALID;
+    if (win_cap > 0 && (!win_k || !win_v || !win_lens)) return TQ_ERR_INVALID;
+    if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
+    if (win_cap > 0 && (!aligned16(win_k) || !aligned16(win_v))) return TQ_ERR_ALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+    const size_t base = al256(decode_workspace_bytes(d, batch, n_q_heads, max_ctx));
+    float *lse = reinterpret_cast<float *>(ws + base);
+    float *part = reinterpret_cast<float *>(ws + base + al256((size_t)batch * n_q_heads * sizeof(float)));
+    cudaError_t e = launch_qprep(d, dtype, params, q, batch, 1, n_q_heads, n_kv_heads, ctx_lens, max_ctx, ws, st);
+    if (e == cudaSuccess)
+        e = launch_splitk(d, params, batch, 1, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
+                          max_blocks, ctx_lens, 0, max_ctx, out, ws, status, st, lse);
+    if (e == cudaSuccess)
+        e = launch_hybrid_window(d, dtype, win_dtype, q, win_k, win_v, batch, n_q_heads, n_kv_heads, win_cap, win_lens,
+                                 part, out, lse, st);
+    return cuda_status(e);
+}
+
 int tq_decode_attn(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads, int n_kv_heads,
                    const void *k_pool, const void *v_pool, int64_t num_blocks, const int32_t *block_table,
                    int max_blocks, const int32_t *ctx_lens, int max_ctx, float *out, void *workspace,

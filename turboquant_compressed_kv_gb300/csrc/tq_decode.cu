@@ -95,7 +95,7 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
                   const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_lens,
                   int ctx_add, int max_ctx, const int64_t *__restrict__ cpre, const int32_t *__restrict__ cta_b,
                   float *__restrict__ part, unsigned int *__restrict__ counters, float *__restrict__ out,
-                  int32_t *status) {
+                  float *__restrict__ lse, int32_t *status) {
     using C = SplitCfg<D, NWARP>;
     constexpr int NT_ = C::NT, BPW = C::BPW, BPC = C::BPC, CH = C::CH;
     constexpr int TPL = CH / 32;               // softmax tokens per lane
@@ -126,7 +126,11 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
     // sequences with nothing to attend get out = 0
     for (int b = cta; b < batch; b += gridDim.x)
         if (attended_len(ctx_lens[b], ctx_add, max_ctx) == 0)
+        {
             for (int i = tid; i < q_len * hq * D; i += NT_) out[(size_t)b * q_len * hq * D + i] = 0.f;
+            if (lse)
+                for (int i = tid; i < q_len * hq; i += NT_) lse[(size_t)b * q_len * hq + i] = -INFINITY;
+        }
 
     // P CTAs share the W chunks, at least one chunk each (as in build_schedule)
     const int64_t W = cpre[batch];
@@ -470,6 +474,7 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
 #pragma unroll
                 for (int r = 0; r < R; ++r) v[r] = sAcc[h * D + 32 * r + lane];
                 finish_row<D>(v, sL[h], params, out + out_row(h) * D, lane);
+                if (lse && lane == 0) lse[out_row(h)] = sL[h] > 0.f ? sM[h] + logf(sL[h]) : -INFINITY;
             }
         } else {
             // leave a partial in this CTA's slot (0: its first segment, 1: its last)
@@ -517,6 +522,7 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
                         for (int r = 0; r < R; ++r) v[r] = fmaf(__ldcg(ps + 4 + 32 * r + lane), wgt, v[r]);
                     }
                     finish_row<D>(v, l, params, out + out_row(h) * D, lane);
+                    if (lse && lane == 0) lse[out_row(h)] = l > 0.f ? M + logf(l) : -INFINITY;
                 }
             }
         }
@@ -610,14 +616,14 @@ template <int D, int G>
 cudaError_t pass_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
                           const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
                           const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
-                          int32_t *status) {
+                          float *lse, int32_t *status) {
     constexpr int NWARP = pass_warps(G);
     constexpr size_t smem = split_smem_bytes<D, G, NWARP>();
     auto kern = decode_mma_kernel<D, G, NWARP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<nctas, NWARP * 32, smem, st>>>(P, w.packs, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx,
-                                         w.cpre, w.cta_b, w.part, w.counters, out, status);
+                                         w.cpre, w.cta_b, w.part, w.counters, out, lse, status);
     return cudaGetLastError();
 }
 
@@ -625,8 +631,8 @@ template <int D>
 cudaError_t pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
                         const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
                         const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
-                        int32_t *status) {
-#define TQ_PASS(GG) return pass_launch_g<D, GG>(nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out, status)
+                        float *lse, int32_t *status) {
+#define TQ_PASS(GG) return pass_launch_g<D, GG>(nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out, lse, status)
     switch (G) {
         case 1: TQ_PASS(1);
         case 2: TQ_PASS(2);
@@ -660,7 +666,7 @@ cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, in
 cudaError_t launch_splitk(int d, const void *params, int batch, int q_len, int hq, int hkv, const void *k_pool,
                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
                           const int32_t *ctx_lens, int ctx_add, int max_ctx, float *out, void *ws, int32_t *status,
-                          cudaStream_t st) {
+                          cudaStream_t st, float *lse) {
     const WsLayout w = ws_layout(ws, d, batch, q_len * hq);
     const int G = q_len * hq / hkv;   // operand columns per kv head
     const int nctas = pass_ctas_any(d, G);
@@ -668,12 +674,12 @@ cudaError_t launch_splitk(int d, const void *params, int batch, int q_len, int h
     const uint8_t *P = (const uint8_t *)params;
     if (d == 128 && TQ_DECODE_WARP)
         return warp_pass_launch(G, nctas, st, P, batch, q_len, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
-                                num_blocks, block_table, max_blocks, ctx_lens, ctx_add, max_ctx, w, out, status);
+                                num_blocks, block_table, max_blocks, ctx_lens, ctx_add, max_ctx, w, out, lse, status);
     if (d == 128)
         return pass_launch<128>(G, nctas, st, P, batch, q_len, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
-                                num_blocks, block_table, max_blocks, ctx_lens, ctx_add, max_ctx, w, out, status);
+                                num_blocks, block_table, max_blocks, ctx_lens, ctx_add, max_ctx, w, out, lse, status);
     return pass_launch<256>(G, nctas, st, P, batch, q_len, hq, hkv, (const uint8_t *)k_pool, (const uint8_t *)v_pool,
-                            num_blocks, block_table, max_blocks, ctx_lens, ctx_add, max_ctx, w, out, status);
+                            num_blocks, block_table, max_blocks, ctx_lens, ctx_add, max_ctx, w, out, lse, status);
 }
 
 // ---------------------------------------------------------------- the decode step: append, then attend

@@ -84,7 +84,7 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                    const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_lens,
                    int ctx_add, int max_ctx, const int64_t *__restrict__ cpre, const int32_t *__restrict__ cta_b,
                    float *__restrict__ part, unsigned int *__restrict__ counters, float *__restrict__ out,
-                   int32_t *status) {
+                   float *__restrict__ lse, int32_t *status) {
     constexpr int D = kWD, NT = kWWarps * 32, NWARP = kWWarps, BPW = kWBpw;
     constexpr int CH = kBlock * NWARP * BPW;    // tokens per chunk (the schedule's unit)
     constexpr int NTK = w_ntk<G>();             // K-side n-tiles; thread holds heads 4*nt + tig
@@ -92,7 +92,7 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
     constexpr int KREC = kWKrec, VREC = kWVrec, REC = kWRec;
     constexpr size_t kStage = (size_t)NWARP * 2 * BPW * REC;
     constexpr size_t kMerge = (size_t)(NWARP + 1) * G * D * 4;
-    constexpr float kLog2e = 1.4426950408889634f;
+    constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
 
     extern __shared__ __align__(16) uint8_t smem[];
     const int cta = blockIdx.x;
@@ -107,7 +107,11 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
 
     for (int b = cta; b < batch; b += gridDim.x)
         if (attended_len(ctx_lens[b], ctx_add, max_ctx) == 0)
+        {
             for (int i = tid; i < q_len * hq * D; i += NT) out[(size_t)b * q_len * hq * D + i] = 0.f;
+            if (lse)
+                for (int i = tid; i < q_len * hq; i += NT) lse[(size_t)b * q_len * hq + i] = -INFINITY;
+        }
 
     const int64_t W = cpre[batch];
     const int P = (int)(W < (int64_t)gridDim.x ? W : (int64_t)gridDim.x);
@@ -592,6 +596,7 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
 #pragma unroll
                 for (int r = 0; r < R; ++r) v[r] = sAcc[h * D + 32 * r + lane];
                 finish_row<D>(v, sL[h], params, out + out_row(h) * D, lane);
+                if (lse && lane == 0) lse[out_row(h)] = sL[h] > 0.f ? sM[h] * kLn2 + logf(sL[h]) : -INFINITY;
             }
         } else {
             const int slot = first_seg ? 0 : 1;
@@ -636,6 +641,7 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                         for (int r = 0; r < R; ++r) v[r] = fmaf(__ldcg(ps + 4 + 32 * r + lane), wgt, v[r]);
                     }
                     finish_row<D>(v, l, params, out + out_row(h) * D, lane);
+                    if (lse && lane == 0) lse[out_row(h)] = l > 0.f ? M * kLn2 + logf(l) : -INFINITY;
                 }
             }
         }
@@ -663,13 +669,13 @@ template <int G>
 cudaError_t warp_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
                           const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
                           const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
-                          int32_t *status) {
+                          float *lse, int32_t *status) {
     constexpr size_t smem = warp_smem_bytes<G>();
     auto kern = decode_warp_kernel<G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<nctas, kWWarps * 32, smem, st>>>(P, w.packs, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx,
-                                            w.cpre, w.cta_b, w.part, w.counters, out, status);
+                                            w.cpre, w.cta_b, w.part, w.counters, out, lse, status);
     return cudaGetLastError();
 }
 
@@ -691,8 +697,8 @@ int warp_pass_ctas(int G) {
 cudaError_t warp_pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
                              const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
                              const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
-                             int32_t *status) {
-#define TQ_WPASS(GG) return warp_launch_g<GG>(nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out, status)
+                             float *lse, int32_t *status) {
+#define TQ_WPASS(GG) return warp_launch_g<GG>(nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out, lse, status)
     switch (G) {
         case 1: TQ_WPASS(1);
         case 2: TQ_WPASS(2);

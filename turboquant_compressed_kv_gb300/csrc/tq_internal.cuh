@@ -305,6 +305,12 @@ cudaError_t launch_dequant(bool is_k, int d, int out_dtype, const void *params, 
                            int n_heads, const int32_t *block_ids, int n_ids, void *out, int32_t *status,
                            cudaStream_t st);
 size_t decode_workspace_bytes(int d, int batch, int hq, int max_ctx);
+// Hybrid attention: the window pass and the merge (tq_hybrid.cu).  `out` holds the compressed
+// pass's output and `lse` its log-sum-exp on entry; `part` holds hybrid_part_bytes().
+size_t hybrid_part_bytes(int d, int batch, int hq, int win_cap);
+cudaError_t launch_hybrid_window(int d, int q_dtype, int w_dtype, const void *q, const void *wk, const void *wv,
+                                 int batch, int hq, int hkv, int win_cap, const int32_t *win_lens, float *part,
+                                 float *out, const float *lse, cudaStream_t st);
 // Decode launches take q_len queries per sequence (q[b][i][h], out[b][i][h]); query i attends
 // the first L - (q_len - 1 - i) of the sequence's L attended tokens.  The workspace is laid
 // out for batch sequences of q_len * hq query rows.
@@ -313,7 +319,7 @@ cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, in
 cudaError_t launch_splitk(int d, const void *params, int batch, int q_len, int hq, int hkv, const void *k_pool,
                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
                           const int32_t *ctx_lens, int ctx_add, int max_ctx, float *out, void *ws, int32_t *status,
-                          cudaStream_t st);
+                          cudaStream_t st, float *lse = nullptr);
 cudaError_t launch_step(int d, int dtype, const void *params, const void *k_new, const void *v_new, const void *q,
                         int batch, int q_len, int hq, int hkv, const int32_t *block_table, int max_blocks,
                         const int32_t *pre_lens, int max_ctx, void *k_pool, void *v_pool, int64_t num_blocks,

@@ -108,6 +108,6 @@ int warp_pass_ctas(int G);
 cudaError_t warp_pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
                              const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
                              const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
-                             int32_t *status);
+                             float *lse, int32_t *status);
 
 }  // namespace tq
