@@ -433,6 +433,70 @@ def extra_dequant(steps, warmup, dev):
     return res
 
 
+def extra_hybrid(steps, warmup, dev, history=30720, window=2048):
+    """Hybrid-cache decode on the llama8b_decode head shape at 32K context: 30720 compressed tokens plus
+    a 2048-token bf16 window of the most recent ones, one softmax over both (tq_decode_attn_hybrid)."""
+    import dataclasses
+
+    import torch
+
+    import turboquant_compressed_kv_gb300 as tq
+    from turboquant_compressed_kv_gb300 import synth
+    from turboquant_compressed_kv_gb300.cache import PagedCache, to_device
+    w0 = synth.workload("llama8b_decode")
+    w = dataclasses.replace(w0, ctx_lens=[history] * w0.batch, prefill_lens=[history] * w0.batch, append=False)
+    d, B, Hq, Hkv = w.head_dim, w.batch, w.n_q_heads, w.n_kv_heads
+    cache = PagedCache.create(w, dev)
+    cache.prefill_device()
+    per_cache = cache.k_pool.numel() + cache.v_pool.numel() + 2 * B * window * Hkv * d * 2
+    nrep = max(2, math.ceil(3 * L2_BYTES / per_cache))
+    g = torch.Generator(device=dev).manual_seed(4321)
+    sets = []
+    for r in range(nrep):
+        kp, vp = (cache.k_pool, cache.v_pool) if r == 0 else (cache.k_pool.clone(), cache.v_pool.clone())
+        wk = torch.randn((B, window, Hkv, d), generator=g, device=dev).to(torch.bfloat16)
+        wv = torch.randn((B, window, Hkv, d), generator=g, device=dev).to(torch.bfloat16)
+        sets.append((kp, vp, wk, wv))
+    q = to_device(synth.queries(w), w.dtype, dev)
+    ctx = torch.tensor(w.ctx_lens, dtype=torch.int32, device=dev)
+    wl = torch.full((B,), window, dtype=torch.int32, device=dev)
+    ws = torch.empty(int(tq.load_library().tq_decode_workspace_bytes_hybrid(d, B, Hq, history, window)),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        kp, vp, wk, wv = sets[i % nrep]
+        tq.decode_attn_hybrid(cache.params, d, q, Hkv, kp, vp, cache.block_table, ctx, history, wk, wv, wl, out=out,
+                              workspace=ws, status=status)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the hybrid decode")
+    ms = e0.elapsed_time(e1) / steps
+    nb = step_bytes(w)
+    win_b = 2 * B * window * Hkv * d * 2
+    step_b = nb["partial"] + win_b + nb["q"] + nb["out"]
+    res = {"config": {"workload": "llama8b_hybrid32k", "batch": B, "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": d,
+                      "compressed_tokens": history, "window_tokens": window, "window_dtype": "bf16",
+                      "l2": f"{nrep} copies of cache and window cycled ({nrep * per_cache / 2**20:.0f} MiB > L2)"},
+           "value": round(step_b / (ms * 1e-3) / 1e9, 3), "unit": "GB/s", "ms_per_step": round(ms, 6),
+           "bytes_per_step": {"compressed": nb["partial"], "window": win_b},
+           "steps": steps, "warmup": warmup, "launches_per_step": 4}
+    del sets, cache
+    torch.cuda.empty_cache()
+    return res
+
+
 def extra_encode(steps, warmup, dev):
     """Bulk encode of the prefill workload (8 x 32768 tokens x 8 kv heads, d=128, bf16) into paged storage."""
     import torch
@@ -661,6 +725,7 @@ def bench_tq(args):
         line["workloads"] = {"ragged": extra_decode("ragged", ksteps, max(3, args.warmup), dev),
                              "long256": extra_decode("long256", ksteps, max(3, args.warmup), dev),
                              "verify_q2": extra_verify(ksteps, max(3, args.warmup), dev),
+                             "hybrid32k": extra_hybrid(ksteps, max(3, args.warmup), dev),
                              "prefill_encode": extra_encode(max(3, min(args.steps, 50)), max(3, args.warmup), dev),
                              "prefill_dequant": extra_dequant(max(3, min(args.steps, 50)), max(3, args.warmup), dev)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
