@@ -36,8 +36,18 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attn compressed-KV GB/s & % of GB300 HBM peak; encode Mtok/s vs CPU oracle"
 WORKLOAD = "llama8b_decode"
 L2_BYTES = 129 * 1024 * 1024
-DECODE_SRC = os.path.join(ROOT, "turboquant_compressed_kv_gb300", "csrc", "tq_decode.cu")
-PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_splitk_llama8b_decode_traffic.txt")
+# the d = 128 pass and the headers it is built from: the committed traffic figure is used only
+# while their combined hash matches the one the counters were taken on
+DECODE_SRC = [os.path.join(ROOT, "turboquant_compressed_kv_gb300", "csrc", f)
+              for f in ("tq_decode_warp.cu", "tq_split.cuh", "tq_prep.cuh", "tq_internal.cuh")]
+PROFILE_JSON = os.path.join(ROOT, "profiles", "decode_warp_llama8b_decode_traffic.txt")
+
+
+def decode_src_hash():
+    h = hashlib.sha256()
+    for f in DECODE_SRC:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
 
 
 def parse():
@@ -239,8 +249,7 @@ def profile_traffic(bytes_per_launch):
     try:
         with open(PROFILE_JSON) as f:
             prof = json.load(f)
-        src_hash = hashlib.sha256(open(DECODE_SRC, "rb").read()).hexdigest()[:16]
-        if prof.get("source_sha256_16") != src_hash:
+        if prof.get("source_sha256_16") != decode_src_hash():
             return None
         return float(prof["dram_bytes_per_launch_full"])
     except Exception:
