@@ -145,7 +145,8 @@ int tq_paged_append(const void *params, int d, const void *k_new, const void *v_
  *              and sets TQ_STATUS_BAD_SLOT in *status.
  *   out        device [n_ids * 16][n_kv_heads][d] in out_dtype (TQ_DTYPE_F32 or TQ_DTYPE_BF16,
  *              rounded to nearest even).  Slots never written hold whatever the pool held.
- * Errors: TQ_ERR_HEAD_DIM, TQ_ERR_DTYPE, TQ_ERR_INVALID, TQ_ERR_ALIGN, TQ_ERR_CUDA. */
+ * Errors: TQ_ERR_HEAD_DIM, TQ_ERR_DTYPE, TQ_ERR_INVALID (also n_ids > 0 with num_blocks = 0),
+ * TQ_ERR_ALIGN, TQ_ERR_CUDA. */
 int tq_dequant_k(const void *params, int d, const void *k_pool, int64_t num_blocks, int n_kv_heads,
                  const int32_t *block_ids, int n_ids, void *out, int out_dtype, int32_t *status,
                  tq_stream_t stream);

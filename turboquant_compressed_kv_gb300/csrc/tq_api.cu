@@ -169,6 +169,7 @@ static int dequant_call(bool is_k, const void *params, int d, const void *pool, 
     if (out_dtype != TQ_DTYPE_F32 && out_dtype != TQ_DTYPE_BF16) return TQ_ERR_DTYPE;
     if (n_ids < 0 || n_kv_heads <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
     if (n_ids == 0) return TQ_OK;
+    if (num_blocks == 0) return TQ_ERR_INVALID;   // no block to read
     if (!params || !pool || !block_ids || !out) return TQ_ERR_INVALID;
     if (!aligned16(params) || !aligned16(pool)) return TQ_ERR_ALIGN;
     return cuda_status(launch_dequant(is_k, d, out_dtype, params, pool, num_blocks, n_kv_heads, block_ids, n_ids, out,

@@ -17,7 +17,14 @@
 //     at d = 128, streamed at d = 256);
 //  3. one warp per slot: codebook values plus the QJL term, the inverse rotation in
 //     registers and shuffles, the norm, and the store.
+// K at d = 128 has a tensor-core path (dequant128k_tc_kernel, below): S^T b for 128 vectors is
+// one 128 x 128 x 128 product.
 #include "tq_internal.cuh"
+#include "tq_tc.cuh"
+
+#ifndef TQ_DEQUANT_TC
+#define TQ_DEQUANT_TC 1          // K at d = 128 through the tcgen05 path
+#endif
 
 namespace tq {
 namespace {
@@ -150,6 +157,239 @@ dequant_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ p
     }
 }
 
+// ---------------------------------------------------------------- K at d = 128 on tcgen05
+// Two warpgroups take alternate tiles of 128 rows (8 records x 16 slots); thread r of a
+// warpgroup owns row r:
+//  1. the tile's records arrive by bulk copy (two tiles in flight per warpgroup);
+//  2. the row's 128 sign bits become the A operand (f16 +-1, 128-byte swizzle) with one shift
+//     and one LOP3 per two elements: K index 32 tig + 2 p + e holds coordinate
+//     16 (p & 7) + 8 (p >> 3) + 2 tig + e, whose bit is bit p + 16 e of sign word tig;
+//  3. one thread issues p = S^T b as S_hi + S_lo (B rows = output coordinates, K-major, 16
+//     f16 MMAs of K = 16) into the warpgroup's 128 tensor-memory columns;
+//  4. the thread reads its row back (tcgen05.ld), adds the codebook values, runs the 128-point
+//     inverse transform in registers, and stores the row.
+namespace dq128 {
+constexpr int D = 128, kRows = 128, kUnits = kRows / kBlock, kThreads = 256;
+constexpr int kRec = (int)k_record(D);
+constexpr int oB = 0;          // S hi, S lo: 2 x 32 KB
+constexpr int oA = 65536;      // A operand of each warpgroup: 2 x 32 KB
+constexpr int oR = 131072;     // records: [warpgroup][buffer][unit][kRec]
+constexpr int kSmem = oR + 2 * 2 * kUnits * kRec;
+}  // namespace dq128
+
+template <typename TO>
+__global__ void __launch_bounds__(dq128::kThreads, 1)
+dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ pool, int64_t num_blocks,
+                      int n_heads, const int32_t *__restrict__ block_ids, int n_ids, TO *__restrict__ out,
+                      int32_t *status) {
+    using namespace dq128;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint64_t recbar[2][2], mmabar[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ float s_cent[8];
+    const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
+    if (ph->magic != kParamsMagic || ph->d != D) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
+        return;
+    }
+    const int tid = threadIdx.x, wg = tid >> 7, row = tid & 127, warp = tid >> 5;
+    const int64_t units = (int64_t)n_ids * n_heads, ntiles = (units + kUnits - 1) / kUnits;
+    if ((int64_t)blockIdx.x >= ntiles) return;
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&recbar[i][0], 1);
+            tc::mbar_init(&recbar[i][1], 1);
+            tc::mbar_init(&mmabar[i], 1);
+        }
+    }
+    if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
+    if (tid < 8) s_cent[tid] = ph->centroid[tid];
+    {   // B: row n = output coordinate n, K index k' as in the A operand; S as f16 hi + lo
+        const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
+        for (int e = tid; e < D * D; e += kThreads) {
+            const int n = e >> 7, k = e & 127;
+            const int tig = k >> 5, p = (k & 31) >> 1, ee = k & 1;
+            const int coord = 16 * (p & 7) + 8 * (p >> 3) + 2 * tig + ee;
+            const float sv = __ldg(S + coord * D + n);
+            const __half hi = __float2half_rn(sv);
+            const __half lo = __float2half_rn(sv - __half2float(hi));
+            const int off = tc::sw128_off(n, k, D);
+            *reinterpret_cast<__half *>(smem + oB + off) = hi;
+            *reinterpret_cast<__half *>(smem + oB + 32768 + off) = lo;
+        }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base + 128u * wg;
+    const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
+    const float inv_sd = rsqrtf((float)D);
+    const float qjl = 1.2533141373155003f / (float)D;   // sqrt(pi/2) / d
+    bool timed_out = false;
+
+    // tiles of this warpgroup: blockIdx.x + (2 i + wg) * gridDim.x
+    auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)(2 * i + wg) * gridDim.x; };
+    auto issue = [&](int i, int buf) {   // one thread: the tile's records into buffer buf
+        const int64_t tile = tile_of(i);
+        uint32_t bytes = 0;
+        for (int k = 0; k < kUnits; ++k) {
+            const int64_t u = tile * kUnits + k;
+            if (u >= units) break;
+            bytes += kRec;
+        }
+        tc::mbar_arrive_expect_tx(&recbar[wg][buf], bytes);
+        for (int k = 0; k < kUnits; ++k) {
+            const int64_t u = tile * kUnits + k;
+            if (u >= units) break;
+            const int64_t blk = block_ids[u / n_heads];
+            const int64_t bc = (blk >= 0 && blk < num_blocks) ? blk : 0;   // a bad id reads block 0, output zeroed
+            tc::bulk_g2s(smem + oR + ((wg * 2 + buf) * kUnits + k) * kRec,
+                         pool + ((size_t)bc * n_heads + (u % n_heads)) * kRec, kRec, &recbar[wg][buf]);
+        }
+    };
+    if (row == 0) {
+        if (tile_of(0) < ntiles) issue(0, 0);
+        if (tile_of(1) < ntiles) issue(1, 1);
+    }
+    uint8_t *sA = smem + oA + wg * 32768;
+    const int bar_id = 1 + wg;   // named barrier of this warpgroup's 128 threads
+
+#pragma unroll 1
+    for (int i = 0; tile_of(i) < ntiles; ++i) {
+        const int64_t tile = tile_of(i);
+        const int buf = i & 1;
+        if (!tc::mbar_wait(&recbar[wg][buf], (i >> 1) & 1)) timed_out = true;
+        const int unit_k = row >> 4, t = row & 15;
+        const int64_t u = tile * kUnits + unit_k;
+        const bool live = u < units;
+        const int64_t blk = live ? block_ids[u / n_heads] : -1;
+        const bool good = live && blk >= 0 && blk < num_blocks;
+        if (live && !good && t == 0) flag_status(status, TQ_STATUS_BAD_SLOT);
+        const uint8_t *rec = smem + oR + ((wg * 2 + buf) * kUnits + unit_k) * kRec;
+        const uint32_t *planes = reinterpret_cast<const uint32_t *>(rec);
+        constexpr int PW = 2 * D / 4;
+        const int gid = t & 7, th = t >> 3;
+        uint32_t cw[3][4], sw[4];
+#pragma unroll
+        for (int tig = 0; tig < 4; ++tig) {
+            const int word = (4 * gid + tig) * 2 + th;
+            cw[0][tig] = live ? planes[word] : 0u;
+            cw[1][tig] = live ? planes[PW + word] : 0u;
+            cw[2][tig] = live ? planes[2 * PW + word] : 0u;
+            sw[tig] = live ? planes[3 * PW + word] : 0u;
+        }
+        const __half2 ng = live ? *reinterpret_cast<const __half2 *>(rec + 8 * D + 4 * t) : __floats2half2_rn(0.f, 0.f);
+        const float nrm = __low2float(ng), gam = __high2float(ng);
+        // A operand: 16-byte chunks of 8 K elements (four f16x2 registers)
+#pragma unroll
+        for (int tig = 0; tig < 4; ++tig)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t r4[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int p = 4 * c + q;
+                    r4[q] = ((sw[tig] << (15 - p)) & 0x80008000u) ^ 0xBC00BC00u;
+                }
+                *reinterpret_cast<uint4 *>(sA + tc::sw128_off(row, 32 * tig + 8 * c, kRows)) =
+                    make_uint4(r4[0], r4[1], r4[2], r4[3]);
+            }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        tc::named_sync(bar_id, 128);   // A built, the records read: the buffer can be refilled
+        tc::fence_after_sync();
+        if (row == 0) {
+            const uint32_t bh = tc::smem_u32(smem + oB), bl = bh + 32768, a = tc::smem_u32(sA);
+            constexpr uint32_t id = tc::idesc_f16(kRows, D);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                tc::mma_ss_f16(tmem, tc::sw128_desc(a, ks, kRows), tc::sw128_desc(bh, ks, D), id, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                tc::mma_ss_f16(tmem, tc::sw128_desc(a, ks, kRows), tc::sw128_desc(bl, ks, D), id, true);
+            tc::mma_commit(&mmabar[wg]);
+            if (tile_of(i + 2) < ntiles) issue(i + 2, buf);
+        }
+        if (!tc::mbar_wait(&mmabar[wg], i & 1)) timed_out = true;
+        tc::fence_after_sync();
+        // y = c[cell] / sqrt d + sqrt(pi/2)/d gamma p, coordinate n in column n
+        float y[D];
+        const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+#pragma unroll
+        for (int j = 0; j < D / 16; ++j) {
+            float pv[16];
+            tc::ld16(taddr + 16 * j, pv);
+            tc::wait_ld();
+#pragma unroll
+            for (int x = 0; x < 16; ++x) y[16 * j + x] = pv[x];
+        }
+        tc::fence_before_sync();
+        const float gq = qjl * gam;
+#pragma unroll
+        for (int n = 0; n < D; ++n) {
+            const int tig = (n >> 1) & 3, e = n & 1, h = (n >> 3) & 1, s = n >> 4, bit = 8 * h + s + 16 * e;
+            const int cell = (int)((cw[0][tig] >> bit) & 1u) | (int)(((cw[1][tig] >> bit) & 1u) << 1) |
+                             (int)(((cw[2][tig] >> bit) & 1u) << 2);
+            y[n] = fmaf(gq, y[n], s_cent[cell] * inv_sd);
+        }
+        // inverse rotation: D (H y) / sqrt d, then the norm
+#pragma unroll
+        for (int st = 1; st < D; st <<= 1)
+#pragma unroll
+            for (int n = 0; n < D; ++n)
+                if ((n & st) == 0) {
+                    const float a0 = y[n], a1 = y[n | st];
+                    y[n] = a0 + a1;
+                    y[n | st] = a0 - a1;
+                }
+        const float sc = good ? nrm * inv_sd : 0.f;
+        if (live) {
+            TO *orow = out + (((size_t)(u / n_heads) * kBlock + t) * n_heads + (u % n_heads)) * D;
+#pragma unroll
+            for (int n = 0; n < D; n += 4) {
+                float o4[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) o4[x] = good ? y[n + x] * sc * __ldg(Dsign + n + x) : 0.f;
+                if constexpr (sizeof(TO) == 4) {
+                    *reinterpret_cast<float4 *>(orow + n) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+                } else {
+                    const __nv_bfloat162 b01 = __floats2bfloat162_rn(o4[0], o4[1]);
+                    const __nv_bfloat162 b23 = __floats2bfloat162_rn(o4[2], o4[3]);
+                    uint2 v;
+                    v.x = *reinterpret_cast<const uint32_t *>(&b01);
+                    v.y = *reinterpret_cast<const uint32_t *>(&b23);
+                    *reinterpret_cast<uint2 *>(orow + n) = v;
+                }
+            }
+        }
+        tc::named_sync(bar_id, 128);   // every row of the accumulator is read before the next MMA
+        tc::fence_after_sync();
+    }
+    if (timed_out) flag_status(status, TQ_STATUS_TIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
+}
+
+template <typename TO>
+cudaError_t dq128k_launch(const void *params, const void *pool, int64_t num_blocks, int n_heads, const int32_t *ids,
+                          int n_ids, void *out, int32_t *status, cudaStream_t st) {
+    const int64_t ntiles = ((int64_t)n_ids * n_heads + dq128::kUnits - 1) / dq128::kUnits;
+    if (ntiles <= 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    auto kern = dequant128k_tc_kernel<TO>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dq128::kSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t grid = ntiles < sms ? ntiles : sms;
+    kern<<<(unsigned)grid, dq128::kThreads, dq128::kSmem, st>>>((const uint8_t *)params, (const uint8_t *)pool,
+                                                              num_blocks, n_heads, ids, n_ids, (TO *)out, status);
+    return cudaGetLastError();
+}
+
 template <int D, typename TO>
 cudaError_t dq_launch(const void *params, const void *pool, int64_t num_blocks, int n_heads, const int32_t *ids,
                       int n_ids, bool is_k, void *out, int32_t *status, cudaStream_t st) {
@@ -173,6 +413,10 @@ cudaError_t dq_launch(const void *params, const void *pool, int64_t num_blocks, 
 cudaError_t launch_dequant(bool is_k, int d, int out_dtype, const void *params, const void *pool, int64_t num_blocks,
                            int n_heads, const int32_t *block_ids, int n_ids, void *out, int32_t *status,
                            cudaStream_t st) {
+    if (d == 128 && is_k && TQ_DEQUANT_TC)
+        return out_dtype == TQ_DTYPE_BF16
+                   ? dq128k_launch<__nv_bfloat16>(params, pool, num_blocks, n_heads, block_ids, n_ids, out, status, st)
+                   : dq128k_launch<float>(params, pool, num_blocks, n_heads, block_ids, n_ids, out, status, st);
     if (d == 128)
         return out_dtype == TQ_DTYPE_BF16
                    ? dq_launch<128, __nv_bfloat16>(params, pool, num_blocks, n_heads, block_ids, n_ids, is_k, out,
