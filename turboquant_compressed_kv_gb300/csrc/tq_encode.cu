@@ -15,7 +15,8 @@
 //     row k for every vector of the tile from S^T in shared memory (resident
 //     for d=128, streamed in chunks for d=256); sign bits to shared memory;
 //  3. one warp per vector: ballot-pack cells and signs, byte/word stores.
-// One launch may carry K (blockIdx.y == 0) and V (blockIdx.y == 1) tiles.
+// One launch may carry K (blockIdx.y == 0) and V (blockIdx.y == 1) tiles.  Bulk encodes at
+// d = 128 with 16-byte aligned input take the thread-per-row kernel below instead.
 #include "tq_internal.cuh"
 #include "tq_tc.cuh"
 #include "tq_prep.cuh"
@@ -34,273 +35,286 @@ encode_kernel(const uint8_t *__restrict__ params, const T *__restrict__ xk, cons
                              blockIdx.x, gridDim.x, smem, status);
 }
 
-// ---------------------------------------------------------------- bulk encode at d = 128, QJL on tcgen05
-// A persistent CTA (16 warps) encodes tiles of 128 vectors:
-//  1. the tile's inputs (contiguous rows) arrive by one bulk copy, two tiles in flight;
-//  2. one warp per vector: norm, rotation, cells, residual, ballot-packed cell planes and
-//     norms, as in encode_kernel; for K the residual rho (x 256) is written as f16 hi and lo
-//     rows of the A operand (128-byte swizzle, K index 4 * lane + r);
-//  3. K only: p = S rho for the 128 vectors as three f16 products S_hi rho_hi + S_lo rho_hi +
-//     S_hi rho_lo on the tensor cores (M = 128 vectors, N = 128, K = 128, fp32 accumulation),
-//     with S's rows permuted so that thread (vector, word) reads 32 consecutive columns in the
-//     bit order of one sign-plane word.
-namespace enc128 {
-constexpr int D = 128, kRows = 128, kThreads = 512, kTileWarps = 16;
-constexpr float kRhoScale = 256.f;          // keeps the f16 low parts of rho out of the subnormals
-constexpr int oB = 0;                        // S hi, S lo: 2 x 32 KB
-constexpr int oA = 65536;                    // rho hi, rho lo: 2 x 32 KB
-constexpr int oX = 131072;                   // input tiles
-template <typename T> __host__ __device__ constexpr int x_bytes() { return kRows * D * (int)sizeof(T); }
-template <typename T> __host__ __device__ constexpr int n_xbuf() { return sizeof(T) == 2 ? 2 : 1; }
-template <typename T> __host__ __device__ constexpr int smem_bytes() { return oX + n_xbuf<T>() * x_bytes<T>(); }
-}  // namespace enc128
+// ---------------------------------------------------------------- bulk encode at d = 128, thread per row
+// Two warpgroups take alternate tiles of 128 vectors; thread r of a warpgroup owns vector r of
+// the tile from input to record:
+//  1. the tile's rows arrive by one bulk copy per row into a padded row stride (16-byte chunks of
+//     the 32 rows a warp reads then fall in distinct bank groups), NX tiles in flight;
+//  2. norm, signs D, the 128-point transform in registers (no shuffles), z = H D x / n;
+//  3. the cell by a three-level binary search over the thresholds, whose outcomes are the cell's
+//     bits b2, b1, b0 (cell >= k iff z >= t_{k-1}; ties go up), packed into the plane words;
+//  4. K: the residual rho = z - c[cell] (x 256) as f16 hi and lo goes straight from registers into
+//     tensor memory (this row's lane); one thread issues S rho = S_hi rho_hi + S_hi rho_lo +
+//     S_lo rho_hi (24 f16 MMAs, A in tensor memory, B = S rows reordered so that accumulator
+//     column 32 tig + b is sign bit b of sign word tig); the thread reads its row back and packs
+//     the signs;
+//  5. the record words of the row's slot are stored.
+namespace encr {
+constexpr int D = 128, kRows = 128, kThreads = 256;
+template <typename T> __host__ __device__ constexpr int nx() { return sizeof(T) == 2 ? 2 : 1; }   // tiles in flight per warpgroup
+template <typename T> __host__ __device__ constexpr int row_bytes() { return D * (int)sizeof(T); }
+template <typename T> __host__ __device__ constexpr int row_stride() { return row_bytes<T>() + 16; }
+template <typename T> __host__ __device__ constexpr int xbuf_bytes() { return kRows * row_stride<T>(); }
+template <bool K> __host__ __device__ constexpr int oX() { return K ? 65536 : 0; }          // after S hi / lo
+template <typename T, bool K> __host__ __device__ constexpr int smem_bytes() {
+    return oX<K>() + 2 * nx<T>() * xbuf_bytes<T>();
+}
+}  // namespace encr
 
-template <typename T>
-__global__ void __launch_bounds__(enc128::kThreads, 1)
-encode128_tc_kernel(const uint8_t *__restrict__ params, const T *__restrict__ x, int64_t n_vec, SlotMap map,
-                    uint8_t *__restrict__ pool, int is_k, int32_t *status) {
-    using namespace enc128;
-    constexpr int R = D / 32, NXB = n_xbuf<T>(), XB = x_bytes<T>();
+template <typename T, bool IS_K>
+__global__ void __launch_bounds__(encr::kThreads, 1)
+encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ x, int64_t n_vec, SlotMap map,
+                      uint8_t *__restrict__ pool, int32_t *status) {
+    using namespace encr;
+    constexpr int NX = nx<T>(), RS = row_stride<T>(), RB = row_bytes<T>(), EPC = 16 / (int)sizeof(T);
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ uint64_t xfull[2], mmabar;
+    __shared__ uint64_t xfull[2][2], mmabar[2];
     __shared__ uint32_t tmem_base;
-    __shared__ int64_t sSlot[kRows];
-    __shared__ float s_cent[8], s_thr[8];
+    __shared__ float s_D[D];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     if (ph->magic != kParamsMagic || ph->d != D) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
         return;
     }
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, wg = tid >> 7, row = tid & 127, warp = tid >> 5;
     const int64_t ntiles = (n_vec + kRows - 1) / kRows;
     if ((int64_t)blockIdx.x >= ntiles) return;
     if (tid == 0) {
-        tc::mbar_init(&xfull[0], 1);
-        tc::mbar_init(&xfull[1], 1);
-        tc::mbar_init(&mmabar, 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&xfull[i][0], 1);
+            tc::mbar_init(&xfull[i][1], 1);
+            tc::mbar_init(&mmabar[i], 1);
+        }
     }
-    if (is_k && warp == 0) tc::tmem_alloc(&tmem_base, 128);
-    if (tid < 8) {
-        s_cent[tid] = ph->centroid[tid];
-        s_thr[tid] = ph->threshold[tid];
-    }
-    if (is_k) {
-        // B = S with rows permuted to sign-plane bit order and columns to the A operand's K order
+    if (IS_K && warp == 0) tc::tmem_alloc(&tmem_base, 512);
+    if (tid < D) s_D[tid] = reinterpret_cast<const float *>(params + params_off_D(D))[tid];
+    if (IS_K) {   // B row n = S row sigma(n), sigma(32 tig + b) = 16 (b & 7) + 8 ((b >> 3) & 1) + 2 tig + (b >> 4)
         const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
         for (int e = tid; e < D * D; e += kThreads) {
             const int n = e >> 7, k = e & 127;
-            const float sv = __ldg(S + kdim<D>(n & 31, n >> 5) * D + kdim<D>(k >> 2, k & 3));
+            const int tig = n >> 5, b = n & 31;
+            const int sr = 16 * (b & 7) + 8 * ((b >> 3) & 1) + 2 * tig + (b >> 4);
+            const float sv = __ldg(S + sr * D + k);
             const __half hi = __float2half_rn(sv);
             const __half lo = __float2half_rn(sv - __half2float(hi));
             const int off = tc::sw128_off(n, k, D);
-            *reinterpret_cast<__half *>(smem + oB + off) = hi;
-            *reinterpret_cast<__half *>(smem + oB + 32768 + off) = lo;
+            *reinterpret_cast<__half *>(smem + off) = hi;
+            *reinterpret_cast<__half *>(smem + 32768 + off) = lo;
         }
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = is_k ? tmem_base : 0u;
-    const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
+    const uint32_t tmem = IS_K ? tmem_base + 256u * wg : 0u;
+    const float t0 = ph->threshold[0], t1 = ph->threshold[1], t2 = ph->threshold[2], t3 = ph->threshold[3];
+    const float t4 = ph->threshold[4], t5 = ph->threshold[5], t6 = ph->threshold[6];
+    float cen[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) cen[k] = ph->centroid[k];
+    const float inv_sd = rsqrtf((float)D);
     bool timed_out = false;
 
-    auto issue = [&](int64_t tile, int buf) {
-        const int64_t v0 = tile * kRows;
+    auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)(2 * i + wg) * gridDim.x; };
+    // the first warp of the warpgroup: the tile's rows, one bulk copy per row, spread over its lanes
+    auto issue = [&](int i, int buf) {
+        const int64_t v0 = tile_of(i) * kRows;
         const int rows = (int)min((int64_t)kRows, n_vec - v0);
-        const uint32_t bytes = (uint32_t)rows * D * sizeof(T);
-        tc::mbar_arrive_expect_tx(&xfull[buf], bytes);
-        tc::bulk_g2s(smem + oX + buf * XB, x + v0 * D, bytes, &xfull[buf]);
+        uint8_t *dst = smem + oX<IS_K>() + (wg * NX + buf) * xbuf_bytes<T>();
+        if (row == 0) tc::mbar_arrive_expect_tx(&xfull[wg][buf], (uint32_t)rows * RB);
+        for (int r = row; r < rows; r += 32)
+            tc::bulk_g2s(dst + r * RS, x + (v0 + r) * D, RB, &xfull[wg][buf]);
     };
-    if (tid == 0)
-        for (int b2 = 0; b2 < NXB; ++b2) {
-            const int64_t t2 = blockIdx.x + (int64_t)b2 * gridDim.x;
-            if (t2 < ntiles) issue(t2, b2);
-        }
+    if (row < 32)
+        for (int b2 = 0; b2 < NX; ++b2)
+            if (tile_of(b2) < ntiles) issue(b2, b2);
+    const int bar_id = 1 + wg;
 
-    int it = 0;
 #pragma unroll 1
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
-        const int buf = (NXB == 2) ? (it & 1) : 0, use = (NXB == 2) ? (it >> 1) : it;
-        const int64_t v0 = tile * kRows;
-        const int rows = (int)min((int64_t)kRows, n_vec - v0);
-        if (tid < kRows) {
-            const int64_t v = v0 + tid;
-            sSlot[tid] = (tid < rows) ? map.slot(v / map.n_heads, status, (v % map.n_heads) == 0) : -1;
-        }
-        if (!tc::mbar_wait(&xfull[buf], use & 1)) timed_out = true;
-        __syncthreads();
-        const T *xt = reinterpret_cast<const T *>(smem + oX + buf * XB);
-        // ---- one warp per vector
-#pragma unroll 1
-        for (int j = 0; j < kRows / kTileWarps; ++j) {
-            const int v = warp + kTileWarps * j;
-            const bool valid = v < rows;
-            int dims[R];
-            float val[R];
+    for (int i = 0; tile_of(i) < ntiles; ++i) {
+        const int buf = i % NX, use = i / NX;
+        const int64_t v0 = tile_of(i) * kRows, v = v0 + row;
+        const bool valid = v < n_vec;
+        const int64_t slot = valid ? map.slot(v / map.n_heads, status, (v % map.n_heads) == 0) : -1;
+        if (!tc::mbar_wait(&xfull[wg][buf], use & 1)) timed_out = true;
+        // ---- 1. the row, in natural coordinate order
+        float val[D];
+        {
+            const uint8_t *xr = smem + oX<IS_K>() + (wg * NX + buf) * xbuf_bytes<T>() + row * RS;
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                dims[r] = is_k ? kdim<D>(lane, r) : vdim<D>(lane, r);
-                val[r] = valid ? to_f32<T>(xt[v * D + dims[r]]) : 0.f;
-            }
-            float ss = 0.f;
+            for (int c = 0; c < RB / 16; ++c) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(xr + 16 * c);
+                if constexpr (sizeof(T) == 2) {
+                    const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int r = 0; r < R; ++r) ss = fmaf(val[r], val[r], ss);
-            const float n = sqrtf(warp_sum(ss));
-#pragma unroll
-            for (int r = 0; r < R; ++r) val[r] *= __ldg(Dsign + dims[r]);
-            fwht_warp<R>(val, lane);                 // z = H(D x) / n = sqrt(d) Pi (x/n)
-            int code[R];
-            float rho[R], g2 = 0.f;
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const float z = (n > 0.f) ? val[r] / n : 0.f;
-                int k = 0;
-#pragma unroll
-                for (int t = 0; t < 7; ++t) k += (z >= s_thr[t]) ? 1 : 0;
-                code[r] = k;
-                rho[r] = z - s_cent[k];
-                g2 = fmaf(rho[r], rho[r], g2);
-            }
-            const int64_t slot = sSlot[v];
-            if (is_k) {
-                const float gam = sqrtf(warp_sum(g2)) / sqrtf((float)D);
-                __half h[R], l[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const float rs = valid ? rho[r] * kRhoScale : 0.f;
-                    h[r] = __float2half_rn(rs);
-                    l[r] = __float2half_rn(rs - __half2float(h[r]));
-                }
-                const int off = tc::sw128_off(v, 4 * lane, D);
-                uint2 hw, lw;
-                hw.x = (uint32_t)__half_as_ushort(h[0]) | ((uint32_t)__half_as_ushort(h[1]) << 16);
-                hw.y = (uint32_t)__half_as_ushort(h[2]) | ((uint32_t)__half_as_ushort(h[3]) << 16);
-                lw.x = (uint32_t)__half_as_ushort(l[0]) | ((uint32_t)__half_as_ushort(l[1]) << 16);
-                lw.y = (uint32_t)__half_as_ushort(l[2]) | ((uint32_t)__half_as_ushort(l[3]) << 16);
-                *reinterpret_cast<uint2 *>(smem + oA + off) = hw;
-                *reinterpret_cast<uint2 *>(smem + oA + 32768 + off) = lw;
-                if (slot >= 0) {
-                    const int64_t blk = slot / kBlock;
-                    const int o = (int)(slot % kBlock), head = (int)((v0 + v) % map.n_heads);
-                    uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * k_record(D);
-                    uint32_t *planes = reinterpret_cast<uint32_t *>(rec);
-                    const int gid = o & 7, th = o >> 3;
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint32_t w0 = __ballot_sync(0xffffffffu, code[r] & 1);
-                        const uint32_t w1 = __ballot_sync(0xffffffffu, (code[r] >> 1) & 1);
-                        const uint32_t w2 = __ballot_sync(0xffffffffu, (code[r] >> 2) & 1);
-                        if (lane == r) {
-                            const size_t word = (size_t)(4 * gid + r) * 2 + th;
-                            constexpr size_t PW = 2 * D / 4;
-                            planes[word] = w0;
-                            planes[PW + word] = w1;
-                            planes[2 * PW + word] = w2;
-                        }
+                    for (int q = 0; q < 4; ++q) {
+                        val[EPC * c + 2 * q] = valid ? __uint_as_float(w4[q] << 16) : 0.f;
+                        val[EPC * c + 2 * q + 1] = valid ? __uint_as_float(w4[q] & 0xFFFF0000u) : 0.f;
                     }
-                    if (lane == 0)
-                        *reinterpret_cast<__half2 *>(rec + 8 * D + 4 * o) =
-                            __halves2half2(__float2half_rn(n), __float2half_rn(gam));
+                } else {
+                    val[EPC * c] = valid ? __uint_as_float(u.x) : 0.f;
+                    val[EPC * c + 1] = valid ? __uint_as_float(u.y) : 0.f;
+                    val[EPC * c + 2] = valid ? __uint_as_float(u.z) : 0.f;
+                    val[EPC * c + 3] = valid ? __uint_as_float(u.w) : 0.f;
                 }
-            } else if (slot >= 0) {
-                const int64_t blk = slot / kBlock;
-                const int o = (int)(slot % kBlock), head = (int)((v0 + v) % map.n_heads);
-                uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * v_record(D);
-                constexpr int NWV = D / 64, NM = D / 128;
-                const int tigv = (o & 7) >> 1, jb = (o >> 3) + 2 * (o & 1);
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const uint32_t w0 = __ballot_sync(0xffffffffu, code[r] & 1);
-                    const uint32_t w1 = __ballot_sync(0xffffffffu, (code[r] >> 1) & 1);
-                    const uint32_t w2 = __ballot_sync(0xffffffffu, (code[r] >> 2) & 1);
-                    if ((lane >> 2) == r) {
-                        const int beta = lane & 3, tau = 4 * r + beta;
-                        const int mhi = tau % NM, rh = (tau / NM) & 1, gid = tau / (2 * NM);
-                        const size_t byte = ((size_t)(4 * gid + tigv) * NWV + 2 * mhi + rh) * 4 + jb;
-                        rec[byte] = (uint8_t)(w0 >> (8 * beta));
-                        rec[2 * D + byte] = (uint8_t)(w1 >> (8 * beta));
-                        rec[4 * D + byte] = (uint8_t)(w2 >> (8 * beta));
-                    }
-                }
-                if (lane == 0) *reinterpret_cast<__half *>(rec + 6 * D + 2 * o) = __float2half_rn(n);
             }
         }
-        // ---- K: QJL projections of the tile on the tensor cores, then the sign plane
-        if (is_k) {
-            tc::fence_async_smem();
+        tc::named_sync(bar_id, 128);   // every row is read: the buffer takes the tile NX ahead
+        if (row < 32 && tile_of(i + NX) < ntiles) issue(i + NX, buf);
+        if (slot < 0) {
+#pragma unroll
+            for (int n = 0; n < D; ++n) val[n] = 0.f;
+        }
+        // ---- 2. norm, signs, transform
+        float ss = 0.f;
+#pragma unroll
+        for (int n = 0; n < D; ++n) ss = fmaf(val[n], val[n], ss);
+        const float nrm = sqrtf(ss);
+#pragma unroll
+        for (int n = 0; n < D; ++n) val[n] *= s_D[n];
+#pragma unroll
+        for (int st = 1; st < D; st <<= 1)
+#pragma unroll
+            for (int n = 0; n < D; ++n)
+                if ((n & st) == 0) {
+                    const float a0 = val[n], a1 = val[n | st];
+                    val[n] = a0 + a1;
+                    val[n | st] = a0 - a1;
+                }
+        const float rn = nrm > 0.f ? 1.f / nrm : 0.f;
+        // ---- 3. cells: the three bits of the binary search, into the plane words
+        uint32_t w[3][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
+        float g2 = 0.f;
+#pragma unroll
+        for (int n = 0; n < D; ++n) {
+            const float z = val[n] * rn;
+            const bool b2 = z >= t3;
+            const bool b1 = z >= (b2 ? t5 : t1);
+            const bool b0 = z >= (b2 ? (b1 ? t6 : t4) : (b1 ? t2 : t0));
+            if (IS_K) {
+                const int tig = (n >> 1) & 3, bit = 8 * ((n >> 3) & 1) + (n >> 4) + 16 * (n & 1);
+                w[0][tig] |= (uint32_t)b0 << bit;
+                w[1][tig] |= (uint32_t)b1 << bit;
+                w[2][tig] |= (uint32_t)b2 << bit;
+                const float c = b2 ? (b1 ? (b0 ? cen[7] : cen[6]) : (b0 ? cen[5] : cen[4]))
+                                   : (b1 ? (b0 ? cen[3] : cen[2]) : (b0 ? cen[1] : cen[0]));
+                const float rho = z - c;
+                g2 = fmaf(rho, rho, g2);
+                val[n] = rho * 256.f;   // exact scaling; keeps the f16 low parts out of the subnormals
+            } else {
+                // V: coordinate n = 16 mt + gid + 8 rh is bit mt of byte 2 gid + rh (bytes 4 per word)
+                const int byte = 2 * (n & 7) + ((n >> 3) & 1), bit = 8 * (byte & 3) + (n >> 4);
+                w[0][byte >> 2] |= (uint32_t)b0 << bit;
+                w[1][byte >> 2] |= (uint32_t)b1 << bit;
+                w[2][byte >> 2] |= (uint32_t)b2 << bit;
+            }
+        }
+        uint32_t sgn[4] = {0u, 0u, 0u, 0u};
+        if constexpr (IS_K) {
+            // ---- 4. rho (x 256) as f16 hi / lo into this row's tensor-memory lane, then S rho
+            const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint32_t hw[32], lw[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const float a0 = val[64 * q + 2 * c], a1 = val[64 * q + 2 * c + 1];
+                    const __half2 h = __floats2half2_rn(a0, a1);
+                    const float2 hf = __half22float2(h);
+                    const __half2 l = __floats2half2_rn(a0 - hf.x, a1 - hf.y);
+                    hw[c] = *reinterpret_cast<const uint32_t *>(&h);
+                    lw[c] = *reinterpret_cast<const uint32_t *>(&l);
+                }
+                tc::st32(lane_addr + 32 * q, hw);
+                tc::st32(lane_addr + 64 + 32 * q, lw);
+            }
+            tc::wait_st();
             tc::fence_before_sync();
-            __syncthreads();
-            if (tid == 0) {
-                tc::fence_after_sync();
-                const uint32_t bh = tc::smem_u32(smem + oB), bl = bh + 32768;
-                const uint32_t ah = tc::smem_u32(smem + oA), al = ah + 32768;
+            tc::named_sync(bar_id, 128);
+            tc::fence_after_sync();
+            if (row == 0) {
+                const uint32_t bh = tc::smem_u32(smem), bl = bh + 32768;
                 constexpr uint32_t id = tc::idesc_f16(kRows, D);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    tc::mma_ss_f16(tmem, tc::sw128_desc(ah, ks, kRows), tc::sw128_desc(bh, ks, D), id, ks > 0);
+                    tc::mma_ts_f16(tmem + 128, tmem + 8 * ks, tc::sw128_desc(bh, ks, D), id, ks > 0);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    tc::mma_ss_f16(tmem, tc::sw128_desc(al, ks, kRows), tc::sw128_desc(bh, ks, D), id, true);
+                    tc::mma_ts_f16(tmem + 128, tmem + 64 + 8 * ks, tc::sw128_desc(bh, ks, D), id, true);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
-                    tc::mma_ss_f16(tmem, tc::sw128_desc(ah, ks, kRows), tc::sw128_desc(bl, ks, D), id, true);
-                tc::mma_commit(&mmabar);
+                    tc::mma_ts_f16(tmem + 128, tmem + 8 * ks, tc::sw128_desc(bl, ks, D), id, true);
+                tc::mma_commit(&mmabar[wg]);
             }
-            if (!tc::mbar_wait(&mmabar, it & 1)) timed_out = true;
+            if (!tc::mbar_wait(&mmabar[wg], i & 1)) timed_out = true;
             tc::fence_after_sync();
-            // thread: vector row 32 (warp % 4) + lane, sign word tig = warp / 4 (columns 32 tig ..)
-            const int vrow = 32 * (warp & 3) + lane, tig = warp >> 2;
-            const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * tig;
-            uint32_t sw = 0u;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
+            for (int j = 0; j < D / 16; ++j) {
                 float pv[16];
-                tc::ld16(taddr + 16 * q, pv);
+                tc::ld16(lane_addr + 128 + 16 * j, pv);
                 tc::wait_ld();
 #pragma unroll
-                for (int x2 = 0; x2 < 16; ++x2) sw |= (pv[x2] >= 0.f ? 1u : 0u) << (16 * q + x2);
-            }
-            const int64_t slot = (vrow < rows) ? sSlot[vrow] : -1;
-            if (slot >= 0) {
-                const int64_t blk = slot / kBlock;
-                const int o = (int)(slot % kBlock), head = (int)((v0 + vrow) % map.n_heads);
-                uint32_t *planes = reinterpret_cast<uint32_t *>(pool + ((size_t)blk * map.n_heads + head) * k_record(D));
-                constexpr size_t PW = 2 * D / 4;
-                planes[3 * PW + (size_t)(4 * (o & 7) + tig) * 2 + (o >> 3)] = sw;
+                for (int b = 0; b < 16; ++b) sgn[j >> 1] |= (pv[b] >= 0.f ? 1u : 0u) << (16 * (j & 1) + b);
             }
             tc::fence_before_sync();
         }
-        __syncthreads();   // the input buffer, the A operand and the accumulator are free
-        if (tid == 0) {
-            const int64_t nt = tile + (int64_t)NXB * gridDim.x;
-            if (nt < ntiles) issue(nt, buf);
+        // ---- 5. the record words of this row's slot
+        if (slot >= 0) {
+            const int64_t blk = slot / kBlock;
+            const int o = (int)(slot % kBlock), head = (int)(v % map.n_heads);
+            if (IS_K) {
+                uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * k_record(D);
+                uint32_t *planes = reinterpret_cast<uint32_t *>(rec);
+                constexpr int PW = 2 * D / 4;
+                const int gid = o & 7, th = o >> 3;
+#pragma unroll
+                for (int tig = 0; tig < 4; ++tig) {
+                    const int word = (4 * gid + tig) * 2 + th;
+                    planes[word] = w[0][tig];
+                    planes[PW + word] = w[1][tig];
+                    planes[2 * PW + word] = w[2][tig];
+                    planes[3 * PW + word] = sgn[tig];
+                }
+                const float gam = sqrtf(g2) * inv_sd;
+                *reinterpret_cast<__half2 *>(rec + 8 * D + 4 * o) = __halves2half2(__float2half_rn(nrm), __float2half_rn(gam));
+            } else {
+                uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * v_record(D);
+                const int tigv = (o & 7) >> 1, jb = (o >> 3) + 2 * (o & 1);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {   // byte k = 2 gid + rh of each plane
+                    const int gid = k >> 1, rh = k & 1;
+                    const size_t byte = ((size_t)(4 * gid + tigv) * 2 + rh) * 4 + jb;
+#pragma unroll
+                    for (int p = 0; p < 3; ++p) rec[p * 2 * D + byte] = (uint8_t)(w[p][k >> 2] >> (8 * (k & 3)));
+                }
+                *reinterpret_cast<__half *>(rec + 6 * D + 2 * o) = __float2half_rn(nrm);
+            }
         }
+        if (IS_K) tc::named_sync(bar_id, 128);   // the accumulator and A lanes are free for the next tile
     }
     if (timed_out) flag_status(status, TQ_STATUS_TIMEOUT);
-    if (is_k) {
+    if (IS_K) {
         tc::fence_before_sync();
         __syncthreads();
-        if (warp == 0) tc::tmem_dealloc(tmem, 128);
+        if (warp == 0) tc::tmem_dealloc(tmem_base, 512);
     }
 }
 
-template <typename T>
-cudaError_t launch_enc128(const void *params, const void *x, int64_t n_vec, const SlotMap &map, void *pool, bool is_k,
-                          int32_t *status, cudaStream_t st) {
-    const int64_t ntiles = (n_vec + enc128::kRows - 1) / enc128::kRows;
+template <typename T, bool IS_K>
+cudaError_t launch_encr(const void *params, const void *x, int64_t n_vec, const SlotMap &map, void *pool,
+                        int32_t *status, cudaStream_t st) {
+    const int64_t ntiles = (n_vec + encr::kRows - 1) / encr::kRows;
     if (ntiles <= 0) return cudaSuccess;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    constexpr int smem = enc128::smem_bytes<T>();
-    auto kern = encode128_tc_kernel<T>;
+    constexpr int smem = encr::smem_bytes<T, IS_K>();
+    auto kern = encode128_rows_kernel<T, IS_K>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(ntiles < sms ? ntiles : sms);
-    kern<<<grid, enc128::kThreads, smem, st>>>((const uint8_t *)params, (const T *)x, n_vec, map, (uint8_t *)pool,
-                                               is_k ? 1 : 0, status);
+    kern<<<grid, encr::kThreads, smem, st>>>((const uint8_t *)params, (const T *)x, n_vec, map, (uint8_t *)pool, status);
     return cudaGetLastError();
 }
 
@@ -339,10 +353,14 @@ cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const
                           int n_heads, const int64_t *slots, void *pool, int64_t num_blocks, int32_t *status,
                           cudaStream_t st) {
     SlotMap map{slots, nullptr, nullptr, 0, num_blocks, n_heads};
-    if (d == 128 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0)
-        return dtype == TQ_DTYPE_BF16
-                   ? launch_enc128<__nv_bfloat16>(params, x, n_tokens * n_heads, map, pool, is_k, status, st)
-                   : launch_enc128<float>(params, x, n_tokens * n_heads, map, pool, is_k, status, st);
+    if (d == 128 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
+        const int64_t nv = n_tokens * n_heads;
+        if (dtype == TQ_DTYPE_BF16)
+            return is_k ? launch_encr<__nv_bfloat16, true>(params, x, nv, map, pool, status, st)
+                        : launch_encr<__nv_bfloat16, false>(params, x, nv, map, pool, status, st);
+        return is_k ? launch_encr<float, true>(params, x, nv, map, pool, status, st)
+                    : launch_encr<float, false>(params, x, nv, map, pool, status, st);
+    }
     return launch_any<16>(d, dtype, params, is_k ? x : nullptr, is_k ? nullptr : x, n_tokens * n_heads, map,
                           is_k ? pool : nullptr, is_k ? nullptr : pool, is_k ? 1 : 2, status, st);
 }
