@@ -59,6 +59,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--main-only", action="store_true",
                     help="skip the ragged / long-context decode and the prefill encode measurements")
+    ap.add_argument("--workload", default=None,
+                    help="run only this side workload (ragged, long256, verify_q2, hybrid32k, prefill_encode, "
+                         "prefill_dequant) and print its JSON object; for profiling")
     return ap.parse_args()
 
 
@@ -750,10 +753,32 @@ def bench_tq(args):
     return 0
 
 
+def side_workload(args):
+    import torch
+
+    import turboquant_compressed_kv_gb300 as tq
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    tq.load_library()
+    steps, warmup = max(1, args.steps), max(1, args.warmup)
+    runs = {"ragged": lambda: extra_decode("ragged", steps, warmup, dev),
+            "long256": lambda: extra_decode("long256", steps, warmup, dev),
+            "verify_q2": lambda: extra_verify(steps, warmup, dev),
+            "hybrid32k": lambda: extra_hybrid(steps, warmup, dev),
+            "prefill_encode": lambda: extra_encode(steps, warmup, dev),
+            "prefill_dequant": lambda: extra_dequant(steps, warmup, dev)}
+    if args.workload not in runs:
+        raise SystemExit(f"unknown workload {args.workload}; one of {sorted(runs)}")
+    print(json.dumps({"workload": args.workload, **runs[args.workload]()}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return bench_reference(args)
+    if args.workload:
+        return side_workload(args)
     return bench_tq(args)
 
 
