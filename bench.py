@@ -61,7 +61,7 @@ def parse():
                     help="skip the ragged / long-context decode and the prefill encode measurements")
     ap.add_argument("--workload", default=None,
                     help="run only this side workload (ragged, long256, verify_q2, hybrid32k, prefill_encode, "
-                         "prefill_dequant) and print its JSON object; for profiling")
+                         "prefill_dequant, gq_compare) and print its JSON object; for profiling")
     return ap.parse_args()
 
 
@@ -577,6 +577,90 @@ def extra_encode(steps, warmup, dev):
     return res
 
 
+def extra_gq(steps, warmup, dev, group=64):
+    """Fidelity comparator on the llama8b_decode shape (every sequence at 4096 tokens): the same
+    bf16 K / V encoded by TurboQuant and by 4- and 8-bit group quantisation; for each, the decode
+    attention's cosine similarity to dense fp32 attention over the uncompressed K / V (information,
+    per (sequence, query head)), and the group-quantised decode's time over its own cache bytes."""
+    import torch
+
+    import turboquant_compressed_kv_gb300 as tq
+    from turboquant_compressed_kv_gb300 import synth
+    from turboquant_compressed_kv_gb300.cache import PagedCache, to_device
+    w = synth.workload("llama8b_decode")
+    d, B, Hq, Hkv = w.head_dim, w.batch, w.n_q_heads, w.n_kv_heads
+    G, L = Hq // Hkv, max(w.ctx_lens)
+    cache = PagedCache.create(w, dev)
+    nblk = cache.num_blocks
+    gk = {bits: tq.gq_empty_pool(nblk, Hkv, d, bits, group, dev) for bits in (4, 8)}
+    gv = {bits: tq.gq_empty_pool(nblk, Hkv, d, bits, group, dev) for bits in (4, 8)}
+    Kd = torch.empty((B, L, Hkv, d), dtype=torch.bfloat16, device=dev)
+    Vd = torch.empty_like(Kd)
+    for b in range(B):
+        K, V = synth.kv_tokens_device(w, b, 0, L, dev)
+        Kd[b], Vd[b] = K, V
+        slots = torch.from_numpy(synth.slots_for(cache.block_table_np, b, 0, L)).to(dev)
+        tq.encode_k(cache.params, d, K, slots, cache.k_pool)
+        tq.encode_v(cache.params, d, V, slots, cache.v_pool)
+        for bits in (4, 8):
+            tq.gq_encode(d, bits, group, K, slots, gk[bits])
+            tq.gq_encode(d, bits, group, V, slots, gv[bits])
+    q = to_device(synth.queries(w), w.dtype, dev)
+    ctx = torch.full((B,), L, dtype=torch.int32, device=dev)
+    qf = q.float().view(B, Hkv, G, d)
+    p = torch.softmax(torch.einsum("bhgd,blhd->bhgl", qf, Kd.float()) / math.sqrt(d), -1)
+    ref = torch.einsum("bhgl,blhd->bhgd", p, Vd.float()).reshape(B, Hq, d).double()
+    del p, Kd, Vd
+
+    def fidelity(o):
+        c = torch.nn.functional.cosine_similarity(o.double(), ref, dim=-1)
+        return {"cos_mean": round(float(c.mean()), 6), "cos_min": round(float(c.min()), 6)}
+
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = tq.decode_attn(cache.params, d, q, Hkv, cache.k_pool, cache.v_pool, cache.block_table, ctx, L,
+                         status=status)
+    kb, vb = tq.k_record_bytes(d), tq.v_record_bytes(d)
+    res = {"config": {"workload": "gq_compare", "batch": B, "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": d,
+                      "ctx": L, "group": group, "reference": "dense fp32 attention over the bf16 K / V"},
+           "turboquant": {"bits_per_dim": round((kb + vb) * 8 / (2 * 16 * d), 4), **fidelity(out)}}
+    bt = cache.block_table
+    del cache
+    stream = torch.cuda.current_stream()
+    peak, _ = measured_peak()
+    for bits in (4, 8):
+        per_cache = gk[bits].numel() + gv[bits].numel()
+        nrep = max(2, math.ceil(3 * L2_BYTES / per_cache))
+        pools = [(gk[bits], gv[bits])] + [(gk[bits].clone(), gv[bits].clone()) for _ in range(nrep - 1)]
+        ws = torch.empty(tq.gq_decode_workspace_bytes(d, B, Hq, Hkv, L), dtype=torch.uint8, device=dev)
+        o = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+
+        def step(i):
+            kp, vp = pools[i % nrep]
+            tq.gq_decode_attn(d, bits, group, q, Hkv, kp, vp, bt, ctx, L, out=o, workspace=ws, status=status)
+
+        for i in range(warmup):
+            step(i)
+        torch.cuda.synchronize(dev)
+        fid = fidelity(o)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            step(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        nbytes = B * L * Hkv * 2 * tq.gq_record_bytes(d, bits, group) / 16
+        res[f"gq{bits}"] = {"bits_per_dim": tq.gq_record_bytes(d, bits, group) * 8 / (16 * d), **fid,
+                            "ms_per_step": round(ms, 6), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 3),
+                            "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4), "launches_per_step": 2,
+                            "l2": f"{nrep} cache copies cycled ({nrep * per_cache / 2**20:.0f} MiB > L2)"}
+        del pools, ws
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in gq_compare")
+    torch.cuda.empty_cache()
+    return res
+
+
 def bench_tq(args):
     import numpy as np
     import torch
@@ -739,7 +823,8 @@ def bench_tq(args):
                              "verify_q2": extra_verify(ksteps, max(3, args.warmup), dev),
                              "hybrid32k": extra_hybrid(ksteps, max(3, args.warmup), dev),
                              "prefill_encode": extra_encode(max(3, min(args.steps, 50)), max(3, args.warmup), dev),
-                             "prefill_dequant": extra_dequant(max(3, min(args.steps, 50)), max(3, args.warmup), dev)}
+                             "prefill_dequant": extra_dequant(max(3, min(args.steps, 50)), max(3, args.warmup), dev),
+                             "gq_compare": extra_gq(max(3, min(args.steps, 100)), max(3, args.warmup), dev)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         gbs, dt, _ = run_cpu_oracle(w, 3, 1, 2)
         line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
@@ -766,7 +851,8 @@ def side_workload(args):
             "verify_q2": lambda: extra_verify(steps, warmup, dev),
             "hybrid32k": lambda: extra_hybrid(steps, warmup, dev),
             "prefill_encode": lambda: extra_encode(steps, warmup, dev),
-            "prefill_dequant": lambda: extra_dequant(steps, warmup, dev)}
+            "prefill_dequant": lambda: extra_dequant(steps, warmup, dev),
+            "gq_compare": lambda: extra_gq(steps, warmup, dev)}
     if args.workload not in runs:
         raise SystemExit(f"unknown workload {args.workload}; one of {sorted(runs)}")
     print(json.dumps({"workload": args.workload, **runs[args.workload]()}), flush=True)

@@ -308,6 +308,49 @@ int tq_decode_attn_noalloc(const void *params, int d, const void *q, int dtype, 
                            const int32_t *ctx_lens, int max_ctx, float *out, int32_t *status,
                            tq_stream_t stream);
 
+/* ---- Group-quantised KV cache: the fidelity comparator beside TurboQuant.
+ * [README "Per-Request API Parameters": kv_bits (4 or 8) selects MLX-native standard group
+ *  quantization of the KV cache from token 0, kv_group_size its group (default 64), "~2-4x vs
+ *  FP16"; ART "TurboQuant V2+V3ハイブリッド実装": the V2 route, linear affine quantization.]
+ * For each group of `group` consecutive coordinates of a (token, kv head) vector x:
+ *   scale = fp16((max - min) / (2^bits - 1)),  bias = fp16(min),
+ *   code_i = clamp(rint((x_i - bias) / scale), 0, 2^bits - 1)   (0 when scale is 0),
+ * every step in fp32 with round-to-nearest-even; the decoded coordinate is scale * code + bias.
+ * K and V use the same format (no rotation, no QJL).  Supported: d 128 or 256, bits 4 or 8,
+ * group 32, 64 or 128.
+ * Record of one (block, kv head), tq_gq_record_bytes(d, bits, group) bytes:
+ *   codes  [16 slots][d * bits / 8]  4-bit: coordinate 2j in the low nibble of byte j
+ *   params [16 slots][d / group][2]  fp16 scale, fp16 bias
+ * At d = 128, group 64: 1152 B (4.5 bits/dim) at 4 bits, 2176 B (8.5 bits/dim) at 8 bits.
+ * 0 for an unsupported combination. */
+size_t tq_gq_record_bytes(int d, int bits, int group);
+
+/* tq_gq_encode -- quantise x [n_tokens][n_kv_heads][d] (dtype, contiguous, 16-byte aligned)
+ * into slot slot_mapping[token] of `pool` (num_blocks records per kv head, 16-byte aligned).
+ * Slots as tq_encode_k: negative skipped silently, >= 16 num_blocks flagged
+ * TQ_STATUS_BAD_SLOT and skipped.  Coordinates must be finite and within fp16 range.
+ * Errors: TQ_ERR_HEAD_DIM, TQ_ERR_INVALID (also bits or group unsupported), TQ_ERR_DTYPE,
+ * TQ_ERR_ALIGN, TQ_ERR_CUDA. */
+int tq_gq_encode(int d, int bits, int group, const void *x, int dtype, int64_t n_tokens,
+                 int n_kv_heads, const int64_t *slot_mapping, void *pool, int64_t num_blocks,
+                 int32_t *status, tq_stream_t stream);
+
+/* Workspace of tq_gq_decode_attn: per (sequence, kv head, 128-token chunk of max_ctx, query
+ * head of the group rounded up to 1, 2, 4 or 8) a partial of d + 4 floats.  0 if invalid. */
+size_t tq_gq_decode_workspace_bytes(int d, int batch, int n_q_heads, int n_kv_heads, int max_ctx);
+
+/* tq_gq_decode_attn -- decode attention over group-quantised paged K and V pools: for query
+ * head h of sequence b (kv head h / G) over its ctx_lens[b] tokens,
+ *   s_j = q . k~_j / sqrt d,  P = softmax(s),  out = sum_j P_j v~_j,
+ * with k~, v~ the decoded vectors; fp32 arithmetic, out float [batch][n_q_heads][d].
+ * Arguments, block-table and ctx_lens semantics, status and errors as tq_decode_attn (no params
+ * buffer; workspace from tq_gq_decode_workspace_bytes, 16-byte aligned). */
+int tq_gq_decode_attn(int d, int bits, int group, const void *q, int dtype, int batch,
+                      int n_q_heads, int n_kv_heads, const void *k_pool, const void *v_pool,
+                      int64_t num_blocks, const int32_t *block_table, int max_blocks,
+                      const int32_t *ctx_lens, int max_ctx, float *out, void *workspace,
+                      size_t workspace_bytes, int32_t *status, tq_stream_t stream);
+
 /* Short English text for a TQ_* return code (static storage). */
 const char *tq_error_string(int code);
 

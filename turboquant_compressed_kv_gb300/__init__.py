@@ -7,7 +7,9 @@ point without the built library raises immediately (there is no fallback).
 
 Entry points (same names as the C ABI, minus the ``tq_`` prefix):
   codebook_init, encode_k, encode_v, paged_append, decode_attn,
-  params_bytes, k_record_bytes, v_record_bytes, decode_workspace_bytes.
+  params_bytes, k_record_bytes, v_record_bytes, decode_workspace_bytes,
+  the decode variants (decode_attn_mq, decode_step, decode_attn_hybrid, ...),
+  dequant_k / dequant_v, and the group-quantised comparator (gq_*).
 """
 from __future__ import annotations
 
@@ -100,6 +102,15 @@ def _declare(L):
                                         _P, _P, _SZ, _P, _P]
     L.tq_decode_attn_noalloc.restype = _I
     L.tq_decode_attn_noalloc.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _P]
+    L.tq_gq_record_bytes.restype = _SZ
+    L.tq_gq_record_bytes.argtypes = [_I, _I, _I]
+    L.tq_gq_encode.restype = _I
+    L.tq_gq_encode.argtypes = [_I, _I, _I, _P, _I, _I64, _I, _P, _P, _I64, _P, _P]
+    L.tq_gq_decode_workspace_bytes.restype = _SZ
+    L.tq_gq_decode_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
+    L.tq_gq_decode_attn.restype = _I
+    L.tq_gq_decode_attn.argtypes = [_I, _I, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _SZ, _P,
+                                    _P]
 
 
 
@@ -392,4 +403,52 @@ def decode_attn_noalloc(params, d: int, q, n_kv_heads: int, k_pool, v_pool, bloc
                                                block_table.shape[1], _ptr(ctx_lens), max_ctx, _ptr(out),
                                                _ptr(status), _stream(stream))
     _check(rc, "tq_decode_attn_noalloc")
+    return out
+
+
+# ---------------------------------------------------------------- group-quantised comparator
+
+def gq_record_bytes(d: int, bits: int, group: int = 64) -> int:
+    """tq_gq_record_bytes: bytes of one (block, kv head) record of the group-quantised cache."""
+    return load_library().tq_gq_record_bytes(d, bits, group)
+
+
+def gq_empty_pool(num_blocks: int, n_kv_heads: int, d: int, bits: int, group: int = 64, device="cuda"):
+    """Zeroed group-quantised pool tensor uint8[num_blocks][n_kv_heads][record_bytes]."""
+    torch = _torch()
+    rec = gq_record_bytes(d, bits, group)
+    if rec == 0:
+        raise TQError(f"unsupported group-quantised format d={d} bits={bits} group={group}")
+    return torch.zeros((num_blocks, n_kv_heads, rec), dtype=torch.uint8, device=device)
+
+
+def gq_encode(d: int, bits: int, group: int, x, slot_mapping, pool, status=None, stream=None):
+    """tq_gq_encode: x [n_tokens][n_kv_heads][d] (f32/bf16) into slot slot_mapping[token] of pool."""
+    _need_cuda(x, slot_mapping, pool, status)
+    n, h = x.shape[0], x.shape[1]
+    rc = load_library().tq_gq_encode(d, bits, group, _ptr(x), _dtype_code(x), n, h, _ptr(slot_mapping), _ptr(pool),
+                                     pool.shape[0], _ptr(status), _stream(stream))
+    _check(rc, "tq_gq_encode")
+
+
+def gq_decode_workspace_bytes(d: int, batch: int, n_q_heads: int, n_kv_heads: int, max_ctx: int) -> int:
+    return load_library().tq_gq_decode_workspace_bytes(d, batch, n_q_heads, n_kv_heads, max_ctx)
+
+
+def gq_decode_attn(d: int, bits: int, group: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens,
+                   max_ctx: int, out=None, workspace=None, status=None, stream=None):
+    """tq_gq_decode_attn: q [batch][n_q_heads][d] -> out float32 [batch][n_q_heads][d]."""
+    torch = _torch()
+    _need_cuda(q, k_pool, v_pool, block_table, ctx_lens, out, workspace, status)
+    B, Hq = q.shape[0], q.shape[1]
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
+    need = gq_decode_workspace_bytes(d, B, Hq, n_kv_heads, max_ctx)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    rc = load_library().tq_gq_decode_attn(d, bits, group, _ptr(q), _dtype_code(q), B, Hq, n_kv_heads, _ptr(k_pool),
+                                          _ptr(v_pool), k_pool.shape[0], _ptr(block_table), block_table.shape[1],
+                                          _ptr(ctx_lens), max_ctx, _ptr(out), _ptr(workspace), workspace.numel(),
+                                          _ptr(status), _stream(stream))
+    _check(rc, "tq_gq_decode_attn")
     return out

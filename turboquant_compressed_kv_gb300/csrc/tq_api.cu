@@ -2,6 +2,7 @@
 // then kernel launches on the caller's stream.  Allocates no device memory.
 #include <math.h>
 
+#include "tq_gq.cuh"
 #include "tq_internal.cuh"
 
 namespace tq {
@@ -327,6 +328,56 @@ int tq_decode_step(const void *params, int d, const void *k_new, const void *v_n
     return tq_decode_step_mq(params, d, k_new, v_new, q, dtype, batch, 1, n_q_heads, n_kv_heads, block_table,
                              max_blocks, pre_lens, max_ctx, k_pool, v_pool, num_blocks, out, workspace,
                              workspace_bytes, status, stream);
+}
+
+size_t tq_gq_record_bytes(int d, int bits, int group) { return gq_valid(d, bits, group) ? gq_region_bytes(d, bits, group) : 0; }
+
+static int check_gq(int d, int bits, int group) {
+    if (d != 128 && d != 256) return TQ_ERR_HEAD_DIM;
+    return gq_valid(d, bits, group) ? TQ_OK : TQ_ERR_INVALID;
+}
+
+int tq_gq_encode(int d, int bits, int group, const void *x, int dtype, int64_t n_tokens, int n_kv_heads,
+                 const int64_t *slot_mapping, void *pool, int64_t num_blocks, int32_t *status, tq_stream_t stream) {
+    int rc = check_gq(d, bits, group);
+    if (rc != TQ_OK) return rc;
+    if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16) return TQ_ERR_DTYPE;
+    if (n_tokens < 0 || n_kv_heads <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
+    if (n_tokens == 0) return TQ_OK;
+    if (!x || !slot_mapping || !pool) return TQ_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(pool)) return TQ_ERR_ALIGN;
+    if (n_tokens > ((int64_t)1 << 40) / n_kv_heads) return TQ_ERR_INVALID;
+    return cuda_status(launch_gq_encode(d, bits, group, dtype, x, n_tokens, n_kv_heads, slot_mapping,
+                                        static_cast<uint8_t *>(pool), num_blocks, status,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t tq_gq_decode_workspace_bytes(int d, int batch, int n_q_heads, int n_kv_heads, int max_ctx) {
+    if ((d != 128 && d != 256) || batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_ctx < 0) return 0;
+    if (n_q_heads % n_kv_heads != 0 || n_q_heads / n_kv_heads > 8) return 0;
+    return gq_workspace_bytes(d, batch, n_q_heads, n_kv_heads, max_ctx);
+}
+
+int tq_gq_decode_attn(int d, int bits, int group, const void *q, int dtype, int batch, int n_q_heads, int n_kv_heads,
+                      const void *k_pool, const void *v_pool, int64_t num_blocks, const int32_t *block_table,
+                      int max_blocks, const int32_t *ctx_lens, int max_ctx, float *out, void *workspace,
+                      size_t workspace_bytes, int32_t *status, tq_stream_t stream) {
+    int rc = check_gq(d, bits, group);
+    if (rc != TQ_OK) return rc;
+    if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16) return TQ_ERR_DTYPE;
+    if (batch < 0 || n_q_heads <= 0 || n_kv_heads <= 0 || max_ctx < 0) return TQ_ERR_INVALID;
+    if (n_q_heads % n_kv_heads != 0 || n_q_heads / n_kv_heads > 8) return TQ_ERR_GQA;
+    if (batch > 65535 || n_kv_heads > 65535) return TQ_ERR_INVALID;
+    if (batch == 0) return TQ_OK;
+    if (max_blocks <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
+    if (!q || !k_pool || !v_pool || !block_table || !ctx_lens || !out) return TQ_ERR_INVALID;
+    if (workspace_bytes < gq_workspace_bytes(d, batch, n_q_heads, n_kv_heads, max_ctx)) return TQ_ERR_WORKSPACE;
+    if (max_ctx > 0 && !workspace) return TQ_ERR_INVALID;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(workspace)) return TQ_ERR_ALIGN;
+    return cuda_status(launch_gq_decode(d, bits, group, dtype, q, batch, n_q_heads, n_kv_heads,
+                                        static_cast<const uint8_t *>(k_pool), static_cast<const uint8_t *>(v_pool),
+                                        num_blocks, block_table, max_blocks, ctx_lens, max_ctx, out,
+                                        static_cast<float *>(workspace), status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -186,7 +186,7 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint64_t recbar[2][2], mmabar[2];
     __shared__ uint32_t tmem_base;
-    __shared__ float s_cent[8];
+    __shared__ float s_cent[8], s_D[D];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     if (ph->magic != kParamsMagic || ph->d != D) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
@@ -204,6 +204,7 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     }
     if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
     if (tid < 8) s_cent[tid] = ph->centroid[tid];
+    if (tid < D) s_D[tid] = reinterpret_cast<const float *>(params + params_off_D(D))[tid];
     {   // B: row n = output coordinate n, K index k' as in the A operand; S as f16 hi + lo
         const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
         for (int e = tid; e < D * D; e += kThreads) {
@@ -223,7 +224,6 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base + 128u * wg;
-    const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
     const float inv_sd = rsqrtf((float)D);
     const float qjl = 1.2533141373155003f / (float)D;   // sqrt(pi/2) / d
     bool timed_out = false;
@@ -350,7 +350,7 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
             for (int n = 0; n < D; n += 4) {
                 float o4[4];
 #pragma unroll
-                for (int x = 0; x < 4; ++x) o4[x] = good ? y[n + x] * sc * __ldg(Dsign + n + x) : 0.f;
+                for (int x = 0; x < 4; ++x) o4[x] = good ? y[n + x] * sc * s_D[n + x] : 0.f;
                 if constexpr (sizeof(TO) == 4) {
                     *reinterpret_cast<float4 *>(orow + n) = make_float4(o4[0], o4[1], o4[2], o4[3]);
                 } else {
