@@ -759,17 +759,20 @@ def bench_tq(args):
         raise RuntimeError(f"device status {int(status.item())} during the bench")
 
     # end-to-end through the public API with pinned host buffers
-    hq = torch.from_numpy(np.ascontiguousarray(q_np)).to(q.dtype).pin_memory()
-    hk = torch.from_numpy(np.ascontiguousarray(K1)).to(k_new.dtype).pin_memory()
-    hv = torch.from_numpy(np.ascontiguousarray(V1)).to(v_new.dtype).pin_memory()
+    # the step's inputs (q, new K, new V) sit in one pinned buffer and go over in one copy
+    assert q.dtype == k_new.dtype == v_new.dtype
+    nq, nk = q.numel(), k_new.numel()
+    hin = torch.empty(nq + 2 * nk, dtype=q.dtype).pin_memory()
+    hin[:nq].copy_(torch.from_numpy(np.ascontiguousarray(q_np)).reshape(-1).to(q.dtype))
+    hin[nq:nq + nk].copy_(torch.from_numpy(np.ascontiguousarray(K1)).reshape(-1).to(q.dtype))
+    hin[nq + nk:].copy_(torch.from_numpy(np.ascontiguousarray(V1)).reshape(-1).to(q.dtype))
     hout = torch.empty((B, Hq, d), dtype=torch.float32).pin_memory()
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+    din = torch.empty(hin.shape, dtype=hin.dtype, device=dev)
+    dq, dk, dv = din[:nq].view(q.shape), din[nq:nq + nk].view(k_new.shape), din[nq + nk:].view(v_new.shape)
 
     def e2e_step(i):
         kp, vp = pools[i % nrep]
-        dq.copy_(hq, non_blocking=True)
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
+        din.copy_(hin, non_blocking=True)
         tq.decode_step(cache.params, d, dk, dv, dq, Hkv, kp, vp, cache.block_table, pre, max_ctx, out=out,
                        workspace=ws)
         hout.copy_(out, non_blocking=True)
@@ -782,7 +785,7 @@ def bench_tq(args):
         e2e_step(i)
     barrier()
     e2e_s = (time.perf_counter() - t0) / args.steps
-    h2d = hq.numel() * hq.element_size() + hk.numel() * hk.element_size() + hv.numel() * hv.element_size()
+    h2d = hin.numel() * hin.element_size()
     d2h = hout.numel() * 4
 
     # max over ranks

@@ -55,6 +55,7 @@ qprep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ q, int ba
              const int32_t *__restrict__ ctx_lens, int max_ctx, int chunk, int P, uint8_t *__restrict__ packs,
              unsigned int *__restrict__ counters, int64_t *__restrict__ cpre, int32_t *__restrict__ cta_b) {
     extern __shared__ __align__(16) uint8_t qsm[];
+    pdl_launch_dependents();
     qprep_rows<D, NTK, T>(params, q, batch, q_len, hq, hkv, ctx_lens, 0, max_ctx, chunk, P, packs, counters, cpre, cta_b,
                           blockIdx.x, qsm);
 }
@@ -122,6 +123,8 @@ decode_mma_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict_
 
     const int cta = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
+
+    pdl_wait();   // everything before this launch (the prep's schedule, packs, counters) is complete
 
     // sequences with nothing to attend get out = 0
     for (int b = cta; b < batch; b += gridDim.x)
@@ -622,9 +625,8 @@ cudaError_t pass_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batc
     auto kern = decode_mma_kernel<D, G, NWARP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<nctas, NWARP * 32, smem, st>>>(P, w.packs, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx,
-                                         w.cpre, w.cta_b, w.part, w.counters, out, lse, status);
-    return cudaGetLastError();
+    return launch_pass(kern, nctas, NWARP * 32, smem, st, P, w.packs, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx,
+                       ctx_add, max_ctx, w.cpre, w.cta_b, w.part, w.counters, out, lse, status);
 }
 
 template <int D>
@@ -697,6 +699,7 @@ step_prep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ k_new
                  unsigned int *__restrict__ counters, int64_t *__restrict__ cpre, int32_t *__restrict__ cta_b,
                  int32_t *status) {
     extern __shared__ __align__(16) uint8_t smem[];
+    pdl_launch_dependents();
     const int blk = blockIdx.x;
     if (blk < 2 * n_app) {
         const bool is_k = blk < n_app;

@@ -105,6 +105,8 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
     __shared__ float sM[8], sL[8];
     __shared__ bool s_last;
 
+    pdl_wait();   // everything before this launch (the prep's schedule, packs, counters) is complete
+
     for (int b = cta; b < batch; b += gridDim.x)
         if (attended_len(ctx_lens[b], ctx_add, max_ctx) == 0)
         {
@@ -674,9 +676,8 @@ cudaError_t warp_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batc
     auto kern = decode_warp_kernel<G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<nctas, kWWarps * 32, smem, st>>>(P, w.packs, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx,
-                                            w.cpre, w.cta_b, w.part, w.counters, out, lse, status);
-    return cudaGetLastError();
+    return launch_pass(kern, nctas, kWWarps * 32, smem, st, P, w.packs, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx,
+                       ctx_add, max_ctx, w.cpre, w.cta_b, w.part, w.counters, out, lse, status);
 }
 
 }  // namespace

@@ -145,6 +145,13 @@ __device__ __forceinline__ void flag_status(int32_t *status, int bits) {
 
 // ---------------------------------------------------------------- async copies
 
+// Programmatic dependent launch.  A prep kernel lets the decode pass launched after it (with
+// cudaLaunchAttributeProgrammaticStreamSerialization) start early; the pass waits for the
+// prep grid's completion and memory before it reads anything the prep wrote.  Both are no-ops
+// for a launch without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
     const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");

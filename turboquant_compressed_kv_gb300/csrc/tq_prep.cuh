@@ -71,12 +71,13 @@ __device__ __forceinline__ void encode_tiles(const uint8_t *__restrict__ params,
     uint8_t (*s_sgn)[D] = reinterpret_cast<uint8_t (*)[D]>(smem + SM::kST + SM::kRho);
     __shared__ float s_cent[8], s_thr[8];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
-    if (ph->magic != kParamsMagic || ph->d != D) {
-        if (threadIdx.x == 0 && blk == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
-        return;
-    }
     const float *gST = reinterpret_cast<const float *>(params + params_off_ST(D));
     if (is_k && SM::kResident) stage_st_rows<D, kEncWarps * 32>(sST, gST, 0, D);   // waited before first use
+    if (ph->magic != kParamsMagic || ph->d != D) {
+        if (threadIdx.x == 0 && blk == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
+        cp_async_wait_all();
+        return;
+    }
     if (threadIdx.x < 8) {
         s_cent[threadIdx.x] = ph->centroid[threadIdx.x];
         s_thr[threadIdx.x] = ph->threshold[threadIdx.x];
@@ -226,6 +227,12 @@ __host__ __device__ constexpr float op_delta(int q) {
          : q == 12 ? -0.9375f : q == 13 ? -0.99609375f : q == 14 ? 2.0f : -2.0f;
 }
 
+// 2 / delta_q, the factor that turns a query coordinate into its B-operand value
+__host__ __device__ constexpr float op_two_over_delta(int q) {
+    return q == 8 ? 8.f : q == 9 ? 4.f : q == 10 ? -4.f : q == 11 ? -2.f / 0.75f
+         : q == 12 ? -2.f / 0.9375f : q == 13 ? -2.f / 0.99609375f : q == 14 ? 1.0f : -1.0f;
+}
+
 __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                         uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
@@ -294,6 +301,8 @@ __device__ __forceinline__ void qprep_rows(const uint8_t *__restrict__ params, c
     const float *Dsign = reinterpret_cast<const float *>(params + params_off_D(D));
     const float *ST = reinterpret_cast<const float *>(params + params_off_ST(D));
     const float inv_sd = rsqrtf((float)D);
+    constexpr bool kOneCopy = qprep_st_rows<D>() == D;
+    if constexpr (kOneCopy) stage_st_rows<D, 128>(sbuf, ST, 0, D);   // in flight while the rows rotate
     {
         const int row = row0 + warp;
         float v[R];
@@ -310,7 +319,13 @@ __device__ __forceinline__ void qprep_rows(const uint8_t *__restrict__ params, c
         for (int u = 0; u < KPT; ++u)
 #pragma unroll
             for (int rr = 0; rr < kQRows; ++rr) acc[u][rr] = 0.f;
-        project_streamed<D, kQRows, 128, qprep_st_rows<D>()>(ST, sbuf, qs, acc);     // u = S qbar
+        if constexpr (kOneCopy) {                                              // u = S qbar
+            cp_async_wait_all();
+            __syncthreads();
+            project_rows<D, kQRows, 128>(sbuf, 0, D, qs, acc);
+        } else {
+            project_streamed<D, kQRows, 128, qprep_st_rows<D>()>(ST, sbuf, qs, acc);
+        }
 #pragma unroll
         for (int u = 0; u < KPT; ++u)
 #pragma unroll
@@ -338,7 +353,7 @@ __device__ __forceinline__ void qprep_rows(const uint8_t *__restrict__ params, c
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const int dim = 32 * r + lane, s = dim >> 4, k = dim & 15, qd = 8 + (s & 7);
-                const float beta = 2.f * (qu == 0 ? v[r] : u[r]) / op_delta(qd);
+                const float beta = (qu == 0 ? v[r] : u[r]) * op_two_over_delta(qd);
                 const __half hi = __float2half_rn(beta);
                 const __half lo = __float2half_rn(beta - __half2float(hi));
                 cs = fmaf(__half2float(hi) + __half2float(lo), op_alpha(qd) + 0.5f * op_delta(qd), cs);

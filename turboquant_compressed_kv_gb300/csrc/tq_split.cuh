@@ -23,6 +23,28 @@ constexpr int kCtasPerSm = TQ_SPLITK_CTAS_PER_SM;
 #ifndef TQ_DECODE_WARP
 #define TQ_DECODE_WARP 1         // d = 128 runs the warp-local pass (tq_decode_warp.cu)
 #endif   // persistent CTAs per SM (at most)
+#ifndef TQ_DECODE_PDL
+#define TQ_DECODE_PDL 1          // the pass may launch while the prep launch before it finishes
+#endif
+
+// Launch of a decode pass.  With TQ_DECODE_PDL it is a programmatic dependent launch: its CTAs
+// may be launched while the prep kernel before it on the stream finishes (the prep signals
+// pdl_launch_dependents as it starts), and they wait for that kernel's completion (pdl_wait)
+// before touching memory.  After any other kernel it behaves as an ordinary launch.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pass(void (*kern)(KArgs...), int nctas, int threads, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nctas);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = TQ_DECODE_PDL ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 // warps of the pass for a group of G query heads, and tokens per chunk
 #ifndef TQ_SPLITK_WIDE_G
