@@ -207,6 +207,29 @@ def run_cpu_oracle(w, steps, warmup, nseq):
     return step_bytes(ws)["step"] / dt / 1e9, dt, ws
 
 
+def run_cpu_encode(w, ntok=4096):
+    """Times the oracle's K and V encode (as it stands, OpenMP over vectors) on the first ntok tokens of
+    sequence 0, all kv heads; returns (tokens/s, seconds, sample description)."""
+    os.environ.setdefault("OMP_NUM_THREADS", str(cores()))
+    import numpy as np
+
+    import oracle
+    from turboquant_compressed_kv_gb300 import synth
+    d, H = w.head_dim, w.n_kv_heads
+    D, S = synth.rotation_signs(d), synth.qjl_matrix(d)
+    K, V = synth.kv_tokens(w, 0, 0, ntok)
+    nblk = (ntok + 15) // 16
+    kp = np.zeros((nblk, H, oracle.record_bytes(True, d)), np.uint8)
+    vp = np.zeros((nblk, H, oracle.record_bytes(False, d)), np.uint8)
+    slots = np.arange(ntok, dtype=np.int64)
+    oracle.encode(True, D, S, K[:64], slots[:64], kp)     # warm-up (library load)
+    t0 = time.perf_counter()
+    oracle.encode(True, D, S, K, slots, kp)
+    oracle.encode(False, D, S, V, slots, vp)
+    dt = time.perf_counter() - t0
+    return ntok / dt, dt, f"{ntok} tokens x {H} kv heads of sequence 0 (K and V), one timed pass"
+
+
 def bench_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -509,8 +532,9 @@ def extra_hybrid(steps, warmup, dev, history=30720, window=2048):
     return res
 
 
-def extra_encode(steps, warmup, dev):
-    """Bulk encode of the prefill workload (8 x 32768 tokens x 8 kv heads, d=128, bf16) into paged storage."""
+def extra_encode(steps, warmup, dev, cpu=False):
+    """Bulk encode of the prefill workload (8 x 32768 tokens x 8 kv heads, d=128, bf16) into paged storage;
+    with cpu, the oracle's encode rate on the host cores beside it."""
     import torch
 
     import turboquant_compressed_kv_gb300 as tq
@@ -574,6 +598,10 @@ def extra_encode(steps, warmup, dev):
                               "frac": round(vbytes / (vms * 1e-3) / 1e9 / peak, 4), "bytes_per_launch": vbytes}}}
     del K, V, cache
     torch.cuda.empty_cache()
+    if cpu:
+        tps, dt, sample = run_cpu_encode(w)
+        res["cpu_baseline"] = {"value": round(tps / 1e6, 6), "unit": "Mtok/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
+                               "kind": "oracle", "sample": sample, "seconds": round(dt, 3)}
     return res
 
 
@@ -825,7 +853,8 @@ def bench_tq(args):
                              "long256": extra_decode("long256", ksteps, max(3, args.warmup), dev),
                              "verify_q2": extra_verify(ksteps, max(3, args.warmup), dev),
                              "hybrid32k": extra_hybrid(ksteps, max(3, args.warmup), dev),
-                             "prefill_encode": extra_encode(max(3, min(args.steps, 50)), max(3, args.warmup), dev),
+                             "prefill_encode": extra_encode(max(3, min(args.steps, 50)), max(3, args.warmup), dev,
+                                                            cpu=rank == 0 and world == 1 and not args.no_cpu_baseline),
                              "prefill_dequant": extra_dequant(max(3, min(args.steps, 50)), max(3, args.warmup), dev),
                              "gq_compare": extra_gq(max(3, min(args.steps, 100)), max(3, args.warmup), dev)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -134,8 +134,9 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
     for (int i = 0; tile_of(i) < ntiles; ++i) {
         const int buf = i % NX, use = i / NX;
         const int64_t v0 = tile_of(i) * kRows, v = v0 + row;
-        const bool valid = v < n_vec;
-        const int64_t slot = valid ? map.slot(v / map.n_heads, status, (v % map.n_heads) == 0) : -1;
+        // the slot is needed only for the stores: a row past the input or without a slot is
+        // computed on whatever its buffer holds (each row's results depend on that row only)
+        const int64_t slot = v < n_vec ? map.slot(v / map.n_heads, status, (v % map.n_heads) == 0) : -1;
         if (!tc::mbar_wait(&xfull[wg][buf], use & 1)) timed_out = true;
         // ---- 1. the row, in natural coordinate order
         float val[D];
@@ -148,23 +149,19 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
                     const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        val[EPC * c + 2 * q] = valid ? __uint_as_float(w4[q] << 16) : 0.f;
-                        val[EPC * c + 2 * q + 1] = valid ? __uint_as_float(w4[q] & 0xFFFF0000u) : 0.f;
+                        val[EPC * c + 2 * q] = __uint_as_float(w4[q] << 16);
+                        val[EPC * c + 2 * q + 1] = __uint_as_float(w4[q] & 0xFFFF0000u);
                     }
                 } else {
-                    val[EPC * c] = valid ? __uint_as_float(u.x) : 0.f;
-                    val[EPC * c + 1] = valid ? __uint_as_float(u.y) : 0.f;
-                    val[EPC * c + 2] = valid ? __uint_as_float(u.z) : 0.f;
-                    val[EPC * c + 3] = valid ? __uint_as_float(u.w) : 0.f;
+                    val[EPC * c] = __uint_as_float(u.x);
+                    val[EPC * c + 1] = __uint_as_float(u.y);
+                    val[EPC * c + 2] = __uint_as_float(u.z);
+                    val[EPC * c + 3] = __uint_as_float(u.w);
                 }
             }
         }
         tc::named_sync(bar_id, 128);   // every row is read: the buffer takes the tile NX ahead
         if (row < 32 && tile_of(i + NX) < ntiles) issue(i + NX, buf);
-        if (slot < 0) {
-#pragma unroll
-            for (int n = 0; n < D; ++n) val[n] = 0.f;
-        }
         // ---- 2. norm, signs, transform
         float ss = 0.f;
 #pragma unroll
@@ -182,15 +179,19 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
                     val[n | st] = a0 - a1;
                 }
         const float rn = nrm > 0.f ? 1.f / nrm : 0.f;
-        // ---- 3. cells: the three bits of the binary search, into the plane words
+        // ---- 3. cells: the three bits of the binary search on z = val / nrm.  V compares val
+        // with the thresholds times nrm instead (a zero vector keeps the unit thresholds: z = 0 is
+        // cell 4); K needs z itself for the residual.
+        const float ns = (IS_K || nrm == 0.f) ? 1.f : nrm, zs = IS_K ? rn : 1.f;
+        const float T0 = t0 * ns, T1 = t1 * ns, T2 = t2 * ns, T3 = t3 * ns, T4 = t4 * ns, T5 = t5 * ns, T6 = t6 * ns;
         uint32_t w[3][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
         float g2 = 0.f;
 #pragma unroll
         for (int n = 0; n < D; ++n) {
-            const float z = val[n] * rn;
-            const bool b2 = z >= t3;
-            const bool b1 = z >= (b2 ? t5 : t1);
-            const bool b0 = z >= (b2 ? (b1 ? t6 : t4) : (b1 ? t2 : t0));
+            const float z = IS_K ? val[n] * zs : val[n];
+            const bool b2 = z >= T3;
+            const bool b1 = z >= (b2 ? T5 : T1);
+            const bool b0 = z >= (b2 ? (b1 ? T6 : T4) : (b1 ? T2 : T0));
             if (IS_K) {
                 const int tig = (n >> 1) & 3, bit = 8 * ((n >> 3) & 1) + (n >> 4) + 16 * (n & 1);
                 w[0][tig] |= (uint32_t)b0 << bit;
@@ -253,6 +254,8 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
                 float pv[16];
                 tc::ld16(lane_addr + 128 + 16 * j, pv);
                 tc::wait_ld();
+#pragma unroll
+                for (int b = 0; b < 16; ++b) asm volatile("" : "+f"(pv[b]));   // no use moves above the wait
 #pragma unroll
                 for (int b = 0; b < 16; ++b) sgn[j >> 1] |= (pv[b] >= 0.f ? 1u : 0u) << (16 * (j & 1) + b);
             }
