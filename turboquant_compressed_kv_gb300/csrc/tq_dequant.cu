@@ -17,13 +17,13 @@
 //     at d = 128, streamed at d = 256);
 //  3. one warp per slot: codebook values plus the QJL term, the inverse rotation in
 //     registers and shuffles, the norm, and the store.
-// K at d = 128 has a tensor-core path (dequant128k_tc_kernel, below): S^T b for 128 vectors is
-// one 128 x 128 x 128 product.
+// At d = 128 both have one-thread-per-row paths with the rotation in registers (below): K on
+// tcgen05, where S^T b for 128 vectors is one 128 x 128 x 128 product, and V.
 #include "tq_internal.cuh"
 #include "tq_tc.cuh"
 
 #ifndef TQ_DEQUANT_TC
-#define TQ_DEQUANT_TC 1          // K at d = 128 through the tcgen05 path
+#define TQ_DEQUANT_TC 1          // d = 128: K through the tcgen05 path, V through the row-per-thread path
 #endif
 
 namespace tq {
@@ -372,6 +372,155 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
 }
 
+// ---------------------------------------------------------------- V at d = 128, one thread per row
+// A CTA of 128 threads walks tiles of 8 records (128 rows); thread r owns row r:
+//  1. the tile's records arrive by bulk copy, two tiles in flight;
+//  2. the row's cells are read back plane word by plane word (each V word holds 8 coordinates of
+//     four slots; the slot's bits are pre-shifted once), y = c[cell] / sqrt d;
+//  3. the 128-point inverse transform in registers, the norm and D, and 16-byte stores.
+namespace dq128v {
+constexpr int D = 128, kRows = 128, kUnits = kRows / kBlock, kThreads = 128, kMinCtas = 3;
+constexpr int kRec = (int)v_record(D);
+constexpr int kSmem = 2 * kUnits * kRec;
+}  // namespace dq128v
+
+template <typename TO>
+__global__ void __launch_bounds__(dq128v::kThreads, dq128v::kMinCtas)
+dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ pool, int64_t num_blocks,
+                        int n_heads, const int32_t *__restrict__ block_ids, int n_ids, TO *__restrict__ out,
+                        int32_t *status) {
+    using namespace dq128v;
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ uint64_t recbar[2];
+    __shared__ float s_cent[8], s_D[D];
+    const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
+    if (ph->magic != kParamsMagic || ph->d != D) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
+        return;
+    }
+    const int row = threadIdx.x;
+    const int64_t units = (int64_t)n_ids * n_heads, ntiles = (units + kUnits - 1) / kUnits;
+    if ((int64_t)blockIdx.x >= ntiles) return;
+    if (row == 0) {
+        tc::mbar_init(&recbar[0], 1);
+        tc::mbar_init(&recbar[1], 1);
+    }
+    const float inv_sd = rsqrtf((float)D);
+    if (row < 8) s_cent[row] = ph->centroid[row] * inv_sd;
+    s_D[row] = reinterpret_cast<const float *>(params + params_off_D(D))[row];
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    bool timed_out = false;
+    auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)i * gridDim.x; };
+    auto issue = [&](int i, int buf) {   // one thread: the tile's records into buffer buf
+        const int64_t tile = tile_of(i);
+        uint32_t bytes = 0;
+        for (int k = 0; k < kUnits; ++k)
+            if (tile * kUnits + k < units) bytes += kRec;
+        tc::mbar_arrive_expect_tx(&recbar[buf], bytes);
+        for (int k = 0; k < kUnits; ++k) {
+            const int64_t u = tile * kUnits + k;
+            if (u >= units) break;
+            const int64_t blk = block_ids[u / n_heads];
+            const int64_t bc = (blk >= 0 && blk < num_blocks) ? blk : 0;   // a bad id reads block 0, output zeroed
+            tc::bulk_g2s(smem + (buf * kUnits + k) * kRec, pool + ((size_t)bc * n_heads + (u % n_heads)) * kRec, kRec,
+                         &recbar[buf]);
+        }
+    };
+    if (row == 0) {
+        if (tile_of(0) < ntiles) issue(0, 0);
+        if (tile_of(1) < ntiles) issue(1, 1);
+    }
+
+#pragma unroll 1
+    for (int i = 0; tile_of(i) < ntiles; ++i) {
+        const int64_t tile = tile_of(i);
+        const int buf = i & 1;
+        if (!tc::mbar_wait(&recbar[buf], (i >> 1) & 1)) timed_out = true;
+        const int unit_k = row >> 4, t = row & 15;
+        const int64_t u = tile * kUnits + unit_k;
+        const bool live = u < units;
+        const int64_t blk = live ? block_ids[u / n_heads] : -1;
+        const bool good = live && blk >= 0 && blk < num_blocks;
+        if (live && !good && t == 0) flag_status(status, TQ_STATUS_BAD_SLOT);
+        const uint8_t *rec = smem + (buf * kUnits + unit_k) * kRec;
+        const uint32_t *planes = reinterpret_cast<const uint32_t *>(rec);
+        // coordinate n = 16 mt + r of slot t: word 2 (4 (r & 7) + (t & 7) / 2) + (r >> 3) of each
+        // plane, bit 8 (t >> 3) + 16 (t & 1) + mt
+        constexpr int PW = 2 * D / 4;   // words per plane
+        const int a = (t & 7) >> 1, sh = 8 * (t >> 3) + 16 * (t & 1);
+        float y[D];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int word = 2 * (4 * c + a) + h;
+                const uint32_t w0 = planes[word] >> sh, w1 = planes[PW + word] >> sh, w2 = planes[2 * PW + word] >> sh;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    const uint32_t cell = ((w0 >> mt) & 1u) | (((w1 >> mt) & 1u) << 1) | (((w2 >> mt) & 1u) << 2);
+                    y[16 * mt + 8 * h + c] = s_cent[cell];
+                }
+            }
+        const __half nh = *reinterpret_cast<const __half *>(rec + 6 * D + 2 * t);
+        tc::fence_async_smem();
+        __syncthreads();   // every row of the buffer is read: it can take the tile two ahead
+        if (row == 0 && tile_of(i + 2) < ntiles) issue(i + 2, buf);
+        // inverse rotation: D (H y) / sqrt d, then the norm
+#pragma unroll
+        for (int st = 1; st < D; st <<= 1)
+#pragma unroll
+            for (int n = 0; n < D; ++n)
+                if ((n & st) == 0) {
+                    const float a0 = y[n], a1 = y[n | st];
+                    y[n] = a0 + a1;
+                    y[n | st] = a0 - a1;
+                }
+        const float sc = good ? __half2float(nh) * inv_sd : 0.f;
+        if (live) {
+            TO *orow = out + (((size_t)(u / n_heads) * kBlock + t) * n_heads + (u % n_heads)) * D;
+#pragma unroll
+            for (int n = 0; n < D; n += 8) {
+                float o8[8];
+#pragma unroll
+                for (int x = 0; x < 8; ++x) o8[x] = y[n + x] * sc * s_D[n + x];
+                if constexpr (sizeof(TO) == 4) {
+                    *reinterpret_cast<float4 *>(orow + n) = make_float4(o8[0], o8[1], o8[2], o8[3]);
+                    *reinterpret_cast<float4 *>(orow + n + 4) = make_float4(o8[4], o8[5], o8[6], o8[7]);
+                } else {
+                    uint4 v;
+                    uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(o8[2 * x], o8[2 * x + 1]);
+                        vw[x] = *reinterpret_cast<const uint32_t *>(&b2);
+                    }
+                    *reinterpret_cast<uint4 *>(orow + n) = v;
+                }
+            }
+        }
+    }
+    if (timed_out) flag_status(status, TQ_STATUS_TIMEOUT);
+}
+
+template <typename TO>
+cudaError_t dq128v_launch(const void *params, const void *pool, int64_t num_blocks, int n_heads, const int32_t *ids,
+                          int n_ids, void *out, int32_t *status, cudaStream_t st) {
+    const int64_t ntiles = ((int64_t)n_ids * n_heads + dq128v::kUnits - 1) / dq128v::kUnits;
+    if (ntiles <= 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    auto kern = dequant128v_rows_kernel<TO>;
+    const int64_t want = (int64_t)sms * dq128v::kMinCtas;
+    const int64_t grid = ntiles < want ? ntiles : want;
+    kern<<<(unsigned)grid, dq128v::kThreads, dq128v::kSmem, st>>>((const uint8_t *)params, (const uint8_t *)pool,
+                                                                num_blocks, n_heads, ids, n_ids, (TO *)out, status);
+    return cudaGetLastError();
+}
+
 template <typename TO>
 cudaError_t dq128k_launch(const void *params, const void *pool, int64_t num_blocks, int n_heads, const int32_t *ids,
                           int n_ids, void *out, int32_t *status, cudaStream_t st) {
@@ -417,6 +566,10 @@ cudaError_t launch_dequant(bool is_k, int d, int out_dtype, const void *params, 
         return out_dtype == TQ_DTYPE_BF16
                    ? dq128k_launch<__nv_bfloat16>(params, pool, num_blocks, n_heads, block_ids, n_ids, out, status, st)
                    : dq128k_launch<float>(params, pool, num_blocks, n_heads, block_ids, n_ids, out, status, st);
+    if (d == 128 && !is_k && TQ_DEQUANT_TC)
+        return out_dtype == TQ_DTYPE_BF16
+                   ? dq128v_launch<__nv_bfloat16>(params, pool, num_blocks, n_heads, block_ids, n_ids, out, status, st)
+                   : dq128v_launch<float>(params, pool, num_blocks, n_heads, block_ids, n_ids, out, status, st);
     if (d == 128)
         return out_dtype == TQ_DTYPE_BF16
                    ? dq_launch<128, __nv_bfloat16>(params, pool, num_blocks, n_heads, block_ids, n_ids, is_k, out,

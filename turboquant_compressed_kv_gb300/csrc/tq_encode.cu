@@ -56,13 +56,18 @@ template <typename T> __host__ __device__ constexpr int row_bytes() { return D *
 template <typename T> __host__ __device__ constexpr int row_stride() { return row_bytes<T>() + 16; }
 template <typename T> __host__ __device__ constexpr int xbuf_bytes() { return kRows * row_stride<T>(); }
 template <bool K> __host__ __device__ constexpr int oX() { return K ? 65536 : 0; }          // after S hi / lo
+// K: one CTA of 2 warpgroups per SM (tensor memory, S in shared memory); V: CTAs of one warpgroup,
+// 3 per SM (no tensor memory: fewer registers and more warps per SM)
+template <bool K> __host__ __device__ constexpr int n_wg() { return K ? 2 : 1; }
+template <bool K> __host__ __device__ constexpr int n_threads() { return 128 * n_wg<K>(); }
+template <bool K> __host__ __device__ constexpr int ctas_per_sm() { return K ? 1 : 3; }
 template <typename T, bool K> __host__ __device__ constexpr int smem_bytes() {
-    return oX<K>() + 2 * nx<T>() * xbuf_bytes<T>();
+    return oX<K>() + n_wg<K>() * nx<T>() * xbuf_bytes<T>();
 }
 }  // namespace encr
 
 template <typename T, bool IS_K>
-__global__ void __launch_bounds__(encr::kThreads, 1)
+__global__ void __launch_bounds__(encr::n_threads<IS_K>(), encr::ctas_per_sm<IS_K>())
 encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ x, int64_t n_vec, SlotMap map,
                       uint8_t *__restrict__ pool, int32_t *status) {
     using namespace encr;
@@ -90,7 +95,7 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
     if (tid < D) s_D[tid] = reinterpret_cast<const float *>(params + params_off_D(D))[tid];
     if (IS_K) {   // B row n = S row sigma(n), sigma(32 tig + b) = 16 (b & 7) + 8 ((b >> 3) & 1) + 2 tig + (b >> 4)
         const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
-        for (int e = tid; e < D * D; e += kThreads) {
+        for (int e = tid; e < D * D; e += n_threads<IS_K>()) {
             const int n = e >> 7, k = e & 127;
             const int tig = n >> 5, b = n & 31;
             const int sr = 16 * (b & 7) + 8 * ((b >> 3) & 1) + 2 * tig + (b >> 4);
@@ -115,7 +120,7 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
     const float inv_sd = rsqrtf((float)D);
     bool timed_out = false;
 
-    auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)(2 * i + wg) * gridDim.x; };
+    auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)(n_wg<IS_K>() * i + wg) * gridDim.x; };
     // the first warp of the warpgroup: the tile's rows, one bulk copy per row, spread over its lanes
     auto issue = [&](int i, int buf) {
         const int64_t v0 = tile_of(i) * kRows;
@@ -316,8 +321,10 @@ cudaError_t launch_encr(const void *params, const void *x, int64_t n_vec, const 
     auto kern = encode128_rows_kernel<T, IS_K>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(ntiles < sms ? ntiles : sms);
-    kern<<<grid, encr::kThreads, smem, st>>>((const uint8_t *)params, (const T *)x, n_vec, map, (uint8_t *)pool, status);
+    const int64_t want = (int64_t)sms * encr::ctas_per_sm<IS_K>();
+    const unsigned grid = (unsigned)(ntiles < want ? ntiles : want);
+    kern<<<grid, encr::n_threads<IS_K>(), smem, st>>>((const uint8_t *)params, (const T *)x, n_vec, map,
+                                                      (uint8_t *)pool, status);
     return cudaGetLastError();
 }
 
