@@ -158,7 +158,7 @@ dequant_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ p
 }
 
 // ---------------------------------------------------------------- K at d = 128 on tcgen05
-// Two warpgroups take alternate tiles of 128 rows (8 records x 16 slots); thread r of a
+// kWg warpgroups take alternate tiles of 128 rows (8 records x 16 slots); thread r of a
 // warpgroup owns row r:
 //  1. the tile's records arrive by bulk copy (two tiles in flight per warpgroup);
 //  2. the row's 128 sign bits become the A operand (f16 +-1, 128-byte swizzle) with one shift
@@ -169,12 +169,15 @@ dequant_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ p
 //  4. the thread reads its row back (tcgen05.ld), adds the codebook values, runs the 128-point
 //     inverse transform in registers, and stores the row.
 namespace dq128 {
-constexpr int D = 128, kRows = 128, kUnits = kRows / kBlock, kThreads = 256;
+#ifndef TQ_DQ128K_WG
+#define TQ_DQ128K_WG 2           // warpgroups per CTA (they share S in shared memory; 3 measured slower)
+#endif
+constexpr int D = 128, kRows = 128, kUnits = kRows / kBlock, kWg = TQ_DQ128K_WG, kThreads = 128 * kWg;
 constexpr int kRec = (int)k_record(D);
 constexpr int oB = 0;          // S hi, S lo: 2 x 32 KB
-constexpr int oA = 65536;      // A operand of each warpgroup: 2 x 32 KB
-constexpr int oR = 131072;     // records: [warpgroup][buffer][unit][kRec]
-constexpr int kSmem = oR + 2 * 2 * kUnits * kRec;
+constexpr int oA = 65536;      // A operand of each warpgroup: kWg x 32 KB
+constexpr int oR = oA + kWg * 32768;   // records: [warpgroup][buffer][unit][kRec]
+constexpr int kSmem = oR + kWg * 2 * kUnits * kRec;
 }  // namespace dq128
 
 template <typename TO>
@@ -184,7 +187,7 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
                       int32_t *status) {
     using namespace dq128;
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ uint64_t recbar[2][2], mmabar[2];
+    __shared__ uint64_t recbar[kWg][2], mmabar[kWg];
     __shared__ uint32_t tmem_base;
     __shared__ float s_cent[8], s_D[D];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
@@ -196,13 +199,14 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     const int64_t units = (int64_t)n_ids * n_heads, ntiles = (units + kUnits - 1) / kUnits;
     if ((int64_t)blockIdx.x >= ntiles) return;
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kWg; ++i) {
             tc::mbar_init(&recbar[i][0], 1);
             tc::mbar_init(&recbar[i][1], 1);
             tc::mbar_init(&mmabar[i], 1);
         }
     }
-    if (warp == 0) tc::tmem_alloc(&tmem_base, 256);
+    constexpr uint32_t kTmemCols = kWg <= 2 ? 256 : 512;   // 128 columns per warpgroup, a power of two
+    if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
     if (tid < 8) s_cent[tid] = ph->centroid[tid];
     if (tid < D) s_D[tid] = reinterpret_cast<const float *>(params + params_off_D(D))[tid];
     {   // B: row n = output coordinate n, K index k' as in the A operand; S as f16 hi + lo
@@ -229,7 +233,7 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     bool timed_out = false;
 
     // tiles of this warpgroup: blockIdx.x + (2 i + wg) * gridDim.x
-    auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)(2 * i + wg) * gridDim.x; };
+    auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)(kWg * i + wg) * gridDim.x; };
     auto issue = [&](int i, int buf) {   // one thread: the tile's records into buffer buf
         const int64_t tile = tile_of(i);
         uint32_t bytes = 0;
@@ -369,7 +373,7 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     if (timed_out) flag_status(status, TQ_STATUS_TIMEOUT);
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem_base, 256);
+    if (warp == 0) tc::tmem_dealloc(tmem_base, kTmemCols);
 }
 
 // ---------------------------------------------------------------- V at d = 128, one thread per row
