@@ -295,6 +295,45 @@ def test_decode_step_appends_then_attends(d, Hq, Hkv, dtype):
     parity.check_attention(o, ref)
 
 
+@pytest.mark.parametrize("d,Hq,Hkv", [(128, 32, 8), (256, 16, 8)])
+def test_decode_step_in_a_cuda_graph(d, Hq, Hkv):
+    """The step captured once in a CUDA graph (both launches, the pass as a programmatic dependent
+    of the prep) and replayed: each replay equals a direct tq_decode_step bit for bit, and the
+    appended records are the same."""
+    lens = [1000, 17, 4095, 250]   # none a multiple of 16: the new token lands in the sequence's own last block
+    D, S, params, bt, kp, vp = _build_cache(d, Hkv, lens, "bf16", seed=31)
+    B = len(lens)
+    rng = np.random.default_rng(37)
+    dbt = torch.from_numpy(bt).to(DEV)
+    pre = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    max_ctx = max(lens) + 1
+    ws = torch.empty(tq.decode_workspace_bytes(d, B, Hq, max_ctx), dtype=torch.uint8, device=DEV)
+    q = torch.empty((B, Hq, d), dtype=torch.bfloat16, device=DEV)
+    k_new = torch.empty((B, Hkv, d), dtype=torch.bfloat16, device=DEV)
+    v_new = torch.empty_like(k_new)
+    kp_g, vp_g = torch.from_numpy(kp).to(DEV), torch.from_numpy(vp).to(DEV)
+    out_g = torch.empty((B, Hq, d), dtype=torch.float32, device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):   # warm-up call (attribute setup) outside the capture
+        tq.decode_step(params, d, k_new.zero_(), v_new.zero_(), q.zero_(), Hkv, kp_g.clone(), vp_g.clone(), dbt,
+                       pre, max_ctx, out=out_g, workspace=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        tq.decode_step(params, d, k_new, v_new, q, Hkv, kp_g, vp_g, dbt, pre, max_ctx, out=out_g, workspace=ws)
+    for rep in range(3):
+        q.copy_(torch.from_numpy(rng.standard_normal((B, Hq, d)).astype(np.float32)).to(torch.bfloat16))
+        k_new.copy_(torch.from_numpy(rng.standard_normal((B, Hkv, d)).astype(np.float32)).to(torch.bfloat16))
+        v_new.copy_(torch.from_numpy(rng.standard_normal((B, Hkv, d)).astype(np.float32)).to(torch.bfloat16))
+        kp_d, vp_d = kp_g.clone(), vp_g.clone()
+        torch.cuda.synchronize()
+        g.replay()
+        want = tq.decode_step(params, d, k_new, v_new, q, Hkv, kp_d, vp_d, dbt, pre, max_ctx)
+        torch.cuda.synchronize()
+        assert torch.equal(out_g, want), f"replay {rep}"
+        assert torch.equal(kp_g, kp_d) and torch.equal(vp_g, vp_d)
+
+
 @pytest.mark.parametrize("d,Hq,Hkv,Q", [(128, 8, 2, 2), (128, 4, 2, 4), (128, 3, 3, 3), (128, 2, 2, 8),
                                          (256, 4, 2, 2), (256, 1, 1, 5)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
