@@ -56,6 +56,10 @@ qprep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ q, int ba
              unsigned int *__restrict__ counters, int64_t *__restrict__ cpre, int32_t *__restrict__ cta_b) {
     extern __shared__ __align__(16) uint8_t qsm[];
     pdl_launch_dependents();
+    if (blockIdx.x == gridDim.x - 1) {   // the last CTA lays out the pass's work
+        build_schedule(ctx_lens, 0, batch, hkv, max_ctx, chunk, P, cpre, cta_b);
+        return;
+    }
     qprep_rows<D, NTK, T>(params, q, batch, q_len, hq, hkv, ctx_lens, 0, max_ctx, chunk, P, packs, counters, cpre, cta_b,
                           blockIdx.x, qsm);
 }
@@ -600,7 +604,7 @@ cudaError_t qprep_launch_t(const uint8_t *P, const void *q, int batch, int q_len
     auto kern = qprep_kernel<D, NTK, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<(batch * q_len * hq + kQRows - 1) / kQRows, 128, smem, st>>>(P, (const T *)q, batch, q_len, hq, hkv, ctx_lens,
+    kern<<<(batch * q_len * hq + kQRows - 1) / kQRows + 1, 128, smem, st>>>(P, (const T *)q, batch, q_len, hq, hkv, ctx_lens,
                                                                        max_ctx, pass_chunk(q_len * hq / hkv), nctas,
                                                                        w.packs, w.counters, w.cpre, w.cta_b);
     return cudaGetLastError();
@@ -706,6 +710,8 @@ step_prep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ k_new
         encode_tiles<D, kAppendTile, T>(params, is_k ? k_new : v_new, (int64_t)batch * q_len * hkv, map,
                                         is_k ? k_pool : v_pool, is_k, is_k, is_k ? blk : blk - n_app, n_app, smem,
                                         status);
+    } else if (blk == gridDim.x - 1) {   // the last CTA lays out the pass's work
+        build_schedule(map.ctx_lens, q_len, batch, hkv, max_ctx, chunk, P, cpre, cta_b);
     } else {
         qprep_rows<D, NTK, T>(params, q, batch, q_len, hq, hkv, map.ctx_lens, q_len, max_ctx, chunk, P, packs, counters, cpre,
                               cta_b, blk - 2 * n_app, smem);
@@ -723,7 +729,7 @@ cudaError_t step_prep_launch(const uint8_t *P, const void *k_new, const void *v_
     if (e != cudaSuccess) return e;
     const int n_app = (batch * q_len * hkv + kAppendTile - 1) / kAppendTile;
     const int n_q = (batch * q_len * hq + kQRows - 1) / kQRows;
-    kern<<<2 * n_app + n_q, 128, smem, st>>>(P, (const T *)k_new, (const T *)v_new, (const T *)q, batch, q_len, hq,
+    kern<<<2 * n_app + n_q + 1, 128, smem, st>>>(P, (const T *)k_new, (const T *)v_new, (const T *)q, batch, q_len, hq,
                                              hkv, map, (uint8_t *)kp, (uint8_t *)vp, n_app, max_ctx,
                                              pass_chunk(q_len * hq / hkv), nctas, w.packs, w.counters, w.cpre, w.cta_b,
                                              status);

@@ -72,10 +72,8 @@ __device__ __forceinline__ void encode_tiles(const uint8_t *__restrict__ params,
     __shared__ float s_cent[8], s_thr[8];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     const float *gST = reinterpret_cast<const float *>(params + params_off_ST(D));
-    if (is_k && SM::kResident) stage_st_rows<D, kEncWarps * 32>(sST, gST, 0, D);   // waited before first use
     if (ph->magic != kParamsMagic || ph->d != D) {
         if (threadIdx.x == 0 && blk == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
-        cp_async_wait_all();
         return;
     }
     if (threadIdx.x < 8) {
@@ -105,13 +103,14 @@ __device__ __forceinline__ void encode_tiles(const uint8_t *__restrict__ params,
                 dims[r] = is_k ? kdim<D>(lane, r) : vdim<D>(lane, r);
                 val[r] = (v < n_vec) ? to_f32<T>(x[v * D + dims[r]]) : 0.f;
             }
+            // the slot (block-table lookups) is needed only by the stores: a vector without one is
+            // encoded from whatever it holds and not stored, so nothing here waits for the lookup
             slot[j] = -1;
             if (v < n_vec)   // a bad slot is reported once per token
                 slot[j] = map.slot(v / map.n_heads, status, report_bad && lane == 0 && (v % map.n_heads) == 0);
-            if (slot[j] < 0) {
-#pragma unroll
-                for (int r = 0; r < R; ++r) val[r] = 0.f;
-            }
+            // S^T (64 KB at d = 128) is copied once, after the first rows are requested, so that
+            // those small loads are not queued behind it; it is waited for before the projection
+            if (is_k && SM::kResident && j == 0 && tile == blk) stage_st_rows<D, kEncWarps * 32>(sST, gST, 0, D);
             float ss = 0.f;
 #pragma unroll
             for (int r = 0; r < R; ++r) ss = fmaf(val[r], val[r], ss);
@@ -273,7 +272,8 @@ __host__ __device__ constexpr int kPackFloatOff(int d) { return 16 * d; }   // i
 // two 64-row chunks in flight at d=256), then each warp writes its row's hi
 // and lo columns (2*hg, 2*hg+1) of the K-side B operand for qbar (qu=0) and
 // u (qu=1) into the pack of the row's (sequence, kv head), and the offset
-// constants.  CTA 0 also lays out the pass's work (build_schedule).
+// constants.  The pass's work schedule (build_schedule) is laid out by a CTA of its own, in
+// parallel with the rows.
 constexpr int kQRows = 4;
 template <int D> __host__ __device__ constexpr int qprep_st_rows() { return D == 128 ? 128 : 64; }
 template <int D> __host__ __device__ constexpr size_t qprep_smem() {
@@ -282,8 +282,8 @@ template <int D> __host__ __device__ constexpr size_t qprep_smem() {
 
 
 // Rows 4*blk .. 4*blk+3 of the query prep, one CTA of 128 threads; `qsm` holds
-// qprep_smem<D>() bytes.  Block 0 also builds the pass's work schedule; ctx_add is added to
-// every non-negative length (the number of tokens the step appends first).  With q_len > 1
+// qprep_smem<D>() bytes.  ctx_add is added to every non-negative length (the number of tokens the
+// step appends first).  With q_len > 1
 // queries per sequence (q[b][i][h]), query i of head hg of a kv head is operand column
 // i * G + hg of the kv head's pack.
 template <int D, int NTK, typename T>
@@ -302,13 +302,15 @@ __device__ __forceinline__ void qprep_rows(const uint8_t *__restrict__ params, c
     const float *ST = reinterpret_cast<const float *>(params + params_off_ST(D));
     const float inv_sd = rsqrtf((float)D);
     constexpr bool kOneCopy = qprep_st_rows<D>() == D;
-    if constexpr (kOneCopy) stage_st_rows<D, 128>(sbuf, ST, 0, D);   // in flight while the rows rotate
     {
         const int row = row0 + warp;
         float v[R];
 #pragma unroll
         for (int r = 0; r < R; ++r)
             v[r] = (row < nrows) ? to_f32<T>(q[(size_t)row * D + 32 * r + lane]) * __ldg(Dsign + 32 * r + lane) : 0.f;
+        // S^T (64 KB at d = 128) is requested after the rows, so they are not queued behind it; it
+        // arrives while the rows rotate
+        if constexpr (kOneCopy) stage_st_rows<D, 128>(sbuf, ST, 0, D);
         fwht_warp<R>(v, lane);
 #pragma unroll
         for (int r = 0; r < R; ++r) qs[warp][32 * r + lane] = v[r] * inv_sd;   // qbar = H D q / sqrt d
@@ -380,7 +382,6 @@ __device__ __forceinline__ void qprep_rows(const uint8_t *__restrict__ params, c
             }
         }
     }
-    if (blk == 0) build_schedule(ctx_lens, ctx_add, batch, hkv, max_ctx, chunk, P, cpre, cta_b);
 }
 
 
