@@ -21,6 +21,10 @@
 #include "tq_tc.cuh"
 #include "tq_prep.cuh"
 
+#ifndef TQ_ENC_SPLIT
+#define TQ_ENC_SPLIT 1           // bulk K at d = 128: two threads per row (encode128k_split_kernel)
+#endif
+
 namespace tq {
 namespace {
 
@@ -308,6 +312,281 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
     }
 }
 
+// ---------------------------------------------------------------- K at d = 128, two threads per row
+// As encode128_rows_kernel for K, with each row split over two threads (halves h = 0, 1), so that
+// a thread holds 64 coordinates and an SM runs 16 warps:
+//  * the transform's stage on index bit 6 is taken first, on the input: half h holds
+//    u_m = (D x)_m + (-1)^h (D x)_{m+64} (m < 64) and finishes the 64-point transform in
+//    registers; its outputs are coordinates 64 h + m (the stages of the transform commute);
+//  * each half reads the whole row (the norm and that first stage need it);
+//  * a plane word holds bits of both halves (half h owns bits n >> 4 = 4h .. 4h + 3 of each byte):
+//    half 1 leaves its partial words and its residual sum in shared memory, half 0 merges and
+//    stores them; accumulator columns 64 h .. 64 h + 63 are sign words 2h, 2h + 1, stored by half h.
+// Two tile groups of 256 threads take alternate tiles of 128 rows.
+namespace encs {
+constexpr int D = 128, kRows = 128, kTg = 2, kThreads = 256 * kTg;
+template <typename T> __host__ __device__ constexpr int nx() { return sizeof(T) == 2 ? 2 : 1; }
+template <typename T> __host__ __device__ constexpr int row_bytes() { return D * (int)sizeof(T); }
+template <typename T> __host__ __device__ constexpr int row_stride() { return row_bytes<T>() + 16; }
+template <typename T> __host__ __device__ constexpr int xbuf_bytes() { return kRows * row_stride<T>(); }
+constexpr int oX = 65536;   // after S hi / lo
+template <typename T> __host__ __device__ constexpr int oW() { return oX + kTg * nx<T>() * xbuf_bytes<T>(); }
+constexpr int kWStride = 15;   // per row: 12 partial plane words, the residual sum of squares, two norm shares
+template <typename T> __host__ __device__ constexpr int smem_bytes() { return oW<T>() + kTg * kRows * kWStride * 4; }
+}  // namespace encs
+
+template <typename T>
+__global__ void __launch_bounds__(encs::kThreads, 1)
+encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict__ x, int64_t n_vec, SlotMap map,
+                        uint8_t *__restrict__ pool, int32_t *status) {
+    using namespace encs;
+    constexpr int NX = nx<T>(), RS = row_stride<T>(), RB = row_bytes<T>(), EPC = 16 / (int)sizeof(T);
+    constexpr int HC = RB / 32;   // 16-byte chunks per half row
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ uint64_t xfull[kTg][2], mmabar[kTg];
+    __shared__ uint32_t tmem_base;
+    __shared__ float s_D[D];
+    const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
+    if (ph->magic != kParamsMagic || ph->d != D) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
+        return;
+    }
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tg = (warp >> 2) & 1, h = warp >> 3, sl = warp & 3, row = 32 * sl + lane;
+    const int64_t ntiles = (n_vec + kRows - 1) / kRows;
+    if ((int64_t)blockIdx.x >= ntiles) return;
+    if (tid == 0) {
+        for (int i = 0; i < kTg; ++i) {
+            tc::mbar_init(&xfull[i][0], 1);
+            tc::mbar_init(&xfull[i][1], 1);
+            tc::mbar_init(&mmabar[i], 1);
+        }
+    }
+    if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
+    if (tid < D) s_D[tid] = reinterpret_cast<const float *>(params + params_off_D(D))[tid];
+    {   // B row n = S row sigma(n), sigma(32 tig + b) = 16 (b & 7) + 8 ((b >> 3) & 1) + 2 tig + (b >> 4)
+        const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
+        for (int e = tid; e < D * D; e += kThreads) {
+            const int n = e >> 7, k = e & 127;
+            const int tig = n >> 5, b = n & 31;
+            const int sr = 16 * (b & 7) + 8 * ((b >> 3) & 1) + 2 * tig + (b >> 4);
+            const float sv = __ldg(S + sr * D + k);
+            const __half hi = __float2half_rn(sv);
+            const __half lo = __float2half_rn(sv - __half2float(hi));
+            const int off = tc::sw128_off(n, k, D);
+            *reinterpret_cast<__half *>(smem + off) = hi;
+            *reinterpret_cast<__half *>(smem + 32768 + off) = lo;
+        }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base + 256u * tg;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * sl) << 16);
+    const float t0 = ph->threshold[0], t1 = ph->threshold[1], t2 = ph->threshold[2], t3 = ph->threshold[3];
+    const float t4 = ph->threshold[4], t5 = ph->threshold[5], t6 = ph->threshold[6];
+    float cen[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) cen[k] = ph->centroid[k];
+    const float inv_sd = rsqrtf((float)D);
+    const float hs = h ? -1.f : 1.f;
+    uint32_t *sW = reinterpret_cast<uint32_t *>(smem + oW<T>()) + ((size_t)tg * kRows + row) * kWStride;
+    bool timed_out = false;
+    const int bar_id = 1 + tg;
+    const bool issuer = warp == 4 * tg;   // the tile group's first warp moves its rows
+
+    auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)(kTg * i + tg) * gridDim.x; };
+    auto issue = [&](int i, int buf) {   // the issuing warp: one bulk copy per row, spread over its lanes
+        const int64_t v0 = tile_of(i) * kRows;
+        const int rows = (int)min((int64_t)kRows, n_vec - v0);
+        uint8_t *dst = smem + oX + (tg * NX + buf) * xbuf_bytes<T>();
+        if (lane == 0) tc::mbar_arrive_expect_tx(&xfull[tg][buf], (uint32_t)rows * RB);
+        __syncwarp();
+        for (int r = lane; r < rows; r += 32) tc::bulk_g2s(dst + r * RS, x + (v0 + r) * D, RB, &xfull[tg][buf]);
+    };
+    if (issuer)
+        for (int b2 = 0; b2 < NX; ++b2)
+            if (tile_of(b2) < ntiles) issue(b2, b2);
+
+#pragma unroll 1
+    for (int i = 0; tile_of(i) < ntiles; ++i) {
+        const int buf = i % NX, use = i / NX;
+        const int64_t v0 = tile_of(i) * kRows, v = v0 + row;
+        const int64_t slot = v < n_vec ? map.slot(v / map.n_heads, status, h == 0 && (v % map.n_heads) == 0) : -1;
+        if (!tc::mbar_wait(&xfull[tg][buf], use & 1)) timed_out = true;
+        // ---- 1. the whole row: norm, signs D, and the transform stage on index bit 6
+        float u[64];
+        float ss = 0.f;
+        {
+            const uint8_t *xr = smem + oX + (tg * NX + buf) * xbuf_bytes<T>() + row * RS;
+#pragma unroll
+            for (int c = 0; c < HC; ++c) {
+                const uint4 ua = *reinterpret_cast<const uint4 *>(xr + 16 * c);
+                const uint4 ub = *reinterpret_cast<const uint4 *>(xr + 16 * (c + HC));
+                float a[EPC], b[EPC];
+                if constexpr (sizeof(T) == 2) {
+                    const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        a[2 * q] = __uint_as_float(wa[q] << 16);
+                        a[2 * q + 1] = __uint_as_float(wa[q] & 0xFFFF0000u);
+                        b[2 * q] = __uint_as_float(wb[q] << 16);
+                        b[2 * q + 1] = __uint_as_float(wb[q] & 0xFFFF0000u);
+                    }
+                } else {
+                    a[0] = __uint_as_float(ua.x); a[1] = __uint_as_float(ua.y);
+                    a[2] = __uint_as_float(ua.z); a[3] = __uint_as_float(ua.w);
+                    b[0] = __uint_as_float(ub.x); b[1] = __uint_as_float(ub.y);
+                    b[2] = __uint_as_float(ub.z); b[3] = __uint_as_float(ub.w);
+                }
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) {
+                    const int m = EPC * c + e;
+                    ss = fmaf(h ? b[e] : a[e], h ? b[e] : a[e], ss);   // this half's share of the norm
+                    u[m] = fmaf(hs, b[e] * s_D[m + 64], a[e] * s_D[m]);
+                }
+            }
+        }
+        float *sSS = reinterpret_cast<float *>(sW) + 13;   // the halves' norm shares (words 13, 14)
+        sSS[1 - h] = ss;
+        tc::named_sync(bar_id, 256);   // every row is read: the buffer takes the tile NX ahead
+        if (issuer && tile_of(i + NX) < ntiles) issue(i + NX, buf);
+        const float nrm = sqrtf(ss + sSS[h]);   // the same sum in both halves (addition commutes)
+        // ---- 2. the 64-point transform of this half (index bits 0..5)
+#pragma unroll
+        for (int st = 1; st < 64; st <<= 1)
+#pragma unroll
+            for (int m = 0; m < 64; ++m)
+                if ((m & st) == 0) {
+                    const float a0 = u[m], a1 = u[m | st];
+                    u[m] = a0 + a1;
+                    u[m | st] = a0 - a1;
+                }
+        const float rn = nrm > 0.f ? 1.f / nrm : 0.f;
+        // ---- 3. cells of coordinates 64 h + m, residual
+        uint32_t w[3][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
+        float g2 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 64; ++m) {
+            const float z = u[m] * rn;
+            const bool b2 = z >= t3;
+            const bool b1 = z >= (b2 ? t5 : t1);
+            const bool b0 = z >= (b2 ? (b1 ? t6 : t4) : (b1 ? t2 : t0));
+            const int tig = (m >> 1) & 3, bit = 8 * ((m >> 3) & 1) + (m >> 4) + 16 * (m & 1);   // + 4 h below
+            w[0][tig] |= (uint32_t)b0 << bit;
+            w[1][tig] |= (uint32_t)b1 << bit;
+            w[2][tig] |= (uint32_t)b2 << bit;
+            const float c = b2 ? (b1 ? (b0 ? cen[7] : cen[6]) : (b0 ? cen[5] : cen[4]))
+                               : (b1 ? (b0 ? cen[3] : cen[2]) : (b0 ? cen[1] : cen[0]));
+            const float rho = z - c;
+            g2 = fmaf(rho, rho, g2);
+            u[m] = rho * 256.f;   // exact scaling; keeps the f16 low parts out of the subnormals
+        }
+        // ---- 4. rho (x 256) as f16 hi / lo into this row's lane: K elements 64 h .. 64 h + 63
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {   // 16 columns at a time (fewer live registers)
+            float hw[16], lw[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const float a0 = u[32 * q + 2 * c], a1 = u[32 * q + 2 * c + 1];
+                const __half2 hh = __floats2half2_rn(a0, a1);
+                const float2 hf = __half22float2(hh);
+                const __half2 ll = __floats2half2_rn(a0 - hf.x, a1 - hf.y);
+                hw[c] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&hh));
+                lw[c] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&ll));
+            }
+            tc::st16(lane_addr + 32 * h + 16 * q, hw);
+            tc::st16(lane_addr + 64 + 32 * h + 16 * q, lw);
+        }
+        if (h == 1) {   // half 1's plane bits and residual sum, for half 0 to merge
+#pragma unroll
+            for (int p = 0; p < 3; ++p)
+#pragma unroll
+                for (int tig = 0; tig < 4; ++tig) sW[4 * p + tig] = w[p][tig] << 4;
+            sW[12] = __float_as_uint(g2);
+        }
+        tc::wait_st();
+        tc::fence_before_sync();
+        tc::named_sync(bar_id, 256);
+        tc::fence_after_sync();
+        if (issuer && lane == 0) {
+            const uint32_t bh = tc::smem_u32(smem), bl = bh + 32768;
+            constexpr uint32_t id = tc::idesc_f16(kRows, D);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                tc::mma_ts_f16(tmem + 128, tmem + 8 * ks, tc::sw128_desc(bh, ks, D), id, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                tc::mma_ts_f16(tmem + 128, tmem + 64 + 8 * ks, tc::sw128_desc(bh, ks, D), id, true);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                tc::mma_ts_f16(tmem + 128, tmem + 8 * ks, tc::sw128_desc(bl, ks, D), id, true);
+            tc::mma_commit(&mmabar[tg]);
+        }
+        if (!tc::mbar_wait(&mmabar[tg], i & 1)) timed_out = true;
+        tc::fence_after_sync();
+        // ---- 5. sign words 2 h, 2 h + 1: accumulator columns 64 h .. 64 h + 63
+        uint32_t sgn[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            float pv[16];
+            tc::ld16(lane_addr + 128 + 64 * h + 16 * j, pv);
+            tc::wait_ld();
+#pragma unroll
+            for (int b = 0; b < 16; ++b) asm volatile("" : "+f"(pv[b]));   // no use moves above the wait
+#pragma unroll
+            for (int b = 0; b < 16; ++b) sgn[j >> 1] |= (pv[b] >= 0.f ? 1u : 0u) << (16 * (j & 1) + b);
+        }
+        tc::fence_before_sync();
+        // ---- 6. the record words of this row's slot
+        if (slot >= 0) {
+            const int64_t blk = slot / kBlock;
+            const int o = (int)(slot % kBlock), head = (int)(v % map.n_heads);
+            uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * k_record(D);
+            uint32_t *planes = reinterpret_cast<uint32_t *>(rec);
+            constexpr int PW = 2 * D / 4;
+            const int gid = o & 7, th = o >> 3;
+            if (h == 0) {
+#pragma unroll
+                for (int tig = 0; tig < 4; ++tig) {
+                    const int word = (4 * gid + tig) * 2 + th;
+                    planes[word] = w[0][tig] | sW[tig];
+                    planes[PW + word] = w[1][tig] | sW[4 + tig];
+                    planes[2 * PW + word] = w[2][tig] | sW[8 + tig];
+                }
+                const float gam = sqrtf(g2 + __uint_as_float(sW[12])) * inv_sd;
+                *reinterpret_cast<__half2 *>(rec + 8 * D + 4 * o) = __halves2half2(__float2half_rn(nrm), __float2half_rn(gam));
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) planes[3 * PW + (4 * gid + 2 * h + k) * 2 + th] = sgn[k];
+        }
+        tc::named_sync(bar_id, 256);   // the accumulator, the A lanes and the merge area are free
+    }
+    if (timed_out) flag_status(status, TQ_STATUS_TIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem_base, 512);
+}
+
+template <typename T>
+cudaError_t launch_encs(const void *params, const void *x, int64_t n_vec, const SlotMap &map, void *pool,
+                        int32_t *status, cudaStream_t st) {
+    const int64_t ntiles = (n_vec + encs::kRows - 1) / encs::kRows;
+    if (ntiles <= 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    constexpr int smem = encs::smem_bytes<T>();
+    auto kern = encode128k_split_kernel<T>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(ntiles < sms ? ntiles : sms);
+    kern<<<grid, encs::kThreads, smem, st>>>((const uint8_t *)params, (const T *)x, n_vec, map, (uint8_t *)pool, status);
+    return cudaGetLastError();
+}
+
 template <typename T, bool IS_K>
 cudaError_t launch_encr(const void *params, const void *x, int64_t n_vec, const SlotMap &map, void *pool,
                         int32_t *status, cudaStream_t st) {
@@ -365,6 +644,9 @@ cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const
     SlotMap map{slots, nullptr, nullptr, 0, num_blocks, n_heads};
     if (d == 128 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
         const int64_t nv = n_tokens * n_heads;
+        if (is_k && TQ_ENC_SPLIT)
+            return dtype == TQ_DTYPE_BF16 ? launch_encs<__nv_bfloat16>(params, x, nv, map, pool, status, st)
+                                          : launch_encs<float>(params, x, nv, map, pool, status, st);
         if (dtype == TQ_DTYPE_BF16)
             return is_k ? launch_encr<__nv_bfloat16, true>(params, x, nv, map, pool, status, st)
                         : launch_encr<__nv_bfloat16, false>(params, x, nv, map, pool, status, st);
