@@ -255,6 +255,22 @@ def bench_reference(args):
 
 # ---------------------------------------------------------------- GPU arm
 
+def max_over_ranks(values, world, device):
+    """Element-wise maximum of a list of floats over all ranks (the job takes as long as its slowest
+    rank); the identity at world == 1."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_gbs(world, bytes_per_step, seconds_per_step):
+    """Whole-job throughput: every rank processes its own batch (replicas), in the slowest rank's time."""
+    return world * bytes_per_step / seconds_per_step / 1e9
+
+
 def workload_config(w, l2_note):
     return {"workload": w.name, "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
             "head_dim": w.head_dim, "ctx": w.ctx_lens[0], "block_size": 16, "kv_dtype_in": w.dtype,
@@ -816,14 +832,10 @@ def bench_tq(args):
     h2d = hin.numel() * hin.element_size()
     d2h = hout.numel() * 4
 
-    # max over ranks
-    t = torch.tensor([total_ms, e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, e2e_s = float(t[0]), float(t[1])
+    total_ms, e2e_s = max_over_ranks([total_ms, e2e_s], world, dev)
     ms_step = total_ms / args.steps
-    value = world * nb["step"] / (ms_step * 1e-3) / 1e9
-    e2e_value = world * nb["step"] / e2e_s / 1e9
+    value = job_gbs(world, nb["step"], ms_step * 1e-3)
+    e2e_value = job_gbs(world, nb["step"], e2e_s)
 
     kern_avg_ms = statistics.mean(kern_ms)
     achieved = nb["partial"] / (kern_avg_ms * 1e-3) / 1e9
