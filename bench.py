@@ -802,35 +802,55 @@ def bench_tq(args):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the bench")
 
-    # end-to-end through the public API with pinned host buffers
-    # the step's inputs (q, new K, new V) sit in one pinned buffer and go over in one copy
+    # end-to-end through the public API with pinned host buffers.  The step's inputs (q, new K, new V)
+    # sit in one pinned buffer and go over in one copy; the output comes back in one copy.  As a
+    # serving loop would, uploads and downloads run on their own streams with double buffers, so
+    # that step i's download and step i+1's upload overlap the kernels (every step makes both).
     assert q.dtype == k_new.dtype == v_new.dtype
     nq, nk = q.numel(), k_new.numel()
     hin = torch.empty(nq + 2 * nk, dtype=q.dtype).pin_memory()
     hin[:nq].copy_(torch.from_numpy(np.ascontiguousarray(q_np)).reshape(-1).to(q.dtype))
     hin[nq:nq + nk].copy_(torch.from_numpy(np.ascontiguousarray(K1)).reshape(-1).to(q.dtype))
     hin[nq + nk:].copy_(torch.from_numpy(np.ascontiguousarray(V1)).reshape(-1).to(q.dtype))
-    hout = torch.empty((B, Hq, d), dtype=torch.float32).pin_memory()
-    din = torch.empty(hin.shape, dtype=hin.dtype, device=dev)
-    dq, dk, dv = din[:nq].view(q.shape), din[nq:nq + nk].view(k_new.shape), din[nq + nk:].view(v_new.shape)
+    hout = [torch.empty((B, Hq, d), dtype=torch.float32).pin_memory() for _ in range(2)]
+    din = [torch.empty(hin.shape, dtype=hin.dtype, device=dev) for _ in range(2)]
+    views = [(x[:nq].view(q.shape), x[nq:nq + nk].view(k_new.shape), x[nq + nk:].view(v_new.shape)) for x in din]
+    dout = [torch.empty((B, Hq, d), dtype=torch.float32, device=dev) for _ in range(2)]
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_up = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_down = [torch.cuda.Event() for _ in range(2)]
 
     def e2e_step(i):
         kp, vp = pools[i % nrep]
-        din.copy_(hin, non_blocking=True)
-        tq.decode_step(cache.params, d, dk, dv, dq, Hkv, kp, vp, cache.block_table, pre, max_ctx, out=out,
+        b = i & 1
+        with torch.cuda.stream(up):        # upload, once step i-2 has read this buffer
+            up.wait_event(ev_done[b])
+            din[b].copy_(hin, non_blocking=True)
+            ev_up[b].record(up)
+        stream.wait_event(ev_up[b])
+        stream.wait_event(ev_down[b])      # step i-2's output has gone back
+        dq, dk, dv = views[b]
+        tq.decode_step(cache.params, d, dk, dv, dq, Hkv, kp, vp, cache.block_table, pre, max_ctx, out=dout[b],
                        workspace=ws)
-        hout.copy_(out, non_blocking=True)
+        ev_done[b].record(stream)
+        with torch.cuda.stream(down):      # download of this step's output
+            down.wait_event(ev_done[b])
+            hout[b].copy_(dout[b], non_blocking=True)
+            ev_down[b].record(down)
 
     for i in range(args.warmup):
         e2e_step(i)
+    torch.cuda.synchronize(dev)
     barrier()
     t0 = time.perf_counter()
     for i in range(args.steps):
         e2e_step(i)
+    torch.cuda.synchronize(dev)
     barrier()
     e2e_s = (time.perf_counter() - t0) / args.steps
     h2d = hin.numel() * hin.element_size()
-    d2h = hout.numel() * 4
+    d2h = hout[0].numel() * 4
 
     total_ms, e2e_s = max_over_ranks([total_ms, e2e_s], world, dev)
     ms_step = total_ms / args.steps
