@@ -693,28 +693,32 @@ cudaError_t launch_splitk(int d, const void *params, int batch, int q_len, int h
 // side by side; the pass follows.  pre_lens[b] is the position of the new token, and the pass
 // attends pre_lens[b] + 1 tokens.
 namespace {
-constexpr int kAppendTile = 4;
+// K append tiles hold one vector (all four warps share its QJL projection: 128 FMA per thread),
+// V tiles four (no projection)
+constexpr int kAppendTileK = 1, kAppendTileV = 4;
 
 template <int D, int NTK, typename T>
 __global__ void __launch_bounds__(128)
 step_prep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ k_new, const T *__restrict__ v_new,
                  const T *__restrict__ q, int batch, int q_len, int hq, int hkv, SlotMap map, uint8_t *__restrict__ k_pool,
-                 uint8_t *__restrict__ v_pool, int n_app, int max_ctx, int chunk, int P, uint8_t *__restrict__ packs,
+                 uint8_t *__restrict__ v_pool, int n_app_k, int n_app_v, int max_ctx, int chunk, int P,
+                 uint8_t *__restrict__ packs,
                  unsigned int *__restrict__ counters, int64_t *__restrict__ cpre, int32_t *__restrict__ cta_b,
                  int32_t *status) {
     extern __shared__ __align__(16) uint8_t smem[];
     pdl_launch_dependents();
     const int blk = blockIdx.x;
-    if (blk < 2 * n_app) {
-        const bool is_k = blk < n_app;
-        encode_tiles<D, kAppendTile, T>(params, is_k ? k_new : v_new, (int64_t)batch * q_len * hkv, map,
-                                        is_k ? k_pool : v_pool, is_k, is_k, is_k ? blk : blk - n_app, n_app, smem,
-                                        status);
+    if (blk < n_app_k) {
+        encode_tiles<D, kAppendTileK, T>(params, k_new, (int64_t)batch * q_len * hkv, map, k_pool, true, true, blk,
+                                         n_app_k, smem, status);
+    } else if (blk < n_app_k + n_app_v) {
+        encode_tiles<D, kAppendTileV, T>(params, v_new, (int64_t)batch * q_len * hkv, map, v_pool, false, false,
+                                         blk - n_app_k, n_app_v, smem, status);
     } else if (blk == gridDim.x - 1) {   // the last CTA lays out the pass's work
         build_schedule(map.ctx_lens, q_len, batch, hkv, max_ctx, chunk, P, cpre, cta_b);
     } else {
         qprep_rows<D, NTK, T>(params, q, batch, q_len, hq, hkv, map.ctx_lens, q_len, max_ctx, chunk, P, packs, counters, cpre,
-                              cta_b, blk - 2 * n_app, smem);
+                              cta_b, blk - n_app_k - n_app_v, smem);
     }
 }
 
@@ -722,15 +726,17 @@ template <int D, int NTK, typename T>
 cudaError_t step_prep_launch(const uint8_t *P, const void *k_new, const void *v_new, const void *q, int batch,
                              int q_len, int hq, int hkv, const SlotMap &map, void *kp, void *vp, int max_ctx,
                              int nctas, const WsLayout &w, int32_t *status, cudaStream_t st) {
-    constexpr size_t es = EncSmem<D, kAppendTile>::kBytes, qs = qprep_smem<D>();
+    constexpr size_t ek = EncSmem<D, kAppendTileK>::kBytes, ev = EncSmem<D, kAppendTileV>::kBytes;
+    constexpr size_t es = ek > ev ? ek : ev, qs = qprep_smem<D>();
     constexpr size_t smem = es > qs ? es : qs;
     auto kern = step_prep_kernel<D, NTK, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int n_app = (batch * q_len * hkv + kAppendTile - 1) / kAppendTile;
+    const int n_app_k = (batch * q_len * hkv + kAppendTileK - 1) / kAppendTileK;
+    const int n_app_v = (batch * q_len * hkv + kAppendTileV - 1) / kAppendTileV;
     const int n_q = (batch * q_len * hq + kQRows - 1) / kQRows;
-    kern<<<2 * n_app + n_q + 1, 128, smem, st>>>(P, (const T *)k_new, (const T *)v_new, (const T *)q, batch, q_len, hq,
-                                             hkv, map, (uint8_t *)kp, (uint8_t *)vp, n_app, max_ctx,
+    kern<<<n_app_k + n_app_v + n_q + 1, 128, smem, st>>>(P, (const T *)k_new, (const T *)v_new, (const T *)q, batch, q_len, hq,
+                                             hkv, map, (uint8_t *)kp, (uint8_t *)vp, n_app_k, n_app_v, max_ctx,
                                              pass_chunk(q_len * hq / hkv), nctas, w.packs, w.counters, w.cpre, w.cta_b,
                                              status);
     return cudaGetLastError();

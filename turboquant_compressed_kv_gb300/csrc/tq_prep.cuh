@@ -64,7 +64,7 @@ __device__ __forceinline__ void encode_tiles(const uint8_t *__restrict__ params,
                                              int64_t n_vec, const SlotMap &map, uint8_t *__restrict__ pool, bool is_k,
                                              bool report_bad, int blk, int nblk, uint8_t *smem, int32_t *status) {
     constexpr int R = D / 32;
-    constexpr int kTile = TILE, kPerWarp = TILE / kEncWarps;
+    constexpr int kTile = TILE, kPerWarp = (TILE + kEncWarps - 1) / kEncWarps;   // tiles below 4 leave warps idle in 1 and 3
     using SM = EncSmem<D, TILE>;
     float *sST = reinterpret_cast<float *>(smem);
     float (*s_rho)[D] = reinterpret_cast<float (*)[D]>(smem + SM::kST);
@@ -95,22 +95,26 @@ __device__ __forceinline__ void encode_tiles(const uint8_t *__restrict__ params,
 #pragma unroll
         for (int j = 0; j < kPerWarp; ++j) {
             const int tv = warp + kEncWarps * j;              // vector within the tile
+            const bool mine = tv < kTile;                     // warp-uniform
             const int64_t v = v0 + tv;
             float val[R];
             int dims[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {   // the input row does not depend on the slot: load it first
                 dims[r] = is_k ? kdim<D>(lane, r) : vdim<D>(lane, r);
-                val[r] = (v < n_vec) ? to_f32<T>(x[v * D + dims[r]]) : 0.f;
+                val[r] = (mine && v < n_vec) ? to_f32<T>(x[v * D + dims[r]]) : 0.f;
             }
             // the slot (block-table lookups) is needed only by the stores: a vector without one is
             // encoded from whatever it holds and not stored, so nothing here waits for the lookup
             slot[j] = -1;
-            if (v < n_vec)   // a bad slot is reported once per token
+            if (mine && v < n_vec)   // a bad slot is reported once per token
                 slot[j] = map.slot(v / map.n_heads, status, report_bad && lane == 0 && (v % map.n_heads) == 0);
             // S^T (64 KB at d = 128) is copied once, after the first rows are requested, so that
             // those small loads are not queued behind it; it is waited for before the projection
             if (is_k && SM::kResident && j == 0 && tile == blk) stage_st_rows<D, kEncWarps * 32>(sST, gST, 0, D);
+            nrm[j] = 0.f;
+            gam[j] = 0.f;
+            if (!mine) continue;
             float ss = 0.f;
 #pragma unroll
             for (int r = 0; r < R; ++r) ss = fmaf(val[r], val[r], ss);
@@ -160,7 +164,7 @@ __device__ __forceinline__ void encode_tiles(const uint8_t *__restrict__ params,
         // ---- 3. pack and store
 #pragma unroll
         for (int j = 0; j < kPerWarp; ++j) {
-            if (slot[j] < 0) continue;                     // warp-uniform
+            if (slot[j] < 0) continue;                     // warp-uniform (also for a warp without a vector)
             const int tv = warp + kEncWarps * j;
             const int head = (int)((v0 + tv) % map.n_heads);
             const int64_t blk = slot[j] / kBlock;
