@@ -328,17 +328,19 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                             w[m][th] = (m < 3) ? Wd[m][th] : (m == 3) ? (Wd[0][th] ^ Wd[1][th] ^ Wd[2][th]) : Wd[3][th];
                             w8[m][th] = w[m][th] << 8;
                         }
-                    float acc[5][NTK][4];
-#pragma unroll
-                    for (int m = 0; m < 5; ++m)
-#pragma unroll
-                        for (int nt = 0; nt < NTK; ++nt)
-#pragma unroll
-                            for (int x = 0; x < 4; ++x) acc[m][nt][x] = 0.f;
+                    float acc[5][NTK][4];   // started by the first k-step's zero-accumulator mma
 #pragma unroll
                     for (int ks = 0; ks < NKS; ++ks) {
                         const int q = 8 + ks;
                         const uint32_t msk = op_mask(q), bas = (q == 14) ? 0u : one16x2;
+                        uint2 bsm[2][NTK];   // this k-step's fragments of q-bar (0) and u (1), shared-memory case
+                        if constexpr (BQS) {
+#pragma unroll
+                            for (int qu = 0; qu < 2; ++qu)
+#pragma unroll
+                                for (int nt = 0; nt < NTK; ++nt)
+                                    bsm[qu][nt] = lds_u2(sBq + ((qu * NKS + ks) * NTK + nt) * 64 + lane * 2);
+                        }
 #pragma unroll
                         for (int m = 0; m < 5; ++m) {
                             const uint32_t a0 = lop_and_xor(w8[m][0], msk, bas), a1 = lop_and_xor(w8[m][1], msk, bas);
@@ -346,12 +348,10 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                             const int qu = (m == 4) ? 1 : 0;
 #pragma unroll
                             for (int nt = 0; nt < NTK; ++nt) {
-                                if constexpr (BQS) {
-                                    const uint2 bb = lds_u2(sBq + ((qu * NKS + ks) * NTK + nt) * 64 + lane * 2);
-                                    mma_f16(acc[m][nt], a0, a1, a2, a3, bb.x, bb.y);
-                                } else {
-                                    mma_f16(acc[m][nt], a0, a1, a2, a3, bq[qu][ks][nt][0], bq[qu][ks][nt][1]);
-                                }
+                                const uint32_t b0 = BQS ? bsm[qu][nt].x : bq[qu][ks][nt][0];
+                                const uint32_t b1 = BQS ? bsm[qu][nt].y : bq[qu][ks][nt][1];
+                                if (ks == 0) mma_f16_z(acc[m][nt], a0, a1, a2, a3, b0, b1);
+                                else mma_f16(acc[m][nt], a0, a1, a2, a3, b0, b1);
                             }
                         }
                     }

@@ -384,11 +384,13 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base + 256u * tg;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * sl) << 16);
-    const float t0 = ph->threshold[0], t1 = ph->threshold[1], t2 = ph->threshold[2], t3 = ph->threshold[3];
-    const float t4 = ph->threshold[4], t5 = ph->threshold[5], t6 = ph->threshold[6];
-    float cen[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) cen[k] = ph->centroid[k];
+    // thresholds x 256 (exact), and x 256 the half-widths of the cell pairs around the odd-index
+    // thresholds: cells 2k and 2k + 1 are t_2k -/+ hw_k; the codebook is symmetric, so pairs 0 and 3
+    // (the outer ones) share hw_out and pairs 1 and 2 share hw_in
+    const float T0 = 256.f * ph->threshold[0], T1 = 256.f * ph->threshold[1], T2 = 256.f * ph->threshold[2];
+    const float T3 = 256.f * ph->threshold[3], T4 = 256.f * ph->threshold[4], T5 = 256.f * ph->threshold[5];
+    const float T6 = 256.f * ph->threshold[6];
+    const float hw_out = 128.f * (ph->centroid[7] - ph->centroid[6]), hw_in = 128.f * (ph->centroid[5] - ph->centroid[4]);
     const float inv_sd = rsqrtf((float)D);
     const float hs = h ? -1.f : 1.f;
     uint32_t *sW = reinterpret_cast<uint32_t *>(smem + oW<T>()) + ((size_t)tg * kRows + row) * kWStride;
@@ -463,25 +465,29 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
                     u[m] = a0 + a1;
                     u[m | st] = a0 - a1;
                 }
-        const float rn = nrm > 0.f ? 1.f / nrm : 0.f;
-        // ---- 3. cells of coordinates 64 h + m, residual
+        // 256 / n (exact scaling of 1 / n): Z = 256 z, and the residual comes out x 256, which keeps
+        // its f16 low parts out of the subnormals
+        const float rs = nrm > 0.f ? 256.f / nrm : 0.f;
+        // ---- 3. cells of coordinates 64 h + m, residual.  The search compares Z with 256 t_j, the
+        // same decisions as z against t_j (ties go up); the last comparison's difference Z - 256 t_2k
+        // gives the residual: Z - 256 c = (Z - 256 t_2k) -/+ 256 hw_k.
         uint32_t w[3][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
-        float g2 = 0.f;
+        float g2 = 0.f;   // sum of squares of the residual x 256
 #pragma unroll
         for (int m = 0; m < 64; ++m) {
-            const float z = u[m] * rn;
-            const bool b2 = z >= t3;
-            const bool b1 = z >= (b2 ? t5 : t1);
-            const bool b0 = z >= (b2 ? (b1 ? t6 : t4) : (b1 ? t2 : t0));
+            const float Z = u[m] * rs;
+            const bool b2 = Z >= T3;
+            const bool b1 = Z >= (b2 ? T5 : T1);
+            const float dz = Z - (b2 ? (b1 ? T6 : T4) : (b1 ? T2 : T0));
+            const bool b0 = dz >= 0.f;
             const int tig = (m >> 1) & 3, bit = 8 * ((m >> 3) & 1) + (m >> 4) + 16 * (m & 1);   // + 4 h below
             w[0][tig] |= (uint32_t)b0 << bit;
             w[1][tig] |= (uint32_t)b1 << bit;
             w[2][tig] |= (uint32_t)b2 << bit;
-            const float c = b2 ? (b1 ? (b0 ? cen[7] : cen[6]) : (b0 ? cen[5] : cen[4]))
-                               : (b1 ? (b0 ? cen[3] : cen[2]) : (b0 ? cen[1] : cen[0]));
-            const float rho = z - c;
+            const float hw = (b1 == b2) ? hw_out : hw_in;
+            const float rho = b0 ? dz - hw : dz + hw;
             g2 = fmaf(rho, rho, g2);
-            u[m] = rho * 256.f;   // exact scaling; keeps the f16 low parts out of the subnormals
+            u[m] = rho;
         }
         // ---- 4. rho (x 256) as f16 hi / lo into this row's lane: K elements 64 h .. 64 h + 63
 #pragma unroll
@@ -526,7 +532,10 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
         }
         if (!tc::mbar_wait(&mmabar[tg], i & 1)) timed_out = true;
         tc::fence_after_sync();
-        // ---- 5. sign words 2 h, 2 h + 1: accumulator columns 64 h .. 64 h + 63
+        // ---- 5. sign words 2 h, 2 h + 1: accumulator columns 64 h .. 64 h + 63.  Column 16 j + b is
+        // bit 16 (j & 1) + b of word j >> 1; the projections' sign bits are shifted in one per funnel
+        // shift (the first column ends in bit 31), then reversed and inverted (bit = projection >= 0;
+        // only an exact zero, a tie, could read as -0)
         uint32_t sgn[2] = {0u, 0u};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -536,8 +545,10 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
 #pragma unroll
             for (int b = 0; b < 16; ++b) asm volatile("" : "+f"(pv[b]));   // no use moves above the wait
 #pragma unroll
-            for (int b = 0; b < 16; ++b) sgn[j >> 1] |= (pv[b] >= 0.f ? 1u : 0u) << (16 * (j & 1) + b);
+            for (int b = 0; b < 16; ++b) sgn[j >> 1] = __funnelshift_l(__float_as_uint(pv[b]), sgn[j >> 1], 1);
         }
+        sgn[0] = ~__brev(sgn[0]);
+        sgn[1] = ~__brev(sgn[1]);
         tc::fence_before_sync();
         // ---- 6. the record words of this row's slot
         if (slot >= 0) {
@@ -555,7 +566,7 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
                     planes[PW + word] = w[1][tig] | sW[4 + tig];
                     planes[2 * PW + word] = w[2][tig] | sW[8 + tig];
                 }
-                const float gam = sqrtf(g2 + __uint_as_float(sW[12])) * inv_sd;
+                const float gam = sqrtf(g2 + __uint_as_float(sW[12])) * (inv_sd * (1.f / 256.f));
                 *reinterpret_cast<__half2 *>(rec + 8 * D + 4 * o) = __halves2half2(__float2half_rn(nrm), __float2half_rn(gam));
             }
 #pragma unroll
