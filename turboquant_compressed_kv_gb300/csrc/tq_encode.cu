@@ -318,7 +318,8 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
 //  * the transform's stage on index bit 6 is taken first, on the input: half h holds
 //    u_m = (D x)_m + (-1)^h (D x)_{m+64} (m < 64) and finishes the 64-point transform in
 //    registers; its outputs are coordinates 64 h + m (the stages of the transform commute);
-//  * each half reads the whole row (the norm and that first stage need it);
+//  * each half reads the whole row (that first stage needs it; the sums of squares of the two
+//    halves' outputs add to twice the squared norm);
 //  * a plane word holds bits of both halves (half h owns bits n >> 4 = 4h .. 4h + 3 of each byte):
 //    half 1 leaves its partial words and its residual sum in shared memory, half 0 merges and
 //    stores them; accumulator columns 64 h .. 64 h + 63 are sign words 2h, 2h + 1, stored by half h.
@@ -345,7 +346,7 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint64_t xfull[kTg][2], mmabar[kTg];
     __shared__ uint32_t tmem_base;
-    __shared__ float s_D[D];
+    __shared__ float s_Dh[2][2][64];   // half h: D_m and (-1)^h D_{m+64}, m < 64
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     if (ph->magic != kParamsMagic || ph->d != D) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
@@ -363,7 +364,11 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
         }
     }
     if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
-    if (tid < D) s_D[tid] = reinterpret_cast<const float *>(params + params_off_D(D))[tid];
+    if (tid < 2 * D) {
+        const float *Dp = reinterpret_cast<const float *>(params + params_off_D(D));
+        const int hh = tid >> 7, k = (tid >> 6) & 1, m = tid & 63;
+        s_Dh[hh][k][m] = (k && hh) ? -Dp[64 + m] : Dp[64 * k + m];
+    }
     {   // B row n = S row sigma(n), sigma(32 tig + b) = 16 (b & 7) + 8 ((b >> 3) & 1) + 2 tig + (b >> 4)
         const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
         for (int e = tid; e < D * D; e += kThreads) {
@@ -384,7 +389,7 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base + 256u * tg;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * sl) << 16);
-    // thresholds x 256 (exact), and x 256 the half-widths of the cell pairs around the odd-index
+    // thresholds x 256 (exact), and x 256 the half-widths of the cell pairs around the even-index
     // thresholds: cells 2k and 2k + 1 are t_2k -/+ hw_k; the codebook is symmetric, so pairs 0 and 3
     // (the outer ones) share hw_out and pairs 1 and 2 share hw_in
     const float T0 = 256.f * ph->threshold[0], T1 = 256.f * ph->threshold[1], T2 = 256.f * ph->threshold[2];
@@ -392,7 +397,7 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
     const float T6 = 256.f * ph->threshold[6];
     const float hw_out = 128.f * (ph->centroid[7] - ph->centroid[6]), hw_in = 128.f * (ph->centroid[5] - ph->centroid[4]);
     const float inv_sd = rsqrtf((float)D);
-    const float hs = h ? -1.f : 1.f;
+    const bool small = n_vec <= (int64_t)0x7fffffff;
     uint32_t *sW = reinterpret_cast<uint32_t *>(smem + oW<T>()) + ((size_t)tg * kRows + row) * kWStride;
     bool timed_out = false;
     const int bar_id = 1 + tg;
@@ -415,7 +420,10 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
     for (int i = 0; tile_of(i) < ntiles; ++i) {
         const int buf = i % NX, use = i / NX;
         const int64_t v0 = tile_of(i) * kRows, v = v0 + row;
-        const int64_t slot = v < n_vec ? map.slot(v / map.n_heads, status, h == 0 && (v % map.n_heads) == 0) : -1;
+        // token and head of row v (32-bit division when the rows fit, as they do in practice)
+        const int64_t tok = small ? (int64_t)((uint32_t)v / (uint32_t)map.n_heads) : v / map.n_heads;
+        const int head = (int)(v - tok * map.n_heads);
+        const int64_t slot = v < n_vec ? map.slot(tok, status, h == 0 && head == 0) : -1;
         if (!tc::mbar_wait(&xfull[tg][buf], use & 1)) timed_out = true;
         // ---- 1. the whole row: norm, signs D, and the transform stage on index bit 6
         float u[64];
@@ -445,8 +453,8 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
 #pragma unroll
                 for (int e = 0; e < EPC; ++e) {
                     const int m = EPC * c + e;
-                    ss = fmaf(h ? b[e] : a[e], h ? b[e] : a[e], ss);   // this half's share of the norm
-                    u[m] = fmaf(hs, b[e] * s_D[m + 64], a[e] * s_D[m]);
+                    u[m] = fmaf(b[e], s_Dh[h][1][m], a[e] * s_Dh[h][0][m]);
+                    ss = fmaf(u[m], u[m], ss);   // the halves' sums add to 2 |x|^2
                 }
             }
         }
@@ -454,7 +462,7 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
         sSS[1 - h] = ss;
         tc::named_sync(bar_id, 256);   // every row is read: the buffer takes the tile NX ahead
         if (issuer && tile_of(i + NX) < ntiles) issue(i + NX, buf);
-        const float nrm = sqrtf(ss + sSS[h]);   // the same sum in both halves (addition commutes)
+        const float nrm = sqrtf(0.5f * (ss + sSS[h]));   // the same sum in both halves (addition commutes)
         // ---- 2. the 64-point transform of this half (index bits 0..5)
 #pragma unroll
         for (int st = 1; st < 64; st <<= 1)
@@ -553,7 +561,7 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
         // ---- 6. the record words of this row's slot
         if (slot >= 0) {
             const int64_t blk = slot / kBlock;
-            const int o = (int)(slot % kBlock), head = (int)(v % map.n_heads);
+            const int o = (int)(slot % kBlock);
             uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * k_record(D);
             uint32_t *planes = reinterpret_cast<uint32_t *>(rec);
             constexpr int PW = 2 * D / 4;
