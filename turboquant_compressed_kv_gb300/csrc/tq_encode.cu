@@ -77,7 +77,7 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
     using namespace encr;
     constexpr int NX = nx<T>(), RS = row_stride<T>(), RB = row_bytes<T>(), EPC = 16 / (int)sizeof(T);
     extern __shared__ __align__(1024) uint8_t smem[];
-    __shared__ uint64_t xfull[2][2], mmabar[2];
+    __shared__ uint64_t xfull[2][2], xempty[2][2], mmabar[2];
     __shared__ uint32_t tmem_base;
     __shared__ float s_D[D];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
@@ -92,6 +92,8 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(&xfull[i][0], 1);
             tc::mbar_init(&xfull[i][1], 1);
+            tc::mbar_init(&xempty[i][0], 4);   // one arrival per warp of the warpgroup
+            tc::mbar_init(&xempty[i][1], 4);
             tc::mbar_init(&mmabar[i], 1);
         }
     }
@@ -169,8 +171,18 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
                 }
             }
         }
-        tc::named_sync(bar_id, 128);   // every row is read: the buffer takes the tile NX ahead
-        if (row < 32 && tile_of(i + NX) < ntiles) issue(i + NX, buf);
+        __syncwarp();
+        if ((row & 31) == 0) tc::mbar_arrive(&xempty[wg][buf]);   // this warp's rows of the buffer are read
+        // the first warp refills the buffer with the tile NX ahead once all four warps have read it:
+        // at once when it is the only buffer, else after this tile's work (the other warps are long
+        // done by then, so nobody waits)
+        auto refill = [&]() {
+            if (row < 32 && tile_of(i + NX) < ntiles) {
+                if (!tc::mbar_wait(&xempty[wg][buf], use & 1)) timed_out = true;
+                issue(i + NX, buf);
+            }
+        };
+        if (NX == 1) refill();
         // ---- 2. norm, signs, transform
         float ss = 0.f;
 #pragma unroll
@@ -303,6 +315,7 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
             }
         }
         if (IS_K) tc::named_sync(bar_id, 128);   // the accumulator and A lanes are free for the next tile
+        if (NX > 1) refill();
     }
     if (timed_out) flag_status(status, TQ_STATUS_TIMEOUT);
     if (IS_K) {
