@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--workload", default=None,
                     help="run only this side workload (ragged, long256, verify_q2, hybrid32k, prefill_encode, "
                          "prefill_dequant, gq_compare) and print its JSON object; for profiling")
+    ap.add_argument("--oracle-single-thread", choices=["decode", "encode"], default=None,
+                    help=argparse.SUPPRESS)   # child run of the oracle on one thread (cpu_baseline)
     return ap.parse_args()
 
 
@@ -617,7 +619,8 @@ def extra_encode(steps, warmup, dev, cpu=False):
     if cpu:
         tps, dt, sample = run_cpu_encode(w)
         res["cpu_baseline"] = {"value": round(tps / 1e6, 6), "unit": "Mtok/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
-                               "kind": "oracle", "sample": sample, "seconds": round(dt, 3)}
+                               "kind": "oracle", "sample": sample, "seconds": round(dt, 3),
+                               "single_thread": oracle_single_thread("encode")}
     return res
 
 
@@ -753,9 +756,12 @@ def bench_tq(args):
                        workspace=ws, status=status)
 
     def stage_step(i, ev):
-        """The same pass through the stage calls, with events around the split-K kernel."""
+        """The same work through the stage calls, with events around each: the append, the query prep
+        and the split-K kernel."""
         kp, vp = pools[i % nrep]
+        ev[2].record(stream)
         tq.paged_append(cache.params, d, k_new, v_new, cache.block_table, pre, kp, vp, status=status)
+        ev[3].record(stream)
         tq.decode_qprep(cache.params, d, q, Hkv, ctx, max_ctx, ws)
         ev[0].record(stream)
         tq.decode_splitk(cache.params, d, B, Hq, Hkv, kp, vp, cache.block_table, ctx, max_ctx, out, ws,
@@ -785,11 +791,13 @@ def bench_tq(args):
     t_wall1 = time.time()
     total_ms = e0.elapsed_time(e1)
     # the dominant kernel: the split-K pass, timed by events on the launching stream over K steps
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
     for i in range(args.steps):
         stage_step(i, kev[i])
     barrier()
-    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    kern_ms = [e[0].elapsed_time(e[1]) for e in kev]
+    append_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in kev)
+    qprep_ms = statistics.mean(e[3].elapsed_time(e[0]) for e in kev)
     # keep the GPU busy a little longer so the sampler sees the loaded clocks
     t_c0 = time.time()
     while time.time() - t_c0 < 1.0:
@@ -874,6 +882,9 @@ def bench_tq(args):
                      "kernel_ms": round(kern_avg_ms, 6), "bytes_per_launch": nb["partial"]},
         "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
+        "stages_ms": {"append": round(append_ms, 6), "qprep": round(qprep_ms, 6), "splitk": round(kern_avg_ms, 6),
+                      "note": "each stage through its own entry point, timed by events on the stream; the step "
+                              "fuses the append with the query prep and overlaps the pass's launch"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
                    "samples": clocks["samples"]},
@@ -894,7 +905,8 @@ def bench_tq(args):
         line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": int(os.environ["OMP_NUM_THREADS"]),
                                 "kind": "oracle",
                                 "sample": "2 of 16 sequences, full step (append + decode of 32 heads over 4096 "
-                                          "tokens), 3 timed repetitions"}
+                                          "tokens), 3 timed repetitions",
+                                "single_thread": oracle_single_thread("decode")}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -923,8 +935,36 @@ def side_workload(args):
     return 0
 
 
+def oracle_single_thread(kind):
+    """The oracle on one host thread, in a child process started with OMP_NUM_THREADS=1 (the thread
+    count is fixed when the oracle's OpenMP runtime loads); None if the child fails."""
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-single-thread", kind], env=env,
+                           capture_output=True, text=True, timeout=600)
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+
+
+def oracle_single_thread_child(kind):
+    from turboquant_compressed_kv_gb300 import synth
+    if kind == "decode":
+        gbs, dt, _ = run_cpu_oracle(synth.workload(WORKLOAD), 1, 0, 1)
+        res = {"value": round(gbs, 6), "unit": "GB/s", "cores": 1,
+               "sample": "1 of 16 sequences, full step (append + decode of 32 heads over 4096 tokens), one timed pass",
+               "seconds": round(dt, 3)}
+    else:
+        tps, dt, sample = run_cpu_encode(synth.workload("prefill"), ntok=512)
+        res = {"value": round(tps / 1e6, 6), "unit": "Mtok/s", "cores": 1, "sample": sample, "seconds": round(dt, 3)}
+    print(json.dumps(res), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.oracle_single_thread:
+        return oracle_single_thread_child(args.oracle_single_thread)
     if args.impl == "reference":
         return bench_reference(args)
     if args.workload:

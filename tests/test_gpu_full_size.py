@@ -1,8 +1,8 @@
 """Full-size decode parity on the benchmark-sized workloads, sampled by (sequence, kv head).
 
 The whole batch is prefilled on the device (synth.kv_tokens_device) and decoded in one call, at
-the sizes and launch configuration the benchmark uses.  For a few sampled (sequence, kv head)
-units, the oracle encodes every token of the unit itself (synth.kv_tokens, seeded) into a
+the sizes and launch configuration the benchmark uses.  For sampled (sequence, kv head) units
+(every kv head of one sequence, plus units of other sequences), the oracle encodes every token of the unit itself (synth.kv_tokens, seeded) into a
 one-unit cache; those records are written over the unit's slots in the device pools, and the
 oracle decodes the unit's query heads.  A unit's attention reads only its own records, so the
 device output of the sampled heads must match the oracle's within the attention tolerance.
@@ -37,9 +37,12 @@ def _oracle_unit(w, cache, b, kvh):
 
 
 @pytest.mark.parametrize("name,units", [
-    ("llama8b_decode", [(0, 0), (9, 5), (15, 7)]),     # 16 x 32/8 heads, d=128, 4096 tokens
-    ("ragged", [(3, 1), (41, 3)]),                      # 64 x 32/4 heads, d=128, 512..32768 tokens
-    ("long256", [(2, 6)]),                              # 4 x 16/8 heads, d=256, 131072 tokens
+    # 16 x 32/8 heads, d=128, 4096 tokens: every kv head of sequence 9, and units of three others
+    ("llama8b_decode", [(9, h) for h in range(8)] + [(0, 0), (6, 3), (15, 7)]),
+    # 64 x 32/4 heads, d=128, 512..32768 tokens: every kv head of sequence 41, and three others
+    ("ragged", [(41, h) for h in range(4)] + [(3, 1), (20, 2), (63, 0)]),
+    # 4 x 16/8 heads, d=256, 131072 tokens (about 8 s of oracle encode per unit)
+    ("long256", [(2, 6), (0, 1)]),
 ])
 def test_full_size_sampled_parity(name, units):
     w = synth.workload(name)
