@@ -281,6 +281,39 @@ int tq_decode_attn_hybrid(const void *params, int d, const void *q, int dtype, i
                           const int32_t *win_lens, float *out, void *workspace, size_t workspace_bytes,
                           int32_t *status, tq_stream_t stream);
 
+/* tq_hybrid_append -- one new token per sequence into a hybrid cache, compressing the oldest
+ * window token once the window is full.  [README, "TurboQuantization: KV Cache Compression":
+ * its options table and its kv_bits / --turbo-kv comparison put the start of compression at
+ * 2048 tokens; the most recent tokens stay uncompressed and older ones are compressed]
+ * Window layout: token p of sequence b, while uncompressed, sits in window slot p mod win_cap.
+ * Tokens 0 .. ctx_lens[b] - 1 are in the compressed paged history and tokens ctx_lens[b] ..
+ * ctx_lens[b] + win_lens[b] - 1 in the window, so the window fills slots 0, 1, ... first and,
+ * once full, every appended token takes the slot of the oldest one.  For each sequence:
+ *   - win_lens[b] == win_cap: the window token at position ctx_lens[b] (slot ctx_lens[b] mod
+ *     win_cap) is encoded (K and V, every kv head, as tq_paged_append) into the paged pools at
+ *     history position ctx_lens[b] through block_table; ctx_lens[b] += 1; the new token takes
+ *     the freed slot;
+ *   - win_lens[b] < win_cap: the new token goes into slot win_lens[b]; win_lens[b] += 1.
+ * The result is the cache tq_decode_attn_hybrid reads (its window slots 0 .. win_lens[b] - 1).
+ *   k_new, v_new  device [batch][n_kv_heads][d] in dtype (TQ_DTYPE_F32 or TQ_DTYPE_BF16);
+ *   win_k, win_v  device [batch][win_cap][n_kv_heads][d], the same dtype;
+ *   win_lens, ctx_lens  device int32[batch], read and updated in place;
+ *   scratch       device, >= tq_hybrid_append_scratch_bytes(d, batch, n_kv_heads, dtype)
+ *                 bytes (the leaving rows and their positions), overwritten.
+ * A sequence whose state is not one this call produces (win_lens outside [0, win_cap],
+ * ctx_lens < 0, or a window that is not full while ctx_lens[b] mod win_cap != 0) is left
+ * unchanged and sets TQ_STATUS_BAD_SLOT; so does a history position without a valid block,
+ * whose token is then dropped from the history while the window still advances.
+ * Three launches on the stream (gather of the leaving rows, their encode, the window write).
+ * Errors: TQ_ERR_HEAD_DIM, TQ_ERR_DTYPE, TQ_ERR_INVALID (win_cap <= 0 among others),
+ * TQ_ERR_ALIGN (every buffer 16-byte aligned), TQ_ERR_WORKSPACE (scratch too small),
+ * TQ_ERR_CUDA. */
+size_t tq_hybrid_append_scratch_bytes(int d, int batch, int n_kv_heads, int dtype);
+int tq_hybrid_append(const void *params, int d, const void *k_new, const void *v_new, int dtype, int batch,
+                     int n_kv_heads, void *win_k, void *win_v, int win_cap, int32_t *win_lens,
+                     const int32_t *block_table, int max_blocks, int32_t *ctx_lens, void *k_pool, void *v_pool,
+                     int64_t num_blocks, void *scratch, size_t scratch_bytes, int32_t *status, tq_stream_t stream);
+
 /* tq_decode_attn_noalloc -- tq_decode_attn without a caller workspace.
  * The pages have no counterpart to this call; it exists for callers that
  * cannot allocate device memory when they decode: a serving runtime that

@@ -346,3 +346,40 @@ def decode_hybrid(D, S, q: np.ndarray, Hkv: int, kpool, vpool, block_table, ctx_
             out[b, h] = (p[:, None] * vals).sum(0) / p.sum()
     return out
 
+
+
+def hybrid_append(D, S, k_new, v_new, win_k, win_v, win_lens, ctx_lens, block_table, kpool, vpool):
+    """One new token per sequence into a hybrid cache (SwiftLM README, "TurboQuantization: KV Cache
+    Compression": compression starts at 2048 tokens, the most recent tokens stay uncompressed).
+
+    Reading taken: while uncompressed, token p of a sequence is kept in window slot p mod W
+    (W = win_k.shape[1]); tokens 0 .. ctx_lens[b] - 1 are compressed, the next win_lens[b] are in
+    the window.  A full window first compresses its oldest token, position ctx_lens[b], into the
+    paged pools at that history position (the K and V encodes of this module); the new token then
+    takes that slot.  Otherwise the new token goes into slot win_lens[b].  A state this step does
+    not produce (lengths out of range, or a window that is not full while ctx_lens[b] mod W != 0)
+    is left as it is; a history position without a valid block loses the leaving token.
+    k_new, v_new [B][H][d]; win_k, win_v [B][W][H][d]; kpool / vpool are updated in place.
+    Returns (win_k, win_v, win_lens, ctx_lens), updated copies."""
+    win_k, win_v = np.array(win_k, copy=True), np.array(win_v, copy=True)
+    win_lens = np.array(win_lens, np.int32, copy=True)
+    ctx_lens = np.array(ctx_lens, np.int32, copy=True)
+    B, W = win_k.shape[:2]
+    nblk, mb = kpool.shape[0], block_table.shape[1]
+    for b in range(B):
+        L, n = int(ctx_lens[b]), int(win_lens[b])
+        if not (L >= 0 and 0 <= n <= W and (n == W or L % W == 0)):
+            continue
+        if n == W:
+            old = L % W
+            blk = int(block_table[b, L // BLOCK]) if L // BLOCK < mb else -1
+            if 0 <= blk < nblk:
+                slot = np.array([blk * BLOCK + L % BLOCK], np.int64)
+                encode(True, D, S, np.asarray(win_k[b, old][None], np.float32), slot, kpool)
+                encode(False, D, S, np.asarray(win_v[b, old][None], np.float32), slot, vpool)
+            win_k[b, old], win_v[b, old] = k_new[b], v_new[b]
+            ctx_lens[b] = L + 1
+        else:
+            win_k[b, n], win_v[b, n] = k_new[b], v_new[b]
+            win_lens[b] = n + 1
+    return win_k, win_v, win_lens, ctx_lens

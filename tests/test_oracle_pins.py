@@ -618,3 +618,73 @@ def test_gq_bits_per_dim_match_the_stated_saving():
         b = gq.record_bytes(128, bits, 64) * 8 / (16 * 128)
         assert b == want
         assert 1.8 <= 16 / b <= 4.0
+
+
+# ------------------------------------------------------------------ hybrid cache upkeep
+
+def _hybrid_run(d, H, W, T, bt, seed=0):
+    """T appends, one token per step, into an empty hybrid cache of window W (one sequence)."""
+    D, S = synth.rotation_signs(d), synth.qjl_matrix(d)
+    rng = np.random.default_rng(seed)
+    K = rng.standard_normal((T, H, d)).astype(np.float32)
+    V = rng.standard_normal((T, H, d)).astype(np.float32)
+    nblk = int(bt.max()) + 2
+    kp = np.zeros((nblk, H, oracle.record_bytes(True, d)), np.uint8)
+    vp = np.zeros((nblk, H, oracle.record_bytes(False, d)), np.uint8)
+    wk = np.zeros((1, W, H, d), np.float32)
+    wv = np.zeros_like(wk)
+    wl, cl = np.zeros(1, np.int32), np.zeros(1, np.int32)
+    for t in range(T):
+        wk, wv, wl, cl = oracle.hybrid_append(D, S, K[t][None], V[t][None], wk, wv, wl, cl, bt, kp, vp)
+    return D, S, K, V, kp, vp, wk, wv, int(wl[0]), int(cl[0])
+
+
+def test_hybrid_append_keeps_the_last_window_tokens_and_compresses_the_rest():
+    # 40 tokens through a window of 12: the first 28 are compressed at their positions, byte for byte
+    # the records a direct encode of those tokens writes, and token p of the last 12 sits in slot p mod 12
+    d, H, W, T = 128, 2, 12, 40
+    bt = np.array([[5, 1, 3]], np.int32)
+    D, S, K, V, kp, vp, wk, wv, wl, cl = _hybrid_run(d, H, W, T, bt)
+    assert (cl, wl) == (T - W, W)
+    for p in range(T - W, T):
+        assert np.array_equal(wk[0, p % W], K[p]) and np.array_equal(wv[0, p % W], V[p])
+    kd, vd = np.zeros_like(kp), np.zeros_like(vp)
+    slots = synth.slots_for(bt, 0, 0, T - W)
+    oracle.encode(True, D, S, K[:T - W], slots, kd)
+    oracle.encode(False, D, S, V[:T - W], slots, vd)
+    assert np.array_equal(kp, kd) and np.array_equal(vp, vd)
+
+
+def test_hybrid_append_fills_the_window_before_compressing():
+    d, H, W, T = 128, 1, 8, 5
+    bt = np.array([[0]], np.int32)
+    _, _, K, _, kp, vp, wk, _, wl, cl = _hybrid_run(d, H, W, T, bt)
+    assert (cl, wl) == (0, T)
+    assert np.array_equal(wk[0, :T], K) and not kp.any() and not vp.any()
+
+
+def test_hybrid_append_attends_the_whole_sequence_while_it_fits_the_window():
+    # no token has left the window: hybrid attention is the textbook softmax over all T tokens
+    d, H, W, T = 128, 2, 16, 11
+    bt = np.array([[0]], np.int32)
+    D, S, K, V, kp, vp, wk, wv, wl, cl = _hybrid_run(d, H, W, T, bt, seed=3)
+    q = np.random.default_rng(4).standard_normal((1, 2 * H, d))
+    out = oracle.decode_hybrid(D, S, q, H, kp, vp, bt, np.array([cl]), wk, wv, np.array([wl]))
+    for h in range(2 * H):
+        s = K[:, h // 2].astype(np.float64) @ q[0, h] / np.sqrt(d)
+        p = np.exp(s - s.max())
+        ref = (p[:, None] * V[:, h // 2]).sum(0) / p.sum()
+        assert np.max(np.abs(out[0, h] - ref)) < 1e-12
+
+
+def test_hybrid_append_leaves_a_state_it_does_not_produce():
+    # a window that is not full while the history length is not a multiple of the window
+    d, H, W = 128, 1, 4
+    D, S = synth.rotation_signs(d), synth.qjl_matrix(d)
+    kp = np.zeros((2, H, oracle.record_bytes(True, d)), np.uint8)
+    vp = np.zeros((2, H, oracle.record_bytes(False, d)), np.uint8)
+    wk = np.ones((1, W, H, d), np.float32)
+    x = np.full((1, H, d), 2.0, np.float32)
+    wk2, _, wl, cl = oracle.hybrid_append(D, S, x, x, wk, wk, np.array([1], np.int32), np.array([3], np.int32),
+                                          np.array([[0]], np.int32), kp, vp)
+    assert np.array_equal(wk2, wk) and (int(wl[0]), int(cl[0])) == (1, 3) and not kp.any()

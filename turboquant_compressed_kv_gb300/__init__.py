@@ -100,6 +100,11 @@ def _declare(L):
     L.tq_decode_attn_hybrid.restype = _I
     L.tq_decode_attn_hybrid.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _I, _I, _P,
                                         _P, _P, _SZ, _P, _P]
+    L.tq_hybrid_append_scratch_bytes.restype = _SZ
+    L.tq_hybrid_append_scratch_bytes.argtypes = [_I, _I, _I, _I]
+    L.tq_hybrid_append.restype = _I
+    L.tq_hybrid_append.argtypes = [_P, _I, _P, _P, _I, _I, _I, _P, _P, _I, _P, _P, _I, _P, _P, _P, _I64, _P, _SZ,
+                                   _P, _P]
     L.tq_decode_attn_noalloc.restype = _I
     L.tq_decode_attn_noalloc.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _P]
     L.tq_gq_record_bytes.restype = _SZ
@@ -340,6 +345,27 @@ def decode_attn_hybrid(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block
                                               _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
     _check(rc, "tq_decode_attn_hybrid")
     return out
+
+
+def hybrid_append(params, d: int, k_new, v_new, win_k, win_v, win_lens, block_table, ctx_lens, k_pool, v_pool,
+                  scratch=None, status=None, stream=None):
+    """tq_hybrid_append: k_new / v_new [batch][n_kv_heads][d] into the window win_k / win_v
+    [batch][win_cap][n_kv_heads][d] (same dtype); a full window first moves its oldest token into
+    the paged pools at history position ctx_lens[b].  win_lens and ctx_lens are updated in place."""
+    torch = _torch()
+    _need_cuda(params, k_new, v_new, win_k, win_v, win_lens, block_table, ctx_lens, k_pool, v_pool, scratch, status)
+    B, H = k_new.shape[0], k_new.shape[1]
+    if _dtype_code(k_new) != _dtype_code(win_k):
+        raise TQError("hybrid_append: the new rows and the window must have the same dtype")
+    need = int(load_library().tq_hybrid_append_scratch_bytes(d, B, H, _dtype_code(k_new)))
+    if scratch is None:
+        scratch = torch.empty(max(need, 16), dtype=torch.uint8, device=k_new.device)
+    rc = load_library().tq_hybrid_append(_ptr(params), d, _ptr(k_new), _ptr(v_new), _dtype_code(k_new), B, H,
+                                         _ptr(win_k), _ptr(win_v), win_k.shape[1], _ptr(win_lens), _ptr(block_table),
+                                         block_table.shape[1], _ptr(ctx_lens), _ptr(k_pool), _ptr(v_pool),
+                                         k_pool.shape[0], _ptr(scratch), scratch.numel(), _ptr(status),
+                                         _stream(stream))
+    _check(rc, "tq_hybrid_append")
 
 
 def decode_attn_mq(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens, max_ctx: int,

@@ -258,6 +258,32 @@ int tq_decode_attn_mq(const void *params, int d, const void *q, int dtype, int b
 
 static size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+size_t tq_hybrid_append_scratch_bytes(int d, int batch, int n_kv_heads, int dtype) {
+    if (!valid_d(d) || batch < 0 || n_kv_heads <= 0) return 0;
+    if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16) return 0;
+    return hybrid_append_scratch_bytes(d, batch, n_kv_heads, dtype);
+}
+
+int tq_hybrid_append(const void *params, int d, const void *k_new, const void *v_new, int dtype, int batch,
+                     int n_kv_heads, void *win_k, void *win_v, int win_cap, int32_t *win_lens,
+                     const int32_t *block_table, int max_blocks, int32_t *ctx_lens, void *k_pool, void *v_pool,
+                     int64_t num_blocks, void *scratch, size_t scratch_bytes, int32_t *status, tq_stream_t stream) {
+    if (!valid_d(d)) return TQ_ERR_HEAD_DIM;
+    if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16) return TQ_ERR_DTYPE;
+    if (batch < 0 || n_kv_heads <= 0 || win_cap <= 0 || max_blocks <= 0 || num_blocks < 0) return TQ_ERR_INVALID;
+    if (batch == 0) return TQ_OK;
+    if (!params || !k_new || !v_new || !win_k || !win_v || !win_lens || !block_table || !ctx_lens || !k_pool ||
+        !v_pool || !scratch)
+        return TQ_ERR_INVALID;
+    if (!aligned16(params) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(win_k) || !aligned16(win_v) ||
+        !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(scratch))
+        return TQ_ERR_ALIGN;
+    if (scratch_bytes < hybrid_append_scratch_bytes(d, batch, n_kv_heads, dtype)) return TQ_ERR_WORKSPACE;
+    return cuda_status(launch_hybrid_append(d, dtype, params, k_new, v_new, batch, n_kv_heads, win_k, win_v, win_cap,
+                                            win_lens, block_table, max_blocks, ctx_lens, k_pool, v_pool, num_blocks,
+                                            scratch, status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t tq_decode_workspace_bytes_hybrid(int d, int batch, int n_q_heads, int max_ctx, int win_cap) {
     const size_t base = decode_workspace_bytes(d, batch, n_q_heads, max_ctx);
     if (base == 0 || win_cap < 0) return 0;

@@ -256,7 +256,93 @@ cudaError_t window_dtypes(int q_dtype, int w_dtype, int G, const void *q, const 
                : window_any<D, float, float>(G, q, wk, wv, batch, hq, hkv, win_cap, win_lens, nchunk, part, st);
 }
 
+// ---------------------------------------------------------------- window upkeep
+// The window is a ring keyed by position: token p of a sequence sits in window slot p mod win_cap
+// while it is uncompressed.  Tokens 0 .. ctx - 1 are in the compressed history, ctx .. ctx + wl - 1
+// in the window.  The window fills first (ctx = 0, slots 0 .. wl - 1); once it is full, every
+// appended token pushes the oldest one, position ctx in slot ctx mod win_cap, into the history.
+// A state is valid when 0 <= wl <= win_cap, ctx >= 0 and, unless the window is full,
+// ctx mod win_cap = 0 (so that the window's slots are 0 .. wl - 1, the ones attention reads).
+
+// 16-byte copy of n bytes (n a multiple of 16) by the CTA's threads
+__device__ __forceinline__ void copy16(uint8_t *__restrict__ dst, const uint8_t *__restrict__ src, size_t n) {
+    for (size_t i = threadIdx.x; i < n / 16; i += blockDim.x)
+        reinterpret_cast<uint4 *>(dst)[i] = reinterpret_cast<const uint4 *>(src)[i];
+}
+
+__device__ __forceinline__ bool window_state_ok(int ctx, int wl, int win_cap) {
+    return ctx >= 0 && wl >= 0 && wl <= win_cap && (wl == win_cap || ctx % win_cap == 0);
+}
+
+// One CTA per sequence: the rows of a full window's oldest token (all kv heads) into ek / ev, and
+// its position into epos (-1: nothing leaves the window).
+__global__ void __launch_bounds__(128)
+window_evict_kernel(const uint8_t *__restrict__ win_k, const uint8_t *__restrict__ win_v, size_t tok_bytes,
+                    int win_cap, const int32_t *__restrict__ ctx_lens, const int32_t *__restrict__ win_lens,
+                    uint8_t *__restrict__ ek, uint8_t *__restrict__ ev, int32_t *__restrict__ epos, int32_t *status) {
+    const int b = blockIdx.x;
+    const int ctx = ctx_lens[b], wl = win_lens[b];
+    const bool ok = window_state_ok(ctx, wl, win_cap), evict = ok && wl == win_cap;
+    if (threadIdx.x == 0) {
+        epos[b] = evict ? ctx : -1;
+        if (!ok) flag_status(status, TQ_STATUS_BAD_SLOT);
+    }
+    if (!evict) return;
+    const size_t src = ((size_t)b * win_cap + ctx % win_cap) * tok_bytes;
+    copy16(ek + (size_t)b * tok_bytes, win_k + src, tok_bytes);
+    copy16(ev + (size_t)b * tok_bytes, win_v + src, tok_bytes);
+}
+
+// One CTA per sequence: the new token's rows into its window slot, then the lengths.
+__global__ void __launch_bounds__(128)
+window_write_kernel(const uint8_t *__restrict__ k_new, const uint8_t *__restrict__ v_new, size_t tok_bytes,
+                    int win_cap, uint8_t *__restrict__ win_k, uint8_t *__restrict__ win_v, int32_t *ctx_lens,
+                    int32_t *win_lens) {
+    const int b = blockIdx.x;
+    const int ctx = ctx_lens[b], wl = win_lens[b];
+    if (!window_state_ok(ctx, wl, win_cap)) return;   // flagged by window_evict_kernel
+    const bool full = wl == win_cap;
+    const int slot = full ? ctx % win_cap : wl;
+    const size_t dst = ((size_t)b * win_cap + slot) * tok_bytes;
+    copy16(win_k + dst, k_new + (size_t)b * tok_bytes, tok_bytes);
+    copy16(win_v + dst, v_new + (size_t)b * tok_bytes, tok_bytes);
+    __syncthreads();   // every thread has read ctx and wl
+    if (threadIdx.x == 0) {
+        ctx_lens[b] = ctx + (full ? 1 : 0);
+        win_lens[b] = full ? win_cap : wl + 1;
+    }
+}
+
+size_t round16(size_t n) { return (n + 15) / 16 * 16; }
+
 }  // namespace
+
+size_t hybrid_append_scratch_bytes(int d, int batch, int hkv, int dtype) {
+    const size_t tok = (size_t)hkv * d * (dtype == TQ_DTYPE_BF16 ? 2 : 4);
+    return round16((size_t)batch * sizeof(int32_t)) + 2 * round16((size_t)batch * tok);
+}
+
+cudaError_t launch_hybrid_append(int d, int dtype, const void *params, const void *k_new, const void *v_new, int batch,
+                                 int hkv, void *win_k, void *win_v, int win_cap, int32_t *win_lens,
+                                 const int32_t *block_table, int max_blocks, int32_t *ctx_lens, void *k_pool,
+                                 void *v_pool, int64_t num_blocks, void *scratch, int32_t *status, cudaStream_t st) {
+    const size_t tok = (size_t)hkv * d * (dtype == TQ_DTYPE_BF16 ? 2 : 4);
+    uint8_t *sc = static_cast<uint8_t *>(scratch);
+    int32_t *epos = reinterpret_cast<int32_t *>(sc);
+    uint8_t *ek = sc + round16((size_t)batch * sizeof(int32_t)), *ev = ek + round16((size_t)batch * tok);
+    window_evict_kernel<<<batch, 128, 0, st>>>(static_cast<const uint8_t *>(win_k), static_cast<const uint8_t *>(win_v),
+                                               tok, win_cap, ctx_lens, win_lens, ek, ev, epos, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // the leaving tokens go into the history at their positions (sequences with epos < 0 are skipped)
+    e = launch_append(d, dtype, params, ek, ev, batch, hkv, block_table, max_blocks, epos, k_pool, v_pool, num_blocks,
+                      status, st);
+    if (e != cudaSuccess) return e;
+    window_write_kernel<<<batch, 128, 0, st>>>(static_cast<const uint8_t *>(k_new), static_cast<const uint8_t *>(v_new),
+                                               tok, win_cap, static_cast<uint8_t *>(win_k),
+                                               static_cast<uint8_t *>(win_v), ctx_lens, win_lens);
+    return cudaGetLastError();
+}
 
 int hybrid_nchunk(int d, int win_cap) {
     const int cw = d == 128 ? win_chunk<128>() : win_chunk<256>();

@@ -318,6 +318,13 @@ size_t hybrid_part_bytes(int d, int batch, int hq, int win_cap);
 cudaError_t launch_hybrid_window(int d, int q_dtype, int w_dtype, const void *q, const void *wk, const void *wv,
                                  int batch, int hq, int hkv, int win_cap, const int32_t *win_lens, float *part,
                                  float *out, const float *lse, cudaStream_t st);
+// Window upkeep of the hybrid cache (tq_hybrid.cu): a full window's oldest token into the paged
+// history, then the new token into the window; lengths updated on the device.
+size_t hybrid_append_scratch_bytes(int d, int batch, int hkv, int dtype);
+cudaError_t launch_hybrid_append(int d, int dtype, const void *params, const void *k_new, const void *v_new, int batch,
+                                 int hkv, void *win_k, void *win_v, int win_cap, int32_t *win_lens,
+                                 const int32_t *block_table, int max_blocks, int32_t *ctx_lens, void *k_pool,
+                                 void *v_pool, int64_t num_blocks, void *scratch, int32_t *status, cudaStream_t st);
 // Decode launches take q_len queries per sequence (q[b][i][h], out[b][i][h]); query i attends
 // the first L - (q_len - 1 - i) of the sequence's L attended tokens.  The workspace is laid
 // out for batch sequences of q_len * hq query rows.
