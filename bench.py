@@ -536,6 +536,30 @@ def extra_hybrid(steps, warmup, dev, history=30720, window=2048):
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in the hybrid decode")
     ms = e0.elapsed_time(e1) / steps
+    # the window upkeep (tq_hybrid_append): every call finds the windows full, moves each sequence's
+    # oldest window token into the compressed history and writes a new token.  The history restarts
+    # 256 tokens short of the table's end so that every moved token has a block.
+    usteps = min(steps, 200)
+    kn = torch.randn((B, Hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    vn = torch.randn((B, Hkv, d), generator=g, device=dev).to(torch.bfloat16)
+    uctx = torch.full((B,), history - 256, dtype=torch.int32, device=dev)
+    uwl = torch.full((B,), window, dtype=torch.int32, device=dev)
+    scratch = torch.empty(int(tq.load_library().tq_hybrid_append_scratch_bytes(d, B, Hkv, tq.DTYPE_BF16)),
+                          dtype=torch.uint8, device=dev)
+    kp0, vp0, wk0, wv0 = sets[0]
+    for _ in range(min(warmup, 10)):
+        tq.hybrid_append(cache.params, d, kn, vn, wk0, wv0, uwl, cache.block_table, uctx, kp0, vp0, scratch=scratch,
+                         status=status)
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    u0.record(stream)
+    for _ in range(usteps):
+        tq.hybrid_append(cache.params, d, kn, vn, wk0, wv0, uwl, cache.block_table, uctx, kp0, vp0, scratch=scratch,
+                         status=status)
+    u1.record(stream)
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the hybrid upkeep")
+    ums = u0.elapsed_time(u1) / usteps
     nb = step_bytes(w)
     win_b = 2 * B * window * Hkv * d * 2
     step_b = nb["partial"] + win_b + nb["q"] + nb["out"]
@@ -544,7 +568,11 @@ def extra_hybrid(steps, warmup, dev, history=30720, window=2048):
                       "l2": f"{nrep} copies of cache and window cycled ({nrep * per_cache / 2**20:.0f} MiB > L2)"},
            "value": round(step_b / (ms * 1e-3) / 1e9, 3), "unit": "GB/s", "ms_per_step": round(ms, 6),
            "bytes_per_step": {"compressed": nb["partial"], "window": win_b},
-           "steps": steps, "warmup": warmup, "launches_per_step": 4}
+           "steps": steps, "warmup": warmup, "launches_per_step": 4,
+           "upkeep": {"call": "tq_hybrid_append", "us_per_call": round(ums * 1e3, 3), "calls": usteps,
+                      "launches_per_call": 3,
+                      "per_call": f"{B * Hkv} K and {B * Hkv} V vectors leave the windows and are encoded; "
+                                  f"{B} new tokens written"}}
     del sets, cache
     torch.cuda.empty_cache()
     return res
