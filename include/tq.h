@@ -314,6 +314,15 @@ int tq_hybrid_append(const void *params, int d, const void *k_new, const void *v
                      const int32_t *block_table, int max_blocks, int32_t *ctx_lens, void *k_pool, void *v_pool,
                      int64_t num_blocks, void *scratch, size_t scratch_bytes, int32_t *status, tq_stream_t stream);
 
+/* tq_selftest_wait_timeout -- check of the library's bounded device waits.  The pages have no
+ * counterpart to this call.  The bulk encode and dequantisation kernels wait on mbarriers for
+ * their tile copies and tensor-core results; every such wait gives up after about 0.5 s, sets
+ * TQ_STATUS_TIMEOUT and lets the kernel finish, so a lost arrival can never hang the GPU.  This
+ * call launches one CTA that runs the same wait on an mbarrier nothing arrives at: after about
+ * 0.5 s it ORs TQ_STATUS_TIMEOUT into the device word *status (required) and exits normally.
+ * Errors: TQ_ERR_INVALID (status NULL), TQ_ERR_CUDA. */
+int tq_selftest_wait_timeout(int32_t *status, tq_stream_t stream);
+
 /* tq_decode_attn_noalloc -- tq_decode_attn without a caller workspace.
  * The pages have no counterpart to this call; it exists for callers that
  * cannot allocate device memory when they decode: a serving runtime that

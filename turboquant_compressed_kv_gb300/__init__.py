@@ -24,6 +24,7 @@ DTYPE_F32 = 0
 DTYPE_BF16 = 1
 STATUS_BAD_SLOT = 1
 STATUS_BAD_PARAMS = 2
+STATUS_TIMEOUT = 4
 
 _lib = None
 
@@ -100,6 +101,8 @@ def _declare(L):
     L.tq_decode_attn_hybrid.restype = _I
     L.tq_decode_attn_hybrid.argtypes = [_P, _I, _P, _I, _I, _I, _I, _P, _P, _I64, _P, _I, _P, _I, _P, _P, _I, _I, _P,
                                         _P, _P, _SZ, _P, _P]
+    L.tq_selftest_wait_timeout.restype = _I
+    L.tq_selftest_wait_timeout.argtypes = [_P, _P]
     L.tq_hybrid_append_scratch_bytes.restype = _SZ
     L.tq_hybrid_append_scratch_bytes.argtypes = [_I, _I, _I, _I]
     L.tq_hybrid_append.restype = _I
@@ -345,6 +348,12 @@ def decode_attn_hybrid(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block
                                               _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
     _check(rc, "tq_decode_attn_hybrid")
     return out
+
+
+def selftest_wait_timeout(status, stream=None):
+    """tq_selftest_wait_timeout: one bounded wait that runs out; ORs STATUS_TIMEOUT into status."""
+    _need_cuda(status)
+    _check(load_library().tq_selftest_wait_timeout(_ptr(status), _stream(stream)), "tq_selftest_wait_timeout")
 
 
 def hybrid_append(params, d: int, k_new, v_new, win_k, win_v, win_lens, block_table, ctx_lens, k_pool, v_pool,

@@ -258,6 +258,11 @@ int tq_decode_attn_mq(const void *params, int d, const void *q, int dtype, int b
 
 static size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+int tq_selftest_wait_timeout(int32_t *status, tq_stream_t stream) {
+    if (!status) return TQ_ERR_INVALID;
+    return cuda_status(launch_wait_timeout_selftest(status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t tq_hybrid_append_scratch_bytes(int d, int batch, int n_kv_heads, int dtype) {
     if (!valid_d(d) || batch < 0 || n_kv_heads <= 0) return 0;
     if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16) return 0;

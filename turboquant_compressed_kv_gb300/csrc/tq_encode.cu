@@ -670,6 +670,24 @@ cudaError_t launch_any(int d, int dtype, const void *params, const void *xk, con
 
 }  // namespace
 
+// Self-test of the bounded device waits: one CTA waits on an mbarrier that nothing arrives at,
+// with the same bounded wait the encode and dequant kernels use; the wait gives up after its
+// limit and the CTA reports TQ_STATUS_TIMEOUT, leaving the context usable.
+namespace {
+__global__ void wait_timeout_selftest_kernel(int32_t *status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) tc::mbar_init(&bar, 1);
+    __syncthreads();
+    const bool done = tc::mbar_wait(&bar, 0);   // phase 0 never completes
+    if (!done && threadIdx.x == 0) flag_status(status, TQ_STATUS_TIMEOUT);
+}
+}  // namespace
+
+cudaError_t launch_wait_timeout_selftest(int32_t *status, cudaStream_t st) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const void *x, int64_t n_tokens,
                           int n_heads, const int64_t *slots, void *pool, int64_t num_blocks, int32_t *status,
                           cudaStream_t st) {

@@ -318,6 +318,8 @@ size_t hybrid_part_bytes(int d, int batch, int hq, int win_cap);
 cudaError_t launch_hybrid_window(int d, int q_dtype, int w_dtype, const void *q, const void *wk, const void *wv,
                                  int batch, int hq, int hkv, int win_cap, const int32_t *win_lens, float *part,
                                  float *out, const float *lse, cudaStream_t st);
+// One CTA whose bounded mbarrier wait runs out (tq_encode.cu): sets TQ_STATUS_TIMEOUT.
+cudaError_t launch_wait_timeout_selftest(int32_t *status, cudaStream_t st);
 // Window upkeep of the hybrid cache (tq_hybrid.cu): a full window's oldest token into the paged
 // history, then the new token into the window; lengths updated on the device.
 size_t hybrid_append_scratch_bytes(int d, int batch, int hkv, int dtype);
