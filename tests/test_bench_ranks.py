@@ -57,3 +57,21 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     args = type("A", (), {"steps": 1, "warmup": 0, "gpus": 2})()
     assert bench.bench_reference(args) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_keeps_the_contract(monkeypatch, capsys):
+    # rank 0 prints one JSON line with the keys the driver reads, on the main workload's metric
+    import json
+    monkeypatch.setenv("RANK", "0")
+    args = type("A", (), {"steps": 1, "warmup": 0, "gpus": 1})()
+    assert bench.bench_reference(args) == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC and line["unit"] == "GB/s"
+    assert line["config"]["workload"] == bench.WORKLOAD and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
