@@ -396,7 +396,10 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
     using namespace dq128v;
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint64_t recbar[2];
-    __shared__ float s_cent[8], s_D[D];
+    __shared__ float s_D[D];
+    // centroid pairs (x 1/sqrt d) of two neighbouring coordinates, by the 6-bit index
+    // a | b << 2 | c << 4, where a, b, c hold the two coordinates' bits of planes 0, 1, 2
+    __shared__ float2 s_pair[64];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     if (ph->magic != kParamsMagic || ph->d != D) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
@@ -410,7 +413,11 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
         tc::mbar_init(&recbar[1], 1);
     }
     const float inv_sd = rsqrtf((float)D);
-    if (row < 8) s_cent[row] = ph->centroid[row] * inv_sd;
+    if (row < 64) {
+        const int a = row & 3, b = (row >> 2) & 3, c = row >> 4;
+        const int lo = (a & 1) | ((b & 1) << 1) | ((c & 1) << 2), hi = (a >> 1) | ((b >> 1) << 1) | ((c >> 1) << 2);
+        s_pair[row] = make_float2(ph->centroid[lo] * inv_sd, ph->centroid[hi] * inv_sd);
+    }
     s_D[row] = reinterpret_cast<const float *>(params + params_off_D(D))[row];
     tc::fence_before_sync();
     __syncthreads();
@@ -453,18 +460,26 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
         // coordinate n = 16 mt + r of slot t: word 2 (4 (r & 7) + (t & 7) / 2) + (r >> 3) of each
         // plane, bit 8 (t >> 3) + 16 (t & 1) + mt
         constexpr int PW = 2 * D / 4;   // words per plane
-        const int a = (t & 7) >> 1, sh = 8 * (t >> 3) + 16 * (t & 1);
+        const int a = (t & 7) >> 1, bi = (t >> 3) + 2 * (t & 1);   // the slot's byte in each plane word
+        // byte bi of planes 0 and 1 into bytes 0 and 1, then byte bi of plane 2 into byte 2
+        const uint32_t sel01 = (uint32_t)bi | ((uint32_t)(4 + bi) << 4), sel2 = 0x10u | ((uint32_t)(4 + bi) << 8);
         float y[D];
 #pragma unroll
         for (int c = 0; c < 8; ++c)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int word = 2 * (4 * c + a) + h;
-                const uint32_t w0 = planes[word] >> sh, w1 = planes[PW + word] >> sh, w2 = planes[2 * PW + word] >> sh;
+                const uint32_t x = __byte_perm(__byte_perm(planes[word], planes[PW + word], sel01),
+                                               planes[2 * PW + word], sel2);
 #pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    const uint32_t cell = ((w0 >> mt) & 1u) | (((w1 >> mt) & 1u) << 1) | (((w2 >> mt) & 1u) << 2);
-                    y[16 * mt + 8 * h + c] = s_cent[cell];
+                for (int mt = 0; mt < 8; mt += 2) {
+                    // bits mt, mt + 1 of the three bytes; the multiply by 4161 = 2^12 + 2^6 + 1 lines
+                    // the three 2-bit fields up in bits 12 + mt .. 17 + mt without carries
+                    const uint32_t v = x & (0x030303u << mt);
+                    const uint32_t idx = (v * 4161u >> (12 + mt)) & 63u;
+                    const float2 cc = s_pair[idx];
+                    y[16 * mt + 8 * h + c] = cc.x;
+                    y[16 * (mt + 1) + 8 * h + c] = cc.y;
                 }
             }
         const __half nh = *reinterpret_cast<const __half *>(rec + 6 * D + 2 * t);
