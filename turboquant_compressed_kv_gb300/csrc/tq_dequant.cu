@@ -189,7 +189,10 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint64_t recbar[kWg][2], mmabar[kWg];
     __shared__ uint32_t tmem_base;
-    __shared__ float s_cent[8], s_D[D];
+    __shared__ float s_D[D];
+    // centroid pairs (x 1/sqrt d) of two coordinates, by the 6-bit index a | b << 2 | c << 4,
+    // where a, b, c hold the two coordinates' bits of planes 0, 1, 2
+    __shared__ float2 s_pair[64];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     if (ph->magic != kParamsMagic || ph->d != D) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
@@ -207,7 +210,12 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     }
     constexpr uint32_t kTmemCols = kWg <= 2 ? 256 : 512;   // 128 columns per warpgroup, a power of two
     if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
-    if (tid < 8) s_cent[tid] = ph->centroid[tid];
+    if (tid < 64) {
+        const int a = tid & 3, b = (tid >> 2) & 3, c = tid >> 4;
+        const int lo = (a & 1) | ((b & 1) << 1) | ((c & 1) << 2), hi = (a >> 1) | ((b >> 1) << 1) | ((c >> 1) << 2);
+        const float isd = rsqrtf((float)D);
+        s_pair[tid] = make_float2(ph->centroid[lo] * isd, ph->centroid[hi] * isd);
+    }
     if (tid < D) s_D[tid] = reinterpret_cast<const float *>(params + params_off_D(D))[tid];
     {   // B: row n = output coordinate n, K index k' as in the A operand; S as f16 hi + lo
         const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
@@ -330,13 +338,24 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
         }
         tc::fence_before_sync();
         const float gq = qjl * gam;
+        // byte j of plane word tig holds bits s = 0..7 of coordinates 16 s + 8 (j & 1) + 2 tig + (j >> 1);
+        // the three planes' bytes side by side, then two coordinates per table lookup (the multiply
+        // by 4161 = 2^12 + 2^6 + 1 lines the three 2-bit fields up in bits 12 + s .. 17 + s)
 #pragma unroll
-        for (int n = 0; n < D; ++n) {
-            const int tig = (n >> 1) & 3, e = n & 1, h = (n >> 3) & 1, s = n >> 4, bit = 8 * h + s + 16 * e;
-            const int cell = (int)((cw[0][tig] >> bit) & 1u) | (int)(((cw[1][tig] >> bit) & 1u) << 1) |
-                             (int)(((cw[2][tig] >> bit) & 1u) << 2);
-            y[n] = fmaf(gq, y[n], s_cent[cell] * inv_sd);
-        }
+        for (int tig = 0; tig < 4; ++tig)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t x = __byte_perm(__byte_perm(cw[0][tig], cw[1][tig], (uint32_t)j | ((uint32_t)(4 + j) << 4)),
+                                               cw[2][tig], 0x10u | ((uint32_t)(4 + j) << 8));
+                const int base = 8 * (j & 1) + 2 * tig + (j >> 1);
+#pragma unroll
+                for (int s2 = 0; s2 < 8; s2 += 2) {
+                    const uint32_t v = x & (0x030303u << s2);
+                    const float2 cc = s_pair[(v * 4161u >> (12 + s2)) & 63u];
+                    y[16 * s2 + base] = fmaf(gq, y[16 * s2 + base], cc.x);
+                    y[16 * (s2 + 1) + base] = fmaf(gq, y[16 * (s2 + 1) + base], cc.y);
+                }
+            }
         // inverse rotation: D (H y) / sqrt d, then the norm
 #pragma unroll
         for (int st = 1; st < D; st <<= 1)
