@@ -191,8 +191,9 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     __shared__ uint32_t tmem_base;
     __shared__ float s_D[D];
     // centroid pairs (x 1/sqrt d) of two coordinates, by the 6-bit index a | b << 2 | c << 4,
-    // where a, b, c hold the two coordinates' bits of planes 0, 1, 2
-    __shared__ float2 s_pair[64];
+    // where a, b, c hold the two coordinates' bits of planes 0, 1, 2; one copy per lane
+    // ([index][lane]), so that a half-warp's lookups never share a bank
+    __shared__ float2 s_pair[64][32];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     if (ph->magic != kParamsMagic || ph->d != D) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
@@ -210,11 +211,11 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     }
     constexpr uint32_t kTmemCols = kWg <= 2 ? 256 : 512;   // 128 columns per warpgroup, a power of two
     if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
-    if (tid < 64) {
-        const int a = tid & 3, b = (tid >> 2) & 3, c = tid >> 4;
+    for (int e = tid; e < 64 * 32; e += kThreads) {
+        const int i = e >> 5, a = i & 3, b = (i >> 2) & 3, c = i >> 4;
         const int lo = (a & 1) | ((b & 1) << 1) | ((c & 1) << 2), hi = (a >> 1) | ((b >> 1) << 1) | ((c >> 1) << 2);
         const float isd = rsqrtf((float)D);
-        s_pair[tid] = make_float2(ph->centroid[lo] * isd, ph->centroid[hi] * isd);
+        s_pair[i][e & 31] = make_float2(ph->centroid[lo] * isd, ph->centroid[hi] * isd);
     }
     if (tid < D) s_D[tid] = reinterpret_cast<const float *>(params + params_off_D(D))[tid];
     {   // B: row n = output coordinate n, K index k' as in the A operand; S as f16 hi + lo
@@ -351,7 +352,7 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
 #pragma unroll
                 for (int s2 = 0; s2 < 8; s2 += 2) {
                     const uint32_t v = x & (0x030303u << s2);
-                    const float2 cc = s_pair[(v * 4161u >> (12 + s2)) & 63u];
+                    const float2 cc = s_pair[(v * 4161u >> (12 + s2)) & 63u][tid & 31];
                     y[16 * s2 + base] = fmaf(gq, y[16 * s2 + base], cc.x);
                     y[16 * (s2 + 1) + base] = fmaf(gq, y[16 * (s2 + 1) + base], cc.y);
                 }
@@ -417,8 +418,9 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
     __shared__ uint64_t recbar[2];
     __shared__ float s_D[D];
     // centroid pairs (x 1/sqrt d) of two neighbouring coordinates, by the 6-bit index
-    // a | b << 2 | c << 4, where a, b, c hold the two coordinates' bits of planes 0, 1, 2
-    __shared__ float2 s_pair[64];
+    // a | b << 2 | c << 4, where a, b, c hold the two coordinates' bits of planes 0, 1, 2; one copy
+    // per lane ([index][lane]), so that a half-warp's lookups never share a bank
+    __shared__ float2 s_pair[64][32];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     if (ph->magic != kParamsMagic || ph->d != D) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
@@ -432,11 +434,12 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
         tc::mbar_init(&recbar[1], 1);
     }
     const float inv_sd = rsqrtf((float)D);
-    if (row < 64) {
-        const int a = row & 3, b = (row >> 2) & 3, c = row >> 4;
+    for (int e = row; e < 64 * 32; e += kThreads) {
+        const int i = e >> 5, a = i & 3, b = (i >> 2) & 3, c = i >> 4;
         const int lo = (a & 1) | ((b & 1) << 1) | ((c & 1) << 2), hi = (a >> 1) | ((b >> 1) << 1) | ((c >> 1) << 2);
-        s_pair[row] = make_float2(ph->centroid[lo] * inv_sd, ph->centroid[hi] * inv_sd);
+        s_pair[i][e & 31] = make_float2(ph->centroid[lo] * inv_sd, ph->centroid[hi] * inv_sd);
     }
+    const int lane = row & 31;
     s_D[row] = reinterpret_cast<const float *>(params + params_off_D(D))[row];
     tc::fence_before_sync();
     __syncthreads();
@@ -496,7 +499,7 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
                     // the three 2-bit fields up in bits 12 + mt .. 17 + mt without carries
                     const uint32_t v = x & (0x030303u << mt);
                     const uint32_t idx = (v * 4161u >> (12 + mt)) & 63u;
-                    const float2 cc = s_pair[idx];
+                    const float2 cc = s_pair[idx][lane];
                     y[16 * mt + 8 * h + c] = cc.x;
                     y[16 * (mt + 1) + 8 * h + c] = cc.y;
                 }
