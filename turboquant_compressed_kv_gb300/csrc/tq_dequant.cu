@@ -415,7 +415,7 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
                         int32_t *status) {
     using namespace dq128v;
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ uint64_t recbar[2];
+    __shared__ uint64_t recbar[2], recfree[2];
     __shared__ float s_D[D];
     // centroid pairs (x 1/sqrt d) of two neighbouring coordinates, by the 6-bit index
     // a | b << 2 | c << 4, where a, b, c hold the two coordinates' bits of planes 0, 1, 2; one copy
@@ -432,6 +432,8 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
     if (row == 0) {
         tc::mbar_init(&recbar[0], 1);
         tc::mbar_init(&recbar[1], 1);
+        tc::mbar_init(&recfree[0], kThreads / 32);   // one arrival per warp once its rows are read
+        tc::mbar_init(&recfree[1], kThreads / 32);
     }
     const float inv_sd = rsqrtf((float)D);
     for (int e = row; e < 64 * 32; e += kThreads) {
@@ -506,8 +508,16 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
             }
         const __half nh = *reinterpret_cast<const __half *>(rec + 6 * D + 2 * t);
         tc::fence_async_smem();
-        __syncthreads();   // every row of the buffer is read: it can take the tile two ahead
-        if (row == 0 && tile_of(i + 2) < ntiles) issue(i + 2, buf);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&recfree[buf]);   // this warp's rows of the buffer are read
+        // thread 0 refills the buffer with the tile two ahead once every warp has read it (after
+        // this tile's work, when they are long done; nobody else waits)
+        auto refill = [&]() {
+            if (row == 0 && tile_of(i + 2) < ntiles) {
+                if (!tc::mbar_wait(&recfree[buf], (i >> 1) & 1)) timed_out = true;
+                issue(i + 2, buf);
+            }
+        };
         // inverse rotation: D (H y) / sqrt d, then the norm
 #pragma unroll
         for (int st = 1; st < D; st <<= 1)
@@ -541,6 +551,7 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
                 }
             }
         }
+        refill();
     }
     if (timed_out) flag_status(status, TQ_STATUS_TIMEOUT);
 }
