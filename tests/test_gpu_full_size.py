@@ -107,3 +107,33 @@ def test_full_size_encode_sampled_parity():
     sk = parity.check_encode(True, cache.D, cache.S, xk, sl[pick], kp, pool_fill=0)
     sv = parity.check_encode(False, cache.D, cache.S, xv, sl[pick], vp, pool_fill=0)
     print(f"prefill encode, 512 tokens x {Hkv} heads: K {sk}, V {sv}")
+
+
+def test_full_size_dequant_sampled_parity():
+    """The prefill dequantisation at its full size (131,072 (block, kv head) records of each pool
+    back to bf16 and fp32), in the launch configuration the benchmark times: one tq_dequant_k and
+    one tq_dequant_v over every block of the cache; 64 sampled blocks (every slot and kv head) are
+    compared with the oracle's reconstruction of the same records read back from the device."""
+    w = synth.workload("prefill")
+    d, Hkv = w.head_dim, w.n_kv_heads
+    tq.load_library()
+    cache = PagedCache.create(w, DEV)
+    cache.prefill_device()
+    ids = torch.cat([cache.block_table[b, :w.prefill_lens[b] // 16] for b in range(w.batch)]).contiguous()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pick = np.sort(np.random.default_rng(13).choice(ids.numel(), 64, replace=False))
+    ids_np = ids.cpu().numpy()
+    for is_k, fn, pool in ((True, tq.dequant_k, cache.k_pool), (False, tq.dequant_v, cache.v_pool)):
+        pool_np = pool.cpu().numpy()
+        ref = oracle.dequant(is_k, cache.D, cache.S, pool_np, Hkv, ids_np[pick]).reshape(64, 16, Hkv, d)
+        for out_dtype, tol in ((torch.float32, None), (torch.bfloat16, 2.0 ** -8)):
+            o = fn(cache.params, d, pool, ids, out_dtype=out_dtype, status=status)
+            torch.cuda.synchronize()
+            assert int(status.item()) == 0
+            g = o.view(ids.numel(), 16, Hkv, d)[torch.from_numpy(pick).to(DEV)].float().cpu().numpy().astype(np.float64)
+            del o
+            if tol is None:
+                err = np.linalg.norm(g - ref, axis=-1) / np.maximum(np.linalg.norm(ref, axis=-1), 1e-30)
+                assert err.max() < 1e-5, (is_k, err.max())
+            else:   # one bf16 rounding of the exact value (plus the fp32 error above)
+                assert np.all(np.abs(g - ref) <= np.abs(ref) * tol + 1e-5 * np.linalg.norm(ref, axis=-1, keepdims=True)), is_k
