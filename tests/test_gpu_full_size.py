@@ -137,3 +137,36 @@ def test_full_size_dequant_sampled_parity():
                 assert err.max() < 1e-5, (is_k, err.max())
             else:   # one bf16 rounding of the exact value (plus the fp32 error above)
                 assert np.all(np.abs(g - ref) <= np.abs(ref) * tol + 1e-5 * np.linalg.norm(ref, axis=-1, keepdims=True)), is_k
+
+
+def test_full_size_hybrid_sampled_parity():
+    """Hybrid attention at the benchmark's size (16 sequences x 32/8 heads, d=128: 30720 compressed
+    tokens plus a 2048-row bf16 window each), in one tq_decode_attn_hybrid call; for two sampled
+    sequences (all 32 query heads) the oracle decodes the same packed records and window rows,
+    read back from the device."""
+    w0 = synth.workload("llama8b_decode")
+    history, window = 30720, 2048
+    w = dataclasses.replace(w0, ctx_lens=[history] * w0.batch, prefill_lens=[history] * w0.batch, append=False)
+    d, B, Hq, Hkv = w.head_dim, w.batch, w.n_q_heads, w.n_kv_heads
+    tq.load_library()
+    cache = PagedCache.create(w, DEV)
+    cache.prefill_device()
+    g = torch.Generator(device=DEV).manual_seed(99)
+    wk = torch.randn((B, window, Hkv, d), generator=g, device=DEV).to(torch.bfloat16)
+    wv = torch.randn((B, window, Hkv, d), generator=g, device=DEV).to(torch.bfloat16)
+    wl = torch.tensor([window - 3 * b for b in range(B)], dtype=torch.int32, device=DEV)   # some windows not full
+    q = synth.queries(w)
+    ctx = torch.tensor(w.ctx_lens, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = tq.decode_attn_hybrid(cache.params, d, to_device(q, w.dtype, DEV), Hkv, cache.k_pool, cache.v_pool,
+                                cache.block_table, ctx, history, wk, wv, wl, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o = out.cpu().numpy()
+    kp, vp = cache.k_pool.cpu().numpy(), cache.v_pool.cpu().numpy()
+    for b in (5, 14):
+        ref = oracle.decode_hybrid(cache.D, cache.S, q[b:b + 1], Hkv, kp, vp, cache.block_table_np[b:b + 1],
+                                   np.array([history], np.int32), wk[b:b + 1].float().cpu().numpy(),
+                                   wv[b:b + 1].float().cpu().numpy(), wl[b:b + 1].cpu().numpy())
+        worst = parity.check_attention(o[b:b + 1], ref)
+        print(f"hybrid sequence {b}: worst max-abs {worst[0]:.3e}, worst relative {worst[1]:.3e}")
