@@ -170,3 +170,38 @@ def test_full_size_hybrid_sampled_parity():
                                    wv[b:b + 1].float().cpu().numpy(), wl[b:b + 1].cpu().numpy())
         worst = parity.check_attention(o[b:b + 1], ref)
         print(f"hybrid sequence {b}: worst max-abs {worst[0]:.3e}, worst relative {worst[1]:.3e}")
+
+
+def test_full_size_verify_step_sampled_parity():
+    """The speculative-verify step at the benchmark's size (16 sequences x 32/8 heads, d=128, 4094
+    cached tokens, 2 draft tokens each) in one tq_decode_step_mq; for two sampled sequences, the
+    appended records are checked against the oracle's encode of the draft rows, and both causal
+    queries against the oracle's multi-query decode of the same packed cache."""
+    q_len = 2
+    w0 = synth.workload("llama8b_decode")
+    w = dataclasses.replace(w0, prefill_lens=[L - q_len for L in w0.ctx_lens])
+    d, B, Hq, Hkv = w.head_dim, w.batch, w.n_q_heads, w.n_kv_heads
+    tq.load_library()
+    cache = PagedCache.create(w, DEV)
+    cache.prefill_device()
+    g = torch.Generator(device=DEV).manual_seed(1234)
+    k_new = torch.randn((B, q_len, Hkv, d), generator=g, device=DEV).to(torch.bfloat16)
+    v_new = torch.randn((B, q_len, Hkv, d), generator=g, device=DEV).to(torch.bfloat16)
+    q = torch.randn((B, q_len, Hq, d), generator=g, device=DEV).to(torch.bfloat16)
+    pre = torch.tensor(w.prefill_lens, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = tq.decode_step_mq(cache.params, d, k_new, v_new, q, Hkv, cache.k_pool, cache.v_pool, cache.block_table,
+                            pre, max(w.ctx_lens), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    o = out.cpu().numpy()
+    kp, vp = cache.k_pool.cpu().numpy(), cache.v_pool.cpu().numpy()
+    for b in (2, 11):
+        P = w.prefill_lens[b]
+        slots = synth.slots_for(cache.block_table_np, b, P, q_len)
+        parity.check_encode(True, cache.D, cache.S, k_new[b].float().cpu().numpy(), slots, kp, pool_fill=0)
+        parity.check_encode(False, cache.D, cache.S, v_new[b].float().cpu().numpy(), slots, vp, pool_fill=0)
+        ref = oracle.decode_mq(cache.D, cache.S, q[b:b + 1].float().cpu().numpy(), Hkv, kp, vp,
+                               cache.block_table_np[b:b + 1], np.array([P + q_len], np.int32))
+        worst = parity.check_attention(o[b], ref[0])
+        print(f"verify sequence {b}: worst max-abs {worst[0]:.3e}, worst relative {worst[1]:.3e}")
