@@ -172,12 +172,13 @@ def test_full_size_hybrid_sampled_parity():
         print(f"hybrid sequence {b}: worst max-abs {worst[0]:.3e}, worst relative {worst[1]:.3e}")
 
 
-def test_full_size_verify_step_sampled_parity():
-    """The speculative-verify step at the benchmark's size (16 sequences x 32/8 heads, d=128, 4094
-    cached tokens, 2 draft tokens each) in one tq_decode_step_mq; for two sampled sequences, the
-    appended records are checked against the oracle's encode of the draft rows, and both causal
-    queries against the oracle's multi-query decode of the same packed cache."""
-    q_len = 2
+@pytest.mark.parametrize("q_len", [1, 2])
+def test_full_size_step_sampled_parity(q_len):
+    """The decode step at the benchmark's size (16 sequences x 32/8 heads, d=128, 4096 attended
+    tokens): q_len = 1 is the benchmark's step (tq_decode_step: append one token, attend), q_len = 2
+    the speculative-verify step (tq_decode_step_mq: append two draft tokens, two causal queries).
+    For two sampled sequences the appended records are checked against the oracle's encode of the
+    new rows, and the queries against the oracle's decode of the same packed cache."""
     w0 = synth.workload("llama8b_decode")
     w = dataclasses.replace(w0, prefill_lens=[L - q_len for L in w0.ctx_lens])
     d, B, Hq, Hkv = w.head_dim, w.batch, w.n_q_heads, w.n_kv_heads
@@ -190,8 +191,13 @@ def test_full_size_verify_step_sampled_parity():
     q = torch.randn((B, q_len, Hq, d), generator=g, device=DEV).to(torch.bfloat16)
     pre = torch.tensor(w.prefill_lens, dtype=torch.int32, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    out = tq.decode_step_mq(cache.params, d, k_new, v_new, q, Hkv, cache.k_pool, cache.v_pool, cache.block_table,
-                            pre, max(w.ctx_lens), status=status)
+    if q_len == 1:
+        out = tq.decode_step(cache.params, d, k_new[:, 0].contiguous(), v_new[:, 0].contiguous(),
+                             q[:, 0].contiguous(), Hkv, cache.k_pool, cache.v_pool, cache.block_table, pre,
+                             max(w.ctx_lens), status=status)[:, None]
+    else:
+        out = tq.decode_step_mq(cache.params, d, k_new, v_new, q, Hkv, cache.k_pool, cache.v_pool,
+                                cache.block_table, pre, max(w.ctx_lens), status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     o = out.cpu().numpy()
@@ -204,4 +210,4 @@ def test_full_size_verify_step_sampled_parity():
         ref = oracle.decode_mq(cache.D, cache.S, q[b:b + 1].float().cpu().numpy(), Hkv, kp, vp,
                                cache.block_table_np[b:b + 1], np.array([P + q_len], np.int32))
         worst = parity.check_attention(o[b], ref[0])
-        print(f"verify sequence {b}: worst max-abs {worst[0]:.3e}, worst relative {worst[1]:.3e}")
+        print(f"step (q_len {q_len}) sequence {b}: worst max-abs {worst[0]:.3e}, worst relative {worst[1]:.3e}")
