@@ -570,7 +570,7 @@ def extra_hybrid(steps, warmup, dev, history=30720, window=2048):
            "bytes_per_step": {"compressed": nb["partial"], "window": win_b},
            "steps": steps, "warmup": warmup, "launches_per_step": 4,
            "upkeep": {"call": "tq_hybrid_append", "us_per_call": round(ums * 1e3, 3), "calls": usteps,
-                      "launches_per_call": 3,
+                      "launches_per_call": 2,
                       "per_call": f"{B * Hkv} K and {B * Hkv} V vectors leave the windows and are encoded; "
                                   f"{B} new tokens written"}}
     del sets, cache

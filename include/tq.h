@@ -304,7 +304,8 @@ int tq_decode_attn_hybrid(const void *params, int d, const void *q, int dtype, i
  * ctx_lens < 0, or a window that is not full while ctx_lens[b] mod win_cap != 0) is left
  * unchanged and sets TQ_STATUS_BAD_SLOT; so does a history position without a valid block,
  * whose token is then dropped from the history while the window still advances.
- * Three launches on the stream (gather of the leaving rows, their encode, the window write).
+ * Two launches on the stream: the window step (the leaving rows copied to scratch, the new token
+ * written, the lengths updated), then the encode of the leaving rows.
  * Errors: TQ_ERR_HEAD_DIM, TQ_ERR_DTYPE, TQ_ERR_INVALID (win_cap <= 0 among others),
  * TQ_ERR_ALIGN (every buffer 16-byte aligned), TQ_ERR_WORKSPACE (scratch too small),
  * TQ_ERR_CUDA. */

@@ -274,39 +274,32 @@ __device__ __forceinline__ bool window_state_ok(int ctx, int wl, int win_cap) {
     return ctx >= 0 && wl >= 0 && wl <= win_cap && (wl == win_cap || ctx % win_cap == 0);
 }
 
-// One CTA per sequence: the rows of a full window's oldest token (all kv heads) into ek / ev, and
-// its position into epos (-1: nothing leaves the window).
+// One CTA per sequence: a full window's oldest token (all kv heads) is copied into ek / ev and its
+// position into epos (-1: nothing leaves the window); then the new token's rows go into its
+// window slot (the freed one when the window was full) and the lengths are updated.  The
+// encode of the leaving token reads ek / ev, so it may follow this kernel.
 __global__ void __launch_bounds__(128)
-window_evict_kernel(const uint8_t *__restrict__ win_k, const uint8_t *__restrict__ win_v, size_t tok_bytes,
-                    int win_cap, const int32_t *__restrict__ ctx_lens, const int32_t *__restrict__ win_lens,
-                    uint8_t *__restrict__ ek, uint8_t *__restrict__ ev, int32_t *__restrict__ epos, int32_t *status) {
+window_step_kernel(const uint8_t *__restrict__ k_new, const uint8_t *__restrict__ v_new, size_t tok_bytes,
+                   int win_cap, uint8_t *__restrict__ win_k, uint8_t *__restrict__ win_v, int32_t *ctx_lens,
+                   int32_t *win_lens, uint8_t *__restrict__ ek, uint8_t *__restrict__ ev, int32_t *__restrict__ epos,
+                   int32_t *status) {
     const int b = blockIdx.x;
     const int ctx = ctx_lens[b], wl = win_lens[b];
-    const bool ok = window_state_ok(ctx, wl, win_cap), evict = ok && wl == win_cap;
+    const bool ok = window_state_ok(ctx, wl, win_cap), full = ok && wl == win_cap;
     if (threadIdx.x == 0) {
-        epos[b] = evict ? ctx : -1;
+        epos[b] = full ? ctx : -1;
         if (!ok) flag_status(status, TQ_STATUS_BAD_SLOT);
     }
-    if (!evict) return;
-    const size_t src = ((size_t)b * win_cap + ctx % win_cap) * tok_bytes;
-    copy16(ek + (size_t)b * tok_bytes, win_k + src, tok_bytes);
-    copy16(ev + (size_t)b * tok_bytes, win_v + src, tok_bytes);
-}
-
-// One CTA per sequence: the new token's rows into its window slot, then the lengths.
-__global__ void __launch_bounds__(128)
-window_write_kernel(const uint8_t *__restrict__ k_new, const uint8_t *__restrict__ v_new, size_t tok_bytes,
-                    int win_cap, uint8_t *__restrict__ win_k, uint8_t *__restrict__ win_v, int32_t *ctx_lens,
-                    int32_t *win_lens) {
-    const int b = blockIdx.x;
-    const int ctx = ctx_lens[b], wl = win_lens[b];
-    if (!window_state_ok(ctx, wl, win_cap)) return;   // flagged by window_evict_kernel
-    const bool full = wl == win_cap;
+    if (!ok) return;   // a state this call does not produce is left as it is
     const int slot = full ? ctx % win_cap : wl;
-    const size_t dst = ((size_t)b * win_cap + slot) * tok_bytes;
-    copy16(win_k + dst, k_new + (size_t)b * tok_bytes, tok_bytes);
-    copy16(win_v + dst, v_new + (size_t)b * tok_bytes, tok_bytes);
-    __syncthreads();   // every thread has read ctx and wl
+    const size_t at = ((size_t)b * win_cap + slot) * tok_bytes;
+    if (full) {
+        copy16(ek + (size_t)b * tok_bytes, win_k + at, tok_bytes);
+        copy16(ev + (size_t)b * tok_bytes, win_v + at, tok_bytes);
+    }
+    __syncthreads();   // the leaving rows are copied (and every thread has read ctx and wl)
+    copy16(win_k + at, k_new + (size_t)b * tok_bytes, tok_bytes);
+    copy16(win_v + at, v_new + (size_t)b * tok_bytes, tok_bytes);
     if (threadIdx.x == 0) {
         ctx_lens[b] = ctx + (full ? 1 : 0);
         win_lens[b] = full ? win_cap : wl + 1;
@@ -330,18 +323,14 @@ cudaError_t launch_hybrid_append(int d, int dtype, const void *params, const voi
     uint8_t *sc = static_cast<uint8_t *>(scratch);
     int32_t *epos = reinterpret_cast<int32_t *>(sc);
     uint8_t *ek = sc + round16((size_t)batch * sizeof(int32_t)), *ev = ek + round16((size_t)batch * tok);
-    window_evict_kernel<<<batch, 128, 0, st>>>(static_cast<const uint8_t *>(win_k), static_cast<const uint8_t *>(win_v),
-                                               tok, win_cap, ctx_lens, win_lens, ek, ev, epos, status);
+    window_step_kernel<<<batch, 128, 0, st>>>(static_cast<const uint8_t *>(k_new), static_cast<const uint8_t *>(v_new),
+                                              tok, win_cap, static_cast<uint8_t *>(win_k), static_cast<uint8_t *>(win_v),
+                                              ctx_lens, win_lens, ek, ev, epos, status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // the leaving tokens go into the history at their positions (sequences with epos < 0 are skipped)
-    e = launch_append(d, dtype, params, ek, ev, batch, hkv, block_table, max_blocks, epos, k_pool, v_pool, num_blocks,
-                      status, st);
-    if (e != cudaSuccess) return e;
-    window_write_kernel<<<batch, 128, 0, st>>>(static_cast<const uint8_t *>(k_new), static_cast<const uint8_t *>(v_new),
-                                               tok, win_cap, static_cast<uint8_t *>(win_k),
-                                               static_cast<uint8_t *>(win_v), ctx_lens, win_lens);
-    return cudaGetLastError();
+    return launch_append(d, dtype, params, ek, ev, batch, hkv, block_table, max_blocks, epos, k_pool, v_pool,
+                         num_blocks, status, st);
 }
 
 int hybrid_nchunk(int d, int win_cap) {
