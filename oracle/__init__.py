@@ -73,9 +73,9 @@ def _declare(L):
     L.tqo_v_record_bytes.restype = ctypes.c_size_t
     L.tqo_v_record_bytes.argtypes = [_I]
     L.tqo_k_bitpos.restype = None
-    L.tqo_k_bitpos.argtypes = [_I, _I, _I, _P, _P]
+    L.tqo_k_bitpos.argtypes = [_I, _I, _I, _I, _P, _P]
     L.tqo_v_bitpos.restype = None
-    L.tqo_v_bitpos.argtypes = [_I, _I, _I, _P, _P]
+    L.tqo_v_bitpos.argtypes = [_I, _I, _I, _I, _P, _P]
     L.tqo_pack_k.restype = None
     L.tqo_pack_k.argtypes = [_I, _P, _I, _P, _P, ctypes.c_uint16, ctypes.c_uint16]
     L.tqo_unpack_k.restype = None
@@ -253,11 +253,28 @@ def unpack(is_k: bool, d: int, pool: np.ndarray, H: int, slots: np.ndarray):
     return dict(codes=codes, signs=signs, n16=n16, g16=g16)
 
 
-def bitpos(is_k: bool, d: int, t: int, i: int):
+def bitpos(is_k: bool, d: int, t: int, i: int, p: int):
+    """Position of bit p of slot t's field for coordinate i in a record: (word, bit) of the
+    little-endian 32-bit words of the cell region.  p = 0..2: cell bit p; p = 3: QJL sign (K)."""
     w = np.zeros(1, np.int32)
     b = np.zeros(1, np.int32)
-    (lib().tqo_k_bitpos if is_k else lib().tqo_v_bitpos)(d, t, i, _ptr(w), _ptr(b))
+    (lib().tqo_k_bitpos if is_k else lib().tqo_v_bitpos)(d, t, i, p, _ptr(w), _ptr(b))
     return int(w[0]), int(b[0])
+
+
+def slot_owner(is_k: bool, d: int) -> np.ndarray:
+    """Byte offset within a record -> the slot whose fields or norms it holds (-1: none)."""
+    owner = np.full(record_bytes(is_k, d), -1, np.int64)
+    for t in range(16):
+        for i in range(d):
+            for p in range(4 if is_k else 3):
+                w, b = bitpos(is_k, d, t, i, p)
+                owner[w * 4 + b // 8] = t
+    nb = 4 if is_k else 2
+    base = (8 if is_k else 6) * d
+    for t in range(16):
+        owner[base + nb * t: base + nb * (t + 1)] = t
+    return owner
 
 
 # ---------------------------------------------------------------- decode

@@ -31,7 +31,8 @@
  *
  * Parity pins live in tests/test_oracle_pins.py.  The packed bit layout
  * (tqo_k_bitpos / tqo_v_bitpos) is a convention of this library and is
- * parity unpinned except by agreement with the CUDA path.
+ * parity unpinned except by agreement with the CUDA path (and by the
+ * bijection and round-trip pins).
  */
 #include <math.h>
 #include <stdint.h>
@@ -243,52 +244,73 @@ void tqo_encode_vector(int is_k, int d, const int8_t *D, const float *S,
 /* One pool holds [num_blocks][n_kv_heads][record bytes]; a record holds
  * the 16 token slots of one block for one head.
  *
- * K record (d=128: 1088 B): 3 code planes, 1 QJL sign plane (each 2d bytes),
- * then 16 x {fp16 n, fp16 gamma}.
- * V record (d=128: 800 B): 3 code planes (2d bytes each), then 16 x fp16 n.
- * Plane p of a code holds bit p of the 3-bit cell index.
+ * K record (d=128: 1088 B): d/2 bytes of 4-bit fields per slot (3 cell bits
+ * and the QJL sign bit of one coordinate), 8*d bytes in all, then
+ * 16 x {fp16 n, fp16 gamma}.
+ * V record (d=128: 800 B): 3*d/8 bytes of cell bits per slot, 6*d bytes in
+ * all, then 16 x fp16 n.
  *
- * Within a plane, 32-bit little-endian words are addressed by a "lane"
- * L = 4*gid + tig; bit 8*j + q of a word belongs to one element. */
+ * The cell bits are addressed as bits of little-endian 32-bit words, which
+ * are grouped by a "lane" L = 4*gid + tig (0..31).  Every byte belongs to
+ * one token slot, so slots can be written independently. */
 
-size_t tqo_k_record_bytes(int d) { return (size_t)4 * (2 * d) + TQO_BLOCK * 4; }
-size_t tqo_v_record_bytes(int d) { return (size_t)3 * (2 * d) + TQO_BLOCK * 2; }
+size_t tqo_k_record_bytes(int d) { return (size_t)8 * d + TQO_BLOCK * 4; }
+size_t tqo_v_record_bytes(int d) { return (size_t)6 * d + TQO_BLOCK * 2; }
 
-/* K plane: token slot t (0..15), coordinate i (0..d-1) -> (word, bit).
- * Coordinate i = 16*s + k: h = k>>3, tig = (k&7)>>1, e = k&1; lane L = 4*(t&7) + tig;
- * word (L*2 + (t>>3)) * (d/128) + (s>>3); bit 8*h + (s&7) + 16*e. */
-void tqo_k_bitpos(int d, int t, int i, int *word, int *bit)
+/* K: slot t, coordinate i, field bit p (0..2: cell bit p, 3: QJL sign bit)
+ * -> (word, bit).  Coordinate i = 16*ks + c with column c = 2*tig + e + 8*h
+ * (e = c&1, h = c>>3); slot t = gid + 8*r.  Lane L = 4*gid + tig holds, per
+ * slot row r, d/32 words; word w holds the 8 coordinates of columns
+ * {2tig, 2tig+1, 2tig+8, 2tig+9} of k-steps 2w and 2w+1 as 4-bit fields:
+ * field f = 4*(ks&1) + e + 2*h, at bits 4f .. 4f+3. */
+void tqo_k_bitpos(int d, int t, int i, int p, int *word, int *bit)
 {
-    int nw = d / 128;                  /* words per (lane, token) */
-    int s = i >> 4, k = i & 15;
-    int h = k >> 3, tig = (k & 7) >> 1, e = k & 1;
-    int lane = 4 * (t & 7) + tig;
-    *word = (lane * 2 + (t >> 3)) * nw + (s >> 3);
-    *bit = 8 * h + (s & 7) + 16 * e;
+    int nw = d / 32;
+    int ks = i >> 4, c = i & 15;
+    int tig = (c & 7) >> 1, e = c & 1, h = c >> 3;
+    int gid = t & 7, r = t >> 3;
+    int f = 4 * (ks & 1) + e + 2 * h;
+    *word = ((4 * gid + tig) * 2 + r) * nw + (ks >> 1);
+    *bit = 4 * f + p;
 }
 
-/* V plane: token slot t, coordinate i -> (word, bit).
- * Coordinate i = 16*mt + gid + 8*rh; token t: tig = (t&7)>>1, e = t&1, tp = t>>3;
- * lane L = 4*gid + tig; word L*(d/64) + 2*(mt>>3) + rh; bit 8*tp + (mt&7) + 16*e. */
-void tqo_v_bitpos(int d, int t, int i, int *word, int *bit)
+/* V: slot t, coordinate i, cell bit p (0..2) -> (word, bit).
+ * Coordinate i = 16*mt + gid + 8*rr; its slot index within the lane is
+ * s = 2*mt + rr (0 .. d/8-1), cut into groups of 16 (g = s/16, sg = s%16).
+ * Slot t: tig = (t&7)>>1, pair P = t>>3, e = t&1 (first or second slot of
+ * the pair).  Lane L = 4*gid + tig holds, per pair P, 3 words per group.
+ * With hf = (sg>>1)&1 and ab = sg&1, the 4-bit field f = 4*hf + 2*e + ab of
+ * word 3*g + (sg>>2) holds the cell in bits 0..2 when sg < 12; the fields of
+ * sg = 12..15 (hf = (sg-12)>>1, ab = sg&1) keep cell bit p in bit 3 of field
+ * f of word 3*g + p.  Field f sits in byte f>>1 = 2*hf + e, so the bytes of
+ * a word alternate between the two slots of the pair. */
+void tqo_v_bitpos(int d, int t, int i, int p, int *word, int *bit)
 {
-    int nw = d / 64;                   /* words per lane */
-    int mt = i >> 4, r = i & 15, gid = r & 7, rh = r >> 3;
-    int tig = (t & 7) >> 1, e = t & 1, tp = t >> 3;
-    int lane = 4 * gid + tig;
-    *word = lane * nw + 2 * (mt >> 3) + rh;
-    *bit = 8 * tp + (mt & 7) + 16 * e;
+    int ng = d / 128;
+    int mt = i >> 4, rr = (i & 15) >> 3, gid = i & 7;
+    int s = 2 * mt + rr, g = s >> 4, sg = s & 15;
+    int tig = (t & 7) >> 1, P = t >> 3, e = t & 1;
+    int base = ((4 * gid + tig) * 2 + P) * 3 * ng + 3 * g;
+    if (sg < 12) {
+        int f = 4 * ((sg >> 1) & 1) + 2 * e + (sg & 1);
+        *word = base + (sg >> 2);
+        *bit = 4 * f + p;
+    } else {
+        int f = 4 * ((sg - 12) >> 1) + 2 * e + (sg & 1);
+        *word = base + p;
+        *bit = 4 * f + 3;
+    }
 }
 
-static void set_bit(uint8_t *plane, int word, int bit, int v)
+static void set_bit(uint8_t *rec, int word, int bit, int v)
 {
-    uint8_t *b = plane + (size_t)word * 4 + (bit >> 3);
+    uint8_t *b = rec + (size_t)word * 4 + (bit >> 3);
     uint8_t m = (uint8_t)(1u << (bit & 7));
     if (v) *b |= m; else *b &= (uint8_t)~m;
 }
-static int get_bit(const uint8_t *plane, int word, int bit)
+static int get_bit(const uint8_t *rec, int word, int bit)
 {
-    return (plane[(size_t)word * 4 + (bit >> 3)] >> (bit & 7)) & 1;
+    return (rec[(size_t)word * 4 + (bit >> 3)] >> (bit & 7)) & 1;
 }
 static void put16(uint8_t *p, uint16_t v) { p[0] = (uint8_t)(v & 255); p[1] = (uint8_t)(v >> 8); }
 static uint16_t get16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
@@ -297,12 +319,13 @@ void tqo_pack_k(int d, uint8_t *rec, int t, const uint8_t *codes, const uint8_t 
                 uint16_t n16, uint16_t g16)
 {
     for (int i = 0; i < d; i++) {
-        int w, b;
-        tqo_k_bitpos(d, t, i, &w, &b);
-        for (int pl = 0; pl < 3; pl++) set_bit(rec + (size_t)pl * 2 * d, w, b, (codes[i] >> pl) & 1);
-        set_bit(rec + (size_t)3 * 2 * d, w, b, signs[i]);
+        for (int pl = 0; pl < 4; pl++) {
+            int w, b;
+            tqo_k_bitpos(d, t, i, pl, &w, &b);
+            set_bit(rec, w, b, pl < 3 ? (codes[i] >> pl) & 1 : signs[i]);
+        }
     }
-    uint8_t *nr = rec + (size_t)4 * 2 * d + 4 * t;
+    uint8_t *nr = rec + (size_t)8 * d + 4 * t;
     put16(nr, n16);
     put16(nr + 2, g16);
 }
@@ -311,14 +334,16 @@ void tqo_unpack_k(int d, const uint8_t *rec, int t, uint8_t *codes, uint8_t *sig
                   uint16_t *n16, uint16_t *g16)
 {
     for (int i = 0; i < d; i++) {
-        int w, b;
-        tqo_k_bitpos(d, t, i, &w, &b);
-        int k = 0;
-        for (int pl = 0; pl < 3; pl++) k |= get_bit(rec + (size_t)pl * 2 * d, w, b) << pl;
+        int k = 0, w, b;
+        for (int pl = 0; pl < 3; pl++) {
+            tqo_k_bitpos(d, t, i, pl, &w, &b);
+            k |= get_bit(rec, w, b) << pl;
+        }
         codes[i] = (uint8_t)k;
-        signs[i] = (uint8_t)get_bit(rec + (size_t)3 * 2 * d, w, b);
+        tqo_k_bitpos(d, t, i, 3, &w, &b);
+        signs[i] = (uint8_t)get_bit(rec, w, b);
     }
-    const uint8_t *nr = rec + (size_t)4 * 2 * d + 4 * t;
+    const uint8_t *nr = rec + (size_t)8 * d + 4 * t;
     *n16 = get16(nr);
     *g16 = get16(nr + 2);
 }
@@ -326,23 +351,27 @@ void tqo_unpack_k(int d, const uint8_t *rec, int t, uint8_t *codes, uint8_t *sig
 void tqo_pack_v(int d, uint8_t *rec, int t, const uint8_t *codes, uint16_t n16)
 {
     for (int i = 0; i < d; i++) {
-        int w, b;
-        tqo_v_bitpos(d, t, i, &w, &b);
-        for (int pl = 0; pl < 3; pl++) set_bit(rec + (size_t)pl * 2 * d, w, b, (codes[i] >> pl) & 1);
+        for (int pl = 0; pl < 3; pl++) {
+            int w, b;
+            tqo_v_bitpos(d, t, i, pl, &w, &b);
+            set_bit(rec, w, b, (codes[i] >> pl) & 1);
+        }
     }
-    put16(rec + (size_t)3 * 2 * d + 2 * t, n16);
+    put16(rec + (size_t)6 * d + 2 * t, n16);
 }
 
 void tqo_unpack_v(int d, const uint8_t *rec, int t, uint8_t *codes, uint16_t *n16)
 {
     for (int i = 0; i < d; i++) {
-        int w, b;
-        tqo_v_bitpos(d, t, i, &w, &b);
         int k = 0;
-        for (int pl = 0; pl < 3; pl++) k |= get_bit(rec + (size_t)pl * 2 * d, w, b) << pl;
+        for (int pl = 0; pl < 3; pl++) {
+            int w, b;
+            tqo_v_bitpos(d, t, i, pl, &w, &b);
+            k |= get_bit(rec, w, b) << pl;
+        }
         codes[i] = (uint8_t)k;
     }
-    *n16 = get16(rec + (size_t)3 * 2 * d + 2 * t);
+    *n16 = get16(rec + (size_t)6 * d + 2 * t);
 }
 
 /* ------------------------------------------------------------------ */

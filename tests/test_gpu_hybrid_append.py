@@ -31,17 +31,8 @@ def _down(t):
 
 
 def _slot_owner(is_k, d):
-    """byte offset within a record -> the slot that owns it (the oracle's layout)."""
-    owner = np.full(oracle.record_bytes(is_k, d), -1, np.int64)
-    planes = 4 if is_k else 3
-    for t in range(16):
-        for i in range(d):
-            w, b = oracle.bitpos(is_k, d, t, i)
-            for p in range(planes):
-                owner[p * 2 * d + w * 4 + b // 8] = t
-    nb = 4 if is_k else 2
-    for t in range(16):
-        owner[planes * 2 * d + nb * t: planes * 2 * d + nb * (t + 1)] = t
+    """byte offset within a record -> owning slot (from the oracle's layout)."""
+    owner = oracle.slot_owner(is_k, d)
     assert (owner >= 0).all()
     return owner
 

@@ -45,18 +45,7 @@ def _inputs(N, H, d, dtype, seed, outliers=True):
 
 def _slot_owner(is_k, d):
     """byte offset within a record -> owning slot (from the oracle's layout)."""
-    rec = oracle.record_bytes(is_k, d)
-    owner = np.full(rec, -1, np.int64)
-    planes = 4 if is_k else 3
-    for t in range(16):
-        for i in range(d):
-            w, b = oracle.bitpos(is_k, d, t, i)
-            for p in range(planes):
-                owner[p * 2 * d + w * 4 + b // 8] = t
-    nb = 4 if is_k else 2
-    base = planes * 2 * d
-    for t in range(16):
-        owner[base + nb * t: base + nb * (t + 1)] = t
+    owner = oracle.slot_owner(is_k, d)
     assert (owner >= 0).all()
     return owner
 

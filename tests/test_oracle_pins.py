@@ -261,13 +261,31 @@ def test_bits_per_dim():
 @pytest.mark.parametrize("is_k", [True, False])
 @pytest.mark.parametrize("d", [128, 256])
 def test_layout_is_a_bijection(is_k, d):
+    """Every (slot, coordinate, field bit) has its own bit of the record's cell region, and the
+    region is used in full: 4 bits per coordinate for K (4.25 bits/dim with the norms at d=128),
+    3 for V (3.125)."""
+    nbits = 4 if is_k else 3
     seen = set()
     for t in range(16):
         for i in range(d):
-            w, b = oracle.bitpos(is_k, d, t, i)
-            assert 0 <= b < 32 and 0 <= w * 32 + b < 16 * d
-            seen.add(w * 32 + b)
-    assert len(seen) == 16 * d
+            for p in range(nbits):
+                w, b = oracle.bitpos(is_k, d, t, i, p)
+                assert 0 <= b < 32 and 0 <= w * 32 + b < 16 * d * nbits
+                seen.add(w * 32 + b)
+    assert len(seen) == 16 * d * nbits
+
+
+@pytest.mark.parametrize("is_k", [True, False])
+@pytest.mark.parametrize("d", [128, 256])
+def test_layout_bytes_have_one_owner(is_k, d):
+    """A byte of a record holds fields of one slot only, so slots are written independently."""
+    owner = oracle.slot_owner(is_k, d)
+    assert (owner >= 0).all()
+    for t in range(16):
+        for i in range(0, d, 7):
+            for p in range(4 if is_k else 3):
+                w, b = oracle.bitpos(is_k, d, t, i, p)
+                assert owner[w * 4 + b // 8] == t
 
 
 def test_pack_unpack_roundtrip():

@@ -1,6 +1,7 @@
 // tq_api.cu -- the C ABI declared in include/tq.h: argument checks on the host,
 // then kernel launches on the caller's stream.  Allocates no device memory.
 #include <math.h>
+#include <string.h>
 
 #include "tq_gq.cuh"
 #include "tq_internal.cuh"
@@ -8,20 +9,18 @@
 namespace tq {
 namespace {
 
-// Lloyd-Max fixed point for the unit Gaussian with 8 levels, in fp64 on the
-// device ("Lloyd-Maxコードブックとは", lilting.ch SwiftLM article: computed
-// once before inference, no calibration).  The optimum is symmetric (the
-// Gaussian is symmetric and log-concave, so the optimum is unique), so only
-// the four positive cells are iterated: edges 0, m1, m2, m3, +inf; each level
-// moves to the Gaussian mean of its cell, each inner edge to the midpoint of
-// its two levels.
-__global__ void codebook_kernel(uint8_t *params, int d) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+// Lloyd-Max fixed point for the unit Gaussian with 8 levels, in fp64 on the host
+// ("Lloyd-Maxコードブックとは", lilting.ch SwiftLM article: computed once before inference,
+// no calibration).  The optimum is symmetric (the Gaussian is symmetric and log-concave, so
+// the optimum is unique), so only the four positive cells are iterated: edges 0, m1, m2, m3,
+// +inf; each level moves to the Gaussian mean of its cell, each inner edge to the midpoint
+// of its two levels.
+void lloyd_max_positive(double (&lv)[4]) {
     const double inv_sqrt2 = 0.70710678118654752440;
     const double inv_sqrt2pi = 0.39894228040143267794;
-    double lv[4] = {0.3, 0.8, 1.4, 2.2};
+    lv[0] = 0.3; lv[1] = 0.8; lv[2] = 1.4; lv[3] = 2.2;
     for (int it = 0; it < 100000; ++it) {
-        double edge[5] = {0.0, 0.5 * (lv[0] + lv[1]), 0.5 * (lv[1] + lv[2]), 0.5 * (lv[2] + lv[3]), 0.0};
+        const double edge[5] = {0.0, 0.5 * (lv[0] + lv[1]), 0.5 * (lv[1] + lv[2]), 0.5 * (lv[2] + lv[3]), 0.0};
         double moved = 0.0;
         for (int k = 0; k < 4; ++k) {
             const double a = edge[k];
@@ -36,19 +35,78 @@ __global__ void codebook_kernel(uint8_t *params, int d) {
         }
         if (moved < 1e-15) break;
     }
-    ParamsHeader *h = reinterpret_cast<ParamsHeader *>(params);
-    for (int k = 0; k < 4; ++k) {
-        h->centroid64[4 + k] = lv[k];
-        h->centroid64[3 - k] = -lv[k];
+}
+
+// Nearest binary16 value of a positive normal-range double (ties to even), and its bits.
+double f16_round_pos(double v, int *ex_out = nullptr) {
+    int e;
+    frexp(v, &e);                     // v = f 2^e, f in [0.5, 1): spacing 2^(e - 11)
+    const double ulp = ldexp(1.0, e - 11);
+    if (ex_out) *ex_out = e;
+    return nearbyint(v / ulp) * ulp;  // default rounding mode: to nearest, ties to even
+}
+uint16_t f16_bits(double v) {
+    const bool neg = v < 0;
+    int e;
+    const double r = f16_round_pos(neg ? -v : v, &e);
+    int ex;
+    const double f = frexp(r, &ex);   // rounding may carry into the next binade
+    const uint32_t mant = (uint32_t)ldexp(f, 11) - 1024u;
+    return (uint16_t)((neg ? 0x8000u : 0u) | ((uint32_t)(ex - 1 + 15) << 10) | mant);
+}
+
+// The decode kernels read the codebook as eight binary16 values T[j] = f16(alpha c[j]) through
+// byte-permute lookups and undo alpha in fp32.  alpha in [1, 2) is chosen to put all four
+// magnitudes closest to binary16 values: the worst relative error of T[j] / alpha against
+// c[j] is then under 2e-5 (plain f16 rounding would leave up to 3e-4).
+double choose_alpha(const double (&lv)[4]) {
+    double best = 1.0, best_err = 1e30;
+    for (int k = 0; k < 1000000; ++k) {
+        const double al = 1.0 + k * 1e-6;
+        double err = 0.0;
+        for (int j = 0; j < 4 && err < best_err; ++j) {
+            const double v = al * lv[j];
+            err = fmax(err, fabs(f16_round_pos(v) - v) / v);
+        }
+        if (err < best_err) {
+            best_err = err;
+            best = al;
+        }
     }
-    for (int j = 0; j < 8; ++j) h->centroid[j] = (float)h->centroid64[j];
-    for (int j = 0; j < 7; ++j) h->threshold[j] = (float)(0.5 * (h->centroid64[j] + h->centroid64[j + 1]));
-    h->threshold[3] = 0.0f;
-    h->threshold[7] = INFINITY;
-    h->one16x2 = 0x3C003C00u;
-    h->d = d;
-    __threadfence();
-    h->magic = kParamsMagic;
+    return best;
+}
+
+ParamsHeader make_header() {
+    ParamsHeader h;
+    memset(&h, 0, sizeof h);
+    double lv[4];
+    lloyd_max_positive(lv);
+    for (int k = 0; k < 4; ++k) {
+        h.centroid64[4 + k] = lv[k];
+        h.centroid64[3 - k] = -lv[k];
+    }
+    for (int j = 0; j < 8; ++j) h.centroid[j] = (float)h.centroid64[j];
+    for (int j = 0; j < 7; ++j) h.threshold[j] = (float)(0.5 * (h.centroid64[j] + h.centroid64[j + 1]));
+    h.threshold[3] = 0.0f;
+    h.threshold[7] = INFINITY;
+    h.one16x2 = 0x3C003C00u;
+    const double al = choose_alpha(lv);
+    h.inv_alpha = (float)(1.0 / al);
+    for (int j = 0; j < 8; ++j) {
+        const uint16_t t = f16_bits(al * h.centroid64[j]);
+        h.t16[j] = t;
+        h.lut_lo[j >> 2] |= (uint32_t)(t & 0xFFu) << (8 * (j & 3));
+        h.lut_hi[j >> 2] |= (uint32_t)(t >> 8) << (8 * (j & 3));
+    }
+    h.magic = kParamsMagic;
+    return h;
+}
+
+// The header depends on d only through its d field: solved once per process.
+void fill_header(ParamsHeader &h, int d) {
+    static const ParamsHeader base = make_header();
+    h = base;
+    h.d = d;
 }
 
 // D signs arrive as int8 in a scratch spot (the start of the S region);
@@ -107,17 +165,19 @@ int tq_codebook_init(int d, const int8_t *D_host, const float *S_host, void *par
         if (D_host[i] != 1 && D_host[i] != -1) return TQ_ERR_INVALID;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     uint8_t *P = static_cast<uint8_t *>(params_dev);
+    ParamsHeader h;
+    fill_header(h, d);
     cudaError_t e = cudaMemsetAsync(P, 0, sizeof(ParamsHeader), st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(P + params_off_S(d), D_host, (size_t)d, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) { signs_kernel<<<(d + 127) / 128, 128, 0, st>>>(P, d); e = cudaGetLastError(); }
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(P + params_off_S(d), S_host, sizeof(float) * (size_t)d * d, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) { transpose_kernel<<<d, d, 0, st>>>(P, d); e = cudaGetLastError(); }
-    if (e == cudaSuccess) { codebook_kernel<<<1, 32, 0, st>>>(P, d); e = cudaGetLastError(); }
+    // the header (magic last in stream order) once D and S are in place; h stays alive until the
+    // stream is synchronised below
+    if (e == cudaSuccess) e = cudaMemcpyAsync(P, &h, sizeof h, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (e == cudaSuccess && centroids_out8)
-        e = cudaMemcpy(centroids_out8, P + offsetof(ParamsHeader, centroid64), 8 * sizeof(double),
-                       cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && centroids_out8) memcpy(centroids_out8, h.centroid64, 8 * sizeof(double));
     return cuda_status(e);
 }
 

@@ -1,70 +1,75 @@
-// tq_decode_warp.cu -- the decode pass at d = 128: every warp scores, weighs and sums its
-// own 16-token blocks end to end.
+// tq_decode_warp.cu -- the decode pass: every warp scores, weighs and sums its own 16-token
+// blocks end to end (d = 128 and d = 256).
 //
-// Method as in tq_decode.cu (scores and value sums in the rotated domain, straight from
-// the packed cells, signs and fp16 norms: the "fused dequantisation" of the SwiftLM
-// README, "TurboQuantization: KV Cache Compression"; blocks through the block table of
-// the vLLM-MLX explainer, "Paged KVキャッシュ"), and the same stream-K schedule,
-// workspace and merge.  What differs is the work split inside a CTA:
-//  * A CTA of 4 warps takes the same 128-token chunks; warp w owns blocks 2w, 2w+1 of
-//    each chunk and stages them itself (cp.async, one pair ahead), so the chunk loop has
-//    no CTA-wide barrier.
-//  * K side as in the coordinate-split pass: five +-1 planes on f16 mma.sync against
-//    the f16 hi/lo query fragments.
+// Method as in tq_decode.cu (scores and value sums in the rotated domain, straight from the
+// packed cells, signs and fp16 norms: the "fused dequantisation" of the SwiftLM README,
+// "TurboQuantization: KV Cache Compression"; blocks through the block table of the vLLM-MLX
+// explainer, "Paged KVキャッシュ"), with the stream-K schedule, workspace and merge described
+// there.  Inside a CTA:
+//  * A CTA of 4 warps takes 128-token chunks; warp w owns blocks 2w, 2w+1 of each chunk and
+//    stages them itself (cp.async, one pair ahead), so the chunk loop has no CTA-wide barrier.
+//  * Operands by table lookup.  The codebook is read as eight binary16 values T[j] =
+//    f16(alpha c[j]) (alpha from the params header, worst level error under 2e-5 after
+//    dividing by alpha).  A record word holds eight 4-bit fields; masked to their cell bits,
+//    four fields are the selector of two PRMTs over byte tables of T (low bytes, high bytes),
+//    and two more PRMTs interleave the bytes into two f16x2 registers: an mma.sync A operand
+//    with the codebook value of each (token, coordinate) (K side) or (coordinate, token)
+//    (V side).  One operand plane replaces four +-1 planes of the codebook's Walsh
+//    decomposition, so the pass issues 24 mma per block instead of 76.
+//  * K side: the codebook plane against q-bar / alpha, the QJL plane (bit 3 of each K field,
+//    one LOP3 per register: 0 / delta or +-2^-14 by bit position) against u, both f16 hi/lo.
 //  * Online softmax in registers, per warp and head, with a lazily moved reference:
 //    weights are 2^(s - m) * nv with s in log2 units, and m only moves when a block's
 //    maximum passes m + 8 (or a weight would leave the f16 range), so the accumulators
 //    are rescaled rarely.
-//  * V side over all 128 coordinates of the warp's block.  The four Walsh planes share
-//    one accumulator per m-tile: plane m's B operand is the weights times A_m in f16 (the
-//    value sum sum_t w_t c[cell_t] = sum_m A_m sum_t w_t sigma_m), with an f16 lo part for
-//    the planes of the two large coefficients (A_1, A_2; A_0 and A_3 are 3.4 and 15 times
-//    smaller than A_2, so their single rounding costs little).
-//    One more mma with a constant A = 1 sums those B operands (for the offset of the
-//    0/delta operands).  Each block's mma sums start from zero and are added to fp32
-//    running sums: chained tensor-core accumulation over thousands of tokens is not
-//    accurate enough for the 2 sum(w b) - sum(w) cancellation.
-//  * At the end of a (sequence, kv head) segment the 4 warps' (m, l, acc) are merged
-//    in shared memory, then the segment is finished or left as a partial exactly as in
-//    the coordinate-split pass (m in log2 units here).
+//  * V side: one mma per m-tile and block, against the weights (f16 hi in columns 0..3 and
+//    f16 lo in 4..7 for up to 4 heads, f16 for 5..8), each block's sum started from zero and
+//    added to fp32 running sums (chained tensor-core accumulation over thousands of tokens is
+//    not accurate enough).
+//  * At the end of a (sequence, kv head) segment the 4 warps' (m, l, acc) are merged in
+//    shared memory, then the segment is finished or left as a partial (m in log2 units).
 #include "tq_split.cuh"
 
 #ifndef TQ_WARP_BQ_SMEM
-#define TQ_WARP_BQ_SMEM 0        // 1: K-side query fragments read from shared memory for every group size
+#define TQ_WARP_BQ_SMEM 0        // 1: K-side query fragments read from shared memory for every shape
 #endif
 #ifndef TQ_WARP_MINBLOCKS
-#define TQ_WARP_MINBLOCKS 3      // resident CTAs per SM the register budget is sized for (G <= 4)
+#define TQ_WARP_MINBLOCKS 3      // resident CTAs per SM the register budget is sized for (d = 128)
 #endif
-#ifndef TQ_WARP_MINBLOCKS_WIDE
-#define TQ_WARP_MINBLOCKS_WIDE 3 // the same for groups of 5..8 heads (two K-side n-tiles)
+#ifndef TQ_WARP_NBUF
+#define TQ_WARP_NBUF 3           // staging buffers per warp: chunks in flight = NBUF - 1 ahead of the one in use
+#endif
+#ifndef TQ_WARP_MINBLOCKS_256
+#define TQ_WARP_MINBLOCKS_256 2  // the same at d = 256
 #endif
 
 namespace tq {
 namespace {
 
-constexpr int kWD = 128, kWWarps = 4, kWBpw = TQ_SPLITK_BPW;
-constexpr int kWKrec = (int)k_record(kWD), kWVrec = (int)v_record(kWD), kWRec = kWKrec + kWVrec;
+constexpr int kWWarps = 4, kWBpw = TQ_SPLITK_BPW, kWBuf = TQ_WARP_NBUF;
 constexpr float kTau = 8.f;          // the reference moves when a block's maximum passes it by this (log2)
 constexpr float kWLimit = 32768.f;   // largest weight held (f16 max is 65504)
 constexpr float kNoRef = -1e30f;     // softmax reference before the first unmasked score
 
 template <int G>
 __host__ __device__ constexpr int w_ntk() { return (2 * G + 7) / 8; }
-// K-side query fragments in shared memory rather than registers: needed above 4 heads
-// (two n-tiles would take 64 registers)
-template <int G>
-__host__ __device__ constexpr bool w_bq_smem() { return TQ_WARP_BQ_SMEM || G > 4; }
+// K-side query fragments in shared memory rather than registers: above 4 heads (two n-tiles)
+// and at d = 256 (16 k-steps), where registers would hold 64 of them
+template <int D, int G>
+__host__ __device__ constexpr bool w_bq_smem() { return TQ_WARP_BQ_SMEM || G > 4 || D > 128; }
+template <int D>
+__host__ __device__ constexpr int w_rec() { return (int)(k_record(D) + v_record(D)); }
 
-template <int G>
+template <int D, int G>
 __host__ __device__ constexpr size_t warp_smem_bytes() {
-    const size_t stage = (size_t)kWWarps * 2 * kWBpw * kWRec;                  // per warp: 2 buffers x BPW blocks
-    const size_t merge = (size_t)(kWWarps + 1) * G * kWD * 4;                  // sAccW + sAcc
-    const size_t bq = w_bq_smem<G>() ? (size_t)2 * (kWD / 16) * w_ntk<G>() * 64 * 4 : 0;
+    const size_t stage = (size_t)kWWarps * kWBuf * kWBpw * w_rec<D>();   // per warp: NBUF buffers x BPW blocks
+    const size_t merge = (size_t)(kWWarps + 1) * G * D * 4;              // sAccW + sAcc
+    const size_t bq = w_bq_smem<D, G>() ? (size_t)2 * (D / 16) * w_ntk<G>() * 64 * 4 : 0;
     return stage + merge + bq;
 }
 
 // ld.shared of a query fragment at each use: a plain load would be hoisted out of the block
-// loop by the compiler and pin 64 registers
+// loop by the compiler and pin the fragments in registers
 __device__ __forceinline__ uint2 lds_u2(const uint32_t *p) {
     uint2 v;
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];"
@@ -77,27 +82,31 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&h);
 }
 
-template <int G>
-__global__ void __launch_bounds__(kWWarps * 32, G <= 4 ? TQ_WARP_MINBLOCKS : TQ_WARP_MINBLOCKS_WIDE)
+template <int D, int G>
+__global__ void __launch_bounds__(kWWarps * 32, D == 128 ? TQ_WARP_MINBLOCKS : TQ_WARP_MINBLOCKS_256)
 decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ packs, int batch, int q_len, int hq, int hkv,
                    const uint8_t *__restrict__ k_pool, const uint8_t *__restrict__ v_pool, int64_t num_blocks,
                    const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_lens,
                    int ctx_add, int max_ctx, const int64_t *__restrict__ cpre, const int32_t *__restrict__ cta_b,
                    float *__restrict__ part, unsigned int *__restrict__ counters, float *__restrict__ out,
                    float *__restrict__ lse, int32_t *status) {
-    constexpr int D = kWD, NT = kWWarps * 32, NWARP = kWWarps, BPW = kWBpw;
+    constexpr int NT = kWWarps * 32, NWARP = kWWarps, BPW = kWBpw, NBUF = kWBuf;
+    static_assert(NBUF * BPW <= 30, "buffer validity bits");
     constexpr int CH = kBlock * NWARP * BPW;    // tokens per chunk (the schedule's unit)
     constexpr int NTK = w_ntk<G>();             // K-side n-tiles; thread holds heads 4*nt + tig
     constexpr int NKS = D / 16, MT = D / 16, R = D / 32;
-    constexpr int KREC = kWKrec, VREC = kWVrec, REC = kWRec;
-    constexpr size_t kStage = (size_t)NWARP * 2 * BPW * REC;
+    constexpr int NW = D / 32;                  // K words per (lane, token row)
+    constexpr int NG = D / 128;                 // V slot groups per lane (3 words per pair each)
+    constexpr int KREC = (int)k_record(D), VREC = (int)v_record(D), REC = KREC + VREC;
+    constexpr size_t kStage = (size_t)NWARP * NBUF * BPW * REC;
     constexpr size_t kMerge = (size_t)(NWARP + 1) * G * D * 4;
     constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
+    constexpr bool BQS = w_bq_smem<D, G>();
 
     extern __shared__ __align__(16) uint8_t smem[];
     const int cta = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
-    uint8_t *sStage = smem + (size_t)warp * 2 * BPW * REC;     // this warp's [2][BPW][K record | V record]
+    uint8_t *sStage = smem + (size_t)warp * NBUF * BPW * REC;  // this warp's [NBUF][BPW][K record | V record]
     float *sAccW = reinterpret_cast<float *>(smem + kStage);     // [NWARP][G][D], segment end only
     float *sAcc = sAccW + NWARP * G * D;                         // [G][D]
     uint32_t *sBq = reinterpret_cast<uint32_t *>(smem + kStage + kMerge);
@@ -121,13 +130,11 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
     const int64_t g0 = sk_begin(cta, P, W), g1 = sk_begin(cta + 1, P, W);
 
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
-    float A[4];
-    walsh4(ph->centroid, A);
-    const float Asum = A[0] + A[1] + A[2] + A[3];
+    const uint32_t L0 = ph->lut_lo[0], L1 = ph->lut_lo[1], H0 = ph->lut_hi[0], H1 = ph->lut_hi[1];
+    const float inv_alpha = ph->inv_alpha;
     const float inv_sd = rsqrtf((float)D);
-    const float c_sc = inv_sd * kLog2e;                 // scores in log2 units
-    const float qjl = 1.2533141373155003f / (float)D;   // sqrt(pi/2) / d
-    const uint32_t one16x2 = (uint32_t)ph->one16x2;
+    const float c_sc = inv_sd * kLog2e;                             // scores in log2 units
+    const float qjl = 1.2533141373155003f / (float)D * 65536.f;    // sqrt(pi/2) / d, and 1 / 2^-16 of the operands
 
     // The CTA's range [g0, g1) of global chunks, walked one (sequence, kv head) segment at a time.
     struct Seg {
@@ -202,8 +209,35 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
         s = make_seg(b0, (int)((g0 - ub0) / n0), ub0, n0, g0);
     }
     bool first_seg = true;
-    int buf = 0;
-    int okm = stage(s, s.t0, 0);
+    // Prefetch cursor: the chunks of the CTA's range in order, NBUF - 1 ahead of the one in use,
+    // across segment boundaries.  Every step commits one cp.async group (empty past the range),
+    // so waiting for all but the newest NBUF - 1 groups completes the chunk in use.
+    Seg ps = s;
+    int ptc = s.t0;
+    bool pmore = true;
+    int okm = 0;   // bit NBUF-slot * BPW + bw: block bw of the buffer is in range with a valid id
+    int buf = 0, pbuf = 0;
+    auto prefetch = [&]() {
+        int bits = 0;
+        if (pmore) {
+            bits = stage(ps, ptc, pbuf);
+            ptc += CH;
+            if (ptc >= ps.t1) {
+                Seg n2;
+                pmore = next_seg(ps, n2);
+                if (pmore) {
+                    ps = n2;
+                    ptc = ps.t0;
+                }
+            }
+        } else {
+            cp_async_commit();
+        }
+        okm = (okm & ~(((1 << BPW) - 1) << (pbuf * BPW))) | (bits << (pbuf * BPW));
+        pbuf = (pbuf + 1 == NBUF) ? 0 : pbuf + 1;
+    };
+#pragma unroll
+    for (int k = 0; k < NBUF - 1; ++k) prefetch();
 
 #pragma unroll 1
     while (true) {
@@ -212,12 +246,12 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
         Seg ns;
         const bool more_segs = next_seg(s, ns);
 
-        // K-side query fragments and offset constants of this (sequence, kv head)
+        // K-side query fragments and the QJL offset constants of this (sequence, kv head)
         const uint8_t *pack = packs + ((size_t)b * hkv + kh) * kPackBytes(D);
         const float *pf = reinterpret_cast<const float *>(pack) + kPackFloatOff(D);
-        constexpr bool BQS = w_bq_smem<G>();
-        uint32_t bq[2][NKS][NTK][2];
+        uint32_t bq[BQS ? 1 : 2][BQS ? 1 : NKS][NTK][2];
         if constexpr (BQS) {
+            __syncthreads();   // the previous segment's reads of sBq are done
             for (int i = tid; i < 2 * NKS * NTK * 64 / 4; i += NT)
                 reinterpret_cast<uint4 *>(sBq)[i] = reinterpret_cast<const uint4 *>(pack)[i];
             __syncthreads();
@@ -234,24 +268,25 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                         bq[qu][ks][nt][1] = w.y;
                     }
         }
-        float cq[NTK], cu[NTK];
+        auto bfrag = [&](int qu, int ks, int nt) -> uint2 {
+            if constexpr (BQS) return lds_u2(sBq + ((qu * NKS + ks) * NTK + nt) * 64 + lane * 2);
+            else return make_uint2(bq[qu][ks][nt][0], bq[qu][ks][nt][1]);
+        };
+        float cu[NTK];
         int tlim[NTK];   // tokens column 4 nt + tig attends in this segment (query i: L - (q_len - 1 - i))
 #pragma unroll
         for (int nt = 0; nt < NTK; ++nt) {
             const int hg = 4 * nt + tig;
-            cq[nt] = hg < G ? pf[hg] * Asum : 0.f;
             cu[nt] = hg < G ? pf[8 + hg] : 0.f;
             tlim[nt] = hg < G ? min(t1, s.L - (q_len - 1 - hg / (G / q_len))) : 0;
         }
 
-        // running value sums (fp32 adds of the per-block mma results) and offset sums
-        float arun[MT][4], Trun[4];
+        // running value sums (fp32 adds of the per-block mma results)
+        float arun[MT][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int k = 0; k < 4; ++k) arun[mt][k] = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) Trun[k] = 0.f;
         float mref[NTK], lpart[NTK];
 #pragma unroll
         for (int nt = 0; nt < NTK; ++nt) {
@@ -278,107 +313,114 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                     arun[mt][e] *= fc;
                     arun[mt][2 + e] *= fc;
                 }
-                Trun[e] *= fc;
-                Trun[2 + e] *= fc;
             }
         };
 
-#pragma unroll 1
-        for (int tc = t0; tc < t1; tc += CH, buf ^= 1) {
-            // stage the next chunk of this segment, or the first chunk of the next segment
-            const bool ahead = tc + CH < t1 || more_segs;
-            if (ahead) {
-                const int nxt = (tc + CH < t1) ? stage(s, tc + CH, buf ^ 1) : stage(ns, ns.t0, buf ^ 1);
-                okm = (okm & ~(((1 << BPW) - 1) << ((buf ^ 1) * BPW))) | (nxt << ((buf ^ 1) * BPW));
-                cp_async_wait_1();
-            } else {
-                cp_async_wait_all();
-            }
-            __syncwarp();
-#pragma unroll 1
-            for (int bw = 0; bw < BPW; ++bw) {
-                const int tb = tc + kBlock * (BPW * warp + bw);   // first token of the block
-                if (tb >= t1) break;
-                const bool ok = (okm >> (buf * BPW + bw)) & 1;
-                const uint8_t *krec = sStage + (size_t)(buf * BPW + bw) * REC;
-                const uint8_t *vrec = krec + KREC;
-
-                // ---- K side: scores of tokens tb + gid + 8r for heads 4 nt + tig (log2 units)
-                float s2[NTK][2];
-                {
-                    uint32_t Wd[4][2];
+        // this lane's V words: pair 0 (tokens 2tig, 2tig+1), pair 1 (+8)
+        auto load_vw = [&](const uint8_t *vrec, uint32_t (&vw)[2][3 * NG]) {
+            if constexpr (NG == 1) {
 #pragma unroll
-                    for (int pl = 0; pl < 4; ++pl) {
-                        const uint2 w = *reinterpret_cast<const uint2 *>(krec + pl * 2 * D + lane * 8);
-                        Wd[pl][0] = w.x;
-                        Wd[pl][1] = w.y;
+                for (int c = 0; c < 3; ++c) {
+                    const uint2 v = reinterpret_cast<const uint2 *>(vrec + lane * 24)[c];
+                    vw[(2 * c) / 3][(2 * c) % 3] = v.x;
+                    vw[(2 * c + 1) / 3][(2 * c + 1) % 3] = v.y;
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 3 * NG / 2; ++c) {
+                    const uint4 v = reinterpret_cast<const uint4 *>(vrec + lane * 24 * NG)[c];
+                    const uint32_t x4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) vw[(4 * c + k) / (3 * NG)][(4 * c + k) % (3 * NG)] = x4[k];
+                }
+            }
+        };
+#pragma unroll 1
+        for (int tc = t0; tc < t1; tc += CH, buf = (buf + 1 == NBUF) ? 0 : buf + 1) {
+            prefetch();                      // into the buffer the previous chunk used
+            cp_async_wait_n<NBUF - 1>();     // the chunk in `buf` has arrived
+            __syncwarp();
+            const int tbw = tc + kBlock * BPW * warp;   // first token of this warp's blocks
+            if (tbw < t1) {
+                // ---- K side of the warp's blocks: scores of tokens tb + gid + 8r, heads 4 nt + tig (log2 units)
+                float s2[BPW][NTK][2];
+#pragma unroll
+                for (int bw = 0; bw < BPW; ++bw) {
+                    const int tb = tbw + kBlock * bw;
+                    const bool ok = (okm >> (buf * BPW + bw)) & 1;
+                    const uint8_t *krec = sStage + (size_t)(buf * BPW + bw) * REC;
+                    uint32_t kw[2][NW];   // this lane's words: token rows gid (r = 0) and gid + 8 (r = 1)
+#pragma unroll
+                    for (int c = 0; c < NW / 2; ++c) {
+                        const uint4 v = reinterpret_cast<const uint4 *>(krec + lane * 8 * NW)[c];
+                        const int r = (4 * c) / NW, w0 = (4 * c) % NW;
+                        kw[r][w0] = v.x;
+                        kw[r][w0 + 1] = v.y;
+                        kw[r][w0 + 2] = v.z;
+                        kw[r][w0 + 3] = v.w;
                     }
                     float nrm[2], gam[2];
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
                         const __half2 ng = *reinterpret_cast<const __half2 *>(krec + 8 * D + 4 * (gid + 8 * r));
-                        nrm[r] = __low2float(ng);
-                        gam[r] = __high2float(ng);
+                        nrm[r] = __low2float(ng) * c_sc;
+                        gam[r] = __high2float(ng) * qjl;
                     }
-                    uint32_t w[5][2], w8[5][2];
-#pragma unroll
-                    for (int m = 0; m < 5; ++m)
-#pragma unroll
-                        for (int th = 0; th < 2; ++th) {
-                            w[m][th] = (m < 3) ? Wd[m][th] : (m == 3) ? (Wd[0][th] ^ Wd[1][th] ^ Wd[2][th]) : Wd[3][th];
-                            w8[m][th] = w[m][th] << 8;
-                        }
-                    float acc[5][NTK][4];   // started by the first k-step's zero-accumulator mma
+                    float accc[NTK][4], accq[NTK][4];   // started by the first k-step's zero-accumulator mma
 #pragma unroll
                     for (int ks = 0; ks < NKS; ++ks) {
-                        const int q = 8 + ks;
-                        const uint32_t msk = op_mask(q), bas = (q == 14) ? 0u : one16x2;
-                        uint2 bsm[2][NTK];   // this k-step's fragments of q-bar (0) and u (1), shared-memory case
-                        if constexpr (BQS) {
-#pragma unroll
-                            for (int qu = 0; qu < 2; ++qu)
-#pragma unroll
-                                for (int nt = 0; nt < NTK; ++nt)
-                                    bsm[qu][nt] = lds_u2(sBq + ((qu * NKS + ks) * NTK + nt) * 64 + lane * 2);
-                        }
-#pragma unroll
-                        for (int m = 0; m < 5; ++m) {
-                            const uint32_t a0 = lop_and_xor(w8[m][0], msk, bas), a1 = lop_and_xor(w8[m][1], msk, bas);
-                            const uint32_t a2 = lop_and_xor(w[m][0], msk, bas), a3 = lop_and_xor(w[m][1], msk, bas);
-                            const int qu = (m == 4) ? 1 : 0;
-#pragma unroll
-                            for (int nt = 0; nt < NTK; ++nt) {
-                                const uint32_t b0 = BQS ? bsm[qu][nt].x : bq[qu][ks][nt][0];
-                                const uint32_t b1 = BQS ? bsm[qu][nt].y : bq[qu][ks][nt][1];
-                                if (ks == 0) mma_f16_z(acc[m][nt], a0, a1, a2, a3, b0, b1);
-                                else mma_f16(acc[m][nt], a0, a1, a2, a3, b0, b1);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int nt = 0; nt < NTK; ++nt) {
-                        const int hg = 4 * nt + tig;
+                        // codebook plane: fields 4h .. 4h+3 of word ks/2 are the columns 2tig, 2tig+1,
+                        // 2tig+8, 2tig+9 of k-step ks
+                        uint32_t a01[2], a23[2];
 #pragma unroll
                         for (int r = 0; r < 2; ++r) {
-                            float code2 = 0.f;
+                            const uint32_t m = kw[r][ks >> 1] & 0x77777777u;
+                            const uint32_t sel = (ks & 1) ? (m >> 16) : m;
+                            const uint32_t pl = prmt(L0, L1, sel), phb = prmt(H0, H1, sel);
+                            a01[r] = prmt(pl, phb, 0x5140u);
+                            a23[r] = prmt(pl, phb, 0x7362u);
+                        }
 #pragma unroll
-                            for (int m = 0; m < 4; ++m)
-                                code2 = fmaf(A[m], acc[m][nt][2 * r] + acc[m][nt][2 * r + 1], code2);
-                            const float dot_c = code2 - cq[nt];
-                            const float dot_q = acc[4][nt][2 * r] + acc[4][nt][2 * r + 1] - cu[nt];
-                            const bool valid = ok && (tb + gid + 8 * r < tlim[nt]);
-                            s2[nt][r] = valid ? nrm[r] * c_sc * (dot_c * inv_sd + gam[r] * qjl * dot_q) : -INFINITY;
+                        for (int nt = 0; nt < NTK; ++nt) {
+                            const uint2 bb = bfrag(0, ks, nt);
+                            if (ks == 0) mma_f16_z(accc[nt], a01[0], a01[1], a23[0], a23[1], bb.x, bb.y);
+                            else mma_f16(accc[nt], a01[0], a01[1], a23[0], a23[1], bb.x, bb.y);
+                        }
+                        // QJL plane, k-step ks: field positions i0 = 2 (ks & 1) (columns 2tig, 2tig+1)
+                        // and i0 + 1 (2tig+8, 2tig+9) of word ks/2, the two halves being the columns' pair
+                        const int i0 = 2 * (ks & 1), i1 = i0 + 1;
+                        const uint32_t m0 = 0x00010001u << (4 * i0 + 3), m1 = 0x00010001u << (4 * i1 + 3);
+                        const uint32_t q0 = lop_and_xor(kw[0][ks >> 1], m0, qjl_base(i0));
+                        const uint32_t q1 = lop_and_xor(kw[1][ks >> 1], m0, qjl_base(i0));
+                        const uint32_t q2 = lop_and_xor(kw[0][ks >> 1], m1, qjl_base(i1));
+                        const uint32_t q3 = lop_and_xor(kw[1][ks >> 1], m1, qjl_base(i1));
+#pragma unroll
+                        for (int nt = 0; nt < NTK; ++nt) {
+                            const uint2 bb = bfrag(1, ks, nt);
+                            if (ks == 0) mma_f16_z(accq[nt], q0, q1, q2, q3, bb.x, bb.y);
+                            else mma_f16(accq[nt], q0, q1, q2, q3, bb.x, bb.y);
                         }
                     }
+#pragma unroll
+                    for (int nt = 0; nt < NTK; ++nt)
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            const float dot_c = accc[nt][2 * r] + accc[nt][2 * r + 1];
+                            const float dot_q = accq[nt][2 * r] + accq[nt][2 * r + 1] - cu[nt];
+                            const bool valid = ok && (tb + gid + 8 * r < tlim[nt]);
+                            s2[bw][nt][r] = valid ? nrm[r] * fmaf(dot_c, inv_sd, gam[r] * dot_q) : -INFINITY;
+                        }
                 }
 
-                // ---- online softmax: move the reference when the block's maximum passes it
+                // ---- online softmax over the warp's blocks: move the reference when their maximum passes it
                 {
                     float f[NTK];
                     bool need = false;
 #pragma unroll
                     for (int nt = 0; nt < NTK; ++nt) {
-                        float bm = fmaxf(s2[nt][0], s2[nt][1]);
+                        float bm = -INFINITY;
+#pragma unroll
+                        for (int bw = 0; bw < BPW; ++bw) bm = fmaxf(bm, fmaxf(s2[bw][nt][0], s2[bw][nt][1]));
                         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
                         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
                         bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
@@ -389,28 +431,33 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                     }
                     if (__any_sync(0xffffffffu, need)) rescale(f);
                 }
-                float wv[NTK][2], pr[NTK][2];
+                float wv[BPW][NTK][2];
                 {
-                    float nv[2];
-#pragma unroll
-                    for (int r = 0; r < 2; ++r)
-                        nv[r] = __half2float(*reinterpret_cast<const __half *>(vrec + 6 * D + 2 * (gid + 8 * r)));
+                    float pr[BPW][NTK][2];
                     float wmax = 0.f;
 #pragma unroll
-                    for (int nt = 0; nt < NTK; ++nt)
+                    for (int bw = 0; bw < BPW; ++bw) {
+                        const uint8_t *vrec = sStage + (size_t)(buf * BPW + bw) * REC + KREC;
 #pragma unroll
                         for (int r = 0; r < 2; ++r) {
-                            const float p = exp2f(s2[nt][r] - mref[nt]);
-                            pr[nt][r] = p;
-                            wv[nt][r] = p * nv[r];
-                            wmax = fmaxf(wmax, wv[nt][r]);
+                            const float nv = __half2float(*reinterpret_cast<const __half *>(vrec + 6 * D + 2 * (gid + 8 * r)));
+#pragma unroll
+                            for (int nt = 0; nt < NTK; ++nt) {
+                                const float p = exp2f(s2[bw][nt][r] - mref[nt]);
+                                pr[bw][nt][r] = p;
+                                wv[bw][nt][r] = p * nv;
+                                wmax = fmaxf(wmax, wv[bw][nt][r]);
+                            }
                         }
+                    }
                     if (__any_sync(0xffffffffu, wmax > kWLimit)) {
                         // a weight would leave the f16 range: raise the reference of that head
                         float f[NTK];
 #pragma unroll
                         for (int nt = 0; nt < NTK; ++nt) {
-                            float hm = fmaxf(wv[nt][0], wv[nt][1]);
+                            float hm = 0.f;
+#pragma unroll
+                            for (int bw = 0; bw < BPW; ++bw) hm = fmaxf(hm, fmaxf(wv[bw][nt][0], wv[bw][nt][1]));
                             hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 4));
                             hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 8));
                             hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 16));
@@ -418,104 +465,105 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                             f[nt] = exp2f(-sh);
                             mref[nt] += sh;
 #pragma unroll
-                            for (int r = 0; r < 2; ++r) {
-                                pr[nt][r] *= f[nt];
-                                wv[nt][r] *= f[nt];
-                            }
+                            for (int bw = 0; bw < BPW; ++bw)
+#pragma unroll
+                                for (int r = 0; r < 2; ++r) {
+                                    pr[bw][nt][r] *= f[nt];
+                                    wv[bw][nt][r] *= f[nt];
+                                }
                         }
                         rescale(f);
                     }
 #pragma unroll
-                    for (int nt = 0; nt < NTK; ++nt) lpart[nt] += pr[nt][0] + pr[nt][1];
+                    for (int nt = 0; nt < NTK; ++nt)
+#pragma unroll
+                        for (int bw = 0; bw < BPW; ++bw) lpart[nt] += pr[bw][nt][0] + pr[bw][nt][1];
                 }
 
-                // ---- weights to the V-side B layout: thread (gid, tig) takes head gid & 3 (G <= 4)
-                // or gid (G > 4), tokens 2 tig, 2 tig + 1 (b0) and 2 tig + 8, 2 tig + 9 (b1); token
-                // t < 8 of head h sits in lane 4 t + (h & 3), slot 0 (t + 8: slot 1), n-tile h >> 2.
-                // Planes 1 and 2 carry w A_m as f16 hi + lo (2^-22): for G <= 4 the lo parts fill
-                // columns 4..7 of the same mma, for G > 4 they take a second mma.  Planes 0 and 3
-                // carry one f16 (columns 4..7 zero).
-                uint32_t Bh[4][2], Bl[4][2];
+                // ---- weights to the V-side B layout.  Thread (gid, tig) holds column gid: head gid & 3
+                // (G <= 4; columns 4..7 carry the f16 lo parts of heads 0..3) or head gid (G > 4), at
+                // tokens 2tig, 2tig+1 (b0) and 2tig+8, 2tig+9 (b1) of each block.  The weights of tokens
+                // t, t+8 of head h sit in lane 4 (t & 7) + (h & 3), n-tile h >> 2, packed as one f16x2.
+                uint32_t bf0[BPW], bf1[BPW];
                 {
-                    const int srcA = 8 * tig + (gid & 3), srcB = srcA + 4;
-                    const int hcol = (G <= 4) ? (gid & 3) : gid;     // head this thread's column carries
-                    float u[4] = {0.f, 0.f, 0.f, 0.f};
+                    const int hcol = (G <= 4) ? (gid & 3) : gid;
+                    const int srcX = 8 * tig + (hcol & 3), srcY = srcX + 4;
 #pragma unroll
-                    for (int nt = 0; nt < NTK; ++nt) {
-                        const float x0 = __shfl_sync(0xffffffffu, wv[nt][0], srcA);
-                        const float x1 = __shfl_sync(0xffffffffu, wv[nt][0], srcB);
-                        const float x2 = __shfl_sync(0xffffffffu, wv[nt][1], srcA);
-                        const float x3 = __shfl_sync(0xffffffffu, wv[nt][1], srcB);
-                        if ((hcol >> 2) == nt) {
-                            u[0] = x0;
-                            u[1] = x1;
-                            u[2] = x2;
-                            u[3] = x3;
-                        }
-                    }
-                    if (hcol >= G) u[0] = u[1] = u[2] = u[3] = 0.f;
+                    for (int bw = 0; bw < BPW; ++bw) {
+                        uint32_t X = 0u, Y = 0u;
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const float x0 = u[0] * A[m], x1 = u[1] * A[m], x2 = u[2] * A[m], x3 = u[3] * A[m];
-                        const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
-                        Bh[m][0] = *reinterpret_cast<const uint32_t *>(&h01);
-                        Bh[m][1] = *reinterpret_cast<const uint32_t *>(&h23);
-                        if (m == 1 || m == 2) {
-                            const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
-                            Bl[m][0] = pack_h2(x0 - f01.x, x1 - f01.y);
-                            Bl[m][1] = pack_h2(x2 - f23.x, x3 - f23.y);
-                        } else {
-                            Bl[m][0] = Bl[m][1] = 0u;
-                        }
-                        if (G <= 4) {   // columns 4..7: the lo parts (or zero)
-                            Bh[m][0] = gid >= 4 ? Bl[m][0] : Bh[m][0];
-                            Bh[m][1] = gid >= 4 ? Bl[m][1] : Bh[m][1];
-                        }
-                    }
-                }
-
-                // ---- V side: all 8 m-tiles, the four planes into one accumulator per m-tile
-                {
-                    uint32_t x[4][2];
-#pragma unroll
-                    for (int pl = 0; pl < 3; ++pl) {
-                        const uint2 v = *reinterpret_cast<const uint2 *>(vrec + pl * 2 * D + lane * 8);
-                        x[pl][0] = v.x;
-                        x[pl][1] = v.y;
-                    }
-                    x[3][0] = x[0][0] ^ x[1][0] ^ x[2][0];
-                    x[3][1] = x[0][1] ^ x[1][1] ^ x[2][1];
-                    float O[MT][4], Tacc[4];
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const uint32_t xs0 = x[m][0] << 8, xs1 = x[m][1] << 8;
-#pragma unroll
-                        for (int mt = 0; mt < MT; ++mt) {
-                            const int q = 8 + mt;
-                            const uint32_t msk = 0x00010001u << q, bas = vop_base(q);
-                            const uint32_t a0 = lop_and_xor(xs0, msk, bas), a1 = lop_and_xor(xs1, msk, bas);
-                            const uint32_t a2 = lop_and_xor(x[m][0], msk, bas), a3 = lop_and_xor(x[m][1], msk, bas);
-                            if (m == 0) mma_f16_z(O[mt], a0, a1, a2, a3, Bh[m][0], Bh[m][1]);
-                            else mma_f16(O[mt], a0, a1, a2, a3, Bh[m][0], Bh[m][1]);
-                            if constexpr (G > 4) {
-                                if (m == 1 || m == 2) mma_f16(O[mt], a0, a1, a2, a3, Bl[m][0], Bl[m][1]);
+                        for (int nt = 0; nt < NTK; ++nt) {
+                            const __half2 hh = __floats2half2_rn(wv[bw][nt][0], wv[bw][nt][1]);
+                            const uint32_t wh = *reinterpret_cast<const uint32_t *>(&hh);
+                            if constexpr (G <= 4) {
+                                const float2 fh = __half22float2(hh);
+                                const uint32_t wl = pack_h2(wv[bw][nt][0] - fh.x, wv[bw][nt][1] - fh.y);
+                                const uint32_t xh = __shfl_sync(0xffffffffu, wh, srcX), yh = __shfl_sync(0xffffffffu, wh, srcY);
+                                const uint32_t xl = __shfl_sync(0xffffffffu, wl, srcX), yl = __shfl_sync(0xffffffffu, wl, srcY);
+                                X = gid >= 4 ? xl : xh;
+                                Y = gid >= 4 ? yl : yh;
+                            } else {
+                                const uint32_t x = __shfl_sync(0xffffffffu, wh, srcX), y = __shfl_sync(0xffffffffu, wh, srcY);
+                                if ((hcol >> 2) == nt) {
+                                    X = x;
+                                    Y = y;
+                                }
                             }
                         }
-                        if (m == 0) mma_f16_z(Tacc, one16x2, one16x2, one16x2, one16x2, Bh[m][0], Bh[m][1]);
-                        else mma_f16(Tacc, one16x2, one16x2, one16x2, one16x2, Bh[m][0], Bh[m][1]);
-                        if constexpr (G > 4) {
-                            if (m == 1 || m == 2) mma_f16(Tacc, one16x2, one16x2, one16x2, one16x2, Bl[m][0], Bl[m][1]);
-                        }
+                        if (hcol >= G) X = Y = 0u;
+                        bf0[bw] = prmt(X, Y, 0x5410u);
+                        bf1[bw] = prmt(X, Y, 0x7632u);
                     }
+                }
+
+                // ---- V side: per pair of m-tiles, the operands of both token pairs of every block; the
+                // blocks' mma chained, then one fp32 add
+                {
+                    uint32_t vw[BPW][2][3 * NG];
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt)
+                    for (int bw = 0; bw < BPW; ++bw)
+                        load_vw(sStage + (size_t)(buf * BPW + bw) * REC + KREC, vw[bw]);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) arun[mt][k] += O[mt][k];
+                    for (int g = 0; g < NG; ++g)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) Trun[k] += Tacc[k];
+                        for (int k = 0; k < 4; ++k) {
+                            uint32_t A[BPW][2][4];   // [block][pair][slot 4k + j of the group]
+#pragma unroll
+                            for (int bw = 0; bw < BPW; ++bw)
+#pragma unroll
+                                for (int pp = 0; pp < 2; ++pp) {
+                                    const uint32_t w0 = vw[bw][pp][3 * g], w1 = vw[bw][pp][3 * g + 1], w2 = vw[bw][pp][3 * g + 2];
+                                    const uint32_t sw = k == 3 ? (((w0 >> 3) & 0x11111111u) | ((w1 >> 2) & 0x22222222u) |
+                                                                  ((w2 >> 1) & 0x44444444u))
+                                                               : (vw[bw][pp][3 * g + k] & 0x77777777u);
+#pragma unroll
+                                    for (int hf = 0; hf < 2; ++hf) {
+                                        const uint32_t sel = hf ? (sw >> 16) : sw;
+                                        const uint32_t pl = prmt(L0, L1, sel), phb = prmt(H0, H1, sel);
+                                        A[bw][pp][2 * hf] = prmt(pl, phb, 0x6240u);
+                                        A[bw][pp][2 * hf + 1] = prmt(pl, phb, 0x7351u);
+                                    }
+                                }
+#pragma unroll
+                            for (int hf = 0; hf < 2; ++hf) {
+                                const int mt = 8 * g + 2 * k + hf;
+                                float o[4];
+#pragma unroll
+                                for (int bw = 0; bw < BPW; ++bw) {
+                                    if (bw == 0)
+                                        mma_f16_z(o, A[bw][0][2 * hf], A[bw][0][2 * hf + 1], A[bw][1][2 * hf],
+                                                  A[bw][1][2 * hf + 1], bf0[bw], bf1[bw]);
+                                    else
+                                        mma_f16(o, A[bw][0][2 * hf], A[bw][0][2 * hf + 1], A[bw][1][2 * hf],
+                                                A[bw][1][2 * hf + 1], bf0[bw], bf1[bw]);
+                                }
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) arun[mt][e] += o[e];
+                            }
+                        }
                 }
             }
-            __syncwarp();   // buffer `buf` is restaged in the next iteration
+            __syncwarp();   // buffer `buf` is restaged NBUF - 1 chunks later
         }
 
         // ---- segment end: merge the warps' (m, l, acc) in shared memory
@@ -542,28 +590,22 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
         if constexpr (G <= 4) {
             // columns 4..7 (tig 2, 3) carry the lo parts of heads 0..3 (tig 0, 1): add them in
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float t = __shfl_xor_sync(0xffffffffu, Trun[k], 2);
-                if (tig < 2) Trun[k] += t;
+            for (int k = 0; k < 4; ++k)
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt) {
                     const float o = __shfl_xor_sync(0xffffffffu, arun[mt][k], 2);
                     if (tig < 2) arun[mt][k] += o;
                 }
-            }
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-            const int q = 8 + mt;
-            const float al = vop_alpha(q), inv_de = 2.f / vop_delta(q);
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int h = 2 * tig + e;
                 if (h < G && (G > 4 || tig < 2)) {
-                    const float T = Trun[e];
 #pragma unroll
                     for (int r = 0; r < 2; ++r)
-                        sAccW[(warp * G + h) * D + 16 * mt + gid + 8 * r] = (arun[mt][2 * r + e] - al * T) * inv_de - T;
+                        sAccW[(warp * G + h) * D + 16 * mt + gid + 8 * r] = arun[mt][2 * r + e] * inv_alpha;
                 }
             }
         }
@@ -611,36 +653,63 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                     dst[1] = sL[h];
                 }
             }
-            __threadfence();
+            // one thread publishes the CTA's partials: its acquire-release add orders every write of
+            // the CTA before the barrier ahead of the count, and (for the CTA that completes the
+            // count) every other CTA's partials ahead of the reads after the next barrier
             __syncthreads();
             if (tid == 0) {
                 const unsigned int nseg = (unsigned int)(hi - lo + 1);
-                const unsigned int done = atomicAdd(&counters[b * hkv + kh], 1u) + 1u;
-                s_last = (done == nseg);
+                unsigned int done;
+                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                             : "=r"(done) : "l"(counters + b * hkv + kh) : "memory");
+                s_last = (done + 1u == nseg);
                 if (s_last) counters[b * hkv + kh] = 0u;
             }
             __syncthreads();
             if (s_last) {
-                __threadfence();
+                // The partials of the CTAs lo..hi, merged by log-sum-exp.  Their (m, l) are read one
+                // per lane, their value rows UN at a time, so every wait covers many loads.
                 const int slot_lo = (sk_begin(lo, P, W) >= us) ? 0 : 1;
+                const int np = hi - lo + 1;
+                constexpr int UN = 32 / R;
                 for (int h = warp; h < G; h += NWARP) {
+                    auto part_of = [&](int j) {
+                        const int c2 = lo + j, sl = (c2 == lo) ? slot_lo : 0;
+                        return part + (((size_t)c2 * 2 + sl) * G + h) * kPartStride(D);
+                    };
                     float M = -INFINITY;
-                    for (int c2 = lo; c2 <= hi; ++c2) {
-                        const int sl = (c2 == lo) ? slot_lo : 0;
-                        M = fmaxf(M, __ldcg(part + (((size_t)c2 * 2 + sl) * G + h) * kPartStride(D)));
+                    for (int j = lane; j < np; j += 32) M = fmaxf(M, __ldcg(part_of(j)));
+                    M = warp_max(M);
+                    float l = 0.f;
+                    for (int j = lane; j < np; j += 32) {
+                        const float *ps = part_of(j);
+                        const float m = __ldcg(ps), lp = __ldcg(ps + 1);
+                        l += (m == -INFINITY) ? 0.f : lp * exp2f(m - M);
                     }
+                    l = warp_sum(l);
                     float v[R];
 #pragma unroll
                     for (int r = 0; r < R; ++r) v[r] = 0.f;
-                    float l = 0.f;
-                    for (int c2 = lo; c2 <= hi; ++c2) {
-                        const int sl = (c2 == lo) ? slot_lo : 0;
-                        const float *ps = part + (((size_t)c2 * 2 + sl) * G + h) * kPartStride(D);
-                        const float m = __ldcg(ps);
-                        const float wgt = (m == -INFINITY) ? 0.f : exp2f(m - M);
-                        l = fmaf(__ldcg(ps + 1), wgt, l);
+#pragma unroll 1
+                    for (int j0 = 0; j0 < np; j0 += UN) {
+                        float vv[UN][R], ww[UN];
 #pragma unroll
-                        for (int r = 0; r < R; ++r) v[r] = fmaf(__ldcg(ps + 4 + 32 * r + lane), wgt, v[r]);
+                        for (int u = 0; u < UN; ++u) {
+                            ww[u] = 0.f;
+#pragma unroll
+                            for (int r = 0; r < R; ++r) vv[u][r] = 0.f;
+                            if (j0 + u < np) {
+                                const float *ps = part_of(j0 + u);
+                                const float m = __ldcg(ps);
+#pragma unroll
+                                for (int r = 0; r < R; ++r) vv[u][r] = __ldcg(ps + 4 + 32 * r + lane);
+                                ww[u] = (m == -INFINITY) ? 0.f : exp2f(m - M);
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < UN; ++u)
+#pragma unroll
+                            for (int r = 0; r < R; ++r) v[r] = fmaf(vv[u][r], ww[u], v[r]);
                     }
                     finish_row<D>(v, l, params, out + out_row(h) * D, lane);
                     if (lse && lane == 0) lse[out_row(h)] = l > 0.f ? M * kLn2 + logf(l) : -INFINITY;
@@ -649,17 +718,17 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
         }
         if (!more_segs) break;
         first_seg = false;
-        s = ns;   // its first chunk is already staged in `buf`
+        s = ns;   // its first chunks are already staged
     }
 }
 
-template <int G>
+template <int D, int G>
 int warp_ctas_g() {
     int dev = 0, sms = 0, occ = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    constexpr size_t smem = warp_smem_bytes<G>();
-    auto kern = decode_warp_kernel<G>;
+    constexpr size_t smem = warp_smem_bytes<D, G>();
+    auto kern = decode_warp_kernel<D, G>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kWWarps * 32, smem) != cudaSuccess) return 0;
     occ = occ < 1 ? 1 : (occ > kCtasPerSm ? kCtasPerSm : occ);
@@ -667,39 +736,39 @@ int warp_ctas_g() {
     return occ * sms;
 }
 
-template <int G>
+template <int D, int G>
 cudaError_t warp_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
                           const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
                           const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
                           float *lse, int32_t *status) {
-    constexpr size_t smem = warp_smem_bytes<G>();
-    auto kern = decode_warp_kernel<G>;
+    constexpr size_t smem = warp_smem_bytes<D, G>();
+    auto kern = decode_warp_kernel<D, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_pass(kern, nctas, kWWarps * 32, smem, st, P, w.packs, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx,
                        ctx_add, max_ctx, w.cpre, w.cta_b, w.part, w.counters, out, lse, status);
 }
 
-}  // namespace
-
-int warp_pass_ctas(int G) {
+template <int D>
+int warp_ctas_d(int G) {
     switch (G) {
-        case 1: return warp_ctas_g<1>();
-        case 2: return warp_ctas_g<2>();
-        case 3: return warp_ctas_g<3>();
-        case 4: return warp_ctas_g<4>();
-        case 5: return warp_ctas_g<5>();
-        case 6: return warp_ctas_g<6>();
-        case 7: return warp_ctas_g<7>();
-        default: return warp_ctas_g<8>();
+        case 1: return warp_ctas_g<D, 1>();
+        case 2: return warp_ctas_g<D, 2>();
+        case 3: return warp_ctas_g<D, 3>();
+        case 4: return warp_ctas_g<D, 4>();
+        case 5: return warp_ctas_g<D, 5>();
+        case 6: return warp_ctas_g<D, 6>();
+        case 7: return warp_ctas_g<D, 7>();
+        default: return warp_ctas_g<D, 8>();
     }
 }
 
-cudaError_t warp_pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
-                             const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
-                             const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
-                             float *lse, int32_t *status) {
-#define TQ_WPASS(GG) return warp_launch_g<GG>(nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out, lse, status)
+template <int D>
+cudaError_t warp_launch_d(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
+                          const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
+                          const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
+                          float *lse, int32_t *status) {
+#define TQ_WPASS(GG) return warp_launch_g<D, GG>(nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out, lse, status)
     switch (G) {
         case 1: TQ_WPASS(1);
         case 2: TQ_WPASS(2);
@@ -711,6 +780,21 @@ cudaError_t warp_pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P
         default: TQ_WPASS(8);
     }
 #undef TQ_WPASS
+}
+
+}  // namespace
+
+int warp_pass_ctas(int d, int G) { return d == 128 ? warp_ctas_d<128>(G) : warp_ctas_d<256>(G); }
+
+cudaError_t warp_pass_launch(int d, int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq,
+                             int hkv, const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
+                             const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
+                             float *lse, int32_t *status) {
+    if (d == 128)
+        return warp_launch_d<128>(G, nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w,
+                                  out, lse, status);
+    return warp_launch_d<256>(G, nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out,
+                              lse, status);
 }
 
 }  // namespace tq

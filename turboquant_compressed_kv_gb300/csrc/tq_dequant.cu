@@ -85,32 +85,41 @@ dequant_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ p
 #pragma unroll
         for (int jj = 0; jj < PER_WARP; ++jj) {
             const int t = warp + kDqWarps * jj;   // slot in the block
+            const uint32_t *words = reinterpret_cast<const uint32_t *>(rec);
             if (is_k) {
-                constexpr int NW = D / 128;
-                constexpr size_t PW = 2 * D / 4;   // words per plane
-                const uint32_t *planes = reinterpret_cast<const uint32_t *>(rec);
+                // field of coordinate x: bits 4f .. 4f+3 of word (L * 2 + row) * d/32 + ks / 2
+                constexpr int NW = D / 32;
                 const int gid = t & 7, th = t >> 3;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const size_t word = (size_t)((4 * gid + (r & 3)) * 2 + th) * NW + (r >> 2);
-                    const int c = (int)((planes[word] >> lane) & 1u) | (int)(((planes[PW + word] >> lane) & 1u) << 1) |
-                                  (int)(((planes[2 * PW + word] >> lane) & 1u) << 2);
-                    val[jj][r] = s_cent[c] * inv_sd;
-                    s_b[t][dims[r]] = ((planes[3 * PW + word] >> lane) & 1u) ? 1.f : -1.f;
+                    const int x = dims[r], ks = x >> 4, c = x & 15;
+                    const int f = 4 * (ks & 1) + (c & 1) + 2 * (c >> 3);
+                    const uint32_t nib = (words[((4 * gid + ((c & 7) >> 1)) * 2 + th) * NW + (ks >> 1)] >> (4 * f)) & 15u;
+                    val[jj][r] = s_cent[nib & 7u] * inv_sd;
+                    s_b[t][x] = (nib & 8u) ? 1.f : -1.f;
                 }
                 const __half2 ng = *reinterpret_cast<const __half2 *>(rec + 8 * D + 4 * t);
                 nrm[jj] = __low2float(ng);
                 gam[jj] = __high2float(ng);
             } else {
-                constexpr int NWV = D / 64, NM = D / 128;
-                const int tigv = (t & 7) >> 1, jb = (t >> 3) + 2 * (t & 1), beta = lane >> 3;
+                // lane slot s = 2 mt + rr of coordinate x, groups of 16 slots: 12 fields, then 4 cells kept
+                // in bit 3 of the fields of the group's three words
+                constexpr int NG = D / 128;
+                const int tigv = (t & 7) >> 1, pr = t >> 3, e = t & 1;
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    const int tau = 4 * r + beta;
-                    const int mhi = tau % NM, rh = (tau / NM) & 1, gid = tau / (2 * NM);
-                    const size_t byte = ((size_t)(4 * gid + tigv) * NWV + 2 * mhi + rh) * 4 + jb;
-                    const int c = ((rec[byte] >> (lane & 7)) & 1) | (((rec[2 * D + byte] >> (lane & 7)) & 1) << 1) |
-                                  (((rec[4 * D + byte] >> (lane & 7)) & 1) << 2);
+                    const int x = dims[r], sl = 2 * (x >> 4) + ((x >> 3) & 1), g = sl >> 4, sg = sl & 15;
+                    const int base = ((4 * (x & 7) + tigv) * 2 + pr) * 3 * NG + 3 * g;
+                    int c;
+                    if (sg < 12) {
+                        const int f = 4 * ((sg >> 1) & 1) + 2 * e + (sg & 1);
+                        c = (int)((words[base + (sg >> 2)] >> (4 * f)) & 7u);
+                    } else {
+                        const int f = 4 * ((sg - 12) >> 1) + 2 * e + (sg & 1);
+                        c = 0;
+#pragma unroll
+                        for (int q = 0; q < 3; ++q) c |= (int)((words[base + q] >> (4 * f + 3)) & 1u) << q;
+                    }
                     val[jj][r] = s_cent[c] * inv_sd;
                 }
                 nrm[jj] = __half2float(*reinterpret_cast<const __half *>(rec + 6 * D + 2 * t));
@@ -162,8 +171,8 @@ dequant_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ p
 // warpgroup owns row r:
 //  1. the tile's records arrive by bulk copy (two tiles in flight per warpgroup);
 //  2. the row's 128 sign bits become the A operand (f16 +-1, 128-byte swizzle) with one shift
-//     and one LOP3 per two elements: K index 32 tig + 2 p + e holds coordinate
-//     16 (p & 7) + 8 (p >> 3) + 2 tig + e, whose bit is bit p + 16 e of sign word tig;
+//     and one LOP3 per two elements: K index 32 tig + 8 w + 2 p + e holds the sign bit of field
+//     p + 4 e of the slot's word (tig, w), bit 4 (p + 4 e) + 3;
 //  3. one thread issues p = S^T b as S_hi + S_lo (B rows = output coordinates, K-major, 16
 //     f16 MMAs of K = 16) into the warpgroup's 128 tensor-memory columns;
 //  4. the thread reads its row back (tcgen05.ld), adds the codebook values, runs the 128-point
@@ -190,10 +199,10 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     __shared__ uint64_t recbar[kWg][2], mmabar[kWg];
     __shared__ uint32_t tmem_base;
     __shared__ float s_D[D];
-    // centroid pairs (x 1/sqrt d) of two coordinates, by the 6-bit index a | b << 2 | c << 4,
-    // where a, b, c hold the two coordinates' bits of planes 0, 1, 2; one copy per lane
-    // ([index][lane]), so that a half-warp's lookups never share a bank
-    __shared__ float2 s_pair[64][32];
+    // centroid pairs (x 1/sqrt d) of two fields, by a record byte masked to its cell bits (0x77):
+    // entry i holds c[i & 7], c[i >> 4]; one copy per lane ([index][lane]), so that a half-warp's
+    // lookups never share a bank
+    __shared__ float2 s_pair[128][32];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     if (ph->magic != kParamsMagic || ph->d != D) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
@@ -211,19 +220,18 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     }
     constexpr uint32_t kTmemCols = kWg <= 2 ? 256 : 512;   // 128 columns per warpgroup, a power of two
     if (warp == 0) tc::tmem_alloc(&tmem_base, kTmemCols);
-    for (int e = tid; e < 64 * 32; e += kThreads) {
-        const int i = e >> 5, a = i & 3, b = (i >> 2) & 3, c = i >> 4;
-        const int lo = (a & 1) | ((b & 1) << 1) | ((c & 1) << 2), hi = (a >> 1) | ((b >> 1) << 1) | ((c >> 1) << 2);
+    for (int e = tid; e < 128 * 32; e += kThreads) {
+        const int i = e >> 5;
         const float isd = rsqrtf((float)D);
-        s_pair[i][e & 31] = make_float2(ph->centroid[lo] * isd, ph->centroid[hi] * isd);
+        s_pair[i][e & 31] = make_float2(ph->centroid[i & 7] * isd, ph->centroid[(i >> 4) & 7] * isd);
     }
     if (tid < D) s_D[tid] = reinterpret_cast<const float *>(params + params_off_D(D))[tid];
     {   // B: row n = output coordinate n, K index k' as in the A operand; S as f16 hi + lo
         const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
         for (int e = tid; e < D * D; e += kThreads) {
             const int n = e >> 7, k = e & 127;
-            const int tig = k >> 5, p = (k & 31) >> 1, ee = k & 1;
-            const int coord = 16 * (p & 7) + 8 * (p >> 3) + 2 * tig + ee;
+            const int tig = k >> 5, w = (k >> 3) & 3, f = ((k >> 1) & 3) + 4 * (k & 1);
+            const int coord = 16 * (2 * w + (f >> 2)) + 2 * tig + (f & 1) + 8 * ((f >> 1) & 1);
             const float sv = __ldg(S + coord * D + n);
             const __half hi = __float2half_rn(sv);
             const __half lo = __float2half_rn(sv - __half2float(hi));
@@ -280,17 +288,15 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
         const bool good = live && blk >= 0 && blk < num_blocks;
         if (live && !good && t == 0) flag_status(status, TQ_STATUS_BAD_SLOT);
         const uint8_t *rec = smem + oR + ((wg * 2 + buf) * kUnits + unit_k) * kRec;
-        const uint32_t *planes = reinterpret_cast<const uint32_t *>(rec);
-        constexpr int PW = 2 * D / 4;
         const int gid = t & 7, th = t >> 3;
-        uint32_t cw[3][4], sw[4];
+        uint32_t kw[4][4];   // the slot's words [tig][w]
 #pragma unroll
         for (int tig = 0; tig < 4; ++tig) {
-            const int word = (4 * gid + tig) * 2 + th;
-            cw[0][tig] = live ? planes[word] : 0u;
-            cw[1][tig] = live ? planes[PW + word] : 0u;
-            cw[2][tig] = live ? planes[2 * PW + word] : 0u;
-            sw[tig] = live ? planes[3 * PW + word] : 0u;
+            const uint4 v = live ? reinterpret_cast<const uint4 *>(rec)[(4 * gid + tig) * 2 + th] : make_uint4(0u, 0u, 0u, 0u);
+            kw[tig][0] = v.x;
+            kw[tig][1] = v.y;
+            kw[tig][2] = v.z;
+            kw[tig][3] = v.w;
         }
         const __half2 ng = live ? *reinterpret_cast<const __half2 *>(rec + 8 * D + 4 * t) : __floats2half2_rn(0.f, 0.f);
         const float nrm = __low2float(ng), gam = __high2float(ng);
@@ -301,10 +307,7 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
             for (int c = 0; c < 4; ++c) {
                 uint32_t r4[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int p = 4 * c + q;
-                    r4[q] = ((sw[tig] << (15 - p)) & 0x80008000u) ^ 0xBC00BC00u;
-                }
+                for (int q = 0; q < 4; ++q) r4[q] = ((kw[tig][c] << (12 - 4 * q)) & 0x80008000u) ^ 0xBC00BC00u;
                 *reinterpret_cast<uint4 *>(sA + tc::sw128_off(row, 32 * tig + 8 * c, kRows)) =
                     make_uint4(r4[0], r4[1], r4[2], r4[3]);
             }
@@ -339,24 +342,19 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
         }
         tc::fence_before_sync();
         const float gq = qjl * gam;
-        // byte j of plane word tig holds bits s = 0..7 of coordinates 16 s + 8 (j & 1) + 2 tig + (j >> 1);
-        // the three planes' bytes side by side, then two coordinates per table lookup (the multiply
-        // by 4161 = 2^12 + 2^6 + 1 lines the three 2-bit fields up in bits 12 + s .. 17 + s)
+        // byte q of word (tig, w) holds fields 2q, 2q + 1: coordinates x and x + 1 with
+        // x = 16 (2 w + (q >> 1)) + 2 tig + 8 (q & 1); one table lookup per byte
 #pragma unroll
         for (int tig = 0; tig < 4; ++tig)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t x = __byte_perm(__byte_perm(cw[0][tig], cw[1][tig], (uint32_t)j | ((uint32_t)(4 + j) << 4)),
-                                               cw[2][tig], 0x10u | ((uint32_t)(4 + j) << 8));
-                const int base = 8 * (j & 1) + 2 * tig + (j >> 1);
+            for (int w = 0; w < 4; ++w)
 #pragma unroll
-                for (int s2 = 0; s2 < 8; s2 += 2) {
-                    const uint32_t v = x & (0x030303u << s2);
-                    const float2 cc = s_pair[(v * 4161u >> (12 + s2)) & 63u][tid & 31];
-                    y[16 * s2 + base] = fmaf(gq, y[16 * s2 + base], cc.x);
-                    y[16 * (s2 + 1) + base] = fmaf(gq, y[16 * (s2 + 1) + base], cc.y);
+                for (int q = 0; q < 4; ++q) {
+                    const float2 cc = s_pair[(kw[tig][w] >> (8 * q)) & 0x77u][tid & 31];
+                    const int x = 16 * (2 * w + (q >> 1)) + 2 * tig + 8 * (q & 1);
+                    y[x] = fmaf(gq, y[x], cc.x);
+                    y[x + 1] = fmaf(gq, y[x + 1], cc.y);
                 }
-            }
         // inverse rotation: D (H y) / sqrt d, then the norm
 #pragma unroll
         for (int st = 1; st < D; st <<= 1)
@@ -399,8 +397,8 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
 // ---------------------------------------------------------------- V at d = 128, one thread per row
 // A CTA of 128 threads walks tiles of 8 records (128 rows); thread r owns row r:
 //  1. the tile's records arrive by bulk copy, two tiles in flight;
-//  2. the row's cells are read back plane word by plane word (each V word holds 8 coordinates of
-//     four slots; the slot's bits are pre-shifted once), y = c[cell] / sqrt d;
+//  2. the row's cells are read back word by word (each V byte holds two cells of one slot and one
+//     bit of two more), y = c[cell] / sqrt d by one table lookup per byte;
 //  3. the 128-point inverse transform in registers, the norm and D, and 16-byte stores.
 namespace dq128v {
 constexpr int D = 128, kRows = 128, kUnits = kRows / kBlock, kThreads = 128, kMinCtas = 3;
@@ -417,10 +415,10 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint64_t recbar[2], recfree[2];
     __shared__ float s_D[D];
-    // centroid pairs (x 1/sqrt d) of two neighbouring coordinates, by the 6-bit index
-    // a | b << 2 | c << 4, where a, b, c hold the two coordinates' bits of planes 0, 1, 2; one copy
-    // per lane ([index][lane]), so that a half-warp's lookups never share a bank
-    __shared__ float2 s_pair[64][32];
+    // centroid pairs (x 1/sqrt d) of two fields, by a record byte masked to its cell bits (0x77):
+    // entry i holds c[i & 7], c[i >> 4]; one copy per lane ([index][lane]), so that a half-warp's
+    // lookups never share a bank
+    __shared__ float2 s_pair[128][32];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     if (ph->magic != kParamsMagic || ph->d != D) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
@@ -436,10 +434,9 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
         tc::mbar_init(&recfree[1], kThreads / 32);
     }
     const float inv_sd = rsqrtf((float)D);
-    for (int e = row; e < 64 * 32; e += kThreads) {
-        const int i = e >> 5, a = i & 3, b = (i >> 2) & 3, c = i >> 4;
-        const int lo = (a & 1) | ((b & 1) << 1) | ((c & 1) << 2), hi = (a >> 1) | ((b >> 1) << 1) | ((c >> 1) << 2);
-        s_pair[i][e & 31] = make_float2(ph->centroid[lo] * inv_sd, ph->centroid[hi] * inv_sd);
+    for (int e = row; e < 128 * 32; e += kThreads) {
+        const int i = e >> 5;
+        s_pair[i][e & 31] = make_float2(ph->centroid[i & 7] * inv_sd, ph->centroid[(i >> 4) & 7] * inv_sd);
     }
     const int lane = row & 31;
     s_D[row] = reinterpret_cast<const float *>(params + params_off_D(D))[row];
@@ -480,32 +477,37 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
         const bool good = live && blk >= 0 && blk < num_blocks;
         if (live && !good && t == 0) flag_status(status, TQ_STATUS_BAD_SLOT);
         const uint8_t *rec = smem + (buf * kUnits + unit_k) * kRec;
-        const uint32_t *planes = reinterpret_cast<const uint32_t *>(rec);
-        // coordinate n = 16 mt + r of slot t: word 2 (4 (r & 7) + (t & 7) / 2) + (r >> 3) of each
-        // plane, bit 8 (t >> 3) + 16 (t & 1) + mt
-        constexpr int PW = 2 * D / 4;   // words per plane
-        const int a = (t & 7) >> 1, bi = (t >> 3) + 2 * (t & 1);   // the slot's byte in each plane word
-        // byte bi of planes 0 and 1 into bytes 0 and 1, then byte bi of plane 2 into byte 2
-        const uint32_t sel01 = (uint32_t)bi | ((uint32_t)(4 + bi) << 4), sel2 = 0x10u | ((uint32_t)(4 + bi) << 8);
+        const uint32_t *words = reinterpret_cast<const uint32_t *>(rec);
+        // the slot's bytes: per lane gid, words 3 (L * 2 + pair) + k (k = 0..2), bytes 2 hf + e.
+        // Byte (k, hf) holds the cells of lane slots 4k + 2hf + ab (ab = 0, 1: coordinates
+        // 16 (2k + hf) + gid + 8 ab) in bits 4ab .. 4ab + 2, and in bit 4ab + 3 bit k of the cell of
+        // lane slot 12 + 2hf + ab (coordinate 16 (6 + hf) + gid + 8 ab)
+        const int a = (t & 7) >> 1, pr = t >> 3, e = t & 1;
         float y[D];
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
+        for (int gid = 0; gid < 8; ++gid) {
+            uint32_t bt[3][2];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int word = 2 * (4 * c + a) + h;
-                const uint32_t x = __byte_perm(__byte_perm(planes[word], planes[PW + word], sel01),
-                                               planes[2 * PW + word], sel2);
-#pragma unroll
-                for (int mt = 0; mt < 8; mt += 2) {
-                    // bits mt, mt + 1 of the three bytes; the multiply by 4161 = 2^12 + 2^6 + 1 lines
-                    // the three 2-bit fields up in bits 12 + mt .. 17 + mt without carries
-                    const uint32_t v = x & (0x030303u << mt);
-                    const uint32_t idx = (v * 4161u >> (12 + mt)) & 63u;
-                    const float2 cc = s_pair[idx][lane];
-                    y[16 * mt + 8 * h + c] = cc.x;
-                    y[16 * (mt + 1) + 8 * h + c] = cc.y;
-                }
+            for (int k = 0; k < 3; ++k) {
+                const uint32_t w = words[((4 * gid + a) * 2 + pr) * 3 + k];
+                bt[k][0] = (w >> (8 * e)) & 0xFFu;
+                bt[k][1] = (w >> (16 + 8 * e)) & 0xFFu;
             }
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                for (int k = 0; k < 3; ++k) {
+                    const float2 cc = s_pair[bt[k][hf] & 0x77u][lane];
+                    y[16 * (2 * k + hf) + gid] = cc.x;
+                    y[16 * (2 * k + hf) + gid + 8] = cc.y;
+                }
+                // bit 3 (ab = 0) and bit 7 (ab = 1) of the three bytes: the cells of slots 12 + 2hf + ab
+                const uint32_t sp = ((bt[0][hf] >> 3) & 0x11u) | ((bt[1][hf] >> 2) & 0x22u) | ((bt[2][hf] >> 1) & 0x44u);
+                const float2 cc = s_pair[sp][lane];
+                y[16 * (6 + hf) + gid] = cc.x;
+                y[16 * (6 + hf) + gid + 8] = cc.y;
+            }
+        }
         const __half nh = *reinterpret_cast<const __half *>(rec + 6 * D + 2 * t);
         tc::fence_async_smem();
         __syncwarp();

@@ -53,6 +53,17 @@ encode_kernel(const uint8_t *__restrict__ params, const T *__restrict__ xk, cons
 //     column 32 tig + b is sign bit b of sign word tig); the thread reads its row back and packs
 //     the signs;
 //  5. the record words of the row's slot are stored.
+// QJL accumulator column n of the d = 128 tcgen05 encoders -> the coordinate whose sign it is.
+// Columns 64 h + 16 tig + 8 wl + f are field f of K word (tig, 2 h + wl) of a slot (the record
+// layout of tq_internal.cuh), so a thread's 16-column read back covers two of its words.
+__host__ __device__ constexpr int k_col_coord(int n) {
+    return 16 * (2 * (2 * (n >> 6) + ((n >> 3) & 1)) + ((n & 7) >> 2)) + 2 * ((n >> 4) & 3) + (n & 1) + 8 * ((n >> 1) & 1);
+}
+// field position of coordinate n (0..127) of a K record word: (tig, word, field)
+__host__ __device__ constexpr int k_tig(int n) { return ((n & 15) & 7) >> 1; }
+__host__ __device__ constexpr int k_word(int n) { return n >> 5; }
+__host__ __device__ constexpr int k_field(int n) { return 4 * ((n >> 4) & 1) + (n & 1) + 2 * ((n & 15) >> 3); }
+
 namespace encr {
 constexpr int D = 128, kRows = 128, kThreads = 256;
 template <typename T> __host__ __device__ constexpr int nx() { return sizeof(T) == 2 ? 2 : 1; }   // tiles in flight per warpgroup
@@ -99,12 +110,11 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
     }
     if (IS_K && warp == 0) tc::tmem_alloc(&tmem_base, 512);
     if (tid < D) s_D[tid] = reinterpret_cast<const float *>(params + params_off_D(D))[tid];
-    if (IS_K) {   // B row n = S row sigma(n), sigma(32 tig + b) = 16 (b & 7) + 8 ((b >> 3) & 1) + 2 tig + (b >> 4)
+    if (IS_K) {   // B row n = S row k_col_coord(n)
         const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
         for (int e = tid; e < D * D; e += n_threads<IS_K>()) {
             const int n = e >> 7, k = e & 127;
-            const int tig = n >> 5, b = n & 31;
-            const int sr = 16 * (b & 7) + 8 * ((b >> 3) & 1) + 2 * tig + (b >> 4);
+            const int sr = k_col_coord(n);
             const float sv = __ldg(S + sr * D + k);
             const __half hi = __float2half_rn(sv);
             const __half lo = __float2half_rn(sv - __half2float(hi));
@@ -205,7 +215,10 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
         // cell 4); K needs z itself for the residual.
         const float ns = (IS_K || nrm == 0.f) ? 1.f : nrm, zs = IS_K ? rn : 1.f;
         const float T0 = t0 * ns, T1 = t1 * ns, T2 = t2 * ns, T3 = t3 * ns, T4 = t4 * ns, T5 = t5 * ns, T6 = t6 * ns;
-        uint32_t w[3][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
+        // K: the 16 words of the slot's fields, [tig][word]; V: the 48 bytes of the slot, byte
+        // (gid, k, hf) at q = 6 gid + 2 k + hf of vb (4 per register)
+        uint32_t kwd[4][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
+        uint32_t vb[12] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
         float g2 = 0.f;
 #pragma unroll
         for (int n = 0; n < D; ++n) {
@@ -213,25 +226,31 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
             const bool b2 = z >= T3;
             const bool b1 = z >= (b2 ? T5 : T1);
             const bool b0 = z >= (b2 ? (b1 ? T6 : T4) : (b1 ? T2 : T0));
+            const uint32_t cell = (uint32_t)b0 | ((uint32_t)b1 << 1) | ((uint32_t)b2 << 2);
             if (IS_K) {
-                const int tig = (n >> 1) & 3, bit = 8 * ((n >> 3) & 1) + (n >> 4) + 16 * (n & 1);
-                w[0][tig] |= (uint32_t)b0 << bit;
-                w[1][tig] |= (uint32_t)b1 << bit;
-                w[2][tig] |= (uint32_t)b2 << bit;
+                kwd[k_tig(n)][k_word(n)] |= cell << (4 * k_field(n));
                 const float c = b2 ? (b1 ? (b0 ? cen[7] : cen[6]) : (b0 ? cen[5] : cen[4]))
                                    : (b1 ? (b0 ? cen[3] : cen[2]) : (b0 ? cen[1] : cen[0]));
                 const float rho = z - c;
                 g2 = fmaf(rho, rho, g2);
                 val[n] = rho * 256.f;   // exact scaling; keeps the f16 low parts out of the subnormals
             } else {
-                // V: coordinate n = 16 mt + gid + 8 rh is bit mt of byte 2 gid + rh (bytes 4 per word)
-                const int byte = 2 * (n & 7) + ((n >> 3) & 1), bit = 8 * (byte & 3) + (n >> 4);
-                w[0][byte >> 2] |= (uint32_t)b0 << bit;
-                w[1][byte >> 2] |= (uint32_t)b1 << bit;
-                w[2][byte >> 2] |= (uint32_t)b2 << bit;
+                // V: coordinate n = 16 mt + gid + 8 ab; lane slot s = 2 mt + ab.  Slots 0..11 are the
+                // field ab (bits 0..2) of byte (gid, k = mt >> 1, hf = mt & 1); slots 12..15 give bit k
+                // of their cell to bit 3 of the field ab of byte (gid, k, hf = mt - 6), k = 0..2
+                const int mt = n >> 4, gid = n & 7, ab = (n >> 3) & 1;
+                if (mt < 6) {
+                    const int q = 6 * gid + 2 * (mt >> 1) + (mt & 1);
+                    vb[q >> 2] |= cell << (8 * (q & 3) + 4 * ab);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 3; ++k) {
+                        const int q = 6 * gid + 2 * k + (mt - 6);
+                        vb[q >> 2] |= ((cell >> k) & 1u) << (8 * (q & 3) + 4 * ab + 3);
+                    }
+                }
             }
         }
-        uint32_t sgn[4] = {0u, 0u, 0u, 0u};
         if constexpr (IS_K) {
             // ---- 4. rho (x 256) as f16 hi / lo into this row's tensor-memory lane, then S rho
             const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
@@ -278,7 +297,8 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
 #pragma unroll
                 for (int b = 0; b < 16; ++b) asm volatile("" : "+f"(pv[b]));   // no use moves above the wait
 #pragma unroll
-                for (int b = 0; b < 16; ++b) sgn[j >> 1] |= (pv[b] >= 0.f ? 1u : 0u) << (16 * (j & 1) + b);
+                for (int b = 0; b < 16; ++b)   // column 16 j + b: field b & 7 of word (tig j & 3, 2 (j >> 2) + (b >> 3))
+                    kwd[j & 3][2 * (j >> 2) + (b >> 3)] |= (pv[b] >= 0.f ? 8u : 0u) << (4 * (b & 7));
             }
             tc::fence_before_sync();
         }
@@ -288,28 +308,20 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
             const int o = (int)(slot % kBlock), head = (int)(v % map.n_heads);
             if (IS_K) {
                 uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * k_record(D);
-                uint32_t *planes = reinterpret_cast<uint32_t *>(rec);
-                constexpr int PW = 2 * D / 4;
                 const int gid = o & 7, th = o >> 3;
 #pragma unroll
-                for (int tig = 0; tig < 4; ++tig) {
-                    const int word = (4 * gid + tig) * 2 + th;
-                    planes[word] = w[0][tig];
-                    planes[PW + word] = w[1][tig];
-                    planes[2 * PW + word] = w[2][tig];
-                    planes[3 * PW + word] = sgn[tig];
-                }
+                for (int tig = 0; tig < 4; ++tig)
+                    reinterpret_cast<uint4 *>(rec)[(4 * gid + tig) * 2 + th] =
+                        make_uint4(kwd[tig][0], kwd[tig][1], kwd[tig][2], kwd[tig][3]);
                 const float gam = sqrtf(g2) * inv_sd;
                 *reinterpret_cast<__half2 *>(rec + 8 * D + 4 * o) = __halves2half2(__float2half_rn(nrm), __float2half_rn(gam));
             } else {
                 uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * v_record(D);
-                const int tigv = (o & 7) >> 1, jb = (o >> 3) + 2 * (o & 1);
+                const int tigv = (o & 7) >> 1, pr = o >> 3, e = o & 1;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {   // byte k = 2 gid + rh of each plane
-                    const int gid = k >> 1, rh = k & 1;
-                    const size_t byte = ((size_t)(4 * gid + tigv) * 2 + rh) * 4 + jb;
-#pragma unroll
-                    for (int p = 0; p < 3; ++p) rec[p * 2 * D + byte] = (uint8_t)(w[p][k >> 2] >> (8 * (k & 3)));
+                for (int q = 0; q < 48; ++q) {   // byte (gid, k, hf) of word 3 (L * 2 + pair) + k, byte 2 hf + e
+                    const int gid = q / 6, k = (q % 6) >> 1, hf = q & 1;
+                    rec[((size_t)((4 * gid + tigv) * 2 + pr) * 3 + k) * 4 + 2 * hf + e] = (uint8_t)(vb[q >> 2] >> (8 * (q & 3)));
                 }
                 *reinterpret_cast<__half *>(rec + 6 * D + 2 * o) = __float2half_rn(nrm);
             }
@@ -333,9 +345,9 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
 //    registers; its outputs are coordinates 64 h + m (the stages of the transform commute);
 //  * each half reads the whole row (that first stage needs it; the sums of squares of the two
 //    halves' outputs add to twice the squared norm);
-//  * a plane word holds bits of both halves (half h owns bits n >> 4 = 4h .. 4h + 3 of each byte):
-//    half 1 leaves its partial words and its residual sum in shared memory, half 0 merges and
-//    stores them; accumulator columns 64 h .. 64 h + 63 are sign words 2h, 2h + 1, stored by half h.
+//  * the record words of coordinates 64 h .. 64 h + 63 (words 2h, 2h + 1 of each tig, cells and QJL
+//    sign bits: accumulator columns 64 h .. 64 h + 63) belong to half h, which stores them; half 1
+//    leaves its residual sum in shared memory for half 0, which stores the norms.
 // Two tile groups of 256 threads take alternate tiles of 128 rows.
 namespace encs {
 constexpr int D = 128, kRows = 128, kTg = 2, kThreads = 256 * kTg;
@@ -382,12 +394,11 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
         const int hh = tid >> 7, k = (tid >> 6) & 1, m = tid & 63;
         s_Dh[hh][k][m] = (k && hh) ? -Dp[64 + m] : Dp[64 * k + m];
     }
-    {   // B row n = S row sigma(n), sigma(32 tig + b) = 16 (b & 7) + 8 ((b >> 3) & 1) + 2 tig + (b >> 4)
+    {   // B row n = S row k_col_coord(n)
         const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
         for (int e = tid; e < D * D; e += kThreads) {
             const int n = e >> 7, k = e & 127;
-            const int tig = n >> 5, b = n & 31;
-            const int sr = 16 * (b & 7) + 8 * ((b >> 3) & 1) + 2 * tig + (b >> 4);
+            const int sr = k_col_coord(n);
             const float sv = __ldg(S + sr * D + k);
             const __half hi = __float2half_rn(sv);
             const __half lo = __float2half_rn(sv - __half2float(hi));
@@ -492,7 +503,8 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
         // ---- 3. cells of coordinates 64 h + m, residual.  The search compares Z with 256 t_j, the
         // same decisions as z against t_j (ties go up); the last comparison's difference Z - 256 t_2k
         // gives the residual: Z - 256 c = (Z - 256 t_2k) -/+ 256 hw_k.
-        uint32_t w[3][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
+        // the words of this half: coordinates 64 h + m are words 2 h, 2 h + 1 of each tig
+        uint32_t kwd[4][2] = {{0u, 0u}, {0u, 0u}, {0u, 0u}, {0u, 0u}};
         float g2 = 0.f;   // sum of squares of the residual x 256
 #pragma unroll
         for (int m = 0; m < 64; ++m) {
@@ -501,10 +513,7 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
             const bool b1 = Z >= (b2 ? T5 : T1);
             const float dz = Z - (b2 ? (b1 ? T6 : T4) : (b1 ? T2 : T0));
             const bool b0 = dz >= 0.f;
-            const int tig = (m >> 1) & 3, bit = 8 * ((m >> 3) & 1) + (m >> 4) + 16 * (m & 1);   // + 4 h below
-            w[0][tig] |= (uint32_t)b0 << bit;
-            w[1][tig] |= (uint32_t)b1 << bit;
-            w[2][tig] |= (uint32_t)b2 << bit;
+            kwd[k_tig(m)][k_word(m)] |= ((uint32_t)b0 | ((uint32_t)b1 << 1) | ((uint32_t)b2 << 2)) << (4 * k_field(m));
             const float hw = (b1 == b2) ? hw_out : hw_in;
             const float rho = b0 ? dz - hw : dz + hw;
             g2 = fmaf(rho, rho, g2);
@@ -526,13 +535,7 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
             tc::st16(lane_addr + 32 * h + 16 * q, hw);
             tc::st16(lane_addr + 64 + 32 * h + 16 * q, lw);
         }
-        if (h == 1) {   // half 1's plane bits and residual sum, for half 0 to merge
-#pragma unroll
-            for (int p = 0; p < 3; ++p)
-#pragma unroll
-                for (int tig = 0; tig < 4; ++tig) sW[4 * p + tig] = w[p][tig] << 4;
-            sW[12] = __float_as_uint(g2);
-        }
+        if (h == 1) sW[12] = __float_as_uint(g2);   // half 1's residual sum, for half 0
         tc::wait_st();
         tc::fence_before_sync();
         tc::named_sync(bar_id, 256);
@@ -553,11 +556,9 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
         }
         if (!tc::mbar_wait(&mmabar[tg], i & 1)) timed_out = true;
         tc::fence_after_sync();
-        // ---- 5. sign words 2 h, 2 h + 1: accumulator columns 64 h .. 64 h + 63.  Column 16 j + b is
-        // bit 16 (j & 1) + b of word j >> 1; the projections' sign bits are shifted in one per funnel
-        // shift (the first column ends in bit 31), then reversed and inverted (bit = projection >= 0;
-        // only an exact zero, a tie, could read as -0)
-        uint32_t sgn[2] = {0u, 0u};
+        // ---- 5. QJL sign bits of this half: accumulator columns 64 h + 16 j + b are field b & 7 of
+        // word (tig j, 2 h + (b >> 3)); bit 3 of the field is set when the projection is >= 0 (its
+        // fp32 sign bit clear; only an exact zero, a tie, could read as -0)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             float pv[16];
@@ -566,32 +567,23 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
 #pragma unroll
             for (int b = 0; b < 16; ++b) asm volatile("" : "+f"(pv[b]));   // no use moves above the wait
 #pragma unroll
-            for (int b = 0; b < 16; ++b) sgn[j >> 1] = __funnelshift_l(__float_as_uint(pv[b]), sgn[j >> 1], 1);
+            for (int b = 0; b < 16; ++b)
+                kwd[j][b >> 3] |= ((~__float_as_uint(pv[b]) >> 31) << 3) << (4 * (b & 7));
         }
-        sgn[0] = ~__brev(sgn[0]);
-        sgn[1] = ~__brev(sgn[1]);
         tc::fence_before_sync();
         // ---- 6. the record words of this row's slot
         if (slot >= 0) {
             const int64_t blk = slot / kBlock;
             const int o = (int)(slot % kBlock);
             uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * k_record(D);
-            uint32_t *planes = reinterpret_cast<uint32_t *>(rec);
-            constexpr int PW = 2 * D / 4;
             const int gid = o & 7, th = o >> 3;
-            if (h == 0) {
 #pragma unroll
-                for (int tig = 0; tig < 4; ++tig) {
-                    const int word = (4 * gid + tig) * 2 + th;
-                    planes[word] = w[0][tig] | sW[tig];
-                    planes[PW + word] = w[1][tig] | sW[4 + tig];
-                    planes[2 * PW + word] = w[2][tig] | sW[8 + tig];
-                }
+            for (int tig = 0; tig < 4; ++tig)   // words 2 h, 2 h + 1 of word row (4 gid + tig) * 2 + th
+                reinterpret_cast<uint2 *>(rec)[((4 * gid + tig) * 2 + th) * 2 + h] = make_uint2(kwd[tig][0], kwd[tig][1]);
+            if (h == 0) {
                 const float gam = sqrtf(g2 + __uint_as_float(sW[12])) * (inv_sd * (1.f / 256.f));
                 *reinterpret_cast<__half2 *>(rec + 8 * D + 4 * o) = __halves2half2(__float2half_rn(nrm), __float2half_rn(gam));
             }
-#pragma unroll
-            for (int k = 0; k < 2; ++k) planes[3 * PW + (4 * gid + 2 * h + k) * 2 + th] = sgn[k];
         }
         tc::named_sync(bar_id, 256);   // the accumulator, the A lanes and the merge area are free
     }

@@ -1,19 +1,21 @@
 // tq_internal.cuh -- layout constants and device helpers shared by the kernels.
 //
 // Packed layout of one record (16 token slots of one block, one kv head):
-//   K: planes 0..2 (bit p of the 3-bit cell), plane 3 (QJL sign bits), each
-//      2*d bytes, then 16 x {fp16 ||x||, fp16 ||r||}.
-//   V: planes 0..2, each 2*d bytes, then 16 x fp16 ||v||.
-// Each plane is an array of 32-bit words indexed by a lane L = 4*gid + tig.
-//   K: coordinate i = 16*s + 8*h + 2*tig + e of slot t = gid + 8*th sits in
-//      word (L*2 + th)*NW + (s>>3), NW = d/128, at bit 8*h + (s&7) + 16*e.
-//   V: coordinate i = 16*mt + gid + 8*rh of slot t = 2*tig + 8*tp + e sits in
-//      word L*NWV + 2*(mt>>3) + rh, NWV = d/64, at bit 8*tp + (mt&7) + 16*e.
-// In both layouts one byte of a word belongs to one token slot, so slots can
-// be written independently with byte stores.  Bits p and p+16 of a word are
-// the two halves of one f16x2 operand register of the m16n8k16 mma.sync used
-// by decode attention (K: token rows x coordinate columns; V: coordinate rows
-// x token columns), so one LOP3 turns them into two f16 operands.
+//   K: 4-bit fields, one per (slot, coordinate): cell bits 0..2 and the QJL sign bit 3,
+//      8*d bytes, then 16 x {fp16 ||x||, fp16 ||r||}.
+//   V: 3-bit cells, 6*d bytes, then 16 x fp16 ||v||.
+// The cell region is an array of 32-bit words grouped by a lane L = 4*gid + tig.
+//   K: coordinate i = 16*ks + c, c = 2*tig + e + 8*h, of slot t = gid + 8*r is field
+//      f = 4*(ks&1) + e + 2*h (bits 4f..4f+3) of word (L*2 + r)*(d/32) + (ks>>1).
+//   V: coordinate i = 16*mt + gid + 8*rr has lane slot s = 2*mt + rr, cut into groups of
+//      16 (g = s>>4, sg = s&15); slot t has tig = (t&7)>>1, pair P = t>>3, e = t&1.  For
+//      sg < 12 the cell is field f = 4*((sg>>1)&1) + 2*e + (sg&1), bits 0..2, of word
+//      (L*2 + P)*3*(d/128) + 3*g + (sg>>2); for sg >= 12 its bit p is bit 3 of field
+//      f = 4*((sg-12)>>1) + 2*e + (sg&1) of word ... + 3*g + p.
+// Every byte belongs to one token slot, so slots are written independently with byte (V) or
+// word (K) stores.  Four fields of a word are the PRMT selector of a table lookup in the
+// decode kernels; the lookups and byte interleaves give f16x2 operand registers of the
+// m16n8k16 mma.sync (K: token rows x coordinate columns; V: coordinate rows x token columns).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -36,8 +38,12 @@ struct ParamsHeader {
     float centroid[8];     // ascending, unit variance
     float threshold[8];    // 7 used: midpoints of neighbouring centroids
     double centroid64[8];  // the same centroids before rounding to fp32
-    uint32_t one16x2;      // 0x3C003C00: f16x2 {1, 1}, operand base of the decode kernels
-    float pad[27];
+    uint32_t one16x2;      // 0x3C003C00: f16x2 {1, 1}
+    uint32_t lut_lo[2];    // byte j: low byte of the f16 T[j] = f16(alpha * centroid[j]), j = 0..7
+    uint32_t lut_hi[2];    // byte j: high byte of T[j]
+    float inv_alpha;       // 1 / alpha (T[j] * inv_alpha = centroid[j] within 2e-5)
+    uint16_t t16[8];       // T[j] as binary16 bits
+    float pad[18];
 };
 static_assert(sizeof(ParamsHeader) == 256, "params header must be 256 bytes");
 
@@ -159,6 +165,8 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_n() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 // ---------------------------------------------------------------- projections by S
 // out[v][k] = sum_i S[k][i] x[v][i] for NV vectors x[v][*] in shared memory,
@@ -340,5 +348,13 @@ cudaError_t launch_step(int d, int dtype, const void *params, const void *k_new,
                         int batch, int q_len, int hq, int hkv, const int32_t *block_table, int max_blocks,
                         const int32_t *pre_lens, int max_ctx, void *k_pool, void *v_pool, int64_t num_blocks,
                         float *out, void *ws, int32_t *status, cudaStream_t st);
+
+// PRMT in its default mode: byte k of the result is byte (c >> 4k) & 7 of {b:a} (the
+// selector's bit 4k+3 must be clear, or the byte's sign is replicated instead).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
 
 }  // namespace tq

@@ -52,7 +52,8 @@ struct EncSmem {
     static constexpr size_t kST = kResident ? (size_t)D * D * 4 : (size_t)2 * kProjRows * D * 4;
     static constexpr size_t kRho = (size_t)TILE * D * 4;
     static constexpr size_t kSgn = (size_t)TILE * D;
-    static constexpr size_t kBytes = kST + kRho + kSgn;
+    static constexpr size_t kCode = (size_t)TILE * D;
+    static constexpr size_t kBytes = kST + kRho + kSgn + kCode;
 };
 
 
@@ -69,6 +70,7 @@ __device__ __forceinline__ void encode_tiles(const uint8_t *__restrict__ params,
     float *sST = reinterpret_cast<float *>(smem);
     float (*s_rho)[D] = reinterpret_cast<float (*)[D]>(smem + SM::kST);
     uint8_t (*s_sgn)[D] = reinterpret_cast<uint8_t (*)[D]>(smem + SM::kST + SM::kRho);
+    uint8_t (*s_code)[D] = reinterpret_cast<uint8_t (*)[D]>(smem + SM::kST + SM::kRho + SM::kSgn);
     __shared__ float s_cent[8], s_thr[8];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     const float *gST = reinterpret_cast<const float *>(params + params_off_ST(D));
@@ -88,7 +90,6 @@ __device__ __forceinline__ void encode_tiles(const uint8_t *__restrict__ params,
 #pragma unroll 1
     for (int64_t tile = blk; tile < ntiles; tile += nblk) {
         const int64_t v0 = tile * kTile;
-        int code[kPerWarp][R];
         float nrm[kPerWarp], gam[kPerWarp];
         int64_t slot[kPerWarp];
         // ---- 1. norm, rotation, cells, residual
@@ -129,7 +130,7 @@ __device__ __forceinline__ void encode_tiles(const uint8_t *__restrict__ params,
                 int k = 0;
 #pragma unroll
                 for (int t = 0; t < 7; ++t) k += (z >= s_thr[t]) ? 1 : 0;
-                code[j][r] = k;
+                s_code[tv][dims[r]] = (uint8_t)k;
                 if (is_k) {
                     const float rho = z - s_cent[k];     // residual, rotated unit-variance domain
                     g2 = fmaf(rho, rho, g2);
@@ -161,7 +162,8 @@ __device__ __forceinline__ void encode_tiles(const uint8_t *__restrict__ params,
                 for (int t = 0; t < kTile; ++t) s_sgn[t][threadIdx.x + 128 * u] = acc[u][t] >= 0.f ? 1 : 0;
             __syncthreads();
         }
-        // ---- 3. pack and store
+        // ---- 3. pack and store (the layout of tq_internal.cuh); a warp packs the vectors it encoded
+        __syncwarp();
 #pragma unroll
         for (int j = 0; j < kPerWarp; ++j) {
             if (slot[j] < 0) continue;                     // warp-uniform (also for a warp without a vector)
@@ -169,47 +171,44 @@ __device__ __forceinline__ void encode_tiles(const uint8_t *__restrict__ params,
             const int head = (int)((v0 + tv) % map.n_heads);
             const int64_t blk = slot[j] / kBlock;
             const int off = (int)(slot[j] % kBlock);
+            const uint8_t *cd = s_code[tv];
             if (is_k) {
+                // 4 D/32 words of 8 fields: word (tig, w) holds columns 2tig, 2tig+1, 2tig+8, 2tig+9 of
+                // k-steps 2w (fields 0..3) and 2w+1 (fields 4..7)
+                constexpr int NW = D / 32;
                 uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * k_record(D);
-                uint32_t *planes = reinterpret_cast<uint32_t *>(rec);
-                constexpr int NW = D / 128;
-                const int gid = off & 7, th = off >> 3;
+                const uint8_t *sg = s_sgn[tv];
+                const int gid = off & 7, rr = off >> 3;
+                for (int wi = lane; wi < 4 * NW; wi += 32) {
+                    const int tg = wi / NW, w = wi % NW;
+                    uint32_t word = 0;
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const uint32_t w0 = __ballot_sync(0xffffffffu, code[j][r] & 1);
-                    const uint32_t w1 = __ballot_sync(0xffffffffu, (code[j][r] >> 1) & 1);
-                    const uint32_t w2 = __ballot_sync(0xffffffffu, (code[j][r] >> 2) & 1);
-                    const uint32_t ws = __ballot_sync(0xffffffffu, s_sgn[tv][kdim<D>(lane, r)]);
-                    if (lane == r) {
-                        const int L = 4 * gid + (r & 3);
-                        const size_t word = (size_t)(L * 2 + th) * NW + (r >> 2);
-                        constexpr size_t PW = 2 * D / 4;   // words per plane
-                        planes[word] = w0;
-                        planes[PW + word] = w1;
-                        planes[2 * PW + word] = w2;
-                        planes[3 * PW + word] = ws;
+                    for (int f = 0; f < 8; ++f) {
+                        const int cs = f & 3, x = 16 * (2 * w + (f >> 2)) + 2 * tg + (cs & 1) + 8 * (cs >> 1);
+                        word |= (uint32_t)(cd[x] | (sg[x] << 3)) << (4 * f);
                     }
+                    reinterpret_cast<uint32_t *>(rec)[((4 * gid + tg) * 2 + rr) * NW + w] = word;
                 }
                 if (lane == 0)
                     *reinterpret_cast<__half2 *>(rec + 8 * D + 4 * off) =
                         __halves2half2(__float2half_rn(nrm[j]), __float2half_rn(gam[j]));
             } else {
+                // the slot's bytes: per lane gid, group g, word k and half hf, the cells of lane slots
+                // 16g + 4k + 2hf + ab (ab = 0, 1: the byte's two fields) with bit k of the cells of lane
+                // slots 16g + 12 + 2hf + ab in bit 3 of the fields
+                constexpr int NG = D / 128;
                 uint8_t *rec = pool + ((size_t)blk * map.n_heads + head) * v_record(D);
-                constexpr int NWV = D / 64, NM = D / 128;
-                const int tigv = (off & 7) >> 1, jb = (off >> 3) + 2 * (off & 1);   // lane tig, byte in word
+                const int tg = (off & 7) >> 1, pr = off >> 3, e = off & 1;
+                for (int bi = lane; bi < 48 * NG; bi += 32) {
+                    const int hf = bi & 1, k = (bi >> 1) % 3, g = ((bi >> 1) / 3) % NG, gid = (bi >> 1) / (3 * NG);
+                    uint32_t byte = 0;
 #pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    const uint32_t w0 = __ballot_sync(0xffffffffu, code[j][r] & 1);
-                    const uint32_t w1 = __ballot_sync(0xffffffffu, (code[j][r] >> 1) & 1);
-                    const uint32_t w2 = __ballot_sync(0xffffffffu, (code[j][r] >> 2) & 1);
-                    if ((lane >> 2) == r) {
-                        const int beta = lane & 3, tau = 4 * r + beta;
-                        const int mhi = tau % NM, rh = (tau / NM) & 1, gid = tau / (2 * NM);
-                        const size_t byte = ((size_t)(4 * gid + tigv) * NWV + 2 * mhi + rh) * 4 + jb;
-                        rec[byte] = (uint8_t)(w0 >> (8 * beta));
-                        rec[2 * D + byte] = (uint8_t)(w1 >> (8 * beta));
-                        rec[4 * D + byte] = (uint8_t)(w2 >> (8 * beta));
+                    for (int ab = 0; ab < 2; ++ab) {
+                        const int sd = 16 * g + 4 * k + 2 * hf + ab, ss = 16 * g + 12 + 2 * hf + ab;
+                        const int xd = 16 * (sd >> 1) + gid + 8 * (sd & 1), xs = 16 * (ss >> 1) + gid + 8 * (ss & 1);
+                        byte |= (uint32_t)(cd[xd] | (((cd[xs] >> k) & 1) << 3)) << (4 * ab);
                     }
+                    rec[((size_t)((4 * gid + tg) * 2 + pr) * 3 * NG + 3 * g + k) * 4 + 2 * hf + e] = (uint8_t)byte;
                 }
                 if (lane == 0) *reinterpret_cast<__half *>(rec + 6 * D + 2 * off) = __float2half_rn(nrm[j]);
             }
@@ -221,19 +220,16 @@ __device__ __forceinline__ void encode_tiles(const uint8_t *__restrict__ params,
 
 // ---------------------------------------------------------------- f16 operand helpers
 
-// Operand bit position q (8..15 within each f16 half): mask, base, and the
-// operand values alpha (bit clear) and alpha + delta (bit set).
-__host__ __device__ constexpr uint32_t op_mask(int q) { return 0x00010001u << q; }
-__host__ __device__ constexpr float op_alpha(int q) { return q == 14 ? 0.f : 1.f; }
-__host__ __device__ constexpr float op_delta(int q) {
-    return q == 8 ? 0.25f : q == 9 ? 0.5f : q == 10 ? -0.5f : q == 11 ? -0.75f
-         : q == 12 ? -0.9375f : q == 13 ? -0.99609375f : q == 14 ? 2.0f : -2.0f;
-}
-
-// 2 / delta_q, the factor that turns a query coordinate into its B-operand value
-__host__ __device__ constexpr float op_two_over_delta(int q) {
-    return q == 8 ? 8.f : q == 9 ? 4.f : q == 10 ? -4.f : q == 11 ? -2.f / 0.75f
-         : q == 12 ? -2.f / 0.9375f : q == 13 ? -2.f / 0.99609375f : q == 14 ? 1.0f : -1.0f;
+// QJL operand of field position i (0..3) of a K record word: bit 4i+3 of each f16 half.
+// Positions 3, 7, 11 give 0 or delta_i (2^-21, 2^-17, 2^-13; the first two subnormal, which
+// the tensor core keeps); position 15 is the sign bit of 2^-14 (base 0x0400), so that operand
+// is -2^-14 sigma.  The B operand is u * qjl_bscale(i), so that every product is
+// 2^-16 (u sigma + u) for i < 3 and 2^-16 u sigma for i = 3; the 2^-16 sum of u over the i < 3
+// coordinates (delta_i / 2 times the B values) is removed afterwards.
+__host__ __device__ constexpr uint32_t qjl_base(int i) { return i == 3 ? 0x04000400u : 0u; }
+__host__ __device__ constexpr float qjl_bscale(int i) { return i == 0 ? 64.f : i == 1 ? 4.f : i == 2 ? 0.25f : -0.25f; }
+__host__ __device__ constexpr float qjl_half_delta(int i) {
+    return i == 0 ? 2.384185791015625e-07f : i == 1 ? 3.814697265625e-06f : i == 2 ? 6.103515625e-05f : 0.f;
 }
 
 __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -254,18 +250,9 @@ __device__ __forceinline__ void mma_f16_z(float (&c)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 
-// exponent e with x * 2^e in [128, 256) for x > 0
-__device__ __forceinline__ int scale_exp(float x) {
-    int ex;
-    frexpf(x, &ex);
-    return 8 - ex;
-}
-
-
-
 // Per (sequence, kv head) query pack: f16x2 B-operand fragments
-// [2 (qbar, u)][d/16 k-steps][2 n-tiles][32 lanes][2 words], then the offset
-// constants [2][8 heads] as floats.
+// [2 (qbar / alpha, QJL-scaled u)][d/16 k-steps][n-tiles][32 lanes][2 words], then floats:
+// [8] unused, [8 heads] the QJL offset constant.
 __host__ __device__ constexpr size_t kPackBytes(int d) { return 64 * (size_t)d + 256; }
 __host__ __device__ constexpr int kPackFloatOff(int d) { return 16 * d; }   // in floats
 
@@ -353,16 +340,28 @@ __device__ __forceinline__ void qprep_rows(const uint8_t *__restrict__ params, c
         uint8_t *pack = packs + ((size_t)b * hkv + kvh) * kPackBytes(D);
         uint16_t *ph = reinterpret_cast<uint16_t *>(pack);
         float *pf = reinterpret_cast<float *>(pack) + kPackFloatOff(D);
+        const float inv_alpha = reinterpret_cast<const ParamsHeader *>(params)->inv_alpha;
 #pragma unroll
         for (int qu = 0; qu < 2; ++qu) {
             float cs = 0.f;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const int dim = 32 * r + lane, s = dim >> 4, k = dim & 15, qd = 8 + (s & 7);
-                const float beta = (qu == 0 ? v[r] : u[r]) * op_two_over_delta(qd);
+                const int dim = 32 * r + lane;
+                // operand row (k-step s, row k) of the coordinate, and its B value
+                int s = dim >> 4, k = dim & 15;
+                float beta = v[r] * inv_alpha;             // codebook plane: natural order, qbar / alpha
+                float hd = 0.f;
+                if (qu == 1) {                              // QJL plane: the K record's field position
+                    const int c = dim & 15, tg = (c & 7) >> 1, h = c >> 3;
+                    const int f = 4 * (s & 1) + (c & 1) + 2 * h, i = f & 3;
+                    k = 2 * tg + 8 * (i & 1) + (f >> 2);
+                    s = 2 * (s >> 1) + (i >> 1);
+                    beta = u[r] * qjl_bscale(i);
+                    hd = qjl_half_delta(i);
+                }
                 const __half hi = __float2half_rn(beta);
                 const __half lo = __float2half_rn(beta - __half2float(hi));
-                cs = fmaf(__half2float(hi) + __half2float(lo), op_alpha(qd) + 0.5f * op_delta(qd), cs);
+                cs = fmaf(__half2float(hi) + __half2float(lo), hd, cs);
                 const int reg = k >> 3, tig = (k & 7) >> 1, e = k & 1;
 #pragma unroll
                 for (int x = 0; x < 2; ++x) {
@@ -371,8 +370,10 @@ __device__ __forceinline__ void qprep_rows(const uint8_t *__restrict__ params, c
                     ph[word * 2 + e] = __half_as_ushort(x == 0 ? hi : lo);
                 }
             }
-            cs = warp_sum(cs);
-            if (lane == 0) pf[qu * 8 + hg] = cs;
+            if (qu == 1) {
+                cs = warp_sum(cs);
+                if (lane == 0) pf[8 + hg] = cs;
+            }
         }
         // columns beyond the group's 2*G*q_len are zero (written by the group's first row)
         if (hg == 0) {

@@ -1,7 +1,6 @@
-// tq_split.cuh -- pieces shared by the two decode passes (tq_decode.cu: the
-// coordinate-split pass used at d = 256; tq_decode_warp.cu: the warp-local pass used at
-// d = 128): tuning switches, the workspace layout, block-table lookup, the V-side
-// operand encoding and the final inverse rotation.
+// tq_split.cuh -- pieces shared by the decode launches (tq_decode.cu: query prep, the fused
+// step and the dispatch; tq_decode_warp.cu: the pass): tuning switches, the workspace layout,
+// block-table lookup and the final inverse rotation.
 #pragma once
 
 #include "tq_internal.cuh"
@@ -12,17 +11,11 @@ namespace tq {
 #ifndef TQ_SPLITK_BPW
 #define TQ_SPLITK_BPW 2          // blocks scored per warp per chunk
 #endif
-#ifndef TQ_SPLITK_MINBLOCKS
-#define TQ_SPLITK_MINBLOCKS 4    // resident CTAs per SM the register budget is sized for (4-warp CTAs)
-#endif
 #ifndef TQ_SPLITK_CTAS_PER_SM
-#define TQ_SPLITK_CTAS_PER_SM 3
+#define TQ_SPLITK_CTAS_PER_SM 3  // persistent CTAs per SM (at most)
 #endif
 constexpr int kCtasPerSm = TQ_SPLITK_CTAS_PER_SM;
 
-#ifndef TQ_DECODE_WARP
-#define TQ_DECODE_WARP 1         // d = 128 runs the warp-local pass (tq_decode_warp.cu)
-#endif   // persistent CTAs per SM (at most)
 #ifndef TQ_DECODE_PDL
 #define TQ_DECODE_PDL 1          // the pass may launch while the prep launch before it finishes
 #endif
@@ -93,19 +86,6 @@ __device__ __forceinline__ int64_t block_of(const int32_t *__restrict__ bt, int 
     return (p >= 0 && p < num_blocks) ? p : -1;
 }
 
-// V-side operand encoding.  The value sums run over whole contexts (up to 10^5 tokens), so
-// the operands carry no offset: with base 0 the f16 with only bit q set is 0 or delta_q
-// (2^-16 .. 2 for q = 8..14, the first two subnormal); bit 15 toggles the sign of 2^-14, so
-// the operand is +-2^-14 and the sum is the +-1 sum itself.  (An offset alpha would leave
-// alpha * sum(P) in the fp32 accumulator and cost (2 alpha / delta)-fold of its rounding.)
-__host__ __device__ constexpr uint32_t vop_base(int q) { return q == 15 ? 0x04000400u : 0u; }
-__host__ __device__ constexpr float vop_alpha(int q) { return q == 15 ? 0.00006103515625f : 0.f; }   // 2^-14
-__host__ __device__ constexpr float vop_delta(int q) {
-    return q == 8 ? 1.52587890625e-05f : q == 9 ? 3.0517578125e-05f : q == 10 ? 6.103515625e-05f
-         : q == 11 ? 0.0001220703125f : q == 12 ? 0.00048828125f : q == 13 ? 0.0078125f : q == 14 ? 2.f
-         : -0.0001220703125f;
-}
-
 // out[row] = Pi^T (v / l): D (H v) / (l sqrt d), v spread over the warp as v[r] at lane
 template <int D>
 __device__ __forceinline__ void finish_row(float (&v)[D / 32], float l, const uint8_t *params, float *out_row,
@@ -122,13 +102,11 @@ __device__ __forceinline__ void finish_row(float (&v)[D / 32], float l, const ui
 }
 
 
-// The warp-local pass at d = 128 (tq_decode_warp.cu): persistent CTAs it runs with on the
-// current device, and its launch.  Same schedule, workspace and partial format as the
-// coordinate-split pass.  G counts operand columns: q_len queries x the query heads of a kv
-// head.
-int warp_pass_ctas(int G);
-cudaError_t warp_pass_launch(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
-                             const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
+// The decode pass (tq_decode_warp.cu): persistent CTAs it runs with on the current device, and
+// its launch.  G counts operand columns: q_len queries x the query heads of a kv head.
+int warp_pass_ctas(int d, int G);
+cudaError_t warp_pass_launch(int d, int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq,
+                             int hkv, const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
                              const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
                              float *lse, int32_t *status);
 
