@@ -27,7 +27,8 @@
 //    added to fp32 running sums (chained tensor-core accumulation over thousands of tokens is
 //    not accurate enough).
 //  * At the end of a (sequence, kv head) segment the 4 warps' (m, l, acc) are merged in
-//    shared memory, then the segment is finished or left as a partial (m in log2 units).
+//    shared memory, then the segment is finished, or, when other CTAs hold parts of it, left as
+//    a partial (m in log2 units) for the merge kernel that follows the pass.
 #include "tq_split.cuh"
 
 #ifndef TQ_WARP_BQ_SMEM
@@ -112,9 +113,9 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
     uint32_t *sBq = reinterpret_cast<uint32_t *>(smem + kStage + kMerge);
     __shared__ float sMW[NWARP][8], sLW[NWARP][8];
     __shared__ float sM[8], sL[8];
-    __shared__ bool s_last;
 
     pdl_wait();   // everything before this launch (the prep's schedule, packs, counters) is complete
+    pdl_launch_dependents();   // the merge kernel's CTAs may be placed as this pass's CTAs exit
 
     for (int b = cta; b < batch; b += gridDim.x)
         if (attended_len(ctx_lens[b], ctx_add, max_ctx) == 0)
@@ -174,13 +175,21 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
     // of the result is set when block bw is in range and has a valid physical id.  Blocks past
     // the context are not copied; a block with a bad id is replaced by block 0 (its scores are
     // masked), so the copies need no per-lane branch.
-    auto stage = [&](const Seg &s, int tc, int buf) -> int {
-        int okm = 0;
+    // The block ids of a position are read one prefetch step before they are used, so that their
+    // load overlaps a chunk of work instead of delaying the copies: id -2 = past the context.
+    auto load_ids = [&](const Seg &s, int tc, int64_t (&ids)[BPW]) {
 #pragma unroll
         for (int bw = 0; bw < BPW; ++bw) {
             const int tb = tc + kBlock * (BPW * warp + bw);
-            if (tb < s.t1) {
-                const int64_t p = block_of(block_table, s.b, max_blocks, tb / kBlock, num_blocks);
+            ids[bw] = (tb < s.t1) ? block_of(block_table, s.b, max_blocks, tb / kBlock, num_blocks) : -2;
+        }
+    };
+    auto stage = [&](const Seg &s, const int64_t (&ids)[BPW], int buf) -> int {
+        int okm = 0;
+#pragma unroll
+        for (int bw = 0; bw < BPW; ++bw) {
+            const int64_t p = ids[bw];
+            if (p != -2) {
                 if (p < 0 && lane == 0) flag_status(status, TQ_STATUS_BAD_SLOT);
                 okm |= (p >= 0) << bw;
                 const size_t row = (size_t)(p < 0 ? 0 : p) * hkv + s.kh;
@@ -217,10 +226,12 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
     bool pmore = true;
     int okm = 0;   // bit NBUF-slot * BPW + bw: block bw of the buffer is in range with a valid id
     int buf = 0, pbuf = 0;
+    int64_t pids[BPW];
+    load_ids(ps, ptc, pids);
     auto prefetch = [&]() {
         int bits = 0;
         if (pmore) {
-            bits = stage(ps, ptc, pbuf);
+            bits = stage(ps, pids, pbuf);
             ptc += CH;
             if (ptc >= ps.t1) {
                 Seg n2;
@@ -230,6 +241,7 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                     ptc = ps.t0;
                 }
             }
+            if (pmore) load_ids(ps, ptc, pids);   // for the next step
         } else {
             cp_async_commit();
         }
@@ -653,73 +665,82 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                     dst[1] = sL[h];
                 }
             }
-            // one thread publishes the CTA's partials: its acquire-release add orders every write of
-            // the CTA before the barrier ahead of the count, and (for the CTA that completes the
-            // count) every other CTA's partials ahead of the reads after the next barrier
-            __syncthreads();
-            if (tid == 0) {
-                const unsigned int nseg = (unsigned int)(hi - lo + 1);
-                unsigned int done;
-                asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
-                             : "=r"(done) : "l"(counters + b * hkv + kh) : "memory");
-                s_last = (done + 1u == nseg);
-                if (s_last) counters[b * hkv + kh] = 0u;
-            }
-            __syncthreads();
-            if (s_last) {
-                // The partials of the CTAs lo..hi, merged by log-sum-exp.  Their (m, l) are read one
-                // per lane, their value rows UN at a time, so every wait covers many loads.
-                const int slot_lo = (sk_begin(lo, P, W) >= us) ? 0 : 1;
-                const int np = hi - lo + 1;
-                constexpr int UN = 32 / R;
-                for (int h = warp; h < G; h += NWARP) {
-                    auto part_of = [&](int j) {
-                        const int c2 = lo + j, sl = (c2 == lo) ? slot_lo : 0;
-                        return part + (((size_t)c2 * 2 + sl) * G + h) * kPartStride(D);
-                    };
-                    float M = -INFINITY;
-                    for (int j = lane; j < np; j += 32) M = fmaxf(M, __ldcg(part_of(j)));
-                    M = warp_max(M);
-                    float l = 0.f;
-                    for (int j = lane; j < np; j += 32) {
-                        const float *ps = part_of(j);
-                        const float m = __ldcg(ps), lp = __ldcg(ps + 1);
-                        l += (m == -INFINITY) ? 0.f : lp * exp2f(m - M);
-                    }
-                    l = warp_sum(l);
-                    float v[R];
-#pragma unroll
-                    for (int r = 0; r < R; ++r) v[r] = 0.f;
-#pragma unroll 1
-                    for (int j0 = 0; j0 < np; j0 += UN) {
-                        float vv[UN][R], ww[UN];
-#pragma unroll
-                        for (int u = 0; u < UN; ++u) {
-                            ww[u] = 0.f;
-#pragma unroll
-                            for (int r = 0; r < R; ++r) vv[u][r] = 0.f;
-                            if (j0 + u < np) {
-                                const float *ps = part_of(j0 + u);
-                                const float m = __ldcg(ps);
-#pragma unroll
-                                for (int r = 0; r < R; ++r) vv[u][r] = __ldcg(ps + 4 + 32 * r + lane);
-                                ww[u] = (m == -INFINITY) ? 0.f : exp2f(m - M);
-                            }
-                        }
-#pragma unroll
-                        for (int u = 0; u < UN; ++u)
-#pragma unroll
-                            for (int r = 0; r < R; ++r) v[r] = fmaf(vv[u][r], ww[u], v[r]);
-                    }
-                    finish_row<D>(v, l, params, out + out_row(h) * D, lane);
-                    if (lse && lane == 0) lse[out_row(h)] = l > 0.f ? M * kLn2 + logf(l) : -INFINITY;
-                }
-            }
         }
         if (!more_segs) break;
         first_seg = false;
         s = ns;   // its first chunks are already staged
     }
+}
+
+// Merge of the (sequence, kv head) segments that the pass left as partials: CTA = segment, warp h
+// merges operand column h by log-sum-exp over the partials of the pass CTAs lo..hi that share the
+// segment, then applies the inverse rotation.  Launched as a programmatic dependent of the pass:
+// its CTAs are placed as the pass's CTAs exit and wait for the whole pass to complete.
+template <int D>
+__global__ void __launch_bounds__(256)
+merge_kernel(const uint8_t *__restrict__ params, int batch, int q_len, int hq, int hkv, int G,
+             const int64_t *__restrict__ cpre, int nctas, const float *__restrict__ part, float *__restrict__ out,
+             float *__restrict__ lse) {
+    constexpr int R = D / 32;
+    constexpr int UN = 32 / R;
+    constexpr float kLn2 = 0.6931471805599453f;
+    pdl_wait();
+    const int b = blockIdx.x / hkv, kh = blockIdx.x % hkv, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = warp;
+    if (h >= G) return;
+    const int64_t W = cpre[batch];
+    const int P = (int)(W < (int64_t)nctas ? W : (int64_t)nctas);
+    const int64_t ub = cpre[b];
+    const int64_t nch = (cpre[b + 1] - ub) / hkv;
+    if (nch == 0 || P == 0) return;
+    const int64_t us = ub + kh * nch, ue = us + nch;
+    const int lo = sk_cta_of(us, P, W), hi = sk_cta_of(ue - 1, P, W);
+    if (lo == hi) return;   // finished by the pass
+    // the CTA lo wrote this segment as its second partial slot when its range began earlier
+    const int slot_lo = (sk_begin(lo, P, W) >= us) ? 0 : 1;
+    const int np = hi - lo + 1;
+    auto part_of = [&](int j) {
+        const int c2 = lo + j, sl = (c2 == lo) ? slot_lo : 0;
+        return part + (((size_t)c2 * 2 + sl) * G + h) * kPartStride(D);
+    };
+    // (m, l) of up to 32 partials per lane pass, one load each
+    float M = -INFINITY, l = 0.f;
+    for (int j0 = 0; j0 < np; j0 += 32) {
+        const int j = j0 + lane;
+        const float2 ml = j < np ? *reinterpret_cast<const float2 *>(part_of(j)) : make_float2(-INFINITY, 0.f);
+        const float Mn = fmaxf(M, warp_max(ml.x));
+        const float lc = (ml.x == -INFINITY) ? 0.f : ml.y * exp2f(ml.x - Mn);
+        l = (M == -INFINITY ? 0.f : l * exp2f(M - Mn)) + warp_sum(lc);
+        M = Mn;
+    }
+    float v[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) v[r] = 0.f;
+#pragma unroll 1
+    for (int j0 = 0; j0 < np; j0 += UN) {
+        float vv[UN][R], ww[UN];
+#pragma unroll
+        for (int u = 0; u < UN; ++u) {
+            ww[u] = 0.f;
+#pragma unroll
+            for (int r = 0; r < R; ++r) vv[u][r] = 0.f;
+            if (j0 + u < np) {
+                const float *ps = part_of(j0 + u);
+                const float m = ps[0];
+#pragma unroll
+                for (int r = 0; r < R; ++r) vv[u][r] = ps[4 + 32 * r + lane];
+                ww[u] = (m == -INFINITY) ? 0.f : exp2f(m - M);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UN; ++u)
+#pragma unroll
+            for (int r = 0; r < R; ++r) v[r] = fmaf(vv[u][r], ww[u], v[r]);
+    }
+    const int gq = G / q_len;
+    const size_t orow = ((size_t)b * q_len + h / gq) * hq + (size_t)kh * gq + h % gq;
+    finish_row<D>(v, l, params, out + orow * D, lane);
+    if (lse && lane == 0) lse[orow] = l > 0.f ? M * kLn2 + logf(l) : -INFINITY;
 }
 
 template <int D, int G>
@@ -745,8 +766,11 @@ cudaError_t warp_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batc
     auto kern = decode_warp_kernel<D, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_pass(kern, nctas, kWWarps * 32, smem, st, P, w.packs, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx,
-                       ctx_add, max_ctx, w.cpre, w.cta_b, w.part, w.counters, out, lse, status);
+    e = launch_pass(kern, nctas, kWWarps * 32, smem, st, P, w.packs, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx,
+                    ctx_add, max_ctx, w.cpre, w.cta_b, w.part, w.counters, out, lse, status);
+    if (e != cudaSuccess) return e;
+    return launch_pass(merge_kernel<D>, batch * hkv, 256, 0, st, P, batch, q_len, hq, hkv, G, (const int64_t *)w.cpre,
+                       nctas, (const float *)w.part, out, lse);
 }
 
 template <int D>
