@@ -114,6 +114,15 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
     __shared__ float sMW[NWARP][8], sLW[NWARP][8];
     __shared__ float sM[8], sL[8];
 
+    // what depends on no earlier kernel of the stream runs before the wait: the params header's
+    // table and the staging area, zeroed so that slots of blocks that are not copied always hold
+    // finite values (old records or zeros), whose weight is exactly 0
+    const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
+    const uint32_t L0 = ph->lut_lo[0], L1 = ph->lut_lo[1], H0 = ph->lut_hi[0], H1 = ph->lut_hi[1];
+    const float inv_alpha = ph->inv_alpha;
+    for (int i = tid; i < (int)(kStage / 16); i += NT) reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+
     pdl_wait();   // everything before this launch (the prep's schedule, packs, counters) is complete
     pdl_launch_dependents();   // the merge kernel's CTAs may be placed as this pass's CTAs exit
 
@@ -130,9 +139,6 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
     if (cta >= P) return;
     const int64_t g0 = sk_begin(cta, P, W), g1 = sk_begin(cta + 1, P, W);
 
-    const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
-    const uint32_t L0 = ph->lut_lo[0], L1 = ph->lut_lo[1], H0 = ph->lut_hi[0], H1 = ph->lut_hi[1];
-    const float inv_alpha = ph->inv_alpha;
     const float inv_sd = rsqrtf((float)D);
     const float c_sc = inv_sd * kLog2e;                             // scores in log2 units
     const float qjl = 1.2533141373155003f / (float)D * 65536.f;    // sqrt(pi/2) / d, and 1 / 2^-16 of the operands
@@ -196,19 +202,16 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                 const uint8_t *gk = k_pool + row * KREC, *gv = v_pool + row * VREC;
                 uint8_t *dk = sStage + (size_t)(buf * BPW + bw) * REC, *dv = dk + KREC;
 #pragma unroll
-                for (int j = lane; j < KREC / 16; j += 32) cp_async16(dk + 16 * j, gk + 16 * j);
+                for (int j0 = 0; j0 < KREC / 16; j0 += 32)
+                    if (j0 + 32 <= KREC / 16 || j0 + lane < KREC / 16) cp_async16(dk + 16 * (j0 + lane), gk + 16 * (j0 + lane));
 #pragma unroll
-                for (int j = lane; j < VREC / 16; j += 32) cp_async16(dv + 16 * j, gv + 16 * j);
+                for (int j0 = 0; j0 < VREC / 16; j0 += 32)
+                    if (j0 + 32 <= VREC / 16 || j0 + lane < VREC / 16) cp_async16(dv + 16 * (j0 + lane), gv + 16 * (j0 + lane));
             }
         }
         cp_async_commit();
         return okm;
     };
-
-    // the staging area starts zeroed: slots of blocks that are not copied then always hold
-    // finite values (old records or zeros), whose weight is exactly 0
-    for (int i = tid; i < (int)(kStage / 16); i += NT) reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
-    __syncthreads();
 
     Seg s;
     {
@@ -285,7 +288,10 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
             else return make_uint2(bq[qu][ks][nt][0], bq[qu][ks][nt][1]);
         };
         float cu[NTK];
-        int tlim[NTK];   // tokens column 4 nt + tig attends in this segment (query i: L - (q_len - 1 - i))
+        // tokens column 4 nt + tig attends in this segment (query i: L - (q_len - 1 - i)); tmin: all
+        // columns attend the tokens below it
+        int tlim[NTK];
+        const int tmin = min(t1, s.L - (q_len - 1));
 #pragma unroll
         for (int nt = 0; nt < NTK; ++nt) {
             const int hg = 4 * nt + tig;
@@ -360,6 +366,7 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                 for (int bw = 0; bw < BPW; ++bw) {
                     const int tb = tbw + kBlock * bw;
                     const bool ok = (okm >> (buf * BPW + bw)) & 1;
+                    const bool full = ok && tb + kBlock <= tmin;   // every score of the block is attended
                     const uint8_t *krec = sStage + (size_t)(buf * BPW + bw) * REC;
                     uint32_t kw[2][NW];   // this lane's words: token rows gid (r = 0) and gid + 8 (r = 1)
 #pragma unroll
@@ -419,8 +426,8 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                         for (int r = 0; r < 2; ++r) {
                             const float dot_c = accc[nt][2 * r] + accc[nt][2 * r + 1];
                             const float dot_q = accq[nt][2 * r] + accq[nt][2 * r + 1] - cu[nt];
-                            const bool valid = ok && (tb + gid + 8 * r < tlim[nt]);
-                            s2[bw][nt][r] = valid ? nrm[r] * fmaf(dot_c, inv_sd, gam[r] * dot_q) : -INFINITY;
+                            const float sc = nrm[r] * fmaf(dot_c, inv_sd, gam[r] * dot_q);
+                            s2[bw][nt][r] = (full || (ok && tb + gid + 8 * r < tlim[nt])) ? sc : -INFINITY;
                         }
                 }
 
