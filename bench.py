@@ -324,25 +324,33 @@ def extra_decode(name, steps, warmup, dev):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(i, ev=None):
+    def step(i):
+        """One decode call (tq_decode_attn: query prep, then the pass and its merge)."""
+        kp, vp = pools[i % nrep]
+        tq.decode_attn(cache.params, d, q, Hkv, kp, vp, cache.block_table, ctx, max_ctx, out=out, workspace=ws,
+                       status=status)
+
+    def stage_step(i, ev):
+        """The same work through the stage calls, with events around the pass (and its merge)."""
         kp, vp = pools[i % nrep]
         tq.decode_qprep(cache.params, d, q, Hkv, ctx, max_ctx, ws)
-        if ev is not None:
-            ev[0].record(stream)
+        ev[0].record(stream)
         tq.decode_splitk(cache.params, d, B, Hq, Hkv, kp, vp, cache.block_table, ctx, max_ctx, out, ws,
                          status=status)
-        if ev is not None:
-            ev[1].record(stream)
+        ev[1].record(stream)
 
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize(dev)
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(steps):
-        step(i, kev[i])
+        step(i)
     e1.record(stream)
+    torch.cuda.synchronize(dev)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        stage_step(i, kev[i])
     torch.cuda.synchronize(dev)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in {name}")
@@ -351,7 +359,7 @@ def extra_decode(name, steps, warmup, dev):
     peak, _ = measured_peak()
     res = {"config": workload_config(w, f"{nrep} cache copies cycled ({nrep * per_cache / 2**20:.0f} MiB > L2)"),
            "value": round(nb["step"] / (ms * 1e-3) / 1e9, 3), "unit": "GB/s", "ms_per_step": round(ms, 6),
-           "steps": steps, "warmup": warmup, "launches_per_step": 2,
+           "steps": steps, "warmup": warmup, "launches_per_step": 3,
            "roofline": {"bound": "hbm", "kernel": "tq_decode_splitk", "kernel_ms": round(kms, 6),
                         "achieved": round(nb["partial"] / (kms * 1e-3) / 1e9, 3), "peak": peak, "unit": "GB/s",
                         "frac": round(nb["partial"] / (kms * 1e-3) / 1e9 / peak, 4),
@@ -416,7 +424,7 @@ def extra_verify(steps, warmup, dev, q_len=2):
                       "l2": f"{nrep} cache copies cycled ({nrep * per_cache / 2**20:.0f} MiB > L2)"},
            "value": round(step_b / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
            "queries_per_s": round(B * q_len * Hq / (ms * 1e-3), 1), "ms_per_step": round(ms, 6),
-           "steps": steps, "warmup": warmup, "launches_per_step": 2}
+           "steps": steps, "warmup": warmup, "launches_per_step": 3}
     del pools, cache
     torch.cuda.empty_cache()
     return res
@@ -568,7 +576,7 @@ def extra_hybrid(steps, warmup, dev, history=30720, window=2048):
                       "l2": f"{nrep} copies of cache and window cycled ({nrep * per_cache / 2**20:.0f} MiB > L2)"},
            "value": round(step_b / (ms * 1e-3) / 1e9, 3), "unit": "GB/s", "ms_per_step": round(ms, 6),
            "bytes_per_step": {"compressed": nb["partial"], "window": win_b},
-           "steps": steps, "warmup": warmup, "launches_per_step": 4,
+           "steps": steps, "warmup": warmup, "launches_per_step": 5,
            "upkeep": {"call": "tq_hybrid_append", "us_per_call": round(ums * 1e3, 3), "calls": usteps,
                       "launches_per_call": 2,
                       "per_call": f"{B * Hkv} K and {B * Hkv} V vectors leave the windows and are encoded; "
@@ -776,7 +784,7 @@ def bench_tq(args):
     out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
-    launches_per_step = 2          # tq_decode_step: append + query prep in one launch, then the split-K pass
+    launches_per_step = 3          # tq_decode_step: append + query prep in one launch, the split-K pass, its merge
 
     def step(i):
         kp, vp = pools[i % nrep]
@@ -901,7 +909,11 @@ def bench_tq(args):
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16/f32", "data": "synthetic",
+        "arithmetic": ("mixed: mma.sync f16 x f16 with fp32 accumulation; codebook operands are f16 table values "
+                       "alpha c[j], the query (qbar/alpha, QJL-scaled u) and the softmax weights enter as f16 hi+lo "
+                       "pairs (one f16 above 4 heads); norms fp16 as stored; softmax, value sums, merge and the "
+                       "inverse rotation in fp32"),
         "config": workload_config(w, f"{nrep} cache copies cycled ({nrep * per_cache / 2**20:.0f} MiB > L2), "
                                      "no flush needed"),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 3), "peak": peak, "unit": "GB/s",

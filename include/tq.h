@@ -80,9 +80,10 @@ size_t tq_params_bytes(int d);
  *               produces sign bit k).
  *   params_dev  device buffer of >= tq_params_bytes(d) bytes, 16-byte aligned.
  *   centroids_out8  optional host double[8]: the codebook (unit variance).
- * The codebook is solved by a kernel in fp64 (fixed-point Lloyd-Max), stored
- * in fp32.  Copies D and S to the device and derives the tables the kernels
- * use.  Synchronises `stream`.  Errors: TQ_ERR_HEAD_DIM, TQ_ERR_INVALID (NULL
+ * The codebook is solved on the host in fp64 (fixed-point Lloyd-Max, once per
+ * process), stored in fp32 with its fp16 lookup tables.  Copies D and S to the
+ * device and derives the tables the kernels use (S transposed, the QJL offset
+ * weights).  Synchronises `stream`.  Errors: TQ_ERR_HEAD_DIM, TQ_ERR_INVALID (NULL
  * or a D entry not +-1), TQ_ERR_WORKSPACE, TQ_ERR_ALIGN, TQ_ERR_CUDA. */
 int tq_codebook_init(int d, const int8_t *D_host, const float *S_host, void *params_dev,
                      size_t params_bytes, double *centroids_out8, tq_stream_t stream);
@@ -188,16 +189,16 @@ int tq_decode_attn(const void *params, int d, const void *q, int dtype, int batc
  * exactly what tq_decode_attn computes; argument meanings and errors are as
  * there.
  *   tq_decode_qprep   qbar = Pi q and u = S qbar for every (sequence, query head),
- *                     written to the workspace as tensor-core operands, and the
- *                     work schedule of the pass (read from ctx_lens).
+ *                     written to the workspace as tensor-core operands (ctx_lens and
+ *                     max_ctx are checked as by tq_decode_attn; the prep reads neither).
  *   tq_decode_splitk  the pass over the cache.  The context of each (sequence,
  *                     kv head) is cut into chunks of 128 tokens; the chunks of all (sequence,
  *                     kv head) pairs, in that order, are shared out in equal
- *                     contiguous ranges among a fixed set of resident CTAs.  A
- *                     pair whose chunks span several CTAs is combined by the
- *                     last of them from per-CTA online-softmax states; each pair
- *                     writes out = Pi^T a for its query heads.
- * ctx_lens must not change between the two calls. */
+ *                     contiguous ranges among a fixed set of resident CTAs, each of
+ *                     which works out its range from ctx_lens.  A pair whose chunks
+ *                     span several CTAs is combined from their online-softmax states
+ *                     by a merge kernel after the pass; each pair writes
+ *                     out = Pi^T a for its query heads. */
 int tq_decode_qprep(const void *params, int d, const void *q, int dtype, int batch, int n_q_heads,
                     int n_kv_heads, const int32_t *ctx_lens, int max_ctx, void *workspace,
                     size_t workspace_bytes, tq_stream_t stream);

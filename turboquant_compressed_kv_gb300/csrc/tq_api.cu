@@ -1,5 +1,6 @@
 // tq_api.cu -- the C ABI declared in include/tq.h: argument checks on the host,
 // then kernel launches on the caller's stream.  Allocates no device memory.
+#include <vector>
 #include <math.h>
 #include <string.h>
 
@@ -173,6 +174,16 @@ int tq_codebook_init(int d, const int8_t *D_host, const float *S_host, void *par
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(P + params_off_S(d), S_host, sizeof(float) * (size_t)d * d, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) { transpose_kernel<<<d, d, 0, st>>>(P, d); e = cudaGetLastError(); }
+    // the QJL offset weights, summed in fp64 (wv stays alive until the stream is synchronised below)
+    std::vector<float> wv((size_t)d);
+    for (int j = 0; j < d; ++j) {
+        double acc = 0.0;
+        for (int k = 0; k < d; ++k)
+            if (qjl_pos(k) < 3) acc += (double)S_host[(size_t)k * d + j];
+        wv[(size_t)j] = (float)acc;
+    }
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(P + params_off_W(d), wv.data(), sizeof(float) * (size_t)d, cudaMemcpyHostToDevice, st);
     // the header (magic last in stream order) once D and S are in place; h stays alive until the
     // stream is synchronised below
     if (e == cudaSuccess) e = cudaMemcpyAsync(P, &h, sizeof h, cudaMemcpyHostToDevice, st);
@@ -279,8 +290,8 @@ int tq_decode_qprep(const void *params, int d, const void *q, int dtype, int bat
     if (dtype != TQ_DTYPE_F32 && dtype != TQ_DTYPE_BF16) return TQ_ERR_DTYPE;
     if (!q) return TQ_ERR_INVALID;
     if (!ctx_lens) return TQ_ERR_INVALID;
-    return cuda_status(launch_qprep(d, dtype, params, q, batch, 1, n_q_heads, n_kv_heads, ctx_lens, max_ctx,
-                                    workspace, reinterpret_cast<cudaStream_t>(stream)));
+    return cuda_status(launch_qprep(d, dtype, params, q, batch, 1, n_q_heads, n_kv_heads, workspace,
+                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int tq_decode_splitk(const void *params, int d, int batch, int n_q_heads, int n_kv_heads, const void *k_pool,
@@ -294,7 +305,7 @@ int tq_decode_splitk(const void *params, int d, int batch, int n_q_heads, int n_
     if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
     return cuda_status(launch_splitk(d, params, batch, 1, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks,
                                      block_table, max_blocks, ctx_lens, 0, max_ctx, out, workspace, status,
-                                     reinterpret_cast<cudaStream_t>(stream)));
+                                     reinterpret_cast<cudaStream_t>(stream), false));
 }
 
 int tq_decode_attn_mq(const void *params, int d, const void *q, int dtype, int batch, int q_len, int n_q_heads,
@@ -308,11 +319,10 @@ int tq_decode_attn_mq(const void *params, int d, const void *q, int dtype, int b
     if (!q || !k_pool || !v_pool || !block_table || !ctx_lens || !out) return TQ_ERR_INVALID;
     if (!aligned16(k_pool) || !aligned16(v_pool)) return TQ_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_qprep(d, dtype, params, q, batch, q_len, n_q_heads, n_kv_heads, ctx_lens, max_ctx,
-                                 workspace, st);
+    cudaError_t e = launch_qprep(d, dtype, params, q, batch, q_len, n_q_heads, n_kv_heads, workspace, st);
     if (e == cudaSuccess)
         e = launch_splitk(d, params, batch, q_len, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
-                          max_blocks, ctx_lens, 0, max_ctx, out, workspace, status, st);
+                          max_blocks, ctx_lens, 0, max_ctx, out, workspace, status, st, true);
     return cuda_status(e);
 }
 
@@ -377,10 +387,10 @@ int tq_decode_attn_hybrid(const void *params, int d, const void *q, int dtype, i
     const size_t base = al256(decode_workspace_bytes(d, batch, n_q_heads, max_ctx));
     float *lse = reinterpret_cast<float *>(ws + base);
     float *part = reinterpret_cast<float *>(ws + base + al256((size_t)batch * n_q_heads * sizeof(float)));
-    cudaError_t e = launch_qprep(d, dtype, params, q, batch, 1, n_q_heads, n_kv_heads, ctx_lens, max_ctx, ws, st);
+    cudaError_t e = launch_qprep(d, dtype, params, q, batch, 1, n_q_heads, n_kv_heads, ws, st);
     if (e == cudaSuccess)
         e = launch_splitk(d, params, batch, 1, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
-                          max_blocks, ctx_lens, 0, max_ctx, out, ws, status, st, lse);
+                          max_blocks, ctx_lens, 0, max_ctx, out, ws, status, st, true, lse);
     if (e == cudaSuccess)
         e = launch_hybrid_window(d, dtype, win_dtype, q, win_k, win_v, batch, n_q_heads, n_kv_heads, win_cap, win_lens,
                                  part, out, lse, st);

@@ -88,9 +88,8 @@ __global__ void __launch_bounds__(kWWarps * 32, D == 128 ? TQ_WARP_MINBLOCKS : T
 decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ packs, int batch, int q_len, int hq, int hkv,
                    const uint8_t *__restrict__ k_pool, const uint8_t *__restrict__ v_pool, int64_t num_blocks,
                    const int32_t *__restrict__ block_table, int max_blocks, const int32_t *__restrict__ ctx_lens,
-                   int ctx_add, int max_ctx, const int64_t *__restrict__ cpre, const int32_t *__restrict__ cta_b,
-                   float *__restrict__ part, unsigned int *__restrict__ counters, float *__restrict__ out,
-                   float *__restrict__ lse, int32_t *status) {
+                   int ctx_add, int max_ctx, int early, int64_t *__restrict__ cpre, float *__restrict__ part,
+                   float *__restrict__ out, float *__restrict__ lse, int32_t *status) {
     constexpr int NT = kWWarps * 32, NWARP = kWWarps, BPW = kWBpw, NBUF = kWBuf;
     static_assert(NBUF * BPW <= 30, "buffer validity bits");
     constexpr int CH = kBlock * NWARP * BPW;    // tokens per chunk (the schedule's unit)
@@ -123,22 +122,17 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
     for (int i = tid; i < (int)(kStage / 16); i += NT) reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
     __syncthreads();
 
-    pdl_wait();   // everything before this launch (the prep's schedule, packs, counters) is complete
-    pdl_launch_dependents();   // the merge kernel's CTAs may be placed as this pass's CTAs exit
-
-    for (int b = cta; b < batch; b += gridDim.x)
-        if (attended_len(ctx_lens[b], ctx_add, max_ctx) == 0)
-        {
-            for (int i = tid; i < q_len * hq * D; i += NT) out[(size_t)b * q_len * hq * D + i] = 0.f;
-            if (lse)
-                for (int i = tid; i < q_len * hq; i += NT) lse[(size_t)b * q_len * hq + i] = -INFINITY;
-        }
-
-    const int64_t W = cpre[batch];
-    const int P = (int)(W < (int64_t)gridDim.x ? W : (int64_t)gridDim.x);
-    if (cta >= P) return;
-    const int64_t g0 = sk_begin(cta, P, W), g1 = sk_begin(cta + 1, P, W);
-
+    // The schedule, the first segment and its first block ids depend only on the lengths and the
+    // block table, which the prep launch before this one does not write: with `early` they are
+    // worked out before the wait, overlapping that launch (the prep is an ordinary launch, so
+    // every kernel before it has completed).  The packs and the records (the step's appended
+    // token) are read after it.
+    if (!early) pdl_wait();
+    const PassSched sc = pass_schedule<NT>(ctx_lens, ctx_add, batch, hkv, max_ctx, CH, cpre);
+    const int64_t W = sc.W;
+    const int P = sc.P;
+    const bool works = cta < P;
+    const int64_t g0 = works ? sk_begin(cta, P, W) : 0, g1 = works ? sk_begin(cta + 1, P, W) : 0;
     const float inv_sd = rsqrtf((float)D);
     const float c_sc = inv_sd * kLog2e;                             // scores in log2 units
     const float qjl = 1.2533141373155003f / (float)D * 65536.f;    // sqrt(pi/2) / d, and 1 / 2^-16 of the operands
@@ -146,8 +140,10 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
     // The CTA's range [g0, g1) of global chunks, walked one (sequence, kv head) segment at a time.
     struct Seg {
         int b, kh, t0, t1, L;
-        int64_t us, ue, se;
+        int64_t us, ue, se;   // chunks [us, ue) of the segment's (sequence, kv head); the CTA's part ends at se
     };
+    // chunks per kv head of sequence b
+    auto nchunks = [&](int b) { return (attended_len(ctx_lens[b], ctx_add, max_ctx) + CH - 1) / CH; };
     auto make_seg = [&](int b, int kh, int64_t ub, int nchb, int64_t g) {
         Seg s;
         s.b = b;
@@ -163,16 +159,15 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
     // the segment after s, if the range has one
     auto next_seg = [&](const Seg &s, Seg &n) -> bool {
         if (s.se >= g1) return false;
-        int nb = s.b, nkh = s.kh + 1;
-        int64_t nub = cpre[nb];
-        int nn = (int)((cpre[nb + 1] - nub) / hkv);
-        if (nkh == hkv) {
+        int nb = s.b, nkh = s.kh + 1, nn = (int)(s.ue - s.us);
+        int64_t nub = s.us - (int64_t)s.kh * nn;   // the sequence's first chunk
+        if (nkh == hkv) {   // the next sequence with chunks (one exists: s.se < g1 <= W)
             nkh = 0;
+            nub += (int64_t)hkv * nn;
             do {
                 ++nb;
-                nub = cpre[nb];
-                nn = (int)((cpre[nb + 1] - nub) / hkv);
-            } while (nn == 0);
+                nn = nchunks(nb);
+            } while (nn == 0 && nb + 1 < batch);
         }
         n = make_seg(nb, nkh, nub, nn, s.se);
         return true;
@@ -213,12 +208,10 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
         return okm;
     };
 
-    Seg s;
-    {
-        const int b0 = cta_b[cta];
-        const int64_t ub0 = cpre[b0];
-        const int n0 = (int)((cpre[b0 + 1] - ub0) / hkv);
-        s = make_seg(b0, (int)((g0 - ub0) / n0), ub0, n0, g0);
+    Seg s{};
+    if (works) {
+        const int n0 = nchunks(sc.b0);
+        s = make_seg(sc.b0, (int)((g0 - sc.ub0) / n0), sc.ub0, n0, g0);
     }
     bool first_seg = true;
     // Prefetch cursor: the chunks of the CTA's range in order, NBUF - 1 ahead of the one in use,
@@ -230,7 +223,18 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
     int okm = 0;   // bit NBUF-slot * BPW + bw: block bw of the buffer is in range with a valid id
     int buf = 0, pbuf = 0;
     int64_t pids[BPW];
-    load_ids(ps, ptc, pids);
+    if (works) load_ids(ps, ptc, pids);
+    if (early) pdl_wait();
+    pdl_launch_dependents();   // the merge kernel's CTAs may be placed as this pass's CTAs exit
+
+    for (int b = cta; b < batch; b += gridDim.x)
+        if (attended_len(ctx_lens[b], ctx_add, max_ctx) == 0)
+        {
+            for (int i = tid; i < q_len * hq * D; i += NT) out[(size_t)b * q_len * hq * D + i] = 0.f;
+            if (lse)
+                for (int i = tid; i < q_len * hq; i += NT) lse[(size_t)b * q_len * hq + i] = -INFINITY;
+        }
+    if (!works) return;
     auto prefetch = [&]() {
         int bits = 0;
         if (pmore) {
@@ -767,14 +771,14 @@ int warp_ctas_g() {
 template <int D, int G>
 cudaError_t warp_launch_g(int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
                           const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
-                          const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
+                          const int32_t *ctx, int ctx_add, int max_ctx, bool early, const WsLayout &w, float *out,
                           float *lse, int32_t *status) {
     constexpr size_t smem = warp_smem_bytes<D, G>();
     auto kern = decode_warp_kernel<D, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     e = launch_pass(kern, nctas, kWWarps * 32, smem, st, P, w.packs, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx,
-                    ctx_add, max_ctx, w.cpre, w.cta_b, w.part, w.counters, out, lse, status);
+                    ctx_add, max_ctx, early ? 1 : 0, w.cpre, w.part, out, lse, status);
     if (e != cudaSuccess) return e;
     return launch_pass(merge_kernel<D>, batch * hkv, 256, 0, st, P, batch, q_len, hq, hkv, G, (const int64_t *)w.cpre,
                        nctas, (const float *)w.part, out, lse);
@@ -797,9 +801,9 @@ int warp_ctas_d(int G) {
 template <int D>
 cudaError_t warp_launch_d(int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq, int hkv,
                           const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
-                          const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
+                          const int32_t *ctx, int ctx_add, int max_ctx, bool early, const WsLayout &w, float *out,
                           float *lse, int32_t *status) {
-#define TQ_WPASS(GG) return warp_launch_g<D, GG>(nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out, lse, status)
+#define TQ_WPASS(GG) return warp_launch_g<D, GG>(nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, early, w, out, lse, status)
     switch (G) {
         case 1: TQ_WPASS(1);
         case 2: TQ_WPASS(2);
@@ -819,13 +823,13 @@ int warp_pass_ctas(int d, int G) { return d == 128 ? warp_ctas_d<128>(G) : warp_
 
 cudaError_t warp_pass_launch(int d, int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq,
                              int hkv, const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
-                             const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
+                             const int32_t *ctx, int ctx_add, int max_ctx, bool early, const WsLayout &w, float *out,
                              float *lse, int32_t *status) {
     if (d == 128)
-        return warp_launch_d<128>(G, nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w,
-                                  out, lse, status);
-    return warp_launch_d<256>(G, nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, w, out,
-                              lse, status);
+        return warp_launch_d<128>(G, nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx,
+                                  early, w, out, lse, status);
+    return warp_launch_d<256>(G, nctas, st, P, batch, q_len, hq, hkv, kp, vp, nb, bt, mb, ctx, ctx_add, max_ctx, early,
+                              w, out, lse, status);
 }
 
 }  // namespace tq

@@ -699,12 +699,4 @@ cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const
                           is_k ? pool : nullptr, is_k ? nullptr : pool, is_k ? 1 : 2, status, st);
 }
 
-// One new token per sequence, K and V in one launch.
-cudaError_t launch_append(int d, int dtype, const void *params, const void *k_new, const void *v_new, int batch,
-                          int n_heads, const int32_t *bt, int max_blocks, const int32_t *ctx, void *kp, void *vp,
-                          int64_t num_blocks, int32_t *status, cudaStream_t st) {
-    SlotMap map{nullptr, bt, ctx, max_blocks, num_blocks, n_heads};
-    return launch_any<4>(d, dtype, params, k_new, v_new, (int64_t)batch * n_heads, map, kp, vp, 3, status, st);
-}
-
 }  // namespace tq

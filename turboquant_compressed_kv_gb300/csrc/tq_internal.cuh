@@ -47,11 +47,19 @@ struct ParamsHeader {
 };
 static_assert(sizeof(ParamsHeader) == 256, "params header must be 256 bytes");
 
-// Device params: header, D signs (fp32 +-1), S row-major, S transposed.
+// Device params: header, D signs (fp32 +-1), S row-major, S transposed, then the QJL offset
+// weights w (fp32, d): w_j = sum of S[k][j] over the coordinates k at field positions 0..2 of
+// their K record word (qjl_pos below), so that the decode's offset constant of a query is
+// 2^-16 <w, qbar> (the sum of u_k = (S qbar)_k over those coordinates).
 __host__ __device__ constexpr size_t params_off_D(int /*d*/) { return 256; }
 __host__ __device__ constexpr size_t params_off_S(int d) { return 256 + 4 * (size_t)d; }
 __host__ __device__ constexpr size_t params_off_ST(int d) { return params_off_S(d) + 4 * (size_t)d * d; }
-__host__ __device__ constexpr size_t params_total(int d) { return params_off_ST(d) + 4 * (size_t)d * d; }
+__host__ __device__ constexpr size_t params_off_W(int d) { return params_off_ST(d) + 4 * (size_t)d * d; }
+__host__ __device__ constexpr size_t params_total(int d) { return params_off_W(d) + 4 * (size_t)d; }
+
+// Field position (0..3) of coordinate k's QJL bit within its K record word's nibble group:
+// coordinate 16 s + c sits in field 4 (s & 1) + (c & 1) + 2 (c >> 3), position = field & 3.
+__host__ __device__ constexpr int qjl_pos(int k) { return (k & 1) + 2 * ((k & 15) >> 3); }
 
 __host__ __device__ constexpr size_t k_record(int d) { return 8 * (size_t)d + 4 * kBlock; }
 __host__ __device__ constexpr size_t v_record(int d) { return 6 * (size_t)d + 2 * kBlock; }
@@ -247,65 +255,100 @@ __device__ __forceinline__ uint32_t lop_and_xor(uint32_t w, uint32_t mask, uint3
     return d;
 }
 
-// Chunk prefix over sequences (cpre[b] = first global chunk of sequence b's
-// first kv head, cpre[B] = W chunks in all) and the sequence holding the
-// first chunk of each of the P CTAs of the pass.  One CTA of 128 threads.
 // Context length attended for sequence b: the stored length c (plus ctx_add, 1 when the
 // step appends a token first), clamped to [0, max_ctx]; c < 0 means nothing to attend.
 __device__ inline int attended_len(int c, int ctx_add, int max_ctx) {
     return c < 0 ? 0 : clamp_len(c + ctx_add, max_ctx);
 }
 
-constexpr int kSchedCache = 1024;          // sequences whose chunk prefix is searched in shared memory
-
-__device__ inline void build_schedule(const int32_t *__restrict__ ctx_lens, int ctx_add, int batch, int hkv,
-                                      int max_ctx, int chunk, int P, int64_t *__restrict__ cpre,
-                                      int32_t *__restrict__ cta_b) {
-    // P is the pass's grid size; with fewer chunks than CTAs only W CTAs get work
-    __shared__ int64_t s_wsum[4];
-    __shared__ int64_t s_carry;
-    __shared__ int64_t s_cpre[kSchedCache + 1];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        s_carry = 0;
-        cpre[0] = 0;
-        s_cpre[0] = 0;
-    }
-    __syncthreads();
-    for (int base = 0; base < batch; base += 128) {
-        const int b = base + threadIdx.x;
-        int64_t x = 0;
-        if (b < batch) x = (int64_t)hkv * ((attended_len(ctx_lens[b], ctx_add, max_ctx) + chunk - 1) / chunk);
+__device__ __forceinline__ int64_t warp_sum_i64(int64_t x) {
 #pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {      // inclusive warp scan
-            const int64_t y = __shfl_up_sync(0xffffffffu, x, m);
-            if (lane >= m) x += y;
+    for (int m = 16; m > 0; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+    return x;
+}
+
+// The pass's stream-K schedule, worked out by every CTA of the pass from the lengths alone:
+// W = chunks in all (hkv * ceil(len_b / chunk) per sequence b, in (sequence, kv head, chunk)
+// order), P = min(W, grid) working CTAs, and for this CTA (if it works) the sequence b0 holding
+// its first chunk sk_begin(cta, P, W) and that sequence's first chunk ub0.  A block-wide scan
+// over the sequences in tiles of NT threads, stopping at the tile that holds the CTA's first
+// chunk; when cpre is given, CTA 0 scans every tile and writes the prefix (cpre[b] = first
+// chunk of sequence b, cpre[batch] = W) for the merge kernel.
+struct PassSched {
+    int64_t W;
+    int P;
+    int b0;
+    int64_t ub0;
+};
+#ifndef TQ_SCHED_NOINLINE
+#define TQ_SCHED_NOINLINE 1   // the schedule as a call: keeps its registers out of the pass loop's allocation
+#endif
+template <int NT>
+#if TQ_SCHED_NOINLINE
+__device__ __noinline__
+#else
+__device__ __forceinline__
+#endif
+PassSched pass_schedule(const int32_t *__restrict__ ctx_lens, int ctx_add, int batch, int hkv,
+                                   int max_ctx, int chunk, int64_t *__restrict__ cpre) {
+    constexpr int NWP = NT / 32;
+    __shared__ int64_t s_red[NWP];
+    __shared__ int64_t s_hit[2];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    auto nch = [&](int b) -> int64_t {
+        return b < batch ? (int64_t)hkv * ((attended_len(ctx_lens[b], ctx_add, max_ctx) + chunk - 1) / chunk) : 0;
+    };
+    int64_t x = 0;
+    for (int b = tid; b < batch; b += NT) x += nch(b);
+    x = warp_sum_i64(x);
+    if (lane == 0) s_red[warp] = x;
+    if (tid == 0) s_hit[0] = -1;
+    __syncthreads();
+    PassSched r;
+    r.W = 0;
+#pragma unroll
+    for (int w = 0; w < NWP; ++w) r.W += s_red[w];
+    r.P = (int)(r.W < (int64_t)gridDim.x ? r.W : (int64_t)gridDim.x);
+    r.b0 = -1;
+    r.ub0 = 0;
+    __syncthreads();   // s_red is reused below
+    const bool all = (blockIdx.x == 0 && cpre != nullptr);
+    if ((int)blockIdx.x >= r.P && !all) return r;
+    const int64_t g0 = (r.P > 0) ? sk_begin((int)blockIdx.x, r.P, r.W) : 0;
+    if (all && tid == 0) cpre[0] = 0;
+    int64_t carry = 0;
+    for (int base = 0; base < batch; base += NT) {
+        const int b = base + tid;
+        const int64_t own = nch(b);
+        int64_t v = own;   // inclusive scan of the warp
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, v, m);
+            if (lane >= m) v += y;
         }
-        if (lane == 31) s_wsum[warp] = x;
+        if (lane == 31) s_red[warp] = v;
         __syncthreads();
-        int64_t off = s_carry;
-        for (int w = 0; w < warp; ++w) off += s_wsum[w];
+        int64_t off = carry, tot = 0;
+#pragma unroll
+        for (int w = 0; w < NWP; ++w) {
+            off += (w < warp) ? s_red[w] : 0;
+            tot += s_red[w];
+        }
+        const int64_t incl = off + v;
         if (b < batch) {
-            cpre[b + 1] = off + x;
-            if (b < kSchedCache) s_cpre[b + 1] = off + x;
+            if (all) cpre[b + 1] = incl;
+            if (incl > g0 && incl - own <= g0) {   // the one sequence holding chunk g0
+                s_hit[0] = b;
+                s_hit[1] = incl - own;
+            }
         }
-        __syncthreads();                        // every thread has read s_carry and s_wsum
-        if (threadIdx.x == 127) s_carry = off + x;
-        __syncthreads();
+        carry += tot;
+        __syncthreads();   // s_red is read, s_hit is written
+        if (!all && s_hit[0] >= 0) break;
     }
-    const int64_t W = s_carry;
-    if (W < P) P = (int)W;                      // at least one chunk per CTA (the pass does the same)
-    for (int c = threadIdx.x; c < P; c += 128) {
-        const int64_t g0 = sk_begin(c, P, W);
-        int lo = 0, hi = batch - 1;             // first b with cpre[b+1] > g0
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            const int64_t cm = (mid < kSchedCache) ? s_cpre[mid + 1] : cpre[mid + 1];
-            if (cm > g0) hi = mid;
-            else lo = mid + 1;
-        }
-        cta_b[c] = lo;
-    }
+    r.b0 = (int)s_hit[0];
+    r.ub0 = s_hit[1];
+    return r;
 }
 
 // ---------------------------------------------------------------- launchers (defined in the .cu files)
@@ -338,12 +381,15 @@ cudaError_t launch_hybrid_append(int d, int dtype, const void *params, const voi
 // Decode launches take q_len queries per sequence (q[b][i][h], out[b][i][h]); query i attends
 // the first L - (q_len - 1 - i) of the sequence's L attended tokens.  The workspace is laid
 // out for batch sequences of q_len * hq query rows.
-cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int q_len, int hq,
-                         int hkv, const int32_t *ctx_lens, int max_ctx, void *ws, cudaStream_t st);
+// launch_splitk's `early`: the launch before it on the stream is this library's query prep or
+// step prep (an ordinary launch that writes neither the lengths nor the block table), so the pass
+// may read those before waiting for it.  False after any other kernel.
+cudaError_t launch_qprep(int d, int dtype, const void *params, const void *q, int batch, int q_len, int hq, int hkv,
+                         void *ws, cudaStream_t st);
 cudaError_t launch_splitk(int d, const void *params, int batch, int q_len, int hq, int hkv, const void *k_pool,
                           const void *v_pool, int64_t num_blocks, const int32_t *block_table, int max_blocks,
                           const int32_t *ctx_lens, int ctx_add, int max_ctx, float *out, void *ws, int32_t *status,
-                          cudaStream_t st, float *lse = nullptr);
+                          cudaStream_t st, bool early, float *lse = nullptr);
 cudaError_t launch_step(int d, int dtype, const void *params, const void *k_new, const void *v_new, const void *q,
                         int batch, int q_len, int hq, int hkv, const int32_t *block_table, int max_blocks,
                         const int32_t *pre_lens, int max_ctx, void *k_pool, void *v_pool, int64_t num_blocks,

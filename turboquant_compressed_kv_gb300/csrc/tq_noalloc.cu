@@ -70,12 +70,12 @@ extern "C" int tq_decode_attn_noalloc(const void *params, int d, const void *q, 
     cudaError_t e = scratch_for_current_device(&ws);
     if (e != cudaSuccess) return TQ_ERR_CUDA;
     // Every scratch value the kernels read is written earlier in this same
-    // call (the query-prep kernel also resets the split counters), so the
-    // contents left by a previous call need no clearing.
+    // call (the packs by the query prep, the chunk prefix and the partials by
+    // the pass), so the contents left by a previous call need no clearing.
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    e = launch_qprep(d, dtype, params, q, batch, 1, n_q_heads, n_kv_heads, ctx_lens, max_ctx, ws, st);
+    e = launch_qprep(d, dtype, params, q, batch, 1, n_q_heads, n_kv_heads, ws, st);
     if (e == cudaSuccess)
         e = launch_splitk(d, params, batch, 1, n_q_heads, n_kv_heads, k_pool, v_pool, num_blocks, block_table,
-                          max_blocks, ctx_lens, 0, max_ctx, out, ws, status, st);
+                          max_blocks, ctx_lens, 0, max_ctx, out, ws, status, st, true);
     return e == cudaSuccess ? TQ_OK : TQ_ERR_CUDA;
 }

@@ -48,14 +48,12 @@ __host__ __device__ constexpr int pass_chunk(int G) { return kBlock * pass_warps
 
 __host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Workspace: query packs [B*Hkv] | completion counters [B*Hkv] | chunk prefix
-// int64[B+1] | first sequence of each CTA int32[P] | partials [P][2][G][d+4].
-// Sized with Hq >= Hkv, G <= min(8, Hq) and P <= kCtasPerSm * kMaxSms.
+// Workspace: query packs [B*Hkv] | chunk prefix int64[B+1] (written by the pass for the merge
+// kernel) | partials [P][2][G][d+4].  Sized with Hq >= Hkv, G <= min(8, Hq) and
+// P <= kCtasPerSm * kMaxSms.
 struct WsLayout {
     uint8_t *packs;
-    unsigned int *counters;
     int64_t *cpre;
-    int32_t *cta_b;
     float *part;
 };
 inline size_t ws_sizes(int d, int batch, int hq, size_t *off) {
@@ -64,18 +62,14 @@ inline size_t ws_sizes(int d, int batch, int hq, size_t *off) {
     const size_t per_head = kPackBytes(d);
     off[0] = 0;
     off[1] = off[0] + align256((size_t)batch * hq * per_head);
-    off[2] = off[1] + align256((size_t)batch * hq * 4);
-    off[3] = off[2] + align256(((size_t)batch + 1) * 8);
-    off[4] = off[3] + align256(pmax * 4);
-    return off[4] + pmax * 2 * gmax * kPartStride(d) * sizeof(float);
+    off[2] = off[1] + align256(((size_t)batch + 1) * 8);
+    return off[2] + pmax * 2 * gmax * kPartStride(d) * sizeof(float);
 }
 inline WsLayout ws_layout(void *ws, int d, int batch, int hq) {
-    size_t off[5];
+    size_t off[3];
     ws_sizes(d, batch, hq, off);
     uint8_t *base = reinterpret_cast<uint8_t *>(ws);
-    return WsLayout{base + off[0], reinterpret_cast<unsigned int *>(base + off[1]),
-                    reinterpret_cast<int64_t *>(base + off[2]), reinterpret_cast<int32_t *>(base + off[3]),
-                    reinterpret_cast<float *>(base + off[4])};
+    return WsLayout{base + off[0], reinterpret_cast<int64_t *>(base + off[1]), reinterpret_cast<float *>(base + off[2])};
 }
 
 // physical block of logical block lb, or -1 (past the table or outside the pool)
@@ -107,7 +101,7 @@ __device__ __forceinline__ void finish_row(float (&v)[D / 32], float l, const ui
 int warp_pass_ctas(int d, int G);
 cudaError_t warp_pass_launch(int d, int G, int nctas, cudaStream_t st, const uint8_t *P, int batch, int q_len, int hq,
                              int hkv, const uint8_t *kp, const uint8_t *vp, int64_t nb, const int32_t *bt, int mb,
-                             const int32_t *ctx, int ctx_add, int max_ctx, const WsLayout &w, float *out,
+                             const int32_t *ctx, int ctx_add, int max_ctx, bool early, const WsLayout &w, float *out,
                              float *lse, int32_t *status);
 
 }  // namespace tq
