@@ -303,8 +303,9 @@ int tq_decode_attn_hybrid(const void *params, int d, const void *q, int dtype, i
  *                 bytes (the leaving rows and their positions), overwritten.
  * A sequence whose state is not one this call produces (win_lens outside [0, win_cap],
  * ctx_lens < 0, or a window that is not full while ctx_lens[b] mod win_cap != 0) is left
- * unchanged and sets TQ_STATUS_BAD_SLOT; so does a history position without a valid block,
- * whose token is then dropped from the history while the window still advances.
+ * unchanged and sets TQ_STATUS_BAD_SLOT; so is a full window whose leaving token's history
+ * position ctx_lens[b] has no valid block (past max_blocks, or a block id outside
+ * [0, num_blocks)): nothing moves and neither length changes.
  * Two launches on the stream: the window step (the leaving rows copied to scratch, the new token
  * written, the lengths updated), then the encode of the leaving rows.
  * Errors: TQ_ERR_HEAD_DIM, TQ_ERR_DTYPE, TQ_ERR_INVALID (win_cap <= 0 among others),

@@ -375,7 +375,8 @@ def hybrid_append(D, S, k_new, v_new, win_k, win_v, win_lens, ctx_lens, block_ta
     paged pools at that history position (the K and V encodes of this module); the new token then
     takes that slot.  Otherwise the new token goes into slot win_lens[b].  A state this step does
     not produce (lengths out of range, or a window that is not full while ctx_lens[b] mod W != 0)
-    is left as it is; a history position without a valid block loses the leaving token.
+    is left as it is, and so is a full window whose leaving token's history position has no valid
+    block (past the block table, or an id outside the pool): the step cannot be completed there.
     k_new, v_new [B][H][d]; win_k, win_v [B][W][H][d]; kpool / vpool are updated in place.
     Returns (win_k, win_v, win_lens, ctx_lens), updated copies."""
     win_k, win_v = np.array(win_k, copy=True), np.array(win_v, copy=True)
@@ -390,10 +391,11 @@ def hybrid_append(D, S, k_new, v_new, win_k, win_v, win_lens, ctx_lens, block_ta
         if n == W:
             old = L % W
             blk = int(block_table[b, L // BLOCK]) if L // BLOCK < mb else -1
-            if 0 <= blk < nblk:
-                slot = np.array([blk * BLOCK + L % BLOCK], np.int64)
-                encode(True, D, S, np.asarray(win_k[b, old][None], np.float32), slot, kpool)
-                encode(False, D, S, np.asarray(win_v[b, old][None], np.float32), slot, vpool)
+            if not 0 <= blk < nblk:
+                continue
+            slot = np.array([blk * BLOCK + L % BLOCK], np.int64)
+            encode(True, D, S, np.asarray(win_k[b, old][None], np.float32), slot, kpool)
+            encode(False, D, S, np.asarray(win_v[b, old][None], np.float32), slot, vpool)
             win_k[b, old], win_v[b, old] = k_new[b], v_new[b]
             ctx_lens[b] = L + 1
         else:

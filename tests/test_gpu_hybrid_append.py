@@ -41,8 +41,9 @@ def _slot_owner(is_k, d):
 def test_hybrid_append_parity(d, dtype):
     H, W, steps = 2, 4, 5
     # (history length, window length): empty, partly filled, full with no history, full with a
-    # history ending inside a block, full at a block boundary, and a state the upkeep never makes
-    init = [(0, 0), (0, 2), (0, 4), (9, 4), (16, 4), (3, 1)]
+    # history ending inside a block, full at a block boundary, full with the leaving token's
+    # position past the block table (left unchanged), and a state the upkeep never makes
+    init = [(0, 0), (0, 2), (0, 4), (9, 4), (16, 4), (48, 4), (3, 1)]
     B, mb = len(init), 3
     rng = np.random.default_rng(7)
     D, S = synth.rotation_signs(d), synth.qjl_matrix(d)
@@ -51,6 +52,7 @@ def test_hybrid_append_parity(d, dtype):
     bt = rng.permutation(nblk).reshape(B, mb).astype(np.int32)
     win_k = synth.round_dtype(rng.standard_normal((B, W, H, d)).astype(np.float32), dtype)
     win_v = synth.round_dtype(rng.standard_normal((B, W, H, d)).astype(np.float32), dtype)
+    win_k0, win_v0 = win_k.copy(), win_v.copy()
     ctx = np.array([c for c, _ in init], np.int32)
     wl = np.array([w for _, w in init], np.int32)
     kp_o = np.full((nblk, H, oracle.record_bytes(True, d)), FILL, np.uint8)
@@ -70,7 +72,7 @@ def test_hybrid_append_parity(d, dtype):
             kn[0] = 0.0     # a zero vector enters the window and later leaves it
         for b in range(B):   # the rows that leave the window in this step, by the oracle's state
             L, n = int(ctx[b]), int(wl[b])
-            if L >= 0 and n == W:
+            if L >= 0 and n == W and L // 16 < mb:
                 left_k.append(win_k[b, L % W].copy())
                 left_v.append(win_v[b, L % W].copy())
                 left_slots.append(int(bt[b, L // 16]) * 16 + L % 16)
@@ -80,8 +82,9 @@ def test_hybrid_append_parity(d, dtype):
         torch.cuda.synchronize()
         assert np.array_equal(g_ctx.cpu().numpy(), ctx) and np.array_equal(g_wl.cpu().numpy(), wl), step
         assert np.array_equal(_down(g_wk), win_k) and np.array_equal(_down(g_wv), win_v), step
-    assert int(status.item()) == tq.STATUS_BAD_SLOT     # the last sequence's state, left unchanged
-    assert (ctx[-1], wl[-1]) == (3, 1)
+    assert int(status.item()) == tq.STATUS_BAD_SLOT     # the last two sequences' states, left unchanged
+    assert (ctx[-2], wl[-2]) == (48, 4) and (ctx[-1], wl[-1]) == (3, 1)
+    assert np.array_equal(_down(g_wk)[-2], win_k0[-2]) and np.array_equal(_down(g_wv)[-2], win_v0[-2])
 
     # the tokens that left the window, against the oracle's encode of the same rows
     slots = np.array(left_slots, np.int64)
@@ -96,8 +99,8 @@ def test_hybrid_append_parity(d, dtype):
         for blk in range(nblk):   # bytes of slots nothing was encoded into keep the fill
             assert np.all(pool[blk][:, ~written[blk][owner]] == FILL)
 
-    # hybrid attention over the result (the five sequences in states the upkeep makes)
-    n = B - 1
+    # hybrid attention over the result (the five sequences the upkeep advanced)
+    n = B - 2
     Hq = 2 * H
     q = synth.round_dtype(rng.standard_normal((n, Hq, d)).astype(np.float32), dtype)
     out = tq.decode_attn_hybrid(params, d, _up(q, dtype), H, g_kp, g_vp, g_bt[:n].contiguous(),

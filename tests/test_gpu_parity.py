@@ -95,6 +95,38 @@ def test_encode_parity(d, dtype, is_k):
         assert np.all(gp[blk][:, untouched] == FILL)
 
 
+@pytest.mark.parametrize("H", [8, 2, 3])
+def test_encode_v_whole_blocks_and_exceptions(H):
+    """Bulk V encodes whose 16-token blocks map to whole records in token order take the
+    assembled-record path; blocks broken in several ways must still match the oracle: two tokens
+    swapped, a block shifted off the 16-slot alignment, a ragged last tile, and (H = 3) every tile."""
+    d = 128
+    D, S, params, _ = _params(d)
+    nb_tok = 24                                          # 16-token blocks of input
+    N = 16 * nb_tok + 5
+    nblk = nb_tok + 8
+    perm = np.random.default_rng(H).permutation(nblk)
+    slots = np.concatenate([perm[t // 16] * 16 + np.arange(16) for t in range(0, 16 * (nb_tok + 1), 16)])[:N]
+    slots = slots.astype(np.int64)
+    slots[[16 * 3 + 2, 16 * 3 + 9]] = slots[[16 * 3 + 9, 16 * 3 + 2]]   # block 3: two tokens swapped
+    slots[16 * 7:16 * 8] = perm[nb_tok + 2] * 16 + (np.arange(16) + 5) % 16   # block 7: rotated offsets
+    slots[16 * 11:16 * 12] = -1                                           # block 11: padding, skipped
+    x = _inputs(N, H, d, "bf16", seed=H + 100, outliers=False)
+    pool = torch.full((nblk, H, tq.v_record_bytes(d)), FILL, dtype=torch.uint8, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tq.encode_v(params, d, _upload(x, "bf16"), torch.from_numpy(slots).to(DEV), pool, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    gp = pool.cpu().numpy()
+    ok = slots >= 0
+    parity.check_encode(False, D, S, x[ok], slots[ok], gp, pool_fill=FILL)
+    owner = _slot_owner(False, d)
+    written = np.zeros((nblk, 16), bool)
+    written[slots[ok] // 16, slots[ok] % 16] = True
+    for blk in range(nblk):
+        assert np.all(gp[blk][:, ~written[blk][owner]] == FILL)
+
+
 def test_encode_skips_bad_slots_and_flags():
     d, H = 128, 2
     D, S, params, _ = _params(d)

@@ -706,3 +706,19 @@ def test_hybrid_append_leaves_a_state_it_does_not_produce():
     wk2, _, wl, cl = oracle.hybrid_append(D, S, x, x, wk, wk, np.array([1], np.int32), np.array([3], np.int32),
                                           np.array([[0]], np.int32), kp, vp)
     assert np.array_equal(wk2, wk) and (int(wl[0]), int(cl[0])) == (1, 3) and not kp.any()
+
+
+def test_hybrid_append_leaves_a_full_window_whose_token_has_no_block():
+    # the leaving token's history position (16) is past the one-block table: nothing can move,
+    # so neither the window nor the lengths change and the pools stay untouched
+    d, H, W = 128, 1, 4
+    D, S = synth.rotation_signs(d), synth.qjl_matrix(d)
+    kp = np.zeros((2, H, oracle.record_bytes(True, d)), np.uint8)
+    vp = np.zeros((2, H, oracle.record_bytes(False, d)), np.uint8)
+    wk = np.arange(W * H * d, dtype=np.float32).reshape(1, W, H, d)
+    x = np.full((1, H, d), 2.0, np.float32)
+    for table in (np.array([[0]], np.int32), np.array([[0, 7]], np.int32)):   # past the table; id 7 outside the pool
+        wk2, wv2, wl, cl = oracle.hybrid_append(D, S, x, x, wk, wk, np.array([W], np.int32),
+                                                np.array([16], np.int32), table, kp, vp)
+        assert np.array_equal(wk2, wk) and np.array_equal(wv2, wk)
+        assert (int(wl[0]), int(cl[0])) == (W, 16) and not kp.any() and not vp.any()

@@ -184,6 +184,29 @@ def _need_cuda(*ts):
             raise TQError("all tensors must be contiguous")
 
 
+def _on_device(fn):
+    """Run a wrapper with the device of its tensor arguments current, so that the library takes
+    that device's scratch and default stream; tensors (or a stream) on different devices are an
+    error."""
+    import functools
+
+    @functools.wraps(fn)
+    def call(*args, **kwargs):
+        torch = _torch()
+        devs = {a.device for a in list(args) + list(kwargs.values()) if isinstance(a, torch.Tensor) and a.is_cuda}
+        if len(devs) > 1:
+            raise TQError(f"{fn.__name__}: tensors on more than one device ({sorted(map(str, devs))})")
+        if not devs:
+            return fn(*args, **kwargs)
+        dev = devs.pop()
+        st = kwargs.get("stream")
+        if st is not None and st.device != dev:
+            raise TQError(f"{fn.__name__}: the stream is on {st.device}, the tensors on {dev}")
+        with torch.cuda.device(dev):
+            return fn(*args, **kwargs)
+    return call
+
+
 def empty_pool(num_blocks: int, n_kv_heads: int, d: int, kind: str, device="cuda"):
     """Zeroed K or V pool tensor uint8[num_blocks][n_kv_heads][record_bytes]."""
     torch = _torch()
@@ -208,12 +231,14 @@ def codebook_init(d: int, D, S, device="cuda", stream=None):
         raise TQError(f"unsupported head_dim {d}")
     params = torch.empty(nb, dtype=torch.uint8, device=device)
     cent = (ctypes.c_double * 8)()
-    rc = load_library().tq_codebook_init(d, Dn.ctypes.data_as(_P), Sn.ctypes.data_as(_P), _ptr(params), nb,
-                                         cent, _stream(stream))
+    with torch.cuda.device(params.device):
+        rc = load_library().tq_codebook_init(d, Dn.ctypes.data_as(_P), Sn.ctypes.data_as(_P), _ptr(params), nb,
+                                             cent, _stream(stream))
     _check(rc, "tq_codebook_init")
     return params, [float(x) for x in cent]
 
 
+@_on_device
 def encode_k(params, d: int, k, slot_mapping, k_pool, status=None, stream=None):
     """tq_encode_k: k [n_tokens][n_kv_heads][d] (f32/bf16), slot_mapping int64[n_tokens]."""
     _need_cuda(params, k, slot_mapping, k_pool, status)
@@ -223,6 +248,7 @@ def encode_k(params, d: int, k, slot_mapping, k_pool, status=None, stream=None):
     _check(rc, "tq_encode_k")
 
 
+@_on_device
 def encode_v(params, d: int, v, slot_mapping, v_pool, status=None, stream=None):
     """tq_encode_v: v [n_tokens][n_kv_heads][d] (f32/bf16), slot_mapping int64[n_tokens]."""
     _need_cuda(params, v, slot_mapping, v_pool, status)
@@ -232,6 +258,7 @@ def encode_v(params, d: int, v, slot_mapping, v_pool, status=None, stream=None):
     _check(rc, "tq_encode_v")
 
 
+@_on_device
 def paged_append(params, d: int, k_new, v_new, block_table, ctx_lens, k_pool, v_pool, status=None, stream=None):
     """tq_paged_append: one token per sequence at slot ctx_lens[b] (lengths before the append)."""
     _need_cuda(params, k_new, v_new, block_table, ctx_lens, k_pool, v_pool, status)
@@ -242,6 +269,7 @@ def paged_append(params, d: int, k_new, v_new, block_table, ctx_lens, k_pool, v_
     _check(rc, "tq_paged_append")
 
 
+@_on_device
 def decode_attn(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens, max_ctx: int,
                 out=None, workspace=None, status=None, stream=None):
     """tq_decode_attn: q [batch][n_q_heads][d] -> out float32 [batch][n_q_heads][d]."""
@@ -263,6 +291,7 @@ def decode_attn(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table,
 
 # ---------------------------------------------------------------- decode stages
 
+@_on_device
 def decode_qprep(params, d: int, q, n_kv_heads: int, ctx_lens, max_ctx: int, workspace, stream=None):
     """tq_decode_qprep: qbar = Pi q, u = S qbar and the pass's work schedule into the workspace."""
     _need_cuda(params, q, ctx_lens, workspace)
@@ -273,6 +302,7 @@ def decode_qprep(params, d: int, q, n_kv_heads: int, ctx_lens, max_ctx: int, wor
     _check(rc, "tq_decode_qprep")
 
 
+@_on_device
 def decode_splitk(params, d: int, batch: int, n_q_heads: int, n_kv_heads: int, k_pool, v_pool, block_table,
                   ctx_lens, max_ctx: int, out, workspace, status=None, stream=None):
     """tq_decode_splitk: the split-K pass over the compressed cache, merged into out."""
@@ -284,6 +314,7 @@ def decode_splitk(params, d: int, batch: int, n_q_heads: int, n_kv_heads: int, k
     _check(rc, "tq_decode_splitk")
 
 
+@_on_device
 def decode_step(params, d: int, k_new, v_new, q, n_kv_heads: int, k_pool, v_pool, block_table, pre_lens,
                 max_ctx: int, out=None, workspace=None, status=None, stream=None):
     """tq_decode_step: append (k_new, v_new) at position pre_lens[b], then attend pre_lens[b] + 1 tokens."""
@@ -318,16 +349,19 @@ def _dequant(is_k: bool, params, d: int, pool, block_ids, out_dtype, out, status
     return out
 
 
+@_on_device
 def dequant_k(params, d: int, k_pool, block_ids, out_dtype=None, out=None, status=None, stream=None):
     """tq_dequant_k: dense K [len(block_ids) * 16][n_kv_heads][d] of whole paged blocks."""
     return _dequant(True, params, d, k_pool, block_ids, out_dtype or _torch().bfloat16, out, status, stream)
 
 
+@_on_device
 def dequant_v(params, d: int, v_pool, block_ids, out_dtype=None, out=None, status=None, stream=None):
     """tq_dequant_v: dense V [len(block_ids) * 16][n_kv_heads][d] of whole paged blocks."""
     return _dequant(False, params, d, v_pool, block_ids, out_dtype or _torch().bfloat16, out, status, stream)
 
 
+@_on_device
 def decode_attn_hybrid(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens, max_ctx: int,
                        win_k, win_v, win_lens, out=None, workspace=None, status=None, stream=None):
     """tq_decode_attn_hybrid: one softmax over the compressed history (ctx_lens[b] tokens) and the
@@ -350,12 +384,14 @@ def decode_attn_hybrid(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block
     return out
 
 
+@_on_device
 def selftest_wait_timeout(status, stream=None):
     """tq_selftest_wait_timeout: one bounded wait that runs out; ORs STATUS_TIMEOUT into status."""
     _need_cuda(status)
     _check(load_library().tq_selftest_wait_timeout(_ptr(status), _stream(stream)), "tq_selftest_wait_timeout")
 
 
+@_on_device
 def hybrid_append(params, d: int, k_new, v_new, win_k, win_v, win_lens, block_table, ctx_lens, k_pool, v_pool,
                   scratch=None, status=None, stream=None):
     """tq_hybrid_append: k_new / v_new [batch][n_kv_heads][d] into the window win_k / win_v
@@ -377,6 +413,7 @@ def hybrid_append(params, d: int, k_new, v_new, win_k, win_v, win_lens, block_ta
     _check(rc, "tq_hybrid_append")
 
 
+@_on_device
 def decode_attn_mq(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens, max_ctx: int,
                    out=None, workspace=None, status=None, stream=None):
     """tq_decode_attn_mq: q [batch][q_len][n_q_heads][d] -> out float32 of the same shape.
@@ -398,6 +435,7 @@ def decode_attn_mq(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_tab
     return out
 
 
+@_on_device
 def decode_step_mq(params, d: int, k_new, v_new, q, n_kv_heads: int, k_pool, v_pool, block_table, pre_lens,
                    max_ctx: int, out=None, workspace=None, status=None, stream=None):
     """tq_decode_step_mq: append k_new/v_new [batch][q_len][n_kv_heads][d] at pre_lens[b] + i, then
@@ -421,6 +459,7 @@ def decode_step_mq(params, d: int, k_new, v_new, q, n_kv_heads: int, k_pool, v_p
     return out
 
 
+@_on_device
 def decode_attn_noalloc(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens, max_ctx: int,
                         out=None, status=None, stream=None):
     """tq_decode_attn_noalloc: decode attention with the library's fixed scratch instead of a workspace.
@@ -457,6 +496,7 @@ def gq_empty_pool(num_blocks: int, n_kv_heads: int, d: int, bits: int, group: in
     return torch.zeros((num_blocks, n_kv_heads, rec), dtype=torch.uint8, device=device)
 
 
+@_on_device
 def gq_encode(d: int, bits: int, group: int, x, slot_mapping, pool, status=None, stream=None):
     """tq_gq_encode: x [n_tokens][n_kv_heads][d] (f32/bf16) into slot slot_mapping[token] of pool."""
     _need_cuda(x, slot_mapping, pool, status)
@@ -470,6 +510,7 @@ def gq_decode_workspace_bytes(d: int, batch: int, n_q_heads: int, n_kv_heads: in
     return load_library().tq_gq_decode_workspace_bytes(d, batch, n_q_heads, n_kv_heads, max_ctx)
 
 
+@_on_device
 def gq_decode_attn(d: int, bits: int, group: int, q, n_kv_heads: int, k_pool, v_pool, block_table, ctx_lens,
                    max_ctx: int, out=None, workspace=None, status=None, stream=None):
     """tq_gq_decode_attn: q [batch][n_q_heads][d] -> out float32 [batch][n_q_heads][d]."""

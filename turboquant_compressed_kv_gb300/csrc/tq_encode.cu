@@ -17,10 +17,16 @@
 //  3. one warp per vector: ballot-pack cells and signs, byte/word stores.
 // One launch may carry K (blockIdx.y == 0) and V (blockIdx.y == 1) tiles.  Bulk encodes at
 // d = 128 with 16-byte aligned input take the thread-per-row kernel below instead.
+#include <string.h>
+
 #include "tq_internal.cuh"
 #include "tq_tc.cuh"
 #include "tq_prep.cuh"
+#include "tq_tmap.h"
 
+#ifndef TQ_ENC_V_TMA
+#define TQ_ENC_V_TMA 1           // bulk bf16 V at d = 128: TMA tiles, packed transform, whole records (encode128v_tma_kernel)
+#endif
 #ifndef TQ_ENC_SPLIT
 #define TQ_ENC_SPLIT 1           // bulk K at d = 128: two threads per row (encode128k_split_kernel)
 #endif
@@ -156,8 +162,9 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
         const int buf = i % NX, use = i / NX;
         const int64_t v0 = tile_of(i) * kRows, v = v0 + row;
         // the slot is needed only for the stores: a row past the input or without a slot is
-        // computed on whatever its buffer holds (each row's results depend on that row only)
-        const int64_t slot = v < n_vec ? map.slot(v / map.n_heads, status, (v % map.n_heads) == 0) : -1;
+        // computed on whatever its buffer holds (each row's results depend on that row only); its
+        // load is issued here and checked there
+        const int64_t sraw = v < n_vec ? map.slot_raw(v / map.n_heads) : -1;
         if (!tc::mbar_wait(&xfull[wg][buf], use & 1)) timed_out = true;
         // ---- 1. the row, in natural coordinate order
         float val[D];
@@ -303,6 +310,7 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
             tc::fence_before_sync();
         }
         // ---- 5. the record words of this row's slot
+        const int64_t slot = map.slot_check(sraw, status, v < n_vec && (v % map.n_heads) == 0);
         if (slot >= 0) {
             const int64_t blk = slot / kBlock;
             const int o = (int)(slot % kBlock), head = (int)(v % map.n_heads);
@@ -337,6 +345,205 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
     }
 }
 
+// ---------------------------------------------------------------- V at d = 128 from bf16, TMA input
+// Thread r of a CTA of 128 owns row r of a 128-row tile from input to record:
+//  1. the tile arrives as two TMA tensor boxes (columns 0..63 and 64..127, 128 rows x 128 bytes,
+//     swizzled: the 16-byte chunk c of row r sits at chunk c ^ (r & 7)), kNX tiles in flight;
+//  2. the signs D by an XOR of the input words (bit 15 / 31 of each bf16 pair), then the norm and
+//     the 128-point transform on f32x2 pairs (x_k, x_{k+64}): the stage on index bit 6 inside
+//     each pair, the other six between pairs, a packed add and a packed subtract for two
+//     butterflies at once;
+//  3. cells by the three-compare search against the thresholds times the norm;
+//  4. a tile whose 16-token blocks are whole (16-aligned slots in token order; the kv heads H
+//     divide 8, so the tile is 8 / H blocks of H records) assembles its 8 records in shared
+//     memory and writes them with 16-byte stores; any other tile stores its bytes one by one.
+namespace encv {
+constexpr int D = 128, kRows = 128, kThreads = 128, kNX = 2, kCtasPerSm = 3;
+constexpr int kBox = kRows * 128;            // one box: 128 rows x 128 bytes
+constexpr int kTile = 2 * kBox;              // bf16 rows of 256 bytes
+constexpr int kRec = 6 * D + 2 * kBlock;     // V record bytes
+constexpr int kImg = 8 * kRec;               // the 8 records of a whole tile
+constexpr int smem_bytes() { return 1024 + kNX * kTile + kImg; }   // 1024: slack to align the boxes
+}  // namespace encv
+
+__global__ void __launch_bounds__(encv::kThreads, encv::kCtasPerSm)
+encode128v_tma_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__restrict__ params, int64_t n_vec,
+                      SlotMap map, int whole_ok, uint8_t *__restrict__ pool, int32_t *status) {
+    using namespace encv;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *tiles = smem;                  // [kNX][2 boxes][128 rows][128 bytes]
+    uint8_t *img = smem + kNX * kTile;      // [8][kRec]
+    __shared__ uint64_t full[kNX], empty[kNX];
+    __shared__ __align__(16) uint32_t s_sg[D / 2];   // XOR masks of the bf16 pairs
+    __shared__ int64_t s_blk[2][8];                  // first-token slot of each block, by tile parity
+    const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
+    if (ph->magic != kParamsMagic || ph->d != D) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
+        return;
+    }
+    const int tid = threadIdx.x, lane = tid & 31, row = tid;
+    const int64_t ntiles = (n_vec + kRows - 1) / kRows;
+    if ((int64_t)blockIdx.x >= ntiles) return;
+    if (tid == 0) {
+        for (int i = 0; i < kNX; ++i) {
+            tc::mbar_init(&full[i], 1);
+            tc::mbar_init(&empty[i], kThreads / 32);   // one arrival per warp
+        }
+    }
+    if (tid < D / 2) {
+        const float *Dp = reinterpret_cast<const float *>(params + params_off_D(D));
+        s_sg[tid] = (Dp[2 * tid] < 0.f ? 0x8000u : 0u) | (Dp[2 * tid + 1] < 0.f ? 0x80000000u : 0u);
+    }
+    tc::fence_async_smem();
+    __syncthreads();
+    const float t0 = ph->threshold[0], t1 = ph->threshold[1], t2 = ph->threshold[2], t3 = ph->threshold[3];
+    const float t4 = ph->threshold[4], t5 = ph->threshold[5], t6 = ph->threshold[6];
+    const int H = map.n_heads;
+    const bool small = n_vec <= (int64_t)0x7fffffff;
+    bool timed_out = false;
+
+    auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)i * gridDim.x; };
+    auto issue = [&](int i, int buf) {   // thread 0: the tile's two boxes
+        const int y = (int)(tile_of(i) * kRows);
+        tc::mbar_arrive_expect_tx(&full[buf], (uint32_t)kTile);
+        tc::tma_load_2d(tiles + buf * kTile, &tmap, 0, y, &full[buf]);
+        tc::tma_load_2d(tiles + buf * kTile + kBox, &tmap, 64, y, &full[buf]);
+    };
+    if (tid == 0)
+        for (int b2 = 0; b2 < kNX; ++b2)
+            if (tile_of(b2) < ntiles) issue(b2, b2);
+
+#pragma unroll 1
+    for (int i = 0; tile_of(i) < ntiles; ++i) {
+        const int buf = i % kNX, use = i / kNX;
+        const int64_t v0 = tile_of(i) * kRows, v = v0 + row;
+        const bool live = v < n_vec;
+        const int64_t tok = small ? (int64_t)((uint32_t)v / (uint32_t)H) : v / H;
+        const int head = (int)(v - tok * H);
+        const int64_t sraw = live ? map.slot_raw(tok) : -1;   // checked at the stores
+        if (!tc::mbar_wait(&full[buf], use & 1)) timed_out = true;
+        // ---- 1. the row: word p holds coordinates 2p (low half) and 2p + 1 (high half)
+        uint32_t w[64];
+        {
+            const uint8_t *rb = tiles + buf * kTile + row * 128;
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(rb + q * kBox + ((c ^ (row & 7)) << 4));
+                    w[32 * q + 4 * c] = u.x;
+                    w[32 * q + 4 * c + 1] = u.y;
+                    w[32 * q + 4 * c + 2] = u.z;
+                    w[32 * q + 4 * c + 3] = u.w;
+                }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[buf]);   // this warp's rows of the buffer are read
+        // ---- 2. signs, norm, transform on pairs P[k] = (x_k, x_{k+64})
+        float2 P[64];
+#pragma unroll
+        for (int p4 = 0; p4 < 8; ++p4) {
+            const uint4 sa = reinterpret_cast<const uint4 *>(s_sg)[p4], sb = reinterpret_cast<const uint4 *>(s_sg)[p4 + 8];
+            const uint32_t ma[4] = {sa.x, sa.y, sa.z, sa.w}, mb[4] = {sb.x, sb.y, sb.z, sb.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int p = 4 * p4 + e;
+                const uint32_t a = w[p] ^ ma[e], b = w[p + 32] ^ mb[e];
+                P[2 * p] = make_float2(__uint_as_float(a << 16), __uint_as_float(b << 16));
+                P[2 * p + 1] = make_float2(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u));
+            }
+        }
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 64; ++k) acc = __ffma2_rn(P[k], P[k], acc);
+        const float nrm = sqrtf(acc.x + acc.y);
+#pragma unroll
+        for (int k = 0; k < 64; ++k) P[k] = make_float2(P[k].x + P[k].y, P[k].x - P[k].y);
+        const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+        for (int st = 1; st < 64; st <<= 1)
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+                if ((k & st) == 0) {
+                    const float2 a = P[k], b = P[k | st];
+                    P[k] = __fadd2_rn(a, b);
+                    P[k | st] = __ffma2_rn(b, m1, a);   // a - b
+                }
+        // ---- 3. cells against the thresholds times the norm (a zero row keeps the unit thresholds)
+        const float ns = nrm == 0.f ? 1.f : nrm;
+        const float T0 = t0 * ns, T1 = t1 * ns, T2 = t2 * ns, T3 = t3 * ns, T4 = t4 * ns, T5 = t5 * ns, T6 = t6 * ns;
+        // the 48 bytes of the slot, byte (gid, k, hf) at q = 6 gid + 2 k + hf of vb (4 per register)
+        uint32_t vb[12] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int n = 0; n < D; ++n) {
+            const float z = n < 64 ? P[n].x : P[n - 64].y;
+            const bool b2 = z >= T3;
+            const bool b1 = z >= (b2 ? T5 : T1);
+            const bool b0 = z >= (b2 ? (b1 ? T6 : T4) : (b1 ? T2 : T0));
+            const uint32_t cell = (uint32_t)b0 | ((uint32_t)b1 << 1) | ((uint32_t)b2 << 2);
+            // coordinate n = 16 mt + gid + 8 ab: slots 0..11 are field ab (bits 0..2) of byte
+            // (gid, k = mt >> 1, hf = mt & 1); slots 12..15 give bit k of their cell to bit 3 of
+            // field ab of byte (gid, k, hf = mt - 6), k = 0..2
+            const int mt = n >> 4, gid = n & 7, ab = (n >> 3) & 1;
+            if (mt < 6) {
+                const int q = 6 * gid + 2 * (mt >> 1) + (mt & 1);
+                vb[q >> 2] |= cell << (8 * (q & 3) + 4 * ab);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 3; ++k) {
+                    const int q = 6 * gid + 2 * k + (mt - 6);
+                    vb[q >> 2] |= ((cell >> k) & 1u) << (8 * (q & 3) + 4 * ab + 3);
+                }
+            }
+        }
+        // ---- 4. stores
+        const int64_t slot = map.slot_check(sraw, status, live && head == 0);
+        const int rel = row / H, bi = rel >> 4, o = rel & 15;   // token within the tile, its block and offset
+        bool whole = false;
+        if (whole_ok) {   // CTA-uniform
+            if (o == 0 && head == 0) s_blk[i & 1][bi] = sraw;
+            __syncthreads();
+            const int64_t first = s_blk[i & 1][bi];
+            whole = __syncthreads_and(live && slot >= 0 && (int)(slot & 15) == o && (slot >> 4) == (first >> 4));
+        }
+        if (whole) {
+            uint8_t *rec = img + (bi * H + head) * kRec;
+            const int tigv = (o & 7) >> 1, pr = o >> 3, e = o & 1;
+#pragma unroll
+            for (int q = 0; q < 48; ++q) {   // byte (gid, k, hf) of word 3 (L * 2 + pair) + k, byte 2 hf + e
+                const int gid = q / 6, k = (q % 6) >> 1, hf = q & 1;
+                rec[(((4 * gid + tigv) * 2 + pr) * 3 + k) * 4 + 2 * hf + e] = (uint8_t)(vb[q >> 2] >> (8 * (q & 3)));
+            }
+            *reinterpret_cast<__half *>(rec + 6 * D + 2 * o) = __float2half_rn(nrm);
+            __syncthreads();
+            for (int c = tid; c < 8 * (kRec / 16); c += kThreads) {
+                const int j = c / (kRec / 16), cc = c % (kRec / 16);
+                const int64_t blk = s_blk[i & 1][j / H] >> 4;
+                *reinterpret_cast<uint4 *>(pool + ((size_t)blk * H + j % H) * kRec + 16 * cc) =
+                    *reinterpret_cast<const uint4 *>(img + j * kRec + 16 * cc);
+            }
+        } else if (slot >= 0) {
+            const int64_t blk = slot / kBlock;
+            const int so = (int)(slot % kBlock);
+            uint8_t *rec = pool + ((size_t)blk * H + head) * kRec;
+            const int tigv = (so & 7) >> 1, pr = so >> 3, e = so & 1;
+#pragma unroll
+            for (int q = 0; q < 48; ++q) {
+                const int gid = q / 6, k = (q % 6) >> 1, hf = q & 1;
+                rec[(((4 * gid + tigv) * 2 + pr) * 3 + k) * 4 + 2 * hf + e] = (uint8_t)(vb[q >> 2] >> (8 * (q & 3)));
+            }
+            *reinterpret_cast<__half *>(rec + 6 * D + 2 * so) = __float2half_rn(nrm);
+        }
+        // the buffer takes the tile kNX ahead once all four warps have read it (long done by now)
+        if (tid == 0 && tile_of(i + kNX) < ntiles) {
+            if (!tc::mbar_wait(&empty[buf], use & 1)) timed_out = true;
+            issue(i + kNX, buf);
+        }
+    }
+    if (timed_out) flag_status(status, TQ_STATUS_TIMEOUT);
+}
+
 // ---------------------------------------------------------------- K at d = 128, two threads per row
 // As encode128_rows_kernel for K, with each row split over two threads (halves h = 0, 1), so that
 // a thread holds 64 coordinates and an SM runs 16 warps:
@@ -348,13 +555,18 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
 //  * the record words of coordinates 64 h .. 64 h + 63 (words 2h, 2h + 1 of each tig, cells and QJL
 //    sign bits: accumulator columns 64 h .. 64 h + 63) belong to half h, which stores them; half 1
 //    leaves its residual sum in shared memory for half 0, which stores the norms.
-// Two tile groups of 256 threads take alternate tiles of 128 rows.
+// Two tile groups of 256 threads take alternate tiles of 128 rows.  From bf16 the tile arrives as
+// two TMA tensor boxes, the signs D are an XOR of the input words and the transform runs on f32x2
+// pairs (u_m, u_{m+32}): the stage on index bit 5 inside each pair, the five others between pairs.
 namespace encs {
 constexpr int D = 128, kRows = 128, kTg = 2, kThreads = 256 * kTg;
 template <typename T> __host__ __device__ constexpr int nx() { return sizeof(T) == 2 ? 2 : 1; }
 template <typename T> __host__ __device__ constexpr int row_bytes() { return D * (int)sizeof(T); }
 template <typename T> __host__ __device__ constexpr int row_stride() { return row_bytes<T>() + 16; }
-template <typename T> __host__ __device__ constexpr int xbuf_bytes() { return kRows * row_stride<T>(); }
+// bf16 tiles arrive as two TMA boxes (128 rows x 128 bytes, 128-byte swizzle); fp32 rows by one
+// bulk copy each into a padded row stride
+template <typename T> __host__ __device__ constexpr bool tma() { return sizeof(T) == 2; }
+template <typename T> __host__ __device__ constexpr int xbuf_bytes() { return tma<T>() ? 2 * kRows * 128 : kRows * row_stride<T>(); }
 constexpr int oX = 65536;   // after S hi / lo
 template <typename T> __host__ __device__ constexpr int oW() { return oX + kTg * nx<T>() * xbuf_bytes<T>(); }
 constexpr int kWStride = 15;   // per row: 12 partial plane words, the residual sum of squares, two norm shares
@@ -363,15 +575,18 @@ template <typename T> __host__ __device__ constexpr int smem_bytes() { return oW
 
 template <typename T>
 __global__ void __launch_bounds__(encs::kThreads, 1)
-encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict__ x, int64_t n_vec, SlotMap map,
-                        uint8_t *__restrict__ pool, int32_t *status) {
+encode128k_split_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__restrict__ params,
+                        const T *__restrict__ x, int64_t n_vec, SlotMap map, uint8_t *__restrict__ pool,
+                        int32_t *status) {
     using namespace encs;
+    constexpr bool TM = tma<T>();
     constexpr int NX = nx<T>(), RS = row_stride<T>(), RB = row_bytes<T>(), EPC = 16 / (int)sizeof(T);
     constexpr int HC = RB / 32;   // 16-byte chunks per half row
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint64_t xfull[kTg][2], mmabar[kTg];
     __shared__ uint32_t tmem_base;
     __shared__ float s_Dh[2][2][64];   // half h: D_m and (-1)^h D_{m+64}, m < 64
+    __shared__ __align__(16) uint32_t s_sg[D / 2];   // XOR masks of the bf16 pairs (bit 15 / 31: D_2p / D_2p+1 < 0)
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     if (ph->magic != kParamsMagic || ph->d != D) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
@@ -393,6 +608,7 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
         const float *Dp = reinterpret_cast<const float *>(params + params_off_D(D));
         const int hh = tid >> 7, k = (tid >> 6) & 1, m = tid & 63;
         s_Dh[hh][k][m] = (k && hh) ? -Dp[64 + m] : Dp[64 * k + m];
+        if (tid < D / 2) s_sg[tid] = (Dp[2 * tid] < 0.f ? 0x8000u : 0u) | (Dp[2 * tid + 1] < 0.f ? 0x80000000u : 0u);
     }
     {   // B row n = S row k_col_coord(n)
         const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
@@ -428,13 +644,21 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
     const bool issuer = warp == 4 * tg;   // the tile group's first warp moves its rows
 
     auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)(kTg * i + tg) * gridDim.x; };
-    auto issue = [&](int i, int buf) {   // the issuing warp: one bulk copy per row, spread over its lanes
+    auto issue = [&](int i, int buf) {   // the issuing warp: the two boxes, or one bulk copy per row
         const int64_t v0 = tile_of(i) * kRows;
-        const int rows = (int)min((int64_t)kRows, n_vec - v0);
         uint8_t *dst = smem + oX + (tg * NX + buf) * xbuf_bytes<T>();
-        if (lane == 0) tc::mbar_arrive_expect_tx(&xfull[tg][buf], (uint32_t)rows * RB);
-        __syncwarp();
-        for (int r = lane; r < rows; r += 32) tc::bulk_g2s(dst + r * RS, x + (v0 + r) * D, RB, &xfull[tg][buf]);
+        if constexpr (TM) {
+            if (lane == 0) {
+                tc::mbar_arrive_expect_tx(&xfull[tg][buf], (uint32_t)xbuf_bytes<T>());
+                tc::tma_load_2d(dst, &tmap, 0, (int)v0, &xfull[tg][buf]);
+                tc::tma_load_2d(dst + kRows * 128, &tmap, 64, (int)v0, &xfull[tg][buf]);
+            }
+        } else {
+            const int rows = (int)min((int64_t)kRows, n_vec - v0);
+            if (lane == 0) tc::mbar_arrive_expect_tx(&xfull[tg][buf], (uint32_t)rows * RB);
+            __syncwarp();
+            for (int r = lane; r < rows; r += 32) tc::bulk_g2s(dst + r * RS, x + (v0 + r) * D, RB, &xfull[tg][buf]);
+        }
     };
     if (issuer)
         for (int b2 = 0; b2 < NX; ++b2)
@@ -447,12 +671,57 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
         // token and head of row v (32-bit division when the rows fit, as they do in practice)
         const int64_t tok = small ? (int64_t)((uint32_t)v / (uint32_t)map.n_heads) : v / map.n_heads;
         const int head = (int)(v - tok * map.n_heads);
-        const int64_t slot = v < n_vec ? map.slot(tok, status, h == 0 && head == 0) : -1;
+        const int64_t sraw = v < n_vec ? map.slot_raw(tok) : -1;   // checked at the stores
         if (!tc::mbar_wait(&xfull[tg][buf], use & 1)) timed_out = true;
         // ---- 1. the whole row: norm, signs D, and the transform stage on index bit 6
         float u[64];
         float ss = 0.f;
-        {
+        if constexpr (TM) {
+            // pairs P[k] = (u_k, u_{k+32}) of this half; box 0 word p holds x_2p, x_2p+1 and box 1 word p
+            // holds x_64+2p, x_65+2p
+            const uint8_t *xb = smem + oX + (tg * NX + buf) * xbuf_bytes<T>() + row * 128;
+            uint32_t wa[32], wb[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 ua = *reinterpret_cast<const uint4 *>(xb + ((c ^ (row & 7)) << 4));
+                const uint4 ub = *reinterpret_cast<const uint4 *>(xb + kRows * 128 + ((c ^ (row & 7)) << 4));
+                const uint4 ma = reinterpret_cast<const uint4 *>(s_sg)[c], mb = reinterpret_cast<const uint4 *>(s_sg)[c + 8];
+                wa[4 * c] = ua.x ^ ma.x; wa[4 * c + 1] = ua.y ^ ma.y; wa[4 * c + 2] = ua.z ^ ma.z; wa[4 * c + 3] = ua.w ^ ma.w;
+                wb[4 * c] = ub.x ^ mb.x; wb[4 * c + 1] = ub.y ^ mb.y; wb[4 * c + 2] = ub.z ^ mb.z; wb[4 * c + 3] = ub.w ^ mb.w;
+            }
+            const float2 sgn = make_float2(h ? -1.f : 1.f, h ? -1.f : 1.f);
+            float2 P[32];
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {   // u_k = x_k +- x_{k+64}, u_{k+32} = x_{k+32} +- x_{k+96}
+                const uint32_t a0 = wa[k >> 1], a1 = wa[16 + (k >> 1)], b0 = wb[k >> 1], b1 = wb[16 + (k >> 1)];
+                const float2 av = (k & 1) ? make_float2(__uint_as_float(a0 & 0xFFFF0000u), __uint_as_float(a1 & 0xFFFF0000u))
+                                          : make_float2(__uint_as_float(a0 << 16), __uint_as_float(a1 << 16));
+                const float2 bv = (k & 1) ? make_float2(__uint_as_float(b0 & 0xFFFF0000u), __uint_as_float(b1 & 0xFFFF0000u))
+                                          : make_float2(__uint_as_float(b0 << 16), __uint_as_float(b1 << 16));
+                P[k] = __ffma2_rn(bv, sgn, av);
+                acc = __ffma2_rn(P[k], P[k], acc);   // the halves' sums add to 2 |x|^2
+            }
+            ss = acc.x + acc.y;
+            // the 64-point transform of this half: index bit 5 inside the pairs, bits 0..4 between them
+#pragma unroll
+            for (int k = 0; k < 32; ++k) P[k] = make_float2(P[k].x + P[k].y, P[k].x - P[k].y);
+            const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+            for (int st = 1; st < 32; st <<= 1)
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    if ((k & st) == 0) {
+                        const float2 a = P[k], b = P[k | st];
+                        P[k] = __fadd2_rn(a, b);
+                        P[k | st] = __ffma2_rn(b, m1, a);   // a - b
+                    }
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                u[k] = P[k].x;
+                u[k + 32] = P[k].y;
+            }
+        } else {
             const uint8_t *xr = smem + oX + (tg * NX + buf) * xbuf_bytes<T>() + row * RS;
 #pragma unroll
             for (int c = 0; c < HC; ++c) {
@@ -487,16 +756,18 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
         tc::named_sync(bar_id, 256);   // every row is read: the buffer takes the tile NX ahead
         if (issuer && tile_of(i + NX) < ntiles) issue(i + NX, buf);
         const float nrm = sqrtf(0.5f * (ss + sSS[h]));   // the same sum in both halves (addition commutes)
-        // ---- 2. the 64-point transform of this half (index bits 0..5)
+        // ---- 2. the 64-point transform of this half (index bits 0..5; done above from bf16)
+        if constexpr (!TM) {
 #pragma unroll
-        for (int st = 1; st < 64; st <<= 1)
+            for (int st = 1; st < 64; st <<= 1)
 #pragma unroll
-            for (int m = 0; m < 64; ++m)
-                if ((m & st) == 0) {
-                    const float a0 = u[m], a1 = u[m | st];
-                    u[m] = a0 + a1;
-                    u[m | st] = a0 - a1;
-                }
+                for (int m = 0; m < 64; ++m)
+                    if ((m & st) == 0) {
+                        const float a0 = u[m], a1 = u[m | st];
+                        u[m] = a0 + a1;
+                        u[m | st] = a0 - a1;
+                    }
+        }
         // 256 / n (exact scaling of 1 / n): Z = 256 z, and the residual comes out x 256, which keeps
         // its f16 low parts out of the subnormals
         const float rs = nrm > 0.f ? 256.f / nrm : 0.f;
@@ -572,6 +843,7 @@ encode128k_split_kernel(const uint8_t *__restrict__ params, const T *__restrict_
         }
         tc::fence_before_sync();
         // ---- 6. the record words of this row's slot
+        const int64_t slot = map.slot_check(sraw, status, v < n_vec && h == 0 && head == 0);
         if (slot >= 0) {
             const int64_t blk = slot / kBlock;
             const int o = (int)(slot % kBlock);
@@ -606,8 +878,42 @@ cudaError_t launch_encs(const void *params, const void *x, int64_t n_vec, const 
     auto kern = encode128k_split_kernel<T>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    CUtensorMap tm;   // the bf16 input's map (unused from fp32)
+    memset(&tm, 0, sizeof tm);
+    if (encs::tma<T>() && (n_vec > (int64_t)0x7fffffff - encs::kRows || !make_tmap_2d(&tm, x, 2, (unsigned long long)n_vec, encs::D, encs::kRows)))
+        return cudaErrorNotSupported;
     const unsigned grid = (unsigned)(ntiles < sms ? ntiles : sms);
-    kern<<<grid, encs::kThreads, smem, st>>>((const uint8_t *)params, (const T *)x, n_vec, map, (uint8_t *)pool, status);
+    kern<<<grid, encs::kThreads, smem, st>>>(tm, (const uint8_t *)params, (const T *)x, n_vec, map, (uint8_t *)pool, status);
+    return cudaGetLastError();
+}
+
+// The bf16 V encode through TMA; false in *used when the input cannot be mapped (rows past
+// 2^31 - 128, or the driver's tensor-map encoder missing), for the caller to fall back.
+cudaError_t launch_encv_tma(const void *params, const void *x, int64_t n_vec, const SlotMap &map, void *pool,
+                            int32_t *status, cudaStream_t st, bool *used) {
+    *used = false;
+    const int64_t ntiles = (n_vec + encv::kRows - 1) / encv::kRows;
+    if (ntiles <= 0) {
+        *used = true;
+        return cudaSuccess;
+    }
+    if (n_vec > (int64_t)0x7fffffff - encv::kRows) return cudaSuccess;
+    CUtensorMap tm;
+    if (!make_tmap_2d(&tm, x, 2, (unsigned long long)n_vec, encv::D, encv::kRows)) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    constexpr int smem = encv::smem_bytes();
+    e = cudaFuncSetAttribute(encode128v_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t want = (int64_t)sms * encv::kCtasPerSm;
+    const unsigned grid = (unsigned)(ntiles < want ? ntiles : want);
+    const int H = map.n_heads;
+    const int whole_ok = (H == 1 || H == 2 || H == 4 || H == 8) ? 1 : 0;
+    encode128v_tma_kernel<<<grid, encv::kThreads, smem, st>>>(tm, (const uint8_t *)params, n_vec, map, whole_ok,
+                                                              (uint8_t *)pool, status);
+    *used = true;
     return cudaGetLastError();
 }
 
@@ -687,8 +993,18 @@ cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const
     if (d == 128 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0) {
         const int64_t nv = n_tokens * n_heads;
         if (is_k && TQ_ENC_SPLIT)
-            return dtype == TQ_DTYPE_BF16 ? launch_encs<__nv_bfloat16>(params, x, nv, map, pool, status, st)
-                                          : launch_encs<float>(params, x, nv, map, pool, status, st);
+        {
+            if (dtype != TQ_DTYPE_BF16) return launch_encs<float>(params, x, nv, map, pool, status, st);
+            // a bf16 input the tensor map cannot describe takes the thread-per-row kernel
+            const cudaError_t e = launch_encs<__nv_bfloat16>(params, x, nv, map, pool, status, st);
+            if (e != cudaErrorNotSupported) return e;
+            return launch_encr<__nv_bfloat16, true>(params, x, nv, map, pool, status, st);
+        }
+        if (dtype == TQ_DTYPE_BF16 && !is_k && TQ_ENC_V_TMA) {
+            bool used = false;
+            const cudaError_t e = launch_encv_tma(params, x, nv, map, pool, status, st, &used);
+            if (used || e != cudaSuccess) return e;
+        }
         if (dtype == TQ_DTYPE_BF16)
             return is_k ? launch_encr<__nv_bfloat16, true>(params, x, nv, map, pool, status, st)
                         : launch_encr<__nv_bfloat16, false>(params, x, nv, map, pool, status, st);

@@ -277,15 +277,24 @@ __device__ __forceinline__ bool window_state_ok(int ctx, int wl, int win_cap) {
 // One CTA per sequence: a full window's oldest token (all kv heads) is copied into ek / ev and its
 // position into epos (-1: nothing leaves the window); then the new token's rows go into its
 // window slot (the freed one when the window was full) and the lengths are updated.  The
-// encode of the leaving token reads ek / ev, so it may follow this kernel.
+// encode of the leaving token reads ek / ev, so it may follow this kernel.  A state this call
+// does not produce, or a full window whose leaving token has no block in the history (position
+// past the block table, or a block id outside the pool), is flagged TQ_STATUS_BAD_SLOT and left
+// as it is: nothing moves and neither length changes.
 __global__ void __launch_bounds__(128)
 window_step_kernel(const uint8_t *__restrict__ k_new, const uint8_t *__restrict__ v_new, size_t tok_bytes,
                    int win_cap, uint8_t *__restrict__ win_k, uint8_t *__restrict__ win_v, int32_t *ctx_lens,
-                   int32_t *win_lens, uint8_t *__restrict__ ek, uint8_t *__restrict__ ev, int32_t *__restrict__ epos,
-                   int32_t *status) {
+                   int32_t *win_lens, const int32_t *__restrict__ block_table, int max_blocks, int64_t num_blocks,
+                   uint8_t *__restrict__ ek, uint8_t *__restrict__ ev, int32_t *__restrict__ epos, int32_t *status) {
     const int b = blockIdx.x;
     const int ctx = ctx_lens[b], wl = win_lens[b];
-    const bool ok = window_state_ok(ctx, wl, win_cap), full = ok && wl == win_cap;
+    bool ok = window_state_ok(ctx, wl, win_cap);
+    if (ok && wl == win_cap) {   // the leaving token goes to history position ctx: it needs a block
+        const int lb = ctx / kBlock;
+        const int64_t blk = lb < max_blocks ? (int64_t)block_table[(size_t)b * max_blocks + lb] : -1;
+        ok = blk >= 0 && blk < num_blocks;
+    }
+    const bool full = ok && wl == win_cap;
     if (threadIdx.x == 0) {
         epos[b] = full ? ctx : -1;
         if (!ok) flag_status(status, TQ_STATUS_BAD_SLOT);
@@ -325,7 +334,8 @@ cudaError_t launch_hybrid_append(int d, int dtype, const void *params, const voi
     uint8_t *ek = sc + round16((size_t)batch * sizeof(int32_t)), *ev = ek + round16((size_t)batch * tok);
     window_step_kernel<<<batch, 128, 0, st>>>(static_cast<const uint8_t *>(k_new), static_cast<const uint8_t *>(v_new),
                                               tok, win_cap, static_cast<uint8_t *>(win_k), static_cast<uint8_t *>(win_v),
-                                              ctx_lens, win_lens, ek, ev, epos, status);
+                                              ctx_lens, win_lens, block_table, max_blocks, num_blocks, ek, ev, epos,
+                                              status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // the leaving tokens go into the history at their positions (sequences with epos < 0 are skipped)

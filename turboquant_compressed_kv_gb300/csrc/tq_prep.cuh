@@ -23,7 +23,13 @@ struct SlotMap {
             const int L0 = len_of(token);
             return slot_of_block(token, L0, block_at(token, L0), status, report);
         }
-        const int64_t s = slots[token];
+        return slot_check(slots[token], status, report);
+    }
+    // The slot-mapping lookup in two steps, so that the load is issued long before its value is
+    // needed (a branch on it would wait for it): slot_raw reads slots[token], slot_check turns the
+    // value into a slot or -1 (skipped; flagged when outside the pool).
+    __device__ int64_t slot_raw(int64_t token) const { return slots[token]; }
+    __device__ int64_t slot_check(int64_t s, int32_t *status, bool report) const {
         if (s < 0) return -1;
         if (s / kBlock >= num_blocks) {
             if (report) flag_status(status, TQ_STATUS_BAD_SLOT);

@@ -126,6 +126,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, uint32
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_u32(dst_smem)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
+// Tiled copy of one box of a 2-D tensor map (created on the host with cuTensorMapEncodeTiled) to
+// shared memory, at element coordinates (x inner, y outer), completing its bytes on the mbarrier.
+// x times the element size must be a multiple of 16; rows past the tensor's end are filled with
+// zeros (and still counted).  `tmap` is the address of a __grid_constant__ kernel parameter.
+__device__ __forceinline__ void tma_load_2d(void *dst_smem, const void *tmap, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst_smem)), "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)) : "memory");
+}
 // Make this thread's generic-proxy shared-memory writes visible to the tensor core.
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // Named barrier among `count` threads (a multiple of 32).
