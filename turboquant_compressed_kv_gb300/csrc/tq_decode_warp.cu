@@ -224,17 +224,6 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
     int buf = 0, pbuf = 0;
     int64_t pids[BPW];
     if (works) load_ids(ps, ptc, pids);
-    if (early) pdl_wait();
-    pdl_launch_dependents();   // the merge kernel's CTAs may be placed as this pass's CTAs exit
-
-    for (int b = cta; b < batch; b += gridDim.x)
-        if (attended_len(ctx_lens[b], ctx_add, max_ctx) == 0)
-        {
-            for (int i = tid; i < q_len * hq * D; i += NT) out[(size_t)b * q_len * hq * D + i] = 0.f;
-            if (lse)
-                for (int i = tid; i < q_len * hq; i += NT) lse[(size_t)b * q_len * hq + i] = -INFINITY;
-        }
-    if (!works) return;
     auto prefetch = [&]() {
         int bits = 0;
         if (pmore) {
@@ -255,8 +244,27 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
         okm = (okm & ~(((1 << BPW) - 1) << (pbuf * BPW))) | (bits << (pbuf * BPW));
         pbuf = (pbuf + 1 == NBUF) ? 0 : pbuf + 1;
     };
-#pragma unroll
-    for (int k = 0; k < NBUF - 1; ++k) prefetch();
+    // With `early`, the first chunks are staged before the wait too, as long as they hold no
+    // position the step appends (tokens from the stored length ctx_lens[b] on): the prep writes
+    // only those records (and the packs, read after the wait).
+    int npre = 0;
+    if (early && works)
+        while (npre < NBUF - 1 && pmore && ptc + CH <= ctx_lens[ps.b]) {
+            prefetch();
+            ++npre;
+        }
+    if (early) pdl_wait();
+    pdl_launch_dependents();   // the merge kernel's CTAs may be placed as this pass's CTAs exit
+
+    for (int b = cta; b < batch; b += gridDim.x)
+        if (attended_len(ctx_lens[b], ctx_add, max_ctx) == 0)
+        {
+            for (int i = tid; i < q_len * hq * D; i += NT) out[(size_t)b * q_len * hq * D + i] = 0.f;
+            if (lse)
+                for (int i = tid; i < q_len * hq; i += NT) lse[(size_t)b * q_len * hq + i] = -INFINITY;
+        }
+    if (!works) return;
+    for (int k = npre; k < NBUF - 1; ++k) prefetch();
 
 #pragma unroll 1
     while (true) {
