@@ -61,7 +61,7 @@ def parse():
                     help="skip the ragged / long-context decode and the prefill encode measurements")
     ap.add_argument("--workload", default=None,
                     help="run only this side workload (ragged, long256, verify_q2, hybrid32k, prefill_encode, "
-                         "prefill_dequant, gq_compare) and print its JSON object; for profiling")
+                         "prefill_encode256, prefill_dequant, gq_compare) and print its JSON object; for profiling")
     ap.add_argument("--oracle-single-thread", choices=["decode", "encode"], default=None,
                     help=argparse.SUPPRESS)   # child run of the oracle on one thread (cpu_baseline)
     return ap.parse_args()
@@ -586,15 +586,16 @@ def extra_hybrid(steps, warmup, dev, history=30720, window=2048):
     return res
 
 
-def extra_encode(steps, warmup, dev, cpu=False):
-    """Bulk encode of the prefill workload (8 x 32768 tokens x 8 kv heads, d=128, bf16) into paged storage;
-    with cpu, the oracle's encode rate on the host cores beside it."""
+def extra_encode(steps, warmup, dev, cpu=False, name="prefill"):
+    """Bulk encode of a prefill workload into paged storage: "prefill" (8 x 32768 tokens x 8 kv heads,
+    d=128, bf16) or "prefill256" (4 x 32768 tokens x 8 kv heads, d=256, bf16, lognormal K scales); with
+    cpu, the oracle's encode rate on the host cores beside it."""
     import torch
 
     import turboquant_compressed_kv_gb300 as tq
     from turboquant_compressed_kv_gb300 import synth
     from turboquant_compressed_kv_gb300.cache import PagedCache
-    w = synth.workload("prefill")
+    w = synth.workload(name)
     d, Hkv = w.head_dim, w.n_kv_heads
     cache = PagedCache.create(w, dev)
     ntok = sum(w.prefill_lens)
@@ -938,6 +939,8 @@ def bench_tq(args):
                              "hybrid32k": extra_hybrid(ksteps, max(3, args.warmup), dev),
                              "prefill_encode": extra_encode(max(3, min(args.steps, 50)), max(3, args.warmup), dev,
                                                             cpu=rank == 0 and world == 1 and not args.no_cpu_baseline),
+                             "prefill_encode256": extra_encode(max(3, min(args.steps, 50)), max(3, args.warmup),
+                                                               dev, name="prefill256"),
                              "prefill_dequant": extra_dequant(max(3, min(args.steps, 50)), max(3, args.warmup), dev),
                              "gq_compare": extra_gq(max(3, min(args.steps, 100)), max(3, args.warmup), dev)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -967,6 +970,7 @@ def side_workload(args):
             "verify_q2": lambda: extra_verify(steps, warmup, dev),
             "hybrid32k": lambda: extra_hybrid(steps, warmup, dev),
             "prefill_encode": lambda: extra_encode(steps, warmup, dev),
+            "prefill_encode256": lambda: extra_encode(steps, warmup, dev, name="prefill256"),
             "prefill_dequant": lambda: extra_dequant(steps, warmup, dev),
             "gq_compare": lambda: extra_gq(steps, warmup, dev)}
     if args.workload not in runs:

@@ -76,12 +76,14 @@ def test_full_size_sampled_parity(name, units):
         print(f"{name} unit ({b}, {kvh}): worst max-abs {worst[0]:.3e}, worst relative {worst[1]:.3e}")
 
 
-def test_full_size_encode_sampled_parity():
-    """The prefill encode at its full size (8 x 32768 tokens x 8 kv heads, bf16, 2% of K channels
-    x 10), in the launch configuration the benchmark times: the whole batch is encoded in one
+@pytest.mark.parametrize("name", ["prefill", "prefill256"])
+def test_full_size_encode_sampled_parity(name):
+    """The prefill encodes at their full size (prefill: 8 x 32768 tokens x 8 kv heads, d=128, bf16,
+    2% of K channels x 10; prefill256: 4 x 32768 tokens x 8 kv heads, d=256, bf16, lognormal K
+    scales), in the launch configuration the benchmark times: the whole batch is encoded in one
     tq_encode_k and one tq_encode_v call, then 512 sampled tokens (every kv head, K and V) are
     compared with the oracle's encode of the same input rows, read back from the device."""
-    w = synth.workload("prefill")
+    w = synth.workload(name)
     d, Hkv = w.head_dim, w.n_kv_heads
     tq.load_library()
     cache = PagedCache.create(w, DEV)
@@ -106,7 +108,7 @@ def test_full_size_encode_sampled_parity():
     kp, vp = cache.k_pool.cpu().numpy(), cache.v_pool.cpu().numpy()
     sk = parity.check_encode(True, cache.D, cache.S, xk, sl[pick], kp, pool_fill=0)
     sv = parity.check_encode(False, cache.D, cache.S, xv, sl[pick], vp, pool_fill=0)
-    print(f"prefill encode, 512 tokens x {Hkv} heads: K {sk}, V {sv}")
+    print(f"{name} encode, 512 tokens x {Hkv} heads: K {sk}, V {sv}")
 
 
 def test_full_size_dequant_sampled_parity():

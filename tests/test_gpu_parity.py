@@ -95,12 +95,11 @@ def test_encode_parity(d, dtype, is_k):
         assert np.all(gp[blk][:, untouched] == FILL)
 
 
-@pytest.mark.parametrize("H", [8, 2, 3])
-def test_encode_v_whole_blocks_and_exceptions(H):
+@pytest.mark.parametrize("d,H", [(128, 8), (128, 2), (128, 3), (256, 8), (256, 4)])
+def test_encode_v_whole_blocks_and_exceptions(d, H):
     """Bulk V encodes whose 16-token blocks map to whole records in token order take the
     assembled-record path; blocks broken in several ways must still match the oracle: two tokens
     swapped, a block shifted off the 16-slot alignment, a ragged last tile, and (H = 3) every tile."""
-    d = 128
     D, S, params, _ = _params(d)
     nb_tok = 24                                          # 16-token blocks of input
     N = 16 * nb_tok + 5
@@ -111,7 +110,7 @@ def test_encode_v_whole_blocks_and_exceptions(H):
     slots[[16 * 3 + 2, 16 * 3 + 9]] = slots[[16 * 3 + 9, 16 * 3 + 2]]   # block 3: two tokens swapped
     slots[16 * 7:16 * 8] = perm[nb_tok + 2] * 16 + (np.arange(16) + 5) % 16   # block 7: rotated offsets
     slots[16 * 11:16 * 12] = -1                                           # block 11: padding, skipped
-    x = _inputs(N, H, d, "bf16", seed=H + 100, outliers=False)
+    x = _inputs(N, H, d, "bf16", seed=H + 100 + d, outliers=False)
     pool = torch.full((nblk, H, tq.v_record_bytes(d)), FILL, dtype=torch.uint8, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     tq.encode_v(params, d, _upload(x, "bf16"), torch.from_numpy(slots).to(DEV), pool, status=status)

@@ -544,6 +544,192 @@ encode128v_tma_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *_
     if (timed_out) flag_status(status, TQ_STATUS_TIMEOUT);
 }
 
+// ---------------------------------------------------------------- V at d = 256 from bf16, TMA input
+// Two threads per row: thread (row, h) owns coordinates 128 h .. 128 h + 127, which are exactly
+// slot group g = h of the V record (its 48 bytes), so the halves share only the norm.
+//  1. the tile (128 rows x 512 bytes) arrives as four TMA boxes of 64 columns; one tile in
+//     flight, the buffer refilled as soon as every warp has read its rows;
+//  2. half h takes the transform's stage on index bit 7 on the input (u_m = x_m +- x_{m+128},
+//     signs D by XOR), then the 128-point transform of its coordinates on f32x2 pairs
+//     (u_k, u_{k+64}); the halves' sums of squares add to twice |x|^2;
+//  3. cells against the thresholds times the norm, and the group's bytes;
+//  4. whole tiles (as encode128v_tma_kernel) assemble their 8 records in shared memory.
+namespace encv2 {
+constexpr int D = 256, kRows = 128, kThreads = 256, kCtasPerSm = 1;
+constexpr int kBox = kRows * 128;            // one box: 128 rows x 64 bf16
+constexpr int kTile = 4 * kBox;
+constexpr int kRec = 6 * D + 2 * kBlock;
+constexpr int kImg = 8 * kRec;
+constexpr int smem_bytes() { return 1024 + kTile + kImg; }
+}  // namespace encv2
+
+__global__ void __launch_bounds__(encv2::kThreads, encv2::kCtasPerSm)
+encode256v_tma_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__restrict__ params, int64_t n_vec,
+                      SlotMap map, int whole_ok, uint8_t *__restrict__ pool, int32_t *status) {
+    using namespace encv2;
+    constexpr int NG = D / 128;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *tile = smem;                   // [4 boxes][128 rows][128 bytes]
+    uint8_t *img = smem + kTile;            // [8][kRec]
+    __shared__ uint64_t full, empty;
+    __shared__ __align__(16) uint32_t s_sg[D / 2];
+    __shared__ int64_t s_blk[2][8];
+    __shared__ float s_ss[2][kRows];                // the halves' sums of squares
+    const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
+    if (ph->magic != kParamsMagic || ph->d != D) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
+        return;
+    }
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, h = warp >> 2, row = 32 * (warp & 3) + lane;
+    const int64_t ntiles = (n_vec + kRows - 1) / kRows;
+    if ((int64_t)blockIdx.x >= ntiles) return;
+    if (tid == 0) {
+        tc::mbar_init(&full, 1);
+        tc::mbar_init(&empty, kThreads / 32);
+    }
+    if (tid < D / 2) {
+        const float *Dp = reinterpret_cast<const float *>(params + params_off_D(D));
+        s_sg[tid] = (Dp[2 * tid] < 0.f ? 0x8000u : 0u) | (Dp[2 * tid + 1] < 0.f ? 0x80000000u : 0u);
+    }
+    tc::fence_async_smem();
+    __syncthreads();
+    const float t0 = ph->threshold[0], t1 = ph->threshold[1], t2 = ph->threshold[2], t3 = ph->threshold[3];
+    const float t4 = ph->threshold[4], t5 = ph->threshold[5], t6 = ph->threshold[6];
+    const int H = map.n_heads;
+    const bool small = n_vec <= (int64_t)0x7fffffff;
+    bool timed_out = false;
+    auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)i * gridDim.x; };
+    auto issue = [&](int i) {   // thread 0: the tile's four boxes
+        const int y = (int)(tile_of(i) * kRows);
+        tc::mbar_arrive_expect_tx(&full, (uint32_t)kTile);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tc::tma_load_2d(tile + q * kBox, &tmap, 64 * q, y, &full);
+    };
+    if (tid == 0) issue(0);
+
+#pragma unroll 1
+    for (int i = 0; tile_of(i) < ntiles; ++i) {
+        const int64_t v0 = tile_of(i) * kRows, v = v0 + row;
+        const bool live = v < n_vec;
+        const int64_t tok = small ? (int64_t)((uint32_t)v / (uint32_t)H) : v / H;
+        const int head = (int)(v - tok * H);
+        const int64_t sraw = live ? map.slot_raw(tok) : -1;   // checked at the stores
+        if (!tc::mbar_wait(&full, i & 1)) timed_out = true;
+        // ---- 1. pairs P[k] = (u_k, u_{k+64}) of this half: u_m = x_m +- x_{m+128} (signs applied);
+        // box q word p holds coordinates 64 q + 2 p, 64 q + 2 p + 1
+        float2 P[64];
+        {
+            const uint8_t *rb = tile + row * 128;
+            const float2 sgn = make_float2(h ? -1.f : 1.f, h ? -1.f : 1.f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int off = (c ^ (row & 7)) << 4;
+                const uint4 a0 = *reinterpret_cast<const uint4 *>(rb + off);              // x_{8c .. 8c+7}
+                const uint4 a1 = *reinterpret_cast<const uint4 *>(rb + kBox + off);       // x_{64+8c ..}
+                const uint4 b0 = *reinterpret_cast<const uint4 *>(rb + 2 * kBox + off);   // x_{128+8c ..}
+                const uint4 b1 = *reinterpret_cast<const uint4 *>(rb + 3 * kBox + off);   // x_{192+8c ..}
+                const uint4 m0 = reinterpret_cast<const uint4 *>(s_sg)[c], m1 = reinterpret_cast<const uint4 *>(s_sg)[8 + c];
+                const uint4 m2 = reinterpret_cast<const uint4 *>(s_sg)[16 + c], m3 = reinterpret_cast<const uint4 *>(s_sg)[24 + c];
+                const uint32_t wa0[4] = {a0.x ^ m0.x, a0.y ^ m0.y, a0.z ^ m0.z, a0.w ^ m0.w};
+                const uint32_t wa1[4] = {a1.x ^ m1.x, a1.y ^ m1.y, a1.z ^ m1.z, a1.w ^ m1.w};
+                const uint32_t wb0[4] = {b0.x ^ m2.x, b0.y ^ m2.y, b0.z ^ m2.z, b0.w ^ m2.w};
+                const uint32_t wb1[4] = {b1.x ^ m3.x, b1.y ^ m3.y, b1.z ^ m3.z, b1.w ^ m3.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int k = 8 * c + 2 * e;   // pairs k (even) and k + 1 (odd coordinates)
+                    const float2 lo_a = make_float2(__uint_as_float(wa0[e] << 16), __uint_as_float(wa1[e] << 16));
+                    const float2 hi_a = make_float2(__uint_as_float(wa0[e] & 0xFFFF0000u), __uint_as_float(wa1[e] & 0xFFFF0000u));
+                    const float2 lo_b = make_float2(__uint_as_float(wb0[e] << 16), __uint_as_float(wb1[e] << 16));
+                    const float2 hi_b = make_float2(__uint_as_float(wb0[e] & 0xFFFF0000u), __uint_as_float(wb1[e] & 0xFFFF0000u));
+                    P[k] = __ffma2_rn(lo_b, sgn, lo_a);
+                    P[k + 1] = __ffma2_rn(hi_b, sgn, hi_a);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty);   // this warp's rows of the buffer are read
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 64; ++k) acc = __ffma2_rn(P[k], P[k], acc);
+        s_ss[h][row] = acc.x + acc.y;
+        // the buffer takes the next tile once every warp has read it
+        if (tid == 0 && tile_of(i + 1) < ntiles) {
+            if (!tc::mbar_wait(&empty, i & 1)) timed_out = true;
+            issue(i + 1);
+        }
+#pragma unroll
+        for (int k = 0; k < 64; ++k) P[k] = make_float2(P[k].x + P[k].y, P[k].x - P[k].y);
+        const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+        for (int st = 1; st < 64; st <<= 1)
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+                if ((k & st) == 0) {
+                    const float2 a = P[k], b = P[k | st];
+                    P[k] = __fadd2_rn(a, b);
+                    P[k | st] = __ffma2_rn(b, m1, a);   // a - b
+                }
+        __syncthreads();   // both halves' sums of squares are in
+        const float nrm = sqrtf(0.5f * (s_ss[0][row] + s_ss[1][row]));
+        // ---- 2. cells of coordinates 128 h + n against the thresholds times the norm
+        const float ns = nrm == 0.f ? 1.f : nrm;
+        const float T0 = t0 * ns, T1 = t1 * ns, T2 = t2 * ns, T3 = t3 * ns, T4 = t4 * ns, T5 = t5 * ns, T6 = t6 * ns;
+        uint32_t vb[12] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int n = 0; n < 128; ++n) {
+            const float z = n < 64 ? P[n].x : P[n - 64].y;
+            const bool b2 = z >= T3;
+            const bool b1 = z >= (b2 ? T5 : T1);
+            const bool b0 = z >= (b2 ? (b1 ? T6 : T4) : (b1 ? T2 : T0));
+            const uint32_t cell = (uint32_t)b0 | ((uint32_t)b1 << 1) | ((uint32_t)b2 << 2);
+            const int mt = n >> 4, gid = n & 7, ab = (n >> 3) & 1;
+            if (mt < 6) {
+                const int q = 6 * gid + 2 * (mt >> 1) + (mt & 1);
+                vb[q >> 2] |= cell << (8 * (q & 3) + 4 * ab);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 3; ++k) {
+                    const int q = 6 * gid + 2 * k + (mt - 6);
+                    vb[q >> 2] |= ((cell >> k) & 1u) << (8 * (q & 3) + 4 * ab + 3);
+                }
+            }
+        }
+        // ---- 3. stores: byte (gid, k, hf) of group g = h in word ((4 gid + tig) 2 + pair) 3 NG + 3 g + k
+        const int64_t slot = map.slot_check(sraw, status, live && head == 0 && h == 0);
+        const int rel = row / H, bi = rel >> 4, o = rel & 15;
+        bool whole = false;
+        if (whole_ok) {   // CTA-uniform
+            if (o == 0 && head == 0 && h == 0) s_blk[i & 1][bi] = sraw;
+            __syncthreads();
+            const int64_t first = s_blk[i & 1][bi];
+            whole = __syncthreads_and(live && slot >= 0 && (int)(slot & 15) == o && (slot >> 4) == (first >> 4));
+        }
+        auto put = [&](uint8_t *rec, int so) {
+            const int tigv = (so & 7) >> 1, pr = so >> 3, e = so & 1;
+#pragma unroll
+            for (int q = 0; q < 48; ++q) {
+                const int gid = q / 6, k = (q % 6) >> 1, hf = q & 1;
+                rec[(((4 * gid + tigv) * 2 + pr) * 3 * NG + 3 * h + k) * 4 + 2 * hf + e] = (uint8_t)(vb[q >> 2] >> (8 * (q & 3)));
+            }
+            if (h == 0) *reinterpret_cast<__half *>(rec + 6 * D + 2 * so) = __float2half_rn(nrm);
+        };
+        if (whole) {
+            put(img + (bi * H + head) * kRec, o);
+            __syncthreads();
+            for (int c = tid; c < 8 * (kRec / 16); c += kThreads) {
+                const int j = c / (kRec / 16), cc = c % (kRec / 16);
+                const int64_t blk = s_blk[i & 1][j / H] >> 4;
+                *reinterpret_cast<uint4 *>(pool + ((size_t)blk * H + j % H) * kRec + 16 * cc) =
+                    *reinterpret_cast<const uint4 *>(img + j * kRec + 16 * cc);
+            }
+        } else if (slot >= 0) {
+            put(pool + ((size_t)(slot / kBlock) * H + head) * kRec, (int)(slot % kBlock));
+        }
+    }
+    if (timed_out) flag_status(status, TQ_STATUS_TIMEOUT);
+}
+
 // ---------------------------------------------------------------- K at d = 128, two threads per row
 // As encode128_rows_kernel for K, with each row split over two threads (halves h = 0, 1), so that
 // a thread holds 64 coordinates and an SM runs 16 warps:
@@ -917,6 +1103,35 @@ cudaError_t launch_encv_tma(const void *params, const void *x, int64_t n_vec, co
     return cudaGetLastError();
 }
 
+// The bf16 V encode at d = 256 through TMA (as launch_encv_tma).
+cudaError_t launch_encv256_tma(const void *params, const void *x, int64_t n_vec, const SlotMap &map, void *pool,
+                               int32_t *status, cudaStream_t st, bool *used) {
+    *used = false;
+    const int64_t ntiles = (n_vec + encv2::kRows - 1) / encv2::kRows;
+    if (ntiles <= 0) {
+        *used = true;
+        return cudaSuccess;
+    }
+    if (n_vec > (int64_t)0x7fffffff - encv2::kRows) return cudaSuccess;
+    CUtensorMap tm;
+    if (!make_tmap_2d(&tm, x, 2, (unsigned long long)n_vec, encv2::D, encv2::kRows)) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    constexpr int smem = encv2::smem_bytes();
+    e = cudaFuncSetAttribute(encode256v_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t want = (int64_t)sms * encv2::kCtasPerSm;
+    const unsigned grid = (unsigned)(ntiles < want ? ntiles : want);
+    const int H = map.n_heads;
+    const int whole_ok = (H == 1 || H == 2 || H == 4 || H == 8) ? 1 : 0;
+    encode256v_tma_kernel<<<grid, encv2::kThreads, smem, st>>>(tm, (const uint8_t *)params, n_vec, map, whole_ok,
+                                                               (uint8_t *)pool, status);
+    *used = true;
+    return cudaGetLastError();
+}
+
 template <typename T, bool IS_K>
 cudaError_t launch_encr(const void *params, const void *x, int64_t n_vec, const SlotMap &map, void *pool,
                         int32_t *status, cudaStream_t st) {
@@ -1010,6 +1225,11 @@ cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const
                         : launch_encr<__nv_bfloat16, false>(params, x, nv, map, pool, status, st);
         return is_k ? launch_encr<float, true>(params, x, nv, map, pool, status, st)
                     : launch_encr<float, false>(params, x, nv, map, pool, status, st);
+    }
+    if (d == 256 && !is_k && dtype == TQ_DTYPE_BF16 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && TQ_ENC_V_TMA) {
+        bool used = false;
+        const cudaError_t e = launch_encv256_tma(params, x, n_tokens * n_heads, map, pool, status, st, &used);
+        if (used || e != cudaSuccess) return e;
     }
     return launch_any<16>(d, dtype, params, is_k ? x : nullptr, is_k ? nullptr : x, n_tokens * n_heads, map,
                           is_k ? pool : nullptr, is_k ? nullptr : pool, is_k ? 1 : 2, status, st);

@@ -71,13 +71,16 @@ def workload(name: str) -> Workload:
     if name == "prefill":     # 8 x 32768 tokens x Hkv8 x d128, encode only
         return Workload(name, 8, 8, 8, 128, [32768] * 8, "bf16", "outlier10x2pct", [32768] * 8,
                         False, False, 0.0)
+    if name == "prefill256":  # 4 x 32768 tokens x Hkv8 x d256, encode only (shaped like long256)
+        return Workload(name, 4, 8, 8, 256, [32768] * 4, "bf16", "lognormal", [32768] * 4,
+                        False, False, 0.0)
     if name == "long256":     # B4, Hq16, Hkv8, d256, ctx 131072
         return Workload(name, 4, 16, 8, 256, [131072] * 4, "bf16", "lognormal", [131072] * 4,
                         False, False, 0.0)
     raise KeyError(name)
 
 
-WORKLOADS = ["tiny", "llama8b_decode", "ragged", "prefill", "long256"]
+WORKLOADS = ["tiny", "llama8b_decode", "ragged", "prefill", "long256", "prefill256"]
 
 
 def scaled_down(w: Workload, batch: int, max_ctx: int, seed_shift: int = 0) -> Workload:
