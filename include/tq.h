@@ -77,7 +77,9 @@ size_t tq_params_bytes(int d);
  * README K-Cache steps 2 and 5: the random WHT signs and the QJL matrix.]
  *   D_host      host int8[d], the rotation's random sign diagonal (+1/-1).
  *   S_host      host float[d*d], the QJL Gaussian matrix, row-major (row k
- *               produces sign bit k).
+ *               produces sign bit k).  It is held at binary16 precision: each
+ *               entry is rounded to the nearest binary16 value (ties to even), and
+ *               every call uses the rounded matrix.
  *   params_dev  device buffer of >= tq_params_bytes(d) bytes, 16-byte aligned.
  *   centroids_out8  optional host double[8]: the codebook (unit variance).
  * The codebook is solved on the host in fp64 (fixed-point Lloyd-Max, once per

@@ -64,6 +64,12 @@ def test_codebook_on_device(d):
     tf = hdr[48:80].view(np.float32)
     np.testing.assert_array_equal(cf, c.astype(np.float32))
     np.testing.assert_array_equal(tf[:7], t.astype(np.float32))
+    # S is held at binary16 precision: the test matrix is binary16 already, so it is stored as is
+    S = synth.qjl_matrix(d)
+    assert np.array_equal(S.astype(np.float16).astype(np.float32), S)
+    off = 256 + 4 * d
+    sp = params[off:off + 4 * d * d].cpu().numpy().view(np.float32).reshape(d, d)
+    np.testing.assert_array_equal(sp, S)
 
 
 # ------------------------------------------------------------------ encode

@@ -46,6 +46,14 @@ double f16_round_pos(double v, int *ex_out = nullptr) {
     if (ex_out) *ex_out = e;
     return nearbyint(v / ulp) * ulp;  // default rounding mode: to nearest, ties to even
 }
+// Nearest binary16 value of any finite double in the binary16 range (ties to even, subnormals
+// included).
+double f16_round(double v) {
+    const double a = fabs(v);
+    if (a == 0.0) return v;
+    const double r = a < ldexp(1.0, -14) ? nearbyint(a / ldexp(1.0, -24)) * ldexp(1.0, -24) : f16_round_pos(a);
+    return copysign(r, v);
+}
 uint16_t f16_bits(double v) {
     const bool neg = v < 0;
     int e;
@@ -171,15 +179,19 @@ int tq_codebook_init(int d, const int8_t *D_host, const float *S_host, void *par
     cudaError_t e = cudaMemsetAsync(P, 0, sizeof(ParamsHeader), st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(P + params_off_S(d), D_host, (size_t)d, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) { signs_kernel<<<(d + 127) / 128, 128, 0, st>>>(P, d); e = cudaGetLastError(); }
+    // S is held at binary16 precision: the QJL projections then need no low-order part of S on
+    // the tensor cores (sr stays alive until the stream is synchronised below)
+    std::vector<float> sr((size_t)d * d);
+    for (size_t i = 0; i < sr.size(); ++i) sr[i] = (float)f16_round((double)S_host[i]);
     if (e == cudaSuccess)
-        e = cudaMemcpyAsync(P + params_off_S(d), S_host, sizeof(float) * (size_t)d * d, cudaMemcpyHostToDevice, st);
+        e = cudaMemcpyAsync(P + params_off_S(d), sr.data(), sizeof(float) * (size_t)d * d, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) { transpose_kernel<<<d, d, 0, st>>>(P, d); e = cudaGetLastError(); }
     // the QJL offset weights, summed in fp64 (wv stays alive until the stream is synchronised below)
     std::vector<float> wv((size_t)d);
     for (int j = 0; j < d; ++j) {
         double acc = 0.0;
         for (int k = 0; k < d; ++k)
-            if (qjl_pos(k) < 3) acc += (double)S_host[(size_t)k * d + j];
+            if (qjl_pos(k) < 3) acc += (double)sr[(size_t)k * d + j];
         wv[(size_t)j] = (float)acc;
     }
     if (e == cudaSuccess)

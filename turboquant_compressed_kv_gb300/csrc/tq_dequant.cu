@@ -173,7 +173,8 @@ dequant_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ p
 //  2. the row's 128 sign bits become the A operand (f16 +-1, 128-byte swizzle) with one shift
 //     and one LOP3 per two elements: K index 32 tig + 8 w + 2 p + e holds the sign bit of field
 //     p + 4 e of the slot's word (tig, w), bit 4 (p + 4 e) + 3;
-//  3. one thread issues p = S^T b as S_hi + S_lo (B rows = output coordinates, K-major, 16
+//  3. one thread issues p = S^T b with S as one f16 operand (S is held at binary16 precision;
+//     B rows = output coordinates, K-major, 8
 //     f16 MMAs of K = 16) into the warpgroup's 128 tensor-memory columns;
 //  4. the thread reads its row back (tcgen05.ld), adds the codebook values, runs the 128-point
 //     inverse transform in registers, and stores the row.
@@ -226,7 +227,7 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
         s_pair[i][e & 31] = make_float2(ph->centroid[i & 7] * isd, ph->centroid[(i >> 4) & 7] * isd);
     }
     if (tid < D) s_D[tid] = reinterpret_cast<const float *>(params + params_off_D(D))[tid];
-    {   // B: row n = output coordinate n, K index k' as in the A operand; S as f16 hi + lo
+    {   // B: row n = output coordinate n, K index k' as in the A operand; S as f16 (exact), lo = 0
         const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
         for (int e = tid; e < D * D; e += kThreads) {
             const int n = e >> 7, k = e & 127;
@@ -321,9 +322,7 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
                 tc::mma_ss_f16(tmem, tc::sw128_desc(a, ks, kRows), tc::sw128_desc(bh, ks, D), id, ks > 0);
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
-                tc::mma_ss_f16(tmem, tc::sw128_desc(a, ks, kRows), tc::sw128_desc(bl, ks, D), id, true);
+            (void)bl;   // S is held at binary16 precision: its low part is zero
             tc::mma_commit(&mmabar[wg]);
             if (tile_of(i + 2) < ntiles) issue(i + 2, buf);
         }

@@ -54,8 +54,8 @@ encode_kernel(const uint8_t *__restrict__ params, const T *__restrict__ xk, cons
 //  3. the cell by a three-level binary search over the thresholds, whose outcomes are the cell's
 //     bits b2, b1, b0 (cell >= k iff z >= t_{k-1}; ties go up), packed into the plane words;
 //  4. K: the residual rho = z - c[cell] (x 256) as f16 hi and lo goes straight from registers into
-//     tensor memory (this row's lane); one thread issues S rho = S_hi rho_hi + S_hi rho_lo +
-//     S_lo rho_hi (24 f16 MMAs, A in tensor memory, B = S rows reordered so that accumulator
+//     tensor memory (this row's lane); one thread issues S rho = S rho_hi + S rho_lo (S is held at
+//     binary16 precision; 16 f16 MMAs, A in tensor memory, B = S rows reordered so that accumulator
 //     column 32 tig + b is sign bit b of sign word tig); the thread reads its row back and packs
 //     the signs;
 //  5. the record words of the row's slot are stored.
@@ -289,9 +289,7 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
                     tc::mma_ts_f16(tmem + 128, tmem + 64 + 8 * ks, tc::sw128_desc(bh, ks, D), id, true);
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    tc::mma_ts_f16(tmem + 128, tmem + 8 * ks, tc::sw128_desc(bl, ks, D), id, true);
+                (void)bl;   // S is held at binary16 precision: no S_lo rho_hi term
                 tc::mma_commit(&mmabar[wg]);
             }
             if (!tc::mbar_wait(&mmabar[wg], i & 1)) timed_out = true;
@@ -730,6 +728,247 @@ encode256v_tma_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *_
     if (timed_out) flag_status(status, TQ_STATUS_TIMEOUT);
 }
 
+// ---------------------------------------------------------------- K at d = 256 from bf16 on tcgen05
+// A CTA of 256 threads per SM walks tiles of 128 rows; thread (row, h) owns coordinates
+// 128 h .. 128 h + 127 of its row:
+//  1. the tile arrives as four TMA boxes (one tile in flight, refilled once every warp has read
+//     it); half h takes the transform's stage on index bit 7 on the input (u_m = x_m +- x_{m+128},
+//     signs D by XOR), then its 128-point transform on f32x2 pairs (u_k, u_{k+64});
+//  2. the halves' sums of squares give the norm; cells and the residual (x 256) as in the d = 128
+//     encoder, the residual's f16 hi and lo going to this row's tensor-memory lane (A operand:
+//     hi in columns 0..127, lo in 128..255, coordinate 2c and 2c + 1 in column c);
+//  3. one thread issues p = S rho (M = 128 rows, N = 256 projections, K = 256 coordinates) as
+//     S rho_hi + S rho_lo: 32 MMAs into columns 256..511.  S is held at binary16 precision, so
+//     it is one f16 operand (128 KB of shared memory, rows reordered so that accumulator column
+//     64 h2 + 16 tig + 8 wl + f is field f of word (tig, 2 h2 + wl));
+//  4. each half reads back its 128 columns (its own four words per tig) and stores them; half 0
+//     stores fp16 n and gamma.
+namespace enck2 {
+constexpr int D = 256, kRows = 128, kThreads = 256;
+constexpr int kBox = kRows * 128;
+constexpr int kTile = 4 * kBox;                 // 64 KB of bf16 rows
+constexpr int oS = 0;                           // S, f16, 128-byte swizzled K-major, 256 rows
+constexpr int oX = D * D * 2;                   // the input tile
+constexpr int smem_bytes() { return 1024 + oX + kTile; }
+}  // namespace enck2
+
+__global__ void __launch_bounds__(enck2::kThreads, 1)
+encode256k_tc_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *__restrict__ params, int64_t n_vec,
+                     SlotMap map, uint8_t *__restrict__ pool, int32_t *status) {
+    using namespace enck2;
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *tile = smem + oX;
+    __shared__ uint64_t full, empty, mmabar;
+    __shared__ uint32_t tmem_base;
+    __shared__ __align__(16) uint32_t s_sg[D / 2];
+    __shared__ float s_ss[2][kRows], s_g2[kRows];
+    const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
+    if (ph->magic != kParamsMagic || ph->d != D) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
+        return;
+    }
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, h = warp >> 2, row = 32 * (warp & 3) + lane;
+    const int64_t ntiles = (n_vec + kRows - 1) / kRows;
+    if ((int64_t)blockIdx.x >= ntiles) return;
+    if (tid == 0) {
+        tc::mbar_init(&full, 1);
+        tc::mbar_init(&empty, kThreads / 32);
+        tc::mbar_init(&mmabar, 1);
+    }
+    if (warp == 0) tc::tmem_alloc(&tmem_base, 512);
+    if (tid < D / 2) {
+        const float *Dp = reinterpret_cast<const float *>(params + params_off_D(D));
+        s_sg[tid] = (Dp[2 * tid] < 0.f ? 0x8000u : 0u) | (Dp[2 * tid + 1] < 0.f ? 0x80000000u : 0u);
+    }
+    {   // B row n = S row k_col_coord(n), f16 (exact: S is held at binary16 precision)
+        const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
+        for (int e = tid; e < D * D; e += kThreads) {
+            const int n = e >> 8, k = e & 255;
+            *reinterpret_cast<__half *>(smem + oS + tc::sw128_off(n, k, D)) =
+                __float2half_rn(__ldg(S + k_col_coord(n) * D + k));
+        }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const float T0 = 256.f * ph->threshold[0], T1 = 256.f * ph->threshold[1], T2 = 256.f * ph->threshold[2];
+    const float T3 = 256.f * ph->threshold[3], T4 = 256.f * ph->threshold[4], T5 = 256.f * ph->threshold[5];
+    const float T6 = 256.f * ph->threshold[6];
+    const float hw_out = 128.f * (ph->centroid[7] - ph->centroid[6]), hw_in = 128.f * (ph->centroid[5] - ph->centroid[4]);
+    const float inv_sd = rsqrtf((float)D);
+    const int H = map.n_heads;
+    const bool small = n_vec <= (int64_t)0x7fffffff;
+    bool timed_out = false;
+    auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)i * gridDim.x; };
+    auto issue = [&](int i) {   // thread 0: the tile's four boxes
+        const int y = (int)(tile_of(i) * kRows);
+        tc::mbar_arrive_expect_tx(&full, (uint32_t)kTile);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tc::tma_load_2d(tile + q * kBox, &tmap, 64 * q, y, &full);
+    };
+    if (tid == 0) issue(0);
+
+#pragma unroll 1
+    for (int i = 0; tile_of(i) < ntiles; ++i) {
+        const int64_t v0 = tile_of(i) * kRows, v = v0 + row;
+        const bool live = v < n_vec;
+        const int64_t tok = small ? (int64_t)((uint32_t)v / (uint32_t)H) : v / H;
+        const int head = (int)(v - tok * H);
+        const int64_t sraw = live ? map.slot_raw(tok) : -1;   // checked at the stores
+        if (!tc::mbar_wait(&full, i & 1)) timed_out = true;
+        // ---- 1. pairs P[k] = (u_k, u_{k+64}) of this half (as encode256v_tma_kernel)
+        float2 P[64];
+        {
+            const uint8_t *rb = tile + row * 128;
+            const float2 sgn = make_float2(h ? -1.f : 1.f, h ? -1.f : 1.f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const int off = (c ^ (row & 7)) << 4;
+                const uint4 a0 = *reinterpret_cast<const uint4 *>(rb + off);
+                const uint4 a1 = *reinterpret_cast<const uint4 *>(rb + kBox + off);
+                const uint4 b0 = *reinterpret_cast<const uint4 *>(rb + 2 * kBox + off);
+                const uint4 b1 = *reinterpret_cast<const uint4 *>(rb + 3 * kBox + off);
+                const uint4 m0 = reinterpret_cast<const uint4 *>(s_sg)[c], m1 = reinterpret_cast<const uint4 *>(s_sg)[8 + c];
+                const uint4 m2 = reinterpret_cast<const uint4 *>(s_sg)[16 + c], m3 = reinterpret_cast<const uint4 *>(s_sg)[24 + c];
+                const uint32_t wa0[4] = {a0.x ^ m0.x, a0.y ^ m0.y, a0.z ^ m0.z, a0.w ^ m0.w};
+                const uint32_t wa1[4] = {a1.x ^ m1.x, a1.y ^ m1.y, a1.z ^ m1.z, a1.w ^ m1.w};
+                const uint32_t wb0[4] = {b0.x ^ m2.x, b0.y ^ m2.y, b0.z ^ m2.z, b0.w ^ m2.w};
+                const uint32_t wb1[4] = {b1.x ^ m3.x, b1.y ^ m3.y, b1.z ^ m3.z, b1.w ^ m3.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int k = 8 * c + 2 * e;
+                    const float2 lo_a = make_float2(__uint_as_float(wa0[e] << 16), __uint_as_float(wa1[e] << 16));
+                    const float2 hi_a = make_float2(__uint_as_float(wa0[e] & 0xFFFF0000u), __uint_as_float(wa1[e] & 0xFFFF0000u));
+                    const float2 lo_b = make_float2(__uint_as_float(wb0[e] << 16), __uint_as_float(wb1[e] << 16));
+                    const float2 hi_b = make_float2(__uint_as_float(wb0[e] & 0xFFFF0000u), __uint_as_float(wb1[e] & 0xFFFF0000u));
+                    P[k] = __ffma2_rn(lo_b, sgn, lo_a);
+                    P[k + 1] = __ffma2_rn(hi_b, sgn, hi_a);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty);
+        {
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < 64; ++k) acc = __ffma2_rn(P[k], P[k], acc);
+            s_ss[h][row] = acc.x + acc.y;
+        }
+        if (tid == 0 && tile_of(i + 1) < ntiles) {
+            if (!tc::mbar_wait(&empty, i & 1)) timed_out = true;
+            issue(i + 1);
+        }
+#pragma unroll
+        for (int k = 0; k < 64; ++k) P[k] = make_float2(P[k].x + P[k].y, P[k].x - P[k].y);
+        {
+            const float2 m1 = make_float2(-1.f, -1.f);
+#pragma unroll
+            for (int st = 1; st < 64; st <<= 1)
+#pragma unroll
+                for (int k = 0; k < 64; ++k)
+                    if ((k & st) == 0) {
+                        const float2 a = P[k], b = P[k | st];
+                        P[k] = __fadd2_rn(a, b);
+                        P[k | st] = __ffma2_rn(b, m1, a);
+                    }
+        }
+        tc::named_sync(1, kThreads);   // both halves' sums of squares are in
+        const float nrm = sqrtf(0.5f * (s_ss[0][row] + s_ss[1][row]));
+        const float rs = nrm > 0.f ? 256.f / nrm : 0.f;
+        // ---- 2. cells and residual of coordinates 128 h + m (Z = 256 z; see the d = 128 encoder)
+        uint32_t kwd[4][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
+        float g2 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 128; ++m) {
+            float &pz = (m < 64) ? P[m].x : P[m - 64].y;
+            const float Z = pz * rs;
+            const bool b2 = Z >= T3;
+            const bool b1 = Z >= (b2 ? T5 : T1);
+            const float dz = Z - (b2 ? (b1 ? T6 : T4) : (b1 ? T2 : T0));
+            const bool b0 = dz >= 0.f;
+            kwd[k_tig(m)][k_word(m)] |= ((uint32_t)b0 | ((uint32_t)b1 << 1) | ((uint32_t)b2 << 2)) << (4 * k_field(m));
+            const float hw = (b1 == b2) ? hw_out : hw_in;
+            const float rho = b0 ? dz - hw : dz + hw;
+            g2 = fmaf(rho, rho, g2);
+            pz = rho;
+        }
+        if (h == 1) s_g2[row] = g2;
+        // ---- 3. rho (x 256) as f16 hi / lo into this row's lane: columns 64 h + c (hi) and
+        // 128 + 64 h + c (lo) hold coordinates 128 h + 2c, 128 h + 2c + 1
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float hw16[16], lw16[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const int m0 = 32 * q + 2 * c;   // this half's coordinates m0, m0 + 1
+                const float a0 = m0 < 64 ? P[m0].x : P[m0 - 64].y, a1 = (m0 + 1) < 64 ? P[m0 + 1].x : P[m0 + 1 - 64].y;
+                const __half2 hh = __floats2half2_rn(a0, a1);
+                const float2 hf = __half22float2(hh);
+                const __half2 ll = __floats2half2_rn(a0 - hf.x, a1 - hf.y);
+                hw16[c] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&hh));
+                lw16[c] = __uint_as_float(*reinterpret_cast<const uint32_t *>(&ll));
+            }
+            tc::st16(lane_addr + 64 * h + 16 * q, hw16);
+            tc::st16(lane_addr + 128 + 64 * h + 16 * q, lw16);
+        }
+        tc::wait_st();
+        tc::fence_before_sync();
+        tc::named_sync(1, kThreads);
+        tc::fence_after_sync();
+        if (tid == 0) {
+            const uint32_t bs = tc::smem_u32(smem + oS);
+            constexpr uint32_t id = tc::idesc_f16(kRows, D);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                tc::mma_ts_f16(tmem + 256, tmem + 8 * ks, tc::sw128_desc(bs, ks, D), id, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                tc::mma_ts_f16(tmem + 256, tmem + 128 + 8 * ks, tc::sw128_desc(bs, ks, D), id, true);
+            tc::mma_commit(&mmabar);
+        }
+        if (!tc::mbar_wait(&mmabar, i & 1)) timed_out = true;
+        tc::fence_after_sync();
+        // ---- 4. QJL signs: accumulator column 128 h + 16 j + b is field b & 7 of this half's word
+        // (tig j & 3, 2 (j >> 2) + (b >> 3))
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float pv[16];
+            tc::ld16(lane_addr + 256 + 128 * h + 16 * j, pv);
+            tc::wait_ld();
+#pragma unroll
+            for (int b = 0; b < 16; ++b) asm volatile("" : "+f"(pv[b]));   // no use moves above the wait
+#pragma unroll
+            for (int b = 0; b < 16; ++b)
+                kwd[j & 3][2 * (j >> 2) + (b >> 3)] |= ((~__float_as_uint(pv[b]) >> 31) << 3) << (4 * (b & 7));
+        }
+        tc::fence_before_sync();
+        tc::named_sync(1, kThreads);   // half 1's residual sum is in; the accumulator and A are free
+        const int64_t slot = map.slot_check(sraw, status, live && h == 0 && head == 0);
+        if (slot >= 0) {
+            const int64_t blk = slot / kBlock;
+            const int o = (int)(slot % kBlock);
+            uint8_t *rec = pool + ((size_t)blk * H + head) * k_record(D);
+            const int gid = o & 7, th = o >> 3;
+#pragma unroll
+            for (int tig = 0; tig < 4; ++tig)   // words 4 h .. 4 h + 3 of word row (4 gid + tig) * 2 + th
+                reinterpret_cast<uint4 *>(rec)[((4 * gid + tig) * 2 + th) * 2 + h] =
+                    make_uint4(kwd[tig][0], kwd[tig][1], kwd[tig][2], kwd[tig][3]);
+            if (h == 0) {
+                const float gam = sqrtf(g2 + s_g2[row]) * (inv_sd * (1.f / 256.f));
+                *reinterpret_cast<__half2 *>(rec + 8 * D + 4 * o) = __halves2half2(__float2half_rn(nrm), __float2half_rn(gam));
+            }
+        }
+    }
+    if (timed_out) flag_status(status, TQ_STATUS_TIMEOUT);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem_base, 512);
+}
+
 // ---------------------------------------------------------------- K at d = 128, two threads per row
 // As encode128_rows_kernel for K, with each row split over two threads (halves h = 0, 1), so that
 // a thread holds 64 coordinates and an SM runs 16 warps:
@@ -1006,9 +1245,8 @@ encode128k_split_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t 
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
                 tc::mma_ts_f16(tmem + 128, tmem + 64 + 8 * ks, tc::sw128_desc(bh, ks, D), id, true);
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
-                tc::mma_ts_f16(tmem + 128, tmem + 8 * ks, tc::sw128_desc(bl, ks, D), id, true);
+            // S is held at binary16 precision (its low part is zero): no S_lo rho_hi term
+            (void)bl;
             tc::mma_commit(&mmabar[tg]);
         }
         if (!tc::mbar_wait(&mmabar[tg], i & 1)) timed_out = true;
@@ -1132,6 +1370,32 @@ cudaError_t launch_encv256_tma(const void *params, const void *x, int64_t n_vec,
     return cudaGetLastError();
 }
 
+// The bf16 K encode at d = 256 on tcgen05 (as launch_encv_tma).
+cudaError_t launch_enck256_tc(const void *params, const void *x, int64_t n_vec, const SlotMap &map, void *pool,
+                              int32_t *status, cudaStream_t st, bool *used) {
+    *used = false;
+    const int64_t ntiles = (n_vec + enck2::kRows - 1) / enck2::kRows;
+    if (ntiles <= 0) {
+        *used = true;
+        return cudaSuccess;
+    }
+    if (n_vec > (int64_t)0x7fffffff - enck2::kRows) return cudaSuccess;
+    CUtensorMap tm;
+    if (!make_tmap_2d(&tm, x, 2, (unsigned long long)n_vec, enck2::D, enck2::kRows)) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    constexpr int smem = enck2::smem_bytes();
+    e = cudaFuncSetAttribute(encode256k_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(ntiles < sms ? ntiles : sms);
+    encode256k_tc_kernel<<<grid, enck2::kThreads, smem, st>>>(tm, (const uint8_t *)params, n_vec, map, (uint8_t *)pool,
+                                                              status);
+    *used = true;
+    return cudaGetLastError();
+}
+
 template <typename T, bool IS_K>
 cudaError_t launch_encr(const void *params, const void *x, int64_t n_vec, const SlotMap &map, void *pool,
                         int32_t *status, cudaStream_t st) {
@@ -1226,9 +1490,10 @@ cudaError_t launch_encode(bool is_k, int d, int dtype, const void *params, const
         return is_k ? launch_encr<float, true>(params, x, nv, map, pool, status, st)
                     : launch_encr<float, false>(params, x, nv, map, pool, status, st);
     }
-    if (d == 256 && !is_k && dtype == TQ_DTYPE_BF16 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && TQ_ENC_V_TMA) {
+    if (d == 256 && dtype == TQ_DTYPE_BF16 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && TQ_ENC_V_TMA) {
         bool used = false;
-        const cudaError_t e = launch_encv256_tma(params, x, n_tokens * n_heads, map, pool, status, st, &used);
+        const cudaError_t e = is_k ? launch_enck256_tc(params, x, n_tokens * n_heads, map, pool, status, st, &used)
+                                   : launch_encv256_tma(params, x, n_tokens * n_heads, map, pool, status, st, &used);
         if (used || e != cudaSuccess) return e;
     }
     return launch_any<16>(d, dtype, params, is_k ? x : nullptr, is_k ? nullptr : x, n_tokens * n_heads, map,

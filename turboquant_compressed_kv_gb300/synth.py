@@ -7,7 +7,7 @@ device memory.
 
 Random streams (numpy PCG64):
   * rotation sign diagonal D:   default_rng(1), D = 1 - 2*integers(0, 2, d)
-  * QJL Gaussian matrix S[d,d]: default_rng(2), standard_normal, fp32
+  * QJL Gaussian matrix S[d,d]: default_rng(2), standard_normal, rounded to binary16 (held as fp32)
   * data: default_rng([seed, stream, index]) so that any one sequence (or
     prefill chunk) can be regenerated alone, without drawing the others.
 """
@@ -29,8 +29,9 @@ def rotation_signs(d: int, seed: int = 1) -> np.ndarray:
 
 
 def qjl_matrix(d: int, seed: int = 2) -> np.ndarray:
+    """N(0,1) draws rounded to binary16 (the precision the library holds S at), as fp32."""
     rng = np.random.default_rng(seed)
-    return rng.standard_normal((d, d)).astype(np.float32)
+    return rng.standard_normal((d, d)).astype(np.float32).astype(np.float16).astype(np.float32)
 
 
 # ---------------------------------------------------------------- workloads
