@@ -199,7 +199,8 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ uint64_t recbar[kWg][2], mmabar[kWg];
     __shared__ uint32_t tmem_base;
-    __shared__ float s_D[D];
+    __shared__ __align__(16) float s_D[D];
+    __shared__ __align__(16) uint32_t s_dsg[D / 2];   // bf16 pair sign masks of D (bit 15 / 31: D_2j / D_2j+1 < 0)
     // centroid pairs (x 1/sqrt d) of two fields, by a record byte masked to its cell bits (0x77):
     // entry i holds c[i & 7], c[i >> 4]; one copy per lane ([index][lane]), so that a half-warp's
     // lookups never share a bank
@@ -227,6 +228,10 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
         s_pair[i][e & 31] = make_float2(ph->centroid[i & 7] * isd, ph->centroid[(i >> 4) & 7] * isd);
     }
     if (tid < D) s_D[tid] = reinterpret_cast<const float *>(params + params_off_D(D))[tid];
+    if (tid < D / 2) {
+        const float *Dp = reinterpret_cast<const float *>(params + params_off_D(D));
+        s_dsg[tid] = (Dp[2 * tid] < 0.f ? 0x8000u : 0u) | (Dp[2 * tid + 1] < 0.f ? 0x80000000u : 0u);
+    }
     {   // B: row n = output coordinate n, K index k' as in the A operand; S as f16 (exact), lo = 0
         const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
         for (int e = tid; e < D * D; e += kThreads) {
@@ -285,9 +290,7 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
         const int unit_k = row >> 4, t = row & 15;
         const int64_t u = tile * kUnits + unit_k;
         const bool live = u < units;
-        const int64_t blk = live ? block_ids[u / n_heads] : -1;
-        const bool good = live && blk >= 0 && blk < num_blocks;
-        if (live && !good && t == 0) flag_status(status, TQ_STATUS_BAD_SLOT);
+        const int64_t blk = live ? block_ids[u / n_heads] : -1;   // checked at the store
         const uint8_t *rec = smem + oR + ((wg * 2 + buf) * kUnits + unit_k) * kRec;
         const int gid = t & 7, th = t >> 3;
         uint32_t kw[4][4];   // the slot's words [tig][w]
@@ -328,8 +331,9 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
         }
         if (!tc::mbar_wait(&mmabar[wg], i & 1)) timed_out = true;
         tc::fence_after_sync();
-        // y = c[cell] / sqrt d + sqrt(pi/2)/d gamma p, coordinate n in column n
-        float y[D];
+        // y = c[cell] / sqrt d + sqrt(pi/2)/d gamma p on pairs Y[j] = (y_2j, y_2j+1): coordinate n in
+        // column n
+        float2 Y[D / 2];
         const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
 #pragma unroll
         for (int j = 0; j < D / 16; ++j) {
@@ -337,10 +341,11 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
             tc::ld16(taddr + 16 * j, pv);
             tc::wait_ld();
 #pragma unroll
-            for (int x = 0; x < 16; ++x) y[16 * j + x] = pv[x];
+            for (int x = 0; x < 8; ++x) Y[8 * j + x] = make_float2(pv[2 * x], pv[2 * x + 1]);
         }
         tc::fence_before_sync();
         const float gq = qjl * gam;
+        const float2 gq2 = make_float2(gq, gq);
         // byte q of word (tig, w) holds fields 2q, 2q + 1: coordinates x and x + 1 with
         // x = 16 (2 w + (q >> 1)) + 2 tig + 8 (q & 1); one table lookup per byte
 #pragma unroll
@@ -351,36 +356,52 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
                 for (int q = 0; q < 4; ++q) {
                     const float2 cc = s_pair[(kw[tig][w] >> (8 * q)) & 0x77u][tid & 31];
                     const int x = 16 * (2 * w + (q >> 1)) + 2 * tig + 8 * (q & 1);
-                    y[x] = fmaf(gq, y[x], cc.x);
-                    y[x + 1] = fmaf(gq, y[x + 1], cc.y);
+                    Y[x >> 1] = __ffma2_rn(gq2, Y[x >> 1], cc);
                 }
-        // inverse rotation: D (H y) / sqrt d, then the norm
+        // inverse rotation D (H y) / sqrt d: the stage on index bit 0 inside the pairs, bits 1..6
+        // between them (f32x2)
 #pragma unroll
-        for (int st = 1; st < D; st <<= 1)
+        for (int j = 0; j < D / 2; ++j) Y[j] = make_float2(Y[j].x + Y[j].y, Y[j].x - Y[j].y);
+        {
+            const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
-            for (int n = 0; n < D; ++n)
-                if ((n & st) == 0) {
-                    const float a0 = y[n], a1 = y[n | st];
-                    y[n] = a0 + a1;
-                    y[n | st] = a0 - a1;
-                }
+            for (int st = 1; st < D / 2; st <<= 1)
+#pragma unroll
+                for (int j = 0; j < D / 2; ++j)
+                    if ((j & st) == 0) {
+                        const float2 a = Y[j], b = Y[j | st];
+                        Y[j] = __fadd2_rn(a, b);
+                        Y[j | st] = __ffma2_rn(b, m1, a);   // a - b
+                    }
+        }
+        const bool good = live && blk >= 0 && blk < num_blocks;
+        if (live && !good && t == 0) flag_status(status, TQ_STATUS_BAD_SLOT);
         const float sc = good ? nrm * inv_sd : 0.f;
+        const float2 sc2 = make_float2(sc, sc);
         if (live) {
             TO *orow = out + (((size_t)(u / n_heads) * kBlock + t) * n_heads + (u % n_heads)) * D;
 #pragma unroll
-            for (int n = 0; n < D; n += 4) {
-                float o4[4];
+            for (int n = 0; n < D; n += 8) {
+                float2 o[4];
 #pragma unroll
-                for (int x = 0; x < 4; ++x) o4[x] = good ? y[n + x] * sc * s_D[n + x] : 0.f;
+                for (int x = 0; x < 4; ++x) o[x] = __fmul2_rn(Y[n / 2 + x], sc2);
                 if constexpr (sizeof(TO) == 4) {
-                    *reinterpret_cast<float4 *>(orow + n) = make_float4(o4[0], o4[1], o4[2], o4[3]);
-                } else {
-                    const __nv_bfloat162 b01 = __floats2bfloat162_rn(o4[0], o4[1]);
-                    const __nv_bfloat162 b23 = __floats2bfloat162_rn(o4[2], o4[3]);
-                    uint2 v;
-                    v.x = *reinterpret_cast<const uint32_t *>(&b01);
-                    v.y = *reinterpret_cast<const uint32_t *>(&b23);
-                    *reinterpret_cast<uint2 *>(orow + n) = v;
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        const float4 dv = *reinterpret_cast<const float4 *>(&s_D[n + 4 * x]);
+                        *reinterpret_cast<float4 *>(orow + n + 4 * x) =
+                            make_float4(o[2 * x].x * dv.x, o[2 * x].y * dv.y, o[2 * x + 1].x * dv.z, o[2 * x + 1].y * dv.w);
+                    }
+                } else {   // bf16: the signs D by an XOR of the packed words
+                    const uint4 sm = *reinterpret_cast<const uint4 *>(&s_dsg[n / 2]);
+                    const uint32_t smw[4] = {sm.x, sm.y, sm.z, sm.w};
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const __nv_bfloat162 b = __floats2bfloat162_rn(o[x].x, o[x].y);
+                        pk[x] = *reinterpret_cast<const uint32_t *>(&b) ^ smw[x];
+                    }
+                    *reinterpret_cast<uint4 *>(orow + n) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
         }
@@ -413,7 +434,8 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
     using namespace dq128v;
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint64_t recbar[2], recfree[2];
-    __shared__ float s_D[D];
+    __shared__ __align__(16) float s_D[D];
+    __shared__ __align__(16) uint32_t s_dsg[D / 2];   // bf16 pair sign masks of D (bit 15 / 31: D_2j / D_2j+1 < 0)
     // centroid pairs (x 1/sqrt d) of two fields, by a record byte masked to its cell bits (0x77):
     // entry i holds c[i & 7], c[i >> 4]; one copy per lane ([index][lane]), so that a half-warp's
     // lookups never share a bank
@@ -439,6 +461,10 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
     }
     const int lane = row & 31;
     s_D[row] = reinterpret_cast<const float *>(params + params_off_D(D))[row];
+    if (row < D / 2) {
+        const float *Dp = reinterpret_cast<const float *>(params + params_off_D(D));
+        s_dsg[row] = (Dp[2 * row] < 0.f ? 0x8000u : 0u) | (Dp[2 * row + 1] < 0.f ? 0x80000000u : 0u);
+    }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
@@ -472,9 +498,7 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
         const int unit_k = row >> 4, t = row & 15;
         const int64_t u = tile * kUnits + unit_k;
         const bool live = u < units;
-        const int64_t blk = live ? block_ids[u / n_heads] : -1;
-        const bool good = live && blk >= 0 && blk < num_blocks;
-        if (live && !good && t == 0) flag_status(status, TQ_STATUS_BAD_SLOT);
+        const int64_t blk = live ? block_ids[u / n_heads] : -1;   // checked at the store
         const uint8_t *rec = smem + (buf * kUnits + unit_k) * kRec;
         const uint32_t *words = reinterpret_cast<const uint32_t *>(rec);
         // the slot's bytes: per lane gid, words 3 (L * 2 + pair) + k (k = 0..2), bytes 2 hf + e.
@@ -482,7 +506,8 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
         // 16 (2k + hf) + gid + 8 ab) in bits 4ab .. 4ab + 2, and in bit 4ab + 3 bit k of the cell of
         // lane slot 12 + 2hf + ab (coordinate 16 (6 + hf) + gid + 8 ab)
         const int a = (t & 7) >> 1, pr = t >> 3, e = t & 1;
-        float y[D];
+        // pairs P[8 m + g] = (y_{16 m + g}, y_{16 m + g + 8}): one table lookup fills one pair
+        float2 P[D / 2];
 #pragma unroll
         for (int gid = 0; gid < 8; ++gid) {
             uint32_t bt[3][2];
@@ -495,16 +520,10 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-                for (int k = 0; k < 3; ++k) {
-                    const float2 cc = s_pair[bt[k][hf] & 0x77u][lane];
-                    y[16 * (2 * k + hf) + gid] = cc.x;
-                    y[16 * (2 * k + hf) + gid + 8] = cc.y;
-                }
+                for (int k = 0; k < 3; ++k) P[8 * (2 * k + hf) + gid] = s_pair[bt[k][hf] & 0x77u][lane];
                 // bit 3 (ab = 0) and bit 7 (ab = 1) of the three bytes: the cells of slots 12 + 2hf + ab
                 const uint32_t sp = ((bt[0][hf] >> 3) & 0x11u) | ((bt[1][hf] >> 2) & 0x22u) | ((bt[2][hf] >> 1) & 0x44u);
-                const float2 cc = s_pair[sp][lane];
-                y[16 * (6 + hf) + gid] = cc.x;
-                y[16 * (6 + hf) + gid + 8] = cc.y;
+                P[8 * (6 + hf) + gid] = s_pair[sp][lane];
             }
         }
         const __half nh = *reinterpret_cast<const __half *>(rec + 6 * D + 2 * t);
@@ -519,36 +538,52 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
                 issue(i + 2, buf);
             }
         };
-        // inverse rotation: D (H y) / sqrt d, then the norm
+        // inverse rotation D (H y) / sqrt d: index bit 3 inside the pairs; bits 0..2 and 4..6 between
+        // them (pair index bits 0..2 and 3..5), on f32x2
 #pragma unroll
-        for (int st = 1; st < D; st <<= 1)
+        for (int j = 0; j < D / 2; ++j) P[j] = make_float2(P[j].x + P[j].y, P[j].x - P[j].y);
+        {
+            const float2 m1 = make_float2(-1.f, -1.f);
 #pragma unroll
-            for (int n = 0; n < D; ++n)
-                if ((n & st) == 0) {
-                    const float a0 = y[n], a1 = y[n | st];
-                    y[n] = a0 + a1;
-                    y[n | st] = a0 - a1;
-                }
+            for (int st = 1; st < D / 2; st <<= 1)
+#pragma unroll
+                for (int j = 0; j < D / 2; ++j)
+                    if ((j & st) == 0) {
+                        const float2 a2 = P[j], b2 = P[j | st];
+                        P[j] = __fadd2_rn(a2, b2);
+                        P[j | st] = __ffma2_rn(b2, m1, a2);   // a - b
+                    }
+        }
+        const bool good = live && blk >= 0 && blk < num_blocks;
+        if (live && !good && t == 0) flag_status(status, TQ_STATUS_BAD_SLOT);
         const float sc = good ? __half2float(nh) * inv_sd : 0.f;
+        const float2 sc2 = make_float2(sc, sc);
         if (live) {
             TO *orow = out + (((size_t)(u / n_heads) * kBlock + t) * n_heads + (u % n_heads)) * D;
+            // coordinate n is component (n >> 3) & 1 of pair 8 (n >> 4) + (n & 7)
+            auto yv = [&](int n) -> float { return ((n >> 3) & 1) ? P[8 * (n >> 4) + (n & 7)].y : P[8 * (n >> 4) + (n & 7)].x; };
 #pragma unroll
             for (int n = 0; n < D; n += 8) {
-                float o8[8];
+                float2 o[4];
 #pragma unroll
-                for (int x = 0; x < 8; ++x) o8[x] = y[n + x] * sc * s_D[n + x];
+                for (int x = 0; x < 4; ++x) o[x] = __fmul2_rn(make_float2(yv(n + 2 * x), yv(n + 2 * x + 1)), sc2);
                 if constexpr (sizeof(TO) == 4) {
-                    *reinterpret_cast<float4 *>(orow + n) = make_float4(o8[0], o8[1], o8[2], o8[3]);
-                    *reinterpret_cast<float4 *>(orow + n + 4) = make_float4(o8[4], o8[5], o8[6], o8[7]);
-                } else {
-                    uint4 v;
-                    uint32_t *vw = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        const float4 dv = *reinterpret_cast<const float4 *>(&s_D[n + 4 * x]);
+                        *reinterpret_cast<float4 *>(orow + n + 4 * x) =
+                            make_float4(o[2 * x].x * dv.x, o[2 * x].y * dv.y, o[2 * x + 1].x * dv.z, o[2 * x + 1].y * dv.w);
+                    }
+                } else {   // bf16: the signs D by an XOR of the packed words
+                    const uint4 sm = *reinterpret_cast<const uint4 *>(&s_dsg[n / 2]);
+                    const uint32_t smw[4] = {sm.x, sm.y, sm.z, sm.w};
+                    uint32_t pk[4];
 #pragma unroll
                     for (int x = 0; x < 4; ++x) {
-                        const __nv_bfloat162 b2 = __floats2bfloat162_rn(o8[2 * x], o8[2 * x + 1]);
-                        vw[x] = *reinterpret_cast<const uint32_t *>(&b2);
+                        const __nv_bfloat162 b = __floats2bfloat162_rn(o[x].x, o[x].y);
+                        pk[x] = *reinterpret_cast<const uint32_t *>(&b) ^ smw[x];
                     }
-                    *reinterpret_cast<uint4 *>(orow + n) = v;
+                    *reinterpret_cast<uint4 *>(orow + n) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
         }
