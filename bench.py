@@ -20,6 +20,7 @@ With --impl reference the same metric is measured for the fp64 CPU oracle.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -705,8 +706,40 @@ def extra_gq(steps, warmup, dev, group=64):
                          status=status)
     kb, vb = tq.k_record_bytes(d), tq.v_record_bytes(d)
     res = {"config": {"workload": "gq_compare", "batch": B, "n_q_heads": Hq, "n_kv_heads": Hkv, "head_dim": d,
-                      "ctx": L, "group": group, "reference": "dense fp32 attention over the bf16 K / V"},
+                      "ctx": L, "group": group, "reference": "dense fp32 attention over the bf16 K / V",
+                      "k_scales": w.k_scale},
            "turboquant": {"bits_per_dim": round((kb + vb) * 8 / (2 * 16 * d), 4), **fidelity(out)}}
+    # the same comparison with plain N(0,1) keys (no channel scales), information only
+    wn = dataclasses.replace(w, k_scale="none")
+    Kn = torch.empty((B, L, Hkv, d), dtype=torch.bfloat16, device=dev)
+    Vn = torch.empty_like(Kn)
+    kpn, vpn = torch.zeros_like(cache.k_pool), torch.zeros_like(cache.v_pool)
+    gkn = {bits: tq.gq_empty_pool(nblk, Hkv, d, bits, group, dev) for bits in (4, 8)}
+    gvn = {bits: tq.gq_empty_pool(nblk, Hkv, d, bits, group, dev) for bits in (4, 8)}
+    for b in range(B):
+        K, V = synth.kv_tokens_device(wn, b, 0, L, dev)
+        Kn[b], Vn[b] = K, V
+        slots = torch.from_numpy(synth.slots_for(cache.block_table_np, b, 0, L)).to(dev)
+        tq.encode_k(cache.params, d, K, slots, kpn)
+        tq.encode_v(cache.params, d, V, slots, vpn)
+        for bits in (4, 8):
+            tq.gq_encode(d, bits, group, K, slots, gkn[bits])
+            tq.gq_encode(d, bits, group, V, slots, gvn[bits])
+    pn = torch.softmax(torch.einsum("bhgd,blhd->bhgl", qf, Kn.float()) / math.sqrt(d), -1)
+    refn = torch.einsum("bhgl,blhd->bhgd", pn, Vn.float()).reshape(B, Hq, d).double()
+    del pn, Kn, Vn
+
+    def fid_n(o):
+        c = torch.nn.functional.cosine_similarity(o.double(), refn, dim=-1)
+        return {"cos_mean": round(float(c.mean()), 6), "cos_min": round(float(c.min()), 6)}
+
+    on = tq.decode_attn(cache.params, d, q, Hkv, kpn, vpn, cache.block_table, ctx, L, status=status)
+    res["fidelity_n01_keys"] = {"turboquant": fid_n(on)}
+    for bits in (4, 8):
+        og = tq.gq_decode_attn(d, bits, group, q, Hkv, gkn[bits], gvn[bits], cache.block_table, ctx, L,
+                               status=status)
+        res["fidelity_n01_keys"][f"gq{bits}"] = fid_n(og)
+    del kpn, vpn, gkn, gvn, refn
     bt = cache.block_table
     del cache
     stream = torch.cuda.current_stream()
