@@ -39,13 +39,6 @@ cudaError_t launch_pass(void (*kern)(KArgs...), int nctas, int threads, size_t s
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
-// warps of the pass for a group of G query heads, and tokens per chunk
-#ifndef TQ_SPLITK_WIDE_G
-#define TQ_SPLITK_WIDE_G 8       // groups larger than this use 8-warp CTAs (none: 4-warp CTAs measured faster)
-#endif
-__host__ __device__ constexpr int pass_warps(int G) { return G <= TQ_SPLITK_WIDE_G ? 4 : 8; }
-__host__ __device__ constexpr int pass_chunk(int G) { return kBlock * pass_warps(G) * TQ_SPLITK_BPW; }
-
 __host__ __device__ constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Workspace: query packs [B*Hkv] | chunk prefix int64[B+1] (written by the pass for the merge
