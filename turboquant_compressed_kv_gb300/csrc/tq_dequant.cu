@@ -257,27 +257,44 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
 
     // tiles of this warpgroup: blockIdx.x + (2 i + wg) * gridDim.x
     auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)(kWg * i + wg) * gridDim.x; };
-    auto issue = [&](int i, int buf) {   // one thread: the tile's records into buffer buf
+    // the block ids of tile i's records (read a tile before the copies that use them, so that the
+    // issuing thread does not wait for them between the MMA and the read-back)
+    auto load_tile_ids = [&](int i, int32_t (&ids)[kUnits]) {
         const int64_t tile = tile_of(i);
-        uint32_t bytes = 0;
+#pragma unroll
         for (int k = 0; k < kUnits; ++k) {
             const int64_t u = tile * kUnits + k;
-            if (u >= units) break;
-            bytes += kRec;
-        }
-        tc::mbar_arrive_expect_tx(&recbar[wg][buf], bytes);
-        for (int k = 0; k < kUnits; ++k) {
-            const int64_t u = tile * kUnits + k;
-            if (u >= units) break;
-            const int64_t blk = block_ids[u / n_heads];
-            const int64_t bc = (blk >= 0 && blk < num_blocks) ? blk : 0;   // a bad id reads block 0, output zeroed
-            tc::bulk_g2s(smem + oR + ((wg * 2 + buf) * kUnits + k) * kRec,
-                         pool + ((size_t)bc * n_heads + (u % n_heads)) * kRec, kRec, &recbar[wg][buf]);
+            ids[k] = u < units ? block_ids[u / n_heads] : 0;
         }
     };
+    auto issue = [&](int i, int buf, const int32_t (&ids)[kUnits]) {   // one thread: the tile's records into buffer buf
+        const int64_t tile = tile_of(i);
+        uint32_t bytes = 0;
+        for (int k = 0; k < kUnits; ++k)
+            if (tile * kUnits + k < units) bytes += kRec;
+        tc::mbar_arrive_expect_tx(&recbar[wg][buf], bytes);
+#pragma unroll
+        for (int k = 0; k < kUnits; ++k) {
+            const int64_t u = tile * kUnits + k;
+            if (u < units) {
+                const int64_t blk = ids[k];
+                const int64_t bc = (blk >= 0 && blk < num_blocks) ? blk : 0;   // a bad id reads block 0, output zeroed
+                tc::bulk_g2s(smem + oR + ((wg * 2 + buf) * kUnits + k) * kRec,
+                             pool + ((size_t)bc * n_heads + (u % n_heads)) * kRec, kRec, &recbar[wg][buf]);
+            }
+        }
+    };
+    int32_t nids[kUnits];   // row 0: the ids of the tile two ahead
     if (row == 0) {
-        if (tile_of(0) < ntiles) issue(0, 0);
-        if (tile_of(1) < ntiles) issue(1, 1);
+        int32_t ids0[kUnits];
+        if (tile_of(0) < ntiles) {
+            load_tile_ids(0, ids0);
+            issue(0, 0, ids0);
+        }
+        if (tile_of(1) < ntiles) {
+            load_tile_ids(1, ids0);
+            issue(1, 1, ids0);
+        }
     }
     uint8_t *sA = smem + oA + wg * 32768;
     const int bar_id = 1 + wg;   // named barrier of this warpgroup's 128 threads
@@ -286,6 +303,7 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     for (int i = 0; tile_of(i) < ntiles; ++i) {
         const int64_t tile = tile_of(i);
         const int buf = i & 1;
+        if (row == 0 && tile_of(i + 2) < ntiles) load_tile_ids(i + 2, nids);
         if (!tc::mbar_wait(&recbar[wg][buf], (i >> 1) & 1)) timed_out = true;
         const int unit_k = row >> 4, t = row & 15;
         const int64_t u = tile * kUnits + unit_k;
@@ -327,7 +345,7 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
                 tc::mma_ss_f16(tmem, tc::sw128_desc(a, ks, kRows), tc::sw128_desc(bh, ks, D), id, ks > 0);
             (void)bl;   // S is held at binary16 precision: its low part is zero
             tc::mma_commit(&mmabar[wg]);
-            if (tile_of(i + 2) < ntiles) issue(i + 2, buf);
+            if (tile_of(i + 2) < ntiles) issue(i + 2, buf, nids);
         }
         if (!tc::mbar_wait(&mmabar[wg], i & 1)) timed_out = true;
         tc::fence_after_sync();
