@@ -78,6 +78,15 @@ __device__ __forceinline__ uint2 lds_u2(const uint32_t *p) {
     return v;
 }
 
+// 2^x for a per-token softmax weight (x <= 8 in log2 units, or -inf): the hardware approximation
+// with results below 2^-126 flushed to 0, which drops the subnormal range handling of exp2f (a
+// weight that small is below the fp32 resolution of the sum it joins)
+__device__ __forceinline__ float weight_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     const __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&h);
@@ -474,7 +483,7 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
                             const float nv = __half2float(*reinterpret_cast<const __half *>(vrec + 6 * D + 2 * (gid + 8 * r)));
 #pragma unroll
                             for (int nt = 0; nt < NTK; ++nt) {
-                                const float p = exp2f(s2[bw][nt][r] - mref[nt]);
+                                const float p = weight_exp2(s2[bw][nt][r] - mref[nt]);
                                 pr[bw][nt][r] = p;
                                 wv[bw][nt][r] = p * nv;
                                 wmax = fmaxf(wmax, wv[bw][nt][r]);
