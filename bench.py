@@ -301,6 +301,21 @@ def profile_traffic(bytes_per_launch):
         return None
 
 
+def run_ahead(dev, n_iters, body, batch=100, lead_ms=30.0):
+    """body(i) for i < n_iters, in batches that each start behind a short spin kernel on the current
+    stream, so that the interpreter has queued the whole batch before the GPU reaches it.  Event pairs
+    inside body then time device work only: in a plain loop whose calls take the interpreter longer
+    to issue than the GPU takes to run them, an event pair around one call also spans the time the
+    GPU sat waiting for that call to be queued."""
+    import torch
+    cycles = int(lead_ms * 1e-3 * 2.2e9)
+    for b0 in range(0, n_iters, batch):
+        torch.cuda._sleep(cycles)
+        for i in range(b0, min(n_iters, b0 + batch)):
+            body(i)
+        torch.cuda.synchronize(dev)
+
+
 def extra_decode(name, steps, warmup, dev):
     """Decode pass (query prep + split-K) on another decode workload; inputs drawn on the device."""
     import torch
@@ -350,9 +365,7 @@ def extra_decode(name, steps, warmup, dev):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for i in range(steps):
-        stage_step(i, kev[i])
-    torch.cuda.synchronize(dev)
+    run_ahead(dev, steps, lambda i: stage_step(i, kev[i]))
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} in {name}")
     ms = e0.elapsed_time(e1) / steps
@@ -889,8 +902,7 @@ def bench_tq(args):
     total_ms = e0.elapsed_time(e1)
     # the dominant kernel: the split-K pass, timed by events on the launching stream over K steps
     kev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(args.steps)]
-    for i in range(args.steps):
-        stage_step(i, kev[i])
+    run_ahead(dev, args.steps, lambda i: stage_step(i, kev[i]))
     barrier()
     kern_ms = [e[0].elapsed_time(e[1]) for e in kev]
     append_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in kev)
