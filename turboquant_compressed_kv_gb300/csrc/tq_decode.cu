@@ -43,9 +43,6 @@ __global__ void __launch_bounds__(128)
 qprep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ q, int batch, int q_len, int hq, int hkv,
              uint8_t *__restrict__ packs) {
     extern __shared__ __align__(16) uint8_t qsm[];
-#if TQ_PREP_PDL
-    pdl_wait();   // launched as a dependent: every earlier kernel of the stream has completed past this
-#endif
     pdl_launch_dependents();
     qprep_slice<D, NTK, T>(params, q, batch, q_len, hq, hkv, packs, blockIdx.x, qsm);
 }
@@ -75,13 +72,8 @@ cudaError_t qprep_launch_t(const uint8_t *P, const void *q, int batch, int q_len
     auto kern = qprep_kernel<D, NTK, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-#if TQ_PREP_PDL
-    return launch_pass(kern, qprep_ctas(D, batch * q_len * hq), 128, smem, st, P, (const T *)q, batch, q_len, hq, hkv,
-                       w.packs);
-#else
     kern<<<qprep_ctas(D, batch * q_len * hq), 128, smem, st>>>(P, (const T *)q, batch, q_len, hq, hkv, w.packs);
     return cudaGetLastError();
-#endif
 }
 
 template <int D, typename T>
@@ -135,9 +127,6 @@ step_prep_kernel(const uint8_t *__restrict__ params, const T *__restrict__ k_new
                  const T *__restrict__ q, int batch, int q_len, int hq, int hkv, SlotMap map, uint8_t *__restrict__ k_pool,
                  uint8_t *__restrict__ v_pool, int n_app_k, int n_app_v, uint8_t *__restrict__ packs, int32_t *status) {
     extern __shared__ __align__(16) uint8_t smem[];
-#if TQ_PREP_PDL
-    pdl_wait();   // launched as a dependent: every earlier kernel of the stream has completed past this
-#endif
     pdl_launch_dependents();
     const int blk = blockIdx.x;
     const int64_t n_vec = (int64_t)batch * q_len * hkv;
@@ -161,16 +150,10 @@ cudaError_t step_prep_launch(const uint8_t *P, const void *k_new, const void *v_
     const int64_t n_vec = (int64_t)batch * q_len * hkv;
     const int n_app_k = append_k_ctas(D, n_vec), n_app_v = append_v_ctas(n_vec);
     const int n_q = q ? qprep_ctas(D, batch * q_len * hq) : 0;
-#if TQ_PREP_PDL
-    return launch_pass(kern, n_app_k + n_app_v + n_q, 128, q ? smem : as, st, P, (const T *)k_new, (const T *)v_new,
-                       (const T *)q, batch, q_len, hq, hkv, map, (uint8_t *)kp, (uint8_t *)vp, n_app_k, n_app_v, packs,
-                       status);
-#else
     kern<<<n_app_k + n_app_v + n_q, 128, q ? smem : as, st>>>(P, (const T *)k_new, (const T *)v_new, (const T *)q, batch,
                                                              q_len, hq, hkv, map, (uint8_t *)kp, (uint8_t *)vp, n_app_k,
                                                              n_app_v, packs, status);
     return cudaGetLastError();
-#endif
 }
 
 template <int D, typename T>

@@ -133,9 +133,9 @@ decode_warp_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict
 
     // The schedule, the first segment and its first block ids depend only on the lengths and the
     // block table, which the prep launch before this one does not write: with `early` they are
-    // worked out before the wait, overlapping that launch (the prep lets this pass launch only
-    // after its own wait, so every kernel before the prep has completed).  The packs and the
-    // records (the step's appended token) are read after it.
+    // worked out before the wait, overlapping that launch (the prep is an ordinary launch, so
+    // every kernel before it has completed).  The packs and the records (the step's appended
+    // token) are read after it.
     if (!early) pdl_wait();
     const PassSched sc = pass_schedule<NT>(ctx_lens, ctx_add, batch, hkv, max_ctx, CH, cpre);
     const int64_t W = sc.W;
@@ -713,9 +713,6 @@ merge_kernel(const uint8_t *__restrict__ params, int batch, int q_len, int hq, i
     constexpr int UN = 32 / R;
     constexpr float kLn2 = 0.6931471805599453f;
     pdl_wait();
-#if TQ_PREP_PDL
-    pdl_launch_dependents();   // a following prep launch may be placed now; it waits for this kernel itself
-#endif
     const int b = blockIdx.x / hkv, kh = blockIdx.x % hkv, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = warp;
     if (h >= G) return;

@@ -19,13 +19,6 @@ constexpr int kCtasPerSm = TQ_SPLITK_CTAS_PER_SM;
 #ifndef TQ_DECODE_PDL
 #define TQ_DECODE_PDL 1          // the pass may launch while the prep launch before it finishes
 #endif
-#ifndef TQ_PREP_PDL
-// The prep launches (append, query prep) are programmatic dependents of the kernel before them
-// too: their CTAs may be placed while it finishes (the merge kernel signals as soon as it starts),
-// and wait for it (griddepcontrol.wait) before anything else, so that a pass launched after them
-// still starts only once every earlier kernel of the stream has completed.
-#define TQ_PREP_PDL 1
-#endif
 
 // Launch of a decode pass.  With TQ_DECODE_PDL it is a programmatic dependent launch: its CTAs
 // may be launched while the prep kernel before it on the stream finishes (the prep signals
