@@ -184,8 +184,8 @@ namespace dq128 {
 #endif
 constexpr int D = 128, kRows = 128, kUnits = kRows / kBlock, kWg = TQ_DQ128K_WG, kThreads = 128 * kWg;
 constexpr int kRec = (int)k_record(D);
-constexpr int oB = 0;          // S hi, S lo: 2 x 32 KB
-constexpr int oA = 65536;      // A operand of each warpgroup: kWg x 32 KB
+constexpr int oB = 0;          // S as f16 (exact: S is held at binary16 precision): 32 KB
+constexpr int oA = 32768;      // A operand of each warpgroup: kWg x 32 KB
 constexpr int oR = oA + kWg * 32768;   // records: [warpgroup][buffer][unit][kRec]
 constexpr int kSmem = oR + kWg * 2 * kUnits * kRec;
 }  // namespace dq128
@@ -232,18 +232,14 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
         const float *Dp = reinterpret_cast<const float *>(params + params_off_D(D));
         s_dsg[tid] = (Dp[2 * tid] < 0.f ? 0x8000u : 0u) | (Dp[2 * tid + 1] < 0.f ? 0x80000000u : 0u);
     }
-    {   // B: row n = output coordinate n, K index k' as in the A operand; S as f16 (exact), lo = 0
+    {   // B: row n = output coordinate n, K index k' as in the A operand; S as f16 (exact)
         const float *S = reinterpret_cast<const float *>(params + params_off_S(D));
         for (int e = tid; e < D * D; e += kThreads) {
             const int n = e >> 7, k = e & 127;
             const int tig = k >> 5, w = (k >> 3) & 3, f = ((k >> 1) & 3) + 4 * (k & 1);
             const int coord = 16 * (2 * w + (f >> 2)) + 2 * tig + (f & 1) + 8 * ((f >> 1) & 1);
-            const float sv = __ldg(S + coord * D + n);
-            const __half hi = __float2half_rn(sv);
-            const __half lo = __float2half_rn(sv - __half2float(hi));
-            const int off = tc::sw128_off(n, k, D);
-            *reinterpret_cast<__half *>(smem + oB + off) = hi;
-            *reinterpret_cast<__half *>(smem + oB + 32768 + off) = lo;
+            // S is held at binary16 precision: one exact f16 operand
+            *reinterpret_cast<__half *>(smem + oB + tc::sw128_off(n, k, D)) = __float2half_rn(__ldg(S + coord * D + n));
         }
     }
     tc::fence_async_smem();
@@ -338,12 +334,11 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
         tc::named_sync(bar_id, 128);   // A built, the records read: the buffer can be refilled
         tc::fence_after_sync();
         if (row == 0) {
-            const uint32_t bh = tc::smem_u32(smem + oB), bl = bh + 32768, a = tc::smem_u32(sA);
+            const uint32_t bh = tc::smem_u32(smem + oB), a = tc::smem_u32(sA);
             constexpr uint32_t id = tc::idesc_f16(kRows, D);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
                 tc::mma_ss_f16(tmem, tc::sw128_desc(a, ks, kRows), tc::sw128_desc(bh, ks, D), id, ks > 0);
-            (void)bl;   // S is held at binary16 precision: its low part is zero
             tc::mma_commit(&mmabar[wg]);
             if (tile_of(i + 2) < ntiles) issue(i + 2, buf, nids);
         }

@@ -76,7 +76,7 @@ template <typename T> __host__ __device__ constexpr int nx() { return sizeof(T) 
 template <typename T> __host__ __device__ constexpr int row_bytes() { return D * (int)sizeof(T); }
 template <typename T> __host__ __device__ constexpr int row_stride() { return row_bytes<T>() + 16; }
 template <typename T> __host__ __device__ constexpr int xbuf_bytes() { return kRows * row_stride<T>(); }
-template <bool K> __host__ __device__ constexpr int oX() { return K ? 65536 : 0; }          // after S hi / lo
+template <bool K> __host__ __device__ constexpr int oX() { return K ? 32768 : 0; }          // after S (f16)
 // K: one CTA of 2 warpgroups per SM (tensor memory, S in shared memory); V: CTAs of one warpgroup,
 // 3 per SM (no tensor memory: fewer registers and more warps per SM)
 template <bool K> __host__ __device__ constexpr int n_wg() { return K ? 2 : 1; }
@@ -121,12 +121,8 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
         for (int e = tid; e < D * D; e += n_threads<IS_K>()) {
             const int n = e >> 7, k = e & 127;
             const int sr = k_col_coord(n);
-            const float sv = __ldg(S + sr * D + k);
-            const __half hi = __float2half_rn(sv);
-            const __half lo = __float2half_rn(sv - __half2float(hi));
-            const int off = tc::sw128_off(n, k, D);
-            *reinterpret_cast<__half *>(smem + off) = hi;
-            *reinterpret_cast<__half *>(smem + 32768 + off) = lo;
+            // S is held at binary16 precision: one exact f16 operand
+            *reinterpret_cast<__half *>(smem + tc::sw128_off(n, k, D)) = __float2half_rn(__ldg(S + sr * D + k));
         }
     }
     tc::fence_async_smem();
@@ -281,7 +277,7 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
             tc::named_sync(bar_id, 128);
             tc::fence_after_sync();
             if (row == 0) {
-                const uint32_t bh = tc::smem_u32(smem), bl = bh + 32768;
+                const uint32_t bh = tc::smem_u32(smem);
                 constexpr uint32_t id = tc::idesc_f16(kRows, D);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
@@ -289,7 +285,6 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
                     tc::mma_ts_f16(tmem + 128, tmem + 64 + 8 * ks, tc::sw128_desc(bh, ks, D), id, true);
-                (void)bl;   // S is held at binary16 precision: no S_lo rho_hi term
                 tc::mma_commit(&mmabar[wg]);
             }
             if (!tc::mbar_wait(&mmabar[wg], i & 1)) timed_out = true;
@@ -992,7 +987,7 @@ template <typename T> __host__ __device__ constexpr int row_stride() { return ro
 // bulk copy each into a padded row stride
 template <typename T> __host__ __device__ constexpr bool tma() { return sizeof(T) == 2; }
 template <typename T> __host__ __device__ constexpr int xbuf_bytes() { return tma<T>() ? 2 * kRows * 128 : kRows * row_stride<T>(); }
-constexpr int oX = 65536;   // after S hi / lo
+constexpr int oX = 32768;   // after S (f16)
 template <typename T> __host__ __device__ constexpr int oW() { return oX + kTg * nx<T>() * xbuf_bytes<T>(); }
 constexpr int kWStride = 15;   // per row: 12 partial plane words, the residual sum of squares, two norm shares
 template <typename T> __host__ __device__ constexpr int smem_bytes() { return oW<T>() + kTg * kRows * kWStride * 4; }
@@ -1040,12 +1035,8 @@ encode128k_split_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t 
         for (int e = tid; e < D * D; e += kThreads) {
             const int n = e >> 7, k = e & 127;
             const int sr = k_col_coord(n);
-            const float sv = __ldg(S + sr * D + k);
-            const __half hi = __float2half_rn(sv);
-            const __half lo = __float2half_rn(sv - __half2float(hi));
-            const int off = tc::sw128_off(n, k, D);
-            *reinterpret_cast<__half *>(smem + off) = hi;
-            *reinterpret_cast<__half *>(smem + 32768 + off) = lo;
+            // S is held at binary16 precision: one exact f16 operand
+            *reinterpret_cast<__half *>(smem + tc::sw128_off(n, k, D)) = __float2half_rn(__ldg(S + sr * D + k));
         }
     }
     tc::fence_async_smem();
@@ -1237,7 +1228,7 @@ encode128k_split_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t 
         tc::named_sync(bar_id, 256);
         tc::fence_after_sync();
         if (issuer && lane == 0) {
-            const uint32_t bh = tc::smem_u32(smem), bl = bh + 32768;
+            const uint32_t bh = tc::smem_u32(smem);
             constexpr uint32_t id = tc::idesc_f16(kRows, D);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
@@ -1245,8 +1236,7 @@ encode128k_split_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t 
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
                 tc::mma_ts_f16(tmem + 128, tmem + 64 + 8 * ks, tc::sw128_desc(bh, ks, D), id, true);
-            // S is held at binary16 precision (its low part is zero): no S_lo rho_hi term
-            (void)bl;
+            // S is held at binary16 precision (exact in f16): S rho_hi + S rho_lo is the product
             tc::mma_commit(&mmabar[tg]);
         }
         if (!tc::mbar_wait(&mmabar[tg], i & 1)) timed_out = true;
