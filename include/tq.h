@@ -217,8 +217,9 @@ int tq_decode_splitk(const void *params, int d, int batch, int n_q_heads, int n_
  * are encoded into the slot of position pre_lens[b] (as tq_paged_append), and query head h
  * of sequence b attends the pre_lens[b] + 1 tokens (as tq_decode_attn, clamped to
  * max_ctx).  A sequence with pre_lens[b] < 0 appends nothing and gets out = 0.
- * The append and the query preparation run in one launch, followed by the split-K pass;
- * the result equals tq_paged_append followed by tq_decode_attn with ctx_lens = pre_lens + 1.
+ * The append and the query preparation run in one launch, followed by the split-K pass and
+ * its merge (three launches); the result equals tq_paged_append followed by tq_decode_attn
+ * with ctx_lens = pre_lens + 1, bit for bit.
  *   k_new, v_new  device [batch][n_kv_heads][d] in dtype;  q  device [batch][n_q_heads][d].
  *   pre_lens      device int32[batch].
  *   workspace     >= tq_decode_workspace_bytes(d, batch, n_q_heads, max_ctx) bytes.
@@ -254,8 +255,8 @@ int tq_decode_attn_mq(const void *params, int d, const void *q, int dtype, int b
  * of position pre_lens[b] + i, then the q_len queries attend as in tq_decode_attn_mq with
  * ctx_lens = pre_lens + q_len (query i sees pre_lens[b] + 1 + i tokens).  A sequence with
  * pre_lens[b] < 0 appends nothing and gets out = 0.  One launch for the append and the query
- * preparation, one for the pass; the result equals tq_paged_append of each token followed
- * by tq_decode_attn_mq.  Errors as tq_decode_step and tq_decode_attn_mq. */
+ * preparation, one for the pass, one for its merge; the result equals tq_paged_append of each
+ * token followed by tq_decode_attn_mq.  Errors as tq_decode_step and tq_decode_attn_mq. */
 int tq_decode_step_mq(const void *params, int d, const void *k_new, const void *v_new, const void *q,
                       int dtype, int batch, int q_len, int n_q_heads, int n_kv_heads,
                       const int32_t *block_table, int max_blocks, const int32_t *pre_lens, int max_ctx,
