@@ -193,7 +193,9 @@ def _on_device(fn):
     @functools.wraps(fn)
     def call(*args, **kwargs):
         torch = _torch()
-        devs = {a.device for a in list(args) + list(kwargs.values()) if isinstance(a, torch.Tensor) and a.is_cuda}
+        tensor = torch.Tensor
+        devs = {a.device for a in args if isinstance(a, tensor) and a.is_cuda}
+        devs.update(a.device for a in kwargs.values() if isinstance(a, tensor) and a.is_cuda)
         if len(devs) > 1:
             raise TQError(f"{fn.__name__}: tensors on more than one device ({sorted(map(str, devs))})")
         if not devs:
@@ -202,6 +204,8 @@ def _on_device(fn):
         st = kwargs.get("stream")
         if st is not None and st.device != dev:
             raise TQError(f"{fn.__name__}: the stream is on {st.device}, the tensors on {dev}")
+        if torch.cuda.current_device() == dev.index:   # already current: no device switch
+            return fn(*args, **kwargs)
         with torch.cuda.device(dev):
             return fn(*args, **kwargs)
     return call
@@ -278,8 +282,8 @@ def decode_attn(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_table,
     B, Hq = q.shape[0], q.shape[1]
     if out is None:
         out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
-    need = decode_workspace_bytes(d, B, Hq, max_ctx)
-    if workspace is None:
+    if workspace is None:   # (the library checks a given workspace's size itself)
+        need = decode_workspace_bytes(d, B, Hq, max_ctx)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     rc = load_library().tq_decode_attn(_ptr(params), d, _ptr(q), _dtype_code(q), B, Hq, n_kv_heads,
                                        _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
@@ -323,8 +327,8 @@ def decode_step(params, d: int, k_new, v_new, q, n_kv_heads: int, k_pool, v_pool
     B, Hq = q.shape[0], q.shape[1]
     if out is None:
         out = torch.empty((B, Hq, d), dtype=torch.float32, device=q.device)
-    need = decode_workspace_bytes(d, B, Hq, max_ctx)
-    if workspace is None:
+    if workspace is None:   # (the library checks a given workspace's size itself)
+        need = decode_workspace_bytes(d, B, Hq, max_ctx)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     if k_new.dtype != q.dtype or v_new.dtype != q.dtype:
         raise TQError("k_new, v_new and q must share one dtype")
@@ -424,8 +428,8 @@ def decode_attn_mq(params, d: int, q, n_kv_heads: int, k_pool, v_pool, block_tab
     B, Q, Hq = q.shape[0], q.shape[1], q.shape[2]
     if out is None:
         out = torch.empty((B, Q, Hq, d), dtype=torch.float32, device=q.device)
-    need = decode_workspace_bytes_mq(d, B, Q, Hq, max_ctx)
-    if workspace is None:
+    if workspace is None:   # (the library checks a given workspace's size itself)
+        need = decode_workspace_bytes_mq(d, B, Q, Hq, max_ctx)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     rc = load_library().tq_decode_attn_mq(_ptr(params), d, _ptr(q), _dtype_code(q), B, Q, Hq, n_kv_heads,
                                           _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], _ptr(block_table),
@@ -445,8 +449,8 @@ def decode_step_mq(params, d: int, k_new, v_new, q, n_kv_heads: int, k_pool, v_p
     B, Q, Hq = q.shape[0], q.shape[1], q.shape[2]
     if out is None:
         out = torch.empty((B, Q, Hq, d), dtype=torch.float32, device=q.device)
-    need = decode_workspace_bytes_mq(d, B, Q, Hq, max_ctx)
-    if workspace is None:
+    if workspace is None:   # (the library checks a given workspace's size itself)
+        need = decode_workspace_bytes_mq(d, B, Q, Hq, max_ctx)
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     if k_new.dtype != q.dtype or v_new.dtype != q.dtype:
         raise TQError("k_new, v_new and q must share one dtype")
