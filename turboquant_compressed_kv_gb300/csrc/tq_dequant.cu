@@ -169,7 +169,9 @@ dequant_kernel(const uint8_t *__restrict__ params, const uint8_t *__restrict__ p
 // ---------------------------------------------------------------- K at d = 128 on tcgen05
 // kWg warpgroups take alternate tiles of 128 rows (8 records x 16 slots); thread r of a
 // warpgroup owns row r:
-//  1. the tile's records arrive by bulk copy (two tiles in flight per warpgroup);
+//  1. the tile's records arrive by bulk copy (two tiles in flight per warpgroup), one record per
+//     lane of the warpgroup's second warp, so that the copies leave together and the thread that
+//     issues the MMA does nothing else;
 //  2. the row's 128 sign bits become the A operand (f16 +-1, 128-byte swizzle) with one shift
 //     and one LOP3 per two elements: K index 32 tig + 8 w + 2 p + e holds the sign bit of field
 //     p + 4 e of the slot's word (tig, w), bit 4 (p + 4 e) + 3;
@@ -253,44 +255,30 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
 
     // tiles of this warpgroup: blockIdx.x + (2 i + wg) * gridDim.x
     auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)(kWg * i + wg) * gridDim.x; };
-    // the block ids of tile i's records (read a tile before the copies that use them, so that the
-    // issuing thread does not wait for them between the MMA and the read-back)
-    auto load_tile_ids = [&](int i, int32_t (&ids)[kUnits]) {
-        const int64_t tile = tile_of(i);
-#pragma unroll
-        for (int k = 0; k < kUnits; ++k) {
-            const int64_t u = tile * kUnits + k;
-            ids[k] = u < units ? block_ids[u / n_heads] : 0;
+    // Warp 1 of the warpgroup moves the records, lane k < kUnits the record of unit k, while row 0
+    // (warp 0) issues the MMA.  A lane reads its block id one tile before the copy that uses it.
+    const int lane = tid & 31;
+    const bool mover = (warp & 3) == 1;
+    auto load_id = [&](int i) -> int32_t {
+        const int64_t u = tile_of(i) * kUnits + lane;
+        return (lane < kUnits && u < units) ? block_ids[u / n_heads] : 0;
+    };
+    auto issue = [&](int i, int buf, int32_t id) {   // warp 1: tile i's records into buffer buf
+        const int64_t left = units - tile_of(i) * kUnits;
+        const int n = left < kUnits ? (int)left : kUnits;
+        if (lane == 0) tc::mbar_arrive_expect_tx(&recbar[wg][buf], (uint32_t)(n * kRec));
+        __syncwarp();
+        if (lane < n) {
+            const int64_t u = tile_of(i) * kUnits + lane;
+            const int64_t bc = (id >= 0 && id < num_blocks) ? id : 0;   // a bad id reads block 0, output zeroed
+            tc::bulk_g2s(smem + oR + ((wg * 2 + buf) * kUnits + lane) * kRec,
+                         pool + ((size_t)bc * n_heads + (u % n_heads)) * kRec, kRec, &recbar[wg][buf]);
         }
     };
-    auto issue = [&](int i, int buf, const int32_t (&ids)[kUnits]) {   // one thread: the tile's records into buffer buf
-        const int64_t tile = tile_of(i);
-        uint32_t bytes = 0;
-        for (int k = 0; k < kUnits; ++k)
-            if (tile * kUnits + k < units) bytes += kRec;
-        tc::mbar_arrive_expect_tx(&recbar[wg][buf], bytes);
-#pragma unroll
-        for (int k = 0; k < kUnits; ++k) {
-            const int64_t u = tile * kUnits + k;
-            if (u < units) {
-                const int64_t blk = ids[k];
-                const int64_t bc = (blk >= 0 && blk < num_blocks) ? blk : 0;   // a bad id reads block 0, output zeroed
-                tc::bulk_g2s(smem + oR + ((wg * 2 + buf) * kUnits + k) * kRec,
-                             pool + ((size_t)bc * n_heads + (u % n_heads)) * kRec, kRec, &recbar[wg][buf]);
-            }
-        }
-    };
-    int32_t nids[kUnits];   // row 0: the ids of the tile two ahead
-    if (row == 0) {
-        int32_t ids0[kUnits];
-        if (tile_of(0) < ntiles) {
-            load_tile_ids(0, ids0);
-            issue(0, 0, ids0);
-        }
-        if (tile_of(1) < ntiles) {
-            load_tile_ids(1, ids0);
-            issue(1, 1, ids0);
-        }
+    int32_t nid = 0;   // warp 1: this lane's block id of the tile two ahead
+    if (mover) {
+        if (tile_of(0) < ntiles) issue(0, 0, load_id(0));
+        if (tile_of(1) < ntiles) issue(1, 1, load_id(1));
     }
     uint8_t *sA = smem + oA + wg * 32768;
     const int bar_id = 1 + wg;   // named barrier of this warpgroup's 128 threads
@@ -299,9 +287,12 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
     for (int i = 0; tile_of(i) < ntiles; ++i) {
         const int64_t tile = tile_of(i);
         const int buf = i & 1;
-        if (row == 0 && tile_of(i + 2) < ntiles) load_tile_ids(i + 2, nids);
+        if (mover && tile_of(i + 2) < ntiles) nid = load_id(i + 2);
         if (!tc::mbar_wait(&recbar[wg][buf], (i >> 1) & 1)) timed_out = true;
-        const int unit_k = row >> 4, t = row & 15;
+        // row 32 q + l holds slot (l >> 2) + 8 (bit 1 of l) of unit 2 q + (l & 1): a quarter-warp's
+        // record reads fall on 4 different 16-byte bank groups (units are 1088 bytes apart), where
+        // a unit per 16 rows put 8 lanes on one group
+        const int lq = row & 31, unit_k = 2 * (row >> 5) + (lq & 1), t = (lq >> 2) + 8 * ((lq >> 1) & 1);
         const int64_t u = tile * kUnits + unit_k;
         const bool live = u < units;
         const int64_t blk = live ? block_ids[u / n_heads] : -1;   // checked at the store
@@ -340,21 +331,28 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
             for (int ks = 0; ks < D / 16; ++ks)
                 tc::mma_ss_f16(tmem, tc::sw128_desc(a, ks, kRows), tc::sw128_desc(bh, ks, D), id, ks > 0);
             tc::mma_commit(&mmabar[wg]);
-            if (tile_of(i + 2) < ntiles) issue(i + 2, buf, nids);
         }
+        if (mover && tile_of(i + 2) < ntiles) issue(i + 2, buf, nid);
         if (!tc::mbar_wait(&mmabar[wg], i & 1)) timed_out = true;
         tc::fence_after_sync();
         // y = c[cell] / sqrt d + sqrt(pi/2)/d gamma p on pairs Y[j] = (y_2j, y_2j+1): coordinate n in
         // column n
         float2 Y[D / 2];
         const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        {
+            uint32_t pv[D / 16][16];   // the eight loads share one wait
 #pragma unroll
-        for (int j = 0; j < D / 16; ++j) {
-            float pv[16];
-            tc::ld16(taddr + 16 * j, pv);
+            for (int j = 0; j < D / 16; ++j) tc::ld16_raw(taddr + 16 * j, pv[j]);
             tc::wait_ld();
 #pragma unroll
-            for (int x = 0; x < 8; ++x) Y[8 * j + x] = make_float2(pv[2 * x], pv[2 * x + 1]);
+            for (int j = 0; j < D / 16; ++j)
+#pragma unroll
+                for (int x = 0; x < 16; ++x) tc::reg_fence(pv[j][x]);
+#pragma unroll
+            for (int j = 0; j < D / 16; ++j)
+#pragma unroll
+                for (int x = 0; x < 8; ++x)
+                    Y[8 * j + x] = make_float2(__uint_as_float(pv[j][2 * x]), __uint_as_float(pv[j][2 * x + 1]));
         }
         tc::fence_before_sync();
         const float gq = qjl * gam;
@@ -429,7 +427,8 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
 
 // ---------------------------------------------------------------- V at d = 128, one thread per row
 // A CTA of 128 threads walks tiles of 8 records (128 rows); thread r owns row r:
-//  1. the tile's records arrive by bulk copy, two tiles in flight;
+//  1. the tile's records arrive by bulk copy, two tiles in flight, one record per lane of warp 0,
+//     which also leaves the records' block ids in shared memory for the rows' stores;
 //  2. the row's cells are read back word by word (each V byte holds two cells of one slot and one
 //     bit of two more), y = c[cell] / sqrt d by one table lookup per byte;
 //  3. the 128-point inverse transform in registers, the norm and D, and 16-byte stores.
@@ -447,6 +446,7 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
     using namespace dq128v;
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ uint64_t recbar[2], recfree[2];
+    __shared__ int32_t s_ids[2][kUnits];   // block ids of the records in each buffer
     __shared__ __align__(16) float s_D[D];
     __shared__ __align__(16) uint32_t s_dsg[D / 2];   // bf16 pair sign masks of D (bit 15 / 31: D_2j / D_2j+1 < 0)
     // centroid pairs (x 1/sqrt d) of two fields, by a record byte masked to its cell bits (0x77):
@@ -483,35 +483,42 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
     tc::fence_after_sync();
     bool timed_out = false;
     auto tile_of = [&](int i) { return (int64_t)blockIdx.x + (int64_t)i * gridDim.x; };
-    auto issue = [&](int i, int buf) {   // one thread: the tile's records into buffer buf
-        const int64_t tile = tile_of(i);
-        uint32_t bytes = 0;
-        for (int k = 0; k < kUnits; ++k)
-            if (tile * kUnits + k < units) bytes += kRec;
-        tc::mbar_arrive_expect_tx(&recbar[buf], bytes);
-        for (int k = 0; k < kUnits; ++k) {
-            const int64_t u = tile * kUnits + k;
-            if (u >= units) break;
-            const int64_t blk = block_ids[u / n_heads];
-            const int64_t bc = (blk >= 0 && blk < num_blocks) ? blk : 0;   // a bad id reads block 0, output zeroed
-            tc::bulk_g2s(smem + (buf * kUnits + k) * kRec, pool + ((size_t)bc * n_heads + (u % n_heads)) * kRec, kRec,
-                         &recbar[buf]);
+    // Warp 0 moves the records: lane k < kUnits reads the block id of unit k one tile ahead and
+    // copies that unit's record.
+    auto load_id = [&](int i) -> int32_t {
+        const int64_t u = tile_of(i) * kUnits + lane;
+        return (lane < kUnits && u < units) ? block_ids[u / n_heads] : 0;
+    };
+    auto issue = [&](int i, int buf, int32_t id) {   // warp 0: tile i's records into buffer buf
+        const int64_t left = units - tile_of(i) * kUnits;
+        const int n = left < kUnits ? (int)left : kUnits;
+        if (lane < kUnits) s_ids[buf][lane] = id;   // for the rows' stores, visible once the buffer is full
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive_expect_tx(&recbar[buf], (uint32_t)(n * kRec));
+        if (lane < n) {
+            const int64_t u = tile_of(i) * kUnits + lane;
+            const int64_t bc = (id >= 0 && id < num_blocks) ? id : 0;   // a bad id reads block 0, output zeroed
+            tc::bulk_g2s(smem + (buf * kUnits + lane) * kRec, pool + ((size_t)bc * n_heads + (u % n_heads)) * kRec,
+                         kRec, &recbar[buf]);
         }
     };
-    if (row == 0) {
-        if (tile_of(0) < ntiles) issue(0, 0);
-        if (tile_of(1) < ntiles) issue(1, 1);
+    const bool mover = row < 32;
+    int32_t nid = 0;   // warp 0: this lane's block id of the tile two ahead
+    if (mover) {
+        if (tile_of(0) < ntiles) issue(0, 0, load_id(0));
+        if (tile_of(1) < ntiles) issue(1, 1, load_id(1));
     }
 
 #pragma unroll 1
     for (int i = 0; tile_of(i) < ntiles; ++i) {
         const int64_t tile = tile_of(i);
         const int buf = i & 1;
+        if (mover && tile_of(i + 2) < ntiles) nid = load_id(i + 2);
         if (!tc::mbar_wait(&recbar[buf], (i >> 1) & 1)) timed_out = true;
         const int unit_k = row >> 4, t = row & 15;
         const int64_t u = tile * kUnits + unit_k;
         const bool live = u < units;
-        const int64_t blk = live ? block_ids[u / n_heads] : -1;   // checked at the store
+        const int64_t blk = live ? s_ids[buf][unit_k] : -1;   // checked at the store
         const uint8_t *rec = smem + (buf * kUnits + unit_k) * kRec;
         const uint32_t *words = reinterpret_cast<const uint32_t *>(rec);
         // the slot's bytes: per lane gid, words 3 (L * 2 + pair) + k (k = 0..2), bytes 2 hf + e.
@@ -543,12 +550,12 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
         tc::fence_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&recfree[buf]);   // this warp's rows of the buffer are read
-        // thread 0 refills the buffer with the tile two ahead once every warp has read it (after
+        // warp 0 refills the buffer with the tile two ahead once every warp has read it (after
         // this tile's work, when they are long done; nobody else waits)
         auto refill = [&]() {
-            if (row == 0 && tile_of(i + 2) < ntiles) {
+            if (mover && tile_of(i + 2) < ntiles) {
                 if (!tc::mbar_wait(&recfree[buf], (i >> 1) & 1)) timed_out = true;
-                issue(i + 2, buf);
+                issue(i + 2, buf, nid);
             }
         };
         // inverse rotation D (H y) / sqrt d: index bit 3 inside the pairs; bits 0..2 and 4..6 between

@@ -56,6 +56,17 @@ __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32]) {
         "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
 }
+// The same without the wait: the registers hold the columns only after wait_ld, and reg_fence
+// on each of them after that wait keeps their uses behind it.  Several loads may then share one wait.
+__device__ __forceinline__ void ld16_raw(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+// No instruction: x is redefined after the volatile asm before it (a tcgen05.wait::ld).
+__device__ __forceinline__ void reg_fence(uint32_t &x) { asm volatile("" : "+r"(x)); }
 // 32 lanes x 16 columns: thread i loads lane (base lane + i), columns [col, col + 16).
 __device__ __forceinline__ void ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
