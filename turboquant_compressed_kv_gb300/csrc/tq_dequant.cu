@@ -389,30 +389,56 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
         if (live && !good && t == 0) flag_status(status, TQ_STATUS_BAD_SLOT);
         const float sc = good ? nrm * inv_sd : 0.f;
         const float2 sc2 = make_float2(sc, sc);
-        if (live) {
-            TO *orow = out + (((size_t)(u / n_heads) * kBlock + t) * n_heads + (u % n_heads)) * D;
+        if constexpr (sizeof(TO) == 4) {
+            if (live) {
+                TO *orow = out + (((size_t)(u / n_heads) * kBlock + t) * n_heads + (u % n_heads)) * D;
 #pragma unroll
-            for (int n = 0; n < D; n += 8) {
-                float2 o[4];
+                for (int n = 0; n < D; n += 8) {
+                    float2 o[4];
 #pragma unroll
-                for (int x = 0; x < 4; ++x) o[x] = __fmul2_rn(Y[n / 2 + x], sc2);
-                if constexpr (sizeof(TO) == 4) {
+                    for (int x = 0; x < 4; ++x) o[x] = __fmul2_rn(Y[n / 2 + x], sc2);
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
                         const float4 dv = *reinterpret_cast<const float4 *>(&s_D[n + 4 * x]);
                         *reinterpret_cast<float4 *>(orow + n + 4 * x) =
                             make_float4(o[2 * x].x * dv.x, o[2 * x].y * dv.y, o[2 * x + 1].x * dv.z, o[2 * x + 1].y * dv.w);
                     }
-                } else {   // bf16: the signs D by an XOR of the packed words
-                    const uint4 sm = *reinterpret_cast<const uint4 *>(&s_dsg[n / 2]);
-                    const uint32_t smw[4] = {sm.x, sm.y, sm.z, sm.w};
-                    uint32_t pk[4];
+                }
+            }
+        } else {
+            // bf16, the signs D by an XOR of the packed words.  The row (256 bytes) goes to its own
+            // bytes of the A operand, free once the MMA has completed (16-byte chunk c to half c >> 3,
+            // position (c & 7) ^ (row & 7)); then each store of the warp writes two whole rows.
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const __nv_bfloat162 b = __floats2bfloat162_rn(o[x].x, o[x].y);
-                        pk[x] = *reinterpret_cast<const uint32_t *>(&b) ^ smw[x];
-                    }
-                    *reinterpret_cast<uint4 *>(orow + n) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int n = 0; n < D; n += 8) {
+                float2 o[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) o[x] = __fmul2_rn(Y[n / 2 + x], sc2);
+                const uint4 sm = *reinterpret_cast<const uint4 *>(&s_dsg[n / 2]);
+                const uint32_t smw[4] = {sm.x, sm.y, sm.z, sm.w};
+                uint32_t pk[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const __nv_bfloat162 b = __floats2bfloat162_rn(o[x].x, o[x].y);
+                    pk[x] = *reinterpret_cast<const uint32_t *>(&b) ^ smw[x];
+                }
+                const int c = n >> 3;
+                *reinterpret_cast<uint4 *>(sA + (c >> 3) * (kRows * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            __syncwarp();
+            // store j: lanes 0..15 write slot j of the warp's first unit, lanes 16..31 of its second
+            // (rows 32 q + 4 (j & 7) + 2 (j >> 3) + e, e = lane >> 4), chunk lane & 15 each
+            const int e = lane >> 4, c = lane & 15;
+            const int64_t ue = tile * kUnits + 2 * (warp & 3) + e;
+            if (ue < units) {
+                TO *obase = out + (((size_t)(ue / n_heads) * kBlock) * n_heads + (ue % n_heads)) * D + 8 * c;
+#pragma unroll
+                for (int j = 0; j < kBlock; ++j) {
+                    const int r = 32 * (warp & 3) + 4 * (j & 7) + 2 * (j >> 3) + e;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(sA + (c >> 3) * (kRows * 128) + r * 128 +
+                                                                     (((c & 7) ^ (r & 7)) << 4));
+                    *reinterpret_cast<uint4 *>(obase + (size_t)j * n_heads * D) = v;
                 }
             }
         }
@@ -435,7 +461,8 @@ dequant128k_tc_kernel(const uint8_t *__restrict__ params, const uint8_t *__restr
 namespace dq128v {
 constexpr int D = 128, kRows = 128, kUnits = kRows / kBlock, kThreads = 128, kMinCtas = 3;
 constexpr int kRec = (int)v_record(D);
-constexpr int kSmem = 2 * kUnits * kRec;
+constexpr int oStage = 2 * kUnits * kRec;                 // records: two buffers of 8
+constexpr int kSmem = oStage + (kThreads / 32) * 32 * 256;   // bf16 rows of each warp, staged for the stores
 }  // namespace dq128v
 
 template <typename TO>
@@ -450,9 +477,9 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
     __shared__ __align__(16) float s_D[D];
     __shared__ __align__(16) uint32_t s_dsg[D / 2];   // bf16 pair sign masks of D (bit 15 / 31: D_2j / D_2j+1 < 0)
     // centroid pairs (x 1/sqrt d) of two fields, by a record byte masked to its cell bits (0x77):
-    // entry i holds c[i & 7], c[i >> 4]; one copy per lane ([index][lane]), so that a half-warp's
-    // lookups never share a bank
-    __shared__ float2 s_pair[128][32];
+    // entry i holds c[i & 7], c[i >> 4]; one copy per lane of a half-warp ([index][lane & 15]): an
+    // 8-byte load is served a half-warp at a time, so its lookups never share a bank
+    __shared__ float2 s_pair[128][16];
     const ParamsHeader *ph = reinterpret_cast<const ParamsHeader *>(params);
     if (ph->magic != kParamsMagic || ph->d != D) {
         if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, TQ_STATUS_BAD_PARAMS);
@@ -468,9 +495,9 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
         tc::mbar_init(&recfree[1], kThreads / 32);
     }
     const float inv_sd = rsqrtf((float)D);
-    for (int e = row; e < 128 * 32; e += kThreads) {
-        const int i = e >> 5;
-        s_pair[i][e & 31] = make_float2(ph->centroid[i & 7] * inv_sd, ph->centroid[(i >> 4) & 7] * inv_sd);
+    for (int e = row; e < 128 * 16; e += kThreads) {
+        const int i = e >> 4;
+        s_pair[i][e & 15] = make_float2(ph->centroid[i & 7] * inv_sd, ph->centroid[(i >> 4) & 7] * inv_sd);
     }
     const int lane = row & 31;
     s_D[row] = reinterpret_cast<const float *>(params + params_off_D(D))[row];
@@ -540,10 +567,10 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-                for (int k = 0; k < 3; ++k) P[8 * (2 * k + hf) + gid] = s_pair[bt[k][hf] & 0x77u][lane];
+                for (int k = 0; k < 3; ++k) P[8 * (2 * k + hf) + gid] = s_pair[bt[k][hf] & 0x77u][lane & 15];
                 // bit 3 (ab = 0) and bit 7 (ab = 1) of the three bytes: the cells of slots 12 + 2hf + ab
                 const uint32_t sp = ((bt[0][hf] >> 3) & 0x11u) | ((bt[1][hf] >> 2) & 0x22u) | ((bt[2][hf] >> 1) & 0x44u);
-                P[8 * (6 + hf) + gid] = s_pair[sp][lane];
+                P[8 * (6 + hf) + gid] = s_pair[sp][lane & 15];
             }
         }
         const __half nh = *reinterpret_cast<const __half *>(rec + 6 * D + 2 * t);
@@ -578,34 +605,60 @@ dequant128v_rows_kernel(const uint8_t *__restrict__ params, const uint8_t *__res
         if (live && !good && t == 0) flag_status(status, TQ_STATUS_BAD_SLOT);
         const float sc = good ? __half2float(nh) * inv_sd : 0.f;
         const float2 sc2 = make_float2(sc, sc);
-        if (live) {
-            TO *orow = out + (((size_t)(u / n_heads) * kBlock + t) * n_heads + (u % n_heads)) * D;
-            // coordinate n is component (n >> 3) & 1 of pair 8 (n >> 4) + (n & 7)
-            auto yv = [&](int n) -> float { return ((n >> 3) & 1) ? P[8 * (n >> 4) + (n & 7)].y : P[8 * (n >> 4) + (n & 7)].x; };
+        // coordinate n is component (n >> 3) & 1 of pair 8 (n >> 4) + (n & 7)
+        auto yv = [&](int n) -> float { return ((n >> 3) & 1) ? P[8 * (n >> 4) + (n & 7)].y : P[8 * (n >> 4) + (n & 7)].x; };
+        if constexpr (sizeof(TO) == 4) {
+            if (live) {
+                TO *orow = out + (((size_t)(u / n_heads) * kBlock + t) * n_heads + (u % n_heads)) * D;
 #pragma unroll
-            for (int n = 0; n < D; n += 8) {
-                float2 o[4];
+                for (int n = 0; n < D; n += 8) {
+                    float2 o[4];
 #pragma unroll
-                for (int x = 0; x < 4; ++x) o[x] = __fmul2_rn(make_float2(yv(n + 2 * x), yv(n + 2 * x + 1)), sc2);
-                if constexpr (sizeof(TO) == 4) {
+                    for (int x = 0; x < 4; ++x) o[x] = __fmul2_rn(make_float2(yv(n + 2 * x), yv(n + 2 * x + 1)), sc2);
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
                         const float4 dv = *reinterpret_cast<const float4 *>(&s_D[n + 4 * x]);
                         *reinterpret_cast<float4 *>(orow + n + 4 * x) =
                             make_float4(o[2 * x].x * dv.x, o[2 * x].y * dv.y, o[2 * x + 1].x * dv.z, o[2 * x + 1].y * dv.w);
                     }
-                } else {   // bf16: the signs D by an XOR of the packed words
-                    const uint4 sm = *reinterpret_cast<const uint4 *>(&s_dsg[n / 2]);
-                    const uint32_t smw[4] = {sm.x, sm.y, sm.z, sm.w};
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const __nv_bfloat162 b = __floats2bfloat162_rn(o[x].x, o[x].y);
-                        pk[x] = *reinterpret_cast<const uint32_t *>(&b) ^ smw[x];
-                    }
-                    *reinterpret_cast<uint4 *>(orow + n) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
             }
+        } else {
+            // bf16, the signs D by an XOR of the packed words.  The row (256 bytes) goes to the
+            // warp's staging area (16-byte chunk c at position c ^ (row & 15)); then each store of
+            // the warp writes two whole rows.
+            uint8_t *stg = smem + oStage + (row >> 5) * (32 * 256);
+#pragma unroll
+            for (int n = 0; n < D; n += 8) {
+                float2 o[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) o[x] = __fmul2_rn(make_float2(yv(n + 2 * x), yv(n + 2 * x + 1)), sc2);
+                const uint4 sm = *reinterpret_cast<const uint4 *>(&s_dsg[n / 2]);
+                const uint32_t smw[4] = {sm.x, sm.y, sm.z, sm.w};
+                uint32_t pk[4];
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const __nv_bfloat162 b = __floats2bfloat162_rn(o[x].x, o[x].y);
+                    pk[x] = *reinterpret_cast<const uint32_t *>(&b) ^ smw[x];
+                }
+                *reinterpret_cast<uint4 *>(stg + lane * 256 + (((n >> 3) ^ (lane & 15)) << 4)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            __syncwarp();
+            // store j: lanes 0..15 write slot j of the warp's first unit (its lane j), lanes 16..31
+            // of its second (lane 16 + j), chunk lane & 15 each
+            const int e = lane >> 4, c = lane & 15;
+            const int64_t ue = tile * kUnits + 2 * (row >> 5) + e;
+            if (ue < units) {
+                TO *obase = out + (((size_t)(ue / n_heads) * kBlock) * n_heads + (ue % n_heads)) * D + 8 * c;
+#pragma unroll
+                for (int j = 0; j < kBlock; ++j) {
+                    const int r = 16 * e + j;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 256 + ((c ^ (r & 15)) << 4));
+                    *reinterpret_cast<uint4 *>(obase + (size_t)j * n_heads * D) = v;
+                }
+            }
+            __syncwarp();   // the staging area is read before the next tile's rows overwrite it
         }
         refill();
     }
@@ -622,6 +675,8 @@ cudaError_t dq128v_launch(const void *params, const void *pool, int64_t num_bloc
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     auto kern = dequant128v_rows_kernel<TO>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dq128v::kSmem);
+    if (e != cudaSuccess) return e;
     const int64_t want = (int64_t)sms * dq128v::kMinCtas;
     const int64_t grid = ntiles < want ? ntiles : want;
     kern<<<(unsigned)grid, dq128v::kThreads, dq128v::kSmem, st>>>((const uint8_t *)params, (const uint8_t *)pool,
