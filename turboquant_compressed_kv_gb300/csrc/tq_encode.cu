@@ -34,6 +34,15 @@
 namespace tq {
 namespace {
 
+// a * b, rounded to nearest (the same as the C++ product), in a form the compiler keeps as one
+// value: a threshold times the norm then stays in a register, where the compiler would otherwise
+// select among the unscaled thresholds and multiply again at every comparison
+__device__ __forceinline__ float held_mul(float a, float b) {
+    float y;
+    asm("mul.rn.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+    return y;
+}
+
 // kinds: 1 = K only, 2 = V only, 3 = K (blockIdx.y 0) and V (blockIdx.y 1).
 template <int D, int TILE, typename T>
 __global__ void __launch_bounds__(kEncWarps * 32)
@@ -217,7 +226,8 @@ encode128_rows_kernel(const uint8_t *__restrict__ params, const T *__restrict__ 
         // with the thresholds times nrm instead (a zero vector keeps the unit thresholds: z = 0 is
         // cell 4); K needs z itself for the residual.
         const float ns = (IS_K || nrm == 0.f) ? 1.f : nrm, zs = IS_K ? rn : 1.f;
-        const float T0 = t0 * ns, T1 = t1 * ns, T2 = t2 * ns, T3 = t3 * ns, T4 = t4 * ns, T5 = t5 * ns, T6 = t6 * ns;
+        const float T0 = held_mul(t0, ns), T1 = held_mul(t1, ns), T2 = held_mul(t2, ns), T3 = held_mul(t3, ns),
+                    T4 = held_mul(t4, ns), T5 = held_mul(t5, ns), T6 = held_mul(t6, ns);
         // K: the 16 words of the slot's fields, [tig][word]; V: the 48 bytes of the slot, byte
         // (gid, k, hf) at q = 6 gid + 2 k + hf of vb (4 per register)
         uint32_t kwd[4][4] = {{0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}, {0u, 0u, 0u, 0u}};
@@ -465,7 +475,8 @@ encode128v_tma_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *_
                 }
         // ---- 3. cells against the thresholds times the norm (a zero row keeps the unit thresholds)
         const float ns = nrm == 0.f ? 1.f : nrm;
-        const float T0 = t0 * ns, T1 = t1 * ns, T2 = t2 * ns, T3 = t3 * ns, T4 = t4 * ns, T5 = t5 * ns, T6 = t6 * ns;
+        const float T0 = held_mul(t0, ns), T1 = held_mul(t1, ns), T2 = held_mul(t2, ns), T3 = held_mul(t3, ns),
+                    T4 = held_mul(t4, ns), T5 = held_mul(t5, ns), T6 = held_mul(t6, ns);
         // the 48 bytes of the slot, byte (gid, k, hf) at q = 6 gid + 2 k + hf of vb (4 per register)
         uint32_t vb[12] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
@@ -667,7 +678,8 @@ encode256v_tma_kernel(const __grid_constant__ CUtensorMap tmap, const uint8_t *_
         const float nrm = sqrtf(0.5f * (s_ss[0][row] + s_ss[1][row]));
         // ---- 2. cells of coordinates 128 h + n against the thresholds times the norm
         const float ns = nrm == 0.f ? 1.f : nrm;
-        const float T0 = t0 * ns, T1 = t1 * ns, T2 = t2 * ns, T3 = t3 * ns, T4 = t4 * ns, T5 = t5 * ns, T6 = t6 * ns;
+        const float T0 = held_mul(t0, ns), T1 = held_mul(t1, ns), T2 = held_mul(t2, ns), T3 = held_mul(t3, ns),
+                    T4 = held_mul(t4, ns), T5 = held_mul(t5, ns), T6 = held_mul(t6, ns);
         uint32_t vb[12] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
         for (int n = 0; n < 128; ++n) {
